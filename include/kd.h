@@ -1,0 +1,211 @@
+/*
+ * kd.h -- C ABI of the GB300 (sm_103a) fused LM-head + cross-entropy + KL
+ * knowledge-distillation loss.
+ *
+ * What it computes (per token n, vocabulary column v):
+ *   z_s = H_s W_s^T (or given student logits), z_t = H_t W_t^T (or given
+ *   teacher logits, or a cached top-K teacher), a_s = z_s / T_s,
+ *   a_t = z_t / T_t, p = softmax(a_s) (student), q = softmax(a_t) (teacher).
+ *   CE_s = logsumexp(z_s) - z_s[y], CE_t likewise on z_t (T = 1)
+ *     -- flash_kd API doc, flash_ce_kd_loss, "labels" / "Returns".
+ *   KL variants forward KL(q||p), reverse KL(p||q), Jeffreys (their sum),
+ *   skew-JS (1-b) KL(q||m) + b KL(p||m), m = (1-b) q + b p
+ *     -- orda-kernel README, "KL variants" (skew-JS's split is this
+ *        library's reading: the page names it and its two halves only).
+ *   Sparse top-K objective sum_S p log p - sum_S p a + M logsumexp(a),
+ *   gradient M softmax(a) - p -- Full-Chunked-KL-Loss README, "Methods",
+ *   "Full Chunked KL".
+ *   loss = sum_valid (w_sce CE_s + w_tce CE_t + w_kl T_s^2 KL) / denom
+ *     -- orda-kernel README, "Parameters" (each KL row scales by T_s^2,
+ *        reduction "mean"/"sum"); nemo_automodel KDLoss (T^2, mean over
+ *        valid tokens or sum / num_batch_labels).
+ * The (tokens x vocab) logits are never stored: the forward keeps running
+ * online-softmax statistics per token (flash_kd: "online-softmax (running
+ * max + rescale)"), the backward recomputes each logit tile and applies the
+ * closed-form gradient (Full-Chunked-KL-Loss README, "Full Chunked KL").
+ *
+ * Conventions
+ *   - Every pointer in kd_inputs and every output/workspace pointer is a
+ *     DEVICE pointer on the current CUDA device, owned by the caller.  The
+ *     library never allocates device memory; scratch space is the caller's
+ *     `workspace` of at least the size kd_workspace_size() reports.
+ *   - All matrices are dense row-major with the last dimension contiguous:
+ *     H_s [N, D_s], W_s [V, D_s], H_t [N, D_t], W_t [V, D_t],
+ *     logits [N, V], labels int64 [N], topk_idx int32 [N, K],
+ *     topk_p fp32 [N, K].  Element type of H / W / logits is kd_problem.dtype.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream).  Host-checkable errors (shapes, NULL
+ *     pointers, parameter ranges, unsupported combinations, a workspace that
+ *     is too small) return synchronously and enqueue nothing.
+ *   - Data-dependent errors are OR-ed into the device word `dev_status`
+ *     (KD_DEV_* bits), never raised: a label that is neither ignore_index
+ *     nor in [0, V) (its CE becomes NaN; it is never used as a memory
+ *     index -- orda-kernel README, "Parameters", ignore_index), a top-K id
+ *     outside [0, V) or repeated in a row, a bounded device wait that timed
+ *     out.  The caller zeroes dev_status before the call and reads it after
+ *     synchronising (unless assume_valid_labels is set and it opts out).
+ *   - No exception crosses this ABI.
+ */
+#ifndef KD_H_
+#define KD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KD_ABI_VERSION 1
+
+typedef enum kd_status {
+  KD_OK = 0,
+  KD_ERR_INVALID_ARG = 1,  /* bad shape, NULL pointer, parameter out of range   */
+  KD_ERR_UNSUPPORTED = 2,  /* valid but unsupported combination / layout      */
+  KD_ERR_WORKSPACE = 3,    /* workspace NULL or smaller than required          */
+  KD_ERR_BAD_LABEL = 4,    /* reported through dev_status only                 */
+  KD_ERR_BAD_TOPK = 5,     /* reported through dev_status only                 */
+  KD_ERR_TIMEOUT = 6,      /* reported through dev_status only                 */
+  KD_ERR_CUDA = 7,         /* a CUDA runtime/driver call failed                */
+  KD_ERR_NO_DEVICE = 8     /* current device is not an sm_103 GPU              */
+} kd_status;
+
+/* bits OR-ed into *dev_status by the kernels */
+#define KD_DEV_BAD_LABEL 0x1u
+#define KD_DEV_BAD_TOPK 0x2u
+#define KD_DEV_TIMEOUT 0x4u
+
+typedef enum kd_dtype { KD_BF16 = 0, KD_FP32 = 1 } kd_dtype;
+
+/* orda-kernel README, "Quickstart" (student hidden + weight) and flash_kd
+ * (already-materialised student logits). */
+typedef enum kd_student_kind { KD_STUDENT_HIDDEN = 0, KD_STUDENT_LOGITS = 1 } kd_student_kind;
+
+/* orda-kernel README, "Teacher descriptors": TiedTeacher (teacher hidden
+ * through the student's W_s), SeparateTeacher / PrecomputedTeacher with
+ * teacher_hidden + teacher_weight (own W_t), PrecomputedTeacher(logits=...);
+ * Full-Chunked-KL-Loss README, "Methods": cached top-K probabilities.
+ * KD_TEACHER_NONE: plain fused linear + CE (no KL, no teacher). */
+typedef enum kd_teacher_kind {
+  KD_TEACHER_NONE = 0,
+  KD_TEACHER_TIED = 1,
+  KD_TEACHER_SEPARATE = 2,
+  KD_TEACHER_LOGITS = 3,
+  KD_TEACHER_TOPK = 4
+} kd_teacher_kind;
+
+/* orda-kernel README, "KL variants" (teacher-detached subset). */
+typedef enum kd_variant {
+  KD_KL_FORWARD = 0,  /* KL(q||p)                                   */
+  KD_KL_REVERSE = 1,  /* KL(p||q)                                   */
+  KD_KL_JEFFREYS = 2, /* KL(q||p) + KL(p||q)                        */
+  KD_KL_SKEW_JS = 3   /* (1-b) KL(q||m) + b KL(p||m), m=(1-b)q+bp   */
+} kd_variant;
+
+typedef enum kd_reduction { KD_REDUCE_MEAN = 0, KD_REDUCE_SUM = 1 } kd_reduction;
+
+/* Problem description (host memory, read during the call only). */
+typedef struct kd_problem {
+  int64_t n_tokens;      /* N >= 0                                            */
+  int64_t vocab;         /* V >= 1                                            */
+  int64_t d_student;     /* D_s (hidden students), multiple of 8 for bf16     */
+  int64_t d_teacher;     /* D_t (separate teachers; tied uses D_s)            */
+  int64_t topk;          /* K (top-K teachers), 1..1024                       */
+  int32_t dtype;         /* kd_dtype of H, W and logits                       */
+  int32_t student;       /* kd_student_kind                                   */
+  int32_t teacher;       /* kd_teacher_kind                                   */
+  int32_t variant;       /* kd_variant                                        */
+  int32_t reduction;     /* kd_reduction                                      */
+  float t_student;       /* T_s > 0 (kl_temperature)                          */
+  float t_teacher;       /* T_t > 0 (kl_teacher_temperature; set = T_s)       */
+  float w_student_ce;    /* >= 0, finite                                      */
+  float w_teacher_ce;    /* >= 0, finite; 0 for top-K                         */
+  float w_kl;            /* >= 0, finite                                      */
+  float beta;            /* skew-JS b in (0,1)                                */
+  int64_t ignore_index;  /* label value excluded from CE and KL               */
+  int64_t num_batch_labels; /* > 0: mean divides by this instead of N_valid  */
+  int32_t assume_valid_labels; /* 1: caller promises labels in range          */
+  int32_t reserved0;
+  int64_t vocab_chunk;   /* backward G-workspace vocab chunk (0 = auto); the  */
+  int64_t seq_chunk;     /* token chunk (0 = auto). Results do not depend on  */
+                         /* either beyond rounding (flash_kd chunk_size,      */
+                         /* Full-Chunked-KL-Loss --chunk-sizes: memory knobs). */
+} kd_problem;
+
+/* Input tensors (device pointers; NULL where the problem does not use one). */
+typedef struct kd_inputs {
+  const void* h_s;       /* [N, D_s]  student hidden (KD_STUDENT_HIDDEN)      */
+  const void* w_s;       /* [V, D_s]  student head weight                     */
+  const void* logits_s;  /* [N, V]    student logits (KD_STUDENT_LOGITS)      */
+  const void* h_t;       /* [N, D_t]  teacher hidden (TIED: D_t = D_s)        */
+  const void* w_t;       /* [V, D_t]  teacher head weight (SEPARATE)          */
+  const void* logits_t;  /* [N, V]    teacher logits (KD_TEACHER_LOGITS)      */
+  const int64_t* labels; /* [N] or NULL: every token valid, no CE allowed     */
+  const int32_t* topk_idx; /* [N, K] distinct ids in [0, V), any order        */
+  const float* topk_p;   /* [N, K] teacher probabilities (not renormalised)   */
+} kd_inputs;
+
+/* Number of floats per token in the saved statistics written by kd_fwd and
+ * read by kd_bwd: logsumexp(z_s), logsumexp(a_s), logsumexp(z_t),
+ * logsumexp(a_t), KL(p||q), KL(p||m), top-K mass M, reserved. */
+#define KD_STATS_PER_TOKEN 8
+
+/* Bytes of device workspace kd_fwd and kd_bwd need for this problem on the
+ * current device.  Either output pointer may be NULL. */
+kd_status kd_workspace_size(const kd_problem* problem, size_t* fwd_bytes, size_t* bwd_bytes);
+
+/* Forward.  Writes per-token outputs (fp32 [N]; any may be NULL to skip):
+ *   ce_s  student CE (0 on ignored tokens; NaN on a bad label),
+ *   ce_t  teacher CE (tied / separate / logits teachers),
+ *   kl    raw per-token divergence of `variant` (NOT multiplied by T_s^2,
+ *         flash_kd "Returns"; 0 on ignored tokens),
+ *   stats [N, KD_STATS_PER_TOKEN] saved statistics for kd_bwd,
+ *   loss  one fp32 device scalar (the weighted, reduced loss).
+ * workspace: device scratch of ws_bytes >= kd_workspace_size().fwd_bytes,
+ * 256-byte aligned.  Its contents need not be initialised. */
+kd_status kd_fwd(const kd_problem* problem, const kd_inputs* inputs, float* ce_s, float* ce_t,
+                 float* kl, float* stats, float* loss, uint32_t* dev_status, void* workspace,
+                 size_t ws_bytes, void* stream);
+
+/* Backward.  Reads `stats` from a kd_fwd on the same inputs (it may be
+ * reused for several backward calls).  The upstream gradient of `loss` is
+ * grad_scale * (*d_loss) (d_loss is a device fp32 scalar, or NULL for 1).
+ * Writes (overwrites) the requested gradients, each in kd_problem.dtype;
+ * NULL skips that gradient:
+ *   d_h_s      [N, D_s] d loss / d H_s      (hidden students)
+ *   d_w_s      [V, D_s] d loss / d W_s      (hidden students; a tied
+ *              teacher's CE term also flows into it -- orda-kernel README,
+ *              "Teacher descriptors", tied teachers share the weight)
+ *   d_logits_s [N, V]   d loss / d z_s      (logit students)
+ * The teacher is detached from every KL variant (orda-kernel README, "KL
+ * variants").  Ignored tokens get exactly zero gradient rows. */
+kd_status kd_bwd(const kd_problem* problem, const kd_inputs* inputs, const float* stats,
+                 const float* d_loss, float grad_scale, void* d_h_s, void* d_w_s,
+                 void* d_logits_s, uint32_t* dev_status, void* workspace, size_t ws_bytes,
+                 void* stream);
+
+/* Static description of a status code. */
+const char* kd_status_string(kd_status status);
+
+/* 1 if `device` is a GPU this library's kernels run on (compute capability
+ * 10.3, i.e. sm_103), else 0 -- the analogue of orda-kernel's
+ * is_available() (orda-kernel README, "Installation"). */
+int kd_device_supported(int device);
+
+/* KD_ABI_VERSION of the loaded library. */
+int kd_abi_version(void);
+
+/* Diagnostic for validating the tensor-core GEMM core on its own (not part of
+ * the loss): C[M, N] = A[M, K] B[N, K]^T with bf16 A, B (row-major, K
+ * contiguous, K a multiple of 8, 16-byte aligned) and fp32 C (row-major,
+ * pitch N), accumulated in fp32 on tcgen05 tensor cores.  Device pointers,
+ * asynchronous on `stream`.  This is the operation the backward applies to
+ * form dH = G W and dW = G^T H from a gradient chunk G. */
+kd_status kd_diag_gemm_bf16(const void* a, const void* b, float* c, int64_t m, int64_t n,
+                            int64_t k, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KD_H_ */

@@ -1,0 +1,770 @@
+// C ABI of the fused LM-head + CE + KL distillation loss: argument
+// validation, the per-problem plan (which kernel family, vocabulary splits,
+// backward chunking, workspace layout) and the launch sequence on the
+// caller's stream.  The library never allocates device memory.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+
+#include "../../include/kd.h"
+#include "kd_internal.h"
+
+using namespace kd;
+
+namespace {
+
+enum Path { PATH_STREAM = 0, PATH_SIMT = 1, PATH_TC = 2 };
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct Layout {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes);
+    return o;
+  }
+};
+
+struct Plan {
+  Path path;
+  bool s_gemm, s_logits, t_gemm, t_logits, topk, has_t, tied, is_bf16;
+  int64_t n, v, ds, dt;
+  Consts c;
+  int nsm;
+  int n_splits;   // forward vocabulary splits
+  int n_parts;    // partial records per row
+  int64_t R, C;   // backward chunk (rows x vocabulary columns)
+  // forward workspace
+  size_t f_count, f_ce_s, f_ce_t, f_kl, f_stats, f_part, f_sidx, f_sp, f_mass, f_ent, f_bytes;
+  // backward workspace
+  size_t b_count, b_scale, b_sidx, b_sp, b_mass, b_ent, b_wt, b_hst, b_htt, b_g, b_gT, b_gtT,
+      b_dh, b_dw, b_bytes;
+  int64_t ldv, ldn;  // pitches of W^T [D, ldv] and H^T [D, ldn]
+};
+
+bool finite_nonneg(float x) { return std::isfinite(x) && x >= 0.f; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+kd_status check_problem(const kd_problem* p) {
+  if (!p) return KD_ERR_INVALID_ARG;
+  if (p->n_tokens < 0 || p->vocab < 1 || p->n_tokens > (int64_t)1 << 31 ||
+      p->vocab > (int64_t)1 << 30)
+    return KD_ERR_INVALID_ARG;
+  if (p->dtype != KD_BF16 && p->dtype != KD_FP32) return KD_ERR_INVALID_ARG;
+  if (p->student != KD_STUDENT_HIDDEN && p->student != KD_STUDENT_LOGITS)
+    return KD_ERR_INVALID_ARG;
+  if (p->teacher < KD_TEACHER_NONE || p->teacher > KD_TEACHER_TOPK) return KD_ERR_INVALID_ARG;
+  if (p->variant < KD_KL_FORWARD || p->variant > KD_KL_SKEW_JS) return KD_ERR_INVALID_ARG;
+  if (p->reduction != KD_REDUCE_MEAN && p->reduction != KD_REDUCE_SUM) return KD_ERR_INVALID_ARG;
+  // orda-kernel README, "Parameters": term weights finite and >= 0
+  if (!finite_nonneg(p->w_student_ce) || !finite_nonneg(p->w_teacher_ce) ||
+      !finite_nonneg(p->w_kl))
+    return KD_ERR_INVALID_ARG;
+  if (!(std::isfinite(p->t_student) && p->t_student > 0.f) ||
+      !(std::isfinite(p->t_teacher) && p->t_teacher > 0.f))
+    return KD_ERR_INVALID_ARG;
+  // orda-kernel README, "KL variants": kl_beta in (0, 1) for the skew family
+  if (p->variant == KD_KL_SKEW_JS && !(p->beta > 0.f && p->beta < 1.f)) return KD_ERR_INVALID_ARG;
+  if (p->student == KD_STUDENT_HIDDEN && p->d_student < 1) return KD_ERR_INVALID_ARG;
+  if (p->teacher == KD_TEACHER_SEPARATE && p->d_teacher < 1) return KD_ERR_INVALID_ARG;
+  if (p->teacher == KD_TEACHER_TIED) {
+    if (p->student != KD_STUDENT_HIDDEN) return KD_ERR_INVALID_ARG;
+    if (p->d_teacher != 0 && p->d_teacher != p->d_student) return KD_ERR_INVALID_ARG;
+  }
+  if (p->teacher == KD_TEACHER_TOPK) {
+    if (p->topk < 1 || p->topk > 1024 || p->topk > p->vocab) return KD_ERR_INVALID_ARG;
+    if (p->w_teacher_ce != 0.f) return KD_ERR_UNSUPPORTED;  // no teacher logits
+  }
+  if (p->teacher == KD_TEACHER_NONE && p->w_teacher_ce != 0.f) return KD_ERR_INVALID_ARG;
+  return KD_OK;
+}
+
+kd_status check_inputs(const kd_problem* p, const kd_inputs* in) {
+  if (!in) return KD_ERR_INVALID_ARG;
+  if (p->n_tokens == 0) return KD_OK;
+  if (p->student == KD_STUDENT_HIDDEN && (!in->h_s || !in->w_s)) return KD_ERR_INVALID_ARG;
+  if (p->student == KD_STUDENT_LOGITS && !in->logits_s) return KD_ERR_INVALID_ARG;
+  switch (p->teacher) {
+    case KD_TEACHER_TIED:
+      if (!in->h_t) return KD_ERR_INVALID_ARG;
+      break;
+    case KD_TEACHER_SEPARATE:
+      if (!in->h_t || !in->w_t) return KD_ERR_INVALID_ARG;
+      break;
+    case KD_TEACHER_LOGITS:
+      if (!in->logits_t) return KD_ERR_INVALID_ARG;
+      break;
+    case KD_TEACHER_TOPK:
+      if (!in->topk_idx || !in->topk_p) return KD_ERR_INVALID_ARG;
+      break;
+    default:
+      break;
+  }
+  // CE needs labels (flash_kd: per-token CE against ground-truth labels)
+  if (!in->labels && (p->w_student_ce != 0.f || p->w_teacher_ce != 0.f)) return KD_ERR_INVALID_ARG;
+  return KD_OK;
+}
+
+// Host copy of the constants the kernels use.
+Consts make_consts(const kd_problem* p, bool has_labels, bool has_t) {
+  Consts c;
+  c.inv_ts = 1.f / p->t_student;
+  c.inv_tt = 1.f / p->t_teacher;
+  c.k_s1 = kL2E;
+  c.k_sT = kL2E / p->t_student;
+  c.k_t1 = kL2E;
+  c.k_tT = kL2E / p->t_teacher;
+  c.beta = p->beta;
+  const float b = (p->beta > 0.f && p->beta < 1.f) ? p->beta : 0.5f;
+  c.log_b = std::log(b);
+  c.log_1mb = std::log1p(-b);
+  c.need_s1 = has_labels ? 1 : 0;
+  c.need_t1 = (has_labels && has_t) ? 1 : 0;
+  c.kl_mode = 0;
+  if (has_t) {
+    if (p->variant == KD_KL_FORWARD) c.kl_mode = 1;
+    else if (p->variant == KD_KL_REVERSE) c.kl_mode = 2;
+    else if (p->variant == KD_KL_JEFFREYS) c.kl_mode = 3;
+  }
+  return c;
+}
+
+// Forward vocabulary split: m_tiles * splits items spread over the persistent
+// CTAs with the smallest makespan in tiles (plus a small per-item cost for the
+// partial record).
+int choose_splits(int64_t m_tiles, int64_t n_tiles, int nsm) {
+  int best = 1;
+  double best_cost = 1e300;
+  const int64_t max_s = std::min<int64_t>(n_tiles, 4096);
+  for (int64_t s = 1; s <= max_s; ++s) {
+    const int64_t items = m_tiles * s;
+    const double waves = (double)cdiv(items, nsm);
+    const double cost = waves * (double)cdiv(n_tiles, s) + 0.02 * waves;
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = (int)s;
+    }
+  }
+  return best;
+}
+
+// Backward chunk (R rows x C columns of G).  Cost model in bytes: every extra
+// vocabulary chunk re-reads and re-writes the fp32 dH accumulator, every extra
+// row chunk the fp32 dW accumulator, plus a fixed cost per chunk.  A chunk
+// holds at most budget_elems elements and never more than N*V/8, so no
+// (tokens x vocab) matrix is ever allocated.
+void choose_chunk(const kd_problem* p, int64_t budget_elems, int64_t col_quant, int64_t& R,
+                  int64_t& C) {
+  const int64_t n = std::max<int64_t>(p->n_tokens, 1), v = p->vocab;
+  const int64_t d = p->student == KD_STUDENT_HIDDEN ? p->d_student : 1;
+  const int64_t cap = std::max<int64_t>(col_quant * 128, std::min<int64_t>(budget_elems, n * v / 8));
+  int64_t best_r = 128, best_c = col_quant;
+  double best = 1e300;
+  for (int64_t r = round_up(n, 128);; r = round_up(r / 2, 128)) {
+    int64_t rr = p->seq_chunk > 0 ? round_up(p->seq_chunk, 128) : r;
+    int64_t c = std::min<int64_t>(round_up(v, col_quant), cap / rr / col_quant * col_quant);
+    if (c < col_quant) c = col_quant;
+    if (p->vocab_chunk > 0) c = round_up(p->vocab_chunk, col_quant);
+    const int64_t nr = cdiv(n, rr), nc = cdiv(v, c);
+    const double cost = (nc > 1 ? (double)nc * n * d * 8.0 : 0.0) +
+                        (nr > 1 ? (double)nr * v * d * 8.0 : 0.0) + (double)nr * nc * 1.5e8;
+    if (cost < best) {
+      best = cost;
+      best_r = rr;
+      best_c = c;
+    }
+    if (p->seq_chunk > 0 || r <= 128) break;
+  }
+  R = std::min<int64_t>(best_r, round_up(n, 128));
+  C = std::min<int64_t>(best_c, round_up(v, col_quant));
+}
+
+kd_status make_plan(const kd_problem* p, bool has_labels, Plan& P) {
+  memset(&P, 0, sizeof(P));
+  P.n = p->n_tokens;
+  P.v = p->vocab;
+  P.is_bf16 = p->dtype == KD_BF16;
+  P.s_gemm = p->student == KD_STUDENT_HIDDEN;
+  P.s_logits = !P.s_gemm;
+  P.t_gemm = p->teacher == KD_TEACHER_TIED || p->teacher == KD_TEACHER_SEPARATE;
+  P.t_logits = p->teacher == KD_TEACHER_LOGITS;
+  P.topk = p->teacher == KD_TEACHER_TOPK;
+  P.tied = p->teacher == KD_TEACHER_TIED;
+  P.has_t = P.t_gemm || P.t_logits;
+  P.ds = P.s_gemm ? p->d_student : 0;
+  P.dt = p->teacher == KD_TEACHER_TIED ? p->d_student
+         : p->teacher == KD_TEACHER_SEPARATE ? p->d_teacher
+                                             : 0;
+  P.c = make_consts(p, has_labels, P.has_t);
+  P.nsm = std::max(1, tc_num_sms());
+  if (!P.s_gemm && !P.t_gemm) P.path = PATH_STREAM;
+  else if (!P.is_bf16) P.path = PATH_SIMT;
+  else P.path = PATH_TC;
+  if (P.path == PATH_TC) {
+    // TMA: row pitches must be multiples of 16 bytes
+    if ((P.s_gemm && P.ds % 8) || (P.t_gemm && P.dt % 8)) return KD_ERR_UNSUPPORTED;
+  }
+  if (P.path == PATH_SIMT && P.s_logits) return KD_ERR_UNSUPPORTED;  // fp32 logits + GEMM teacher
+  const int64_t n = P.n, v = P.v;
+  // ---- forward
+  Layout f;
+  P.f_count = f.take(16);
+  P.f_ce_s = f.take(n * 4);
+  P.f_ce_t = f.take(n * 4);
+  P.f_kl = f.take(n * 4);
+  P.f_stats = f.take(n * KD_STATS_PER_TOKEN * 4);
+  if (P.topk) {
+    P.f_sidx = f.take(n * p->topk * 4);
+    P.f_sp = f.take(n * p->topk * 4);
+    P.f_mass = f.take(n * 4);
+    P.f_ent = f.take(n * 4);
+  }
+  if (P.path == PATH_TC) {
+    const int bn = (P.s_gemm && P.t_gemm) ? 128 : 256;
+    P.n_splits = choose_splits(cdiv(std::max<int64_t>(n, 1), 128), cdiv(v, bn), P.nsm);
+    P.n_parts = 2 * P.n_splits;
+  } else if (P.path == PATH_SIMT) {
+    const int64_t mt = cdiv(std::max<int64_t>(n, 1), 32), nt = cdiv(v, 64);
+    P.n_splits = (int)std::max<int64_t>(1, std::min<int64_t>(nt, cdiv(4 * P.nsm, mt)));
+    P.n_parts = P.n_splits;
+  }
+  if (P.n_parts) P.f_part = f.take((size_t)P.n_parts * n * kRec * 4);
+  P.f_bytes = f.off;
+  // ---- backward
+  Layout b;
+  P.b_count = b.take(16);
+  P.b_scale = b.take(n * 4);
+  if (P.topk) {
+    P.b_sidx = b.take(n * p->topk * 4);
+    P.b_sp = b.take(n * p->topk * 4);
+    P.b_mass = b.take(n * 4);
+    P.b_ent = b.take(n * 4);
+  }
+  if (P.path == PATH_TC) {
+    choose_chunk(p, (int64_t)16 << 20, 256, P.R, P.C);
+    P.ldv = round_up(v, 8);
+    P.ldn = round_up(n, 8);
+    if (P.s_gemm) {
+      P.b_wt = b.take(P.ds * P.ldv * 2);               // W_s^T
+      P.b_hst = b.take(P.ds * P.ldn * 2);              // H_s^T
+      if (P.tied) P.b_htt = b.take(P.ds * P.ldn * 2);  // H_t^T
+      P.b_g = b.take(P.R * P.C * 2);
+      P.b_gT = b.take(P.C * P.R * 2);
+      if (P.tied) P.b_gtT = b.take(P.C * P.R * 2);
+      if (cdiv(v, P.C) > 1) P.b_dh = b.take(n * P.ds * 4);
+      if (cdiv(n, P.R) > 1) P.b_dw = b.take(v * P.ds * 4);
+    }
+  } else if (P.path == PATH_SIMT) {
+    choose_chunk(p, (int64_t)8 << 20, 64, P.R, P.C);
+    P.b_g = b.take(P.R * P.C * 4);
+    if (P.tied) P.b_gT = b.take(P.R * P.C * 4);  // teacher-CE gradient tile
+  }
+  P.b_bytes = b.off;
+  return KD_OK;
+}
+
+template <class T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+kd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KD_OK : KD_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int kd_abi_version(void) { return KD_ABI_VERSION; }
+
+const char* kd_status_string(kd_status s) {
+  switch (s) {
+    case KD_OK: return "ok";
+    case KD_ERR_INVALID_ARG: return "invalid argument";
+    case KD_ERR_UNSUPPORTED: return "unsupported combination or layout";
+    case KD_ERR_WORKSPACE: return "workspace missing or too small";
+    case KD_ERR_BAD_LABEL: return "label outside [0, vocab) that is not ignore_index";
+    case KD_ERR_BAD_TOPK: return "top-K id outside [0, vocab) or repeated in a row";
+    case KD_ERR_TIMEOUT: return "a bounded device wait timed out";
+    case KD_ERR_CUDA: return "CUDA error";
+    case KD_ERR_NO_DEVICE: return "no supported (sm_103) CUDA device";
+  }
+  return "unknown status";
+}
+
+int kd_device_supported(int device) {
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess)
+    return 0;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess)
+    return 0;
+  return (major == 10 && minor == 3) ? 1 : 0;
+}
+
+}  // extern "C"
+
+namespace {
+kd_status check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KD_ERR_NO_DEVICE;
+  return kd_device_supported(dev) ? KD_OK : KD_ERR_NO_DEVICE;
+}
+}  // namespace
+
+extern "C" {
+
+kd_status kd_workspace_size(const kd_problem* problem, size_t* fwd_bytes, size_t* bwd_bytes) {
+  kd_status st = check_problem(problem);
+  if (st != KD_OK) return st;
+  Plan P;
+  st = make_plan(problem, true, P);
+  if (st != KD_OK) return st;
+  if (fwd_bytes) *fwd_bytes = P.f_bytes;
+  if (bwd_bytes) *bwd_bytes = P.b_bytes;
+  return KD_OK;
+}
+
+kd_status kd_fwd(const kd_problem* problem, const kd_inputs* in, float* ce_s, float* ce_t,
+                 float* kl, float* stats, float* loss, uint32_t* dev_status, void* workspace,
+                 size_t ws_bytes, void* stream_) {
+  kd_status st = check_problem(problem);
+  if (st != KD_OK) return st;
+  st = check_inputs(problem, in);
+  if (st != KD_OK) return st;
+  const kd_problem* p = problem;
+  Plan P;
+  st = make_plan(p, in->labels != nullptr, P);
+  if (st != KD_OK) return st;
+  if (!workspace || ws_bytes < P.f_bytes || (reinterpret_cast<uintptr_t>(workspace) % kAlign))
+    return KD_ERR_WORKSPACE;
+  st = check_device();
+  if (st != KD_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream_);
+  const int64_t n = P.n;
+  float* w_ce_s = ce_s ? ce_s : at<float>(workspace, P.f_ce_s);
+  float* w_ce_t = ce_t ? ce_t : at<float>(workspace, P.f_ce_t);
+  float* w_kl = kl ? kl : at<float>(workspace, P.f_kl);
+  float* w_stats = stats ? stats : at<float>(workspace, P.f_stats);
+  int32_t* count = at<int32_t>(workspace, P.f_count);
+  if (n == 0) {
+    if (loss && cudaMemsetAsync(loss, 0, sizeof(float), s) != cudaSuccess) return KD_ERR_CUDA;
+    return KD_OK;
+  }
+  if (cudaMemsetAsync(count, 0, 16, s) != cudaSuccess) return KD_ERR_CUDA;
+  if (in->labels) launch_label_check(in->labels, n, P.v, p->ignore_index, count, dev_status, s);
+  int32_t* sidx = nullptr;
+  float *sp = nullptr, *mass = nullptr, *ent = nullptr;
+  if (P.topk) {
+    sidx = at<int32_t>(workspace, P.f_sidx);
+    sp = at<float>(workspace, P.f_sp);
+    mass = at<float>(workspace, P.f_mass);
+    ent = at<float>(workspace, P.f_ent);
+    launch_topk_prep(in->topk_idx, in->topk_p, n, (int)p->topk, P.v, sidx, sp, mass, ent,
+                     dev_status, s);
+  }
+  const bool js = P.has_t && p->variant == KD_KL_SKEW_JS;
+  if (P.path == PATH_STREAM) {
+    StreamArgs a;
+    memset(&a, 0, sizeof(a));
+    a.zs = in->logits_s;
+    a.zt = P.t_logits ? in->logits_t : nullptr;
+    a.n = n;
+    a.vocab = P.v;
+    a.c = P.c;
+    a.variant = p->variant;
+    a.is_bf16 = P.is_bf16;
+    a.topk = P.topk;
+    a.k = (int)p->topk;
+    a.sidx = sidx;
+    a.sp = sp;
+    a.mass = mass;
+    a.ent = ent;
+    a.labels = in->labels;
+    a.ignore = p->ignore_index;
+    a.ce_s = w_ce_s;
+    a.ce_t = w_ce_t;
+    a.kl = w_kl;
+    a.stats = w_stats;
+    launch_stream_fwd(a, s);
+  } else {
+    float* part = at<float>(workspace, P.f_part);
+    CombineArgs cb;
+    memset(&cb, 0, sizeof(cb));
+    cb.partials = part;
+    cb.n_parts = P.n_parts;
+    cb.n = n;
+    cb.vocab = P.v;
+    cb.c = P.c;
+    cb.variant = p->variant;
+    cb.has_t = P.has_t;
+    cb.topk = P.topk;
+    cb.labels = in->labels;
+    cb.ignore = p->ignore_index;
+    cb.mass = mass;
+    cb.ent = ent;
+    cb.ce_s = w_ce_s;
+    cb.ce_t = w_ce_t;
+    cb.kl = w_kl;
+    cb.stats = w_stats;
+    for (int pass = 0; pass < (js ? 2 : 1); ++pass) {
+      if (P.path == PATH_SIMT) {
+        SimtArgs a;
+        memset(&a, 0, sizeof(a));
+        a.h_s = static_cast<const float*>(in->h_s);
+        a.w_s = static_cast<const float*>(in->w_s);
+        a.h_t = static_cast<const float*>(in->h_t);
+        a.w_t = static_cast<const float*>(in->w_t);
+        a.zt = static_cast<const float*>(in->logits_t);
+        a.n = n;
+        a.vocab = P.v;
+        a.d_s = P.ds;
+        a.d_t = P.dt;
+        a.teacher = p->teacher;
+        a.c = P.c;
+        a.variant = p->variant;
+        a.labels = in->labels;
+        a.ignore = p->ignore_index;
+        a.sidx = sidx;
+        a.sp = sp;
+        a.k = (int)p->topk;
+        a.n_splits = P.n_splits;
+        a.partials = part;
+        a.stats = w_stats;
+        a.js_pass = pass;
+        launch_simt_fwd(a, s);
+      } else {
+        TcFwdArgs a;
+        memset(&a, 0, sizeof(a));
+        a.h_s = in->h_s;
+        a.w_s = in->w_s;
+        a.h_t = in->h_t;
+        a.w_t = p->teacher == KD_TEACHER_SEPARATE ? in->w_t : nullptr;
+        a.zs_logits = P.s_logits ? in->logits_s : nullptr;
+        a.zt_logits = P.t_logits ? in->logits_t : nullptr;
+        a.n = n;
+        a.vocab = P.v;
+        a.d_s = P.ds;
+        a.d_t = P.dt;
+        a.s_gemm = P.s_gemm;
+        a.t_gemm = P.t_gemm;
+        a.s_logits = P.s_logits;
+        a.t_logits = P.t_logits;
+        a.topk = P.topk;
+        a.c = P.c;
+        a.variant = p->variant;
+        a.labels = in->labels;
+        a.ignore = p->ignore_index;
+        a.sidx = sidx;
+        a.sp = sp;
+        a.k = (int)p->topk;
+        a.n_splits = P.n_splits;
+        a.partials = part;
+        a.stats = w_stats;
+        a.js_pass = pass;
+        a.status = dev_status;
+        if (launch_tc_fwd(a, P.nsm, s) != 0) return KD_ERR_CUDA;
+      }
+      cb.js_pass = pass;
+      launch_combine(cb, s);
+    }
+  }
+  if (loss) {
+    ReduceArgs r;
+    memset(&r, 0, sizeof(r));
+    r.ce_s = w_ce_s;
+    r.ce_t = w_ce_t;
+    r.kl = w_kl;
+    r.labels = in->labels;
+    r.n = n;
+    r.ignore = p->ignore_index;
+    r.w_sce = p->w_student_ce;
+    r.w_tce = P.has_t ? p->w_teacher_ce : 0.f;
+    r.w_kl_t2 = (P.has_t || P.topk) ? p->w_kl * p->t_student * p->t_student : 0.f;
+    r.reduction = p->reduction;
+    r.num_batch_labels = p->num_batch_labels;
+    r.count = count;
+    r.loss = loss;
+    launch_loss_reduce(r, s);
+  }
+  return cuda_status(cudaGetLastError());
+}
+
+kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* stats,
+                 const float* d_loss, float grad_scale, void* d_h_s, void* d_w_s,
+                 void* d_logits_s, uint32_t* dev_status, void* workspace, size_t ws_bytes,
+                 void* stream_) {
+  kd_status st = check_problem(problem);
+  if (st != KD_OK) return st;
+  st = check_inputs(problem, in);
+  if (st != KD_OK) return st;
+  const kd_problem* p = problem;
+  if (!std::isfinite(grad_scale)) return KD_ERR_INVALID_ARG;
+  if (p->student == KD_STUDENT_HIDDEN && d_logits_s) return KD_ERR_INVALID_ARG;
+  if (p->student == KD_STUDENT_LOGITS && (d_h_s || d_w_s)) return KD_ERR_INVALID_ARG;
+  Plan P;
+  st = make_plan(p, in->labels != nullptr, P);
+  if (st != KD_OK) return st;
+  if (P.n == 0 || (!d_h_s && !d_w_s && !d_logits_s)) return KD_OK;
+  if (!stats) return KD_ERR_INVALID_ARG;
+  if (!workspace || ws_bytes < P.b_bytes || (reinterpret_cast<uintptr_t>(workspace) % kAlign))
+    return KD_ERR_WORKSPACE;
+  st = check_device();
+  if (st != KD_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream_);
+  const int64_t n = P.n, v = P.v;
+  int32_t* count = at<int32_t>(workspace, P.b_count);
+  float* scale = at<float>(workspace, P.b_scale);
+  if (cudaMemsetAsync(count, 0, 16, s) != cudaSuccess) return KD_ERR_CUDA;
+  if (in->labels) launch_label_check(in->labels, n, v, p->ignore_index, count, dev_status, s);
+  launch_row_scale(in->labels, n, p->ignore_index, grad_scale, d_loss, p->reduction,
+                   p->num_batch_labels, count, scale, s);
+  int32_t* sidx = nullptr;
+  float *sp = nullptr, *mass = nullptr, *ent = nullptr;
+  if (P.topk) {
+    sidx = at<int32_t>(workspace, P.b_sidx);
+    sp = at<float>(workspace, P.b_sp);
+    mass = at<float>(workspace, P.b_mass);
+    ent = at<float>(workspace, P.b_ent);
+    launch_topk_prep(in->topk_idx, in->topk_p, n, (int)p->topk, v, sidx, sp, mass, ent,
+                     dev_status, s);
+  }
+  const float w_kl_ts = (P.has_t || P.topk) ? p->w_kl * p->t_student : 0.f;
+  const float w_tce = (P.tied && d_w_s) ? p->w_teacher_ce : 0.f;
+  if (P.path == PATH_STREAM) {
+    StreamArgs a;
+    memset(&a, 0, sizeof(a));
+    a.zs = in->logits_s;
+    a.zt = P.t_logits ? in->logits_t : nullptr;
+    a.n = n;
+    a.vocab = v;
+    a.c = P.c;
+    a.variant = p->variant;
+    a.is_bf16 = P.is_bf16;
+    a.topk = P.topk;
+    a.k = (int)p->topk;
+    a.sidx = sidx;
+    a.sp = sp;
+    a.labels = in->labels;
+    a.ignore = p->ignore_index;
+    a.stats = const_cast<float*>(stats);
+    a.row_scale = scale;
+    a.w_sce = p->w_student_ce;
+    a.w_kl_ts = w_kl_ts;
+    a.dz = d_logits_s;
+    launch_stream_bwd(a, s);
+    return cuda_status(cudaGetLastError());
+  }
+  const int64_t R = P.R, C = P.C;
+  const int64_t nr = cdiv(n, R), nc = cdiv(v, C);
+  if (P.path == PATH_SIMT) {
+    float* g = at<float>(workspace, P.b_g);
+    float* gt = w_tce != 0.f ? at<float>(workspace, P.b_gT) : nullptr;
+    const int64_t D = P.ds;
+    for (int64_t ri = 0; ri < nr; ++ri) {
+      const int64_t r0 = ri * R, rc = std::min(R, n - r0);
+      for (int64_t ci = 0; ci < nc; ++ci) {
+        const int64_t c0 = ci * C, cc = std::min(C, v - c0);
+        SimtArgs a;
+        memset(&a, 0, sizeof(a));
+        a.h_s = static_cast<const float*>(in->h_s);
+        a.w_s = static_cast<const float*>(in->w_s);
+        a.h_t = static_cast<const float*>(in->h_t);
+        a.w_t = static_cast<const float*>(in->w_t);
+        a.zt = static_cast<const float*>(in->logits_t);
+        a.n = n;
+        a.vocab = v;
+        a.d_s = P.ds;
+        a.d_t = P.dt;
+        a.teacher = p->teacher;
+        a.c = P.c;
+        a.variant = p->variant;
+        a.labels = in->labels;
+        a.ignore = p->ignore_index;
+        a.sidx = sidx;
+        a.sp = sp;
+        a.k = (int)p->topk;
+        a.stats = stats;
+        a.r0 = r0;
+        a.rc = rc;
+        a.c0 = c0;
+        a.cc = cc;
+        a.row_scale = scale;
+        a.w_sce = p->w_student_ce;
+        a.w_tce = w_tce;
+        a.w_kl_ts = w_kl_ts;
+        a.g = g;
+        a.gt = gt;
+        launch_simt_gprod(a, s);
+        const float* W = static_cast<const float*>(in->w_s);
+        const float* H = static_cast<const float*>(in->h_s);
+        if (d_h_s)  // dH[r0.., :] (+)= G W[c0.., :]
+          launch_simt_gemm(g, cc, 1, W + c0 * D, D, 1, static_cast<float*>(d_h_s) + r0 * D, D,
+                           rc, D, cc, ci > 0, s);
+        if (d_w_s) {  // dW[c0.., :] (+)= G^T H[r0.., :]
+          float* dw = static_cast<float*>(d_w_s) + c0 * D;
+          launch_simt_gemm(g, 1, cc, H + r0 * D, D, 1, dw, D, cc, D, rc, ri > 0, s);
+          if (gt)
+            launch_simt_gemm(gt, 1, cc, static_cast<const float*>(in->h_t) + r0 * D, D, 1, dw, D,
+                             cc, D, rc, true, s);
+        }
+      }
+    }
+    return cuda_status(cudaGetLastError());
+  }
+  // ---------------------------------------------------------------- tcgen05
+  const int64_t D = P.ds;
+  __nv_bfloat16* g = P.s_gemm ? at<__nv_bfloat16>(workspace, P.b_g) : nullptr;
+  __nv_bfloat16* gT = P.s_gemm ? at<__nv_bfloat16>(workspace, P.b_gT) : nullptr;
+  __nv_bfloat16* gtT = w_tce != 0.f ? at<__nv_bfloat16>(workspace, P.b_gtT) : nullptr;
+  __nv_bfloat16* wT = P.s_gemm ? at<__nv_bfloat16>(workspace, P.b_wt) : nullptr;
+  __nv_bfloat16* hsT = P.s_gemm ? at<__nv_bfloat16>(workspace, P.b_hst) : nullptr;
+  __nv_bfloat16* htT = (P.tied && P.s_gemm) ? at<__nv_bfloat16>(workspace, P.b_htt) : nullptr;
+  float* dh_acc = (P.s_gemm && nc > 1) ? at<float>(workspace, P.b_dh) : nullptr;
+  float* dw_acc = (P.s_gemm && nr > 1) ? at<float>(workspace, P.b_dw) : nullptr;
+  if (P.s_gemm) {
+    const __nv_bfloat16* Ws = static_cast<const __nv_bfloat16*>(in->w_s);
+    const __nv_bfloat16* Hs = static_cast<const __nv_bfloat16*>(in->h_s);
+    if (d_h_s) launch_transpose_bf16(Ws, v, D, D, wT, P.ldv, s);
+    if (d_w_s) launch_transpose_bf16(Hs, n, D, D, hsT, P.ldn, s);
+    if (gtT)
+      launch_transpose_bf16(static_cast<const __nv_bfloat16*>(in->h_t), n, D, D, htT, P.ldn, s);
+  }
+  for (int64_t ri = 0; ri < nr; ++ri) {
+    const int64_t r0 = ri * R, rc = std::min(R, n - r0);
+    for (int64_t ci = 0; ci < nc; ++ci) {
+      const int64_t c0 = ci * C, cc = std::min(C, v - c0);
+      TcGradArgs a;
+      memset(&a, 0, sizeof(a));
+      a.h_s = in->h_s;
+      a.w_s = in->w_s;
+      a.h_t = in->h_t;
+      a.w_t = p->teacher == KD_TEACHER_SEPARATE ? in->w_t : nullptr;
+      a.zs_logits = P.s_logits ? in->logits_s : nullptr;
+      a.zt_logits = P.t_logits ? in->logits_t : nullptr;
+      a.n = n;
+      a.vocab = v;
+      a.d_s = P.ds;
+      a.d_t = P.dt;
+      a.s_gemm = P.s_gemm;
+      a.s_logits = P.s_logits;
+      a.t_gemm = P.t_gemm;
+      a.t_logits = P.t_logits;
+      a.topk = P.topk;
+      a.c = P.c;
+      a.variant = p->variant;
+      a.labels = in->labels;
+      a.ignore = p->ignore_index;
+      a.sidx = sidx;
+      a.sp = sp;
+      a.k = (int)p->topk;
+      a.stats = stats;
+      a.row_scale = scale;
+      a.w_sce = p->w_student_ce;
+      a.w_tce = w_tce;
+      a.w_kl_ts = w_kl_ts;
+      a.r0 = r0;
+      a.rc = rc;
+      a.c0 = c0;
+      a.cc = cc;
+      if (P.s_logits) {  // logit students: G is the requested d z_s itself
+        a.g = static_cast<__nv_bfloat16*>(d_logits_s) + c0;
+        a.ldg = v;
+        a.gT = nullptr;
+      } else {
+        a.g = g;
+        a.ldg = C;
+        a.gT = d_w_s ? gT : nullptr;
+      }
+      a.ldgt = R;
+      a.gtT = gtT;
+      a.status = dev_status;
+      if (launch_tc_grad(a, P.nsm, s) != 0) return KD_ERR_CUDA;
+      if (P.s_logits) continue;
+      if (d_h_s) {  // dH[r0.., :] (+)= G[:, chunk] W[chunk, :]
+        TcGemmArgs m;
+        memset(&m, 0, sizeof(m));
+        m.a0 = g;
+        m.lda0 = C;
+        m.b0 = wT + c0;
+        m.ldb0 = P.ldv;
+        m.M = rc;
+        m.N = D;
+        m.K0 = cc;
+        m.status = dev_status;
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(d_h_s) + r0 * D;
+        if (nc == 1) {
+          m.mode = TC_OUT_BF16;
+        } else {
+          m.mode = ci == 0 ? TC_OUT_F32 : (ci + 1 < nc ? TC_OUT_F32_ACC : TC_OUT_F32_ACC_BF16);
+          m.c32 = dh_acc + r0 * D;
+          m.ldc32 = D;
+        }
+        m.c16 = out;
+        m.ldc16 = D;
+        if (launch_tc_gemm(m, P.nsm, s) != 0) return KD_ERR_CUDA;
+      }
+      if (d_w_s) {  // dW[chunk, :] (+)= G[:, chunk]^T H[r0.., :] (+ G_t^T H_t)
+        TcGemmArgs m;
+        memset(&m, 0, sizeof(m));
+        m.a0 = gT;
+        m.lda0 = R;
+        m.b0 = hsT + r0;
+        m.ldb0 = P.ldn;
+        m.M = cc;
+        m.N = D;
+        m.K0 = rc;
+        if (gtT) {
+          m.a1 = gtT;
+          m.lda1 = R;
+          m.b1 = htT + r0;
+          m.ldb1 = P.ldn;
+          m.K1 = rc;
+        }
+        m.status = dev_status;
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(d_w_s) + c0 * D;
+        if (nr == 1) {
+          m.mode = TC_OUT_BF16;
+        } else {
+          m.mode = ri == 0 ? TC_OUT_F32 : (ri + 1 < nr ? TC_OUT_F32_ACC : TC_OUT_F32_ACC_BF16);
+          m.c32 = dw_acc + c0 * D;
+          m.ldc32 = D;
+        }
+        m.c16 = out;
+        m.ldc16 = D;
+        if (launch_tc_gemm(m, P.nsm, s) != 0) return KD_ERR_CUDA;
+      }
+    }
+  }
+  return cuda_status(cudaGetLastError());
+}
+
+// Diagnostic: C[M, N] = A[M, K] B[N, K]^T on the tensor-core GEMM core.
+kd_status kd_diag_gemm_bf16(const void* a, const void* b, float* c, int64_t m, int64_t n,
+                            int64_t k, void* stream) {
+  if (!a || !b || !c || m < 1 || n < 1 || k < 1 || (k % 8) || !aligned16(a) || !aligned16(b))
+    return KD_ERR_INVALID_ARG;
+  kd_status st = check_device();
+  if (st != KD_OK) return st;
+  TcGemmArgs g;
+  memset(&g, 0, sizeof(g));
+  g.a0 = static_cast<const __nv_bfloat16*>(a);
+  g.b0 = static_cast<const __nv_bfloat16*>(b);
+  g.lda0 = k;
+  g.ldb0 = k;
+  g.M = m;
+  g.N = n;
+  g.K0 = k;
+  g.mode = TC_OUT_F32;
+  g.c32 = c;
+  g.ldc32 = n;
+  if (launch_tc_gemm(g, std::max(1, tc_num_sms()), static_cast<cudaStream_t>(stream)) != 0)
+    return KD_ERR_CUDA;
+  return cuda_status(cudaGetLastError());
+}
+
+}  // extern "C"

@@ -1,0 +1,317 @@
+// Device-side building blocks shared by every kernel of the fused LM-head +
+// CE + KL loss: the per-token online-softmax state, its chunk update, the
+// associative merge of two partial states, and the per-token finalisation.
+//
+// Online softmax (flash_kd API doc, module description): keep a running max
+// and rescale the running sums whenever it grows, so that the vocabulary can
+// be visited in any number of chunks with the full-row result.
+//
+// Per token the state carries, with a_s = z_s/T_s, a_t = z_t/T_t and
+// d = a_t - a_s (orda-kernel README, "KL variants": p = student, q = teacher):
+//   ms, ls1, lsT : max z_s, sum e^{z_s-ms} (T=1, for CE), sum e^{(z_s-ms)/T_s}
+//   mt, lt1, ltT : the same for the teacher
+//   qd = sum e^{a_t-Mt} d               -> E_q[d]
+//   qx = sum (e^{a_s-Mt} - e^{a_t-Mt})  -> E_q[e^{-d}] - 1
+//   pd = sum e^{a_s-Ms} (-d)            -> E_p[-d]
+//   px = sum (e^{a_t-Ms} - e^{a_s-Ms})  -> E_p[e^{d}] - 1
+// with Ms = ms/T_s, Mt = mt/T_t.  Then
+//   KL(q||p) = E_q[d] + log E_q[e^{-d}],   KL(p||q) = E_p[-d] + log E_p[e^{d}],
+// and both logs are taken as log1p of the small sums above, which keeps the
+// relative error of small divergences at fp32 rounding level instead of the
+// absolute error of a difference of two log-sum-exps.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kd.h"
+
+namespace kd {
+
+constexpr float kL2E = 1.4426950408889634f;  // log2(e)
+constexpr int kRec = 16;                     // floats per partial-state record
+
+// fields of the saved per-token statistics (KD_STATS_PER_TOKEN floats)
+enum StatField { S_LSE_S1 = 0, S_LSE_ST, S_LSE_T1, S_LSE_TT, S_KL_REV, S_KL_PM, S_MASS, S_SPARE };
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// number of valid columns in a chunk of `width` that starts `rem` columns before the end
+__device__ __forceinline__ int valid_cols(int64_t rem, int width) {
+  return rem <= 0 ? 0 : (rem >= width ? width : (int)rem);
+}
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+__device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Constants of one problem, precomputed on the host.
+struct Consts {
+  float inv_ts, inv_tt;        // 1/T_s, 1/T_t
+  float k_s1, k_sT;            // log2e, log2e/T_s   (exponent scales, student)
+  float k_t1, k_tT;            // log2e, log2e/T_t
+  float beta, log_b, log_1mb;  // b, log b, log(1-b)  (skew-JS)
+  int need_s1, need_t1;        // student / teacher CE needed (T = 1 sums)
+  int kl_mode;                 // bit0: forward cross sums, bit1: reverse cross sums
+};
+
+struct RowState {
+  float ms, ls1, lsT, mt, lt1, ltT, qd, qx, pd, px, zys, zyt, tk, jq, jp;
+
+  __device__ __forceinline__ void init() {
+    ms = mt = neg_inf();
+    ls1 = lsT = lt1 = ltT = qd = qx = pd = px = zys = zyt = tk = jq = jp = 0.f;
+  }
+  __device__ __forceinline__ void store(float* r) const {
+    float4* o = reinterpret_cast<float4*>(r);
+    o[0] = make_float4(ms, ls1, lsT, mt);
+    o[1] = make_float4(lt1, ltT, qd, qx);
+    o[2] = make_float4(pd, px, zys, zyt);
+    o[3] = make_float4(tk, jq, jp, 0.f);
+  }
+  __device__ __forceinline__ void load(const float* r) {
+    const float4* i = reinterpret_cast<const float4*>(r);
+    float4 a = i[0], b = i[1], c = i[2], d = i[3];
+    ms = a.x; ls1 = a.y; lsT = a.z; mt = a.w;
+    lt1 = b.x; ltT = b.y; qd = b.z; qx = b.w;
+    pd = c.x; px = c.y; zys = c.z; zyt = c.w;
+    tk = d.x; jq = d.y; jp = d.z;
+  }
+};
+
+// e^{(old-new)*k} with the empty-state convention (old == new covers -inf).
+__device__ __forceinline__ float rescale(float m_old, float m_new, float k) {
+  return m_old == m_new ? 1.f : ex2((m_old - m_new) * k);
+}
+
+// Associative merge of b into a (shuffles, half tiles, vocabulary splits).
+__device__ __forceinline__ void merge(RowState& a, const RowState& b, const Consts& c) {
+  {
+    const float m = fmaxf(a.ms, b.ms);
+    const float fa1 = rescale(a.ms, m, c.k_s1), fb1 = rescale(b.ms, m, c.k_s1);
+    const float faT = rescale(a.ms, m, c.k_sT), fbT = rescale(b.ms, m, c.k_sT);
+    a.ls1 = a.ls1 * fa1 + b.ls1 * fb1;
+    a.lsT = a.lsT * faT + b.lsT * fbT;
+    a.pd = a.pd * faT + b.pd * fbT;
+    a.px = a.px * faT + b.px * fbT;
+    a.ms = m;
+  }
+  {
+    const float m = fmaxf(a.mt, b.mt);
+    const float fa1 = rescale(a.mt, m, c.k_t1), fb1 = rescale(b.mt, m, c.k_t1);
+    const float faT = rescale(a.mt, m, c.k_tT), fbT = rescale(b.mt, m, c.k_tT);
+    a.lt1 = a.lt1 * fa1 + b.lt1 * fb1;
+    a.ltT = a.ltT * faT + b.ltT * fbT;
+    a.qd = a.qd * faT + b.qd * fbT;
+    a.qx = a.qx * faT + b.qx * fbT;
+    a.mt = m;
+  }
+  a.zys += b.zys;
+  a.zyt += b.zyt;
+  a.tk += b.tk;
+  a.jq += b.jq;
+  a.jp += b.jp;
+}
+
+__device__ __forceinline__ RowState shfl_xor(const RowState& s, int m) {
+  RowState o;
+  o.ms = __shfl_xor_sync(0xffffffffu, s.ms, m);
+  o.ls1 = __shfl_xor_sync(0xffffffffu, s.ls1, m);
+  o.lsT = __shfl_xor_sync(0xffffffffu, s.lsT, m);
+  o.mt = __shfl_xor_sync(0xffffffffu, s.mt, m);
+  o.lt1 = __shfl_xor_sync(0xffffffffu, s.lt1, m);
+  o.ltT = __shfl_xor_sync(0xffffffffu, s.ltT, m);
+  o.qd = __shfl_xor_sync(0xffffffffu, s.qd, m);
+  o.qx = __shfl_xor_sync(0xffffffffu, s.qx, m);
+  o.pd = __shfl_xor_sync(0xffffffffu, s.pd, m);
+  o.px = __shfl_xor_sync(0xffffffffu, s.px, m);
+  o.zys = __shfl_xor_sync(0xffffffffu, s.zys, m);
+  o.zyt = __shfl_xor_sync(0xffffffffu, s.zyt, m);
+  o.tk = __shfl_xor_sync(0xffffffffu, s.tk, m);
+  o.jq = __shfl_xor_sync(0xffffffffu, s.jq, m);
+  o.jp = __shfl_xor_sync(0xffffffffu, s.jp, m);
+  return o;
+}
+
+// Chunk update of the online state with NC columns of student (and, when
+// HAS_T, teacher) logits.  With MASKED, only the first `nvalid` columns count
+// (the ragged end of the vocabulary).
+template <int NC, bool HAS_T, bool MASKED>
+__device__ __forceinline__ void update(RowState& st, const float* zs, const float* zt,
+                                       int nvalid, const Consts& c) {
+  float cms = neg_inf(), cmt = neg_inf();
+#pragma unroll
+  for (int j = 0; j < NC; ++j) {
+    if (!MASKED || j < nvalid) {
+      cms = fmaxf(cms, zs[j]);
+      if (HAS_T) cmt = fmaxf(cmt, zt[j]);
+    }
+  }
+  if (MASKED && nvalid <= 0) return;
+  const float ms = fmaxf(st.ms, cms);
+  {
+    const float f1 = rescale(st.ms, ms, c.k_s1), fT = rescale(st.ms, ms, c.k_sT);
+    st.ls1 *= f1;
+    st.lsT *= fT;
+    st.pd *= fT;
+    st.px *= fT;
+    st.ms = ms;
+  }
+  float mt = 0.f;
+  if (HAS_T) {
+    mt = fmaxf(st.mt, cmt);
+    const float f1 = rescale(st.mt, mt, c.k_t1), fT = rescale(st.mt, mt, c.k_tT);
+    st.lt1 *= f1;
+    st.ltT *= fT;
+    st.qd *= fT;
+    st.qx *= fT;
+    st.mt = mt;
+  }
+  const float os1 = -ms * c.k_s1, osT = -ms * c.k_sT;
+  const float ot1 = -mt * c.k_t1, otT = -mt * c.k_tT;
+  float ls1 = 0.f, lsT = 0.f, lt1 = 0.f, ltT = 0.f, qd = 0.f, qx = 0.f, pd = 0.f, px = 0.f;
+  if (!HAS_T) {
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+      if (!MASKED || j < nvalid) {
+        lsT += ex2(fmaf(zs[j], c.k_sT, osT));
+        if (c.need_s1) ls1 += ex2(fmaf(zs[j], c.k_s1, os1));
+      }
+    }
+  } else {
+    // e^{a_s-Mt} = e^{a_s-Ms} * cq and e^{a_t-Ms} = e^{a_t-Mt} * cp
+    const float dM = (ms * c.inv_ts - mt * c.inv_tt) * kL2E;
+    const float cq = ex2(dM), cp = ex2(-dM);
+    const bool fwd = c.kl_mode & 1, rev = c.kl_mode & 2;
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+      if (!MASKED || j < nvalid) {
+        const float es = ex2(fmaf(zs[j], c.k_sT, osT));
+        const float et = ex2(fmaf(zt[j], c.k_tT, otT));
+        lsT += es;
+        ltT += et;
+        const float d = zt[j] * c.inv_tt - zs[j] * c.inv_ts;
+        if (fwd) {
+          qd = fmaf(et, d, qd);
+          qx += fmaf(es, cq, -et);
+        }
+        if (rev) {
+          pd = fmaf(es, -d, pd);
+          px += fmaf(et, cp, -es);
+        }
+      }
+    }
+    if (c.need_s1) {
+#pragma unroll
+      for (int j = 0; j < NC; ++j)
+        if (!MASKED || j < nvalid) ls1 += ex2(fmaf(zs[j], c.k_s1, os1));
+    }
+    if (c.need_t1) {
+#pragma unroll
+      for (int j = 0; j < NC; ++j)
+        if (!MASKED || j < nvalid) lt1 += ex2(fmaf(zt[j], c.k_t1, ot1));
+    }
+  }
+  st.ls1 += ls1;
+  st.lsT += lsT;
+  st.lt1 += lt1;
+  st.ltT += ltT;
+  st.qd += qd;
+  st.qx += qx;
+  st.pd += pd;
+  st.px += px;
+}
+
+// log E[e^{x}] from its "minus 1" form when that is finite and well inside
+// the log1p domain, else from the difference of the two log-sum-exps.
+__device__ __forceinline__ float log_mean_exp(float x_minus_1, float lse_diff) {
+  return (isfinite(x_minus_1) && x_minus_1 > -0.5f) ? log1pf(x_minus_1) : lse_diff;
+}
+
+struct RowOut {
+  float ce_s, ce_t, kl, lse_s1, lse_sT, lse_t1, lse_tT, kl_rev, kl_pm;
+};
+
+// Finalise one token.  variant: KD_KL_*; topk: sparse objective with mass M
+// and entropy E = sum_S p log p (Full-Chunked-KL-Loss README, "Methods").
+__device__ __forceinline__ RowOut finalize(const RowState& s, const Consts& c, int variant,
+                                           bool has_t, bool topk, float mass, float ent) {
+  RowOut o;
+  o.lse_s1 = s.ms + logf(s.ls1);
+  o.lse_sT = s.ms * c.inv_ts + logf(s.lsT);
+  o.ce_s = o.lse_s1 - s.zys;
+  o.lse_t1 = o.lse_tT = 0.f;
+  o.ce_t = 0.f;
+  o.kl_rev = o.kl_pm = 0.f;
+  o.kl = 0.f;
+  if (topk) {
+    o.kl = ent - s.tk + mass * o.lse_sT;
+  } else if (has_t) {
+    o.lse_t1 = s.mt + logf(s.lt1);
+    o.lse_tT = s.mt * c.inv_tt + logf(s.ltT);
+    o.ce_t = o.lse_t1 - s.zyt;
+    const float kl_f = s.qd / s.ltT + log_mean_exp(s.qx / s.ltT, o.lse_sT - o.lse_tT);
+    const float kl_r = s.pd / s.lsT + log_mean_exp(s.px / s.lsT, o.lse_tT - o.lse_sT);
+    o.kl_rev = kl_r;
+    if (variant == KD_KL_FORWARD) o.kl = kl_f;
+    else if (variant == KD_KL_REVERSE) o.kl = kl_r;
+    else if (variant == KD_KL_JEFFREYS) o.kl = kl_f + kl_r;
+    else {  // skew-JS: second-pass sums jq = sum q log(q/m), jp = sum p log(p/m)
+      o.kl_pm = s.jp;
+      o.kl = (1.f - c.beta) * s.jq + c.beta * s.jp;
+    }
+  }
+  return o;
+}
+
+// log m = log((1-b) q + b p) from log p and log q, evaluated as a log-add so
+// that neither an underflowing p nor q/p overflow can reach it.
+__device__ __forceinline__ float log_mix(float lp, float lq, const Consts& c) {
+  const float u = lq + c.log_1mb, v = lp + c.log_b;
+  const float mx = fmaxf(u, v), mn = fminf(u, v);
+  return mx + __logf(1.f + ex2((mn - mx) * kL2E));
+}
+
+// Skew-JS second pass: with the final log-normalisers known, accumulate
+// jq += q log(q/m) and jp += p log(p/m), m = (1-b) q + b p.
+__device__ __forceinline__ void js_terms(float zs, float zt, float lse_sT, float lse_tT,
+                                         const Consts& c, float& jq, float& jp) {
+  const float lp = zs * c.inv_ts - lse_sT;
+  const float lq = zt * c.inv_tt - lse_tT;
+  const float lm = log_mix(lp, lq, c);
+  jq = fmaf(ex2(lq * kL2E), lq - lm, jq);
+  jp = fmaf(ex2(lp * kL2E), lp - lm, jp);
+}
+
+// Gradient of the KL part w.r.t. a_s (teacher detached), per element, from
+// the saved statistics:
+//   forward  p - q;  reverse p (log p - log q - KL(p||q));  Jeffreys the sum;
+//   skew-JS  b p (log p - log m - KL(p||m)).
+__device__ __forceinline__ float kl_grad(float zs, float zt, const float* stt, int variant,
+                                         const Consts& c) {
+  const float lp = zs * c.inv_ts - stt[S_LSE_ST];
+  const float lq = zt * c.inv_tt - stt[S_LSE_TT];
+  const float p = ex2(lp * kL2E);
+  if (variant == KD_KL_SKEW_JS) return c.beta * p * (lp - log_mix(lp, lq, c) - stt[S_KL_PM]);
+  float g = 0.f;
+  if (variant != KD_KL_REVERSE) g = p - ex2(lq * kL2E);
+  if (variant != KD_KL_FORWARD) g = fmaf(p, lp - lq - stt[S_KL_REV], g);
+  return g;
+}
+
+__device__ __forceinline__ void set_status(uint32_t* st, uint32_t bits) {
+  if (st) atomicOr(st, bits);
+}
+
+}  // namespace kd

@@ -1,0 +1,179 @@
+// Host-side internal interface between the C ABI (kd_api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/kd.h"
+#include "kd_common.cuh"
+
+namespace kd {
+
+// ---------------------------------------------------------------- aux kernels
+// Count valid labels into *count (int32, zeroed by the caller) and flag bad ones.
+void launch_label_check(const int64_t* labels, int64_t n, int64_t vocab, int64_t ignore,
+                        int32_t* count, uint32_t* status, cudaStream_t s);
+// Sort each row's top-K ids ascending (probabilities follow), validate them,
+// and write M = sum p and E = sum p log p per row.
+void launch_topk_prep(const int32_t* idx, const float* p, int64_t n, int k, int64_t vocab,
+                      int32_t* sidx, float* sp, float* mass, float* ent, uint32_t* status,
+                      cudaStream_t s);
+// Merge per-split partial records [n_parts][n][kRec] and finalise every row.
+struct CombineArgs {
+  const float* partials;
+  int n_parts;
+  int64_t n, vocab;
+  Consts c;
+  int variant;
+  int has_t, topk;
+  int js_pass;            // 1: records hold skew-JS second-pass sums only
+  const int64_t* labels;  // may be NULL
+  int64_t ignore;
+  const float* mass;      // top-K
+  const float* ent;
+  float *ce_s, *ce_t, *kl, *stats;  // stats must be non-NULL
+};
+void launch_combine(const CombineArgs& a, cudaStream_t s);
+// Weighted, reduced scalar loss from the per-token outputs.
+struct ReduceArgs {
+  const float *ce_s, *ce_t, *kl;
+  const int64_t* labels;
+  int64_t n, ignore;
+  float w_sce, w_tce, w_kl_t2;
+  int reduction;
+  int64_t num_batch_labels;
+  const int32_t* count;
+  float* loss;
+};
+void launch_loss_reduce(const ReduceArgs& a, cudaStream_t s);
+// Per-row gradient scale: valid ? grad_scale * (*d_loss) / denom : 0.
+void launch_row_scale(const int64_t* labels, int64_t n, int64_t ignore, float grad_scale,
+                      const float* d_loss, int reduction, int64_t num_batch_labels,
+                      const int32_t* count, float* scale, cudaStream_t s);
+// dst[c][r] = src[r][c] for a [rows, cols] bf16 matrix (pitches in elements).
+void launch_transpose_bf16(const __nv_bfloat16* src, int64_t rows, int64_t cols, int64_t lds,
+                           __nv_bfloat16* dst, int64_t ldd, cudaStream_t s);
+
+// ---------------------------------------------------------- streaming path
+struct StreamArgs {
+  const void* zs;       // [n, vocab]
+  const void* zt;       // [n, vocab] or NULL
+  int64_t n, vocab;
+  Consts c;
+  int variant;
+  int is_bf16;
+  int topk;             // top-K teacher: use sidx/sp/mass/ent
+  int k;
+  const int32_t* sidx;
+  const float* sp;
+  const float* mass;
+  const float* ent;
+  const int64_t* labels;
+  int64_t ignore;
+  float *ce_s, *ce_t, *kl, *stats;
+  // backward
+  const float* row_scale;
+  float w_sce, w_kl_ts;  // w_sce, w_kl * T_s
+  void* dz;              // [n, vocab] gradient of the student logits
+};
+void launch_stream_fwd(const StreamArgs& a, cudaStream_t s);
+void launch_stream_bwd(const StreamArgs& a, cudaStream_t s);
+
+// ------------------------------------------------------------- fp32 SIMT path
+struct SimtArgs {
+  // student: hidden (h_s, w_s, d_s); teacher: hidden (h_t, w_t, d_t) or logits zt
+  const float *h_s, *w_s, *h_t, *w_t, *zt;
+  int64_t n, vocab, d_s, d_t;
+  int teacher;           // kd_teacher_kind
+  Consts c;
+  int variant;
+  const int64_t* labels;
+  int64_t ignore;
+  const int32_t* sidx;
+  const float* sp;
+  int k;
+  int n_splits;
+  float* partials;       // [n_splits][n][kRec]
+  const float* stats;    // pass-2 / backward
+  int js_pass;
+  // backward G producer over rows [r0, r0+rc) x cols [c0, c0+cc)
+  int64_t r0, rc, c0, cc;
+  const float* row_scale;
+  float w_sce, w_tce, w_kl_ts;
+  float* g;              // [rc, cc] student gradient tile
+  float* gt;             // [rc, cc] tied teacher-CE gradient tile or NULL
+};
+void launch_simt_fwd(const SimtArgs& a, cudaStream_t s);
+void launch_simt_gprod(const SimtArgs& a, cudaStream_t s);
+// C[m, n] (+)= sum_k A(m, k) B(k, n) with element strides.
+void launch_simt_gemm(const float* A, int64_t sam, int64_t sak, const float* B, int64_t sbk,
+                      int64_t sbn, float* C, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                      bool accumulate, cudaStream_t s);
+
+// ------------------------------------------------------------ tcgen05 path
+int tc_num_sms();
+struct TcFwdArgs {
+  const void *h_s, *w_s, *h_t, *w_t, *zs_logits, *zt_logits;
+  int64_t n, vocab, d_s, d_t;
+  int s_gemm, t_gemm;      // sides computed by tcgen05
+  int s_logits, t_logits;  // sides read from materialised logits
+  int topk;
+  Consts c;
+  int variant;
+  const int64_t* labels;
+  int64_t ignore;
+  const int32_t* sidx;
+  const float* sp;
+  int k;
+  int n_splits;
+  float* partials;
+  const float* stats;      // js pass
+  int js_pass;
+  uint32_t* status;
+};
+// Returns a cudaError_t-compatible code (0 = success).
+int launch_tc_fwd(const TcFwdArgs& a, int num_ctas, cudaStream_t s);
+
+struct TcGradArgs {
+  const void *h_s, *w_s, *h_t, *w_t, *zs_logits, *zt_logits;
+  int64_t n, vocab, d_s, d_t;
+  int s_gemm, t_gemm, s_logits, t_logits, topk;
+  Consts c;
+  int variant;
+  const int64_t* labels;
+  int64_t ignore;
+  const int32_t* sidx;
+  const float* sp;
+  int k;
+  const float* stats;
+  const float* row_scale;
+  float w_sce, w_tce, w_kl_ts;
+  int64_t r0, rc, c0, cc;  // chunk
+  __nv_bfloat16* g;        // [rc, ldg] row-major student G (or d z_s)
+  int64_t ldg;
+  __nv_bfloat16* gT;       // [cc, ldgt] transposed student G, or NULL
+  int64_t ldgt;
+  __nv_bfloat16* gtT;      // [cc, ldgt] transposed tied teacher-CE G, or NULL
+  uint32_t* status;
+};
+int launch_tc_grad(const TcGradArgs& a, int num_ctas, cudaStream_t s);
+
+// Tensor-core GEMM: C[M, N] = sum_k A[M, K] B[N, K] (+ A1 B1 over K1), K-major
+// bf16 operands with row pitches lda/ldb (elements), fp32 accumulate.
+enum TcOutMode { TC_OUT_BF16 = 0, TC_OUT_F32 = 1, TC_OUT_F32_ACC = 2, TC_OUT_F32_ACC_BF16 = 3 };
+struct TcGemmArgs {
+  const __nv_bfloat16 *a0, *b0, *a1, *b1;
+  int64_t lda0, ldb0, lda1, ldb1;
+  int64_t M, N, K0, K1;    // K1 = 0: single segment
+  int mode;
+  float* c32;              // fp32 accumulator / output [M, ldc32]
+  int64_t ldc32;
+  __nv_bfloat16* c16;      // bf16 output [M, ldc16]
+  int64_t ldc16;
+  uint32_t* status;
+};
+int launch_tc_gemm(const TcGemmArgs& a, int num_ctas, cudaStream_t s);
+
+}  // namespace kd

@@ -1,0 +1,350 @@
+// HBM-streaming path for materialised logits (nemo_automodel KDLoss on
+// student_logits / teacher_logits; flash_kd with upcast=True): one CTA per
+// token row streams both logit rows with 128-bit read-only loads, keeps the
+// online-softmax state per thread (fp32), merges it across the block, and
+// finalises CE / KL / saved statistics.  Skew-JS needs both final
+// normalisers before log m, so it takes a second sweep of the same row while
+// it is still resident in L2.  The backward is a pure elementwise sweep that
+// reads z_s, z_t and the row statistics and writes d z_s.
+#include <cuda_bf16.h>
+
+#include "kd_internal.h"
+
+namespace kd {
+
+namespace {
+
+constexpr int kThreads = 512;
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// 8 consecutive elements of a row at vector index vec.
+template <typename T>
+__device__ __forceinline__ void load8(const T* row, int64_t vec, float* out);
+
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* row, int64_t vec,
+                                                      float* out) {
+  const uint4 u = ldg_stream(row + vec * 8);
+  out[0] = bf16lo(u.x); out[1] = bf16hi(u.x);
+  out[2] = bf16lo(u.y); out[3] = bf16hi(u.y);
+  out[4] = bf16lo(u.z); out[5] = bf16hi(u.z);
+  out[6] = bf16lo(u.w); out[7] = bf16hi(u.w);
+}
+
+template <>
+__device__ __forceinline__ void load8<float>(const float* row, int64_t vec, float* out) {
+  const uint4 a = ldg_stream(row + vec * 8), b = ldg_stream(row + vec * 8 + 4);
+  out[0] = __uint_as_float(a.x); out[1] = __uint_as_float(a.y);
+  out[2] = __uint_as_float(a.z); out[3] = __uint_as_float(a.w);
+  out[4] = __uint_as_float(b.x); out[5] = __uint_as_float(b.y);
+  out[6] = __uint_as_float(b.z); out[7] = __uint_as_float(b.w);
+}
+
+template <typename T>
+__device__ __forceinline__ float ld1(const T* p) {
+  return static_cast<float>(*p);
+}
+template <>
+__device__ __forceinline__ float ld1<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat162float(*p);
+}
+
+template <typename T>
+__device__ __forceinline__ void st8(T* row, int64_t vec, const float* g);
+template <>
+__device__ __forceinline__ void st8<__nv_bfloat16>(__nv_bfloat16* row, int64_t vec,
+                                                    const float* g) {
+  uint4 u;
+  u.x = pack_bf16(g[0], g[1]);
+  u.y = pack_bf16(g[2], g[3]);
+  u.z = pack_bf16(g[4], g[5]);
+  u.w = pack_bf16(g[6], g[7]);
+  *reinterpret_cast<uint4*>(row + vec * 8) = u;
+}
+template <>
+__device__ __forceinline__ void st8<float>(float* row, int64_t vec, const float* g) {
+  float4* o = reinterpret_cast<float4*>(row + vec * 8);
+  o[0] = make_float4(g[0], g[1], g[2], g[3]);
+  o[1] = make_float4(g[4], g[5], g[6], g[7]);
+}
+
+template <typename T>
+__device__ __forceinline__ void st1(T* p, float v) {
+  *p = static_cast<T>(v);
+}
+template <>
+__device__ __forceinline__ void st1<__nv_bfloat16>(__nv_bfloat16* p, float v) {
+  *p = __float2bfloat16(v);
+}
+
+// Merge every thread's state into thread 0 (result valid in thread 0 only).
+__device__ __forceinline__ void block_merge(RowState& st, const Consts& c, float* sh) {
+  for (int o = 16; o > 0; o >>= 1) merge(st, shfl_xor(st, o), c);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) st.store(sh + w * kRec);
+  __syncthreads();
+  if (w == 0) {
+    const int nw = blockDim.x >> 5;
+    if (l < nw) st.load(sh + l * kRec);
+    else st.init();
+    for (int o = 16; o > 0; o >>= 1) merge(st, shfl_xor(st, o), c);
+  }
+}
+
+__device__ __forceinline__ float2 block_sum2(float a, float b, float* sh) {
+  for (int o = 16; o > 0; o >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, o);
+    b += __shfl_xor_sync(0xffffffffu, b, o);
+  }
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) {
+    sh[2 * w] = a;
+    sh[2 * w + 1] = b;
+  }
+  __syncthreads();
+  float2 r = make_float2(0.f, 0.f);
+  if (threadIdx.x == 0)
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) {
+      r.x += sh[2 * i];
+      r.y += sh[2 * i + 1];
+    }
+  return r;
+}
+
+}  // namespace
+
+template <typename T, bool HAS_T, bool VEC>
+__global__ void __launch_bounds__(kThreads) k_stream_fwd(StreamArgs a) {
+  __shared__ __align__(16) float sh[32 * kRec];
+  __shared__ float sh_lse[2];
+  const Consts c = a.c;
+  const int64_t V = a.vocab;
+  for (int64_t row = blockIdx.x; row < a.n; row += gridDim.x) {
+    const T* zs = static_cast<const T*>(a.zs) + row * V;
+    const T* zt = HAS_T ? static_cast<const T*>(a.zt) + row * V : nullptr;
+    RowState st;
+    st.init();
+    if (VEC) {
+      const int64_t nvec = V / 8;
+      int64_t v = threadIdx.x;
+      for (; v + 3 * kThreads < nvec; v += 4 * kThreads) {
+        float fs[32], ft[32];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          load8<T>(zs, v + u * kThreads, fs + 8 * u);
+          if (HAS_T) load8<T>(zt, v + u * kThreads, ft + 8 * u);
+        }
+        update<32, HAS_T, false>(st, fs, ft, 32, c);
+      }
+      for (; v < nvec; v += kThreads) {
+        float fs[8], ft[8];
+        load8<T>(zs, v, fs);
+        if (HAS_T) load8<T>(zt, v, ft);
+        update<8, HAS_T, false>(st, fs, ft, 8, c);
+      }
+    } else {
+      for (int64_t e0 = threadIdx.x; e0 < V; e0 += 8 * kThreads) {
+        float fs[8], ft[8];
+        int nv = 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int64_t e = e0 + (int64_t)u * kThreads;
+          fs[u] = ft[u] = 0.f;
+          if (e < V) {
+            fs[u] = ld1<T>(zs + e);
+            if (HAS_T) ft[u] = ld1<T>(zt + e);
+            nv = u + 1;
+          }
+        }
+        update<8, HAS_T, true>(st, fs, ft, nv, c);
+      }
+    }
+    if (a.topk) {  // sparse cross term sum_S p a_s (ids validated by the prep kernel)
+      const int32_t* ids = a.sidx + row * a.k;
+      const float* ps = a.sp + row * a.k;
+      for (int j = threadIdx.x; j < a.k; j += kThreads) {
+        const int32_t id = ids[j];
+        if (id >= 0 && (int64_t)id < V) st.tk = fmaf(ps[j], ld1<T>(zs + id) * c.inv_ts, st.tk);
+      }
+    }
+    block_merge(st, c, sh);
+    if (threadIdx.x == 0) {
+      bool valid = true, bad = false;
+      if (a.labels) {
+        const int64_t y = a.labels[row];
+        valid = y != a.ignore;
+        bad = valid && (y < 0 || y >= V);
+        if (valid && !bad) {
+          st.zys = ld1<T>(zs + y);
+          if (HAS_T) st.zyt = ld1<T>(zt + y);
+        }
+      }
+      const float mass = a.topk ? a.mass[row] : 0.f, ent = a.topk ? a.ent[row] : 0.f;
+      const RowOut o = finalize(st, c, a.variant, HAS_T, a.topk, mass, ent);
+      const float nan = __int_as_float(0x7fc00000);
+      if (a.ce_s) a.ce_s[row] = !valid ? 0.f : (bad ? nan : o.ce_s);
+      if (a.ce_t) a.ce_t[row] = !valid ? 0.f : (bad ? nan : o.ce_t);
+      if (a.kl && !(HAS_T && a.variant == KD_KL_SKEW_JS)) a.kl[row] = valid ? o.kl : 0.f;
+      float4* s4 = reinterpret_cast<float4*>(a.stats + row * KD_STATS_PER_TOKEN);
+      s4[0] = make_float4(o.lse_s1, o.lse_sT, o.lse_t1, o.lse_tT);
+      s4[1] = make_float4(o.kl_rev, 0.f, mass, 0.f);
+      sh_lse[0] = o.lse_sT;
+      sh_lse[1] = o.lse_tT;
+    }
+    if (HAS_T && a.variant == KD_KL_SKEW_JS) {
+      __syncthreads();
+      const float lse_sT = sh_lse[0], lse_tT = sh_lse[1];
+      float jq = 0.f, jp = 0.f;
+      if (VEC) {
+        const int64_t nvec = V / 8;
+        for (int64_t v = threadIdx.x; v < nvec; v += kThreads) {
+          float fs[8], ft[8];
+          load8<T>(zs, v, fs);
+          load8<T>(zt, v, ft);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) js_terms(fs[u], ft[u], lse_sT, lse_tT, c, jq, jp);
+        }
+      } else {
+        for (int64_t e = threadIdx.x; e < V; e += kThreads)
+          js_terms(ld1<T>(zs + e), ld1<T>(zt + e), lse_sT, lse_tT, c, jq, jp);
+      }
+      const float2 r = block_sum2(jq, jp, sh);
+      if (threadIdx.x == 0) {
+        const bool v_ok = !a.labels || a.labels[row] != a.ignore;
+        a.stats[row * KD_STATS_PER_TOKEN + S_KL_PM] = r.y;
+        if (a.kl) a.kl[row] = v_ok ? (1.f - c.beta) * r.x + c.beta * r.y : 0.f;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------- backward
+// d z_s = s_row [ w_sce (softmax(z_s) - e_y) + w_kl T_s dKL/da_s ], exactly 0
+// on ignored rows.  Top-K teachers: dKL/da = M softmax(a) - p; the -p part at
+// the K support columns is applied by k_stream_bwd_topk afterwards.
+template <typename T, bool HAS_T, bool VEC>
+__global__ void __launch_bounds__(256) k_stream_bwd(StreamArgs a) {
+  const Consts c = a.c;
+  const int64_t V = a.vocab;
+  constexpr int U = 4;  // vectors per thread per CTA
+  for (int64_t row = blockIdx.y; row < a.n; row += gridDim.y) {
+    const T* zs = static_cast<const T*>(a.zs) + row * V;
+    const T* zt = HAS_T ? static_cast<const T*>(a.zt) + row * V : nullptr;
+    T* dz = static_cast<T*>(a.dz) + row * V;
+    const float scale = a.row_scale[row];
+    const float* stt = a.stats + row * KD_STATS_PER_TOKEN;
+    const float lse_s1 = stt[S_LSE_S1], lse_sT = stt[S_LSE_ST], mass = stt[S_MASS];
+    int64_t y = -1;
+    if (a.labels) y = a.labels[row];
+    const float wk = a.w_kl_ts, wc = a.w_sce;
+    auto grad = [&](float s, float t, int64_t col) -> float {
+      if (scale == 0.f) return 0.f;
+      float g = 0.f;
+      if (HAS_T) g = wk * kl_grad(s, t, stt, a.variant, c);
+      else if (a.topk) g = wk * mass * ex2((s * c.inv_ts - lse_sT) * kL2E);
+      if (wc != 0.f) g = fmaf(wc, ex2((s - lse_s1) * kL2E) - (col == y ? 1.f : 0.f), g);
+      return scale * g;
+    };
+    if (VEC) {
+      const int64_t nvec = V / 8;
+      const int64_t v0 = (int64_t)blockIdx.x * (blockDim.x * U) + threadIdx.x;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t v = v0 + (int64_t)u * blockDim.x;
+        if (v < nvec) {
+          float fs[8], ft[8], g[8];
+          load8<T>(zs, v, fs);
+          if (HAS_T) load8<T>(zt, v, ft);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) g[j] = grad(fs[j], HAS_T ? ft[j] : 0.f, v * 8 + j);
+          st8<T>(dz, v, g);
+        }
+      }
+    } else {
+      const int64_t e0 = (int64_t)blockIdx.x * (blockDim.x * U * 8) + threadIdx.x;
+      for (int u = 0; u < U * 8; ++u) {
+        const int64_t e = e0 + (int64_t)u * blockDim.x;
+        if (e < V) st1<T>(dz + e, grad(ld1<T>(zs + e), HAS_T ? ld1<T>(zt + e) : 0.f, e));
+      }
+    }
+  }
+}
+
+// Sparse correction of the top-K gradient at the support columns: recompute
+// the full value in fp32 including the -p_k term (ids are distinct).
+template <typename T>
+__global__ void k_stream_bwd_topk(StreamArgs a) {
+  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (i >= a.n * a.k) return;
+  const int64_t row = i / a.k;
+  const int32_t id = a.sidx[i];
+  if (id < 0 || (int64_t)id >= a.vocab) return;
+  const float scale = a.row_scale[row];
+  if (scale == 0.f) return;
+  const Consts c = a.c;
+  const float* stt = a.stats + row * KD_STATS_PER_TOKEN;
+  const T* zs = static_cast<const T*>(a.zs) + row * a.vocab;
+  const float s = ld1<T>(zs + id);
+  float g = a.w_kl_ts * (stt[S_MASS] * ex2((s * c.inv_ts - stt[S_LSE_ST]) * kL2E) - a.sp[i]);
+  if (a.w_sce != 0.f) {
+    const int64_t y = a.labels ? a.labels[row] : -1;
+    g = fmaf(a.w_sce, ex2((s - stt[S_LSE_S1]) * kL2E) - (id == y ? 1.f : 0.f), g);
+  }
+  st1<T>(static_cast<T*>(a.dz) + row * a.vocab + id, scale * g);
+}
+
+namespace {
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+}  // namespace
+
+template <typename T>
+static void fwd_dispatch(const StreamArgs& a, cudaStream_t s) {
+  const bool vec = (a.vocab % 8 == 0) && aligned16(a.zs) && (!a.zt || aligned16(a.zt));
+  const unsigned grid = (unsigned)(a.n < 2147483647 ? a.n : 2147483647);
+  const bool has_t = a.zt != nullptr;
+  if (has_t && vec) k_stream_fwd<T, true, true><<<grid, kThreads, 0, s>>>(a);
+  else if (has_t) k_stream_fwd<T, true, false><<<grid, kThreads, 0, s>>>(a);
+  else if (vec) k_stream_fwd<T, false, true><<<grid, kThreads, 0, s>>>(a);
+  else k_stream_fwd<T, false, false><<<grid, kThreads, 0, s>>>(a);
+}
+
+template <typename T>
+static void bwd_dispatch(const StreamArgs& a, cudaStream_t s) {
+  const bool vec = (a.vocab % 8 == 0) && aligned16(a.zs) && (!a.zt || aligned16(a.zt)) &&
+                   aligned16(a.dz);
+  const int64_t per_cta = 256 * 4 * 8;
+  dim3 grid((unsigned)((a.vocab + per_cta - 1) / per_cta),
+            (unsigned)(a.n < 65535 ? a.n : 65535));
+  const bool has_t = a.zt != nullptr;
+  if (has_t && vec) k_stream_bwd<T, true, true><<<grid, 256, 0, s>>>(a);
+  else if (has_t) k_stream_bwd<T, true, false><<<grid, 256, 0, s>>>(a);
+  else if (vec) k_stream_bwd<T, false, true><<<grid, 256, 0, s>>>(a);
+  else k_stream_bwd<T, false, false><<<grid, 256, 0, s>>>(a);
+  if (a.topk && a.k > 0) {
+    const int64_t tot = a.n * a.k;
+    k_stream_bwd_topk<T><<<(unsigned)((tot + 255) / 256), 256, 0, s>>>(a);
+  }
+}
+
+void launch_stream_fwd(const StreamArgs& a, cudaStream_t s) {
+  if (a.n <= 0) return;
+  if (a.is_bf16) fwd_dispatch<__nv_bfloat16>(a, s);
+  else fwd_dispatch<float>(a, s);
+}
+
+void launch_stream_bwd(const StreamArgs& a, cudaStream_t s) {
+  if (a.n <= 0) return;
+  if (a.is_bf16) bwd_dispatch<__nv_bfloat16>(a, s);
+  else bwd_dispatch<float>(a, s);
+}
+
+}  // namespace kd

@@ -1,0 +1,851 @@
+// Tensor-core (tcgen05 / TMA / TMEM) kernels for sm_103a.
+//
+// One persistent, warp-specialised kernel skeleton serves three jobs:
+//   EPI_FWD   fused logits tile(s) -> online-softmax CE / KL state per row
+//             (student tile z_s = H_s W_s^T and teacher tile z_t = H_t W_t^T
+//             for the same 128 rows x BN vocabulary columns; either side may
+//             instead be streamed from materialised logits) -> partial record
+//             per (row, vocabulary split, half tile)
+//   EPI_GRAD  recomputed logits tile(s) -> closed-form gradient G (bf16),
+//             written row-major (feeds dH = G W) and transposed (feeds
+//             dW = G^T H) into a bounded chunk workspace
+//             (Full-Chunked-KL-Loss README, "Full Chunked KL": the backward
+//             recomputes each chunk and applies M softmax(z) - p)
+//   EPI_GEMM  plain C = A B^T with an fp32 / bf16 / accumulate epilogue
+//             (dH and dW from the G chunks)
+//
+// Roles (320 threads): warp 0 issues TMA loads into a STAGES-deep shared
+// memory ring; warp 1 owns the TMEM allocation (512 columns: two accumulator
+// stages of 256) and issues tcgen05.mma from one lane; warps 2..9 drain TMEM
+// with tcgen05.ld (warp w reads TMEM lanes 32*(w%4).., half (w-2)/4 of the
+// tile's columns), so the epilogue of tile i overlaps the MMAs of tile i+1.
+// Every mbarrier wait is bounded in time; on expiry the kernel raises
+// KD_DEV_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "kd_internal.h"
+
+namespace kd {
+
+namespace {
+
+constexpr int BM = 128;             // rows per tile (TMEM lanes)
+constexpr int BK = 64;              // k elements per stage (one 128-byte swizzle row)
+constexpr int kThreads = 320;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
+
+enum Epi { EPI_FWD = 0, EPI_GRAD = 1, EPI_GEMM = 2 };
+
+// ------------------------------------------------------------------ PTX
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols));
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
+}
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+// 32 lanes x 16 consecutive 32-bit columns
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (tiles 1024-byte aligned).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
+  uint64_t d = (uint64_t)((addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;             // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1 << 46;             // descriptor version (tcgen05)
+  d |= (uint64_t)2 << 61;             // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor: kind::f16 with bf16 A/B, fp32 D, K-major A and B.
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// ------------------------------------------------------------------ params
+struct __align__(64) TcParams {
+  CUtensorMap ma[2];
+  CUtensorMap mb[2];
+  int kb[2];          // k blocks per segment (0: segment absent)
+  int acc_off[2];     // TMEM column offset of the segment's accumulator in a stage
+  int a_row0[2];      // row offset added to the A tile row coordinate
+  int b_row0[2];      // row offset added to the B tile row coordinate
+  int seg_accum[2];   // 1: the segment adds to an accumulator an earlier segment wrote
+  int m_tiles, n_tiles, n_splits, items;
+  int logits_vec;     // materialised logits rows are 16-byte aligned
+  TcFwdArgs fwd;
+  TcGradArgs grad;
+  TcGemmArgs gemm;
+};
+
+template <int BN>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (STAGE_BYTES <= 32768) ? 6 : 4;
+  static constexpr int TILE_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM_BYTES = TILE_BYTES + BAR_BYTES + 1024;  // + alignment slack
+  static constexpr uint32_t IDESC = make_idesc(BM, BN);
+};
+
+struct Sync {
+  uint32_t full, empty, acc_full, acc_empty, drain;  // smem addresses of barrier arrays
+  volatile int* abort_flag;
+  uint32_t* status;
+};
+
+// Lane 0 waits (bounded in time), the outcome is broadcast to the warp.
+__device__ __forceinline__ bool warp_wait(const Sync& s, uint32_t bar, uint32_t parity,
+                                          bool honour_abort = true) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) {
+    if (!mbar_try(bar, parity)) {
+      const uint64_t t0 = globaltimer();
+      ok = 0;
+      for (uint32_t it = 1;; ++it) {
+        if (mbar_try(bar, parity)) {
+          ok = 1;
+          break;
+        }
+        if ((it & 63) == 0) {
+          if (honour_abort && *s.abort_flag) break;
+          if (globaltimer() - t0 > kWaitLimitNs) {
+            *s.abort_flag = 1;
+            set_status(s.status, KD_DEV_TIMEOUT);
+            break;
+          }
+        }
+      }
+    }
+  }
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ void item_range(const TcParams& P, int item, int& m_tile, int& t0,
+                                           int& t1) {
+  m_tile = item % P.m_tiles;
+  const int split = item / P.m_tiles;
+  t0 = (int)((int64_t)P.n_tiles * split / P.n_splits);
+  t1 = (int)((int64_t)P.n_tiles * (split + 1) / P.n_splits);
+}
+
+// v[j] for a runtime j in [0, 32) without dynamic register indexing
+__device__ __forceinline__ float pick32(const float* v, int j) {
+  float r = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) r = (i == j) ? v[i] : r;
+  return r;
+}
+
+// 32 consecutive logits of one row from global memory (bf16)
+__device__ __forceinline__ void load_logits32(const __nv_bfloat16* row, int64_t col0, int nv,
+                                              bool vec, float* v) {
+  if (vec && nv == 32) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 u = ldg_nc_v4(row + col0 + 8 * q);
+      v[8 * q + 0] = bf16lo(u.x); v[8 * q + 1] = bf16hi(u.x);
+      v[8 * q + 2] = bf16lo(u.y); v[8 * q + 3] = bf16hi(u.y);
+      v[8 * q + 4] = bf16lo(u.z); v[8 * q + 5] = bf16hi(u.z);
+      v[8 * q + 6] = bf16lo(u.w); v[8 * q + 7] = bf16hi(u.w);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = j < nv ? __bfloat162float(row[col0 + j]) : 0.f;
+  }
+}
+
+// ------------------------------------------------------------------ epilogues
+// Fused forward: one RowState per (row, half) over the item's vocabulary tiles.
+template <int BN>
+struct FwdEpi {
+  RowState st;
+  int64_t row, y;
+  bool row_ok;
+  const int32_t* ids;
+  const float* ps;
+  int kp;
+
+  __device__ __forceinline__ void begin(const TcParams& P, int m_tile, int t0, int r_in_tile,
+                                        int half) {
+    const TcFwdArgs& a = P.fwd;
+    st.init();
+    row = (int64_t)m_tile * BM + r_in_tile;
+    row_ok = row < a.n;
+    y = (row_ok && a.labels) ? a.labels[row] : -1;
+    ids = nullptr;
+    ps = nullptr;
+    kp = 0;
+    if (a.topk && row_ok) {
+      ids = a.sidx + row * a.k;
+      ps = a.sp + row * a.k;
+      const int64_t first = (int64_t)t0 * BN + half * (BN / 2);
+      while (kp < a.k && (int64_t)ids[kp] < first) ++kp;
+    }
+  }
+
+  template <bool HAS_T>
+  __device__ __forceinline__ void chunk(const TcParams& P, const float* vs, const float* vt,
+                                        int64_t col0) {
+    const TcFwdArgs& a = P.fwd;
+    if (!row_ok) return;
+    const int nv = valid_cols(a.vocab - col0, 32);
+    if (nv <= 0) return;
+    if (a.js_pass) {
+      const float* stt = a.stats + row * KD_STATS_PER_TOKEN;
+      const float ls = stt[S_LSE_ST], lt = stt[S_LSE_TT];
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < nv) js_terms(vs[j], vt[j], ls, lt, a.c, st.jq, st.jp);
+      return;
+    }
+    if (nv == 32) update<32, HAS_T, false>(st, vs, vt, 32, a.c);
+    else update<32, HAS_T, true>(st, vs, vt, nv, a.c);
+    if (y >= col0 && y < col0 + nv) {
+      const int j = (int)(y - col0);
+      st.zys += pick32(vs, j);
+      if (HAS_T) st.zyt += pick32(vt, j);
+    }
+    if (ids) {
+      // skip ids of the other half, then consume this chunk's matches
+      while (kp < a.k && (int64_t)ids[kp] < col0) ++kp;
+      while (kp < a.k && (int64_t)ids[kp] < col0 + nv) {
+        st.tk = fmaf(ps[kp], pick32(vs, (int)(ids[kp] - col0)) * a.c.inv_ts, st.tk);
+        ++kp;
+      }
+    }
+  }
+
+  __device__ __forceinline__ void end(const TcParams& P, int item, int half) {
+    const TcFwdArgs& a = P.fwd;
+    if (!row_ok) return;
+    const int split = item / P.m_tiles;
+    st.store(a.partials + ((int64_t)(split * 2 + half) * a.n + row) * kRec);
+  }
+};
+
+// ------------------------------------------------------------------ kernel
+template <int EPI, int BN, bool HAS_T>
+__global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcParams P) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sA = base;
+  const uint32_t sB = base + C::STAGES * C::A_BYTES;
+  const uint32_t bars = base + C::TILE_BYTES;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + C::TILE_BYTES + 200);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::TILE_BYTES + 208);
+
+  Sync S;
+  S.full = bars;                              // [STAGES]
+  S.empty = bars + 8 * C::STAGES;             // [STAGES]
+  S.acc_full = bars + 16 * C::STAGES;         // [2]
+  S.acc_empty = bars + 16 * C::STAGES + 16;   // [2]
+  S.drain = bars + 16 * C::STAGES + 32;       // [1]
+  S.abort_flag = abort_flag;
+  S.status = EPI == EPI_FWD ? P.fwd.status : EPI == EPI_GRAD ? P.grad.status : P.gemm.status;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::STAGES; ++i) {
+      mbar_init(S.full + 8 * i, 1);
+      mbar_init(S.empty + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(S.acc_full + 8 * i, 1);
+      mbar_init(S.acc_empty + 8 * i, 8);  // one arrive per epilogue warp
+    }
+    mbar_init(S.drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int s = 0; s < 2; ++s)
+      if (P.kb[s] > 0) {
+        prefetch_map(&P.ma[s]);
+        prefetch_map(&P.mb[s]);
+      }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- TMA producer
+    int stage = 0;
+    uint32_t phase = 0, issued = 0, par = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < P.items; item += gridDim.x) {
+      int m_tile, t0, t1;
+      item_range(P, item, m_tile, t0, t1);
+      for (int t = t0; ok && t < t1; ++t)
+        for (int sg = 0; ok && sg < 2; ++sg)
+          for (int kb = 0; ok && kb < P.kb[sg]; ++kb) {
+            if (!warp_wait(S, S.empty + 8 * stage, phase ^ 1)) {
+              ok = false;
+              break;
+            }
+            if (lane == 0) {
+              const uint32_t fb = S.full + 8 * stage;
+              mbar_expect_tx(fb, C::STAGE_BYTES);
+              tma_load_2d(sA + stage * C::A_BYTES, &P.ma[sg], fb, kb * BK,
+                          P.a_row0[sg] + m_tile * BM);
+              tma_load_2d(sB + stage * C::B_BYTES, &P.mb[sg], fb, kb * BK,
+                          P.b_row0[sg] + t * BN);
+            }
+            __syncwarp();
+            issued |= 1u << stage;
+            par = (par & ~(1u << stage)) | (phase << stage);
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+    }
+    if (!ok) {  // wait for our own copies before the CTA exits
+      for (int s = 0; s < C::STAGES; ++s)
+        if (issued & (1u << s)) warp_wait(S, S.full + 8 * s, (par >> s) & 1u, false);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < P.items; item += gridDim.x) {
+      int m_tile, t0, t1;
+      item_range(P, item, m_tile, t0, t1);
+      for (int t = t0; ok && t < t1; ++t) {
+        if (!warp_wait(S, S.acc_empty + 8 * acc, acc_phase ^ 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int sg = 0; ok && sg < 2; ++sg) {
+          const uint32_t d = tmem + acc * 256 + P.acc_off[sg];
+          for (int kb = 0; kb < P.kb[sg]; ++kb) {
+            if (!warp_wait(S, S.full + 8 * stage, phase)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
+              const uint64_t ad = smem_desc(sA + stage * C::A_BYTES);
+              const uint64_t bd = smem_desc(sB + stage * C::B_BYTES);
+#pragma unroll
+              for (int k = 0; k < BK / 16; ++k)
+                mma_bf16(d, ad + 2 * k, bd + 2 * k, C::IDESC,
+                         (kb > 0 || k > 0 || P.seg_accum[sg]) ? 1u : 0u);
+              mma_commit(S.empty + 8 * stage);
+            }
+            __syncwarp();
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) mma_commit(S.acc_full + 8 * acc);
+        __syncwarp();
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+    }
+    // wait until every MMA this thread issued has completed
+    if (lane == 0) mma_commit(S.drain);
+    __syncwarp();
+    warp_wait(S, S.drain, 0, false);
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int q = warp & 3;              // TMEM lane quarter
+    const int half = (warp - 2) >> 2;    // column half of the tile
+    const int r_in_tile = 32 * q + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < P.items; item += gridDim.x) {
+      int m_tile, t0, t1;
+      item_range(P, item, m_tile, t0, t1);
+      FwdEpi<BN> fe;
+      if (EPI == EPI_FWD) fe.begin(P, m_tile, t0, r_in_tile, half);
+      for (int t = t0; t < t1; ++t) {
+        if (!warp_wait(S, S.acc_full + 8 * acc, acc_phase)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tbase = lane_base + acc * 256;
+        if (EPI == EPI_FWD) {
+          const TcFwdArgs& a = P.fwd;
+          const int64_t row = (int64_t)m_tile * BM + r_in_tile;
+#pragma unroll 1
+          for (int cc = 0; cc < BN / 2; cc += 32) {
+            const int col_in_tile = half * (BN / 2) + cc;
+            const int64_t col0 = (int64_t)t * BN + col_in_tile;
+            float vs[32], vt[32];
+            __syncwarp();
+            if (a.s_gemm) {
+              tmem_ld16(tbase + P.acc_off[0] + col_in_tile, vs);
+              tmem_ld16(tbase + P.acc_off[0] + col_in_tile + 16, vs + 16);
+            }
+            if (HAS_T && a.t_gemm) {
+              const int off = P.acc_off[a.s_gemm ? 1 : 0];
+              tmem_ld16(tbase + off + col_in_tile, vt);
+              tmem_ld16(tbase + off + col_in_tile + 16, vt + 16);
+            }
+            tmem_ld_wait();
+            const int nv = valid_cols(a.vocab - col0, 32);
+            if (row < a.n) {
+              if (a.s_logits)
+                load_logits32(static_cast<const __nv_bfloat16*>(a.zs_logits) + row * a.vocab,
+                              col0, nv, P.logits_vec, vs);
+              if (HAS_T && a.t_logits)
+                load_logits32(static_cast<const __nv_bfloat16*>(a.zt_logits) + row * a.vocab,
+                              col0, nv, P.logits_vec, vt);
+            }
+            fe.template chunk<HAS_T>(P, vs, vt, col0);
+          }
+        } else if (EPI == EPI_GRAD) {
+          const TcGradArgs& a = P.grad;
+          const int64_t row = a.r0 + (int64_t)m_tile * BM + r_in_tile;
+          const bool row_ok = row < a.r0 + a.rc;
+          float scale = 0.f;
+          const float* stt = nullptr;
+          int64_t y = -1;
+          const int32_t* ids = nullptr;
+          const float* ps = nullptr;
+          int kp = 0;
+          if (row_ok) {
+            scale = a.row_scale[row];
+            stt = a.stats + row * KD_STATS_PER_TOKEN;
+            if (a.labels) y = a.labels[row];
+            if (a.topk) {
+              ids = a.sidx + row * a.k;
+              ps = a.sp + row * a.k;
+              const int64_t first = a.c0 + (int64_t)t * BN + half * (BN / 2);
+              while (kp < a.k && (int64_t)ids[kp] < first) ++kp;
+            }
+          }
+#pragma unroll 1
+          for (int cc = 0; cc < BN / 2; cc += 32) {
+            const int col_in_tile = half * (BN / 2) + cc;
+            const int64_t lc0 = (int64_t)t * BN + col_in_tile;   // column within the chunk
+            const int64_t col0 = a.c0 + lc0;                       // vocabulary column
+            float vs[32], vt[32];
+            __syncwarp();
+            if (a.s_gemm) {
+              tmem_ld16(tbase + P.acc_off[0] + col_in_tile, vs);
+              tmem_ld16(tbase + P.acc_off[0] + col_in_tile + 16, vs + 16);
+            }
+            if (HAS_T && a.t_gemm) {
+              const int off = P.acc_off[a.s_gemm ? 1 : 0];
+              tmem_ld16(tbase + off + col_in_tile, vt);
+              tmem_ld16(tbase + off + col_in_tile + 16, vt + 16);
+            }
+            tmem_ld_wait();
+            const int nv = valid_cols(a.cc - lc0, 32);
+            if (row_ok && nv > 0) {
+              if (a.s_logits)
+                load_logits32(static_cast<const __nv_bfloat16*>(a.zs_logits) + row * a.vocab,
+                              col0, nv, P.logits_vec, vs);
+              if (HAS_T && a.t_logits)
+                load_logits32(static_cast<const __nv_bfloat16*>(a.zt_logits) + row * a.vocab,
+                              col0, nv, P.logits_vec, vt);
+              float g[32], gt[32];
+              const bool want_gt = a.gtT != nullptr;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                float gg = 0.f, gtt = 0.f;
+                if (scale != 0.f) {
+                  if (HAS_T) gg = a.w_kl_ts * kl_grad(vs[j], vt[j], stt, a.variant, a.c);
+                  else if (a.topk)
+                    gg = a.w_kl_ts * stt[S_MASS] *
+                         ex2((vs[j] * a.c.inv_ts - stt[S_LSE_ST]) * kL2E);
+                  const float ey = (col0 + j == y) ? 1.f : 0.f;
+                  if (a.w_sce != 0.f)
+                    gg = fmaf(a.w_sce, ex2((vs[j] - stt[S_LSE_S1]) * kL2E) - ey, gg);
+                  gg *= scale;
+                  if (HAS_T && want_gt)
+                    gtt = scale * a.w_tce * (ex2((vt[j] - stt[S_LSE_T1]) * kL2E) - ey);
+                }
+                g[j] = gg;
+                gt[j] = gtt;
+              }
+              if (ids && scale != 0.f) {
+                while (kp < a.k && (int64_t)ids[kp] < col0) ++kp;
+                while (kp < a.k && (int64_t)ids[kp] < col0 + nv) {
+                  const int jj = (int)(ids[kp] - col0);
+                  const float sub = scale * a.w_kl_ts * ps[kp];
+#pragma unroll
+                  for (int i = 0; i < 32; ++i)
+                    if (i == jj) g[i] -= sub;
+                  ++kp;
+                }
+              }
+              // row-major G (or d z_s): 32 consecutive bf16 of this row
+              __nv_bfloat16* grow = a.g + (row - a.r0) * a.ldg + lc0;
+              if (nv == 32 && (a.ldg % 8) == 0 &&
+                  (reinterpret_cast<uintptr_t>(grow) & 15) == 0) {
+#pragma unroll
+                for (int qv = 0; qv < 4; ++qv) {
+                  uint4 u;
+                  u.x = pack_bf16(g[8 * qv + 0], g[8 * qv + 1]);
+                  u.y = pack_bf16(g[8 * qv + 2], g[8 * qv + 3]);
+                  u.z = pack_bf16(g[8 * qv + 4], g[8 * qv + 5]);
+                  u.w = pack_bf16(g[8 * qv + 6], g[8 * qv + 7]);
+                  *reinterpret_cast<uint4*>(grow + 8 * qv) = u;
+                }
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (j < nv) grow[j] = __float2bfloat16(g[j]);
+              }
+              if (a.gT) {
+                __nv_bfloat16* gcol = a.gT + lc0 * a.ldgt + (row - a.r0);
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (j < nv) gcol[(int64_t)j * a.ldgt] = __float2bfloat16(g[j]);
+              }
+              if (HAS_T && want_gt) {
+                __nv_bfloat16* gcol = a.gtT + lc0 * a.ldgt + (row - a.r0);
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (j < nv) gcol[(int64_t)j * a.ldgt] = __float2bfloat16(gt[j]);
+              }
+            }
+          }
+        } else {  // EPI_GEMM
+          const TcGemmArgs& a = P.gemm;
+          const int64_t row = (int64_t)m_tile * BM + r_in_tile;
+#pragma unroll 1
+          for (int cc = 0; cc < BN / 2; cc += 32) {
+            const int col_in_tile = half * (BN / 2) + cc;
+            const int64_t col0 = (int64_t)t * BN + col_in_tile;
+            float v[32];
+            __syncwarp();
+            tmem_ld16(tbase + col_in_tile, v);
+            tmem_ld16(tbase + col_in_tile + 16, v + 16);
+            tmem_ld_wait();
+            const int nv = valid_cols(a.N - col0, 32);
+            if (row < a.M && nv > 0) {
+              const bool full = nv == 32;
+              if (a.mode != TC_OUT_BF16) {
+                float* c = a.c32 + row * a.ldc32 + col0;
+                const bool vec = full && (a.ldc32 % 4) == 0;
+                if (a.mode != TC_OUT_F32) {
+                  if (vec) {
+#pragma unroll
+                    for (int qv = 0; qv < 8; ++qv) {
+                      const float4 o = *reinterpret_cast<const float4*>(c + 4 * qv);
+                      v[4 * qv + 0] += o.x;
+                      v[4 * qv + 1] += o.y;
+                      v[4 * qv + 2] += o.z;
+                      v[4 * qv + 3] += o.w;
+                    }
+                  } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                      if (j < nv) v[j] += c[j];
+                  }
+                }
+                if (a.mode != TC_OUT_F32_ACC_BF16) {
+                  if (vec) {
+#pragma unroll
+                    for (int qv = 0; qv < 8; ++qv)
+                      *reinterpret_cast<float4*>(c + 4 * qv) =
+                          make_float4(v[4 * qv], v[4 * qv + 1], v[4 * qv + 2], v[4 * qv + 3]);
+                  } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                      if (j < nv) c[j] = v[j];
+                  }
+                }
+              }
+              if (a.mode == TC_OUT_BF16 || a.mode == TC_OUT_F32_ACC_BF16) {
+                __nv_bfloat16* c = a.c16 + row * a.ldc16 + col0;
+                if (full && (a.ldc16 % 8) == 0) {
+#pragma unroll
+                  for (int qv = 0; qv < 4; ++qv) {
+                    uint4 u;
+                    u.x = pack_bf16(v[8 * qv + 0], v[8 * qv + 1]);
+                    u.y = pack_bf16(v[8 * qv + 2], v[8 * qv + 3]);
+                    u.z = pack_bf16(v[8 * qv + 4], v[8 * qv + 5]);
+                    u.w = pack_bf16(v[8 * qv + 6], v[8 * qv + 7]);
+                    *reinterpret_cast<uint4*>(c + 8 * qv) = u;
+                  }
+                } else {
+#pragma unroll
+                  for (int j = 0; j < 32; ++j)
+                    if (j < nv) c[j] = __float2bfloat16(v[j]);
+                }
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(S.acc_empty + 8 * acc);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      if (EPI == EPI_FWD && ok) fe.end(P, item, half);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ------------------------------------------------------------------ host
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// 2-D bf16 map over a [rows, cols] matrix with row pitch `pitch` elements,
+// box = 64 columns x box_rows rows, 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t pitch,
+              int box_rows) {
+  if (!get_encoder()) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(pitch * 2)};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr),
+                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int EPI, int BN, bool HAS_T>
+int launch(const TcParams& P, int num_ctas, cudaStream_t s) {
+  using C = Cfg<BN>;
+  auto kern = k_tc<EPI, BN, HAS_T>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return (int)e;
+  const int grid = P.items < num_ctas ? P.items : num_ctas;
+  if (grid <= 0) return 0;
+  kern<<<grid, kThreads, C::SMEM_BYTES, s>>>(P);
+  return (int)cudaGetLastError();
+}
+
+bool logits_vec_ok(const void* p, int64_t vocab) {
+  return p == nullptr || (((reinterpret_cast<uintptr_t>(p) & 15) == 0) && (vocab % 8) == 0);
+}
+
+int fail_map() { return (int)cudaErrorInvalidValue; }
+
+// Segment setup shared by the fused forward and the gradient producer.
+template <class A>
+bool setup_segments(TcParams& P, const A& a, int bn, int64_t r0, int64_t rows, int64_t c0,
+                    int64_t cols) {
+  int ns = 0;
+  if (a.s_gemm) {
+    if (!make_map(&P.ma[ns], a.h_s, a.n, a.d_s, a.d_s, BM) ||
+        !make_map(&P.mb[ns], a.w_s, a.vocab, a.d_s, a.d_s, bn))
+      return false;
+    P.kb[ns] = (int)((a.d_s + BK - 1) / BK);
+    P.acc_off[ns] = 0;
+    P.a_row0[ns] = (int)r0;
+    P.b_row0[ns] = (int)c0;
+    ++ns;
+  }
+  if (a.t_gemm) {
+    const void* wt = a.w_t ? a.w_t : a.w_s;  // tied teachers use the student head
+    if (!make_map(&P.ma[ns], a.h_t, a.n, a.d_t, a.d_t, BM) ||
+        !make_map(&P.mb[ns], wt, a.vocab, a.d_t, a.d_t, bn))
+      return false;
+    P.kb[ns] = (int)((a.d_t + BK - 1) / BK);
+    P.acc_off[ns] = a.s_gemm ? bn : 0;
+    P.a_row0[ns] = (int)r0;
+    P.b_row0[ns] = (int)c0;
+    ++ns;
+  }
+  P.m_tiles = (int)((rows + BM - 1) / BM);
+  P.n_tiles = (int)((cols + bn - 1) / bn);
+  return true;
+}
+
+}  // namespace
+
+int tc_num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+int launch_tc_fwd(const TcFwdArgs& a, int num_ctas, cudaStream_t s) {
+  TcParams P;
+  memset(&P, 0, sizeof(P));
+  const int bn = (a.s_gemm && a.t_gemm) ? 128 : 256;
+  if (!setup_segments(P, a, bn, 0, a.n, 0, a.vocab)) return fail_map();
+  P.n_splits = a.n_splits;
+  P.items = P.m_tiles * P.n_splits;
+  P.logits_vec = logits_vec_ok(a.zs_logits, a.vocab) && logits_vec_ok(a.zt_logits, a.vocab);
+  P.fwd = a;
+  const bool has_t = a.t_gemm || a.t_logits;
+  if (bn == 128)
+    return has_t ? launch<EPI_FWD, 128, true>(P, num_ctas, s)
+                 : launch<EPI_FWD, 128, false>(P, num_ctas, s);
+  return has_t ? launch<EPI_FWD, 256, true>(P, num_ctas, s)
+               : launch<EPI_FWD, 256, false>(P, num_ctas, s);
+}
+
+int launch_tc_grad(const TcGradArgs& a, int num_ctas, cudaStream_t s) {
+  TcParams P;
+  memset(&P, 0, sizeof(P));
+  const int bn = (a.s_gemm && a.t_gemm) ? 128 : 256;
+  if (!setup_segments(P, a, bn, a.r0, a.rc, a.c0, a.cc)) return fail_map();
+  P.n_splits = P.n_tiles;  // one tile per item
+  P.items = P.m_tiles * P.n_tiles;
+  P.logits_vec = logits_vec_ok(a.zs_logits, a.vocab) && logits_vec_ok(a.zt_logits, a.vocab);
+  P.grad = a;
+  const bool has_t = a.t_gemm || a.t_logits;
+  if (bn == 128)
+    return has_t ? launch<EPI_GRAD, 128, true>(P, num_ctas, s)
+                 : launch<EPI_GRAD, 128, false>(P, num_ctas, s);
+  return has_t ? launch<EPI_GRAD, 256, true>(P, num_ctas, s)
+               : launch<EPI_GRAD, 256, false>(P, num_ctas, s);
+}
+
+int launch_tc_gemm(const TcGemmArgs& a, int num_ctas, cudaStream_t s) {
+  TcParams P;
+  memset(&P, 0, sizeof(P));
+  constexpr int bn = 256;
+  if (!make_map(&P.ma[0], a.a0, a.M, a.K0, a.lda0, BM) ||
+      !make_map(&P.mb[0], a.b0, a.N, a.K0, a.ldb0, bn))
+    return fail_map();
+  P.kb[0] = (int)((a.K0 + BK - 1) / BK);
+  if (a.K1 > 0) {
+    if (!make_map(&P.ma[1], a.a1, a.M, a.K1, a.lda1, BM) ||
+        !make_map(&P.mb[1], a.b1, a.N, a.K1, a.ldb1, bn))
+      return fail_map();
+    P.kb[1] = (int)((a.K1 + BK - 1) / BK);
+    P.seg_accum[1] = 1;  // both segments sum into the same accumulator
+  }
+  P.m_tiles = (int)((a.M + BM - 1) / BM);
+  P.n_tiles = (int)((a.N + bn - 1) / bn);
+  P.n_splits = P.n_tiles;
+  P.items = P.m_tiles * P.n_tiles;
+  P.gemm = a;
+  return launch<EPI_GEMM, 256, false>(P, num_ctas, s);
+}
+
+}  // namespace kd
