@@ -1,0 +1,306 @@
+"""Thin Python binding of the ``kd.h`` C ABI (argument marshalling only).
+
+Every step of the loss runs inside ``libkdgb.so``; this module only turns
+PyTorch tensors into device pointers, allocates outputs / workspace with the
+PyTorch caching allocator and passes the current CUDA stream.  There is no
+fallback: if the library is missing or the device is not an sm_103 GPU the
+calls raise.
+
+Low-level names mirror the ABI one to one: ``kd_workspace_size``, ``kd_fwd``,
+``kd_bwd``, ``kd_status_string``, ``kd_device_supported``, ``kd_abi_version``,
+``kd_diag_gemm_bf16``.  ``forward`` / ``backward`` are conveniences that build
+the structs from keyword arguments and tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkdgb.so")
+
+# ---------------------------------------------------------------- enums
+KD_OK, KD_ERR_INVALID_ARG, KD_ERR_UNSUPPORTED, KD_ERR_WORKSPACE = 0, 1, 2, 3
+KD_ERR_BAD_LABEL, KD_ERR_BAD_TOPK, KD_ERR_TIMEOUT, KD_ERR_CUDA, KD_ERR_NO_DEVICE = 4, 5, 6, 7, 8
+KD_DEV_BAD_LABEL, KD_DEV_BAD_TOPK, KD_DEV_TIMEOUT = 0x1, 0x2, 0x4
+KD_BF16, KD_FP32 = 0, 1
+KD_STUDENT_HIDDEN, KD_STUDENT_LOGITS = 0, 1
+KD_TEACHER_NONE, KD_TEACHER_TIED, KD_TEACHER_SEPARATE, KD_TEACHER_LOGITS, KD_TEACHER_TOPK = range(5)
+KD_KL_FORWARD, KD_KL_REVERSE, KD_KL_JEFFREYS, KD_KL_SKEW_JS = range(4)
+KD_REDUCE_MEAN, KD_REDUCE_SUM = 0, 1
+KD_STATS_PER_TOKEN = 8
+
+DTYPES = {"bf16": KD_BF16, "fp32": KD_FP32}
+STUDENTS = {"hidden": KD_STUDENT_HIDDEN, "logits": KD_STUDENT_LOGITS}
+TEACHERS = {"none": KD_TEACHER_NONE, "tied": KD_TEACHER_TIED, "separate": KD_TEACHER_SEPARATE,
+            "logits": KD_TEACHER_LOGITS, "topk": KD_TEACHER_TOPK}
+VARIANTS = {"forward": KD_KL_FORWARD, "reverse": KD_KL_REVERSE, "jeffreys": KD_KL_JEFFREYS,
+            "skew_js": KD_KL_SKEW_JS}
+REDUCTIONS = {"mean": KD_REDUCE_MEAN, "sum": KD_REDUCE_SUM}
+
+
+class kd_problem(ctypes.Structure):
+    _fields_ = [
+        ("n_tokens", ctypes.c_int64), ("vocab", ctypes.c_int64), ("d_student", ctypes.c_int64),
+        ("d_teacher", ctypes.c_int64), ("topk", ctypes.c_int64),
+        ("dtype", ctypes.c_int32), ("student", ctypes.c_int32), ("teacher", ctypes.c_int32),
+        ("variant", ctypes.c_int32), ("reduction", ctypes.c_int32),
+        ("t_student", ctypes.c_float), ("t_teacher", ctypes.c_float),
+        ("w_student_ce", ctypes.c_float), ("w_teacher_ce", ctypes.c_float),
+        ("w_kl", ctypes.c_float), ("beta", ctypes.c_float),
+        ("ignore_index", ctypes.c_int64), ("num_batch_labels", ctypes.c_int64),
+        ("assume_valid_labels", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("vocab_chunk", ctypes.c_int64), ("seq_chunk", ctypes.c_int64),
+    ]
+
+
+class kd_inputs(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_void_p) for name in
+                ("h_s", "w_s", "logits_s", "h_t", "w_t", "logits_t", "labels", "topk_idx",
+                 "topk_p")]
+
+
+class KDError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {kd_status_string(status)} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libkdgb.so (built by ``lm_head_cross_vocab_gb300.build``); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    P, I, vp = ctypes.POINTER(kd_problem), ctypes.POINTER(kd_inputs), ctypes.c_void_p
+    sz = ctypes.POINTER(ctypes.c_size_t)
+    lib.kd_workspace_size.argtypes = [P, sz, sz]
+    lib.kd_fwd.argtypes = [P, I, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.kd_bwd.argtypes = [P, I, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp, ctypes.c_size_t,
+                           vp]
+    lib.kd_status_string.argtypes = [ctypes.c_int]
+    lib.kd_status_string.restype = ctypes.c_char_p
+    lib.kd_device_supported.argtypes = [ctypes.c_int]
+    lib.kd_diag_gemm_bf16.argtypes = [vp, vp, vp, ctypes.c_int64, ctypes.c_int64,
+                                      ctypes.c_int64, vp]
+    for f in ("kd_workspace_size", "kd_fwd", "kd_bwd", "kd_device_supported", "kd_abi_version",
+              "kd_diag_gemm_bf16"):
+        getattr(lib, f).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+# ---------------------------------------------------------------- raw ABI
+
+def kd_status_string(status: int) -> str:
+    return load_library().kd_status_string(int(status)).decode()
+
+
+def kd_device_supported(device: int = 0) -> bool:
+    return bool(load_library().kd_device_supported(int(device)))
+
+
+def kd_abi_version() -> int:
+    return int(load_library().kd_abi_version())
+
+
+def kd_workspace_size(problem: kd_problem):
+    f, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    st = load_library().kd_workspace_size(ctypes.byref(problem), ctypes.byref(f), ctypes.byref(b))
+    if st != KD_OK:
+        raise KDError(st, "kd_workspace_size")
+    return int(f.value), int(b.value)
+
+
+def kd_fwd(problem, inputs, ce_s, ce_t, kl, stats, loss, dev_status, workspace, ws_bytes, stream):
+    return int(load_library().kd_fwd(ctypes.byref(problem), ctypes.byref(inputs), ce_s, ce_t, kl,
+                                     stats, loss, dev_status, workspace, ws_bytes, stream))
+
+
+def kd_bwd(problem, inputs, stats, d_loss, grad_scale, d_h_s, d_w_s, d_logits_s, dev_status,
+           workspace, ws_bytes, stream):
+    return int(load_library().kd_bwd(ctypes.byref(problem), ctypes.byref(inputs), stats, d_loss,
+                                     ctypes.c_float(grad_scale), d_h_s, d_w_s, d_logits_s,
+                                     dev_status, workspace, ws_bytes, stream))
+
+
+def kd_diag_gemm_bf16(a: torch.Tensor, b: torch.Tensor) -> torch.Tensor:
+    """C = A B^T on the library's tcgen05 GEMM core (diagnostic)."""
+    assert a.dtype == torch.bfloat16 and b.dtype == torch.bfloat16 and a.is_contiguous() \
+        and b.is_contiguous() and a.shape[1] == b.shape[1]
+    c = torch.empty(a.shape[0], b.shape[0], device=a.device, dtype=torch.float32)
+    st = load_library().kd_diag_gemm_bf16(a.data_ptr(), b.data_ptr(), c.data_ptr(), a.shape[0],
+                                          b.shape[0], a.shape[1], _stream(a.device))
+    if st != KD_OK:
+        raise KDError(st, "kd_diag_gemm_bf16")
+    return c
+
+
+# ---------------------------------------------------------------- helpers
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+@dataclasses.dataclass
+class Problem:
+    """Keyword form of ``kd_problem`` (orda-kernel style parameter names)."""
+
+    n_tokens: int
+    vocab: int
+    d_student: int = 0
+    d_teacher: int = 0
+    topk: int = 0
+    dtype: str = "bf16"
+    student: str = "hidden"
+    teacher: str = "tied"
+    variant: str = "forward"
+    reduction: str = "mean"
+    t_student: float = 1.0
+    t_teacher: Optional[float] = None
+    w_student_ce: float = 1.0
+    w_teacher_ce: float = 0.0
+    w_kl: float = 1.0
+    beta: float = 0.5
+    ignore_index: int = -100
+    num_batch_labels: int = 0
+    assume_valid_labels: bool = False
+    vocab_chunk: int = 0
+    seq_chunk: int = 0
+
+    def to_c(self) -> kd_problem:
+        p = kd_problem()
+        p.n_tokens, p.vocab = self.n_tokens, self.vocab
+        p.d_student, p.d_teacher, p.topk = self.d_student, self.d_teacher, self.topk
+        p.dtype, p.student = DTYPES[self.dtype], STUDENTS[self.student]
+        p.teacher, p.variant = TEACHERS[self.teacher], VARIANTS[self.variant]
+        p.reduction = REDUCTIONS[self.reduction]
+        p.t_student = self.t_student
+        p.t_teacher = self.t_student if self.t_teacher is None else self.t_teacher
+        p.w_student_ce, p.w_teacher_ce, p.w_kl = self.w_student_ce, self.w_teacher_ce, self.w_kl
+        p.beta, p.ignore_index = self.beta, self.ignore_index
+        p.num_batch_labels = self.num_batch_labels
+        p.assume_valid_labels = int(self.assume_valid_labels)
+        p.vocab_chunk, p.seq_chunk = self.vocab_chunk, self.seq_chunk
+        return p
+
+
+def make_inputs(t: dict) -> kd_inputs:
+    i = kd_inputs()
+    for k in ("h_s", "w_s", "logits_s", "h_t", "w_t", "logits_t", "labels", "topk_idx", "topk_p"):
+        v = t.get(k)
+        if v is not None:
+            assert v.is_cuda and v.is_contiguous(), f"{k} must be a contiguous CUDA tensor"
+        setattr(i, k, _ptr(v))
+    return i
+
+
+def _device_of(t: dict):
+    for v in t.values():
+        if v is not None:
+            return v.device
+    return torch.device("cuda")
+
+
+class Workspace:
+    """Reusable device workspace (PyTorch allocation, 256-byte aligned)."""
+
+    def __init__(self):
+        self.buf = None
+
+    def get(self, nbytes: int, device):
+        if self.buf is None or self.buf.numel() < nbytes + 256 or self.buf.device != device:
+            self.buf = None
+            self.buf = torch.empty(max(nbytes, 1) + 256, dtype=torch.uint8, device=device)
+        base = self.buf.data_ptr()
+        return (base + 255) // 256 * 256, nbytes
+
+
+def check_status(dev_status: torch.Tensor, assume_valid: bool = False):
+    s = int(dev_status.item())
+    if s & KD_DEV_TIMEOUT:
+        raise KDError(KD_ERR_TIMEOUT, "device")
+    if not assume_valid:
+        if s & KD_DEV_BAD_LABEL:
+            raise KDError(KD_ERR_BAD_LABEL, "device")
+        if s & KD_DEV_BAD_TOPK:
+            raise KDError(KD_ERR_BAD_TOPK, "device")
+
+
+def forward(problem: Problem, tensors: dict, workspace: Optional[Workspace] = None,
+            check: bool = True, out: Optional[dict] = None):
+    """Run kd_fwd; returns dict(ce_s, ce_t, kl, stats, loss, dev_status)."""
+    dev = _device_of(tensors)
+    n = problem.n_tokens
+    if out is None:
+        out = {
+            "ce_s": torch.empty(n, device=dev, dtype=torch.float32),
+            "ce_t": torch.empty(n, device=dev, dtype=torch.float32),
+            "kl": torch.empty(n, device=dev, dtype=torch.float32),
+            "stats": torch.empty(n, KD_STATS_PER_TOKEN, device=dev, dtype=torch.float32),
+            "loss": torch.empty((), device=dev, dtype=torch.float32),
+            "dev_status": torch.zeros((), device=dev, dtype=torch.int32),
+        }
+    cp = problem.to_c()
+    fb, _ = kd_workspace_size(cp)
+    ws = workspace or Workspace()
+    wptr, wbytes = ws.get(fb, dev)
+    st = kd_fwd(cp, make_inputs(tensors), _ptr(out["ce_s"]), _ptr(out["ce_t"]), _ptr(out["kl"]),
+                _ptr(out["stats"]), _ptr(out["loss"]), _ptr(out["dev_status"]), wptr, wbytes,
+                _stream(dev))
+    if st != KD_OK:
+        raise KDError(st, "kd_fwd")
+    if check:
+        check_status(out["dev_status"], problem.assume_valid_labels)
+    return out
+
+
+def backward(problem: Problem, tensors: dict, stats: torch.Tensor, *, d_loss=None,
+             grad_scale: float = 1.0, want=("h_s", "w_s", "logits_s"),
+             workspace: Optional[Workspace] = None, check: bool = True,
+             out: Optional[dict] = None):
+    """Run kd_bwd; returns dict of the requested gradients (+ dev_status)."""
+    dev = _device_of(tensors)
+    if out is None:
+        out = {"dev_status": torch.zeros((), device=dev, dtype=torch.int32)}
+        for k in want:
+            src = tensors.get(k)
+            if src is not None:
+                out["d_" + k] = torch.empty_like(src)
+    cp = problem.to_c()
+    _, bb = kd_workspace_size(cp)
+    ws = workspace or Workspace()
+    wptr, wbytes = ws.get(bb, dev)
+    st = kd_bwd(cp, make_inputs(tensors), _ptr(stats), _ptr(d_loss), grad_scale,
+                _ptr(out.get("d_h_s")), _ptr(out.get("d_w_s")), _ptr(out.get("d_logits_s")),
+                _ptr(out["dev_status"]), wptr, wbytes, _stream(dev))
+    if st != KD_OK:
+        raise KDError(st, "kd_bwd")
+    if check:
+        check_status(out["dev_status"], problem.assume_valid_labels)
+    return out
+
+
+def problem_for(w, **overrides) -> Problem:
+    """Problem matching a synthetic workload description (inputs.Workload)."""
+    kw = dict(n_tokens=w.n_tokens, vocab=w.vocab, d_student=w.d_student, d_teacher=w.d_teacher,
+              topk=w.topk, dtype=w.dtype, student=w.student, teacher=w.teacher,
+              variant=w.variant, t_student=w.t_student, t_teacher=w.t_teacher,
+              w_student_ce=w.w_student_ce, w_teacher_ce=w.w_teacher_ce, w_kl=w.w_kl, beta=w.beta,
+              ignore_index=w.ignore_index, vocab_chunk=w.vocab_chunk, seq_chunk=w.seq_chunk)
+    kw.update(overrides)
+    return Problem(**kw)
