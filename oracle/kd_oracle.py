@@ -212,7 +212,8 @@ def forward(z_s, z_t=None, labels=None, *, topk_idx=None, topk_p=None,
             reduction="mean", num_batch_labels=None):
     """Per-token CE_s, CE_t, raw KL and the scalar loss from full fp64 logits.
 
-    z_s: [N, V] student logits; z_t: [N, V] teacher logits (None for top-K).
+    z_s: [N, V] student logits; z_t: [N, V] teacher logits (None for top-K, and
+    None without top-K for a plain CE with no teacher).
     Returns a dict: ce_s, ce_t, kl (per token, raw: no T^2), loss (scalar),
     lse_s1, lse_sT, lse_t1, lse_tT, kl_rev, kl_pm, mass, valid.
     """
@@ -227,6 +228,9 @@ def forward(z_s, z_t=None, labels=None, *, topk_idx=None, topk_p=None,
     if topk_idx is not None:
         kl, mass = topk_rows(a_s, topk_idx, topk_p)
         out.update(ce_t=np.zeros(n), mass=mass)
+    elif z_t is None:  # no teacher: plain CE (orda-kernel "Parameters": kl_weight 0.0)
+        kl = np.zeros(n)
+        out.update(ce_t=np.zeros(n))
     else:
         z_t = as_f64(z_t)
         a_t = z_t / t_teacher
@@ -269,6 +273,8 @@ def grad_logits(z_s, z_t=None, labels=None, *, topk_idx=None, topk_p=None,
     a_s = z_s / t_student
     if topk_idx is not None:
         g_a = topk_grad_rows(a_s, topk_idx, topk_p)
+    elif z_t is None:  # no teacher: no KL term
+        g_a = np.zeros_like(z_s)
     else:
         z_t = as_f64(z_t)
         _, aux = kl_rows(a_s, z_t / t_teacher, variant, beta)

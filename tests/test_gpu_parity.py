@@ -1,0 +1,175 @@
+"""GPU parity: the CUDA path through the C ABI vs the fp64 CPU oracle, element
+by element on the same seeded inputs, at sizes that span several tiles and a
+ragged tail, plus edge cases (ignored tokens, empty batches, bad labels,
+chunking invariance)."""
+import numpy as np
+import pytest
+import torch
+
+from lm_head_cross_vocab_gb300 import inputs as I
+from lm_head_cross_vocab_gb300 import kd
+from tests.parity_util import assert_parity, rel_l2, run_and_compare
+
+pytestmark = pytest.mark.gpu
+
+W = I.WORKLOADS
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    kd.load_library()
+    assert kd.kd_device_supported(0), "tests need an sm_103 GPU"
+
+
+# ----------------------------------------------------------- streaming path
+
+@pytest.mark.parametrize("variant", ["forward", "reverse", "jeffreys", "skew_js"])
+@pytest.mark.parametrize("vocab", [4104, 4099])  # vectorised rows, ragged scalar rows
+def test_logit_pair_streaming(variant, vocab):
+    w = W[5].scaled(n_tokens=67, vocab=vocab, variant=variant)
+    assert_parity(run_and_compare(w), "bf16")
+
+
+def test_logit_pair_streaming_fp32_with_ce():
+    w = W[5].scaled(n_tokens=40, vocab=3000, dtype="fp32", w_student_ce=0.7, variant="jeffreys",
+                    t_teacher=1.5)
+    assert_parity(run_and_compare(w), "fp32")
+
+
+def test_topk_with_logit_student_streaming():
+    w = W[4].scaled(n_tokens=50, vocab=2048, student="logits", d_student=0, topk=16,
+                    student_logit_std=2.0)
+    assert_parity(run_and_compare(w), "bf16")
+
+
+# ----------------------------------------------------------- fp32 CUDA cores
+
+@pytest.mark.parametrize("variant", ["forward", "reverse", "jeffreys", "skew_js"])
+def test_tiny_tied_fp32(variant):
+    """The tiny tied fp32 workload (64 tokens, D=64, V=512, T=2), all variants."""
+    assert_parity(run_and_compare(W[1].scaled(variant=variant)), "fp32")
+
+
+def test_fp32_separate_ragged_multichunk():
+    w = W[2].scaled(n_tokens=77, d_student=40, d_teacher=24, vocab=333, dtype="fp32")
+    assert_parity(run_and_compare(w, vocab_chunk=64, seq_chunk=32), "fp32")
+
+
+def test_fp32_topk():
+    w = W[4].scaled(n_tokens=45, d_student=32, vocab=700, topk=12, dtype="fp32")
+    assert_parity(run_and_compare(w), "fp32")
+
+
+# ----------------------------------------------------------- tcgen05 GEMM core
+
+@pytest.mark.parametrize("m,n,k", [(128, 256, 64), (300, 500, 136), (1000, 777, 1024)])
+def test_tensor_core_gemm_matches_torch(m, n, k):
+    g = torch.Generator(device="cpu").manual_seed(m + n + k)
+    a = torch.randn(m, k, generator=g).to(torch.bfloat16).cuda()
+    b = torch.randn(n, k, generator=g).to(torch.bfloat16).cuda()
+    c = kd.kd_diag_gemm_bf16(a, b)
+    ref = a.double() @ b.double().T
+    torch.cuda.synchronize()
+    assert rel_l2(c.cpu().numpy(), ref.cpu().numpy()) < 1e-5
+
+
+# ----------------------------------------------------------- tcgen05 fused paths
+
+def test_separate_teacher_bf16_small():
+    """Separate-teacher bf16 workload at reduced size, ragged in every dim."""
+    w = W[2].scaled(n_tokens=300, d_student=128, d_teacher=256, vocab=1000)
+    assert_parity(run_and_compare(w), "bf16")
+
+
+@pytest.mark.parametrize("variant", ["forward", "reverse", "skew_js"])
+def test_separate_teacher_bf16_variants(variant):
+    w = W[2].scaled(n_tokens=200, d_student=64, d_teacher=192, vocab=1500, variant=variant,
+                    t_teacher=1.5)
+    assert_parity(run_and_compare(w), "bf16")
+
+
+def test_tied_bf16_teacher_ce_flows_into_weight():
+    w = W[1].scaled(n_tokens=257, d_student=64, d_teacher=64, vocab=777, dtype="bf16")
+    assert_parity(run_and_compare(w), "bf16")
+
+
+def test_topk_bf16():
+    w = W[4].scaled(n_tokens=260, d_student=128, vocab=3000, topk=20)
+    assert_parity(run_and_compare(w), "bf16")
+
+
+def test_plain_ce_no_teacher_bf16():
+    w = W[2].scaled(n_tokens=150, d_student=96, d_teacher=0, vocab=1200, teacher="none",
+                    w_teacher_ce=0.0, w_kl=0.0)
+    assert_parity(run_and_compare(w), "bf16")
+
+
+def test_logit_student_separate_teacher_bf16():
+    """Large-vocab scoring shape at reduced size (student logits, teacher GEMM)."""
+    w = W[3].scaled(n_tokens=130, d_teacher=128, vocab=5000)
+    assert_parity(run_and_compare(w, backward=True), "bf16")
+
+
+@pytest.mark.parametrize("vchunk,schunk", [(256, 128), (512, 0), (0, 128)])
+def test_chunking_invariance_bf16(vchunk, schunk):
+    """Results do not depend on the backward chunk (fp32 accumulation across chunks)."""
+    w = W[2].scaled(n_tokens=300, d_student=64, d_teacher=128, vocab=1000)
+    base = run_and_compare(w)
+    res = run_and_compare(w, vocab_chunk=vchunk, seq_chunk=schunk)
+    assert_parity(res, "bf16")
+    assert abs(res["err_dh"] - base["err_dh"]) < 5e-3
+    assert abs(res["err_dw"] - base["err_dw"]) < 5e-3
+
+
+# ----------------------------------------------------------- edge cases
+
+def test_all_tokens_ignored_gives_zero_loss_and_grads():
+    w = W[2].scaled(n_tokens=130, d_student=64, d_teacher=64, vocab=600)
+
+    def mutate(cpu):
+        cpu["labels"][:] = w.ignore_index
+    res = run_and_compare(w, mutate=mutate)
+    assert res["gpu_fwd"]["loss"].item() == 0.0
+    assert res["ignored_zero"] and res["ignored_grad_zero"]
+
+
+def test_bad_label_is_flagged_not_dereferenced():
+    w = W[2].scaled(n_tokens=130, d_student=64, d_teacher=64, vocab=600)
+    cpu = I.make_inputs(w, "cpu")
+    cpu["labels"][5] = 10 ** 9
+    cpu["labels"][6] = -7
+    t = {k: v.cuda() for k, v in cpu.items()}
+    prob = kd.problem_for(w)
+    out = kd.forward(prob, t, check=False)
+    torch.cuda.synchronize()
+    assert int(out["dev_status"].item()) & kd.KD_DEV_BAD_LABEL
+    ce = out["ce_s"].cpu().numpy()
+    assert np.isnan(ce[5]) and np.isnan(ce[6]) and np.isfinite(np.delete(ce, [5, 6])).all()
+    with pytest.raises(kd.KDError):
+        kd.forward(prob, t)
+
+
+def test_bad_topk_is_flagged():
+    w = W[4].scaled(n_tokens=40, d_student=64, vocab=500, topk=8)
+    cpu = I.make_inputs(w, "cpu")
+    cpu["topk_idx"][3, 1] = cpu["topk_idx"][3, 0]  # repeated id
+    cpu["topk_idx"][4, 2] = 500                     # out of range
+    t = {k: v.cuda() for k, v in cpu.items()}
+    out = kd.forward(kd.problem_for(w), t, check=False)
+    torch.cuda.synchronize()
+    assert int(out["dev_status"].item()) & kd.KD_DEV_BAD_TOPK
+
+
+def test_empty_batch():
+    w = W[2].scaled(n_tokens=0, d_student=64, d_teacher=64, vocab=600)
+    prob = kd.problem_for(w)
+    t = {k: v.cuda() for k, v in I.make_inputs(w.scaled(n_tokens=1), "cpu").items()}
+    out = kd.forward(prob, t)
+    torch.cuda.synchronize()
+    assert out["loss"].item() == 0.0
+
+
+def test_sum_reduction_and_num_batch_labels():
+    w = W[2].scaled(n_tokens=128, d_student=64, d_teacher=64, vocab=512)
+    assert_parity(run_and_compare(w, reduction="sum"), "bf16")
+    assert_parity(run_and_compare(w, num_batch_labels=1000), "bf16")

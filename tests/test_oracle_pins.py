@@ -386,3 +386,18 @@ def test_gradients_match_torch_autograd(variant):
     assert out["loss"] == pytest.approx(loss.item(), rel=1e-12)
     g, _ = O.grad_logits(z_s, z_t, labels, variant=variant, t_student=t)
     np.testing.assert_allclose(g, zs.grad.numpy(), rtol=1e-10, atol=1e-14)
+
+
+def test_no_teacher_is_plain_cross_entropy():
+    """Without a teacher the loss is the mean CE, matching torch's cross_entropy."""
+    z = _rand_logits(12, 30, 2.0)
+    labels = RNG.integers(0, 30, size=12)
+    labels[[0, 5]] = -100
+    out = O.forward(z, None, labels)
+    ref = torch.nn.functional.cross_entropy(torch.from_numpy(z), torch.from_numpy(labels))
+    assert out["loss"] == pytest.approx(ref.item(), rel=1e-12)
+    assert not out["kl"].any()
+    zt = torch.tensor(z, requires_grad=True)
+    torch.nn.functional.cross_entropy(zt, torch.from_numpy(labels)).backward()
+    g, _ = O.grad_logits(z, None, labels)
+    np.testing.assert_allclose(g, zt.grad.numpy(), rtol=1e-10, atol=1e-14)
