@@ -1,0 +1,381 @@
+"""Benchmark of the fused LM-head + CE + KL distillation loss (forward + backward).
+
+One step = the whole hot path through the C ABI on one batch of synthetic
+input: kd_fwd (label check, fused tcgen05 projection + online-softmax CE/KL,
+split combine, loss reduction) and kd_bwd (recomputed logits -> closed-form
+gradient chunks -> dH and dW on tcgen05).  Default workload: the separate-
+teacher bf16 configuration (4096 tokens, D_s = 2048, D_t = 4096, V = 32000,
+Jeffreys KL, T = 2, teacher CE weight 0.5, 5 % ignored labels).
+
+    python bench.py [--gpus N --steps K --warmup W] [--config C] [--impl reference]
+
+Multi-GPU (torchrun): every rank runs its own batch (data parallel, weak
+scaling); no collective is on the data path.  `--impl reference` times the
+fp64 CPU oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from lm_head_cross_vocab_gb300 import inputs as I  # noqa: E402
+
+L2_BYTES = 129 * 2 ** 20
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
+            "fallback"
+
+
+def flops_per_step(w: I.Workload):
+    """Algorithmic FLOPs: projections forward, recompute + dH + dW backward."""
+    n, v = w.n_tokens, w.vocab
+    proj_s = 2 * n * v * w.d_student if w.student == "hidden" else 0
+    proj_t = 2 * n * v * (w.d_teacher if w.teacher == "separate"
+                          else w.d_student if w.teacher == "tied" else 0)
+    fwd = proj_s + proj_t
+    bwd = (fwd + 2 * proj_s) if w.backward else 0
+    return fwd, bwd
+
+
+def bytes_per_step(w: I.Workload):
+    """Algorithmic HBM bytes of the logits-streaming path (bf16 logits)."""
+    n, v = w.n_tokens, w.vocab
+    fwd = 2 * n * v * (1 + (w.teacher == "logits"))
+    bwd = 2 * n * v * (2 + (w.teacher == "logits")) if w.backward else 0
+    return fwd, bwd
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                  "sw_power_cap"), parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- oracle (CPU)
+
+def oracle_step(w: I.Workload, cpu: dict, rows: np.ndarray):
+    """fwd + bwd of the oracle on the sampled token rows (row-local work)."""
+    from oracle import kd_oracle as O
+    sub = {k: (v[rows] if k in ("h_s", "h_t", "logits_s", "logits_t", "labels", "topk_idx",
+                                "topk_p") else v) for k, v in cpu.items()}
+    lab = sub["labels"].numpy() if "labels" in sub else None
+    if w.student == "hidden":
+        z_s = O.project(sub["h_s"], sub["w_s"])
+    else:
+        z_s = O.as_f64(sub["logits_s"])
+    z_t = None
+    if w.teacher == "separate":
+        z_t = O.project(sub["h_t"], sub["w_t"])
+    elif w.teacher == "tied":
+        z_t = O.project(sub["h_t"], sub["w_s"])
+    elif w.teacher == "logits":
+        z_t = O.as_f64(sub["logits_t"])
+    kw = dict(variant=w.variant, t_student=w.t_student, t_teacher=w.t_teacher, beta=w.beta,
+              w_student_ce=w.w_student_ce, w_teacher_ce=w.w_teacher_ce, w_kl=w.w_kl,
+              ignore_index=w.ignore_index)
+    topk = {}
+    if w.teacher == "topk":
+        topk = dict(topk_idx=sub["topk_idx"].numpy(), topk_p=sub["topk_p"].numpy())
+    out = O.forward(z_s, z_t, lab, **topk, **kw)
+    if w.backward:
+        g_s, g_t = O.grad_logits(z_s, z_t, lab, **topk, **kw)
+        if w.student == "hidden":
+            O.hidden_grads(sub["h_s"], sub["w_s"], g_s, sub.get("h_t"), g_t,
+                           tied=w.teacher == "tied")
+    return out["loss"]
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def time_oracle(w: I.Workload, rows_per_step: int, steps: int, warmup: int, seed: int):
+    cpu = I.make_inputs(w, "cpu")
+    rng = np.random.default_rng(seed)
+    for _ in range(warmup):
+        oracle_step(w, cpu, np.sort(rng.choice(w.n_tokens, rows_per_step, replace=False)))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle_step(w, cpu, np.sort(rng.choice(w.n_tokens, rows_per_step, replace=False)))
+    dt = time.perf_counter() - t0
+    return rows_per_step * steps / dt, dt
+
+
+def run_reference(args, w: I.Workload, rank: int):
+    if rank != 0:
+        return
+    rows = args.ref_rows
+    value, dt = time_oracle(w, rows, args.steps, args.warmup, 7)
+    line = {
+        "impl": "reference", "metric": "fused linear+CE+KD fwd+bwd tokens/s", "value": value,
+        "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "tokens": w.n_tokens, "vocab": w.vocab,
+                   "d_student": w.d_student, "d_teacher": w.d_teacher},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_threads(),
+                         "kind": "oracle",
+                         "sample": f"{rows} seeded random tokens of the workload per step "
+                                   f"(fp64 numpy oracle, fwd+bwd)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-rows", type=int, default=32)
+    ap.add_argument("--cpu-rows", type=int, default=256)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = I.WORKLOADS[args.config]
+
+    if args.impl == "reference":
+        run_reference(args, w, rank)
+        return
+
+    from lm_head_cross_vocab_gb300 import kd
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    kd.load_library()
+    if not kd.kd_device_supported(local):
+        raise SystemExit("bench needs an sm_103 GPU")
+
+    # inputs resident in HBM; each rank owns its own batch (weak scaling)
+    t = I.make_inputs(w, dev, seed=I.SEED_BASE + w.cfg + 7919 * rank)
+    prob = kd.problem_for(w, vocab_chunk=0, seq_chunk=0)
+    ws_f, ws_b = kd.Workspace(), kd.Workspace()
+    fwd_out = None
+    bwd_out = None
+    want = ("h_s", "w_s") if w.student == "hidden" else ("logits_s",)
+
+    def step():
+        nonlocal fwd_out, bwd_out
+        fwd_out = kd.forward(prob, t, ws_f, check=False, out=fwd_out)
+        if w.backward:
+            bwd_out = kd.backward(prob, t, fwd_out["stats"], want=want, workspace=ws_b,
+                                  check=False, out=bwd_out)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    kd.check_status(fwd_out["dev_status"])
+
+    # per-section events (fused forward launch; backward recompute + dH/dW)
+    n = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+    for e4 in evs:
+        for e in e4:
+            e.record()  # materialise the handles
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0] or 0) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local
+    launches0 = kd.kd_launch_count()
+    with ClockSampler(gpu_index) as clk:
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        start.record()
+        for i in range(n):
+            kd.kd_set_profile_events(*evs[i]) if w.backward else \
+                kd.kd_set_profile_events(evs[i][0], evs[i][1])
+            step()
+        stop.record()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+    kd.kd_set_profile_events()
+    launches = kd.kd_launch_count() - launches0
+    ms = start.elapsed_time(stop)
+    if dist:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    ms_step = ms / n
+    tokens = w.n_tokens * world
+    value = tokens / (ms_step / 1e3)
+    fwd_ms = statistics.mean(evs[i][0].elapsed_time(evs[i][1]) for i in range(n))
+    bwd_ms = statistics.mean(evs[i][2].elapsed_time(evs[i][3]) for i in range(n)) \
+        if w.backward else 0.0
+
+    peaks, peak_src = load_peaks()
+    f_fwd, f_bwd = flops_per_step(w)
+    if f_fwd > 0:
+        achieved = f_fwd / (fwd_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roofline = {"bound": "tensor", "kernel": "k_tc<EPI_FWD> fused projection + CE/KL",
+                    "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                    "peak_source": f"{peak_src} bf16 sustained", "traffic": None,
+                    "flops_per_launch": f_fwd, "launch_ms": fwd_ms}
+        sections = {"fwd_fused_ms": fwd_ms, "bwd_tensor_ms": bwd_ms,
+                    "bwd_tflops": (f_bwd / (bwd_ms / 1e3) / 1e12) if bwd_ms else None,
+                    "step_tflops": (f_fwd + f_bwd) / (ms_step / 1e3) / 1e12}
+    else:
+        b_fwd, b_bwd = bytes_per_step(w)
+        achieved = b_fwd / (fwd_ms / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roofline = {"bound": "hbm", "kernel": "k_stream_fwd", "achieved": achieved, "peak": peak,
+                    "unit": "GB/s", "frac": achieved / peak, "peak_source": f"{peak_src} copy",
+                    "traffic": None, "bytes_per_launch": b_fwd, "launch_ms": fwd_ms}
+        sections = {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+                    "bwd_gbs": (b_bwd / (bwd_ms / 1e3) / 1e9) if bwd_ms else None}
+
+    # end to end through the C ABI with host buffers: H2D inputs, D2H results
+    e2e = None
+    if not args.no_e2e:
+        host = {k: v.cpu().pin_memory() for k, v in t.items()}
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        res_dev = [fwd_out["loss"]] + ([bwd_out[k] for k in bwd_out if k.startswith("d_")]
+                                       if w.backward else [])
+        res_host = [torch.empty_like(r, device="cpu").pin_memory() for r in res_dev]
+        d2h = sum(r.numel() * r.element_size() for r in res_dev)
+
+        def e2e_step():
+            for k, v in host.items():
+                t[k].copy_(v, non_blocking=True)
+            step()
+            for r_h, r_d in zip(res_host, res_dev):
+                r_h.copy_(r_d, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record()
+        ne = max(3, n // 2)
+        for _ in range(ne):
+            e2e_step()
+        e2.record()
+        torch.cuda.synchronize()
+        ms_e = s2.elapsed_time(e2)
+        if dist:
+            tt = torch.tensor([ms_e], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ms_e = float(tt.item())
+        e2e = {"value": tokens / (ms_e / ne / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ms_e / ne}
+
+    peak_gib = torch.cuda.max_memory_allocated(dev) / 2 ** 30
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rows = min(args.cpu_rows, w.n_tokens)
+        v_cpu, dt = time_oracle(w, rows, 1, 0, 11)
+        cpu_base = {"value": v_cpu, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+                    "sample": f"{rows} seeded random tokens of the {w.name} workload, fwd+bwd, "
+                              f"fp64 numpy oracle ({dt:.1f} s)"}
+
+    in_bytes = sum(v.numel() * v.element_size() for v in t.values())
+    if rank == 0:
+        line = {
+            "metric": "fused linear+CE+KD fwd+bwd tokens/s", "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": n, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic",
+            "config": {"workload": w.name, "tokens_per_gpu": w.n_tokens, "vocab": w.vocab,
+                       "d_student": w.d_student, "d_teacher": w.d_teacher,
+                       "variant": w.variant, "teacher": w.teacher,
+                       "parallelism": f"dp{world}",
+                       "l2": "inputs larger than L2" if in_bytes > L2_BYTES else "L2 not flushed"},
+            "roofline": roofline, "sections": sections,
+            "peak_hbm_gib": peak_gib, "cpu_baseline": cpu_base, "e2e": e2e,
+            "clocks": clk.summary(), "gpu_launches": launches,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -147,7 +147,8 @@ typedef struct kd_inputs {
 
 /* Number of floats per token in the saved statistics written by kd_fwd and
  * read by kd_bwd: logsumexp(z_s), logsumexp(a_s), logsumexp(z_t),
- * logsumexp(a_t), KL(p||q), KL(p||m), top-K mass M, reserved. */
+ * logsumexp(a_t), KL(p||q), KL(p||m), top-K mass M, and
+ * logsumexp(a_t) - logsumexp(a_s) evaluated to full relative precision. */
 #define KD_STATS_PER_TOKEN 8
 
 /* Bytes of device workspace kd_fwd and kd_bwd need for this problem on the
@@ -203,6 +204,17 @@ int kd_abi_version(void);
  * form dH = G W and dW = G^T H from a gradient chunk G. */
 kd_status kd_diag_gemm_bf16(const void* a, const void* b, float* c, int64_t m, int64_t n,
                             int64_t k, void* stream);
+
+/* Profiling aid.  When the events are non-NULL (cudaEvent_t handles created by
+ * the caller), every later kd_fwd records fwd_start right before and fwd_stop
+ * right after its fused projection launch(es) on the call's stream, and
+ * kd_bwd records bwd_start / bwd_stop around its recompute + dH / dW section.
+ * Pass NULLs to stop recording.  Process-wide setting. */
+kd_status kd_set_profile_events(void* fwd_start, void* fwd_stop, void* bwd_start,
+                                void* bwd_stop);
+
+/* Number of kernel launches this library has enqueued in this process. */
+uint64_t kd_launch_count(void);
 
 #ifdef __cplusplus
 }

@@ -11,9 +11,26 @@
 #include "../../include/kd.h"
 #include "kd_internal.h"
 
+#include <atomic>
+
 using namespace kd;
 
+namespace kd {
 namespace {
+std::atomic<uint64_t> g_launches{0};
+}
+void note_launch(int k) { g_launches.fetch_add((uint64_t)k, std::memory_order_relaxed); }
+}  // namespace kd
+
+namespace {
+
+// profiling events set by kd_set_profile_events (fwd start/stop, bwd start/stop)
+std::atomic<void*> g_prof[4] = {};
+
+void prof_record(int i, cudaStream_t s) {
+  void* e = g_prof[i].load(std::memory_order_relaxed);
+  if (e) cudaEventRecord(static_cast<cudaEvent_t>(e), s);
+}
 
 enum Path { PATH_STREAM = 0, PATH_SIMT = 1, PATH_TC = 2 };
 
@@ -131,7 +148,9 @@ Consts make_consts(const kd_problem* p, bool has_labels, bool has_t) {
     if (p->variant == KD_KL_FORWARD) c.kl_mode = 1;
     else if (p->variant == KD_KL_REVERSE) c.kl_mode = 2;
     else if (p->variant == KD_KL_JEFFREYS) c.kl_mode = 3;
+    else c.kl_mode = 1;  // skew-JS: forward sums give the accurate normaliser gap
   }
+  c.precise = p->dtype == KD_FP32 ? 1 : 0;
   return c;
 }
 
@@ -390,7 +409,9 @@ kd_status kd_fwd(const kd_problem* problem, const kd_inputs* in, float* ce_s, fl
     a.ce_t = w_ce_t;
     a.kl = w_kl;
     a.stats = w_stats;
+    prof_record(0, s);
     launch_stream_fwd(a, s);
+    prof_record(1, s);
   } else {
     float* part = at<float>(workspace, P.f_part);
     CombineArgs cb;
@@ -412,6 +433,7 @@ kd_status kd_fwd(const kd_problem* problem, const kd_inputs* in, float* ce_s, fl
     cb.kl = w_kl;
     cb.stats = w_stats;
     for (int pass = 0; pass < (js ? 2 : 1); ++pass) {
+      if (pass == 0) prof_record(0, s);
       if (P.path == PATH_SIMT) {
         SimtArgs a;
         memset(&a, 0, sizeof(a));
@@ -469,6 +491,7 @@ kd_status kd_fwd(const kd_problem* problem, const kd_inputs* in, float* ce_s, fl
         a.status = dev_status;
         if (launch_tc_fwd(a, P.nsm, s) != 0) return KD_ERR_CUDA;
       }
+      if (pass == (js ? 1 : 0)) prof_record(1, s);
       cb.js_pass = pass;
       launch_combine(cb, s);
     }
@@ -556,7 +579,9 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
     a.w_sce = p->w_student_ce;
     a.w_kl_ts = w_kl_ts;
     a.dz = d_logits_s;
+    prof_record(2, s);
     launch_stream_bwd(a, s);
+    prof_record(3, s);
     return cuda_status(cudaGetLastError());
   }
   const int64_t R = P.R, C = P.C;
@@ -565,6 +590,7 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
     float* g = at<float>(workspace, P.b_g);
     float* gt = w_tce != 0.f ? at<float>(workspace, P.b_gT) : nullptr;
     const int64_t D = P.ds;
+    prof_record(2, s);
     for (int64_t ri = 0; ri < nr; ++ri) {
       const int64_t r0 = ri * R, rc = std::min(R, n - r0);
       for (int64_t ci = 0; ci < nc; ++ci) {
@@ -614,6 +640,7 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
         }
       }
     }
+    prof_record(3, s);
     return cuda_status(cudaGetLastError());
   }
   // ---------------------------------------------------------------- tcgen05
@@ -634,6 +661,7 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
     if (gtT)
       launch_transpose_bf16(static_cast<const __nv_bfloat16*>(in->h_t), n, D, D, htT, P.ldn, s);
   }
+  prof_record(2, s);
   for (int64_t ri = 0; ri < nr; ++ri) {
     const int64_t r0 = ri * R, rc = std::min(R, n - r0);
     for (int64_t ci = 0; ci < nc; ++ci) {
@@ -740,8 +768,23 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
       }
     }
   }
+  prof_record(3, s);
   return cuda_status(cudaGetLastError());
 }
+
+kd_status kd_set_profile_events(void* fwd_start, void* fwd_stop, void* bwd_start,
+                                void* bwd_stop) {
+  if ((fwd_start == nullptr) != (fwd_stop == nullptr) ||
+      (bwd_start == nullptr) != (bwd_stop == nullptr))
+    return KD_ERR_INVALID_ARG;
+  g_prof[0] = fwd_start;
+  g_prof[1] = fwd_stop;
+  g_prof[2] = bwd_start;
+  g_prof[3] = bwd_stop;
+  return KD_OK;
+}
+
+uint64_t kd_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 // Diagnostic: C[M, N] = A[M, K] B[N, K]^T on the tensor-core GEMM core.
 kd_status kd_diag_gemm_bf16(const void* a, const void* b, float* c, int64_t m, int64_t n,

@@ -32,6 +32,7 @@ void launch_label_check(const int64_t* labels, int64_t n, int64_t vocab, int64_t
   if (n <= 0) return;
   int blocks = (int)((n + 1023) / 1024);
   if (blocks > 256) blocks = 256;
+  note_launch();
   k_label_check<<<blocks, 1024, 0, s>>>(labels, n, vocab, ignore, count, status);
 }
 
@@ -99,6 +100,7 @@ void launch_topk_prep(const int32_t* idx, const float* p, int64_t n, int k, int6
                       cudaStream_t s) {
   if (n <= 0) return;
   int threads = k <= 128 ? 128 : (k <= 256 ? 256 : 512);
+  note_launch();
   k_topk_prep<<<(unsigned)n, threads, k * sizeof(int32_t), s>>>(idx, p, k, vocab, sidx, sp,
                                                                  mass, ent, status);
 }
@@ -137,11 +139,12 @@ __global__ void k_combine(CombineArgs a) {
   if (a.kl) a.kl[r] = valid ? o.kl : 0.f;
   float4* s4 = reinterpret_cast<float4*>(srow);
   s4[0] = make_float4(o.lse_s1, o.lse_sT, o.lse_t1, o.lse_tT);
-  s4[1] = make_float4(o.kl_rev, o.kl_pm, mass, 0.f);
+  s4[1] = make_float4(o.kl_rev, o.kl_pm, mass, o.dlse);
 }
 
 void launch_combine(const CombineArgs& a, cudaStream_t s) {
   if (a.n <= 0) return;
+  note_launch();
   k_combine<<<(unsigned)((a.n + 255) / 256), 256, 0, s>>>(a);
 }
 
@@ -179,6 +182,7 @@ __global__ void k_loss_reduce(ReduceArgs a) {
 }
 
 void launch_loss_reduce(const ReduceArgs& a, cudaStream_t s) {
+  note_launch();
   k_loss_reduce<<<1, 1024, 0, s>>>(a);
 }
 
@@ -204,6 +208,7 @@ void launch_row_scale(const int64_t* labels, int64_t n, int64_t ignore, float gr
                       const float* d_loss, int reduction, int64_t num_batch_labels,
                       const int32_t* count, float* scale, cudaStream_t s) {
   if (n <= 0) return;
+  note_launch();
   k_row_scale<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(labels, n, ignore, grad_scale, d_loss,
                                                            reduction, num_batch_labels, count,
                                                            scale);
@@ -232,6 +237,7 @@ void launch_transpose_bf16(const __nv_bfloat16* src, int64_t rows, int64_t cols,
                            __nv_bfloat16* dst, int64_t ldd, cudaStream_t s) {
   if (rows <= 0 || cols <= 0) return;
   dim3 grid((unsigned)((cols + 63) / 64), (unsigned)((rows + 63) / 64));
+  note_launch();
   k_transpose_bf16<<<grid, 256, 0, s>>>(src, rows, cols, lds, dst, ldd);
 }
 

@@ -33,7 +33,9 @@ constexpr float kL2E = 1.4426950408889634f;  // log2(e)
 constexpr int kRec = 16;                     // floats per partial-state record
 
 // fields of the saved per-token statistics (KD_STATS_PER_TOKEN floats)
-enum StatField { S_LSE_S1 = 0, S_LSE_ST, S_LSE_T1, S_LSE_TT, S_KL_REV, S_KL_PM, S_MASS, S_SPARE };
+// S_DLSE = logsumexp(a_t) - logsumexp(a_s), taken from the accurate log1p form
+// of the forward-KL sums rather than from the difference of the two stored values.
+enum StatField { S_LSE_S1 = 0, S_LSE_ST, S_LSE_T1, S_LSE_TT, S_KL_REV, S_KL_PM, S_MASS, S_DLSE };
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -64,6 +66,7 @@ struct Consts {
   float beta, log_b, log_1mb;  // b, log b, log(1-b)  (skew-JS)
   int need_s1, need_t1;        // student / teacher CE needed (T = 1 sums)
   int kl_mode;                 // bit0: forward cross sums, bit1: reverse cross sums
+  int precise;                 // fp32 problems: libm expm1/log1p in the skew-JS terms
 };
 
 struct RowState {
@@ -240,7 +243,7 @@ __device__ __forceinline__ float log_mean_exp(float x_minus_1, float lse_diff) {
 }
 
 struct RowOut {
-  float ce_s, ce_t, kl, lse_s1, lse_sT, lse_t1, lse_tT, kl_rev, kl_pm;
+  float ce_s, ce_t, kl, lse_s1, lse_sT, lse_t1, lse_tT, kl_rev, kl_pm, dlse;
 };
 
 // Finalise one token.  variant: KD_KL_*; topk: sparse objective with mass M
@@ -253,7 +256,7 @@ __device__ __forceinline__ RowOut finalize(const RowState& s, const Consts& c, i
   o.ce_s = o.lse_s1 - s.zys;
   o.lse_t1 = o.lse_tT = 0.f;
   o.ce_t = 0.f;
-  o.kl_rev = o.kl_pm = 0.f;
+  o.kl_rev = o.kl_pm = o.dlse = 0.f;
   o.kl = 0.f;
   if (topk) {
     o.kl = ent - s.tk + mass * o.lse_sT;
@@ -261,7 +264,10 @@ __device__ __forceinline__ RowOut finalize(const RowState& s, const Consts& c, i
     o.lse_t1 = s.mt + logf(s.lt1);
     o.lse_tT = s.mt * c.inv_tt + logf(s.ltT);
     o.ce_t = o.lse_t1 - s.zyt;
-    const float kl_f = s.qd / s.ltT + log_mean_exp(s.qx / s.ltT, o.lse_sT - o.lse_tT);
+    // log E_q[e^{-d}] = logsumexp(a_s) - logsumexp(a_t)
+    const float lme_q = log_mean_exp(s.qx / s.ltT, o.lse_sT - o.lse_tT);
+    o.dlse = -lme_q;
+    const float kl_f = s.qd / s.ltT + lme_q;
     const float kl_r = s.pd / s.lsT + log_mean_exp(s.px / s.lsT, o.lse_tT - o.lse_sT);
     o.kl_rev = kl_r;
     if (variant == KD_KL_FORWARD) o.kl = kl_f;
@@ -275,23 +281,36 @@ __device__ __forceinline__ RowOut finalize(const RowState& s, const Consts& c, i
   return o;
 }
 
-// log m = log((1-b) q + b p) from log p and log q, evaluated as a log-add so
-// that neither an underflowing p nor q/p overflow can reach it.
-__device__ __forceinline__ float log_mix(float lp, float lq, const Consts& c) {
-  const float u = lq + c.log_1mb, v = lp + c.log_b;
-  const float mx = fmaxf(u, v), mn = fminf(u, v);
-  return mx + __logf(1.f + ex2((mn - mx) * kL2E));
+// Skew-JS terms in x = log p - log q = (a_s - a_t) + (lse(a_t) - lse(a_s)):
+// with m = (1-b) q + b p,  w = log(m/q) = log((1-b) + b e^x), evaluated as
+//   x <= 0:  log1p(b expm1(x)),   x > 0:  x + log1p((1-b) expm1(-x)),
+// which neither overflows nor loses the small divergences of nearby
+// distributions; then log(q/m) = -w and log(p/m) = x - w.
+__device__ __forceinline__ float js_w(float x, const Consts& c) {
+  const bool neg = x <= 0.f;
+  const float coef = neg ? c.beta : 1.f - c.beta;
+  const float y = neg ? x : -x;
+  float e, l;
+  if (c.precise) {
+    e = expm1f(y);
+    l = log1pf(coef * e);
+  } else {
+    e = ex2(y * kL2E) - 1.f;
+    l = __logf(fmaf(coef, e, 1.f));
+  }
+  return neg ? l : x + l;
 }
 
-// Skew-JS second pass: with the final log-normalisers known, accumulate
-// jq += q log(q/m) and jp += p log(p/m), m = (1-b) q + b p.
-__device__ __forceinline__ void js_terms(float zs, float zt, float lse_sT, float lse_tT,
+// Skew-JS second pass: with the final normalisers known, accumulate
+// jq += q log(q/m) and jp += p log(p/m).
+__device__ __forceinline__ void js_terms(float zs, float zt, float lse_tT, float dlse,
                                          const Consts& c, float& jq, float& jp) {
-  const float lp = zs * c.inv_ts - lse_sT;
+  const float x = fmaf(zs, c.inv_ts, -zt * c.inv_tt) + dlse;
   const float lq = zt * c.inv_tt - lse_tT;
-  const float lm = log_mix(lp, lq, c);
-  jq = fmaf(ex2(lq * kL2E), lq - lm, jq);
-  jp = fmaf(ex2(lp * kL2E), lp - lm, jp);
+  const float w = js_w(x, c);
+  const float q = ex2(lq * kL2E), p = ex2((lq + x) * kL2E);
+  jq = fmaf(q, -w, jq);
+  jp = fmaf(p, x - w, jp);
 }
 
 // Gradient of the KL part w.r.t. a_s (teacher detached), per element, from
@@ -303,7 +322,10 @@ __device__ __forceinline__ float kl_grad(float zs, float zt, const float* stt, i
   const float lp = zs * c.inv_ts - stt[S_LSE_ST];
   const float lq = zt * c.inv_tt - stt[S_LSE_TT];
   const float p = ex2(lp * kL2E);
-  if (variant == KD_KL_SKEW_JS) return c.beta * p * (lp - log_mix(lp, lq, c) - stt[S_KL_PM]);
+  if (variant == KD_KL_SKEW_JS) {
+    const float x = fmaf(zs, c.inv_ts, -zt * c.inv_tt) + stt[S_DLSE];
+    return c.beta * p * (x - js_w(x, c) - stt[S_KL_PM]);
+  }
   float g = 0.f;
   if (variant != KD_KL_REVERSE) g = p - ex2(lq * kL2E);
   if (variant != KD_KL_FORWARD) g = fmaf(p, lp - lq - stt[S_KL_REV], g);

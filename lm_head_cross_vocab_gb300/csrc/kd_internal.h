@@ -11,6 +11,9 @@
 
 namespace kd {
 
+// Count `k` kernel launches (reported by kd_launch_count()).
+void note_launch(int k = 1);
+
 // ---------------------------------------------------------------- aux kernels
 // Count valid labels into *count (int32, zeroed by the caller) and flag bad ones.
 void launch_label_check(const int64_t* labels, int64_t n, int64_t vocab, int64_t ignore,

@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(NT) k_simt_fwd(SimtArgs a) {
       }
       if (a.js_pass) {
         for (int j = 0; j < nv; ++j)
-          js_terms(zs[j], zt[j], stt[S_LSE_ST], stt[S_LSE_TT], c, st.jq, st.jp);
+          js_terms(zs[j], zt[j], stt[S_LSE_TT], stt[S_DLSE], c, st.jq, st.jp);
       } else {
         if (has_t) update<8, true, true>(st, zs, zt, nv, c);
         else update<8, false, true>(st, zs, zt, nv, c);
@@ -197,12 +197,14 @@ __global__ void __launch_bounds__(NT) k_simt_gprod(SimtArgs a) {
 void launch_simt_fwd(const SimtArgs& a, cudaStream_t s) {
   if (a.n <= 0) return;
   dim3 grid((unsigned)((a.n + BM - 1) / BM), (unsigned)a.n_splits);
+  note_launch();
   k_simt_fwd<<<grid, NT, 0, s>>>(a);
 }
 
 void launch_simt_gprod(const SimtArgs& a, cudaStream_t s) {
   if (a.rc <= 0 || a.cc <= 0) return;
   dim3 grid((unsigned)((a.rc + BM - 1) / BM), (unsigned)((a.cc + BN - 1) / BN));
+  note_launch();
   k_simt_gprod<<<grid, NT, 0, s>>>(a);
 }
 
@@ -265,6 +267,7 @@ void launch_simt_gemm(const float* A, int64_t sam, int64_t sak, const float* B, 
                       bool accumulate, cudaStream_t s) {
   if (M <= 0 || N <= 0) return;
   dim3 grid((unsigned)((M + GM - 1) / GM), (unsigned)((N + GN - 1) / GN));
+  note_launch();
   k_simt_gemm<<<grid, NT, 0, s>>>(A, sam, sak, B, sbk, sbn, C, ldc, M, N, K, accumulate ? 1 : 0);
 }
 

@@ -195,13 +195,13 @@ __global__ void __launch_bounds__(kThreads) k_stream_fwd(StreamArgs a) {
       if (a.kl && !(HAS_T && a.variant == KD_KL_SKEW_JS)) a.kl[row] = valid ? o.kl : 0.f;
       float4* s4 = reinterpret_cast<float4*>(a.stats + row * KD_STATS_PER_TOKEN);
       s4[0] = make_float4(o.lse_s1, o.lse_sT, o.lse_t1, o.lse_tT);
-      s4[1] = make_float4(o.kl_rev, 0.f, mass, 0.f);
-      sh_lse[0] = o.lse_sT;
+      s4[1] = make_float4(o.kl_rev, 0.f, mass, o.dlse);
+      sh_lse[0] = o.dlse;
       sh_lse[1] = o.lse_tT;
     }
     if (HAS_T && a.variant == KD_KL_SKEW_JS) {
       __syncthreads();
-      const float lse_sT = sh_lse[0], lse_tT = sh_lse[1];
+      const float dlse = sh_lse[0], lse_tT = sh_lse[1];
       float jq = 0.f, jp = 0.f;
       if (VEC) {
         const int64_t nvec = V / 8;
@@ -210,11 +210,11 @@ __global__ void __launch_bounds__(kThreads) k_stream_fwd(StreamArgs a) {
           load8<T>(zs, v, fs);
           load8<T>(zt, v, ft);
 #pragma unroll
-          for (int u = 0; u < 8; ++u) js_terms(fs[u], ft[u], lse_sT, lse_tT, c, jq, jp);
+          for (int u = 0; u < 8; ++u) js_terms(fs[u], ft[u], lse_tT, dlse, c, jq, jp);
         }
       } else {
         for (int64_t e = threadIdx.x; e < V; e += kThreads)
-          js_terms(ld1<T>(zs + e), ld1<T>(zt + e), lse_sT, lse_tT, c, jq, jp);
+          js_terms(ld1<T>(zs + e), ld1<T>(zt + e), lse_tT, dlse, c, jq, jp);
       }
       const float2 r = block_sum2(jq, jp, sh);
       if (threadIdx.x == 0) {
@@ -311,6 +311,7 @@ static void fwd_dispatch(const StreamArgs& a, cudaStream_t s) {
   const bool vec = (a.vocab % 8 == 0) && aligned16(a.zs) && (!a.zt || aligned16(a.zt));
   const unsigned grid = (unsigned)(a.n < 2147483647 ? a.n : 2147483647);
   const bool has_t = a.zt != nullptr;
+  note_launch();
   if (has_t && vec) k_stream_fwd<T, true, true><<<grid, kThreads, 0, s>>>(a);
   else if (has_t) k_stream_fwd<T, true, false><<<grid, kThreads, 0, s>>>(a);
   else if (vec) k_stream_fwd<T, false, true><<<grid, kThreads, 0, s>>>(a);
@@ -325,12 +326,14 @@ static void bwd_dispatch(const StreamArgs& a, cudaStream_t s) {
   dim3 grid((unsigned)((a.vocab + per_cta - 1) / per_cta),
             (unsigned)(a.n < 65535 ? a.n : 65535));
   const bool has_t = a.zt != nullptr;
+  note_launch();
   if (has_t && vec) k_stream_bwd<T, true, true><<<grid, 256, 0, s>>>(a);
   else if (has_t) k_stream_bwd<T, true, false><<<grid, 256, 0, s>>>(a);
   else if (vec) k_stream_bwd<T, false, true><<<grid, 256, 0, s>>>(a);
   else k_stream_bwd<T, false, false><<<grid, 256, 0, s>>>(a);
   if (a.topk && a.k > 0) {
     const int64_t tot = a.n * a.k;
+    note_launch();
     k_stream_bwd_topk<T><<<(unsigned)((tot + 255) / 256), 256, 0, s>>>(a);
   }
 }

@@ -285,10 +285,10 @@ struct FwdEpi {
     if (nv <= 0) return;
     if (a.js_pass) {
       const float* stt = a.stats + row * KD_STATS_PER_TOKEN;
-      const float ls = stt[S_LSE_ST], lt = stt[S_LSE_TT];
+      const float lt = stt[S_LSE_TT], dl = stt[S_DLSE];
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if (j < nv) js_terms(vs[j], vt[j], ls, lt, a.c, st.jq, st.jp);
+        if (j < nv) js_terms(vs[j], vt[j], lt, dl, a.c, st.jq, st.jp);
       return;
     }
     if (nv == 32) update<32, HAS_T, false>(st, vs, vt, 32, a.c);
@@ -741,6 +741,7 @@ int launch(const TcParams& P, int num_ctas, cudaStream_t s) {
   if (e != cudaSuccess) return (int)e;
   const int grid = P.items < num_ctas ? P.items : num_ctas;
   if (grid <= 0) return 0;
+  note_launch();
   kern<<<grid, kThreads, C::SMEM_BYTES, s>>>(P);
   return (int)cudaGetLastError();
 }

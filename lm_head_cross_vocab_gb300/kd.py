@@ -93,8 +93,10 @@ def load_library(path: str = LIB_PATH):
     lib.kd_device_supported.argtypes = [ctypes.c_int]
     lib.kd_diag_gemm_bf16.argtypes = [vp, vp, vp, ctypes.c_int64, ctypes.c_int64,
                                       ctypes.c_int64, vp]
+    lib.kd_set_profile_events.argtypes = [vp, vp, vp, vp]
+    lib.kd_launch_count.restype = ctypes.c_uint64
     for f in ("kd_workspace_size", "kd_fwd", "kd_bwd", "kd_device_supported", "kd_abi_version",
-              "kd_diag_gemm_bf16"):
+              "kd_diag_gemm_bf16", "kd_set_profile_events"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -144,6 +146,18 @@ def kd_diag_gemm_bf16(a: torch.Tensor, b: torch.Tensor) -> torch.Tensor:
     if st != KD_OK:
         raise KDError(st, "kd_diag_gemm_bf16")
     return c
+
+
+def kd_set_profile_events(fwd_start=None, fwd_stop=None, bwd_start=None, bwd_stop=None):
+    """Record torch.cuda.Event objects around the fused forward / backward sections."""
+    h = [None if e is None else e.cuda_event for e in (fwd_start, fwd_stop, bwd_start, bwd_stop)]
+    st = load_library().kd_set_profile_events(*h)
+    if st != KD_OK:
+        raise KDError(st, "kd_set_profile_events")
+
+
+def kd_launch_count() -> int:
+    return int(load_library().kd_launch_count())
 
 
 # ---------------------------------------------------------------- helpers
