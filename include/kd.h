@@ -205,6 +205,32 @@ int kd_abi_version(void);
 kd_status kd_diag_gemm_bf16(const void* a, const void* b, float* c, int64_t m, int64_t n,
                             int64_t k, void* stream);
 
+/* Size of the fixed device scratch array used by kd_fwd_static_scratch. */
+#define KD_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/* Forward that allocates nothing and takes no workspace (the pages have no
+ * counterpart: this exists for callers of this library, not for the method).
+ * For callers that cannot allocate device memory -- a plugin inside a host
+ * program that owns every device buffer and passes only the step's tensors,
+ * or a runtime that must not call cudaMalloc mid-step because it can
+ * synchronise the device and fail -- it runs exactly kd_fwd, with kd_fwd's
+ * scratch taken from a fixed KD_STATIC_SCRATCH_BYTES array in the library's
+ * device image (held by every GPU that loads the library until the process
+ * exits).  Inputs and outputs are the caller's, as for kd_fwd.
+ *   - Returns KD_ERR_WORKSPACE, without launching anything, when the problem
+ *     needs more scratch than KD_STATIC_SCRATCH_BYTES (kd_workspace_size()'s
+ *     fwd_bytes tells in advance).
+ *   - The first call on a device looks up the array's device address with that
+ *     device current and caches it; make that first call before any stream
+ *     capture.
+ *   - Every call on a device shares the one array and the array keeps the last
+ *     call's contents; the call clears what must start at zero.  Calls whose
+ *     work overlaps on the GPU (for example on two streams at once) race on the
+ *     array: order them on one stream or with events. */
+kd_status kd_fwd_static_scratch(const kd_problem* problem, const kd_inputs* inputs, float* ce_s,
+                                float* ce_t, float* kl, float* stats, float* loss,
+                                uint32_t* dev_status, void* stream);
+
 /* Profiling aid.  When the events are non-NULL (cudaEvent_t handles created by
  * the caller), every later kd_fwd records fwd_start right before and fwd_stop
  * right after its fused projection launch(es) on the call's stream, and

@@ -33,6 +33,7 @@ KD_TEACHER_NONE, KD_TEACHER_TIED, KD_TEACHER_SEPARATE, KD_TEACHER_LOGITS, KD_TEA
 KD_KL_FORWARD, KD_KL_REVERSE, KD_KL_JEFFREYS, KD_KL_SKEW_JS = range(4)
 KD_REDUCE_MEAN, KD_REDUCE_SUM = 0, 1
 KD_STATS_PER_TOKEN = 8
+KD_STATIC_SCRATCH_BYTES = 32 << 20
 
 DTYPES = {"bf16": KD_BF16, "fp32": KD_FP32}
 STUDENTS = {"hidden": KD_STUDENT_HIDDEN, "logits": KD_STUDENT_LOGITS}
@@ -94,9 +95,10 @@ def load_library(path: str = LIB_PATH):
     lib.kd_diag_gemm_bf16.argtypes = [vp, vp, vp, ctypes.c_int64, ctypes.c_int64,
                                       ctypes.c_int64, vp]
     lib.kd_set_profile_events.argtypes = [vp, vp, vp, vp]
+    lib.kd_fwd_static_scratch.argtypes = [P, I, vp, vp, vp, vp, vp, vp, vp]
     lib.kd_launch_count.restype = ctypes.c_uint64
     for f in ("kd_workspace_size", "kd_fwd", "kd_bwd", "kd_device_supported", "kd_abi_version",
-              "kd_diag_gemm_bf16", "kd_set_profile_events"):
+              "kd_diag_gemm_bf16", "kd_set_profile_events", "kd_fwd_static_scratch"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -127,6 +129,12 @@ def kd_workspace_size(problem: kd_problem):
 def kd_fwd(problem, inputs, ce_s, ce_t, kl, stats, loss, dev_status, workspace, ws_bytes, stream):
     return int(load_library().kd_fwd(ctypes.byref(problem), ctypes.byref(inputs), ce_s, ce_t, kl,
                                      stats, loss, dev_status, workspace, ws_bytes, stream))
+
+
+def kd_fwd_static_scratch(problem, inputs, ce_s, ce_t, kl, stats, loss, dev_status, stream):
+    return int(load_library().kd_fwd_static_scratch(ctypes.byref(problem), ctypes.byref(inputs),
+                                                    ce_s, ce_t, kl, stats, loss, dev_status,
+                                                    stream))
 
 
 def kd_bwd(problem, inputs, stats, d_loss, grad_scale, d_h_s, d_w_s, d_logits_s, dev_status,
