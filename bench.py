@@ -209,9 +209,8 @@ def main():
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    from lm_head_cross_vocab_gb300 import dist as D
+    rank, world, local = D.world_from_env()
     w = I.WORKLOADS[args.config]
 
     if args.impl == "reference":
@@ -275,11 +274,7 @@ def main():
             dist.barrier()
     kd.kd_set_profile_events()
     launches = kd.kd_launch_count() - launches0
-    ms = start.elapsed_time(stop)
-    if dist:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = D.max_over_ranks(start.elapsed_time(stop), dev)
     ms_step = ms / n
     tokens = w.n_tokens * world
     value = tokens / (ms_step / 1e3)
@@ -338,11 +333,7 @@ def main():
             e2e_step()
         e2.record()
         torch.cuda.synchronize()
-        ms_e = s2.elapsed_time(e2)
-        if dist:
-            tt = torch.tensor([ms_e], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ms_e = float(tt.item())
+        ms_e = D.max_over_ranks(s2.elapsed_time(e2), dev)
         e2e = {"value": tokens / (ms_e / ne / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e / ne}
 

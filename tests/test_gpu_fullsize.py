@@ -1,0 +1,124 @@
+"""Parity at the workloads' full sizes, in the launch configuration bench.py uses
+(automatic splits and chunking).
+
+* separate-teacher bf16 (4096 tokens, D_s 2048, D_t 4096, V 32000): every token and
+  every gradient element against the oracle, evaluated in row blocks;
+* top-K (32768 tokens, V 151936), scoring (8192 tokens, V 248320) and logit pairs
+  (16384 tokens, V 128256): the oracle evaluates a seeded sample of tokens one by one
+  (row-local quantities: per-token CE / KL, dH rows, d z_s rows).
+"""
+import numpy as np
+import pytest
+import torch
+
+from lm_head_cross_vocab_gb300 import inputs as I
+from lm_head_cross_vocab_gb300 import kd
+from oracle import kd_oracle as O
+from tests.parity_util import GRAD_TOL, TOK_TOL, oracle_kwargs, rel_l2, token_rel_err
+
+pytestmark = pytest.mark.gpu
+
+W = I.WORKLOADS
+
+
+def _run(w, backward=True):
+    t = I.make_inputs(w, "cuda")
+    prob = kd.problem_for(w, vocab_chunk=0, seq_chunk=0)
+    fwd = kd.forward(prob, t)
+    want = ("h_s", "w_s") if w.student == "hidden" else ("logits_s",)
+    bwd = kd.backward(prob, t, fwd["stats"], want=want) if backward else None
+    torch.cuda.synchronize()
+    return t, prob, fwd, bwd
+
+
+def test_fullsize_separate_teacher_every_element():
+    w = W[2]
+    t, prob, fwd, bwd = _run(w)
+    cpu = {k: v.cpu() for k, v in t.items()}
+    labels = cpu["labels"].numpy()
+    kw = oracle_kwargs(w, prob)
+    w_s, w_t = O.as_f64(cpu["w_s"]), O.as_f64(cpu["w_t"])
+    h_s, h_t = O.as_f64(cpu["h_s"]), O.as_f64(cpu["h_t"])
+    n = w.n_tokens
+    valid = labels != w.ignore_index
+    denom = float(valid.sum())
+    ce_s, ce_t, kl = (np.zeros(n) for _ in range(3))
+    d_h = np.zeros_like(h_s)
+    d_w = np.zeros_like(w_s)
+    blk = 512
+    for r0 in range(0, n, blk):
+        sl = slice(r0, r0 + blk)
+        z_s, z_t = h_s[sl] @ w_s.T, h_t[sl] @ w_t.T
+        out = O.forward(z_s, z_t, labels[sl], **{**kw, "reduction": "sum"})
+        ce_s[sl], ce_t[sl], kl[sl] = out["ce_s"], out["ce_t"], out["kl"]
+        g, _ = O.grad_logits(z_s, z_t, labels[sl], **{**kw, "reduction": "sum"})
+        g /= denom  # mean over all valid tokens of the batch
+        d_h[sl] = g @ w_s
+        d_w += g.T @ h_s[sl]
+    loss = float(np.sum(np.where(valid, w.w_student_ce * ce_s + w.w_teacher_ce * ce_t
+                                 + w.w_kl * w.t_student ** 2 * kl, 0.0)) / denom)
+    tol = TOK_TOL["bf16"]
+    for key, ref in (("ce_s", ce_s), ("ce_t", ce_t), ("kl", kl)):
+        err = token_rel_err(fwd[key].cpu().double().numpy(), ref, valid)
+        assert err <= tol, (key, err)
+    assert abs(fwd["loss"].item() - loss) <= tol * abs(loss)
+    assert rel_l2(bwd["d_h_s"].cpu().double().numpy(), d_h) <= GRAD_TOL["bf16"]
+    assert rel_l2(bwd["d_w_s"].cpu().double().numpy(), d_w) <= GRAD_TOL["bf16"]
+    assert not bwd["d_h_s"].cpu()[~torch.from_numpy(valid)].any()
+
+
+def _sample(n, k, seed):
+    return np.sort(np.random.default_rng(seed).choice(n, k, replace=False))
+
+
+def test_fullsize_topk_sampled_tokens():
+    w = W[4]
+    t, prob, fwd, bwd = _run(w)
+    rows = _sample(w.n_tokens, 12, 4)
+    cpu = {k: t[k][rows].cpu() for k in ("h_s", "topk_idx", "topk_p")}
+    w_s = t["w_s"].cpu()
+    z = O.project(cpu["h_s"], w_s)
+    kw = oracle_kwargs(w, prob)
+    idx, p = cpu["topk_idx"].numpy(), cpu["topk_p"].numpy()
+    out = O.forward(z, None, None, topk_idx=idx, topk_p=p, **{**kw, "reduction": "sum"})
+    valid = np.ones(len(rows), bool)
+    err = token_rel_err(fwd["kl"][rows].cpu().double().numpy(), out["kl"], valid)
+    assert err <= TOK_TOL["bf16"], err
+    # dH rows: the batch mean divides by all 32768 tokens (no ignore mask)
+    g, _ = O.grad_logits(z, None, None, topk_idx=idx, topk_p=p, **{**kw, "reduction": "sum"})
+    d_h = (g / w.n_tokens) @ O.as_f64(w_s)
+    assert valid.all()
+    assert rel_l2(bwd["d_h_s"][rows].cpu().double().numpy(), d_h) <= GRAD_TOL["bf16"]
+
+
+def test_fullsize_scoring_sampled_tokens():
+    w = W[3]
+    t, prob, fwd, _ = _run(w, backward=False)
+    rows = _sample(w.n_tokens, 12, 3)
+    z_s = O.as_f64(t["logits_s"][rows].cpu())
+    z_t = O.project(t["h_t"][rows].cpu(), t["w_t"].cpu())
+    labels = t["labels"][rows].cpu().numpy()
+    out = O.forward(z_s, z_t, labels, **{**oracle_kwargs(w, prob), "reduction": "sum"})
+    valid = labels != w.ignore_index
+    for key in ("ce_s", "kl"):
+        err = token_rel_err(fwd[key][rows].cpu().double().numpy(), out[key], valid)
+        assert err <= TOK_TOL["bf16"], (key, err)
+
+
+@pytest.mark.parametrize("variant", ["forward", "reverse", "skew_js"])
+def test_fullsize_logit_pair_sampled_tokens(variant):
+    w = W[5].scaled(variant=variant)
+    t, prob, fwd, bwd = _run(w)
+    rows = _sample(w.n_tokens, 8, 5)
+    z_s = O.as_f64(t["logits_s"][rows].cpu())
+    z_t = O.as_f64(t["logits_t"][rows].cpu())
+    labels = t["labels"][rows].cpu().numpy()
+    kw = {**oracle_kwargs(w, prob), "reduction": "sum"}
+    out = O.forward(z_s, z_t, labels, **kw)
+    valid = labels != w.ignore_index
+    err = token_rel_err(fwd["kl"][rows].cpu().double().numpy(), out["kl"], valid)
+    assert err <= TOK_TOL["bf16"], err
+    n_valid = int((t["labels"] != w.ignore_index).sum().item())
+    g, _ = O.grad_logits(z_s, z_t, labels, **kw)
+    got = bwd["d_logits_s"][rows].cpu().double().numpy()
+    assert rel_l2(got, g / n_valid) <= GRAD_TOL["bf16"]
