@@ -245,8 +245,11 @@ kd_status make_plan(const kd_problem* p, bool has_labels, Plan& P) {
     P.f_ent = f.take(n * 4);
   }
   if (P.path == PATH_TC) {
-    const int bn = (P.s_gemm && P.t_gemm) ? 128 : 256;
-    P.n_splits = choose_splits(cdiv(std::max<int64_t>(n, 1), 128), cdiv(v, bn), P.nsm);
+    const bool pair = tc_use_pairs();
+    const int bn = tc_fused_tile_cols(P.s_gemm && P.t_gemm, pair);
+    const int rows = tc_tile_rows(pair);
+    P.n_splits = choose_splits(cdiv(std::max<int64_t>(n, 1), rows), cdiv(v, bn),
+                               pair ? std::max(1, P.nsm / 2) : P.nsm);
     P.n_parts = 2 * P.n_splits;
   } else if (P.path == PATH_SIMT) {
     const int64_t mt = cdiv(std::max<int64_t>(n, 1), 32), nt = cdiv(v, 64);

@@ -15,16 +15,26 @@
 //             (dH and dW from the G chunks)
 //
 // Roles (320 threads): warp 0 issues TMA loads into a STAGES-deep shared
-// memory ring; warp 1 owns the TMEM allocation (512 columns: two accumulator
-// stages of 256) and issues tcgen05.mma from one lane; warps 2..9 drain TMEM
-// with tcgen05.ld (warp w reads TMEM lanes 32*(w%4).., half (w-2)/4 of the
-// tile's columns), so the epilogue of tile i overlaps the MMAs of tile i+1.
+// memory ring; warp 1 owns the TMEM allocation (512 columns: one or two
+// accumulator stages) and issues tcgen05.mma from one lane; warps 2..9 drain
+// TMEM with tcgen05.ld (warp w reads TMEM lanes 32*(w%4).., half (w-2)/4 of
+// the tile's columns); with two stages the epilogue of tile i overlaps the
+// MMAs of tile i+1.
+//
+// PAIR = true runs the kernel on CTA pairs (clusters of 2, cta_group::2): one
+// MMA of M = 256 rows x N = 256 columns spans both SMs; each CTA loads only its
+// 128 rows of A and its half of the B columns, so each SM moves half the
+// operand bytes per FLOP of a single-CTA 128 x 256 tile.  The even CTA issues
+// the MMAs; both CTAs' TMA loads complete on its barriers, its commits arrive
+// on both CTAs' barriers, and both CTAs' epilogues release the accumulator on
+// its barrier.
 // Every mbarrier wait is bounded in time; on expiry the kernel raises
 // KD_DEV_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -111,6 +121,79 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");
 }
+// ---- CTA-pair (cta_group::2) forms
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// address of the same shared-memory variable in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+// TMA load into this CTA's shared memory, completing on a barrier of either CTA
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols));
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
+}
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+// arrive on the barrier at this offset in both CTAs of the pair
+__device__ __forceinline__ void mma_commit_pair_both(uint32_t bar) {
+  const uint16_t mask = 3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_pair_local(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
 // 32 lanes x 16 consecutive 32-bit columns
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   uint32_t r[16];
@@ -162,28 +245,34 @@ struct __align__(64) TcParams {
   int b_row0[2];      // row offset added to the B tile row coordinate
   int seg_accum[2];   // 1: the segment adds to an accumulator an earlier segment wrote
   int m_tiles, n_tiles, n_splits, items;
+  int acc_stride;     // TMEM columns per accumulator stage
+  int acc_stages;     // 1 or 2 accumulator stages in the 512 allocated columns
   int logits_vec;     // materialised logits rows are 16-byte aligned
   TcFwdArgs fwd;
   TcGradArgs grad;
   TcGemmArgs gemm;
 };
 
-template <int BN>
+template <int BN, bool PAIR>
 struct Cfg {
+  static constexpr int ROWS = PAIR ? 2 * BM : BM;     // tile rows (MMA M)
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;   // B rows this CTA loads
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TX_BYTES = PAIR ? 2 * STAGE_BYTES : STAGE_BYTES;  // per full barrier
   static constexpr int STAGES = (STAGE_BYTES <= 32768) ? 6 : 4;
   static constexpr int TILE_BYTES = STAGES * STAGE_BYTES;
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM_BYTES = TILE_BYTES + BAR_BYTES + 1024;  // + alignment slack
-  static constexpr uint32_t IDESC = make_idesc(BM, BN);
+  static constexpr uint32_t IDESC = make_idesc(ROWS, BN);
 };
 
 struct Sync {
   uint32_t full, empty, acc_full, acc_empty, drain;  // smem addresses of barrier arrays
   volatile int* abort_flag;
   uint32_t* status;
+  bool cluster_acquire;  // waits on barriers the peer CTA arrives on remotely
 };
 
 // Lane 0 waits (bounded in time), the outcome is broadcast to the warp.
@@ -191,11 +280,14 @@ __device__ __forceinline__ bool warp_wait(const Sync& s, uint32_t bar, uint32_t 
                                           bool honour_abort = true) {
   int ok = 1;
   if ((threadIdx.x & 31) == 0) {
-    if (!mbar_try(bar, parity)) {
+    auto probe = [&]() {
+      return s.cluster_acquire ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity);
+    };
+    if (!probe()) {
       const uint64_t t0 = globaltimer();
       ok = 0;
       for (uint32_t it = 1;; ++it) {
-        if (mbar_try(bar, parity)) {
+        if (probe()) {
           ok = 1;
           break;
         }
@@ -258,11 +350,10 @@ struct FwdEpi {
   const float* ps;
   int kp;
 
-  __device__ __forceinline__ void begin(const TcParams& P, int m_tile, int t0, int r_in_tile,
-                                        int half) {
+  __device__ __forceinline__ void begin(const TcParams& P, int64_t row_, int t0, int half) {
     const TcFwdArgs& a = P.fwd;
     st.init();
-    row = (int64_t)m_tile * BM + r_in_tile;
+    row = row_;
     row_ok = row < a.n;
     y = (row_ok && a.labels) ? a.labels[row] : -1;
     ids = nullptr;
@@ -317,9 +408,9 @@ struct FwdEpi {
 };
 
 // ------------------------------------------------------------------ kernel
-template <int EPI, int BN, bool HAS_T>
+template <int EPI, int BN, bool HAS_T, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcParams P) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -338,8 +429,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
   S.drain = bars + 16 * C::STAGES + 32;       // [1]
   S.abort_flag = abort_flag;
   S.status = EPI == EPI_FWD ? P.fwd.status : EPI == EPI_GRAD ? P.grad.status : P.gemm.status;
+  S.cluster_acquire = false;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // CTA rank within the pair
+  const bool leader = rank == 0;                          // issues the MMAs
+  const int cid = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int ncl = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::STAGES; ++i) {
@@ -348,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(S.acc_full + 8 * i, 1);
-      mbar_init(S.acc_empty + 8 * i, 8);  // one arrive per epilogue warp
+      mbar_init(S.acc_empty + 8 * i, PAIR ? 16 : 8);  // one arrive per epilogue warp (both CTAs)
     }
     mbar_init(S.drain, 1);
     *abort_flag = 0;
@@ -360,11 +456,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
       }
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_holder), 512);
-    tmem_relinquish();
+    if (PAIR) {  // one warp of each CTA of the pair allocates collectively
+      tmem_alloc_pair(smem_u32(tmem_holder), 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_holder), 512);
+      tmem_relinquish();
+    }
     tc_fence_before();
   }
   __syncthreads();
+  if (PAIR) cluster_sync();  // the peer's barriers and TMEM exist before any remote use
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
@@ -373,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
     int stage = 0;
     uint32_t phase = 0, issued = 0, par = 0;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < P.items; item += gridDim.x) {
+    for (int item = cid; ok && item < P.items; item += ncl) {
       int m_tile, t0, t1;
       item_range(P, item, m_tile, t0, t1);
       for (int t = t0; ok && t < t1; ++t)
@@ -385,11 +487,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
             }
             if (lane == 0) {
               const uint32_t fb = S.full + 8 * stage;
-              mbar_expect_tx(fb, C::STAGE_BYTES);
-              tma_load_2d(sA + stage * C::A_BYTES, &P.ma[sg], fb, kb * BK,
-                          P.a_row0[sg] + m_tile * BM);
-              tma_load_2d(sB + stage * C::B_BYTES, &P.mb[sg], fb, kb * BK,
-                          P.b_row0[sg] + t * BN);
+              const int ay = P.a_row0[sg] + m_tile * C::ROWS + (int)rank * BM;
+              const int by = P.b_row0[sg] + t * BN + (int)rank * C::B_ROWS;
+              if (PAIR) {
+                // both CTAs' copies complete on the leader's barrier, which
+                // expects the bytes of the whole pair
+                const uint32_t fb0 = mapa_shared(fb, 0);
+                if (leader) mbar_expect_tx(fb, C::TX_BYTES);
+                tma_load_2d_pair(sA + stage * C::A_BYTES, &P.ma[sg], fb0, kb * BK, ay);
+                tma_load_2d_pair(sB + stage * C::B_BYTES, &P.mb[sg], fb0, kb * BK, by);
+              } else {
+                mbar_expect_tx(fb, C::TX_BYTES);
+                tma_load_2d(sA + stage * C::A_BYTES, &P.ma[sg], fb, kb * BK, ay);
+                tma_load_2d(sB + stage * C::B_BYTES, &P.mb[sg], fb, kb * BK, by);
+              }
             }
             __syncwarp();
             issued |= 1u << stage;
@@ -400,26 +511,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
             }
           }
     }
-    if (!ok) {  // wait for our own copies before the CTA exits
+    if (!ok && leader) {  // wait for the copies in flight (the leader's barriers see both CTAs')
       for (int s = 0; s < C::STAGES; ++s)
         if (issued & (1u << s)) warp_wait(S, S.full + 8 * s, (par >> s) & 1u, false);
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 && leader) {
     // ---------------------------------------------------------- MMA issuer
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < P.items; item += gridDim.x) {
+    Sync Sc = S;
+    Sc.cluster_acquire = PAIR;  // the peer's epilogue arrives on acc_empty remotely
+    for (int item = cid; ok && item < P.items; item += ncl) {
       int m_tile, t0, t1;
       item_range(P, item, m_tile, t0, t1);
       for (int t = t0; ok && t < t1; ++t) {
-        if (!warp_wait(S, S.acc_empty + 8 * acc, acc_phase ^ 1)) {
+        if (!warp_wait(Sc, S.acc_empty + 8 * acc, acc_phase ^ 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
         for (int sg = 0; ok && sg < 2; ++sg) {
-          const uint32_t d = tmem + acc * 256 + P.acc_off[sg];
+          const uint32_t d = tmem + acc * P.acc_stride + P.acc_off[sg];
           for (int kb = 0; kb < P.kb[sg]; ++kb) {
             if (!warp_wait(S, S.full + 8 * stage, phase)) {
               ok = false;
@@ -430,10 +543,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
               const uint64_t ad = smem_desc(sA + stage * C::A_BYTES);
               const uint64_t bd = smem_desc(sB + stage * C::B_BYTES);
 #pragma unroll
-              for (int k = 0; k < BK / 16; ++k)
-                mma_bf16(d, ad + 2 * k, bd + 2 * k, C::IDESC,
-                         (kb > 0 || k > 0 || P.seg_accum[sg]) ? 1u : 0u);
-              mma_commit(S.empty + 8 * stage);
+              for (int k = 0; k < BK / 16; ++k) {
+                const uint32_t accum = (kb > 0 || k > 0 || P.seg_accum[sg]) ? 1u : 0u;
+                if (PAIR) mma_bf16_pair(d, ad + 2 * k, bd + 2 * k, C::IDESC, accum);
+                else mma_bf16(d, ad + 2 * k, bd + 2 * k, C::IDESC, accum);
+              }
+              if (PAIR) mma_commit_pair_both(S.empty + 8 * stage);  // frees the stage in both CTAs
+              else mma_commit(S.empty + 8 * stage);
             }
             __syncwarp();
             if (++stage == C::STAGES) {
@@ -443,19 +559,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
           }
         }
         if (!ok) break;
-        if (lane == 0) mma_commit(S.acc_full + 8 * acc);
+        if (lane == 0) {
+          if (PAIR) mma_commit_pair_both(S.acc_full + 8 * acc);
+          else mma_commit(S.acc_full + 8 * acc);
+        }
         __syncwarp();
-        if (++acc == 2) {
+        if (++acc == P.acc_stages) {
           acc = 0;
           acc_phase ^= 1;
         }
       }
     }
     // wait until every MMA this thread issued has completed
-    if (lane == 0) mma_commit(S.drain);
+    if (lane == 0) {
+      if (PAIR) mma_commit_pair_local(S.drain);
+      else mma_commit(S.drain);
+    }
     __syncwarp();
     warp_wait(S, S.drain, 0, false);
-  } else {
+  } else if (warp >= 2) {
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;              // TMEM lane quarter
     const int half = (warp - 2) >> 2;    // column half of the tile
@@ -464,21 +586,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < P.items; item += gridDim.x) {
+    const int r_in_pair = (int)rank * BM + r_in_tile;  // row within the (pair) tile
+    for (int item = cid; ok && item < P.items; item += ncl) {
       int m_tile, t0, t1;
       item_range(P, item, m_tile, t0, t1);
+      const int64_t tile_row = (int64_t)m_tile * C::ROWS + r_in_pair;
       FwdEpi<BN> fe;
-      if (EPI == EPI_FWD) fe.begin(P, m_tile, t0, r_in_tile, half);
+      if (EPI == EPI_FWD) fe.begin(P, tile_row, t0, half);
       for (int t = t0; t < t1; ++t) {
         if (!warp_wait(S, S.acc_full + 8 * acc, acc_phase)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t tbase = lane_base + acc * 256;
+        const uint32_t tbase = lane_base + acc * P.acc_stride;
         if (EPI == EPI_FWD) {
           const TcFwdArgs& a = P.fwd;
-          const int64_t row = (int64_t)m_tile * BM + r_in_tile;
+          const int64_t row = tile_row;
 #pragma unroll 1
           for (int cc = 0; cc < BN / 2; cc += 32) {
             const int col_in_tile = half * (BN / 2) + cc;
@@ -508,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
           }
         } else if (EPI == EPI_GRAD) {
           const TcGradArgs& a = P.grad;
-          const int64_t row = a.r0 + (int64_t)m_tile * BM + r_in_tile;
+          const int64_t row = a.r0 + tile_row;
           const bool row_ok = row < a.r0 + a.rc;
           float scale = 0.f;
           const float* stt = nullptr;
@@ -617,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
           }
         } else {  // EPI_GEMM
           const TcGemmArgs& a = P.gemm;
-          const int64_t row = (int64_t)m_tile * BM + r_in_tile;
+          const int64_t row = tile_row;
 #pragma unroll 1
           for (int cc = 0; cc < BN / 2; cc += 32) {
             const int col_in_tile = half * (BN / 2) + cc;
@@ -685,8 +809,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(S.acc_empty + 8 * acc);
-        if (++acc == 2) {
+        if (lane == 0) {
+          if (PAIR) mbar_arrive_cluster(mapa_shared(S.acc_empty + 8 * acc, 0));
+          else mbar_arrive(S.acc_empty + 8 * acc);
+        }
+        if (++acc == P.acc_stages) {
           acc = 0;
           acc_phase ^= 1;
         }
@@ -696,8 +823,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // no CTA leaves while its peer may still touch it
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 512);
+  if (warp == 1) {
+    if (PAIR) tmem_dealloc_pair(tmem, 512);
+    else tmem_dealloc(tmem, 512);
+  }
 }
 
 // ------------------------------------------------------------------ host
@@ -732,17 +863,44 @@ bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64
   return r == CUDA_SUCCESS;
 }
 
-template <int EPI, int BN, bool HAS_T>
-int launch(const TcParams& P, int num_ctas, cudaStream_t s) {
-  using C = Cfg<BN>;
-  auto kern = k_tc<EPI, BN, HAS_T>;
+template <int EPI, int BN, bool HAS_T, bool PAIR>
+int launch(const TcParams& P, int num_sms, cudaStream_t s) {
+  using C = Cfg<BN, PAIR>;
+  auto kern = k_tc<EPI, BN, HAS_T, PAIR>;
+  static int max_clusters = -1;  // co-resident CTA pairs (cached per instantiation)
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return (int)e;
-  const int grid = P.items < num_ctas ? P.items : num_ctas;
-  if (grid <= 0) return 0;
+  if (P.items <= 0) return 0;
+  if (!PAIR) {
+    const int grid = P.items < num_sms ? P.items : num_sms;
+    note_launch();
+    kern<<<grid, kThreads, C::SMEM_BYTES, s>>>(P);
+    return (int)cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_clusters < 0) {
+    cfg.gridDim = dim3(2 * (num_sms / 2));
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = num_sms / 2;
+    max_clusters = n;
+  }
+  const int clusters = P.items < max_clusters ? P.items : max_clusters;
+  cfg.gridDim = dim3(2 * clusters);
   note_launch();
-  kern<<<grid, kThreads, C::SMEM_BYTES, s>>>(P);
+  e = cudaLaunchKernelEx(&cfg, kern, P);
+  if (e != cudaSuccess) return (int)e;
   return (int)cudaGetLastError();
 }
 
@@ -753,13 +911,14 @@ bool logits_vec_ok(const void* p, int64_t vocab) {
 int fail_map() { return (int)cudaErrorInvalidValue; }
 
 // Segment setup shared by the fused forward and the gradient producer.
+// bn = tile columns, b_box = B rows one CTA loads, rows_per_tile = MMA M.
 template <class A>
-bool setup_segments(TcParams& P, const A& a, int bn, int64_t r0, int64_t rows, int64_t c0,
-                    int64_t cols) {
+bool setup_segments(TcParams& P, const A& a, int bn, int b_box, int rows_per_tile, int64_t r0,
+                    int64_t rows, int64_t c0, int64_t cols) {
   int ns = 0;
   if (a.s_gemm) {
     if (!make_map(&P.ma[ns], a.h_s, a.n, a.d_s, a.d_s, BM) ||
-        !make_map(&P.mb[ns], a.w_s, a.vocab, a.d_s, a.d_s, bn))
+        !make_map(&P.mb[ns], a.w_s, a.vocab, a.d_s, a.d_s, b_box))
       return false;
     P.kb[ns] = (int)((a.d_s + BK - 1) / BK);
     P.acc_off[ns] = 0;
@@ -770,7 +929,7 @@ bool setup_segments(TcParams& P, const A& a, int bn, int64_t r0, int64_t rows, i
   if (a.t_gemm) {
     const void* wt = a.w_t ? a.w_t : a.w_s;  // tied teachers use the student head
     if (!make_map(&P.ma[ns], a.h_t, a.n, a.d_t, a.d_t, BM) ||
-        !make_map(&P.mb[ns], wt, a.vocab, a.d_t, a.d_t, bn))
+        !make_map(&P.mb[ns], wt, a.vocab, a.d_t, a.d_t, b_box))
       return false;
     P.kb[ns] = (int)((a.d_t + BK - 1) / BK);
     P.acc_off[ns] = a.s_gemm ? bn : 0;
@@ -778,7 +937,10 @@ bool setup_segments(TcParams& P, const A& a, int bn, int64_t r0, int64_t rows, i
     P.b_row0[ns] = (int)c0;
     ++ns;
   }
-  P.m_tiles = (int)((rows + BM - 1) / BM);
+  const int sides = ns;
+  P.acc_stride = sides * bn;             // 256 or 512 TMEM columns per stage
+  P.acc_stages = 512 / P.acc_stride;     // 2 or 1
+  P.m_tiles = (int)((rows + rows_per_tile - 1) / rows_per_tile);
   P.n_tiles = (int)((cols + bn - 1) / bn);
   return true;
 }
@@ -792,61 +954,90 @@ int tc_num_sms() {
   return n;
 }
 
-int launch_tc_fwd(const TcFwdArgs& a, int num_ctas, cudaStream_t s) {
+// CTA pairs unless KD_TC_PAIR=0 (debug override: single-CTA tiles).
+bool tc_use_pairs() {
+  const char* e = getenv("KD_TC_PAIR");
+  return !(e && e[0] == '0');
+}
+
+// Tile columns of the fused kernels: two GEMM sides share the 512 TMEM
+// columns (single CTA: 128 per side, double buffered; pairs: 256 per side,
+// one stage); one side always gets 256 columns, double buffered.
+int tc_fused_tile_cols(bool two_sides, bool pair) { return (two_sides && !pair) ? 128 : 256; }
+int tc_tile_rows(bool pair) { return pair ? 2 * BM : BM; }
+
+int launch_tc_fwd(const TcFwdArgs& a, int num_sms, cudaStream_t s) {
   TcParams P;
   memset(&P, 0, sizeof(P));
-  const int bn = (a.s_gemm && a.t_gemm) ? 128 : 256;
-  if (!setup_segments(P, a, bn, 0, a.n, 0, a.vocab)) return fail_map();
+  const bool pair = tc_use_pairs();
+  const bool two = a.s_gemm && a.t_gemm;
+  const int bn = tc_fused_tile_cols(two, pair);
+  if (!setup_segments(P, a, bn, pair ? bn / 2 : bn, tc_tile_rows(pair), 0, a.n, 0, a.vocab))
+    return fail_map();
   P.n_splits = a.n_splits;
   P.items = P.m_tiles * P.n_splits;
   P.logits_vec = logits_vec_ok(a.zs_logits, a.vocab) && logits_vec_ok(a.zt_logits, a.vocab);
   P.fwd = a;
   const bool has_t = a.t_gemm || a.t_logits;
+  if (pair)
+    return has_t ? launch<EPI_FWD, 256, true, true>(P, num_sms, s)
+                 : launch<EPI_FWD, 256, false, true>(P, num_sms, s);
   if (bn == 128)
-    return has_t ? launch<EPI_FWD, 128, true>(P, num_ctas, s)
-                 : launch<EPI_FWD, 128, false>(P, num_ctas, s);
-  return has_t ? launch<EPI_FWD, 256, true>(P, num_ctas, s)
-               : launch<EPI_FWD, 256, false>(P, num_ctas, s);
+    return has_t ? launch<EPI_FWD, 128, true, false>(P, num_sms, s)
+                 : launch<EPI_FWD, 128, false, false>(P, num_sms, s);
+  return has_t ? launch<EPI_FWD, 256, true, false>(P, num_sms, s)
+               : launch<EPI_FWD, 256, false, false>(P, num_sms, s);
 }
 
-int launch_tc_grad(const TcGradArgs& a, int num_ctas, cudaStream_t s) {
+int launch_tc_grad(const TcGradArgs& a, int num_sms, cudaStream_t s) {
   TcParams P;
   memset(&P, 0, sizeof(P));
-  const int bn = (a.s_gemm && a.t_gemm) ? 128 : 256;
-  if (!setup_segments(P, a, bn, a.r0, a.rc, a.c0, a.cc)) return fail_map();
+  const bool pair = tc_use_pairs();
+  const bool two = a.s_gemm && a.t_gemm;
+  const int bn = tc_fused_tile_cols(two, pair);
+  if (!setup_segments(P, a, bn, pair ? bn / 2 : bn, tc_tile_rows(pair), a.r0, a.rc, a.c0, a.cc))
+    return fail_map();
   P.n_splits = P.n_tiles;  // one tile per item
   P.items = P.m_tiles * P.n_tiles;
   P.logits_vec = logits_vec_ok(a.zs_logits, a.vocab) && logits_vec_ok(a.zt_logits, a.vocab);
   P.grad = a;
   const bool has_t = a.t_gemm || a.t_logits;
+  if (pair)
+    return has_t ? launch<EPI_GRAD, 256, true, true>(P, num_sms, s)
+                 : launch<EPI_GRAD, 256, false, true>(P, num_sms, s);
   if (bn == 128)
-    return has_t ? launch<EPI_GRAD, 128, true>(P, num_ctas, s)
-                 : launch<EPI_GRAD, 128, false>(P, num_ctas, s);
-  return has_t ? launch<EPI_GRAD, 256, true>(P, num_ctas, s)
-               : launch<EPI_GRAD, 256, false>(P, num_ctas, s);
+    return has_t ? launch<EPI_GRAD, 128, true, false>(P, num_sms, s)
+                 : launch<EPI_GRAD, 128, false, false>(P, num_sms, s);
+  return has_t ? launch<EPI_GRAD, 256, true, false>(P, num_sms, s)
+               : launch<EPI_GRAD, 256, false, false>(P, num_sms, s);
 }
 
-int launch_tc_gemm(const TcGemmArgs& a, int num_ctas, cudaStream_t s) {
+int launch_tc_gemm(const TcGemmArgs& a, int num_sms, cudaStream_t s) {
   TcParams P;
   memset(&P, 0, sizeof(P));
+  const bool pair = tc_use_pairs();
   constexpr int bn = 256;
+  const int b_box = pair ? bn / 2 : bn;
   if (!make_map(&P.ma[0], a.a0, a.M, a.K0, a.lda0, BM) ||
-      !make_map(&P.mb[0], a.b0, a.N, a.K0, a.ldb0, bn))
+      !make_map(&P.mb[0], a.b0, a.N, a.K0, a.ldb0, b_box))
     return fail_map();
   P.kb[0] = (int)((a.K0 + BK - 1) / BK);
   if (a.K1 > 0) {
     if (!make_map(&P.ma[1], a.a1, a.M, a.K1, a.lda1, BM) ||
-        !make_map(&P.mb[1], a.b1, a.N, a.K1, a.ldb1, bn))
+        !make_map(&P.mb[1], a.b1, a.N, a.K1, a.ldb1, b_box))
       return fail_map();
     P.kb[1] = (int)((a.K1 + BK - 1) / BK);
     P.seg_accum[1] = 1;  // both segments sum into the same accumulator
   }
-  P.m_tiles = (int)((a.M + BM - 1) / BM);
+  P.acc_stride = bn;
+  P.acc_stages = 2;
+  P.m_tiles = (int)((a.M + tc_tile_rows(pair) - 1) / tc_tile_rows(pair));
   P.n_tiles = (int)((a.N + bn - 1) / bn);
   P.n_splits = P.n_tiles;
   P.items = P.m_tiles * P.n_tiles;
   P.gemm = a;
-  return launch<EPI_GEMM, 256, false>(P, num_ctas, s);
+  return pair ? launch<EPI_GEMM, 256, false, true>(P, num_sms, s)
+              : launch<EPI_GEMM, 256, false, false>(P, num_sms, s);
 }
 
 }  // namespace kd
