@@ -185,6 +185,15 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* inputs, const float
                  void* d_logits_s, uint32_t* dev_status, void* workspace, size_t ws_bytes,
                  void* stream);
 
+/* Plan introspection: how kd_fwd / kd_bwd will run this problem on the current
+ * device.  path: 0 logits streaming, 1 fp32 CUDA cores, 2 tensor cores;
+ * vocab_splits: forward vocabulary splits; chunk_rows x chunk_cols: the
+ * backward gradient chunk (tokens x vocabulary columns) staged in the
+ * workspace, always smaller than the full tokens x vocab matrix.  Any output
+ * pointer may be NULL. */
+kd_status kd_plan_info(const kd_problem* problem, int32_t* path, int32_t* vocab_splits,
+                       int64_t* chunk_rows, int64_t* chunk_cols);
+
 /* Static description of a status code. */
 const char* kd_status_string(kd_status status);
 

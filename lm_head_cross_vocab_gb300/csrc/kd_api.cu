@@ -12,6 +12,7 @@
 #include "kd_internal.h"
 
 #include <atomic>
+#include <mutex>
 
 using namespace kd;
 
@@ -151,6 +152,10 @@ Consts make_consts(const kd_problem* p, bool has_labels, bool has_t) {
     else c.kl_mode = 1;  // skew-JS: forward sums give the accurate normaliser gap
   }
   c.precise = p->dtype == KD_FP32 ? 1 : 0;
+  // exact shortcuts for the T = 1 sums when the temperature is 1 or 2 (both sides)
+  const int pw_s = p->t_student == 1.f ? 1 : (p->t_student == 2.f ? 2 : 0);
+  const int pw_t = p->t_teacher == 1.f ? 1 : (p->t_teacher == 2.f ? 2 : 0);
+  c.pw = (!has_t || pw_s == pw_t) ? pw_s : 0;
   return c;
 }
 
@@ -269,16 +274,17 @@ kd_status make_plan(const kd_problem* p, bool has_labels, Plan& P) {
     P.b_ent = b.take(n * 4);
   }
   if (P.path == PATH_TC) {
-    choose_chunk(p, (int64_t)16 << 20, 256, P.R, P.C);
+    choose_chunk(p, (int64_t)64 << 20, 256, P.R, P.C);
     P.ldv = round_up(v, 8);
     P.ldn = round_up(n, 8);
     if (P.s_gemm) {
       P.b_wt = b.take(P.ds * P.ldv * 2);               // W_s^T
       P.b_hst = b.take(P.ds * P.ldn * 2);              // H_s^T
       if (P.tied) P.b_htt = b.take(P.ds * P.ldn * 2);  // H_t^T
-      P.b_g = b.take(P.R * P.C * 2);
-      P.b_gT = b.take(P.C * P.R * 2);
-      if (P.tied) P.b_gtT = b.take(P.C * P.R * 2);
+      // two gradient chunks: the producer fills one while the GEMMs read the other
+      P.b_g = b.take(2 * P.R * P.C * 2);
+      P.b_gT = b.take(2 * P.C * P.R * 2);
+      if (P.tied) P.b_gtT = b.take(2 * P.C * P.R * 2);
       if (cdiv(v, P.C) > 1) P.b_dh = b.take(n * P.ds * 4);
       if (cdiv(n, P.R) > 1) P.b_dw = b.take(v * P.ds * 4);
     }
@@ -297,6 +303,37 @@ T* at(void* ws, size_t off) {
 }
 
 kd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KD_OK : KD_ERR_CUDA; }
+
+// Per-device side stream and events of the backward's two-stream schedule
+// (created once per device, never freed: they live as long as the process).
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, ready[2] = {}, consumed[2] = {};
+};
+
+kd_status side_stream(SideStream** out) {
+  static SideStream per_dev[64];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KD_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  SideStream& ss = per_dev[dev];
+  if (!ss.stream) {
+    const unsigned f = cudaEventDisableTiming;
+    if (cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.fork, f) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.join, f) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.ready[0], f) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.ready[1], f) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.consumed[0], f) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.consumed[1], f) != cudaSuccess) {
+      ss.stream = nullptr;
+      return KD_ERR_CUDA;
+    }
+  }
+  *out = &ss;
+  return KD_OK;
+}
 
 }  // namespace
 
@@ -348,6 +385,20 @@ kd_status kd_workspace_size(const kd_problem* problem, size_t* fwd_bytes, size_t
   if (st != KD_OK) return st;
   if (fwd_bytes) *fwd_bytes = P.f_bytes;
   if (bwd_bytes) *bwd_bytes = P.b_bytes;
+  return KD_OK;
+}
+
+kd_status kd_plan_info(const kd_problem* problem, int32_t* path, int32_t* vocab_splits,
+                       int64_t* chunk_rows, int64_t* chunk_cols) {
+  kd_status st = check_problem(problem);
+  if (st != KD_OK) return st;
+  Plan P;
+  st = make_plan(problem, true, P);
+  if (st != KD_OK) return st;
+  if (path) *path = (int32_t)P.path;
+  if (vocab_splits) *vocab_splits = P.n_splits;
+  if (chunk_rows) *chunk_rows = P.R;
+  if (chunk_cols) *chunk_cols = P.C;
   return KD_OK;
 }
 
@@ -665,10 +716,29 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
       launch_transpose_bf16(static_cast<const __nv_bfloat16*>(in->h_t), n, D, D, htT, P.ldn, s);
   }
   prof_record(2, s);
+  // Two-stream schedule: gradient chunk k is produced on the caller's stream
+  // into buffer k%2 while the dH / dW GEMMs of chunk k-1 run on a side
+  // stream, so each launch's last partial wave overlaps the next launch.
+  SideStream* ss = nullptr;
+  cudaStream_t s2 = s;
+  if (!P.s_logits) {
+    if (side_stream(&ss) != KD_OK) return KD_ERR_CUDA;
+    s2 = ss->stream;
+    if (cudaEventRecord(ss->fork, s) != cudaSuccess ||
+        cudaStreamWaitEvent(s2, ss->fork, 0) != cudaSuccess)
+      return KD_ERR_CUDA;
+  }
+  int64_t k = 0;
   for (int64_t ri = 0; ri < nr; ++ri) {
     const int64_t r0 = ri * R, rc = std::min(R, n - r0);
-    for (int64_t ci = 0; ci < nc; ++ci) {
+    for (int64_t ci = 0; ci < nc; ++ci, ++k) {
       const int64_t c0 = ci * C, cc = std::min(C, v - c0);
+      const int buf = (int)(k & 1);
+      __nv_bfloat16* gk = g ? g + (size_t)buf * R * C : nullptr;
+      __nv_bfloat16* gTk = gT ? gT + (size_t)buf * R * C : nullptr;
+      __nv_bfloat16* gtTk = gtT ? gtT + (size_t)buf * R * C : nullptr;
+      if (ss && k >= 2 && cudaStreamWaitEvent(s, ss->consumed[buf], 0) != cudaSuccess)
+        return KD_ERR_CUDA;
       TcGradArgs a;
       memset(&a, 0, sizeof(a));
       a.h_s = in->h_s;
@@ -707,19 +777,22 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
         a.ldg = v;
         a.gT = nullptr;
       } else {
-        a.g = g;
+        a.g = gk;
         a.ldg = C;
-        a.gT = d_w_s ? gT : nullptr;
+        a.gT = d_w_s ? gTk : nullptr;
       }
       a.ldgt = R;
-      a.gtT = gtT;
+      a.gtT = gtTk;
       a.status = dev_status;
       if (launch_tc_grad(a, P.nsm, s) != 0) return KD_ERR_CUDA;
       if (P.s_logits) continue;
+      if (cudaEventRecord(ss->ready[buf], s) != cudaSuccess ||
+          cudaStreamWaitEvent(s2, ss->ready[buf], 0) != cudaSuccess)
+        return KD_ERR_CUDA;
       if (d_h_s) {  // dH[r0.., :] (+)= G[:, chunk] W[chunk, :]
         TcGemmArgs m;
         memset(&m, 0, sizeof(m));
-        m.a0 = g;
+        m.a0 = gk;
         m.lda0 = C;
         m.b0 = wT + c0;
         m.ldb0 = P.ldv;
@@ -737,20 +810,20 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
         }
         m.c16 = out;
         m.ldc16 = D;
-        if (launch_tc_gemm(m, P.nsm, s) != 0) return KD_ERR_CUDA;
+        if (launch_tc_gemm(m, P.nsm, s2) != 0) return KD_ERR_CUDA;
       }
       if (d_w_s) {  // dW[chunk, :] (+)= G[:, chunk]^T H[r0.., :] (+ G_t^T H_t)
         TcGemmArgs m;
         memset(&m, 0, sizeof(m));
-        m.a0 = gT;
+        m.a0 = gTk;
         m.lda0 = R;
         m.b0 = hsT + r0;
         m.ldb0 = P.ldn;
         m.M = cc;
         m.N = D;
         m.K0 = rc;
-        if (gtT) {
-          m.a1 = gtT;
+        if (gtTk) {
+          m.a1 = gtTk;
           m.lda1 = R;
           m.b1 = htT + r0;
           m.ldb1 = P.ldn;
@@ -767,10 +840,14 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
         }
         m.c16 = out;
         m.ldc16 = D;
-        if (launch_tc_gemm(m, P.nsm, s) != 0) return KD_ERR_CUDA;
+        if (launch_tc_gemm(m, P.nsm, s2) != 0) return KD_ERR_CUDA;
       }
+      if (cudaEventRecord(ss->consumed[buf], s2) != cudaSuccess) return KD_ERR_CUDA;
     }
   }
+  if (ss && (cudaEventRecord(ss->join, s2) != cudaSuccess ||
+             cudaStreamWaitEvent(s, ss->join, 0) != cudaSuccess))
+    return KD_ERR_CUDA;
   prof_record(3, s);
   return cuda_status(cudaGetLastError());
 }

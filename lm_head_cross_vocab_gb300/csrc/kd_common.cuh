@@ -67,6 +67,7 @@ struct Consts {
   int need_s1, need_t1;        // student / teacher CE needed (T = 1 sums)
   int kl_mode;                 // bit0: forward cross sums, bit1: reverse cross sums
   int precise;                 // fp32 problems: libm expm1/log1p in the skew-JS terms
+  int pw;                      // 1: T_s (= T_t) == 1, 2: T_s (= T_t) == 2, 0: otherwise
 };
 
 struct RowState {
@@ -147,6 +148,71 @@ __device__ __forceinline__ RowState shfl_xor(const RowState& s, int m) {
   return o;
 }
 
+// Sums of one chunk against fixed maxima (see update()).  PW: how the T = 1
+// sums follow from the tempered ones (0: own exponential, 1: equal, 2: square).
+template <int NC, bool HAS_T, bool MASKED, int PW>
+__device__ __forceinline__ void accum(const float* zs, const float* zt, int nvalid,
+                                      const Consts& c, float os1, float osT, float ot1, float otT,
+                                      float& ls1, float& lsT, float& lt1, float& ltT, float& qd,
+                                      float& qx, float& pd, float& px, float ms, float mt) {
+  if (!HAS_T) {
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+      if (!MASKED || j < nvalid) {
+        const float es = ex2(fmaf(zs[j], c.k_sT, osT));
+        lsT += es;
+        if (c.need_s1) {
+          if (PW == 2) ls1 = fmaf(es, es, ls1);
+          else if (PW == 1) ls1 += es;
+          else ls1 += ex2(fmaf(zs[j], c.k_s1, os1));
+        }
+      }
+    }
+    return;
+  }
+  // e^{a_s-Mt} = e^{a_s-Ms} * cq and e^{a_t-Ms} = e^{a_t-Mt} * cp
+  const float dM = (ms * c.inv_ts - mt * c.inv_tt) * kL2E;
+  const float cq = ex2(dM), cp = ex2(-dM);
+  const bool fwd = c.kl_mode & 1, rev = c.kl_mode & 2;
+#pragma unroll
+  for (int j = 0; j < NC; ++j) {
+    if (!MASKED || j < nvalid) {
+      const float es = ex2(fmaf(zs[j], c.k_sT, osT));
+      const float et = ex2(fmaf(zt[j], c.k_tT, otT));
+      lsT += es;
+      ltT += et;
+      const float d = zt[j] * c.inv_tt - zs[j] * c.inv_ts;
+      if (fwd) {
+        qd = fmaf(et, d, qd);
+        qx += fmaf(es, cq, -et);
+      }
+      if (rev) {
+        pd = fmaf(es, -d, pd);
+        px += fmaf(et, cp, -es);
+      }
+      if (PW == 2) {
+        if (c.need_s1) ls1 = fmaf(es, es, ls1);
+        if (c.need_t1) lt1 = fmaf(et, et, lt1);
+      } else if (PW == 1) {
+        if (c.need_s1) ls1 += es;
+        if (c.need_t1) lt1 += et;
+      }
+    }
+  }
+  if (PW == 0) {
+    if (c.need_s1) {
+#pragma unroll
+      for (int j = 0; j < NC; ++j)
+        if (!MASKED || j < nvalid) ls1 += ex2(fmaf(zs[j], c.k_s1, os1));
+    }
+    if (c.need_t1) {
+#pragma unroll
+      for (int j = 0; j < NC; ++j)
+        if (!MASKED || j < nvalid) lt1 += ex2(fmaf(zt[j], c.k_t1, ot1));
+    }
+  }
+}
+
 // Chunk update of the online state with NC columns of student (and, when
 // HAS_T, teacher) logits.  With MASKED, only the first `nvalid` columns count
 // (the ragged end of the vocabulary).
@@ -184,47 +250,17 @@ __device__ __forceinline__ void update(RowState& st, const float* zs, const floa
   const float os1 = -ms * c.k_s1, osT = -ms * c.k_sT;
   const float ot1 = -mt * c.k_t1, otT = -mt * c.k_tT;
   float ls1 = 0.f, lsT = 0.f, lt1 = 0.f, ltT = 0.f, qd = 0.f, qx = 0.f, pd = 0.f, px = 0.f;
-  if (!HAS_T) {
-#pragma unroll
-    for (int j = 0; j < NC; ++j) {
-      if (!MASKED || j < nvalid) {
-        lsT += ex2(fmaf(zs[j], c.k_sT, osT));
-        if (c.need_s1) ls1 += ex2(fmaf(zs[j], c.k_s1, os1));
-      }
-    }
+  // T = 1 sums (for CE): with T = 1 they are the tempered sums; with T = 2,
+  // e^{z-m} = (e^{(z-m)/2})^2 exactly, so neither needs its own exponential.
+  if (c.pw == 2) {
+    accum<NC, HAS_T, MASKED, 2>(zs, zt, nvalid, c, os1, osT, ot1, otT, ls1, lsT, lt1, ltT, qd,
+                                qx, pd, px, ms, mt);
+  } else if (c.pw == 1) {
+    accum<NC, HAS_T, MASKED, 1>(zs, zt, nvalid, c, os1, osT, ot1, otT, ls1, lsT, lt1, ltT, qd,
+                                qx, pd, px, ms, mt);
   } else {
-    // e^{a_s-Mt} = e^{a_s-Ms} * cq and e^{a_t-Ms} = e^{a_t-Mt} * cp
-    const float dM = (ms * c.inv_ts - mt * c.inv_tt) * kL2E;
-    const float cq = ex2(dM), cp = ex2(-dM);
-    const bool fwd = c.kl_mode & 1, rev = c.kl_mode & 2;
-#pragma unroll
-    for (int j = 0; j < NC; ++j) {
-      if (!MASKED || j < nvalid) {
-        const float es = ex2(fmaf(zs[j], c.k_sT, osT));
-        const float et = ex2(fmaf(zt[j], c.k_tT, otT));
-        lsT += es;
-        ltT += et;
-        const float d = zt[j] * c.inv_tt - zs[j] * c.inv_ts;
-        if (fwd) {
-          qd = fmaf(et, d, qd);
-          qx += fmaf(es, cq, -et);
-        }
-        if (rev) {
-          pd = fmaf(es, -d, pd);
-          px += fmaf(et, cp, -es);
-        }
-      }
-    }
-    if (c.need_s1) {
-#pragma unroll
-      for (int j = 0; j < NC; ++j)
-        if (!MASKED || j < nvalid) ls1 += ex2(fmaf(zs[j], c.k_s1, os1));
-    }
-    if (c.need_t1) {
-#pragma unroll
-      for (int j = 0; j < NC; ++j)
-        if (!MASKED || j < nvalid) lt1 += ex2(fmaf(zt[j], c.k_t1, ot1));
-    }
+    accum<NC, HAS_T, MASKED, 0>(zs, zt, nvalid, c, os1, osT, ot1, otT, ls1, lsT, lt1, ltT, qd,
+                                qx, pd, px, ms, mt);
   }
   st.ls1 += ls1;
   st.lsT += lsT;
@@ -330,6 +366,28 @@ __device__ __forceinline__ float kl_grad(float zs, float zt, const float* stt, i
   if (variant != KD_KL_REVERSE) g = p - ex2(lq * kL2E);
   if (variant != KD_KL_FORWARD) g = fmaf(p, lp - lq - stt[S_KL_REV], g);
   return g;
+}
+
+// Same gradient from already computed lp = log p, lq = log q, p = e^lp, q = e^lq.
+__device__ __forceinline__ float kl_grad_pq(float zs, float zt, float lp, float lq, float p,
+                                            float q, const float* stt, int variant,
+                                            const Consts& c) {
+  if (variant == KD_KL_SKEW_JS) {
+    const float x = fmaf(zs, c.inv_ts, -zt * c.inv_tt) + stt[S_DLSE];
+    return c.beta * p * (x - js_w(x, c) - stt[S_KL_PM]);
+  }
+  float g = 0.f;
+  if (variant != KD_KL_REVERSE) g = p - q;
+  if (variant != KD_KL_FORWARD) g = fmaf(p, lp - lq - stt[S_KL_REV], g);
+  return g;
+}
+
+// softmax(z) = e^{z - lse(z)} from p = e^{z/T - lse(z/T)} when T is 1 or 2
+// (pw as in Consts; sq = e^{2 lse(z/2) - lse(z)} per row), else directly.
+__device__ __forceinline__ float softmax_t1(float z, float p, float lse1, float sq, int pw) {
+  if (pw == 2) return p * p * sq;
+  if (pw == 1) return p;
+  return ex2((z - lse1) * kL2E);
 }
 
 __device__ __forceinline__ void set_status(uint32_t* st, uint32_t bits) {

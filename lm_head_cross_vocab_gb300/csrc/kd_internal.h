@@ -118,7 +118,8 @@ void launch_simt_gemm(const float* A, int64_t sam, int64_t sak, const float* B, 
 // ------------------------------------------------------------ tcgen05 path
 int tc_num_sms();
 bool tc_use_pairs();                                  // CTA-pair (cta_group::2) tiles
-int tc_fused_tile_cols(bool two_sides, bool pair);    // vocabulary columns per tile
+int tc_fused_tile_cols(bool two_sides, bool pair);    // vocabulary columns per tile (forward)
+int tc_grad_tile_cols(bool two_sides, bool pair);     // ... of the gradient producer
 int tc_tile_rows(bool pair);                          // token rows per tile (MMA M)
 struct TcFwdArgs {
   const void *h_s, *w_s, *h_t, *w_t, *zs_logits, *zt_logits;

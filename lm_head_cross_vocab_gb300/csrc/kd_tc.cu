@@ -261,7 +261,7 @@ struct Cfg {
   static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TX_BYTES = PAIR ? 2 * STAGE_BYTES : STAGE_BYTES;  // per full barrier
-  static constexpr int STAGES = (STAGE_BYTES <= 32768) ? 6 : 4;
+  static constexpr int STAGES = (STAGE_BYTES <= 32768) ? 7 : 4;
   static constexpr int TILE_BYTES = STAGES * STAGE_BYTES;
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM_BYTES = TILE_BYTES + BAR_BYTES + 1024;  // + alignment slack
@@ -640,9 +640,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
           const int32_t* ids = nullptr;
           const float* ps = nullptr;
           int kp = 0;
+          float sv[KD_STATS_PER_TOKEN] = {};  // this row's saved statistics
           if (row_ok) {
             scale = a.row_scale[row];
             stt = a.stats + row * KD_STATS_PER_TOKEN;
+#pragma unroll
+            for (int i = 0; i < KD_STATS_PER_TOKEN; ++i) sv[i] = stt[i];
             if (a.labels) y = a.labels[row];
             if (a.topk) {
               ids = a.sidx + row * a.k;
@@ -678,20 +681,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
                               col0, nv, P.logits_vec, vt);
               float g[32], gt[32];
               const bool want_gt = a.gtT != nullptr;
+              const int pw = a.c.pw;
+              // e^{2 lse(z/2) - lse(z)}: turns p^2 into softmax(z) when T = 2
+              const float sq_s = pw == 2 ? ex2((2.f * sv[S_LSE_ST] - sv[S_LSE_S1]) * kL2E) : 0.f;
+              const float sq_t = pw == 2 ? ex2((2.f * sv[S_LSE_TT] - sv[S_LSE_T1]) * kL2E) : 0.f;
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
                 float gg = 0.f, gtt = 0.f;
                 if (scale != 0.f) {
-                  if (HAS_T) gg = a.w_kl_ts * kl_grad(vs[j], vt[j], stt, a.variant, a.c);
-                  else if (a.topk)
-                    gg = a.w_kl_ts * stt[S_MASS] *
-                         ex2((vs[j] * a.c.inv_ts - stt[S_LSE_ST]) * kL2E);
+                  const float lp = fmaf(vs[j], a.c.inv_ts, -sv[S_LSE_ST]);
+                  const float p = ex2(lp * kL2E);
+                  float q = 0.f;
+                  if (HAS_T) {
+                    const float lq = fmaf(vt[j], a.c.inv_tt, -sv[S_LSE_TT]);
+                    q = ex2(lq * kL2E);
+                    gg = a.w_kl_ts * kl_grad_pq(vs[j], vt[j], lp, lq, p, q, sv, a.variant, a.c);
+                  } else if (a.topk) {
+                    gg = a.w_kl_ts * sv[S_MASS] * p;
+                  }
                   const float ey = (col0 + j == y) ? 1.f : 0.f;
                   if (a.w_sce != 0.f)
-                    gg = fmaf(a.w_sce, ex2((vs[j] - stt[S_LSE_S1]) * kL2E) - ey, gg);
+                    gg = fmaf(a.w_sce, softmax_t1(vs[j], p, sv[S_LSE_S1], sq_s, pw) - ey, gg);
                   gg *= scale;
                   if (HAS_T && want_gt)
-                    gtt = scale * a.w_tce * (ex2((vt[j] - stt[S_LSE_T1]) * kL2E) - ey);
+                    gtt = scale * a.w_tce * (softmax_t1(vt[j], q, sv[S_LSE_T1], sq_t, pw) - ey);
                 }
                 g[j] = gg;
                 gt[j] = gtt;
@@ -964,6 +977,16 @@ bool tc_use_pairs() {
 // columns (single CTA: 128 per side, double buffered; pairs: 256 per side,
 // one stage); one side always gets 256 columns, double buffered.
 int tc_fused_tile_cols(bool two_sides, bool pair) { return (two_sides && !pair) ? 128 : 256; }
+
+// Gradient-producer tile columns.  Two GEMM sides on CTA pairs take 256
+// columns per side (one TMEM stage, full-rate MMAs); the partial last wave of
+// each chunk is covered by the next launch on the backward's second stream.
+// KD_TC_GRAD_COLS=128 selects 128 columns per side with two TMEM stages.
+int tc_grad_tile_cols(bool two_sides, bool pair) {
+  if (!(two_sides && pair)) return tc_fused_tile_cols(two_sides, pair);
+  const char* e = getenv("KD_TC_GRAD_COLS");
+  return (e && e[0] == '1') ? 128 : 256;
+}
 int tc_tile_rows(bool pair) { return pair ? 2 * BM : BM; }
 
 int launch_tc_fwd(const TcFwdArgs& a, int num_sms, cudaStream_t s) {
@@ -994,7 +1017,7 @@ int launch_tc_grad(const TcGradArgs& a, int num_sms, cudaStream_t s) {
   memset(&P, 0, sizeof(P));
   const bool pair = tc_use_pairs();
   const bool two = a.s_gemm && a.t_gemm;
-  const int bn = tc_fused_tile_cols(two, pair);
+  const int bn = tc_grad_tile_cols(two, pair);
   if (!setup_segments(P, a, bn, pair ? bn / 2 : bn, tc_tile_rows(pair), a.r0, a.rc, a.c0, a.cc))
     return fail_map();
   P.n_splits = P.n_tiles;  // one tile per item
@@ -1002,6 +1025,7 @@ int launch_tc_grad(const TcGradArgs& a, int num_sms, cudaStream_t s) {
   P.logits_vec = logits_vec_ok(a.zs_logits, a.vocab) && logits_vec_ok(a.zt_logits, a.vocab);
   P.grad = a;
   const bool has_t = a.t_gemm || a.t_logits;
+  if (pair && bn == 128) return launch<EPI_GRAD, 128, true, true>(P, num_sms, s);
   if (pair)
     return has_t ? launch<EPI_GRAD, 256, true, true>(P, num_sms, s)
                  : launch<EPI_GRAD, 256, false, true>(P, num_sms, s);

@@ -95,10 +95,13 @@ def load_library(path: str = LIB_PATH):
     lib.kd_diag_gemm_bf16.argtypes = [vp, vp, vp, ctypes.c_int64, ctypes.c_int64,
                                       ctypes.c_int64, vp]
     lib.kd_set_profile_events.argtypes = [vp, vp, vp, vp]
+    lib.kd_plan_info.argtypes = [P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                                 ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]
     lib.kd_fwd_static_scratch.argtypes = [P, I, vp, vp, vp, vp, vp, vp, vp]
     lib.kd_launch_count.restype = ctypes.c_uint64
     for f in ("kd_workspace_size", "kd_fwd", "kd_bwd", "kd_device_supported", "kd_abi_version",
-              "kd_diag_gemm_bf16", "kd_set_profile_events", "kd_fwd_static_scratch"):
+              "kd_diag_gemm_bf16", "kd_set_profile_events", "kd_fwd_static_scratch",
+              "kd_plan_info"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -162,6 +165,17 @@ def kd_set_profile_events(fwd_start=None, fwd_stop=None, bwd_start=None, bwd_sto
     st = load_library().kd_set_profile_events(*h)
     if st != KD_OK:
         raise KDError(st, "kd_set_profile_events")
+
+
+def kd_plan_info(problem: kd_problem) -> dict:
+    path, splits = ctypes.c_int32(0), ctypes.c_int32(0)
+    rows, cols = ctypes.c_int64(0), ctypes.c_int64(0)
+    st = load_library().kd_plan_info(ctypes.byref(problem), ctypes.byref(path), ctypes.byref(splits),
+                                     ctypes.byref(rows), ctypes.byref(cols))
+    if st != KD_OK:
+        raise KDError(st, "kd_plan_info")
+    return {"path": path.value, "vocab_splits": splits.value, "chunk_rows": rows.value,
+            "chunk_cols": cols.value}
 
 
 def kd_launch_count() -> int:
