@@ -463,6 +463,7 @@ kd_status kd_fwd(const kd_problem* problem, const kd_inputs* in, float* ce_s, fl
     a.ce_t = w_ce_t;
     a.kl = w_kl;
     a.stats = w_stats;
+    a.status = dev_status;
     prof_record(0, s);
     launch_stream_fwd(a, s);
     prof_record(1, s);
@@ -633,6 +634,7 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
     a.w_sce = p->w_student_ce;
     a.w_kl_ts = w_kl_ts;
     a.dz = d_logits_s;
+    a.status = dev_status;
     prof_record(2, s);
     launch_stream_bwd(a, s);
     prof_record(3, s);

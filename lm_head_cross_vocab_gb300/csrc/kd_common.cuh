@@ -72,10 +72,12 @@ struct Consts {
 
 struct RowState {
   float ms, ls1, lsT, mt, lt1, ltT, qd, qx, pd, px, zys, zyt, tk, jq, jp;
+  float cq, cp;  // cached e^{Ms-Mt}, e^{Mt-Ms} for the current maxima (< 0: stale)
 
   __device__ __forceinline__ void init() {
     ms = mt = neg_inf();
     ls1 = lsT = lt1 = ltT = qd = qx = pd = px = zys = zyt = tk = jq = jp = 0.f;
+    cq = cp = -1.f;
   }
   __device__ __forceinline__ void store(float* r) const {
     float4* o = reinterpret_cast<float4*>(r);
@@ -91,6 +93,7 @@ struct RowState {
     lt1 = b.x; ltT = b.y; qd = b.z; qx = b.w;
     pd = c.x; px = c.y; zys = c.z; zyt = c.w;
     tk = d.x; jq = d.y; jp = d.z;
+    cq = cp = -1.f;
   }
 };
 
@@ -126,6 +129,7 @@ __device__ __forceinline__ void merge(RowState& a, const RowState& b, const Cons
   a.tk += b.tk;
   a.jq += b.jq;
   a.jp += b.jp;
+  a.cq = a.cp = -1.f;
 }
 
 __device__ __forceinline__ RowState shfl_xor(const RowState& s, int m) {
@@ -145,6 +149,7 @@ __device__ __forceinline__ RowState shfl_xor(const RowState& s, int m) {
   o.tk = __shfl_xor_sync(0xffffffffu, s.tk, m);
   o.jq = __shfl_xor_sync(0xffffffffu, s.jq, m);
   o.jp = __shfl_xor_sync(0xffffffffu, s.jp, m);
+  o.cq = o.cp = -1.f;
   return o;
 }
 
@@ -154,7 +159,7 @@ template <int NC, bool HAS_T, bool MASKED, int PW>
 __device__ __forceinline__ void accum(const float* zs, const float* zt, int nvalid,
                                       const Consts& c, float os1, float osT, float ot1, float otT,
                                       float& ls1, float& lsT, float& lt1, float& ltT, float& qd,
-                                      float& qx, float& pd, float& px, float ms, float mt) {
+                                      float& qx, float& pd, float& px, float cq, float cp) {
   if (!HAS_T) {
 #pragma unroll
     for (int j = 0; j < NC; ++j) {
@@ -171,8 +176,6 @@ __device__ __forceinline__ void accum(const float* zs, const float* zt, int nval
     return;
   }
   // e^{a_s-Mt} = e^{a_s-Ms} * cq and e^{a_t-Ms} = e^{a_t-Mt} * cp
-  const float dM = (ms * c.inv_ts - mt * c.inv_tt) * kL2E;
-  const float cq = ex2(dM), cp = ex2(-dM);
   const bool fwd = c.kl_mode & 1, rev = c.kl_mode & 2;
 #pragma unroll
   for (int j = 0; j < NC; ++j) {
@@ -228,25 +231,34 @@ __device__ __forceinline__ void update(RowState& st, const float* zs, const floa
     }
   }
   if (MASKED && nvalid <= 0) return;
-  const float ms = fmaxf(st.ms, cms);
-  {
-    const float f1 = rescale(st.ms, ms, c.k_s1), fT = rescale(st.ms, ms, c.k_sT);
+  // rescale the running sums only when a maximum grows (rare after the
+  // first chunks of a row)
+  bool grew = false;
+  if (cms > st.ms) {
+    const float f1 = ex2((st.ms - cms) * c.k_s1), fT = ex2((st.ms - cms) * c.k_sT);
     st.ls1 *= f1;
     st.lsT *= fT;
     st.pd *= fT;
     st.px *= fT;
-    st.ms = ms;
+    st.ms = cms;
+    grew = true;
   }
-  float mt = 0.f;
-  if (HAS_T) {
-    mt = fmaxf(st.mt, cmt);
-    const float f1 = rescale(st.mt, mt, c.k_t1), fT = rescale(st.mt, mt, c.k_tT);
+  if (HAS_T && cmt > st.mt) {
+    const float f1 = ex2((st.mt - cmt) * c.k_t1), fT = ex2((st.mt - cmt) * c.k_tT);
     st.lt1 *= f1;
     st.ltT *= fT;
     st.qd *= fT;
     st.qx *= fT;
-    st.mt = mt;
+    st.mt = cmt;
+    grew = true;
   }
+  const float ms = st.ms, mt = HAS_T ? st.mt : 0.f;
+  if (HAS_T && (grew || st.cq < 0.f)) {
+    const float dM = (ms * c.inv_ts - mt * c.inv_tt) * kL2E;
+    st.cq = ex2(dM);
+    st.cp = ex2(-dM);
+  }
+  const float cq = st.cq, cp = st.cp;
   const float os1 = -ms * c.k_s1, osT = -ms * c.k_sT;
   const float ot1 = -mt * c.k_t1, otT = -mt * c.k_tT;
   float ls1 = 0.f, lsT = 0.f, lt1 = 0.f, ltT = 0.f, qd = 0.f, qx = 0.f, pd = 0.f, px = 0.f;
@@ -254,13 +266,13 @@ __device__ __forceinline__ void update(RowState& st, const float* zs, const floa
   // e^{z-m} = (e^{(z-m)/2})^2 exactly, so neither needs its own exponential.
   if (c.pw == 2) {
     accum<NC, HAS_T, MASKED, 2>(zs, zt, nvalid, c, os1, osT, ot1, otT, ls1, lsT, lt1, ltT, qd,
-                                qx, pd, px, ms, mt);
+                                qx, pd, px, cq, cp);
   } else if (c.pw == 1) {
     accum<NC, HAS_T, MASKED, 1>(zs, zt, nvalid, c, os1, osT, ot1, otT, ls1, lsT, lt1, ltT, qd,
-                                qx, pd, px, ms, mt);
+                                qx, pd, px, cq, cp);
   } else {
     accum<NC, HAS_T, MASKED, 0>(zs, zt, nvalid, c, os1, osT, ot1, otT, ls1, lsT, lt1, ltT, qd,
-                                qx, pd, px, ms, mt);
+                                qx, pd, px, cq, cp);
   }
   st.ls1 += ls1;
   st.lsT += lsT;

@@ -80,9 +80,14 @@ struct StreamArgs {
   const float* row_scale;
   float w_sce, w_kl_ts;  // w_sce, w_kl * T_s
   void* dz;              // [n, vocab] gradient of the student logits
+  uint32_t* status;      // device status word (bounded-wait timeouts)
 };
 void launch_stream_fwd(const StreamArgs& a, cudaStream_t s);
 void launch_stream_bwd(const StreamArgs& a, cudaStream_t s);
+// Packed bf16 ring kernels for T = 1 / T = 2 (16-byte aligned rows); return
+// false, launching nothing, when the problem needs the generic kernels.
+bool launch_stream_fwd_packed(const StreamArgs& a, cudaStream_t s);
+bool launch_stream_bwd_packed(const StreamArgs& a, cudaStream_t s);
 
 // ------------------------------------------------------------- fp32 SIMT path
 struct SimtArgs {

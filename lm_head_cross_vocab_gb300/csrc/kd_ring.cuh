@@ -1,0 +1,353 @@
+// TMA-staged streaming of materialised logit rows (kd_stream.cu and
+// kd_stream_bf16.cu).
+//
+// One persistent CTA per SM.  A producer warp copies each token row in
+// kChunk-byte pieces (z_s and, with a teacher, z_t) into a kStages-deep
+// shared-memory ring with 1-D bulk copies (cp.async.bulk, completion counted
+// on an mbarrier); kCW consumer warps read the ring, each thread owning 16
+// bytes of every piece, and release each stage as soon as their registers hold
+// it, so memory traffic never waits on the arithmetic.  The per-chunk work is a
+// policy: an accumulator (forward online softmax) or a gradient writer
+// (backward), in a generic form (any dtype and temperature) or a packed bf16
+// form.  Every wait is bounded (see kd_ptx.cuh); after a timeout the kernel
+// drains its own copies and returns with KD_DEV_TIMEOUT set.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "kd_internal.h"
+#include "kd_ptx.cuh"
+
+namespace kd {
+namespace ring {
+
+constexpr int kCW = 16;                // consumer warps
+constexpr int kCT = 32 * kCW;          // consumer threads
+constexpr int kThreads = kCT + 32;     // + one producer warp
+constexpr int kChunk = 8192;           // bytes of one tensor per stage
+constexpr int kStages = 12;
+constexpr int kRingBytes = kStages * 2 * kChunk;
+constexpr int kSmem = kRingBytes + 1024 + 128 + kCW * kRec * 4 + 64;
+
+template <typename T>
+__device__ __forceinline__ float ld1(const T* p) {
+  return static_cast<float>(*p);
+}
+template <>
+__device__ __forceinline__ float ld1<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat162float(*p);
+}
+template <typename T>
+__device__ __forceinline__ void st1(T* p, float v) {
+  *p = static_cast<T>(v);
+}
+template <>
+__device__ __forceinline__ void st1<__nv_bfloat16>(__nv_bfloat16* p, float v) {
+  *p = __float2bfloat16(v);
+}
+
+struct Ring {
+  uint8_t* base;         // [stage][tensor][kChunk]
+  uint32_t full, empty;  // mbarrier arrays (8 bytes each)
+  volatile int* abort;
+  float* red;            // [kCW][kRec] reduction slots
+  float* bcast;          // small broadcast area
+};
+
+__device__ __forceinline__ Ring make_ring(uint8_t* smem) {
+  Ring r;
+  const uint32_t raw = ptx::smem_u32(smem);
+  const uint32_t pad = ((raw + 127u) & ~127u) - raw;
+  r.base = smem + pad;
+  uint8_t* tail = r.base + kRingBytes;
+  r.full = ptx::smem_u32(tail);
+  r.empty = r.full + 8 * kStages;
+  r.abort = reinterpret_cast<volatile int*>(tail + 16 * kStages);
+  r.red = reinterpret_cast<float*>(tail + 16 * kStages + 64);
+  r.bcast = r.red + kCW * kRec;
+  return r;
+}
+
+__device__ __forceinline__ void ring_init(const Ring& R) {
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      ptx::mbar_init(R.full + 8 * i, 1);
+      ptx::mbar_init(R.empty + 8 * i, kCW);  // one arrival per consumer warp
+    }
+    *R.abort = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+}
+
+// Producer: stream `passes` sweeps of every row this CTA owns (rows
+// blockIdx.x, +gridDim.x, ...) in kChunk pieces into the ring.  Rows are
+// 16-byte aligned and the vocabulary a multiple of 16 bytes (the dispatch
+// checks both), so every copy has a 16-byte aligned source, destination and
+// size.
+template <typename T>
+__device__ void producer(const Ring& R, const StreamArgs& a, bool has_t, int passes,
+                         uint32_t* status) {
+  constexpr int EPC = kChunk / (int)sizeof(T);
+  const int64_t V = a.vocab, nch = (V + EPC - 1) / EPC;
+  const int lane = threadIdx.x & 31;
+  int stage = 0;
+  uint32_t phase = 0, issued = 0, par = 0;
+  bool ok = true;
+  for (int64_t row = blockIdx.x; ok && row < a.n; row += gridDim.x) {
+    const T* zs = static_cast<const T*>(a.zs) + row * V;
+    const T* zt = has_t ? static_cast<const T*>(a.zt) + row * V : nullptr;
+    for (int pass = 0; ok && pass < passes; ++pass)
+      for (int64_t ch = 0; ch < nch; ++ch) {
+        if (!ptx::warp_wait(R.empty + 8 * stage, phase ^ 1, R.abort, status)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const int64_t e0 = ch * EPC;
+          const uint32_t bytes = (uint32_t)((V - e0 < EPC ? V - e0 : EPC) * (int64_t)sizeof(T));
+          const uint32_t fb = R.full + 8 * stage;
+          ptx::mbar_expect_tx(fb, has_t ? 2 * bytes : bytes);
+          uint8_t* dst = R.base + (size_t)stage * 2 * kChunk;
+          ptx::bulk_load(ptx::smem_u32(dst), zs + e0, bytes, fb);
+          if (has_t) ptx::bulk_load(ptx::smem_u32(dst + kChunk), zt + e0, bytes, fb);
+        }
+        __syncwarp();
+        issued |= 1u << stage;
+        par = (par & ~(1u << stage)) | (phase << stage);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+  }
+  if (!ok)  // let our own copies land before the CTA exits
+    for (int st = 0; st < kStages; ++st)
+      if (issued & (1u << st))
+        ptx::warp_wait(R.full + 8 * st, (par >> st) & 1u, R.abort, status, false);
+}
+
+// Consumer side of one ring slot.
+struct Cursor {
+  int stage = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ const uint8_t* acquire(const Ring& R, uint32_t* status) {
+    ptx::warp_wait(R.full + 8 * stage, phase, R.abort, status);
+    return R.base + (size_t)stage * 2 * kChunk;
+  }
+  __device__ __forceinline__ void release(const Ring& R) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(R.empty + 8 * stage);
+    if (++stage == kStages) {
+      stage = 0;
+      phase ^= 1;
+    }
+  }
+};
+
+// Merge the consumers' states into consumer thread 0 (all consumers call).
+__device__ __forceinline__ void consumer_merge(RowState& st, const Consts& c, const Ring& R) {
+  for (int o = 16; o > 0; o >>= 1) merge(st, shfl_xor(st, o), c);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) st.store(R.red + w * kRec);
+  ptx::named_sync(1, kCT);
+  if (w == 0) {
+    if (l < kCW) st.load(R.red + l * kRec);
+    else st.init();
+    for (int o = 16; o > 0; o >>= 1) merge(st, shfl_xor(st, o), c);
+  }
+  ptx::named_sync(1, kCT);
+}
+
+__device__ __forceinline__ float2 consumer_sum2(float x, float y, const Ring& R) {
+  for (int o = 16; o > 0; o >>= 1) {
+    x += __shfl_xor_sync(0xffffffffu, x, o);
+    y += __shfl_xor_sync(0xffffffffu, y, o);
+  }
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) {
+    R.red[2 * w] = x;
+    R.red[2 * w + 1] = y;
+  }
+  ptx::named_sync(1, kCT);
+  float2 r = make_float2(0.f, 0.f);
+  if (threadIdx.x == 0)
+    for (int i = 0; i < kCW; ++i) {
+      r.x += R.red[2 * i];
+      r.y += R.red[2 * i + 1];
+    }
+  ptx::named_sync(1, kCT);
+  return r;
+}
+
+// 16 bytes of one staged tensor as floats.
+template <typename T>
+struct Chunk;
+template <>
+struct Chunk<__nv_bfloat16> {
+  static constexpr int EPT = 8;
+  __device__ static void load(const uint8_t* p, int ct, float* v) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p + ct * 16);
+    v[0] = bf16lo(u.x); v[1] = bf16hi(u.x); v[2] = bf16lo(u.y); v[3] = bf16hi(u.y);
+    v[4] = bf16lo(u.z); v[5] = bf16hi(u.z); v[6] = bf16lo(u.w); v[7] = bf16hi(u.w);
+  }
+  __device__ static void store(__nv_bfloat16* dst, const float* g) {
+    uint4 u;
+    u.x = pack_bf16(g[0], g[1]);
+    u.y = pack_bf16(g[2], g[3]);
+    u.z = pack_bf16(g[4], g[5]);
+    u.w = pack_bf16(g[6], g[7]);
+    *reinterpret_cast<uint4*>(dst) = u;
+  }
+};
+template <>
+struct Chunk<float> {
+  static constexpr int EPT = 4;
+  __device__ static void load(const uint8_t* p, int ct, float* v) {
+    const float4 f = *reinterpret_cast<const float4*>(p + ct * 16);
+    v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+  }
+  __device__ static void store(float* dst, const float* g) {
+    *reinterpret_cast<float4*>(dst) = make_float4(g[0], g[1], g[2], g[3]);
+  }
+};
+
+// Forward.  Acc: init(); static load(Frag&, buf, ct); step(const Frag&, nv, c);
+// RowState fold().
+template <typename T, bool HAS_T, class Acc>
+__global__ void __launch_bounds__(kThreads, 1) k_fwd(StreamArgs a, uint32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  const Ring R = make_ring(smem_raw);
+  ring_init(R);
+  const int passes = (HAS_T && a.variant == KD_KL_SKEW_JS) ? 2 : 1;
+  if ((threadIdx.x >> 5) == kCW) {
+    producer<T>(R, a, HAS_T, passes, status);
+  } else {
+    constexpr int EPT = 16 / (int)sizeof(T);
+    constexpr int EPC = kChunk / (int)sizeof(T);
+    const Consts c = a.c;
+    const int64_t V = a.vocab, nch = (V + EPC - 1) / EPC;
+    const int ct = threadIdx.x;
+    Cursor cur;
+    for (int64_t row = blockIdx.x; row < a.n; row += gridDim.x) {
+      Acc acc;
+      acc.init();
+      for (int64_t ch = 0; ch < nch; ++ch) {
+        const uint8_t* buf = cur.acquire(R, status);
+        const int64_t e0 = ch * EPC + (int64_t)ct * EPT;
+        const int nv = valid_cols(V - e0, EPT);
+        typename Acc::Frag f;
+        if (nv > 0) Acc::load(f, buf, ct);
+        cur.release(R);
+        if (nv > 0) acc.step(f, nv, c);
+      }
+      RowState st = acc.fold();
+      const T* zs = static_cast<const T*>(a.zs) + row * V;
+      const T* zt = HAS_T ? static_cast<const T*>(a.zt) + row * V : nullptr;
+      if (a.topk) {  // sparse cross term sum_S p a_s (ids validated by the prep kernel)
+        const int32_t* ids = a.sidx + row * a.k;
+        const float* ps = a.sp + row * a.k;
+        for (int j = ct; j < a.k; j += kCT) {
+          const int32_t id = ids[j];
+          if (id >= 0 && (int64_t)id < V) st.tk = fmaf(ps[j], ld1<T>(zs + id) * c.inv_ts, st.tk);
+        }
+      }
+      consumer_merge(st, c, R);
+      if (ct == 0) {
+        bool valid = true, bad = false;
+        if (a.labels) {
+          const int64_t y = a.labels[row];
+          valid = y != a.ignore;
+          bad = valid && (y < 0 || y >= V);
+          if (valid && !bad) {
+            st.zys = ld1<T>(zs + y);
+            if (HAS_T) st.zyt = ld1<T>(zt + y);
+          }
+        }
+        const float mass = a.topk ? a.mass[row] : 0.f, ent = a.topk ? a.ent[row] : 0.f;
+        const RowOut o = finalize(st, c, a.variant, HAS_T, a.topk, mass, ent);
+        const float nan = __int_as_float(0x7fc00000);
+        if (a.ce_s) a.ce_s[row] = !valid ? 0.f : (bad ? nan : o.ce_s);
+        if (a.ce_t) a.ce_t[row] = !valid ? 0.f : (bad ? nan : o.ce_t);
+        if (a.kl && passes == 1) a.kl[row] = valid ? o.kl : 0.f;
+        float4* s4 = reinterpret_cast<float4*>(a.stats + row * KD_STATS_PER_TOKEN);
+        s4[0] = make_float4(o.lse_s1, o.lse_sT, o.lse_t1, o.lse_tT);
+        s4[1] = make_float4(o.kl_rev, 0.f, mass, o.dlse);
+        R.bcast[0] = o.dlse;
+        R.bcast[1] = o.lse_tT;
+      }
+      if (passes == 2) {  // skew-JS: second sweep once both normalisers are known
+        ptx::named_sync(1, kCT);
+        const float dlse = R.bcast[0], lse_tT = R.bcast[1];
+        float jq = 0.f, jp = 0.f;
+        for (int64_t ch = 0; ch < nch; ++ch) {
+          const uint8_t* buf = cur.acquire(R, status);
+          const int64_t e0 = ch * EPC + (int64_t)ct * EPT;
+          const int nv = valid_cols(V - e0, EPT);
+          float fs[EPT], ft[EPT];
+          if (nv > 0) {
+            Chunk<T>::load(buf, ct, fs);
+            Chunk<T>::load(buf + kChunk, ct, ft);
+          }
+          cur.release(R);
+#pragma unroll
+          for (int u = 0; u < EPT; ++u)
+            if (u < nv) js_terms(fs[u], ft[u], lse_tT, dlse, c, jq, jp);
+        }
+        const float2 r = consumer_sum2(jq, jp, R);
+        if (ct == 0) {
+          const bool v_ok = !a.labels || a.labels[row] != a.ignore;
+          a.stats[row * KD_STATS_PER_TOKEN + S_KL_PM] = r.y;
+          if (a.kl) a.kl[row] = v_ok ? (1.f - c.beta) * r.x + c.beta * r.y : 0.f;
+        }
+      }
+      ptx::named_sync(1, kCT);  // reduction slots are reused by the next row
+    }
+  }
+  __syncthreads();
+}
+
+// Backward.  Grad: row(a, row) once per row; static load(Frag&, buf, ct);
+// chunk(const Frag&, e0, nv, dz_row) writes the d z_s of one 16-byte slot.
+template <typename T, bool HAS_T, class Grad>
+__global__ void __launch_bounds__(kThreads, 1) k_bwd(StreamArgs a, uint32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  const Ring R = make_ring(smem_raw);
+  ring_init(R);
+  if ((threadIdx.x >> 5) == kCW) {
+    producer<T>(R, a, HAS_T, 1, status);
+  } else {
+    constexpr int EPT = 16 / (int)sizeof(T);
+    constexpr int EPC = kChunk / (int)sizeof(T);
+    const int64_t V = a.vocab, nch = (V + EPC - 1) / EPC;
+    const int ct = threadIdx.x;
+    Cursor cur;
+    for (int64_t row = blockIdx.x; row < a.n; row += gridDim.x) {
+      Grad g;
+      g.row(a, row);
+      T* dz = static_cast<T*>(a.dz) + row * V;
+      for (int64_t ch = 0; ch < nch; ++ch) {
+        const uint8_t* buf = cur.acquire(R, status);
+        const int64_t e0 = ch * EPC + (int64_t)ct * EPT;
+        const int nv = valid_cols(V - e0, EPT);
+        typename Grad::Frag f;
+        if (nv > 0) Grad::load(f, buf, ct);
+        cur.release(R);
+        if (nv > 0) g.chunk(f, e0, nv, dz);
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// Launch one persistent CTA per SM (fewer for short batches).
+template <typename K>
+inline void launch(K kernel, const StreamArgs& a, cudaStream_t s) {
+  const int sms = tc_num_sms() > 0 ? tc_num_sms() : 1;
+  const int grid = (int)(a.n < sms ? a.n : sms);
+  cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  kernel<<<grid, kThreads, kSmem, s>>>(a, a.status);
+}
+
+}  // namespace ring
+}  // namespace kd

@@ -1,88 +1,26 @@
 // HBM-streaming path for materialised logits (nemo_automodel KDLoss on
-// student_logits / teacher_logits; flash_kd with upcast=True): one CTA per
-// token row streams both logit rows with 128-bit read-only loads, keeps the
-// online-softmax state per thread (fp32), merges it across the block, and
-// finalises CE / KL / saved statistics.  Skew-JS needs both final
-// normalisers before log m, so it takes a second sweep of the same row while
-// it is still resident in L2.  The backward is a pure elementwise sweep that
-// reads z_s, z_t and the row statistics and writes d z_s.
+// student_logits / teacher_logits; flash_kd with upcast=True).
+//
+// Rows that are 16-byte aligned (the usual case) run the TMA-staged ring
+// kernels of kd_ring.cuh: a producer warp streams each token row through a
+// shared-memory ring with 1-D bulk copies while 16 consumer warps keep the
+// online-softmax state (forward) or write d z_s (backward).  This file holds
+// their generic per-chunk policies (any dtype, any temperature) and the
+// dispatch; kd_stream_bf16.cu holds packed bf16 policies for T = 1 and T = 2.
+// Rows that are not 16-byte aligned fall back to the plain kernels below: one
+// CTA per row, per-thread loads, skew-JS re-reading the row from L2.
 #include <cuda_bf16.h>
 
 #include "kd_internal.h"
+#include "kd_ring.cuh"
 
 namespace kd {
 
 namespace {
 
+using ring::ld1;
+using ring::st1;
 constexpr int kThreads = 512;
-
-__device__ __forceinline__ uint4 ldg_stream(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
-// 8 consecutive elements of a row at vector index vec.
-template <typename T>
-__device__ __forceinline__ void load8(const T* row, int64_t vec, float* out);
-
-template <>
-__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* row, int64_t vec,
-                                                      float* out) {
-  const uint4 u = ldg_stream(row + vec * 8);
-  out[0] = bf16lo(u.x); out[1] = bf16hi(u.x);
-  out[2] = bf16lo(u.y); out[3] = bf16hi(u.y);
-  out[4] = bf16lo(u.z); out[5] = bf16hi(u.z);
-  out[6] = bf16lo(u.w); out[7] = bf16hi(u.w);
-}
-
-template <>
-__device__ __forceinline__ void load8<float>(const float* row, int64_t vec, float* out) {
-  const uint4 a = ldg_stream(row + vec * 8), b = ldg_stream(row + vec * 8 + 4);
-  out[0] = __uint_as_float(a.x); out[1] = __uint_as_float(a.y);
-  out[2] = __uint_as_float(a.z); out[3] = __uint_as_float(a.w);
-  out[4] = __uint_as_float(b.x); out[5] = __uint_as_float(b.y);
-  out[6] = __uint_as_float(b.z); out[7] = __uint_as_float(b.w);
-}
-
-template <typename T>
-__device__ __forceinline__ float ld1(const T* p) {
-  return static_cast<float>(*p);
-}
-template <>
-__device__ __forceinline__ float ld1<__nv_bfloat16>(const __nv_bfloat16* p) {
-  return __bfloat162float(*p);
-}
-
-template <typename T>
-__device__ __forceinline__ void st8(T* row, int64_t vec, const float* g);
-template <>
-__device__ __forceinline__ void st8<__nv_bfloat16>(__nv_bfloat16* row, int64_t vec,
-                                                    const float* g) {
-  uint4 u;
-  u.x = pack_bf16(g[0], g[1]);
-  u.y = pack_bf16(g[2], g[3]);
-  u.z = pack_bf16(g[4], g[5]);
-  u.w = pack_bf16(g[6], g[7]);
-  *reinterpret_cast<uint4*>(row + vec * 8) = u;
-}
-template <>
-__device__ __forceinline__ void st8<float>(float* row, int64_t vec, const float* g) {
-  float4* o = reinterpret_cast<float4*>(row + vec * 8);
-  o[0] = make_float4(g[0], g[1], g[2], g[3]);
-  o[1] = make_float4(g[4], g[5], g[6], g[7]);
-}
-
-template <typename T>
-__device__ __forceinline__ void st1(T* p, float v) {
-  *p = static_cast<T>(v);
-}
-template <>
-__device__ __forceinline__ void st1<__nv_bfloat16>(__nv_bfloat16* p, float v) {
-  *p = __float2bfloat16(v);
-}
 
 // Merge every thread's state into thread 0 (result valid in thread 0 only).
 __device__ __forceinline__ void block_merge(RowState& st, const Consts& c, float* sh) {
@@ -121,7 +59,9 @@ __device__ __forceinline__ float2 block_sum2(float a, float b, float* sh) {
 
 }  // namespace
 
-template <typename T, bool HAS_T, bool VEC>
+// Fallback for rows that are not 16-byte aligned: one CTA per row, plain
+// per-thread loads.
+template <typename T, bool HAS_T>
 __global__ void __launch_bounds__(kThreads) k_stream_fwd(StreamArgs a) {
   __shared__ __align__(16) float sh[32 * kRec];
   __shared__ float sh_lse[2];
@@ -132,40 +72,20 @@ __global__ void __launch_bounds__(kThreads) k_stream_fwd(StreamArgs a) {
     const T* zt = HAS_T ? static_cast<const T*>(a.zt) + row * V : nullptr;
     RowState st;
     st.init();
-    if (VEC) {
-      const int64_t nvec = V / 8;
-      int64_t v = threadIdx.x;
-      for (; v + 3 * kThreads < nvec; v += 4 * kThreads) {
-        float fs[32], ft[32];
+    for (int64_t e0 = threadIdx.x; e0 < V; e0 += 8 * kThreads) {
+      float fs[8], ft[8];
+      int nv = 0;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          load8<T>(zs, v + u * kThreads, fs + 8 * u);
-          if (HAS_T) load8<T>(zt, v + u * kThreads, ft + 8 * u);
+      for (int u = 0; u < 8; ++u) {
+        const int64_t e = e0 + (int64_t)u * kThreads;
+        fs[u] = ft[u] = 0.f;
+        if (e < V) {
+          fs[u] = ld1<T>(zs + e);
+          if (HAS_T) ft[u] = ld1<T>(zt + e);
+          nv = u + 1;
         }
-        update<32, HAS_T, false>(st, fs, ft, 32, c);
       }
-      for (; v < nvec; v += kThreads) {
-        float fs[8], ft[8];
-        load8<T>(zs, v, fs);
-        if (HAS_T) load8<T>(zt, v, ft);
-        update<8, HAS_T, false>(st, fs, ft, 8, c);
-      }
-    } else {
-      for (int64_t e0 = threadIdx.x; e0 < V; e0 += 8 * kThreads) {
-        float fs[8], ft[8];
-        int nv = 0;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int64_t e = e0 + (int64_t)u * kThreads;
-          fs[u] = ft[u] = 0.f;
-          if (e < V) {
-            fs[u] = ld1<T>(zs + e);
-            if (HAS_T) ft[u] = ld1<T>(zt + e);
-            nv = u + 1;
-          }
-        }
-        update<8, HAS_T, true>(st, fs, ft, nv, c);
-      }
+      update<8, HAS_T, true>(st, fs, ft, nv, c);
     }
     if (a.topk) {  // sparse cross term sum_S p a_s (ids validated by the prep kernel)
       const int32_t* ids = a.sidx + row * a.k;
@@ -203,19 +123,8 @@ __global__ void __launch_bounds__(kThreads) k_stream_fwd(StreamArgs a) {
       __syncthreads();
       const float dlse = sh_lse[0], lse_tT = sh_lse[1];
       float jq = 0.f, jp = 0.f;
-      if (VEC) {
-        const int64_t nvec = V / 8;
-        for (int64_t v = threadIdx.x; v < nvec; v += kThreads) {
-          float fs[8], ft[8];
-          load8<T>(zs, v, fs);
-          load8<T>(zt, v, ft);
-#pragma unroll
-          for (int u = 0; u < 8; ++u) js_terms(fs[u], ft[u], lse_tT, dlse, c, jq, jp);
-        }
-      } else {
-        for (int64_t e = threadIdx.x; e < V; e += kThreads)
-          js_terms(ld1<T>(zs + e), ld1<T>(zt + e), lse_tT, dlse, c, jq, jp);
-      }
+      for (int64_t e = threadIdx.x; e < V; e += kThreads)
+        js_terms(ld1<T>(zs + e), ld1<T>(zt + e), lse_tT, dlse, c, jq, jp);
       const float2 r = block_sum2(jq, jp, sh);
       if (threadIdx.x == 0) {
         const bool v_ok = !a.labels || a.labels[row] != a.ignore;
@@ -228,14 +137,15 @@ __global__ void __launch_bounds__(kThreads) k_stream_fwd(StreamArgs a) {
 }
 
 // ---------------------------------------------------------------- backward
+// (fallback for unaligned rows)
 // d z_s = s_row [ w_sce (softmax(z_s) - e_y) + w_kl T_s dKL/da_s ], exactly 0
 // on ignored rows.  Top-K teachers: dKL/da = M softmax(a) - p; the -p part at
 // the K support columns is applied by k_stream_bwd_topk afterwards.
-template <typename T, bool HAS_T, bool VEC>
+template <typename T, bool HAS_T>
 __global__ void __launch_bounds__(256) k_stream_bwd(StreamArgs a) {
   const Consts c = a.c;
   const int64_t V = a.vocab;
-  constexpr int U = 4;  // vectors per thread per CTA
+  constexpr int U = 4;  // 8-element groups per thread per CTA
   for (int64_t row = blockIdx.y; row < a.n; row += gridDim.y) {
     const T* zs = static_cast<const T*>(a.zs) + row * V;
     const T* zt = HAS_T ? static_cast<const T*>(a.zt) + row * V : nullptr;
@@ -254,27 +164,10 @@ __global__ void __launch_bounds__(256) k_stream_bwd(StreamArgs a) {
       if (wc != 0.f) g = fmaf(wc, ex2((s - lse_s1) * kL2E) - (col == y ? 1.f : 0.f), g);
       return scale * g;
     };
-    if (VEC) {
-      const int64_t nvec = V / 8;
-      const int64_t v0 = (int64_t)blockIdx.x * (blockDim.x * U) + threadIdx.x;
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int64_t v = v0 + (int64_t)u * blockDim.x;
-        if (v < nvec) {
-          float fs[8], ft[8], g[8];
-          load8<T>(zs, v, fs);
-          if (HAS_T) load8<T>(zt, v, ft);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) g[j] = grad(fs[j], HAS_T ? ft[j] : 0.f, v * 8 + j);
-          st8<T>(dz, v, g);
-        }
-      }
-    } else {
-      const int64_t e0 = (int64_t)blockIdx.x * (blockDim.x * U * 8) + threadIdx.x;
-      for (int u = 0; u < U * 8; ++u) {
-        const int64_t e = e0 + (int64_t)u * blockDim.x;
-        if (e < V) st1<T>(dz + e, grad(ld1<T>(zs + e), HAS_T ? ld1<T>(zt + e) : 0.f, e));
-      }
+    const int64_t e0 = (int64_t)blockIdx.x * (blockDim.x * U * 8) + threadIdx.x;
+    for (int u = 0; u < U * 8; ++u) {
+      const int64_t e = e0 + (int64_t)u * blockDim.x;
+      if (e < V) st1<T>(dz + e, grad(ld1<T>(zs + e), HAS_T ? ld1<T>(zt + e) : 0.f, e));
     }
   }
 }
@@ -302,6 +195,94 @@ __global__ void k_stream_bwd_topk(StreamArgs a) {
   st1<T>(static_cast<T*>(a.dz) + row * a.vocab + id, scale * g);
 }
 
+// ------------------------------------------------- TMA-staged (aligned rows)
+// Generic policies for the ring kernels (kd_ring.cuh): any dtype, any
+// temperature.  bf16 problems with T = 1 or T = 2 take the packed policies of
+// kd_stream_bf16.cu instead.
+namespace {
+
+template <typename T, bool HAS_T>
+struct GenericAcc {
+  static constexpr int EPT = ring::Chunk<T>::EPT;
+  struct Frag {
+    float s[EPT], t[EPT];
+  };
+  RowState st;
+  __device__ static void load(Frag& f, const uint8_t* buf, int ct) {
+    ring::Chunk<T>::load(buf, ct, f.s);
+    if (HAS_T) ring::Chunk<T>::load(buf + ring::kChunk, ct, f.t);
+  }
+  __device__ void init() { st.init(); }
+  __device__ void step(const Frag& f, int nv, const Consts& c) {
+    if (nv == EPT) update<EPT, HAS_T, false>(st, f.s, f.t, EPT, c);
+    else update<EPT, HAS_T, true>(st, f.s, f.t, nv, c);
+  }
+  __device__ RowState fold() const { return st; }
+};
+
+// d z_s = s_row [ w_sce (softmax(z_s) - e_y) + w_kl T_s dKL/da_s ] for one
+// 16-byte slot; top-K teachers: dKL/da = M softmax(a), the -p part at the K
+// support columns is applied by k_stream_bwd_topk afterwards.
+template <typename T, bool HAS_T>
+struct GenericGrad {
+  static constexpr int EPT = ring::Chunk<T>::EPT;
+  struct Frag {
+    float s[EPT], t[EPT];
+  };
+  Consts c;
+  float sv[KD_STATS_PER_TOKEN];
+  float scale, sq_s, wk, wc;
+  int64_t y;
+  int variant, topk;
+  __device__ static void load(Frag& f, const uint8_t* buf, int ct) {
+    ring::Chunk<T>::load(buf, ct, f.s);
+    if (HAS_T) ring::Chunk<T>::load(buf + ring::kChunk, ct, f.t);
+  }
+  __device__ void row(const StreamArgs& a, int64_t r) {
+    c = a.c;
+    variant = a.variant;
+    topk = a.topk;
+    wk = a.w_kl_ts;
+    wc = a.w_sce;
+    scale = a.row_scale[r];
+#pragma unroll
+    for (int i = 0; i < KD_STATS_PER_TOKEN; ++i) sv[i] = a.stats[r * KD_STATS_PER_TOKEN + i];
+    y = a.labels ? a.labels[r] : -1;
+    sq_s = c.pw == 2 ? ex2((2.f * sv[S_LSE_ST] - sv[S_LSE_S1]) * kL2E) : 0.f;
+  }
+  __device__ void chunk(const Frag& f, int64_t e0, int nv, T* dz) {
+    float g[EPT];
+#pragma unroll
+    for (int u = 0; u < EPT; ++u) {
+      float gg = 0.f;
+      if (scale != 0.f) {
+        const float lp = fmaf(f.s[u], c.inv_ts, -sv[S_LSE_ST]);
+        const float p = ex2(lp * kL2E);
+        if (HAS_T) {
+          const float lq = fmaf(f.t[u], c.inv_tt, -sv[S_LSE_TT]);
+          gg = wk * kl_grad_pq(f.s[u], f.t[u], lp, lq, p, ex2(lq * kL2E), sv, variant, c);
+        } else if (topk) {
+          gg = wk * sv[S_MASS] * p;
+        }
+        if (wc != 0.f)
+          gg = fmaf(wc, softmax_t1(f.s[u], p, sv[S_LSE_S1], sq_s, c.pw) - (e0 + u == y ? 1.f : 0.f),
+                    gg);
+        gg *= scale;
+      }
+      g[u] = gg;
+    }
+    if (nv == EPT) {
+      ring::Chunk<T>::store(dz + e0, g);
+    } else {
+#pragma unroll
+      for (int u = 0; u < EPT; ++u)
+        if (u < nv) ring::st1<T>(dz + e0 + u, g[u]);
+    }
+  }
+};
+
+}  // namespace
+
 namespace {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 }  // namespace
@@ -312,10 +293,15 @@ static void fwd_dispatch(const StreamArgs& a, cudaStream_t s) {
   const unsigned grid = (unsigned)(a.n < 2147483647 ? a.n : 2147483647);
   const bool has_t = a.zt != nullptr;
   note_launch();
-  if (has_t && vec) k_stream_fwd<T, true, true><<<grid, kThreads, 0, s>>>(a);
-  else if (has_t) k_stream_fwd<T, true, false><<<grid, kThreads, 0, s>>>(a);
-  else if (vec) k_stream_fwd<T, false, true><<<grid, kThreads, 0, s>>>(a);
-  else k_stream_fwd<T, false, false><<<grid, kThreads, 0, s>>>(a);
+  if (vec) {  // rows 16-byte aligned: TMA-staged ring kernels
+    if (launch_stream_fwd_packed(a, s)) return;
+    if (has_t) ring::launch(ring::k_fwd<T, true, GenericAcc<T, true>>, a, s);
+    else ring::launch(ring::k_fwd<T, false, GenericAcc<T, false>>, a, s);
+  } else if (has_t) {
+    k_stream_fwd<T, true><<<grid, kThreads, 0, s>>>(a);
+  } else {
+    k_stream_fwd<T, false><<<grid, kThreads, 0, s>>>(a);
+  }
 }
 
 template <typename T>
@@ -327,10 +313,16 @@ static void bwd_dispatch(const StreamArgs& a, cudaStream_t s) {
             (unsigned)(a.n < 65535 ? a.n : 65535));
   const bool has_t = a.zt != nullptr;
   note_launch();
-  if (has_t && vec) k_stream_bwd<T, true, true><<<grid, 256, 0, s>>>(a);
-  else if (has_t) k_stream_bwd<T, true, false><<<grid, 256, 0, s>>>(a);
-  else if (vec) k_stream_bwd<T, false, true><<<grid, 256, 0, s>>>(a);
-  else k_stream_bwd<T, false, false><<<grid, 256, 0, s>>>(a);
+  if (vec) {  // rows 16-byte aligned: TMA-staged ring kernels
+    if (!launch_stream_bwd_packed(a, s)) {
+      if (has_t) ring::launch(ring::k_bwd<T, true, GenericGrad<T, true>>, a, s);
+      else ring::launch(ring::k_bwd<T, false, GenericGrad<T, false>>, a, s);
+    }
+  } else if (has_t) {
+    k_stream_bwd<T, true><<<grid, 256, 0, s>>>(a);
+  } else {
+    k_stream_bwd<T, false><<<grid, 256, 0, s>>>(a);
+  }
   if (a.topk && a.k > 0) {
     const int64_t tot = a.n * a.k;
     note_launch();

@@ -1,0 +1,328 @@
+// Packed bf16 policies for the TMA-staged streaming kernels (kd_ring.cuh),
+// for the common case T_s = T_t in {1, 2}.
+//
+// The arithmetic is the same as the generic policies (online softmax with the
+// q- and p-weighted cross sums of d = a_t - a_s; closed-form gradients), but
+// the variant, the temperature shortcut and whether the T = 1 (CE) sums are
+// needed are template parameters, so no runtime branch stays in the inner
+// loop, and the fp32 work runs on Blackwell's paired fp32 instructions
+// (fma/add/mul .f32x2: one instruction for two columns).  Chunk maxima come
+// from max.bf16x2 on the raw words.  A streamed logit costs about a dozen
+// instructions this way instead of about forty, which is what lets the kernels
+// keep up with HBM.
+#include <cuda_bf16.h>
+
+#include "kd_internal.h"
+#include "kd_ring.cuh"
+
+namespace kd {
+namespace {
+
+using bf16 = __nv_bfloat16;
+
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ float2 splat(float v) { return make_float2(v, v); }
+__device__ __forceinline__ float2 unpack(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
+__device__ __forceinline__ float2 ex2x2(float2 v) { return make_float2(ex2(v.x), ex2(v.y)); }
+__device__ __forceinline__ float hsum(float2 v) { return v.x + v.y; }
+__device__ __forceinline__ float max8(const uint4& u) {
+  const uint32_t m = max_bf16x2(max_bf16x2(u.x, u.y), max_bf16x2(u.z, u.w));
+  return fmaxf(bf16lo(m), bf16hi(m));
+}
+__device__ __forceinline__ uint32_t word(const uint4& u, int i) {
+  return i == 0 ? u.x : (i == 1 ? u.y : (i == 2 ? u.z : u.w));
+}
+
+// ------------------------------------------------------------------ forward
+// KLM: bit0 forward cross sums (q d, q (e^{-d} - 1)), bit1 reverse ones.
+// PW: 1 (T = 1, the CE sums are the tempered ones) or 2 (T = 2, e^{z-m} =
+// (e^{(z-m)/2})^2).  NEED1: labels present, so the T = 1 sums are kept.
+template <bool HAS_T, int KLM, int PW, bool NEED1>
+struct PackedAcc {
+  struct Frag {
+    uint4 s, t;
+  };
+  float ms, mt, cq, cp;
+  float2 osT, otT;  // -m k_T per side (exponent offsets)
+  float2 ls1, lsT, lt1, ltT, qd, qx, pd, px;
+
+  __device__ static void load(Frag& f, const uint8_t* buf, int ct) {
+    f.s = *reinterpret_cast<const uint4*>(buf + ct * 16);
+    if (HAS_T) f.t = *reinterpret_cast<const uint4*>(buf + ring::kChunk + ct * 16);
+  }
+  __device__ void init() {
+    ms = mt = neg_inf();
+    cq = cp = 0.f;
+    osT = otT = ls1 = lsT = lt1 = ltT = qd = qx = pd = px = splat(0.f);
+  }
+  // Rescale the running sums to a larger maximum (rare after a row's first
+  // chunks); the same factors as update() in kd_common.cuh.
+  __device__ __forceinline__ void grow(float cms, float cmt, const Consts& c) {
+    bool grew = false;
+    if (cms > ms) {
+      const float fT = ex2((ms - cms) * c.k_sT);
+      lsT = mul2(lsT, splat(fT));
+      if (KLM & 2) {
+        pd = mul2(pd, splat(fT));
+        px = mul2(px, splat(fT));
+      }
+      if (NEED1) ls1 = mul2(ls1, splat(ex2((ms - cms) * c.k_s1)));
+      ms = cms;
+      osT = splat(-ms * c.k_sT);
+      grew = true;
+    }
+    if (HAS_T && cmt > mt) {
+      const float fT = ex2((mt - cmt) * c.k_tT);
+      ltT = mul2(ltT, splat(fT));
+      if (KLM & 1) {
+        qd = mul2(qd, splat(fT));
+        qx = mul2(qx, splat(fT));
+      }
+      if (NEED1) lt1 = mul2(lt1, splat(ex2((mt - cmt) * c.k_t1)));
+      mt = cmt;
+      otT = splat(-mt * c.k_tT);
+      grew = true;
+    }
+    if (HAS_T && grew) {
+      const float dM = (ms * c.inv_ts - mt * c.inv_tt) * kL2E;
+      cq = ex2(dM);
+      cp = ex2(-dM);
+    }
+  }
+  __device__ __forceinline__ void pair(uint32_t ws, uint32_t wt, const Consts& c) {
+    const float2 s = unpack(ws);
+    const float2 es = ex2x2(fma2(s, splat(c.k_sT), osT));
+    lsT = add2(lsT, es);
+    if (NEED1) ls1 = PW == 2 ? fma2(es, es, ls1) : add2(ls1, es);
+    if (HAS_T) {
+      const float2 t = unpack(wt);
+      const float2 et = ex2x2(fma2(t, splat(c.k_tT), otT));
+      ltT = add2(ltT, et);
+      if (NEED1) lt1 = PW == 2 ? fma2(et, et, lt1) : add2(lt1, et);
+      const float2 d = fma2(t, splat(c.inv_tt), mul2(s, splat(-c.inv_ts)));
+      if (KLM & 1) {
+        qd = fma2(et, d, qd);
+        qx = add2(qx, make_float2(fmaf(es.x, cq, -et.x), fmaf(es.y, cq, -et.y)));
+      }
+      if (KLM & 2) {
+        pd = fma2(es, d, pd);  // sum of p d: the state keeps its negative
+        px = add2(px, make_float2(fmaf(et.x, cp, -es.x), fmaf(et.y, cp, -es.y)));
+      }
+    }
+  }
+  __device__ __forceinline__ void step(const Frag& f, int, const Consts& c) {
+    const float cms = max8(f.s);
+    const float cmt = HAS_T ? max8(f.t) : neg_inf();
+    if (cms > ms || (HAS_T && cmt > mt)) grow(cms, cmt, c);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) pair(word(f.s, i), HAS_T ? word(f.t, i) : 0u, c);
+  }
+  __device__ RowState fold() const {
+    RowState st;
+    st.init();
+    st.ms = ms;
+    st.ls1 = hsum(ls1);
+    st.lsT = hsum(lsT);
+    if (HAS_T) {
+      st.mt = mt;
+      st.lt1 = hsum(lt1);
+      st.ltT = hsum(ltT);
+      st.qd = hsum(qd);
+      st.qx = hsum(qx);
+      st.pd = -hsum(pd);
+      st.px = hsum(px);
+    }
+    return st;
+  }
+};
+
+// ----------------------------------------------------------------- backward
+// VAR: KD_KL_FORWARD / REVERSE / JEFFREYS / SKEW_JS (teacher present; unused
+// otherwise).  CE: w_sce != 0.  Gradients, with p = softmax(a_s), q =
+// softmax(a_t), r = log p - log q - KL(p||q):
+//   forward  p - q;   reverse  p r;   Jeffreys  p - q + p r;
+//   skew-JS  b p (x - w(x) - KL_pm) (see kl_grad_pq);   top-K  M p;
+// each times s_row w_kl T_s, plus s_row w_sce (softmax(z_s) - e_y).
+template <bool HAS_T, int VAR, int PW, bool CE>
+struct PackedGrad {
+  struct Frag {
+    uint4 s, t;
+  };
+  float ks, ns, kt, nt;  // log2 p = s ks + ns, log2 q = t kt + nt
+  float sw, swc, csq, kl_r;
+  int64_t y;
+  bool zero;
+  float sv[KD_STATS_PER_TOKEN];  // skew-JS only
+  Consts c;                      // skew-JS only
+
+  __device__ static void load(Frag& f, const uint8_t* buf, int ct) {
+    f.s = *reinterpret_cast<const uint4*>(buf + ct * 16);
+    if (HAS_T) f.t = *reinterpret_cast<const uint4*>(buf + ring::kChunk + ct * 16);
+  }
+  __device__ void row(const StreamArgs& a, int64_t r) {
+    const float* st = a.stats + r * KD_STATS_PER_TOKEN;
+    const float scale = a.row_scale[r];
+    zero = scale == 0.f;
+    ks = a.c.inv_ts * kL2E;
+    ns = -st[S_LSE_ST] * kL2E;
+    kt = a.c.inv_tt * kL2E;
+    nt = HAS_T ? -st[S_LSE_TT] * kL2E : 0.f;
+    sw = scale * a.w_kl_ts * (HAS_T ? 1.f : (a.topk ? st[S_MASS] : 0.f));
+    swc = CE ? scale * a.w_sce : 0.f;
+    csq = (CE && PW == 2) ? swc * ex2((2.f * st[S_LSE_ST] - st[S_LSE_S1]) * kL2E) : swc;
+    kl_r = HAS_T ? st[S_KL_REV] : 0.f;
+    y = (CE && a.labels) ? a.labels[r] : -1;
+    if (HAS_T && VAR == KD_KL_SKEW_JS) {
+      c = a.c;
+#pragma unroll
+      for (int i = 0; i < KD_STATS_PER_TOKEN; ++i) sv[i] = st[i];
+    }
+  }
+  __device__ __forceinline__ float2 pair(uint32_t ws, uint32_t wt) const {
+    const float2 s = unpack(ws);
+    const float2 lp2 = fma2(s, splat(ks), splat(ns));
+    const float2 p = ex2x2(lp2);
+    float2 g = splat(0.f);
+    if (HAS_T) {
+      const float2 t = unpack(wt);
+      const float2 lq2 = fma2(t, splat(kt), splat(nt));
+      if (VAR == KD_KL_FORWARD) {
+        g = mul2(sub2(p, ex2x2(lq2)), splat(sw));
+      } else if (VAR == KD_KL_REVERSE || VAR == KD_KL_JEFFREYS) {
+        const float2 r = fma2(sub2(lp2, lq2), splat(1.f / kL2E), splat(-kl_r));
+        if (VAR == KD_KL_REVERSE) g = mul2(mul2(p, splat(sw)), r);
+        else g = mul2(fma2(p, r, sub2(p, ex2x2(lq2))), splat(sw));
+      } else {
+        g.x = sw * kl_grad_pq(s.x, t.x, 0.f, 0.f, p.x, 0.f, sv, KD_KL_SKEW_JS, c);
+        g.y = sw * kl_grad_pq(s.y, t.y, 0.f, 0.f, p.y, 0.f, sv, KD_KL_SKEW_JS, c);
+      }
+    } else {
+      g = mul2(p, splat(sw));
+    }
+    if (CE) g = fma2(PW == 2 ? mul2(p, p) : p, splat(csq), g);
+    return g;
+  }
+  __device__ __forceinline__ void chunk(const Frag& f, int64_t e0, int, bf16* dz) {
+    uint4 out = make_uint4(0u, 0u, 0u, 0u);
+    if (!zero) {
+      float2 g[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) g[i] = pair(word(f.s, i), HAS_T ? word(f.t, i) : 0u);
+      if (CE && (uint64_t)(y - e0) < 8u) {  // the label column: - s_row w_sce
+        const int j = (int)(y - e0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (j == 2 * i) g[i].x -= swc;
+          if (j == 2 * i + 1) g[i].y -= swc;
+        }
+      }
+      out.x = pack_bf16(g[0].x, g[0].y);
+      out.y = pack_bf16(g[1].x, g[1].y);
+      out.z = pack_bf16(g[2].x, g[2].y);
+      out.w = pack_bf16(g[3].x, g[3].y);
+    }
+    *reinterpret_cast<uint4*>(dz + e0) = out;
+  }
+};
+
+// ----------------------------------------------------------------- dispatch
+template <bool HAS_T, int KLM, int PW>
+void fwd_need(const StreamArgs& a, cudaStream_t s) {
+  if (a.c.need_s1) ring::launch(ring::k_fwd<bf16, HAS_T, PackedAcc<HAS_T, KLM, PW, true>>, a, s);
+  else ring::launch(ring::k_fwd<bf16, HAS_T, PackedAcc<HAS_T, KLM, PW, false>>, a, s);
+}
+template <bool HAS_T, int KLM>
+void fwd_pw(const StreamArgs& a, cudaStream_t s) {
+  if (a.c.pw == 2) fwd_need<HAS_T, KLM, 2>(a, s);
+  else fwd_need<HAS_T, KLM, 1>(a, s);
+}
+
+template <bool HAS_T, int VAR, int PW>
+void bwd_ce(const StreamArgs& a, cudaStream_t s) {
+  if (a.w_sce != 0.f) ring::launch(ring::k_bwd<bf16, HAS_T, PackedGrad<HAS_T, VAR, PW, true>>, a, s);
+  else ring::launch(ring::k_bwd<bf16, HAS_T, PackedGrad<HAS_T, VAR, PW, false>>, a, s);
+}
+template <bool HAS_T, int VAR>
+void bwd_pw(const StreamArgs& a, cudaStream_t s) {
+  if (a.c.pw == 2) bwd_ce<HAS_T, VAR, 2>(a, s);
+  else bwd_ce<HAS_T, VAR, 1>(a, s);
+}
+
+bool packed_ok(const StreamArgs& a) {
+  if (!a.is_bf16 || (a.c.pw != 1 && a.c.pw != 2)) return false;
+  // with a teacher the T = 1 sums of both sides go together
+  return a.zt == nullptr || a.c.need_s1 == a.c.need_t1;
+}
+
+}  // namespace
+
+bool launch_stream_fwd_packed(const StreamArgs& a, cudaStream_t s) {
+  if (!packed_ok(a)) return false;
+  if (a.zt == nullptr) {
+    fwd_pw<false, 0>(a, s);
+    return true;
+  }
+  switch (a.c.kl_mode) {
+    case 1: fwd_pw<true, 1>(a, s); return true;
+    case 2: fwd_pw<true, 2>(a, s); return true;
+    case 3: fwd_pw<true, 3>(a, s); return true;
+    default: return false;
+  }
+}
+
+bool launch_stream_bwd_packed(const StreamArgs& a, cudaStream_t s) {
+  if (!packed_ok(a)) return false;
+  if (a.zt == nullptr) {
+    bwd_pw<false, KD_KL_FORWARD>(a, s);
+    return true;
+  }
+  switch (a.variant) {
+    case KD_KL_FORWARD: bwd_pw<true, KD_KL_FORWARD>(a, s); return true;
+    case KD_KL_REVERSE: bwd_pw<true, KD_KL_REVERSE>(a, s); return true;
+    case KD_KL_JEFFREYS: bwd_pw<true, KD_KL_JEFFREYS>(a, s); return true;
+    case KD_KL_SKEW_JS: bwd_pw<true, KD_KL_SKEW_JS>(a, s); return true;
+    default: return false;
+  }
+}
+
+}  // namespace kd

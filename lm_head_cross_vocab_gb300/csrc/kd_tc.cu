@@ -275,14 +275,17 @@ struct Sync {
   bool cluster_acquire;  // waits on barriers the peer CTA arrives on remotely
 };
 
-// Lane 0 waits (bounded in time), the outcome is broadcast to the warp.
+// Lane 0 waits (bounded in time), the outcome is broadcast to the warp, and
+// then every lane tests the completed phase itself, so that each thread has
+// the acquire ordering of a successful try_wait before it touches the data the
+// barrier guards.
 __device__ __forceinline__ bool warp_wait(const Sync& s, uint32_t bar, uint32_t parity,
                                           bool honour_abort = true) {
   int ok = 1;
+  auto probe = [&]() {
+    return s.cluster_acquire ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity);
+  };
   if ((threadIdx.x & 31) == 0) {
-    auto probe = [&]() {
-      return s.cluster_acquire ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity);
-    };
     if (!probe()) {
       const uint64_t t0 = globaltimer();
       ok = 0;
@@ -302,7 +305,9 @@ __device__ __forceinline__ bool warp_wait(const Sync& s, uint32_t bar, uint32_t 
       }
     }
   }
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+  const bool done = __shfl_sync(0xffffffffu, ok, 0) != 0;
+  if (done) probe();  // completed phase: succeeds at once, with acquire
+  return done;
 }
 
 __device__ __forceinline__ void item_range(const TcParams& P, int item, int& m_tile, int& t0,

@@ -30,6 +30,52 @@ def test_logit_pair_streaming(variant, vocab):
     assert_parity(run_and_compare(w), "bf16")
 
 
+@pytest.mark.parametrize("variant", ["jeffreys", "skew_js"])
+def test_logit_pair_streaming_more_rows_than_ctas(variant):
+    """More rows than persistent CTAs: each CTA streams several rows (two sweeps
+    each for skew-JS) through one ring, so stage phases carry across rows."""
+    w = W[5].scaled(n_tokens=341, vocab=8200, variant=variant, w_student_ce=0.3)
+    assert_parity(run_and_compare(w), "bf16")
+
+
+@pytest.mark.parametrize("variant", ["forward", "reverse"])
+def test_logit_pair_streaming_rows_longer_than_the_ring(variant):
+    """Rows of 13+ staged chunks: every ring slot is refilled within a row, so
+    consumers often wait on a slot whose copy is still in flight."""
+    w = W[5].scaled(n_tokens=180, vocab=53256, variant=variant)
+    assert_parity(run_and_compare(w), "bf16")
+
+
+@pytest.mark.parametrize("variant", ["forward", "reverse", "jeffreys", "skew_js"])
+def test_logit_pair_streaming_t1_with_student_ce(variant):
+    """T = 1 with a student CE term: the packed kernels' T = 1 shortcut and
+    their label-column correction."""
+    w = W[5].scaled(n_tokens=70, vocab=4104, variant=variant, t_student=1.0, t_teacher=1.0,
+                    w_student_ce=0.6)
+    assert_parity(run_and_compare(w), "bf16")
+
+
+@pytest.mark.parametrize("variant", ["forward", "jeffreys"])
+def test_logit_pair_streaming_without_labels(variant):
+    """No labels at all: no CE sums are kept."""
+    w = W[5].scaled(n_tokens=48, vocab=6000, variant=variant, ignore_frac=0.0)
+    assert "labels" not in I.make_inputs(w.scaled(n_tokens=1, vocab=8), "cpu")
+    assert_parity(run_and_compare(w), "bf16")
+
+
+def test_logit_pair_streaming_general_temperature_bf16():
+    """T = 1.5 (no exact shortcut): the generic ring kernels in bf16."""
+    w = W[5].scaled(n_tokens=60, vocab=5000, variant="jeffreys", t_student=1.5, t_teacher=1.5,
+                    w_student_ce=0.4)
+    assert_parity(run_and_compare(w), "bf16")
+
+
+def test_logit_student_plain_ce_streaming():
+    """Student logits, no teacher: CE only."""
+    w = W[5].scaled(n_tokens=50, vocab=3000, teacher="none", w_student_ce=1.0, w_kl=0.0)
+    assert_parity(run_and_compare(w), "bf16")
+
+
 def test_logit_pair_streaming_fp32_with_ce():
     w = W[5].scaled(n_tokens=40, vocab=3000, dtype="fp32", w_student_ce=0.7, variant="jeffreys",
                     t_teacher=1.5)
@@ -39,6 +85,13 @@ def test_logit_pair_streaming_fp32_with_ce():
 def test_topk_with_logit_student_streaming():
     w = W[4].scaled(n_tokens=50, vocab=2048, student="logits", d_student=0, topk=16,
                     student_logit_std=2.0)
+    assert_parity(run_and_compare(w), "bf16")
+
+
+def test_topk_with_logit_student_t2_and_ce_streaming():
+    w = W[4].scaled(n_tokens=45, vocab=3072, student="logits", d_student=0, topk=24,
+                    student_logit_std=2.0, t_student=2.0, t_teacher=2.0, w_student_ce=0.5,
+                    ignore_frac=0.1)
     assert_parity(run_and_compare(w), "bf16")
 
 
