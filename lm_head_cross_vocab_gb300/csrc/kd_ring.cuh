@@ -21,13 +21,21 @@
 namespace kd {
 namespace ring {
 
-constexpr int kCW = 16;                // consumer warps
-constexpr int kCT = 32 * kCW;          // consumer threads
-constexpr int kThreads = kCT + 32;     // + one producer warp
-constexpr int kChunk = 8192;           // bytes of one tensor per stage
-constexpr int kStages = 12;
+constexpr int kCW = 16;                       // consumer warps
+constexpr int kCT = 32 * kCW;                 // consumer threads
+constexpr int kThreads = kCT + 32;            // + one producer warp
+constexpr int kChunk = 16384;                 // bytes of one tensor per stage
+constexpr int kStages = 6;
+constexpr int kSlots = kChunk / (16 * kCT);   // 16-byte slots per consumer thread per stage
 constexpr int kRingBytes = kStages * 2 * kChunk;
-constexpr int kSmem = kRingBytes + 1024 + 128 + kCW * kRec * 4 + 64;
+// Per-row merge records.  A consumer warp runs at most kStages + 1 chunks
+// (so at most kStages + 2 rows) ahead of the slowest one, so 16 record sets
+// are never reused while still being read.
+constexpr int kMergeSlots = 16;
+constexpr int kRecBytes = kMergeSlots * kCW * kRec * 4;
+constexpr int kSmem = 128 + kRingBytes + 256 + kRecBytes + 64;
+static_assert(kMergeSlots >= kStages + 4, "merge records could be reused too early");
+static_assert(kSlots * 16 * kCT == kChunk, "a stage splits evenly over the consumers");
 
 template <typename T>
 __device__ __forceinline__ float ld1(const T* p) {
@@ -50,7 +58,8 @@ struct Ring {
   uint8_t* base;         // [stage][tensor][kChunk]
   uint32_t full, empty;  // mbarrier arrays (8 bytes each)
   volatile int* abort;
-  float* red;            // [kCW][kRec] reduction slots
+  int* cnt;              // [kMergeSlots] arrivals per merge record set
+  float* recs;           // [kMergeSlots][kCW][kRec] per-warp row states
   float* bcast;          // small broadcast area
 };
 
@@ -63,8 +72,9 @@ __device__ __forceinline__ Ring make_ring(uint8_t* smem) {
   r.full = ptx::smem_u32(tail);
   r.empty = r.full + 8 * kStages;
   r.abort = reinterpret_cast<volatile int*>(tail + 16 * kStages);
-  r.red = reinterpret_cast<float*>(tail + 16 * kStages + 64);
-  r.bcast = r.red + kCW * kRec;
+  r.cnt = reinterpret_cast<int*>(tail + 128);
+  r.recs = reinterpret_cast<float*>(tail + 256);
+  r.bcast = r.recs + kMergeSlots * kCW * kRec;
   return r;
 }
 
@@ -74,6 +84,7 @@ __device__ __forceinline__ void ring_init(const Ring& R) {
       ptx::mbar_init(R.full + 8 * i, 1);
       ptx::mbar_init(R.empty + 8 * i, kCW);  // one arrival per consumer warp
     }
+    for (int i = 0; i < kMergeSlots; ++i) R.cnt[i] = 0;
     *R.abort = 0;
     ptx::fence_mbar_init();
   }
@@ -145,18 +156,42 @@ struct Cursor {
   }
 };
 
-// Merge the consumers' states into consumer thread 0 (all consumers call).
+// Merge warp-reduced states (lane 0 of each consumer warp holds one) into
+// consumer thread 0 behind a barrier (all consumers call).
 __device__ __forceinline__ void consumer_merge(RowState& st, const Consts& c, const Ring& R) {
-  for (int o = 16; o > 0; o >>= 1) merge(st, shfl_xor(st, o), c);
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  if (l == 0) st.store(R.red + w * kRec);
+  if (l == 0) st.store(R.recs + w * kRec);
   ptx::named_sync(1, kCT);
   if (w == 0) {
-    if (l < kCW) st.load(R.red + l * kRec);
+    if (l < kCW) st.load(R.recs + l * kRec);
     else st.init();
     for (int o = 16; o > 0; o >>= 1) merge(st, shfl_xor(st, o), c);
   }
   ptx::named_sync(1, kCT);
+}
+
+// Barrier-free merge: every consumer warp leaves its warp-reduced state in
+// the record set of this row and counts itself in; the last warp to arrive
+// merges the set (returns true in that warp, merged state in its lane 0).
+__device__ __forceinline__ bool async_merge(RowState& st, const Consts& c, const Ring& R,
+                                            int local_row) {
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const int slot = local_row & (kMergeSlots - 1);
+  float* rec = R.recs + slot * kCW * kRec;
+  int last = 0;
+  if (l == 0) {
+    st.store(rec + w * kRec);
+    __threadfence_block();
+    last = atomicAdd(R.cnt + slot, 1) == kCW - 1;
+    __threadfence_block();
+  }
+  if (!__shfl_sync(0xffffffffu, last, 0)) return false;
+  __syncwarp();  // orders the other lanes' reads after lane 0's observation
+  if (l < kCW) st.load(rec + l * kRec);
+  else st.init();
+  for (int o = 16; o > 0; o >>= 1) merge(st, shfl_xor(st, o), c);
+  if (l == 0) R.cnt[slot] = 0;  // released before this warp's next ring arrival
+  return true;
 }
 
 __device__ __forceinline__ float2 consumer_sum2(float x, float y, const Ring& R) {
@@ -166,15 +201,15 @@ __device__ __forceinline__ float2 consumer_sum2(float x, float y, const Ring& R)
   }
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   if (l == 0) {
-    R.red[2 * w] = x;
-    R.red[2 * w + 1] = y;
+    R.recs[2 * w] = x;
+    R.recs[2 * w + 1] = y;
   }
   ptx::named_sync(1, kCT);
   float2 r = make_float2(0.f, 0.f);
   if (threadIdx.x == 0)
     for (int i = 0; i < kCW; ++i) {
-      r.x += R.red[2 * i];
-      r.y += R.red[2 * i + 1];
+      r.x += R.recs[2 * i];
+      r.y += R.recs[2 * i + 1];
     }
   ptx::named_sync(1, kCT);
   return r;
@@ -212,8 +247,39 @@ struct Chunk<float> {
   }
 };
 
-// Forward.  Acc: init(); static load(Frag&, buf, ct); step(const Frag&, nv, c);
-// RowState fold().
+// Outputs of one token from its merged state (one thread).
+template <typename T, bool HAS_T>
+__device__ __forceinline__ RowOut finish_row(const StreamArgs& a, int64_t row, RowState& st,
+                                             bool write_kl) {
+  const Consts& c = a.c;
+  const int64_t V = a.vocab;
+  const T* zs = static_cast<const T*>(a.zs) + row * V;
+  const T* zt = HAS_T ? static_cast<const T*>(a.zt) + row * V : nullptr;
+  bool valid = true, bad = false;
+  if (a.labels) {
+    const int64_t y = a.labels[row];
+    valid = y != a.ignore;
+    bad = valid && (y < 0 || y >= V);
+    if (valid && !bad) {
+      st.zys = ld1<T>(zs + y);
+      if (HAS_T) st.zyt = ld1<T>(zt + y);
+    }
+  }
+  const float mass = a.topk ? a.mass[row] : 0.f, ent = a.topk ? a.ent[row] : 0.f;
+  const RowOut o = finalize(st, c, a.variant, HAS_T, a.topk, mass, ent);
+  const float nan = __int_as_float(0x7fc00000);
+  if (a.ce_s) a.ce_s[row] = !valid ? 0.f : (bad ? nan : o.ce_s);
+  if (a.ce_t) a.ce_t[row] = !valid ? 0.f : (bad ? nan : o.ce_t);
+  if (a.kl && write_kl) a.kl[row] = valid ? o.kl : 0.f;
+  float4* s4 = reinterpret_cast<float4*>(a.stats + row * KD_STATS_PER_TOKEN);
+  s4[0] = make_float4(o.lse_s1, o.lse_sT, o.lse_t1, o.lse_tT);
+  s4[1] = make_float4(o.kl_rev, 0.f, mass, o.dlse);
+  return o;
+}
+
+// Forward.  Acc: init(); static load(Frag&, buf, slot); step(const Frag[kSlots],
+// const int nv[kSlots], c); RowState fold().  Column indices within a row are
+// 32-bit (the dispatch keeps rows below 2^30 elements).
 template <typename T, bool HAS_T, class Acc>
 __global__ void __launch_bounds__(kThreads, 1) k_fwd(StreamArgs a, uint32_t* status) {
   extern __shared__ uint8_t smem_raw[];
@@ -226,80 +292,78 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd(StreamArgs a, uint32_t* sta
     constexpr int EPT = 16 / (int)sizeof(T);
     constexpr int EPC = kChunk / (int)sizeof(T);
     const Consts c = a.c;
-    const int64_t V = a.vocab, nch = (V + EPC - 1) / EPC;
+    const int V = (int)a.vocab, nch = (V + EPC - 1) / EPC;
     const int ct = threadIdx.x;
     Cursor cur;
-    for (int64_t row = blockIdx.x; row < a.n; row += gridDim.x) {
+    int local_row = 0;
+    for (int64_t row = blockIdx.x; row < a.n; row += gridDim.x, ++local_row) {
       Acc acc;
       acc.init();
-      for (int64_t ch = 0; ch < nch; ++ch) {
+      for (int ch = 0; ch < nch; ++ch) {
         const uint8_t* buf = cur.acquire(R, status);
-        const int64_t e0 = ch * EPC + (int64_t)ct * EPT;
-        const int nv = valid_cols(V - e0, EPT);
-        typename Acc::Frag f;
-        if (nv > 0) Acc::load(f, buf, ct);
+        typename Acc::Frag f[kSlots];
+        int nv[kSlots];
+#pragma unroll
+        for (int j = 0; j < kSlots; ++j) {
+          const int slot = j * kCT + ct;
+          nv[j] = valid_cols(V - (ch * EPC + slot * EPT), EPT);
+          if (nv[j] > 0) Acc::load(f[j], buf, slot);
+        }
         cur.release(R);
-        if (nv > 0) acc.step(f, nv, c);
+        acc.step(f, nv, c);
       }
       RowState st = acc.fold();
-      const T* zs = static_cast<const T*>(a.zs) + row * V;
-      const T* zt = HAS_T ? static_cast<const T*>(a.zt) + row * V : nullptr;
       if (a.topk) {  // sparse cross term sum_S p a_s (ids validated by the prep kernel)
+        const T* zs = static_cast<const T*>(a.zs) + row * a.vocab;
         const int32_t* ids = a.sidx + row * a.k;
         const float* ps = a.sp + row * a.k;
         for (int j = ct; j < a.k; j += kCT) {
           const int32_t id = ids[j];
-          if (id >= 0 && (int64_t)id < V) st.tk = fmaf(ps[j], ld1<T>(zs + id) * c.inv_ts, st.tk);
+          if (id >= 0 && id < V) st.tk = fmaf(ps[j], ld1<T>(zs + id) * c.inv_ts, st.tk);
         }
       }
+      for (int o = 16; o > 0; o >>= 1) merge(st, shfl_xor(st, o), c);
+      if (passes == 1) {
+        // no CTA barrier: the last warp to finish the row finalises it
+        if (async_merge(st, c, R, local_row) && (ct & 31) == 0)
+          finish_row<T, HAS_T>(a, row, st, true);
+        continue;
+      }
+      // skew-JS: both normalisers are needed before the second sweep
       consumer_merge(st, c, R);
       if (ct == 0) {
-        bool valid = true, bad = false;
-        if (a.labels) {
-          const int64_t y = a.labels[row];
-          valid = y != a.ignore;
-          bad = valid && (y < 0 || y >= V);
-          if (valid && !bad) {
-            st.zys = ld1<T>(zs + y);
-            if (HAS_T) st.zyt = ld1<T>(zt + y);
-          }
-        }
-        const float mass = a.topk ? a.mass[row] : 0.f, ent = a.topk ? a.ent[row] : 0.f;
-        const RowOut o = finalize(st, c, a.variant, HAS_T, a.topk, mass, ent);
-        const float nan = __int_as_float(0x7fc00000);
-        if (a.ce_s) a.ce_s[row] = !valid ? 0.f : (bad ? nan : o.ce_s);
-        if (a.ce_t) a.ce_t[row] = !valid ? 0.f : (bad ? nan : o.ce_t);
-        if (a.kl && passes == 1) a.kl[row] = valid ? o.kl : 0.f;
-        float4* s4 = reinterpret_cast<float4*>(a.stats + row * KD_STATS_PER_TOKEN);
-        s4[0] = make_float4(o.lse_s1, o.lse_sT, o.lse_t1, o.lse_tT);
-        s4[1] = make_float4(o.kl_rev, 0.f, mass, o.dlse);
+        const RowOut o = finish_row<T, HAS_T>(a, row, st, false);
         R.bcast[0] = o.dlse;
         R.bcast[1] = o.lse_tT;
       }
-      if (passes == 2) {  // skew-JS: second sweep once both normalisers are known
-        ptx::named_sync(1, kCT);
-        const float dlse = R.bcast[0], lse_tT = R.bcast[1];
-        float jq = 0.f, jp = 0.f;
-        for (int64_t ch = 0; ch < nch; ++ch) {
-          const uint8_t* buf = cur.acquire(R, status);
-          const int64_t e0 = ch * EPC + (int64_t)ct * EPT;
-          const int nv = valid_cols(V - e0, EPT);
-          float fs[EPT], ft[EPT];
-          if (nv > 0) {
-            Chunk<T>::load(buf, ct, fs);
-            Chunk<T>::load(buf + kChunk, ct, ft);
+      ptx::named_sync(1, kCT);
+      const float dlse = R.bcast[0], lse_tT = R.bcast[1];
+      float jq = 0.f, jp = 0.f;
+      for (int ch = 0; ch < nch; ++ch) {
+        const uint8_t* buf = cur.acquire(R, status);
+        float fs[kSlots][EPT], ft[kSlots][EPT];
+        int nv[kSlots];
+#pragma unroll
+        for (int j = 0; j < kSlots; ++j) {
+          const int slot = j * kCT + ct;
+          nv[j] = valid_cols(V - (ch * EPC + slot * EPT), EPT);
+          if (nv[j] > 0) {
+            Chunk<T>::load(buf, slot, fs[j]);
+            Chunk<T>::load(buf + kChunk, slot, ft[j]);
           }
-          cur.release(R);
+        }
+        cur.release(R);
+#pragma unroll
+        for (int j = 0; j < kSlots; ++j)
 #pragma unroll
           for (int u = 0; u < EPT; ++u)
-            if (u < nv) js_terms(fs[u], ft[u], lse_tT, dlse, c, jq, jp);
-        }
-        const float2 r = consumer_sum2(jq, jp, R);
-        if (ct == 0) {
-          const bool v_ok = !a.labels || a.labels[row] != a.ignore;
-          a.stats[row * KD_STATS_PER_TOKEN + S_KL_PM] = r.y;
-          if (a.kl) a.kl[row] = v_ok ? (1.f - c.beta) * r.x + c.beta * r.y : 0.f;
-        }
+            if (u < nv[j]) js_terms(fs[j][u], ft[j][u], lse_tT, dlse, c, jq, jp);
+      }
+      const float2 r = consumer_sum2(jq, jp, R);
+      if (ct == 0) {
+        const bool v_ok = !a.labels || a.labels[row] != a.ignore;
+        a.stats[row * KD_STATS_PER_TOKEN + S_KL_PM] = r.y;
+        if (a.kl) a.kl[row] = v_ok ? (1.f - c.beta) * r.x + c.beta * r.y : 0.f;
       }
       ptx::named_sync(1, kCT);  // reduction slots are reused by the next row
     }
@@ -307,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd(StreamArgs a, uint32_t* sta
   __syncthreads();
 }
 
-// Backward.  Grad: row(a, row) once per row; static load(Frag&, buf, ct);
+// Backward.  Grad: row(a, row) once per row; static load(Frag&, buf, slot);
 // chunk(const Frag&, e0, nv, dz_row) writes the d z_s of one 16-byte slot.
 template <typename T, bool HAS_T, class Grad>
 __global__ void __launch_bounds__(kThreads, 1) k_bwd(StreamArgs a, uint32_t* status) {
@@ -319,21 +383,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd(StreamArgs a, uint32_t* sta
   } else {
     constexpr int EPT = 16 / (int)sizeof(T);
     constexpr int EPC = kChunk / (int)sizeof(T);
-    const int64_t V = a.vocab, nch = (V + EPC - 1) / EPC;
+    const int V = (int)a.vocab, nch = (V + EPC - 1) / EPC;
     const int ct = threadIdx.x;
     Cursor cur;
     for (int64_t row = blockIdx.x; row < a.n; row += gridDim.x) {
       Grad g;
       g.row(a, row);
-      T* dz = static_cast<T*>(a.dz) + row * V;
-      for (int64_t ch = 0; ch < nch; ++ch) {
+      T* dz = static_cast<T*>(a.dz) + row * a.vocab;
+      for (int ch = 0; ch < nch; ++ch) {
         const uint8_t* buf = cur.acquire(R, status);
-        const int64_t e0 = ch * EPC + (int64_t)ct * EPT;
-        const int nv = valid_cols(V - e0, EPT);
-        typename Grad::Frag f;
-        if (nv > 0) Grad::load(f, buf, ct);
+        typename Grad::Frag f[kSlots];
+        int nv[kSlots], e0[kSlots];
+#pragma unroll
+        for (int j = 0; j < kSlots; ++j) {
+          const int slot = j * kCT + ct;
+          e0[j] = ch * EPC + slot * EPT;
+          nv[j] = valid_cols(V - e0[j], EPT);
+          if (nv[j] > 0) Grad::load(f[j], buf, slot);
+        }
         cur.release(R);
-        if (nv > 0) g.chunk(f, e0, nv, dz);
+#pragma unroll
+        for (int j = 0; j < kSlots; ++j)
+          if (nv[j] > 0) g.chunk(f[j], e0[j], nv[j], dz);
       }
     }
   }

@@ -213,9 +213,13 @@ struct GenericAcc {
     if (HAS_T) ring::Chunk<T>::load(buf + ring::kChunk, ct, f.t);
   }
   __device__ void init() { st.init(); }
-  __device__ void step(const Frag& f, int nv, const Consts& c) {
-    if (nv == EPT) update<EPT, HAS_T, false>(st, f.s, f.t, EPT, c);
-    else update<EPT, HAS_T, true>(st, f.s, f.t, nv, c);
+  __device__ void step(const Frag (&f)[ring::kSlots], const int (&nv)[ring::kSlots],
+                       const Consts& c) {
+#pragma unroll
+    for (int j = 0; j < ring::kSlots; ++j) {
+      if (nv[j] == EPT) update<EPT, HAS_T, false>(st, f[j].s, f[j].t, EPT, c);
+      else if (nv[j] > 0) update<EPT, HAS_T, true>(st, f[j].s, f[j].t, nv[j], c);
+    }
   }
   __device__ RowState fold() const { return st; }
 };
@@ -250,7 +254,7 @@ struct GenericGrad {
     y = a.labels ? a.labels[r] : -1;
     sq_s = c.pw == 2 ? ex2((2.f * sv[S_LSE_ST] - sv[S_LSE_S1]) * kL2E) : 0.f;
   }
-  __device__ void chunk(const Frag& f, int64_t e0, int nv, T* dz) {
+  __device__ void chunk(const Frag& f, int e0, int nv, T* dz) {
     float g[EPT];
 #pragma unroll
     for (int u = 0; u < EPT; ++u) {
@@ -289,7 +293,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 template <typename T>
 static void fwd_dispatch(const StreamArgs& a, cudaStream_t s) {
-  const bool vec = (a.vocab % 8 == 0) && aligned16(a.zs) && (!a.zt || aligned16(a.zt));
+  const bool vec = (a.vocab % 8 == 0) && a.vocab < (1 << 30) && aligned16(a.zs) &&
+                   (!a.zt || aligned16(a.zt));
   const unsigned grid = (unsigned)(a.n < 2147483647 ? a.n : 2147483647);
   const bool has_t = a.zt != nullptr;
   note_launch();
@@ -306,8 +311,8 @@ static void fwd_dispatch(const StreamArgs& a, cudaStream_t s) {
 
 template <typename T>
 static void bwd_dispatch(const StreamArgs& a, cudaStream_t s) {
-  const bool vec = (a.vocab % 8 == 0) && aligned16(a.zs) && (!a.zt || aligned16(a.zt)) &&
-                   aligned16(a.dz);
+  const bool vec = (a.vocab % 8 == 0) && a.vocab < (1 << 30) && aligned16(a.zs) &&
+                   (!a.zt || aligned16(a.zt)) && aligned16(a.dz);
   const int64_t per_cta = 256 * 4 * 8;
   dim3 grid((unsigned)((a.vocab + per_cta - 1) / per_cta),
             (unsigned)(a.n < 65535 ? a.n : 65535));

@@ -79,46 +79,58 @@ __device__ __forceinline__ uint32_t word(const uint4& u, int i) {
 // (e^{(z-m)/2})^2).  NEED1: labels present, so the T = 1 sums are kept.
 template <bool HAS_T, int KLM, int PW, bool NEED1>
 struct PackedAcc {
+  static constexpr int NS = ring::kSlots;  // one set of partial sums per slot
   struct Frag {
     uint4 s, t;
   };
   float ms, mt, cq, cp;
   float2 osT, otT;  // -m k_T per side (exponent offsets)
-  float2 ls1, lsT, lt1, ltT, qd, qx, pd, px;
+  float2 ls1[NS], lsT[NS], lt1[NS], ltT[NS], qd[NS], qx[NS], pd[NS], px[NS];
 
-  __device__ static void load(Frag& f, const uint8_t* buf, int ct) {
-    f.s = *reinterpret_cast<const uint4*>(buf + ct * 16);
-    if (HAS_T) f.t = *reinterpret_cast<const uint4*>(buf + ring::kChunk + ct * 16);
+  __device__ static void load(Frag& f, const uint8_t* buf, int slot) {
+    f.s = *reinterpret_cast<const uint4*>(buf + slot * 16);
+    if (HAS_T) f.t = *reinterpret_cast<const uint4*>(buf + ring::kChunk + slot * 16);
   }
   __device__ void init() {
     ms = mt = neg_inf();
     cq = cp = 0.f;
-    osT = otT = ls1 = lsT = lt1 = ltT = qd = qx = pd = px = splat(0.f);
+    osT = otT = splat(0.f);
+#pragma unroll
+    for (int j = 0; j < NS; ++j)
+      ls1[j] = lsT[j] = lt1[j] = ltT[j] = qd[j] = qx[j] = pd[j] = px[j] = splat(0.f);
   }
   // Rescale the running sums to a larger maximum (rare after a row's first
   // chunks); the same factors as update() in kd_common.cuh.
   __device__ __forceinline__ void grow(float cms, float cmt, const Consts& c) {
     bool grew = false;
     if (cms > ms) {
-      const float fT = ex2((ms - cms) * c.k_sT);
-      lsT = mul2(lsT, splat(fT));
-      if (KLM & 2) {
-        pd = mul2(pd, splat(fT));
-        px = mul2(px, splat(fT));
+      const float2 fT = splat(ex2((ms - cms) * c.k_sT));
+      const float2 f1 = splat(NEED1 ? ex2((ms - cms) * c.k_s1) : 0.f);
+#pragma unroll
+      for (int j = 0; j < NS; ++j) {
+        lsT[j] = mul2(lsT[j], fT);
+        if (KLM & 2) {
+          pd[j] = mul2(pd[j], fT);
+          px[j] = mul2(px[j], fT);
+        }
+        if (NEED1) ls1[j] = mul2(ls1[j], f1);
       }
-      if (NEED1) ls1 = mul2(ls1, splat(ex2((ms - cms) * c.k_s1)));
       ms = cms;
       osT = splat(-ms * c.k_sT);
       grew = true;
     }
     if (HAS_T && cmt > mt) {
-      const float fT = ex2((mt - cmt) * c.k_tT);
-      ltT = mul2(ltT, splat(fT));
-      if (KLM & 1) {
-        qd = mul2(qd, splat(fT));
-        qx = mul2(qx, splat(fT));
+      const float2 fT = splat(ex2((mt - cmt) * c.k_tT));
+      const float2 f1 = splat(NEED1 ? ex2((mt - cmt) * c.k_t1) : 0.f);
+#pragma unroll
+      for (int j = 0; j < NS; ++j) {
+        ltT[j] = mul2(ltT[j], fT);
+        if (KLM & 1) {
+          qd[j] = mul2(qd[j], fT);
+          qx[j] = mul2(qx[j], fT);
+        }
+        if (NEED1) lt1[j] = mul2(lt1[j], f1);
       }
-      if (NEED1) lt1 = mul2(lt1, splat(ex2((mt - cmt) * c.k_t1)));
       mt = cmt;
       otT = splat(-mt * c.k_tT);
       grew = true;
@@ -129,48 +141,69 @@ struct PackedAcc {
       cp = ex2(-dM);
     }
   }
+  template <int J>
   __device__ __forceinline__ void pair(uint32_t ws, uint32_t wt, const Consts& c) {
     const float2 s = unpack(ws);
     const float2 es = ex2x2(fma2(s, splat(c.k_sT), osT));
-    lsT = add2(lsT, es);
-    if (NEED1) ls1 = PW == 2 ? fma2(es, es, ls1) : add2(ls1, es);
+    lsT[J] = add2(lsT[J], es);
+    if (NEED1) ls1[J] = PW == 2 ? fma2(es, es, ls1[J]) : add2(ls1[J], es);
     if (HAS_T) {
       const float2 t = unpack(wt);
       const float2 et = ex2x2(fma2(t, splat(c.k_tT), otT));
-      ltT = add2(ltT, et);
-      if (NEED1) lt1 = PW == 2 ? fma2(et, et, lt1) : add2(lt1, et);
+      ltT[J] = add2(ltT[J], et);
+      if (NEED1) lt1[J] = PW == 2 ? fma2(et, et, lt1[J]) : add2(lt1[J], et);
       const float2 d = fma2(t, splat(c.inv_tt), mul2(s, splat(-c.inv_ts)));
       if (KLM & 1) {
-        qd = fma2(et, d, qd);
-        qx = add2(qx, make_float2(fmaf(es.x, cq, -et.x), fmaf(es.y, cq, -et.y)));
+        qd[J] = fma2(et, d, qd[J]);
+        qx[J] = add2(qx[J], make_float2(fmaf(es.x, cq, -et.x), fmaf(es.y, cq, -et.y)));
       }
       if (KLM & 2) {
-        pd = fma2(es, d, pd);  // sum of p d: the state keeps its negative
-        px = add2(px, make_float2(fmaf(et.x, cp, -es.x), fmaf(et.y, cp, -es.y)));
+        pd[J] = fma2(es, d, pd[J]);  // sum of p d: the state keeps its negative
+        px[J] = add2(px[J], make_float2(fmaf(et.x, cp, -es.x), fmaf(et.y, cp, -es.y)));
       }
     }
   }
-  __device__ __forceinline__ void step(const Frag& f, int, const Consts& c) {
-    const float cms = max8(f.s);
-    const float cmt = HAS_T ? max8(f.t) : neg_inf();
-    if (cms > ms || (HAS_T && cmt > mt)) grow(cms, cmt, c);
+  template <int J>
+  __device__ __forceinline__ void slot(const Frag& f, const Consts& c) {
+    pair<J>(f.s.x, HAS_T ? f.t.x : 0u, c);
+    pair<J>(f.s.y, HAS_T ? f.t.y : 0u, c);
+    pair<J>(f.s.z, HAS_T ? f.t.z : 0u, c);
+    pair<J>(f.s.w, HAS_T ? f.t.w : 0u, c);
+  }
+  // nv is 0 or 8 here (the vocabulary is a multiple of 8)
+  __device__ __forceinline__ void step(const Frag (&f)[NS], const int (&nv)[NS], const Consts& c) {
+    float cms = neg_inf(), cmt = neg_inf();
 #pragma unroll
-    for (int i = 0; i < 4; ++i) pair(word(f.s, i), HAS_T ? word(f.t, i) : 0u, c);
+    for (int j = 0; j < NS; ++j)
+      if (nv[j] > 0) {
+        cms = fmaxf(cms, max8(f[j].s));
+        if (HAS_T) cmt = fmaxf(cmt, max8(f[j].t));
+      }
+    if (cms > ms || (HAS_T && cmt > mt)) grow(cms, cmt, c);
+    static_assert(NS == 2, "one accumulator set per slot");
+    if (nv[0] > 0) slot<0>(f[0], c);
+    if (nv[1] > 0) slot<1>(f[1], c);
+  }
+  __device__ static float total(const float2 (&v)[NS]) {
+    float2 t = v[0];
+#pragma unroll
+    for (int j = 1; j < NS; ++j) t = add2(t, v[j]);
+    return hsum(t);
   }
   __device__ RowState fold() const {
     RowState st;
     st.init();
     st.ms = ms;
-    st.ls1 = hsum(ls1);
-    st.lsT = hsum(lsT);
+    st.ls1 = total(ls1);
+    st.lsT = total(lsT);
     if (HAS_T) {
       st.mt = mt;
-      st.lt1 = hsum(lt1);
-      st.ltT = hsum(ltT);
-      st.qd = hsum(qd);
-      st.qx = hsum(qx);
-      st.pd = -hsum(pd);
-      st.px = hsum(px);
+      st.lt1 = total(lt1);
+      st.ltT = total(ltT);
+      st.qd = total(qd);
+      st.qx = total(qx);
+      st.pd = -total(pd);
+      st.px = total(px);
     }
     return st;
   }
@@ -195,9 +228,9 @@ struct PackedGrad {
   float sv[KD_STATS_PER_TOKEN];  // skew-JS only
   Consts c;                      // skew-JS only
 
-  __device__ static void load(Frag& f, const uint8_t* buf, int ct) {
-    f.s = *reinterpret_cast<const uint4*>(buf + ct * 16);
-    if (HAS_T) f.t = *reinterpret_cast<const uint4*>(buf + ring::kChunk + ct * 16);
+  __device__ static void load(Frag& f, const uint8_t* buf, int slot) {
+    f.s = *reinterpret_cast<const uint4*>(buf + slot * 16);
+    if (HAS_T) f.t = *reinterpret_cast<const uint4*>(buf + ring::kChunk + slot * 16);
   }
   __device__ void row(const StreamArgs& a, int64_t r) {
     const float* st = a.stats + r * KD_STATS_PER_TOKEN;
@@ -242,13 +275,13 @@ struct PackedGrad {
     if (CE) g = fma2(PW == 2 ? mul2(p, p) : p, splat(csq), g);
     return g;
   }
-  __device__ __forceinline__ void chunk(const Frag& f, int64_t e0, int, bf16* dz) {
+  __device__ __forceinline__ void chunk(const Frag& f, int e0, int, bf16* dz) {
     uint4 out = make_uint4(0u, 0u, 0u, 0u);
     if (!zero) {
       float2 g[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) g[i] = pair(word(f.s, i), HAS_T ? word(f.t, i) : 0u);
-      if (CE && (uint64_t)(y - e0) < 8u) {  // the label column: - s_row w_sce
+      if (CE && (uint64_t)(y - (int64_t)e0) < 8u) {  // the label column: - s_row w_sce
         const int j = (int)(y - e0);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
