@@ -175,8 +175,11 @@ __device__ __forceinline__ void accum(const float* zs, const float* zt, int nval
     }
     return;
   }
-  // e^{a_s-Mt} = e^{a_s-Ms} * cq and e^{a_t-Ms} = e^{a_t-Mt} * cp
-  const bool fwd = c.kl_mode & 1, rev = c.kl_mode & 2;
+  // e^{a_s-Mt} = e^{a_s-Ms} * cq and e^{a_t-Ms} = e^{a_t-Mt} * cp.  Both
+  // directions' cross sums and (T = 1 or 2) the CE sums cost a few FMAs each,
+  // less than a branch per element, so they are always formed; finalize()
+  // reads only what the variant needs (an overflowed unused sum falls back to
+  // the log-sum-exp difference there).
 #pragma unroll
   for (int j = 0; j < NC; ++j) {
     if (!MASKED || j < nvalid) {
@@ -185,20 +188,16 @@ __device__ __forceinline__ void accum(const float* zs, const float* zt, int nval
       lsT += es;
       ltT += et;
       const float d = zt[j] * c.inv_tt - zs[j] * c.inv_ts;
-      if (fwd) {
-        qd = fmaf(et, d, qd);
-        qx += fmaf(es, cq, -et);
-      }
-      if (rev) {
-        pd = fmaf(es, -d, pd);
-        px += fmaf(et, cp, -es);
-      }
+      qd = fmaf(et, d, qd);
+      qx += fmaf(es, cq, -et);
+      pd = fmaf(es, -d, pd);
+      px += fmaf(et, cp, -es);
       if (PW == 2) {
-        if (c.need_s1) ls1 = fmaf(es, es, ls1);
-        if (c.need_t1) lt1 = fmaf(et, et, lt1);
+        ls1 = fmaf(es, es, ls1);
+        lt1 = fmaf(et, et, lt1);
       } else if (PW == 1) {
-        if (c.need_s1) ls1 += es;
-        if (c.need_t1) lt1 += et;
+        ls1 += es;
+        lt1 += et;
       }
     }
   }

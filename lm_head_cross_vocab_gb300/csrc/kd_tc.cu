@@ -412,6 +412,132 @@ struct FwdEpi {
   }
 };
 
+// Gradient epilogue.  Per row, the constants of G with the row's upstream
+// scale folded in; per 32 columns, one loop specialised on the KL form and the
+// temperature shortcut, so no branch is left in the element loop.
+//   G = wk dKL/da_s + wc (softmax(z_s) - e_y)
+// with dKL/da_s = p - q (forward), p (log p - log q - KL(p||q)) (reverse),
+// their sum (Jeffreys), b p (log(p/m) - KL(p||m)) (skew-JS), M p - p_S
+// (top-K; the sparse part is subtracted at the matched ids).
+enum GradVar { GV_FWD = 0, GV_REV = 1, GV_JEF = 2, GV_SJS = 3, GV_P = 4 };
+
+struct GradRow {
+  float ks, ns, kt, nt;  // log2 p = z_s ks + ns, log2 q = z_t kt + nt
+  float wk;              // s w_kl T_s on the KL gradient (times M for top-K, 0 without KL)
+  float wkp;             // s w_kl T_s (top-K matched-id terms)
+  float wk_r, klr;       // s w_kl T_s ln 2, s w_kl T_s KL(p||q)   (reverse terms)
+  float wc, cs, n1s;     // s w_sce; its p^2 coefficient (T = 2); -lse(z_s) log2 e
+  float wt, ct, n1t;     // tied teacher CE: s w_tce; its q^2 coefficient; -lse(z_t) log2 e
+  float bwk, dlse, klpm; // skew-JS: s w_kl T_s b; lse(a_t) - lse(a_s); KL(p||m)
+  bool live;             // row inside the chunk with a nonzero scale
+};
+
+__device__ __forceinline__ GradRow grad_row(const TcGradArgs& a, int64_t row, bool row_ok,
+                                            bool has_t) {
+  GradRow r;
+  const Consts& c = a.c;
+  float sv[KD_STATS_PER_TOKEN];
+  const float scale = row_ok ? a.row_scale[row] : 0.f;
+#pragma unroll
+  for (int i = 0; i < KD_STATS_PER_TOKEN; ++i)
+    sv[i] = row_ok ? a.stats[row * KD_STATS_PER_TOKEN + i] : 0.f;
+  r.live = scale != 0.f;
+  r.ks = c.inv_ts * kL2E;
+  r.ns = -sv[S_LSE_ST] * kL2E;
+  r.kt = c.inv_tt * kL2E;
+  r.nt = -sv[S_LSE_TT] * kL2E;
+  const float wkl = scale * a.w_kl_ts;
+  r.wkp = wkl;
+  r.wk = a.topk ? wkl * sv[S_MASS] : (has_t ? wkl : 0.f);
+  r.wk_r = wkl * 0.6931471805599453f;
+  r.klr = wkl * sv[S_KL_REV];
+  r.wc = scale * a.w_sce;
+  const int pw = c.pw;
+  r.cs = pw == 2 ? r.wc * ex2((2.f * sv[S_LSE_ST] - sv[S_LSE_S1]) * kL2E) : 0.f;
+  r.n1s = -sv[S_LSE_S1] * kL2E;
+  r.wt = scale * a.w_tce;
+  r.ct = (pw == 2 && a.gtT) ? r.wt * ex2((2.f * sv[S_LSE_TT] - sv[S_LSE_T1]) * kL2E) : 0.f;
+  r.n1t = -sv[S_LSE_T1] * kL2E;
+  r.bwk = wkl * c.beta;
+  r.dlse = sv[S_DLSE];
+  r.klpm = sv[S_KL_PM];
+  return r;
+}
+
+// vs <- G for 32 columns (vt: teacher logits of the same columns); jy: the
+// label's column within the 32, or -1.
+template <int VAR, int PW>
+__device__ __forceinline__ void grad32(float* vs, const float* vt, const GradRow& r,
+                                       const Consts& c, int jy) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float l2p = fmaf(vs[j], r.ks, r.ns);
+    const float p = ex2(l2p);
+    float g;
+    if (VAR == GV_P) {
+      g = r.wk * p;
+    } else if (VAR == GV_SJS) {
+      const float x = fmaf(vs[j], c.inv_ts, -vt[j] * c.inv_tt) + r.dlse;
+      g = r.bwk * p * (x - js_w(x, c) - r.klpm);
+    } else {
+      const float l2q = fmaf(vt[j], r.kt, r.nt);
+      if (VAR == GV_FWD) {
+        g = r.wk * (p - ex2(l2q));
+      } else {
+        const float rr = fmaf(l2p - l2q, r.wk_r, -r.klr);
+        g = VAR == GV_REV ? p * rr : fmaf(p, rr, r.wk * (p - ex2(l2q)));
+      }
+    }
+    if (PW == 2) g = fmaf(r.cs * p, p, g);
+    else if (PW == 1) g = fmaf(r.wc, p, g);
+    else g = fmaf(r.wc, ex2(fmaf(vs[j], kL2E, r.n1s)), g);
+    if (j == jy) g -= r.wc;
+    vs[j] = r.live ? g : 0.f;
+  }
+}
+
+// vt <- tied teacher-CE gradient s w_tce (softmax(z_t) - e_y) for 32 columns.
+template <int PW>
+__device__ __forceinline__ void grad32_teacher_ce(float* vt, const GradRow& r, int jy) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    float g;
+    if (PW == 2) {
+      const float q = ex2(fmaf(vt[j], r.kt, r.nt));
+      g = r.ct * q * q;
+    } else if (PW == 1) {
+      g = r.wt * ex2(fmaf(vt[j], r.kt, r.nt));
+    } else {
+      g = r.wt * ex2(fmaf(vt[j], kL2E, r.n1t));
+    }
+    if (j == jy) g -= r.wt;
+    vt[j] = r.live ? g : 0.f;
+  }
+}
+
+template <int VAR>
+__device__ __forceinline__ void grad32_pw(int pw, float* vs, const float* vt, const GradRow& r,
+                                          const Consts& c, int jy) {
+  if (pw == 2) grad32<VAR, 2>(vs, vt, r, c, jy);
+  else if (pw == 1) grad32<VAR, 1>(vs, vt, r, c, jy);
+  else grad32<VAR, 0>(vs, vt, r, c, jy);
+}
+
+template <bool HAS_T>
+__device__ __forceinline__ void grad32_any(int gv, int pw, float* vs, const float* vt,
+                                           const GradRow& r, const Consts& c, int jy) {
+  if constexpr (HAS_T) {
+    switch (gv) {
+      case GV_FWD: grad32_pw<GV_FWD>(pw, vs, vt, r, c, jy); return;
+      case GV_REV: grad32_pw<GV_REV>(pw, vs, vt, r, c, jy); return;
+      case GV_JEF: grad32_pw<GV_JEF>(pw, vs, vt, r, c, jy); return;
+      case GV_SJS: grad32_pw<GV_SJS>(pw, vs, vt, r, c, jy); return;
+      default: break;
+    }
+  }
+  grad32_pw<GV_P>(pw, vs, vt, r, c, jy);
+}
+
 // ------------------------------------------------------------------ kernel
 template <int EPI, int BN, bool HAS_T, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcParams P) {
@@ -639,25 +765,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
           const TcGradArgs& a = P.grad;
           const int64_t row = a.r0 + tile_row;
           const bool row_ok = row < a.r0 + a.rc;
-          float scale = 0.f;
-          const float* stt = nullptr;
-          int64_t y = -1;
+          const bool has_t = HAS_T && (a.t_gemm || a.t_logits);
+          const GradRow gr = grad_row(a, row, row_ok, has_t);
+          const int gv = !has_t ? GV_P
+                         : a.variant == KD_KL_FORWARD ? GV_FWD
+                         : a.variant == KD_KL_REVERSE ? GV_REV
+                         : a.variant == KD_KL_JEFFREYS ? GV_JEF
+                                                       : GV_SJS;
+          const int pw = a.c.pw;
+          const int64_t y = (row_ok && a.labels) ? a.labels[row] : -1;
           const int32_t* ids = nullptr;
           const float* ps = nullptr;
           int kp = 0;
-          float sv[KD_STATS_PER_TOKEN] = {};  // this row's saved statistics
-          if (row_ok) {
-            scale = a.row_scale[row];
-            stt = a.stats + row * KD_STATS_PER_TOKEN;
-#pragma unroll
-            for (int i = 0; i < KD_STATS_PER_TOKEN; ++i) sv[i] = stt[i];
-            if (a.labels) y = a.labels[row];
-            if (a.topk) {
-              ids = a.sidx + row * a.k;
-              ps = a.sp + row * a.k;
-              const int64_t first = a.c0 + (int64_t)t * BN + half * (BN / 2);
-              while (kp < a.k && (int64_t)ids[kp] < first) ++kp;
-            }
+          if (a.topk && row_ok) {
+            ids = a.sidx + row * a.k;
+            ps = a.sp + row * a.k;
+            const int64_t first = a.c0 + (int64_t)t * BN + half * (BN / 2);
+            while (kp < a.k && (int64_t)ids[kp] < first) ++kp;
           }
 #pragma unroll 1
           for (int cc = 0; cc < BN / 2; cc += 32) {
@@ -684,41 +808,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
               if (HAS_T && a.t_logits)
                 load_logits32(static_cast<const __nv_bfloat16*>(a.zt_logits) + row * a.vocab,
                               col0, nv, P.logits_vec, vt);
-              float g[32], gt[32];
-              const bool want_gt = a.gtT != nullptr;
-              const int pw = a.c.pw;
-              // e^{2 lse(z/2) - lse(z)}: turns p^2 into softmax(z) when T = 2
-              const float sq_s = pw == 2 ? ex2((2.f * sv[S_LSE_ST] - sv[S_LSE_S1]) * kL2E) : 0.f;
-              const float sq_t = pw == 2 ? ex2((2.f * sv[S_LSE_TT] - sv[S_LSE_T1]) * kL2E) : 0.f;
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                float gg = 0.f, gtt = 0.f;
-                if (scale != 0.f) {
-                  const float lp = fmaf(vs[j], a.c.inv_ts, -sv[S_LSE_ST]);
-                  const float p = ex2(lp * kL2E);
-                  float q = 0.f;
-                  if (HAS_T) {
-                    const float lq = fmaf(vt[j], a.c.inv_tt, -sv[S_LSE_TT]);
-                    q = ex2(lq * kL2E);
-                    gg = a.w_kl_ts * kl_grad_pq(vs[j], vt[j], lp, lq, p, q, sv, a.variant, a.c);
-                  } else if (a.topk) {
-                    gg = a.w_kl_ts * sv[S_MASS] * p;
-                  }
-                  const float ey = (col0 + j == y) ? 1.f : 0.f;
-                  if (a.w_sce != 0.f)
-                    gg = fmaf(a.w_sce, softmax_t1(vs[j], p, sv[S_LSE_S1], sq_s, pw) - ey, gg);
-                  gg *= scale;
-                  if (HAS_T && want_gt)
-                    gtt = scale * a.w_tce * (softmax_t1(vt[j], q, sv[S_LSE_T1], sq_t, pw) - ey);
-                }
-                g[j] = gg;
-                gt[j] = gtt;
+              const int jy = (y >= col0 && y < col0 + 32) ? (int)(y - col0) : -1;
+              // G in place over vs first (it reads vt), then the tied
+              // teacher-CE gradient in place over vt
+              float* g = vs;
+              grad32_any<HAS_T>(gv, pw, g, vt, gr, a.c, jy);
+              const bool want_gt = HAS_T && a.gtT != nullptr;
+              if (want_gt) {
+                if (pw == 2) grad32_teacher_ce<2>(vt, gr, jy);
+                else if (pw == 1) grad32_teacher_ce<1>(vt, gr, jy);
+                else grad32_teacher_ce<0>(vt, gr, jy);
               }
-              if (ids && scale != 0.f) {
+              if (ids && gr.live) {
                 while (kp < a.k && (int64_t)ids[kp] < col0) ++kp;
                 while (kp < a.k && (int64_t)ids[kp] < col0 + nv) {
                   const int jj = (int)(ids[kp] - col0);
-                  const float sub = scale * a.w_kl_ts * ps[kp];
+                  const float sub = gr.wkp * ps[kp];
 #pragma unroll
                   for (int i = 0; i < 32; ++i)
                     if (i == jj) g[i] -= sub;
@@ -749,11 +854,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
                 for (int j = 0; j < 32; ++j)
                   if (j < nv) gcol[(int64_t)j * a.ldgt] = __float2bfloat16(g[j]);
               }
-              if (HAS_T && want_gt) {
+              if (want_gt) {
                 __nv_bfloat16* gcol = a.gtT + lc0 * a.ldgt + (row - a.r0);
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                  if (j < nv) gcol[(int64_t)j * a.ldgt] = __float2bfloat16(gt[j]);
+                  if (j < nv) gcol[(int64_t)j * a.ldgt] = __float2bfloat16(vt[j]);
               }
             }
           }
