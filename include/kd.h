@@ -56,7 +56,7 @@
 extern "C" {
 #endif
 
-#define KD_ABI_VERSION 1
+#define KD_ABI_VERSION 2
 
 typedef enum kd_status {
   KD_OK = 0,
@@ -206,13 +206,16 @@ int kd_device_supported(int device);
 int kd_abi_version(void);
 
 /* Diagnostic for validating the tensor-core GEMM core on its own (not part of
- * the loss): C[M, N] = A[M, K] B[N, K]^T with bf16 A, B (row-major, K
- * contiguous, K a multiple of 8, 16-byte aligned) and fp32 C (row-major,
- * pitch N), accumulated in fp32 on tcgen05 tensor cores.  Device pointers,
- * asynchronous on `stream`.  This is the operation the backward applies to
- * form dH = G W and dW = G^T H from a gradient chunk G. */
+ * the loss): C[M, N] = sum_k A(m, k) B(n, k) with bf16 operands and fp32 C
+ * (row-major, pitch N), accumulated in fp32 on tcgen05 tensor cores.
+ * `layout` bit 0 clear: A stored [M, K] (K contiguous); set: A stored [K, M]
+ * (M contiguous).  Bit 1 likewise for B: [N, K] or [K, N].  The contiguous
+ * extent of each stored operand must be a multiple of 8 and the pointers
+ * 16-byte aligned.  Device pointers, asynchronous on `stream`.  The backward
+ * forms dH = G W (G [R, C] as stored, W^T: layout 0) and dW = G^T H (G as
+ * stored, H^T: layout 1) this way. */
 kd_status kd_diag_gemm_bf16(const void* a, const void* b, float* c, int64_t m, int64_t n,
-                            int64_t k, void* stream);
+                            int64_t k, int layout, void* stream);
 
 /* Size of the fixed device scratch array used by kd_fwd_static_scratch. */
 #define KD_STATIC_SCRATCH_BYTES ((size_t)32 << 20)

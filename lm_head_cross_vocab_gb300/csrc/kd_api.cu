@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cmath>
 #include <cstring>
 
@@ -61,9 +62,10 @@ struct Plan {
   // forward workspace
   size_t f_count, f_ce_s, f_ce_t, f_kl, f_stats, f_part, f_sidx, f_sp, f_mass, f_ent, f_bytes;
   // backward workspace
-  size_t b_count, b_scale, b_sidx, b_sp, b_mass, b_ent, b_wt, b_hst, b_htt, b_g, b_gT, b_gtT,
-      b_dh, b_dw, b_bytes;
+  size_t b_count, b_scale, b_sidx, b_sp, b_mass, b_ent, b_g, b_gt, b_wt, b_hst, b_htt, b_dh,
+      b_dw, b_bytes;
   int64_t ldv, ldn;  // pitches of W^T [D, ldv] and H^T [D, ldn]
+  bool kmajor_b;     // backward GEMMs take W^T / H^T (transposed per backward) as B
 };
 
 bool finite_nonneg(float x) { return std::isfinite(x) && x >= 0.f; }
@@ -183,11 +185,12 @@ int choose_splits(int64_t m_tiles, int64_t n_tiles, int nsm) {
 // row chunk the fp32 dW accumulator, plus a fixed cost per chunk.  A chunk
 // holds at most budget_elems elements and never more than N*V/8, so no
 // (tokens x vocab) matrix is ever allocated.
-void choose_chunk(const kd_problem* p, int64_t budget_elems, int64_t col_quant, int64_t& R,
-                  int64_t& C) {
+void choose_chunk(const kd_problem* p, int64_t budget_elems, int64_t col_quant, int64_t cap_div,
+                  int64_t& R, int64_t& C) {
   const int64_t n = std::max<int64_t>(p->n_tokens, 1), v = p->vocab;
   const int64_t d = p->student == KD_STUDENT_HIDDEN ? p->d_student : 1;
-  const int64_t cap = std::max<int64_t>(col_quant * 128, std::min<int64_t>(budget_elems, n * v / 8));
+  const int64_t cap =
+      std::max<int64_t>(col_quant * 128, std::min<int64_t>(budget_elems, n * v / cap_div));
   int64_t best_r = 128, best_c = col_quant;
   double best = 1e300;
   for (int64_t r = round_up(n, 128);; r = round_up(r / 2, 128)) {
@@ -207,6 +210,9 @@ void choose_chunk(const kd_problem* p, int64_t budget_elems, int64_t col_quant, 
   }
   R = std::min<int64_t>(best_r, round_up(n, 128));
   C = std::min<int64_t>(best_c, round_up(v, col_quant));
+  // same number of chunks, sizes evened out (no small last chunk)
+  if (p->seq_chunk <= 0) R = std::min(R, round_up(cdiv(n, cdiv(n, R)), 128));
+  if (p->vocab_chunk <= 0) C = std::min(C, round_up(cdiv(v, cdiv(v, C)), col_quant));
 }
 
 kd_status make_plan(const kd_problem* p, bool has_labels, Plan& P) {
@@ -274,24 +280,35 @@ kd_status make_plan(const kd_problem* p, bool has_labels, Plan& P) {
     P.b_ent = b.take(n * 4);
   }
   if (P.path == PATH_TC) {
-    choose_chunk(p, (int64_t)64 << 20, 256, P.R, P.C);
-    P.ldv = round_up(v, 8);
-    P.ldn = round_up(n, 8);
+    // Two bf16 gradient chunks (the producer fills one while the GEMMs read
+    // the other), each at most N*V/4 elements (N*V/8 with a tied teacher-CE
+    // chunk beside it): never more than half a bf16 (tokens x vocab) matrix.
+    const bool tce = P.tied && p->w_teacher_ce != 0.f;
+    choose_chunk(p, (int64_t)64 << 20, 256, tce ? 8 : 4, P.R, P.C);
     if (P.s_gemm) {
-      P.b_wt = b.take(P.ds * P.ldv * 2);               // W_s^T
-      P.b_hst = b.take(P.ds * P.ldn * 2);              // H_s^T
-      if (P.tied) P.b_htt = b.take(P.ds * P.ldn * 2);  // H_t^T
-      // two gradient chunks: the producer fills one while the GEMMs read the other
+      // The tensor cores read an MN-major B operand about 6 % slower than a
+      // K-major one.  Transposing W and H once per backward moves
+      // 4 D (V + N) bytes against that 6 % of 4 N V D GEMM FLOPs, so it pays
+      // when N V / (N + V) is large (measured on GB300: 3.6k -> read W and H
+      // as stored, 27k -> transpose).
+      P.kmajor_b = (double)n * v / (double)(n + v) > 4096.0;
+      if (const char* e = getenv("KD_TC_KMAJOR_B")) P.kmajor_b = e[0] == '1';  // debug override
+      P.ldv = round_up(v, 8);
+      P.ldn = round_up(n, 8);
+      if (P.kmajor_b) {
+        P.b_wt = b.take(P.ds * P.ldv * 2);            // W_s^T (B operand of dH)
+        P.b_hst = b.take(P.ds * P.ldn * 2);           // H_s^T (B operand of dW)
+        if (tce) P.b_htt = b.take(P.ds * P.ldn * 2);  // H_t^T
+      }
       P.b_g = b.take(2 * P.R * P.C * 2);
-      P.b_gT = b.take(2 * P.C * P.R * 2);
-      if (P.tied) P.b_gtT = b.take(2 * P.C * P.R * 2);
+      if (tce) P.b_gt = b.take(2 * P.R * P.C * 2);
       if (cdiv(v, P.C) > 1) P.b_dh = b.take(n * P.ds * 4);
       if (cdiv(n, P.R) > 1) P.b_dw = b.take(v * P.ds * 4);
     }
   } else if (P.path == PATH_SIMT) {
-    choose_chunk(p, (int64_t)8 << 20, 64, P.R, P.C);
+    choose_chunk(p, (int64_t)8 << 20, 64, 8, P.R, P.C);
     P.b_g = b.take(P.R * P.C * 4);
-    if (P.tied) P.b_gT = b.take(P.R * P.C * 4);  // teacher-CE gradient tile
+    if (P.tied) P.b_gt = b.take(P.R * P.C * 4);  // teacher-CE gradient tile
   }
   P.b_bytes = b.off;
   return KD_OK;
@@ -644,7 +661,7 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
   const int64_t nr = cdiv(n, R), nc = cdiv(v, C);
   if (P.path == PATH_SIMT) {
     float* g = at<float>(workspace, P.b_g);
-    float* gt = w_tce != 0.f ? at<float>(workspace, P.b_gT) : nullptr;
+    float* gt = w_tce != 0.f ? at<float>(workspace, P.b_gt) : nullptr;
     const int64_t D = P.ds;
     prof_record(2, s);
     for (int64_t ri = 0; ri < nr; ++ri) {
@@ -702,21 +719,19 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
   // ---------------------------------------------------------------- tcgen05
   const int64_t D = P.ds;
   __nv_bfloat16* g = P.s_gemm ? at<__nv_bfloat16>(workspace, P.b_g) : nullptr;
-  __nv_bfloat16* gT = P.s_gemm ? at<__nv_bfloat16>(workspace, P.b_gT) : nullptr;
-  __nv_bfloat16* gtT = w_tce != 0.f ? at<__nv_bfloat16>(workspace, P.b_gtT) : nullptr;
-  __nv_bfloat16* wT = P.s_gemm ? at<__nv_bfloat16>(workspace, P.b_wt) : nullptr;
-  __nv_bfloat16* hsT = P.s_gemm ? at<__nv_bfloat16>(workspace, P.b_hst) : nullptr;
-  __nv_bfloat16* htT = (P.tied && P.s_gemm) ? at<__nv_bfloat16>(workspace, P.b_htt) : nullptr;
+  __nv_bfloat16* gt = (w_tce != 0.f && P.s_gemm) ? at<__nv_bfloat16>(workspace, P.b_gt) : nullptr;
+  const bool kb = P.s_gemm && P.kmajor_b;
+  __nv_bfloat16* wT = (kb && d_h_s) ? at<__nv_bfloat16>(workspace, P.b_wt) : nullptr;
+  __nv_bfloat16* hsT = (kb && d_w_s) ? at<__nv_bfloat16>(workspace, P.b_hst) : nullptr;
+  __nv_bfloat16* htT = (kb && gt && d_w_s) ? at<__nv_bfloat16>(workspace, P.b_htt) : nullptr;
+  if (wT)
+    launch_transpose_bf16(static_cast<const __nv_bfloat16*>(in->w_s), v, D, D, wT, P.ldv, s);
+  if (hsT)
+    launch_transpose_bf16(static_cast<const __nv_bfloat16*>(in->h_s), n, D, D, hsT, P.ldn, s);
+  if (htT)
+    launch_transpose_bf16(static_cast<const __nv_bfloat16*>(in->h_t), n, D, D, htT, P.ldn, s);
   float* dh_acc = (P.s_gemm && nc > 1) ? at<float>(workspace, P.b_dh) : nullptr;
   float* dw_acc = (P.s_gemm && nr > 1) ? at<float>(workspace, P.b_dw) : nullptr;
-  if (P.s_gemm) {
-    const __nv_bfloat16* Ws = static_cast<const __nv_bfloat16*>(in->w_s);
-    const __nv_bfloat16* Hs = static_cast<const __nv_bfloat16*>(in->h_s);
-    if (d_h_s) launch_transpose_bf16(Ws, v, D, D, wT, P.ldv, s);
-    if (d_w_s) launch_transpose_bf16(Hs, n, D, D, hsT, P.ldn, s);
-    if (gtT)
-      launch_transpose_bf16(static_cast<const __nv_bfloat16*>(in->h_t), n, D, D, htT, P.ldn, s);
-  }
   prof_record(2, s);
   // Two-stream schedule: gradient chunk k is produced on the caller's stream
   // into buffer k%2 while the dH / dW GEMMs of chunk k-1 run on a side
@@ -737,8 +752,7 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
       const int64_t c0 = ci * C, cc = std::min(C, v - c0);
       const int buf = (int)(k & 1);
       __nv_bfloat16* gk = g ? g + (size_t)buf * R * C : nullptr;
-      __nv_bfloat16* gTk = gT ? gT + (size_t)buf * R * C : nullptr;
-      __nv_bfloat16* gtTk = gtT ? gtT + (size_t)buf * R * C : nullptr;
+      __nv_bfloat16* gtk = gt ? gt + (size_t)buf * R * C : nullptr;
       if (ss && k >= 2 && cudaStreamWaitEvent(s, ss->consumed[buf], 0) != cudaSuccess)
         return KD_ERR_CUDA;
       TcGradArgs a;
@@ -777,27 +791,34 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
       if (P.s_logits) {  // logit students: G is the requested d z_s itself
         a.g = static_cast<__nv_bfloat16*>(d_logits_s) + c0;
         a.ldg = v;
-        a.gT = nullptr;
+        a.gt = nullptr;
       } else {
         a.g = gk;
         a.ldg = C;
-        a.gT = d_w_s ? gTk : nullptr;
+        a.gt = gtk;
       }
-      a.ldgt = R;
-      a.gtT = gtTk;
       a.status = dev_status;
       if (launch_tc_grad(a, P.nsm, s) != 0) return KD_ERR_CUDA;
       if (P.s_logits) continue;
       if (cudaEventRecord(ss->ready[buf], s) != cudaSuccess ||
           cudaStreamWaitEvent(s2, ss->ready[buf], 0) != cudaSuccess)
         return KD_ERR_CUDA;
+      // dW = G^T H reads G as stored, as an MN-major A (full rate): no
+      // transposed copy of a gradient chunk is made.  B is W^T / H^T from the
+      // transposes above, or W / H as stored (MN-major) when those don't pay.
       if (d_h_s) {  // dH[r0.., :] (+)= G[:, chunk] W[chunk, :]
         TcGemmArgs m;
         memset(&m, 0, sizeof(m));
         m.a0 = gk;
         m.lda0 = C;
-        m.b0 = wT + c0;
-        m.ldb0 = P.ldv;
+        if (wT) {
+          m.b0 = wT + c0;
+          m.ldb0 = P.ldv;
+        } else {
+          m.b0 = static_cast<const __nv_bfloat16*>(in->w_s) + c0 * D;
+          m.ldb0 = D;
+          m.b0_mn = 1;
+        }
         m.M = rc;
         m.N = D;
         m.K0 = cc;
@@ -817,18 +838,32 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
       if (d_w_s) {  // dW[chunk, :] (+)= G[:, chunk]^T H[r0.., :] (+ G_t^T H_t)
         TcGemmArgs m;
         memset(&m, 0, sizeof(m));
-        m.a0 = gTk;
-        m.lda0 = R;
-        m.b0 = hsT + r0;
-        m.ldb0 = P.ldn;
+        m.a0 = gk;
+        m.lda0 = C;
+        m.a0_mn = 1;
+        if (hsT) {
+          m.b0 = hsT + r0;
+          m.ldb0 = P.ldn;
+        } else {
+          m.b0 = static_cast<const __nv_bfloat16*>(in->h_s) + r0 * D;
+          m.ldb0 = D;
+          m.b0_mn = 1;
+        }
         m.M = cc;
         m.N = D;
         m.K0 = rc;
-        if (gtTk) {
-          m.a1 = gtTk;
-          m.lda1 = R;
-          m.b1 = htT + r0;
-          m.ldb1 = P.ldn;
+        if (gtk) {
+          m.a1 = gtk;
+          m.lda1 = C;
+          m.a1_mn = 1;
+          if (htT) {
+            m.b1 = htT + r0;
+            m.ldb1 = P.ldn;
+          } else {
+            m.b1 = static_cast<const __nv_bfloat16*>(in->h_t) + r0 * D;
+            m.ldb1 = D;
+            m.b1_mn = 1;
+          }
           m.K1 = rc;
         }
         m.status = dev_status;
@@ -870,8 +905,10 @@ uint64_t kd_launch_count(void) { return g_launches.load(std::memory_order_relaxe
 
 // Diagnostic: C[M, N] = A[M, K] B[N, K]^T on the tensor-core GEMM core.
 kd_status kd_diag_gemm_bf16(const void* a, const void* b, float* c, int64_t m, int64_t n,
-                            int64_t k, void* stream) {
-  if (!a || !b || !c || m < 1 || n < 1 || k < 1 || (k % 8) || !aligned16(a) || !aligned16(b))
+                            int64_t k, int layout, void* stream) {
+  const int a_mn = layout & 1, b_mn = (layout >> 1) & 1;
+  if (!a || !b || !c || m < 1 || n < 1 || k < 1 || (layout & ~3) || !aligned16(a) ||
+      !aligned16(b) || ((a_mn ? m : k) % 8) || ((b_mn ? n : k) % 8))
     return KD_ERR_INVALID_ARG;
   kd_status st = check_device();
   if (st != KD_OK) return st;
@@ -879,8 +916,10 @@ kd_status kd_diag_gemm_bf16(const void* a, const void* b, float* c, int64_t m, i
   memset(&g, 0, sizeof(g));
   g.a0 = static_cast<const __nv_bfloat16*>(a);
   g.b0 = static_cast<const __nv_bfloat16*>(b);
-  g.lda0 = k;
-  g.ldb0 = k;
+  g.lda0 = a_mn ? m : k;
+  g.ldb0 = b_mn ? n : k;
+  g.a0_mn = a_mn;
+  g.b0_mn = b_mn;
   g.M = m;
   g.N = n;
   g.K0 = k;

@@ -215,30 +215,67 @@ void launch_row_scale(const int64_t* labels, int64_t n, int64_t ignore, float gr
 }
 
 // ---------------------------------------------------------------- transpose
-// 64x64 tiles through shared memory, 256 threads.
-__global__ void k_transpose_bf16(const __nv_bfloat16* __restrict__ src, int64_t rows,
-                                 int64_t cols, int64_t lds, __nv_bfloat16* __restrict__ dst,
-                                 int64_t ldd) {
-  __shared__ __nv_bfloat16 t[64][66];
+// 64 x 64 tiles, 256 threads.  Rows come in as 16-byte vectors (a warp reads
+// 4 rows x 128 bytes), go through shared memory, and leave as 16-byte vectors
+// of 8 transposed elements; a warp gathers 32 consecutive columns of one row
+// group, so neither shared-memory phase has bank conflicts.  Ragged edges and
+// unaligned pitches take element-wise accesses.
+__global__ void __launch_bounds__(256) k_transpose_bf16(const uint16_t* __restrict__ src,
+                                                        int64_t rows, int64_t cols, int64_t lds,
+                                                        uint16_t* __restrict__ dst, int64_t ldd,
+                                                        int vec) {
+  __shared__ __align__(16) uint16_t t[64][72];
   const int64_t r0 = (int64_t)blockIdx.y * 64, c0 = (int64_t)blockIdx.x * 64;
-  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // ty in [0, 4)
-  for (int i = ty; i < 64; i += 4) {
-    const int64_t r = r0 + i, c = c0 + tx;
-    t[i][tx] = (r < rows && c < cols) ? src[r * lds + c] : __float2bfloat16(0.f);
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int row = tid / 8 + 32 * k, cg = tid % 8;
+    const int64_t r = r0 + row, c = c0 + 8 * cg;
+    if (vec && r < rows && c + 8 <= cols) {
+      *reinterpret_cast<uint4*>(&t[row][8 * cg]) =
+          *reinterpret_cast<const uint4*>(src + r * lds + c);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        t[row][8 * cg + i] = (r < rows && c + i < cols) ? src[r * lds + c + i] : (uint16_t)0;
+    }
   }
   __syncthreads();
-  for (int i = ty; i < 64; i += 4) {
-    const int64_t c = c0 + i, r = r0 + tx;
-    if (c < cols && r < rows) dst[c * ldd + r] = t[tx][i];
+  const int oc = tid % 32;  // column of the tile = row of the output
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int ocol = oc + 32 * k;        // tile column -> output row c0 + ocol
+    const int rg = tid / 32;             // rows 8 rg .. 8 rg + 7 -> output columns
+    const int64_t orow = c0 + ocol, ocol0 = r0 + 8 * rg;
+    if (orow >= cols) continue;
+    uint16_t e[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) e[i] = t[8 * rg + i][ocol];
+    if (vec && ocol0 + 8 <= rows) {
+      uint4 u;
+      u.x = e[0] | ((uint32_t)e[1] << 16);
+      u.y = e[2] | ((uint32_t)e[3] << 16);
+      u.z = e[4] | ((uint32_t)e[5] << 16);
+      u.w = e[6] | ((uint32_t)e[7] << 16);
+      *reinterpret_cast<uint4*>(dst + orow * ldd + ocol0) = u;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (ocol0 + i < rows) dst[orow * ldd + ocol0 + i] = e[i];
+    }
   }
 }
 
 void launch_transpose_bf16(const __nv_bfloat16* src, int64_t rows, int64_t cols, int64_t lds,
                            __nv_bfloat16* dst, int64_t ldd, cudaStream_t s) {
   if (rows <= 0 || cols <= 0) return;
+  const int vec = (lds % 8) == 0 && (ldd % 8) == 0 &&
+                  (reinterpret_cast<uintptr_t>(src) & 15) == 0 &&
+                  (reinterpret_cast<uintptr_t>(dst) & 15) == 0;
   dim3 grid((unsigned)((cols + 63) / 64), (unsigned)((rows + 63) / 64));
   note_launch();
-  k_transpose_bf16<<<grid, 256, 0, s>>>(src, rows, cols, lds, dst, ldd);
+  k_transpose_bf16<<<grid, 256, 0, s>>>(reinterpret_cast<const uint16_t*>(src), rows, cols, lds,
+                                        reinterpret_cast<uint16_t*>(dst), ldd, vec);
 }
 
 }  // namespace kd

@@ -165,20 +165,21 @@ struct TcGradArgs {
   int64_t r0, rc, c0, cc;  // chunk
   __nv_bfloat16* g;        // [rc, ldg] row-major student G (or d z_s)
   int64_t ldg;
-  __nv_bfloat16* gT;       // [cc, ldgt] transposed student G, or NULL
-  int64_t ldgt;
-  __nv_bfloat16* gtT;      // [cc, ldgt] transposed tied teacher-CE G, or NULL
+  __nv_bfloat16* gt;       // [rc, ldg] row-major tied teacher-CE gradient, or NULL
   uint32_t* status;
 };
 int launch_tc_grad(const TcGradArgs& a, int num_ctas, cudaStream_t s);
 
-// Tensor-core GEMM: C[M, N] = sum_k A[M, K] B[N, K] (+ A1 B1 over K1), K-major
-// bf16 operands with row pitches lda/ldb (elements), fp32 accumulate.
+// Tensor-core GEMM: C[M, N] = sum_k A[M, K] B[N, K] (+ A1 B1 over K1); each
+// operand K-major ([M, K] / [N, K]) or, with its _mn flag, MN-major ([K, M] /
+// [K, N]); bf16 operands, ld = pitch of the stored layout in elements, fp32
+// accumulate.
 enum TcOutMode { TC_OUT_BF16 = 0, TC_OUT_F32 = 1, TC_OUT_F32_ACC = 2, TC_OUT_F32_ACC_BF16 = 3 };
 struct TcGemmArgs {
   const __nv_bfloat16 *a0, *b0, *a1, *b1;
   int64_t lda0, ldb0, lda1, ldb1;
   int64_t M, N, K0, K1;    // K1 = 0: single segment
+  int a0_mn, b0_mn, a1_mn, b1_mn;
   int mode;
   float* c32;              // fp32 accumulator / output [M, ldc32]
   int64_t ldc32;

@@ -7,12 +7,12 @@
 //             instead be streamed from materialised logits) -> partial record
 //             per (row, vocabulary split, half tile)
 //   EPI_GRAD  recomputed logits tile(s) -> closed-form gradient G (bf16),
-//             written row-major (feeds dH = G W) and transposed (feeds
-//             dW = G^T H) into a bounded chunk workspace
+//             written row-major into a bounded chunk workspace (dH = G W and
+//             dW = G^T H read it as stored)
 //             (Full-Chunked-KL-Loss README, "Full Chunked KL": the backward
 //             recomputes each chunk and applies M softmax(z) - p)
 //   EPI_GEMM  plain C = A B^T with an fp32 / bf16 / accumulate epilogue
-//             (dH and dW from the G chunks)
+//             (dH and dW from the G chunks); each operand K-major or MN-major
 //
 // Roles (320 threads): warp 0 issues TMA loads into a STAGES-deep shared
 // memory ring; warp 1 owns the TMEM allocation (512 columns: one or two
@@ -221,7 +221,23 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
   d |= (uint64_t)2 << 61;             // 128-byte swizzle
   return d;
 }
-// Instruction descriptor: kind::f16 with bf16 A/B, fp32 D, K-major A and B.
+// Shared-memory matrix descriptor of an MN-major operand (stored [K, M] or
+// [K, N], M / N contiguous), staged as 64 x 64 TMA boxes with 128-byte swizzle:
+// each box holds 64 k-rows of 128 bytes (64 consecutive M / N elements); boxes
+// for successive 64-element blocks of M / N lie 8 KiB apart (leading byte
+// offset), 8-row k groups 1024 bytes apart (stride byte offset).  One K = 16
+// step advances the start by 16 rows = 2048 bytes.
+constexpr int kMnBox = 64 * 64 * 2;  // bytes of one 64 x 64 bf16 box
+__device__ __forceinline__ uint64_t smem_desc_mn(uint32_t addr) {
+  uint64_t d = (uint64_t)((addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(kMnBox >> 4) << 16;  // leading byte offset: next 64 M / N elements
+  d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset: next 8 k-rows
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// Instruction descriptor: kind::f16 with bf16 A/B, fp32 D, K-major A and B
+// (bit 15 / bit 16 set: A / B MN-major).
 __host__ __device__ constexpr uint32_t make_idesc(int m, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
          ((uint32_t)(m >> 4) << 24);
@@ -244,6 +260,7 @@ struct __align__(64) TcParams {
   int a_row0[2];      // row offset added to the A tile row coordinate
   int b_row0[2];      // row offset added to the B tile row coordinate
   int seg_accum[2];   // 1: the segment adds to an accumulator an earlier segment wrote
+  int a_mn[2], b_mn[2];  // 1: the operand is stored MN-major ([K, M] / [K, N])
   int m_tiles, n_tiles, n_splits, items;
   int acc_stride;     // TMEM columns per accumulator stage
   int acc_stages;     // 1 or 2 accumulator stages in the 512 allocated columns
@@ -412,6 +429,26 @@ struct FwdEpi {
   }
 };
 
+// 32 consecutive values of one row as bf16 (16-byte stores when aligned).
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v, int nv,
+                                              int64_t ld) {
+  if (nv == 32 && (ld % 8) == 0 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+#pragma unroll
+    for (int qv = 0; qv < 4; ++qv) {
+      uint4 u;
+      u.x = pack_bf16(v[8 * qv + 0], v[8 * qv + 1]);
+      u.y = pack_bf16(v[8 * qv + 2], v[8 * qv + 3]);
+      u.z = pack_bf16(v[8 * qv + 4], v[8 * qv + 5]);
+      u.w = pack_bf16(v[8 * qv + 6], v[8 * qv + 7]);
+      *reinterpret_cast<uint4*>(dst + 8 * qv) = u;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < nv) dst[j] = __float2bfloat16(v[j]);
+  }
+}
+
 // Gradient epilogue.  Per row, the constants of G with the row's upstream
 // scale folded in; per 32 columns, one loop specialised on the KL form and the
 // temperature shortcut, so no branch is left in the element loop.
@@ -456,7 +493,7 @@ __device__ __forceinline__ GradRow grad_row(const TcGradArgs& a, int64_t row, bo
   r.cs = pw == 2 ? r.wc * ex2((2.f * sv[S_LSE_ST] - sv[S_LSE_S1]) * kL2E) : 0.f;
   r.n1s = -sv[S_LSE_S1] * kL2E;
   r.wt = scale * a.w_tce;
-  r.ct = (pw == 2 && a.gtT) ? r.wt * ex2((2.f * sv[S_LSE_TT] - sv[S_LSE_T1]) * kL2E) : 0.f;
+  r.ct = (pw == 2 && a.gt) ? r.wt * ex2((2.f * sv[S_LSE_TT] - sv[S_LSE_T1]) * kL2E) : 0.f;
   r.n1t = -sv[S_LSE_T1] * kL2E;
   r.bwk = wkl * c.beta;
   r.dlse = sv[S_DLSE];
@@ -620,17 +657,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
               const uint32_t fb = S.full + 8 * stage;
               const int ay = P.a_row0[sg] + m_tile * C::ROWS + (int)rank * BM;
               const int by = P.b_row0[sg] + t * BN + (int)rank * C::B_ROWS;
-              if (PAIR) {
-                // both CTAs' copies complete on the leader's barrier, which
-                // expects the bytes of the whole pair
-                const uint32_t fb0 = mapa_shared(fb, 0);
-                if (leader) mbar_expect_tx(fb, C::TX_BYTES);
-                tma_load_2d_pair(sA + stage * C::A_BYTES, &P.ma[sg], fb0, kb * BK, ay);
-                tma_load_2d_pair(sB + stage * C::B_BYTES, &P.mb[sg], fb0, kb * BK, by);
+              // both CTAs' copies of a pair complete on the leader's barrier,
+              // which expects the bytes of the whole pair
+              const uint32_t fbar = PAIR ? mapa_shared(fb, 0) : fb;
+              if (!PAIR || leader) mbar_expect_tx(fb, C::TX_BYTES);
+              auto load = [&](uint32_t dst, const CUtensorMap* map, int x, int y) {
+                if (PAIR) tma_load_2d_pair(dst, map, fbar, x, y);
+                else tma_load_2d(dst, map, fbar, x, y);
+              };
+              const uint32_t dA = sA + stage * C::A_BYTES, dB = sB + stage * C::B_BYTES;
+              // only the plain GEMM takes MN-major operands
+              const bool a_mn = EPI == EPI_GEMM && P.a_mn[sg];
+              const bool b_mn = EPI == EPI_GEMM && P.b_mn[sg];
+              if (a_mn) {
+                for (int h = 0; h < BM / 64; ++h) load(dA + h * kMnBox, &P.ma[sg], ay + 64 * h, kb * BK);
               } else {
-                mbar_expect_tx(fb, C::TX_BYTES);
-                tma_load_2d(sA + stage * C::A_BYTES, &P.ma[sg], fb, kb * BK, ay);
-                tma_load_2d(sB + stage * C::B_BYTES, &P.mb[sg], fb, kb * BK, by);
+                load(dA, &P.ma[sg], kb * BK, ay);
+              }
+              if (b_mn) {
+                for (int h = 0; h < C::B_ROWS / 64; ++h)
+                  load(dB + h * kMnBox, &P.mb[sg], by + 64 * h, kb * BK);
+              } else {
+                load(dB, &P.mb[sg], kb * BK, by);
               }
             }
             __syncwarp();
@@ -664,6 +712,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
         tc_fence_after();
         for (int sg = 0; ok && sg < 2; ++sg) {
           const uint32_t d = tmem + acc * P.acc_stride + P.acc_off[sg];
+          const bool a_mn = EPI == EPI_GEMM && P.a_mn[sg];
+          const bool b_mn = EPI == EPI_GEMM && P.b_mn[sg];
+          const uint32_t idesc = C::IDESC | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16);
+          const uint32_t a_step = a_mn ? 128u : 2u;  // per K = 16, 16-byte units
+          const uint32_t b_step = b_mn ? 128u : 2u;
           for (int kb = 0; kb < P.kb[sg]; ++kb) {
             if (!warp_wait(S, S.full + 8 * stage, phase)) {
               ok = false;
@@ -671,13 +724,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
             }
             tc_fence_after();
             if (lane == 0) {
-              const uint64_t ad = smem_desc(sA + stage * C::A_BYTES);
-              const uint64_t bd = smem_desc(sB + stage * C::B_BYTES);
+              const uint32_t a_addr = sA + stage * C::A_BYTES, b_addr = sB + stage * C::B_BYTES;
+              const uint64_t ad = a_mn ? smem_desc_mn(a_addr) : smem_desc(a_addr);
+              const uint64_t bd = b_mn ? smem_desc_mn(b_addr) : smem_desc(b_addr);
 #pragma unroll
               for (int k = 0; k < BK / 16; ++k) {
                 const uint32_t accum = (kb > 0 || k > 0 || P.seg_accum[sg]) ? 1u : 0u;
-                if (PAIR) mma_bf16_pair(d, ad + 2 * k, bd + 2 * k, C::IDESC, accum);
-                else mma_bf16(d, ad + 2 * k, bd + 2 * k, C::IDESC, accum);
+                if (PAIR) mma_bf16_pair(d, ad + a_step * k, bd + b_step * k, idesc, accum);
+                else mma_bf16(d, ad + a_step * k, bd + b_step * k, idesc, accum);
               }
               if (PAIR) mma_commit_pair_both(S.empty + 8 * stage);  // frees the stage in both CTAs
               else mma_commit(S.empty + 8 * stage);
@@ -813,7 +867,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
               // teacher-CE gradient in place over vt
               float* g = vs;
               grad32_any<HAS_T>(gv, pw, g, vt, gr, a.c, jy);
-              const bool want_gt = HAS_T && a.gtT != nullptr;
+              const bool want_gt = HAS_T && a.gt != nullptr;
               if (want_gt) {
                 if (pw == 2) grad32_teacher_ce<2>(vt, gr, jy);
                 else if (pw == 1) grad32_teacher_ce<1>(vt, gr, jy);
@@ -830,36 +884,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
                   ++kp;
                 }
               }
-              // row-major G (or d z_s): 32 consecutive bf16 of this row
-              __nv_bfloat16* grow = a.g + (row - a.r0) * a.ldg + lc0;
-              if (nv == 32 && (a.ldg % 8) == 0 &&
-                  (reinterpret_cast<uintptr_t>(grow) & 15) == 0) {
-#pragma unroll
-                for (int qv = 0; qv < 4; ++qv) {
-                  uint4 u;
-                  u.x = pack_bf16(g[8 * qv + 0], g[8 * qv + 1]);
-                  u.y = pack_bf16(g[8 * qv + 2], g[8 * qv + 3]);
-                  u.z = pack_bf16(g[8 * qv + 4], g[8 * qv + 5]);
-                  u.w = pack_bf16(g[8 * qv + 6], g[8 * qv + 7]);
-                  *reinterpret_cast<uint4*>(grow + 8 * qv) = u;
-                }
-              } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                  if (j < nv) grow[j] = __float2bfloat16(g[j]);
-              }
-              if (a.gT) {
-                __nv_bfloat16* gcol = a.gT + lc0 * a.ldgt + (row - a.r0);
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                  if (j < nv) gcol[(int64_t)j * a.ldgt] = __float2bfloat16(g[j]);
-              }
-              if (want_gt) {
-                __nv_bfloat16* gcol = a.gtT + lc0 * a.ldgt + (row - a.r0);
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                  if (j < nv) gcol[(int64_t)j * a.ldgt] = __float2bfloat16(vt[j]);
-              }
+              // row-major G (or d z_s) and G_t: 32 consecutive bf16 of this row
+              store_bf16x32(a.g + (row - a.r0) * a.ldg + lc0, g, nv, a.ldg);
+              if (want_gt) store_bf16x32(a.gt + (row - a.r0) * a.ldg + lc0, vt, nv, a.ldg);
             }
           }
         } else {  // EPI_GEMM
@@ -978,6 +1005,22 @@ bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)(pitch * 2)};
   cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr),
+                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Map of an MN-major operand stored [k_rows, mn_cols] (pitch in elements),
+// read in 64 (M / N) x 64 (K) boxes.
+bool make_map_mn(CUtensorMap* m, const void* ptr, int64_t k_rows, int64_t mn_cols,
+                 int64_t pitch) {
+  if (!get_encoder()) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)mn_cols, (cuuint64_t)k_rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(pitch * 2)};
+  cuuint32_t box[2] = {64u, (cuuint32_t)BK};
   cuuint32_t estr[2] = {1, 1};
   const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr),
                               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1152,15 +1195,24 @@ int launch_tc_gemm(const TcGemmArgs& a, int num_sms, cudaStream_t s) {
   const bool pair = tc_use_pairs();
   constexpr int bn = 256;
   const int b_box = pair ? bn / 2 : bn;
-  if (!make_map(&P.ma[0], a.a0, a.M, a.K0, a.lda0, BM) ||
-      !make_map(&P.mb[0], a.b0, a.N, a.K0, a.ldb0, b_box))
+  // operand maps: K-major [rows, K] or MN-major [K, rows]
+  auto map = [&](CUtensorMap* m, const void* ptr, int64_t rows, int64_t k, int64_t ld, int box,
+                 int mn) {
+    return mn ? make_map_mn(m, ptr, k, rows, ld) : make_map(m, ptr, rows, k, ld, box);
+  };
+  if (!map(&P.ma[0], a.a0, a.M, a.K0, a.lda0, BM, a.a0_mn) ||
+      !map(&P.mb[0], a.b0, a.N, a.K0, a.ldb0, b_box, a.b0_mn))
     return fail_map();
   P.kb[0] = (int)((a.K0 + BK - 1) / BK);
+  P.a_mn[0] = a.a0_mn;
+  P.b_mn[0] = a.b0_mn;
   if (a.K1 > 0) {
-    if (!make_map(&P.ma[1], a.a1, a.M, a.K1, a.lda1, BM) ||
-        !make_map(&P.mb[1], a.b1, a.N, a.K1, a.ldb1, b_box))
+    if (!map(&P.ma[1], a.a1, a.M, a.K1, a.lda1, BM, a.a1_mn) ||
+        !map(&P.mb[1], a.b1, a.N, a.K1, a.ldb1, b_box, a.b1_mn))
       return fail_map();
     P.kb[1] = (int)((a.K1 + BK - 1) / BK);
+    P.a_mn[1] = a.a1_mn;
+    P.b_mn[1] = a.b1_mn;
     P.seg_accum[1] = 1;  // both segments sum into the same accumulator
   }
   P.acc_stride = bn;

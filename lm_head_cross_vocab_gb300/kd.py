@@ -34,6 +34,7 @@ KD_KL_FORWARD, KD_KL_REVERSE, KD_KL_JEFFREYS, KD_KL_SKEW_JS = range(4)
 KD_REDUCE_MEAN, KD_REDUCE_SUM = 0, 1
 KD_STATS_PER_TOKEN = 8
 KD_STATIC_SCRATCH_BYTES = 32 << 20
+KD_ABI_VERSION = 2  # the kd.h this binding follows
 
 DTYPES = {"bf16": KD_BF16, "fp32": KD_FP32}
 STUDENTS = {"hidden": KD_STUDENT_HIDDEN, "logits": KD_STUDENT_LOGITS}
@@ -93,7 +94,7 @@ def load_library(path: str = LIB_PATH):
     lib.kd_status_string.restype = ctypes.c_char_p
     lib.kd_device_supported.argtypes = [ctypes.c_int]
     lib.kd_diag_gemm_bf16.argtypes = [vp, vp, vp, ctypes.c_int64, ctypes.c_int64,
-                                      ctypes.c_int64, vp]
+                                      ctypes.c_int64, ctypes.c_int, vp]
     lib.kd_set_profile_events.argtypes = [vp, vp, vp, vp]
     lib.kd_plan_info.argtypes = [P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
                                  ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]
@@ -147,13 +148,19 @@ def kd_bwd(problem, inputs, stats, d_loss, grad_scale, d_h_s, d_w_s, d_logits_s,
                                      dev_status, workspace, ws_bytes, stream))
 
 
-def kd_diag_gemm_bf16(a: torch.Tensor, b: torch.Tensor) -> torch.Tensor:
-    """C = A B^T on the library's tcgen05 GEMM core (diagnostic)."""
+def kd_diag_gemm_bf16(a: torch.Tensor, b: torch.Tensor, a_kmajor: bool = True,
+                      b_kmajor: bool = True) -> torch.Tensor:
+    """C = A B^T on the library's tcgen05 GEMM core (diagnostic).  `a` is A
+    [M, K] (a_kmajor) or A^T stored [K, M]; `b` is B [N, K] or B^T stored [K, N]."""
     assert a.dtype == torch.bfloat16 and b.dtype == torch.bfloat16 and a.is_contiguous() \
-        and b.is_contiguous() and a.shape[1] == b.shape[1]
-    c = torch.empty(a.shape[0], b.shape[0], device=a.device, dtype=torch.float32)
-    st = load_library().kd_diag_gemm_bf16(a.data_ptr(), b.data_ptr(), c.data_ptr(), a.shape[0],
-                                          b.shape[0], a.shape[1], _stream(a.device))
+        and b.is_contiguous()
+    m, ka = (a.shape[0], a.shape[1]) if a_kmajor else (a.shape[1], a.shape[0])
+    n, kb = (b.shape[0], b.shape[1]) if b_kmajor else (b.shape[1], b.shape[0])
+    assert ka == kb
+    c = torch.empty(m, n, device=a.device, dtype=torch.float32)
+    layout = (0 if a_kmajor else 1) | (0 if b_kmajor else 2)
+    st = load_library().kd_diag_gemm_bf16(a.data_ptr(), b.data_ptr(), c.data_ptr(), m, n, ka,
+                                          layout, _stream(a.device))
     if st != KD_OK:
         raise KDError(st, "kd_diag_gemm_bf16")
     return c

@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(kd):
 
 
 def test_abi_version_and_status_strings(kd):
-    assert kd.kd_abi_version() == 1
+    assert kd.kd_abi_version() == 2
     for code in range(9):
         s = kd.kd_status_string(code)
         assert s and s != "unknown status"
@@ -142,8 +142,9 @@ def test_backward_argument_rules(kd):
 
 
 def test_no_scratch_buffer_spans_tokens_by_vocab(kd):
-    """The backward's gradient chunk is at most an eighth of the (tokens x vocab)
-    matrix for every workload, and the forward never holds logits at all."""
+    """The backward's gradient chunk is at most a quarter of the (tokens x vocab)
+    matrix for every workload (its two bf16 buffers together at most half a bf16
+    logits matrix), and the forward never holds logits at all."""
     from lm_head_cross_vocab_gb300 import inputs as I
     for cfg in (1, 2, 3, 4, 5):
         w = I.WORKLOADS[cfg]
@@ -152,7 +153,7 @@ def test_no_scratch_buffer_spans_tokens_by_vocab(kd):
         fb, bb = kd.kd_workspace_size(p)
         full = w.n_tokens * w.vocab
         if info["path"] != 0:  # streaming path keeps no chunk
-            assert info["chunk_rows"] * info["chunk_cols"] <= max(full // 8, 128 * 256), (cfg, info)
+            assert info["chunk_rows"] * info["chunk_cols"] <= max(full // 4, 128 * 256), (cfg, info)
         assert fb < full * 2, (cfg, fb)
 
 

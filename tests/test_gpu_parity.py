@@ -115,15 +115,21 @@ def test_fp32_topk():
 
 # ----------------------------------------------------------- tcgen05 GEMM core
 
-@pytest.mark.parametrize("m,n,k", [(128, 256, 64), (300, 500, 136), (1000, 777, 1024)])
-def test_tensor_core_gemm_matches_torch(m, n, k):
+@pytest.mark.parametrize("a_kmajor,b_kmajor", [(True, True), (True, False), (False, True),
+                                                (False, False)])
+@pytest.mark.parametrize("m,n,k", [(128, 256, 64), (304, 504, 136), (1000, 776, 1024)])
+def test_tensor_core_gemm_matches_torch(m, n, k, a_kmajor, b_kmajor):
+    """GEMM core against fp64 torch for every operand layout (K-major [rows, K]
+    or MN-major [K, rows]); ragged in M, N and K."""
     g = torch.Generator(device="cpu").manual_seed(m + n + k)
-    a = torch.randn(m, k, generator=g).to(torch.bfloat16).cuda()
-    b = torch.randn(n, k, generator=g).to(torch.bfloat16).cuda()
-    c = kd.kd_diag_gemm_bf16(a, b)
+    a = torch.randn(m, k, generator=g).to(torch.bfloat16)
+    b = torch.randn(n, k, generator=g).to(torch.bfloat16)
+    a_dev = (a if a_kmajor else a.T.contiguous()).cuda()
+    b_dev = (b if b_kmajor else b.T.contiguous()).cuda()
+    c = kd.kd_diag_gemm_bf16(a_dev, b_dev, a_kmajor, b_kmajor)
     ref = a.double() @ b.double().T
     torch.cuda.synchronize()
-    assert rel_l2(c.cpu().numpy(), ref.cpu().numpy()) < 1e-5
+    assert rel_l2(c.cpu().numpy(), ref.numpy()) < 1e-5
 
 
 # ----------------------------------------------------------- tcgen05 fused paths
