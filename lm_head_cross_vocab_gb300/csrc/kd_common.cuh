@@ -153,6 +153,44 @@ __device__ __forceinline__ RowState shfl_xor(const RowState& s, int m) {
   return o;
 }
 
+// Merge the RowStates of the 32 lanes of a warp (result in every lane): the
+// maxima first, then every lane rescales its sums once to the warp maxima,
+// then plain sum reductions -- the same result as merge() over the lanes with
+// one exponential per sum instead of one per level.
+__device__ __forceinline__ void warp_merge(RowState& s, const Consts& c) {
+  float m_s = s.ms, m_t = s.mt;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    m_s = fmaxf(m_s, __shfl_xor_sync(0xffffffffu, m_s, o));
+    m_t = fmaxf(m_t, __shfl_xor_sync(0xffffffffu, m_t, o));
+  }
+  const float fs1 = rescale(s.ms, m_s, c.k_s1), fsT = rescale(s.ms, m_s, c.k_sT);
+  const float ft1 = rescale(s.mt, m_t, c.k_t1), ftT = rescale(s.mt, m_t, c.k_tT);
+  float v[13] = {s.ls1 * fs1, s.lsT * fsT, s.pd * fsT, s.px * fsT, s.lt1 * ft1, s.ltT * ftT,
+                 s.qd * ftT, s.qx * ftT, s.zys, s.zyt, s.tk, s.jq, s.jp};
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+    for (int i = 0; i < 13; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
+  }
+  s.ms = m_s;
+  s.mt = m_t;
+  s.ls1 = v[0];
+  s.lsT = v[1];
+  s.pd = v[2];
+  s.px = v[3];
+  s.lt1 = v[4];
+  s.ltT = v[5];
+  s.qd = v[6];
+  s.qx = v[7];
+  s.zys = v[8];
+  s.zyt = v[9];
+  s.tk = v[10];
+  s.jq = v[11];
+  s.jp = v[12];
+  s.cq = s.cp = -1.f;
+}
+
 // Sums of one chunk against fixed maxima (see update()).  PW: how the T = 1
 // sums follow from the tempered ones (0: own exponential, 1: equal, 2: square).
 template <int NC, bool HAS_T, bool MASKED, int PW>

@@ -21,11 +21,11 @@
 namespace kd {
 namespace ring {
 
-constexpr int kCW = 16;                       // consumer warps
+constexpr int kCW = 24;                       // consumer warps
 constexpr int kCT = 32 * kCW;                 // consumer threads
 constexpr int kThreads = kCT + 32;            // + one producer warp
-constexpr int kChunk = 16384;                 // bytes of one tensor per stage
-constexpr int kStages = 6;
+constexpr int kChunk = 12288;                 // bytes of one tensor per stage
+constexpr int kStages = 8;
 constexpr int kSlots = kChunk / (16 * kCT);   // 16-byte slots per consumer thread per stage
 constexpr int kRingBytes = kStages * 2 * kChunk;
 // Per-row merge records.  A consumer warp runs at most kStages + 1 chunks
@@ -165,7 +165,7 @@ __device__ __forceinline__ void consumer_merge(RowState& st, const Consts& c, co
   if (w == 0) {
     if (l < kCW) st.load(R.recs + l * kRec);
     else st.init();
-    for (int o = 16; o > 0; o >>= 1) merge(st, shfl_xor(st, o), c);
+    warp_merge(st, c);
   }
   ptx::named_sync(1, kCT);
 }
@@ -189,7 +189,7 @@ __device__ __forceinline__ bool async_merge(RowState& st, const Consts& c, const
   __syncwarp();  // orders the other lanes' reads after lane 0's observation
   if (l < kCW) st.load(rec + l * kRec);
   else st.init();
-  for (int o = 16; o > 0; o >>= 1) merge(st, shfl_xor(st, o), c);
+  warp_merge(st, c);
   if (l == 0) R.cnt[slot] = 0;  // released before this warp's next ring arrival
   return true;
 }
@@ -248,22 +248,17 @@ struct Chunk<float> {
 };
 
 // Outputs of one token from its merged state (one thread).
+// y: the row's label (no labels: -1 with has_label false); st.zys / st.zyt
+// already hold the label's logits, picked up while the row streamed past.
 template <typename T, bool HAS_T>
 __device__ __forceinline__ RowOut finish_row(const StreamArgs& a, int64_t row, RowState& st,
-                                             bool write_kl) {
+                                             int64_t y, bool write_kl) {
   const Consts& c = a.c;
   const int64_t V = a.vocab;
-  const T* zs = static_cast<const T*>(a.zs) + row * V;
-  const T* zt = HAS_T ? static_cast<const T*>(a.zt) + row * V : nullptr;
   bool valid = true, bad = false;
   if (a.labels) {
-    const int64_t y = a.labels[row];
     valid = y != a.ignore;
     bad = valid && (y < 0 || y >= V);
-    if (valid && !bad) {
-      st.zys = ld1<T>(zs + y);
-      if (HAS_T) st.zyt = ld1<T>(zt + y);
-    }
   }
   const float mass = a.topk ? a.mass[row] : 0.f, ent = a.topk ? a.ent[row] : 0.f;
   const RowOut o = finalize(st, c, a.variant, HAS_T, a.topk, mass, ent);
@@ -277,15 +272,18 @@ __device__ __forceinline__ RowOut finish_row(const StreamArgs& a, int64_t row, R
   return o;
 }
 
-// Forward.  Acc: init(); static load(Frag&, buf, slot); step(const Frag[kSlots],
-// const int nv[kSlots], c); RowState fold().  Column indices within a row are
-// 32-bit (the dispatch keeps rows below 2^30 elements).
-template <typename T, bool HAS_T, class Acc>
+// Forward.  Acc: init(); static load(Frag&, buf, slot); static pick(const
+// Frag&, i, zs, zt) (element i of a slot); step(const Frag[kSlots],
+// const int nv[kSlots], c); RowState fold(c).  Column indices within a row are
+// 32-bit (the dispatch keeps rows below 2^30 elements).  PASSES = 2 for
+// skew-JS (a second sweep once both normalisers are known), else 1; a
+// template parameter so single-pass kernels carry no second-sweep code.
+template <typename T, bool HAS_T, class Acc, int PASSES>
 __global__ void __launch_bounds__(kThreads, 1) k_fwd(StreamArgs a, uint32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   const Ring R = make_ring(smem_raw);
   ring_init(R);
-  const int passes = (HAS_T && a.variant == KD_KL_SKEW_JS) ? 2 : 1;
+  constexpr int passes = PASSES;
   if ((threadIdx.x >> 5) == kCW) {
     producer<T>(R, a, HAS_T, passes, status);
   } else {
@@ -296,9 +294,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd(StreamArgs a, uint32_t* sta
     const int ct = threadIdx.x;
     Cursor cur;
     int local_row = 0;
+    // labels one row ahead: the load's latency hides behind a whole row
+    int64_t y_next = (a.labels && (int64_t)blockIdx.x < a.n) ? a.labels[blockIdx.x] : -1;
     for (int64_t row = blockIdx.x; row < a.n; row += gridDim.x, ++local_row) {
+      const int64_t y = y_next;
+      if (a.labels && row + gridDim.x < a.n) y_next = a.labels[row + gridDim.x];
+      // column of the label within the row, -1 if it is ignored or out of range
+      const int yc = (a.labels && y != a.ignore && y >= 0 && y < a.vocab) ? (int)y : -1;
       Acc acc;
       acc.init();
+      float zys = 0.f, zyt = 0.f;
       for (int ch = 0; ch < nch; ++ch) {
         const uint8_t* buf = cur.acquire(R, status);
         typename Acc::Frag f[kSlots];
@@ -306,13 +311,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd(StreamArgs a, uint32_t* sta
 #pragma unroll
         for (int j = 0; j < kSlots; ++j) {
           const int slot = j * kCT + ct;
-          nv[j] = valid_cols(V - (ch * EPC + slot * EPT), EPT);
-          if (nv[j] > 0) Acc::load(f[j], buf, slot);
+          const int e0 = ch * EPC + slot * EPT;
+          nv[j] = valid_cols(V - e0, EPT);
+          if (nv[j] > 0) {
+            Acc::load(f[j], buf, slot);
+            // the label's logits, from the staged copy (one thread per row)
+            if ((unsigned)(yc - e0) < (unsigned)EPT) Acc::pick(f[j], yc - e0, zys, zyt);
+          }
         }
         cur.release(R);
         acc.step(f, nv, c);
       }
-      RowState st = acc.fold();
+      RowState st = acc.fold(c);
+      st.zys = zys;
+      st.zyt = zyt;
       if (a.topk) {  // sparse cross term sum_S p a_s (ids validated by the prep kernel)
         const T* zs = static_cast<const T*>(a.zs) + row * a.vocab;
         const int32_t* ids = a.sidx + row * a.k;
@@ -322,17 +334,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd(StreamArgs a, uint32_t* sta
           if (id >= 0 && id < V) st.tk = fmaf(ps[j], ld1<T>(zs + id) * c.inv_ts, st.tk);
         }
       }
-      for (int o = 16; o > 0; o >>= 1) merge(st, shfl_xor(st, o), c);
-      if (passes == 1) {
+      warp_merge(st, c);
+      if constexpr (passes == 1) {
         // no CTA barrier: the last warp to finish the row finalises it
         if (async_merge(st, c, R, local_row) && (ct & 31) == 0)
-          finish_row<T, HAS_T>(a, row, st, true);
+          finish_row<T, HAS_T>(a, row, st, y, true);
         continue;
       }
       // skew-JS: both normalisers are needed before the second sweep
       consumer_merge(st, c, R);
       if (ct == 0) {
-        const RowOut o = finish_row<T, HAS_T>(a, row, st, false);
+        const RowOut o = finish_row<T, HAS_T>(a, row, st, y, false);
         R.bcast[0] = o.dlse;
         R.bcast[1] = o.lse_tT;
       }
@@ -361,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd(StreamArgs a, uint32_t* sta
       }
       const float2 r = consumer_sum2(jq, jp, R);
       if (ct == 0) {
-        const bool v_ok = !a.labels || a.labels[row] != a.ignore;
+        const bool v_ok = !a.labels || y != a.ignore;
         a.stats[row * KD_STATS_PER_TOKEN + S_KL_PM] = r.y;
         if (a.kl) a.kl[row] = v_ok ? (1.f - c.beta) * r.x + c.beta * r.y : 0.f;
       }
@@ -411,6 +423,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd(StreamArgs a, uint32_t* sta
   __syncthreads();
 }
 
+// Forward with the pass count the variant needs.
+template <typename T, bool HAS_T, class Acc>
+inline void launch_fwd(const StreamArgs& a, cudaStream_t s);
+
 // Launch one persistent CTA per SM (fewer for short batches).
 template <typename K>
 inline void launch(K kernel, const StreamArgs& a, cudaStream_t s) {
@@ -418,6 +434,17 @@ inline void launch(K kernel, const StreamArgs& a, cudaStream_t s) {
   const int grid = (int)(a.n < sms ? a.n : sms);
   cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   kernel<<<grid, kThreads, kSmem, s>>>(a, a.status);
+}
+
+template <typename T, bool HAS_T, class Acc>
+inline void launch_fwd(const StreamArgs& a, cudaStream_t s) {
+  if constexpr (HAS_T) {
+    if (a.variant == KD_KL_SKEW_JS) {
+      launch(k_fwd<T, HAS_T, Acc, 2>, a, s);
+      return;
+    }
+  }
+  launch(k_fwd<T, HAS_T, Acc, 1>, a, s);
 }
 
 }  // namespace ring

@@ -212,6 +212,14 @@ struct GenericAcc {
     ring::Chunk<T>::load(buf, ct, f.s);
     if (HAS_T) ring::Chunk<T>::load(buf + ring::kChunk, ct, f.t);
   }
+  __device__ static void pick(const Frag& f, int i, float& zs, float& zt) {
+#pragma unroll
+    for (int u = 0; u < EPT; ++u)
+      if (u == i) {
+        zs = f.s[u];
+        if (HAS_T) zt = f.t[u];
+      }
+  }
   __device__ void init() { st.init(); }
   __device__ void step(const Frag (&f)[ring::kSlots], const int (&nv)[ring::kSlots],
                        const Consts& c) {
@@ -221,7 +229,7 @@ struct GenericAcc {
       else if (nv[j] > 0) update<EPT, HAS_T, true>(st, f[j].s, f[j].t, nv[j], c);
     }
   }
-  __device__ RowState fold() const { return st; }
+  __device__ RowState fold(const Consts&) const { return st; }
 };
 
 // d z_s = s_row [ w_sce (softmax(z_s) - e_y) + w_kl T_s dKL/da_s ] for one
@@ -300,8 +308,8 @@ static void fwd_dispatch(const StreamArgs& a, cudaStream_t s) {
   note_launch();
   if (vec) {  // rows 16-byte aligned: TMA-staged ring kernels
     if (launch_stream_fwd_packed(a, s)) return;
-    if (has_t) ring::launch(ring::k_fwd<T, true, GenericAcc<T, true>>, a, s);
-    else ring::launch(ring::k_fwd<T, false, GenericAcc<T, false>>, a, s);
+    if (has_t) ring::launch_fwd<T, true, GenericAcc<T, true>>(a, s);
+    else ring::launch_fwd<T, false, GenericAcc<T, false>>(a, s);
   } else if (has_t) {
     k_stream_fwd<T, true><<<grid, kThreads, 0, s>>>(a);
   } else {

@@ -77,6 +77,8 @@ __device__ __forceinline__ uint32_t word(const uint4& u, int i) {
 // KLM: bit0 forward cross sums (q d, q (e^{-d} - 1)), bit1 reverse ones.
 // PW: 1 (T = 1, the CE sums are the tempered ones) or 2 (T = 2, e^{z-m} =
 // (e^{(z-m)/2})^2).  NEED1: labels present, so the T = 1 sums are kept.
+constexpr float kStale = 8.f;  // log2 of the largest term a stale maximum may leave
+
 template <bool HAS_T, int KLM, int PW, bool NEED1>
 struct PackedAcc {
   static constexpr int NS = ring::kSlots;  // one set of partial sums per slot
@@ -90,6 +92,14 @@ struct PackedAcc {
   __device__ static void load(Frag& f, const uint8_t* buf, int slot) {
     f.s = *reinterpret_cast<const uint4*>(buf + slot * 16);
     if (HAS_T) f.t = *reinterpret_cast<const uint4*>(buf + ring::kChunk + slot * 16);
+  }
+  __device__ static void pick(const Frag& f, int i, float& zs, float& zt) {
+    const uint32_t ws = word(f.s, i >> 1);
+    zs = (i & 1) ? bf16hi(ws) : bf16lo(ws);
+    if (HAS_T) {
+      const uint32_t wt = word(f.t, i >> 1);
+      zt = (i & 1) ? bf16hi(wt) : bf16lo(wt);
+    }
   }
   __device__ void init() {
     ms = mt = neg_inf();
@@ -141,8 +151,9 @@ struct PackedAcc {
       cp = ex2(-dM);
     }
   }
-  template <int J>
-  __device__ __forceinline__ void pair(uint32_t ws, uint32_t wt, const Consts& c) {
+  // With a teacher this path has T_s = T_t = T, so d = (t - s) / T: the
+  // cross sums keep sum e (t - s) and fold() applies 1/T once.
+  __device__ __forceinline__ void pair(int J, uint32_t ws, uint32_t wt, const Consts& c) {
     const float2 s = unpack(ws);
     const float2 es = ex2x2(fma2(s, splat(c.k_sT), osT));
     lsT[J] = add2(lsT[J], es);
@@ -152,23 +163,24 @@ struct PackedAcc {
       const float2 et = ex2x2(fma2(t, splat(c.k_tT), otT));
       ltT[J] = add2(ltT[J], et);
       if (NEED1) lt1[J] = PW == 2 ? fma2(et, et, lt1[J]) : add2(lt1[J], et);
-      const float2 d = fma2(t, splat(c.inv_tt), mul2(s, splat(-c.inv_ts)));
+      const float2 dt = sub2(t, s);
+      // e^{-d} - 1 terms as (sum + e_s c_q) - e_t: the partial sum is rounded
+      // at the size of one term, as fine as ex2's own error
       if (KLM & 1) {
-        qd[J] = fma2(et, d, qd[J]);
-        qx[J] = add2(qx[J], make_float2(fmaf(es.x, cq, -et.x), fmaf(es.y, cq, -et.y)));
+        qd[J] = fma2(et, dt, qd[J]);
+        qx[J] = sub2(fma2(es, splat(cq), qx[J]), et);
       }
       if (KLM & 2) {
-        pd[J] = fma2(es, d, pd[J]);  // sum of p d: the state keeps its negative
-        px[J] = add2(px[J], make_float2(fmaf(et.x, cp, -es.x), fmaf(et.y, cp, -es.y)));
+        pd[J] = fma2(es, dt, pd[J]);  // sum of p d: the state keeps its negative
+        px[J] = sub2(fma2(et, splat(cp), px[J]), es);
       }
     }
   }
-  template <int J>
-  __device__ __forceinline__ void slot(const Frag& f, const Consts& c) {
-    pair<J>(f.s.x, HAS_T ? f.t.x : 0u, c);
-    pair<J>(f.s.y, HAS_T ? f.t.y : 0u, c);
-    pair<J>(f.s.z, HAS_T ? f.t.z : 0u, c);
-    pair<J>(f.s.w, HAS_T ? f.t.w : 0u, c);
+  __device__ __forceinline__ void slot(int J, const Frag& f, const Consts& c) {
+    pair(J, f.s.x, HAS_T ? f.t.x : 0u, c);
+    pair(J, f.s.y, HAS_T ? f.t.y : 0u, c);
+    pair(J, f.s.z, HAS_T ? f.t.z : 0u, c);
+    pair(J, f.s.w, HAS_T ? f.t.w : 0u, c);
   }
   // nv is 0 or 8 here (the vocabulary is a multiple of 8)
   __device__ __forceinline__ void step(const Frag (&f)[NS], const int (&nv)[NS], const Consts& c) {
@@ -179,10 +191,14 @@ struct PackedAcc {
         cms = fmaxf(cms, max8(f[j].s));
         if (HAS_T) cmt = fmaxf(cmt, max8(f[j].t));
       }
-    if (cms > ms || (HAS_T && cmt > mt)) grow(cms, cmt, c);
-    static_assert(NS == 2, "one accumulator set per slot");
-    if (nv[0] > 0) slot<0>(f[0], c);
-    if (nv[1] > 0) slot<1>(f[1], c);
+    // The running maxima are only exponent offsets: a stale one is exact as
+    // long as no term exceeds 2^8 (squares 2^16), so the sums are rescaled
+    // only when a chunk's maximum passes the offset by that much -- after a
+    // row's first chunk, almost never.
+    if ((cms - ms) * c.k_sT > kStale || (HAS_T && (cmt - mt) * c.k_tT > kStale)) grow(cms, cmt, c);
+#pragma unroll
+    for (int j = 0; j < NS; ++j)
+      if (nv[j] > 0) slot(j, f[j], c);
   }
   __device__ static float total(const float2 (&v)[NS]) {
     float2 t = v[0];
@@ -190,7 +206,7 @@ struct PackedAcc {
     for (int j = 1; j < NS; ++j) t = add2(t, v[j]);
     return hsum(t);
   }
-  __device__ RowState fold() const {
+  __device__ RowState fold(const Consts& c) const {
     RowState st;
     st.init();
     st.ms = ms;
@@ -200,9 +216,9 @@ struct PackedAcc {
       st.mt = mt;
       st.lt1 = total(lt1);
       st.ltT = total(ltT);
-      st.qd = total(qd);
+      st.qd = total(qd) * c.inv_tt;
       st.qx = total(qx);
-      st.pd = -total(pd);
+      st.pd = -total(pd) * c.inv_ts;
       st.px = total(px);
     }
     return st;
@@ -301,8 +317,8 @@ struct PackedGrad {
 // ----------------------------------------------------------------- dispatch
 template <bool HAS_T, int KLM, int PW>
 void fwd_need(const StreamArgs& a, cudaStream_t s) {
-  if (a.c.need_s1) ring::launch(ring::k_fwd<bf16, HAS_T, PackedAcc<HAS_T, KLM, PW, true>>, a, s);
-  else ring::launch(ring::k_fwd<bf16, HAS_T, PackedAcc<HAS_T, KLM, PW, false>>, a, s);
+  if (a.c.need_s1) ring::launch_fwd<bf16, HAS_T, PackedAcc<HAS_T, KLM, PW, true>>(a, s);
+  else ring::launch_fwd<bf16, HAS_T, PackedAcc<HAS_T, KLM, PW, false>>(a, s);
 }
 template <bool HAS_T, int KLM>
 void fwd_pw(const StreamArgs& a, cudaStream_t s) {
