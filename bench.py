@@ -63,6 +63,33 @@ def bytes_per_step(w: I.Workload):
     return fwd, bwd
 
 
+def kernel_sources_hash() -> str:
+    """Hash of the library sources (kernels and launch planning)."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "lm_head_cross_vocab_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic() -> dict:
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum from
+    one ncu capture, profiles/traffic.json), keyed "workload:kernel family";
+    empty once the library sources differ from the ones that were captured."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return {}
+    if d.get("sources_sha256_16") != kernel_sources_hash():
+        return {}
+    return d.get("bytes_per_launch", {})
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
 
@@ -201,9 +228,12 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="run the workload at this many tokens (small cases for profiler captures)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-rows", type=int, default=32)
-    ap.add_argument("--cpu-rows", type=int, default=256)
+    ap.add_argument("--cpu-rows", type=int, default=0, help="oracle sample size (0: sized by time)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
@@ -212,6 +242,8 @@ def main():
     from lm_head_cross_vocab_gb300 import dist as D
     rank, world, local = D.world_from_env()
     w = I.WORKLOADS[args.config]
+    if args.tokens > 0:
+        w = w.scaled(n_tokens=args.tokens)
 
     if args.impl == "reference":
         run_reference(args, w, rank)
@@ -249,9 +281,21 @@ def main():
     kd.check_status(fwd_out["dev_status"])
 
     # per-section events (fused forward launch; backward recompute + dH/dW)
+    # and, on the tensor-core path, one event pair per gradient-producer and
+    # per backward GEMM launch
     n = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
-    for e4 in evs:
+    plan = kd.kd_plan_info(prob.to_c())
+    n_chunks = 0
+    if w.backward and plan["path"] == 2 and w.student == "hidden":
+        n_chunks = -(-w.n_tokens // plan["chunk_rows"]) * -(-w.vocab // plan["chunk_cols"])
+
+    def new_events(k):
+        return [torch.cuda.Event(enable_timing=True) for _ in range(k)]
+
+    evs = [new_events(4) for _ in range(n)]
+    lev = [(new_events(n_chunks), new_events(n_chunks), new_events(2 * n_chunks),
+            new_events(2 * n_chunks)) for _ in range(n)]
+    for e4 in evs + [e for grp in lev for e in grp]:
         for e in e4:
             e.record()  # materialise the handles
     torch.cuda.synchronize()
@@ -267,12 +311,17 @@ def main():
         for i in range(n):
             kd.kd_set_profile_events(*evs[i]) if w.backward else \
                 kd.kd_set_profile_events(evs[i][0], evs[i][1])
+            if n_chunks:
+                kd.kd_set_profile_launch_events(0, lev[i][0], lev[i][1])
+                kd.kd_set_profile_launch_events(1, lev[i][2], lev[i][3])
             step()
         stop.record()
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
     kd.kd_set_profile_events()
+    kd.kd_set_profile_launch_events(0)
+    kd.kd_set_profile_launch_events(1)
     launches = kd.kd_launch_count() - launches0
     ms = D.max_over_ranks(start.elapsed_time(stop), dev)
     ms_step = ms / n
@@ -284,25 +333,48 @@ def main():
 
     peaks, peak_src = load_peaks()
     f_fwd, f_bwd = flops_per_step(w)
+    # kernel families of one step: device time per step, launches per step and
+    # algorithmic work per step (FLOPs on the tensor-core path, HBM bytes on
+    # the streaming path).  The roofline is reported for the largest family
+    # on the caller's stream; the backward GEMMs run on a second stream,
+    # concurrently with the next gradient chunk, so their event times include
+    # waiting for SMs the producer holds (reported, never chosen).
+    fams = {}
+    side_stream = {"backward_gemm"}
     if f_fwd > 0:
-        achieved = f_fwd / (fwd_ms / 1e3) / 1e12
-        peak = peaks["bf16_tflops_sustained"]
-        roofline = {"bound": "tensor", "kernel": "k_tc<EPI_FWD> fused projection + CE/KL",
-                    "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                    "peak_source": f"{peak_src} bf16 sustained", "traffic": None,
-                    "flops_per_launch": f_fwd, "launch_ms": fwd_ms}
-        sections = {"fwd_fused_ms": fwd_ms, "bwd_tensor_ms": bwd_ms,
-                    "bwd_tflops": (f_bwd / (bwd_ms / 1e3) / 1e12) if bwd_ms else None,
-                    "step_tflops": (f_fwd + f_bwd) / (ms_step / 1e3) / 1e12}
+        unit, scale, peak = "TFLOP/s", 1e12, peaks["bf16_tflops_sustained"]
+        bound, psrc = "tensor", f"{peak_src} bf16 sustained"
+        fams["fused_forward"] = ("k_tc<EPI_FWD>: fused projections + online CE/KL", fwd_ms, 1, f_fwd)
+        if n_chunks:
+            def launch_ms(k0, k1, cnt):
+                return statistics.mean(sum(lev[i][k0][j].elapsed_time(lev[i][k1][j])
+                                           for j in range(cnt)) for i in range(n))
+            fams["gradient_producer"] = ("k_tc<EPI_GRAD>: recomputed projections -> G chunk",
+                                         launch_ms(0, 1, n_chunks), n_chunks, f_fwd)
+            fams["backward_gemm"] = ("k_tc<EPI_GEMM>: dH = G W, dW = G^T H",
+                                     launch_ms(2, 3, 2 * n_chunks), 2 * n_chunks, f_bwd - f_fwd)
     else:
+        unit, scale, peak = "GB/s", 1e9, peaks["hbm_gbs"]
+        bound, psrc = "hbm", f"{peak_src} copy"
         b_fwd, b_bwd = bytes_per_step(w)
-        achieved = b_fwd / (fwd_ms / 1e3) / 1e9
-        peak = peaks["hbm_gbs"]
-        roofline = {"bound": "hbm", "kernel": "k_stream_fwd", "achieved": achieved, "peak": peak,
-                    "unit": "GB/s", "frac": achieved / peak, "peak_source": f"{peak_src} copy",
-                    "traffic": None, "bytes_per_launch": b_fwd, "launch_ms": fwd_ms}
-        sections = {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
-                    "bwd_gbs": (b_bwd / (bwd_ms / 1e3) / 1e9) if bwd_ms else None}
+        fams["stream_forward"] = ("k_fwd: streamed logits -> online CE/KL", fwd_ms, 1, b_fwd)
+        if w.backward:
+            fams["stream_backward"] = ("k_bwd: streamed logits -> d z_s", bwd_ms, 1, b_bwd)
+    dom = max((f for f in fams if f not in side_stream), key=lambda k: fams[k][1])
+    name, k_ms, k_n, k_work = fams[dom]
+    per_launch_ms = k_ms / k_n
+    achieved = (k_work / k_n) / (per_launch_ms / 1e3) / scale
+    traffic = load_traffic().get(f"{w.name}:{dom}") if not args.tokens else None
+    roofline = {"bound": bound, "kernel": name, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "peak_source": psrc, "traffic": traffic,
+                ("flops_per_launch" if bound == "tensor" else "bytes_per_launch"): k_work / k_n,
+                "launch_ms": per_launch_ms, "launches_per_step": k_n}
+    sections = {f: {"ms_per_step": v[1], "launches": v[2],
+                    "achieved": v[3] / (v[1] / 1e3) / scale if v[1] else None, "unit": unit,
+                    **({"overlapped": True} if f in side_stream else {})}
+                for f, v in fams.items()}
+    if f_fwd > 0:
+        sections["step_tflops"] = (f_fwd + f_bwd) / (ms_step / 1e3) / 1e12
 
     # end to end through the C ABI with host buffers: H2D inputs, D2H results
     e2e = None
@@ -340,7 +412,12 @@ def main():
     peak_gib = torch.cuda.max_memory_allocated(dev) / 2 ** 30
     cpu_base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rows = min(args.cpu_rows, w.n_tokens)
+        # a probe sizes the sample to about --cpu-seconds of oracle work
+        probe = min(64, w.n_tokens)
+        v_probe, _ = time_oracle(w, probe, 1, 0, 13)
+        rows = int(min(w.n_tokens, max(probe, args.cpu_seconds * v_probe)))
+        if args.cpu_rows > 0:
+            rows = min(args.cpu_rows, w.n_tokens)
         v_cpu, dt = time_oracle(w, rows, 1, 0, 11)
         cpu_base = {"value": v_cpu, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
                     "sample": f"{rows} seeded random tokens of the {w.name} workload, fwd+bwd, "

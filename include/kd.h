@@ -251,6 +251,16 @@ kd_status kd_fwd_static_scratch(const kd_problem* problem, const kd_inputs* inpu
 kd_status kd_set_profile_events(void* fwd_start, void* fwd_stop, void* bwd_start,
                                 void* bwd_stop);
 
+/* Profiling aid for the tensor-core backward.  kind 0: kd_bwd records
+ * starts[k] / stops[k] (cudaEvent_t handles) right before / after the launch
+ * of the gradient producer for chunk k, on the call's stream; kind 1: around
+ * backward GEMM launch j (2k: dH of chunk k, 2k + 1: dW of chunk k) on the
+ * stream that GEMM runs on.  Launches with an index >= n record nothing.  The
+ * arrays stay owned by the caller and must outlive every kd_bwd enqueued
+ * while they are set; n = 0 stops recording.  Process-wide setting;
+ * KD_ERR_INVALID_ARG for an unknown kind or a NULL handle. */
+kd_status kd_set_profile_launch_events(int kind, void* const* starts, void* const* stops, int n);
+
 /* Number of kernel launches this library has enqueued in this process. */
 uint64_t kd_launch_count(void);
 

@@ -34,6 +34,23 @@ void prof_record(int i, cudaStream_t s) {
   if (e) cudaEventRecord(static_cast<cudaEvent_t>(e), s);
 }
 
+// per-launch events set by kd_set_profile_launch_events: [kind] = (starts,
+// stops, n); kind 0 = gradient producer launches, 1 = backward GEMM launches
+struct LaunchEvents {
+  void* const* starts;
+  void* const* stops;
+  int n;
+};
+std::mutex g_lprof_mu;
+LaunchEvents g_lprof[2] = {};
+
+// Records start (stop = false) or stop event `idx` of kind `kind` on `s`.
+void launch_record(int kind, int64_t idx, bool stop, cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_lprof_mu);
+  const LaunchEvents& e = g_lprof[kind];
+  if (idx < e.n) cudaEventRecord(static_cast<cudaEvent_t>(stop ? e.stops[idx] : e.starts[idx]), s);
+}
+
 enum Path { PATH_STREAM = 0, PATH_SIMT = 1, PATH_TC = 2 };
 
 constexpr size_t kAlign = 256;
@@ -66,6 +83,7 @@ struct Plan {
       b_dw, b_bytes;
   int64_t ldv, ldn;  // pitches of W^T [D, ldv] and H^T [D, ldn]
   bool kmajor_b;     // backward GEMMs take W^T / H^T (transposed per backward) as B
+  bool two_streams;  // backward GEMMs of chunk k on a side stream beside chunk k+1
 };
 
 bool finite_nonneg(float x) { return std::isfinite(x) && x >= 0.f; }
@@ -293,6 +311,7 @@ kd_status make_plan(const kd_problem* p, bool has_labels, Plan& P) {
       // as stored, 27k -> transpose).
       P.kmajor_b = (double)n * v / (double)(n + v) > 4096.0;
       if (const char* e = getenv("KD_TC_KMAJOR_B")) P.kmajor_b = e[0] == '1';  // debug override
+      P.two_streams = true;
       P.ldv = round_up(v, 8);
       P.ldn = round_up(n, 8);
       if (P.kmajor_b) {
@@ -738,7 +757,10 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
   // stream, so each launch's last partial wave overlaps the next launch.
   SideStream* ss = nullptr;
   cudaStream_t s2 = s;
-  if (!P.s_logits) {
+  const char* env_streams = getenv("KD_BWD_STREAMS");  // debug override: 1 = one stream
+  const bool two_streams = (P.two_streams && !(env_streams && env_streams[0] == '1')) ||
+                           (env_streams && env_streams[0] == '2');
+  if (!P.s_logits && two_streams) {
     if (side_stream(&ss) != KD_OK) return KD_ERR_CUDA;
     s2 = ss->stream;
     if (cudaEventRecord(ss->fork, s) != cudaSuccess ||
@@ -798,10 +820,12 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
         a.gt = gtk;
       }
       a.status = dev_status;
+      launch_record(0, k, false, s);
       if (launch_tc_grad(a, P.nsm, s) != 0) return KD_ERR_CUDA;
+      launch_record(0, k, true, s);
       if (P.s_logits) continue;
-      if (cudaEventRecord(ss->ready[buf], s) != cudaSuccess ||
-          cudaStreamWaitEvent(s2, ss->ready[buf], 0) != cudaSuccess)
+      if (ss && (cudaEventRecord(ss->ready[buf], s) != cudaSuccess ||
+                 cudaStreamWaitEvent(s2, ss->ready[buf], 0) != cudaSuccess))
         return KD_ERR_CUDA;
       // dW = G^T H reads G as stored, as an MN-major A (full rate): no
       // transposed copy of a gradient chunk is made.  B is W^T / H^T from the
@@ -833,7 +857,9 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
         }
         m.c16 = out;
         m.ldc16 = D;
+        launch_record(1, 2 * k, false, s2);
         if (launch_tc_gemm(m, P.nsm, s2) != 0) return KD_ERR_CUDA;
+        launch_record(1, 2 * k, true, s2);
       }
       if (d_w_s) {  // dW[chunk, :] (+)= G[:, chunk]^T H[r0.., :] (+ G_t^T H_t)
         TcGemmArgs m;
@@ -877,9 +903,11 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
         }
         m.c16 = out;
         m.ldc16 = D;
+        launch_record(1, 2 * k + 1, false, s2);
         if (launch_tc_gemm(m, P.nsm, s2) != 0) return KD_ERR_CUDA;
+        launch_record(1, 2 * k + 1, true, s2);
       }
-      if (cudaEventRecord(ss->consumed[buf], s2) != cudaSuccess) return KD_ERR_CUDA;
+      if (ss && cudaEventRecord(ss->consumed[buf], s2) != cudaSuccess) return KD_ERR_CUDA;
     }
   }
   if (ss && (cudaEventRecord(ss->join, s2) != cudaSuccess ||
@@ -887,6 +915,16 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
     return KD_ERR_CUDA;
   prof_record(3, s);
   return cuda_status(cudaGetLastError());
+}
+
+kd_status kd_set_profile_launch_events(int kind, void* const* starts, void* const* stops,
+                                       int n) {
+  if (kind < 0 || kind > 1 || n < 0 || (n > 0 && (!starts || !stops))) return KD_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i)
+    if (!starts[i] || !stops[i]) return KD_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_lprof_mu);
+  g_lprof[kind] = LaunchEvents{n ? starts : nullptr, n ? stops : nullptr, n};
+  return KD_OK;
 }
 
 kd_status kd_set_profile_events(void* fwd_start, void* fwd_stop, void* bwd_start,

@@ -268,10 +268,15 @@ __device__ __forceinline__ void update(RowState& st, const float* zs, const floa
     }
   }
   if (MASKED && nvalid <= 0) return;
-  // rescale the running sums only when a maximum grows (rare after the
-  // first chunks of a row)
+  // The running maxima are only exponent offsets: a stale one is exact while
+  // no term exceeds 2^8, so the sums are rescaled only when a chunk's maximum
+  // passes the offset by that much on either exponent scale (T = 1 or T) --
+  // after a row's first chunk, almost never, and never divergently per chunk.
+  const float kss = fmaxf(c.k_s1, c.k_sT), kst = fmaxf(c.k_t1, c.k_tT);
+  const bool grow_s = (cms - st.ms) * kss > 8.f;
+  const bool grow_t = HAS_T && (cmt - st.mt) * kst > 8.f;
   bool grew = false;
-  if (cms > st.ms) {
+  if (grow_s) {
     const float f1 = ex2((st.ms - cms) * c.k_s1), fT = ex2((st.ms - cms) * c.k_sT);
     st.ls1 *= f1;
     st.lsT *= fT;
@@ -280,7 +285,7 @@ __device__ __forceinline__ void update(RowState& st, const float* zs, const floa
     st.ms = cms;
     grew = true;
   }
-  if (HAS_T && cmt > st.mt) {
+  if (grow_t) {
     const float f1 = ex2((st.mt - cmt) * c.k_t1), fT = ex2((st.mt - cmt) * c.k_tT);
     st.lt1 *= f1;
     st.ltT *= fT;

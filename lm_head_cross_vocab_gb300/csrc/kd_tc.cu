@@ -34,6 +34,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -262,6 +263,7 @@ struct __align__(64) TcParams {
   int seg_accum[2];   // 1: the segment adds to an accumulator an earlier segment wrote
   int a_mn[2], b_mn[2];  // 1: the operand is stored MN-major ([K, M] / [K, N])
   int m_tiles, n_tiles, n_splits, items;
+  int m_band;         // row tiles per band of the item order (see item_range)
   int acc_stride;     // TMEM columns per accumulator stage
   int acc_stages;     // 1 or 2 accumulator stages in the 512 allocated columns
   int logits_vec;     // materialised logits rows are 16-byte aligned
@@ -327,10 +329,20 @@ __device__ __forceinline__ bool warp_wait(const Sync& s, uint32_t bar, uint32_t 
   return done;
 }
 
-__device__ __forceinline__ void item_range(const TcParams& P, int item, int& m_tile, int& t0,
-                                           int& t1) {
-  m_tile = item % P.m_tiles;
-  const int split = item / P.m_tiles;
+// Items (row tile, vocabulary split) are ordered in bands of m_band row tiles:
+// all splits of band 0 first, row tile fastest within a band.  The persistent
+// CTAs work on consecutive items, so at any time they share a few row tiles,
+// whose A rows (m_band of them, sized on the host to a slice of L2) stay
+// resident while the B tiles stream past; with all row tiles in one band the
+// A rows of every concurrent item could not all stay in L2.
+__device__ __forceinline__ void item_range(const TcParams& P, int item, int& m_tile, int& split,
+                                           int& t0, int& t1) {
+  const int per_band = P.m_band * P.n_splits;
+  const int band = item / per_band, idx = item - band * per_band;
+  const int m0 = band * P.m_band;
+  const int mb = min(P.m_band, P.m_tiles - m0);  // row tiles in this band
+  m_tile = m0 + idx % mb;
+  split = idx / mb;
   t0 = (int)((int64_t)P.n_tiles * split / P.n_splits);
   t1 = (int)((int64_t)P.n_tiles * (split + 1) / P.n_splits);
 }
@@ -421,10 +433,9 @@ struct FwdEpi {
     }
   }
 
-  __device__ __forceinline__ void end(const TcParams& P, int item, int half) {
+  __device__ __forceinline__ void end(const TcParams& P, int split, int half) {
     const TcFwdArgs& a = P.fwd;
     if (!row_ok) return;
-    const int split = item / P.m_tiles;
     st.store(a.partials + ((int64_t)(split * 2 + half) * a.n + row) * kRec);
   }
 };
@@ -644,8 +655,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
     uint32_t phase = 0, issued = 0, par = 0;
     bool ok = true;
     for (int item = cid; ok && item < P.items; item += ncl) {
-      int m_tile, t0, t1;
-      item_range(P, item, m_tile, t0, t1);
+      int m_tile, split, t0, t1;
+      item_range(P, item, m_tile, split, t0, t1);
       for (int t = t0; ok && t < t1; ++t)
         for (int sg = 0; ok && sg < 2; ++sg)
           for (int kb = 0; ok && kb < P.kb[sg]; ++kb) {
@@ -702,8 +713,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
     Sync Sc = S;
     Sc.cluster_acquire = PAIR;  // the peer's epilogue arrives on acc_empty remotely
     for (int item = cid; ok && item < P.items; item += ncl) {
-      int m_tile, t0, t1;
-      item_range(P, item, m_tile, t0, t1);
+      int m_tile, split, t0, t1;
+      item_range(P, item, m_tile, split, t0, t1);
       for (int t = t0; ok && t < t1; ++t) {
         if (!warp_wait(Sc, S.acc_empty + 8 * acc, acc_phase ^ 1)) {
           ok = false;
@@ -773,8 +784,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
     bool ok = true;
     const int r_in_pair = (int)rank * BM + r_in_tile;  // row within the (pair) tile
     for (int item = cid; ok && item < P.items; item += ncl) {
-      int m_tile, t0, t1;
-      item_range(P, item, m_tile, t0, t1);
+      int m_tile, split, t0, t1;
+      item_range(P, item, m_tile, split, t0, t1);
       const int64_t tile_row = (int64_t)m_tile * C::ROWS + r_in_pair;
       FwdEpi<BN> fe;
       if (EPI == EPI_FWD) fe.begin(P, tile_row, t0, half);
@@ -968,7 +979,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
           acc_phase ^= 1;
         }
       }
-      if (EPI == EPI_FWD && ok) fe.end(P, item, half);
+      if (EPI == EPI_FWD && ok) fe.end(P, split, half);
     }
   }
   tc_fence_before();
@@ -1076,6 +1087,15 @@ bool logits_vec_ok(const void* p, int64_t vocab) {
 
 int fail_map() { return (int)cudaErrorInvalidValue; }
 
+// Row tiles per band of the item order: the A rows of one band (rows_per_tile
+// x K bf16 per row tile, all segments) take at most 48 MiB of L2.
+int band_tiles(const TcParams& P, int rows_per_tile) {
+  const int64_t k = (int64_t)(P.kb[0] + P.kb[1]) * BK;
+  const int64_t per_tile = std::max<int64_t>(1, (int64_t)rows_per_tile * k * 2);
+  const int64_t b = ((int64_t)48 << 20) / per_tile;
+  return (int)std::max<int64_t>(1, std::min<int64_t>(b, P.m_tiles));
+}
+
 // Segment setup shared by the fused forward and the gradient producer.
 // bn = tile columns, b_box = B rows one CTA loads, rows_per_tile = MMA M.
 template <class A>
@@ -1152,6 +1172,7 @@ int launch_tc_fwd(const TcFwdArgs& a, int num_sms, cudaStream_t s) {
     return fail_map();
   P.n_splits = a.n_splits;
   P.items = P.m_tiles * P.n_splits;
+  P.m_band = band_tiles(P, tc_tile_rows(pair));
   P.logits_vec = logits_vec_ok(a.zs_logits, a.vocab) && logits_vec_ok(a.zt_logits, a.vocab);
   P.fwd = a;
   const bool has_t = a.t_gemm || a.t_logits;
@@ -1175,6 +1196,7 @@ int launch_tc_grad(const TcGradArgs& a, int num_sms, cudaStream_t s) {
     return fail_map();
   P.n_splits = P.n_tiles;  // one tile per item
   P.items = P.m_tiles * P.n_tiles;
+  P.m_band = band_tiles(P, tc_tile_rows(pair));
   P.logits_vec = logits_vec_ok(a.zs_logits, a.vocab) && logits_vec_ok(a.zt_logits, a.vocab);
   P.grad = a;
   const bool has_t = a.t_gemm || a.t_logits;
@@ -1221,6 +1243,7 @@ int launch_tc_gemm(const TcGemmArgs& a, int num_sms, cudaStream_t s) {
   P.n_tiles = (int)((a.N + bn - 1) / bn);
   P.n_splits = P.n_tiles;
   P.items = P.m_tiles * P.n_tiles;
+  P.m_band = band_tiles(P, tc_tile_rows(pair));
   P.gemm = a;
   return pair ? launch<EPI_GEMM, 256, false, true>(P, num_sms, s)
               : launch<EPI_GEMM, 256, false, false>(P, num_sms, s);

@@ -96,12 +96,14 @@ def load_library(path: str = LIB_PATH):
     lib.kd_diag_gemm_bf16.argtypes = [vp, vp, vp, ctypes.c_int64, ctypes.c_int64,
                                       ctypes.c_int64, ctypes.c_int, vp]
     lib.kd_set_profile_events.argtypes = [vp, vp, vp, vp]
+    lib.kd_set_profile_launch_events.argtypes = [ctypes.c_int, vp, vp, ctypes.c_int]
     lib.kd_plan_info.argtypes = [P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
                                  ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]
     lib.kd_fwd_static_scratch.argtypes = [P, I, vp, vp, vp, vp, vp, vp, vp]
     lib.kd_launch_count.restype = ctypes.c_uint64
     for f in ("kd_workspace_size", "kd_fwd", "kd_bwd", "kd_device_supported", "kd_abi_version",
-              "kd_diag_gemm_bf16", "kd_set_profile_events", "kd_fwd_static_scratch",
+              "kd_diag_gemm_bf16", "kd_set_profile_events", "kd_set_profile_launch_events",
+              "kd_fwd_static_scratch",
               "kd_plan_info"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
@@ -172,6 +174,27 @@ def kd_set_profile_events(fwd_start=None, fwd_stop=None, bwd_start=None, bwd_sto
     st = load_library().kd_set_profile_events(*h)
     if st != KD_OK:
         raise KDError(st, "kd_set_profile_events")
+
+
+_launch_event_arrays = {}  # kind -> (starts, stops, events): kept alive while set
+
+
+def kd_set_profile_launch_events(kind: int, starts=(), stops=()):
+    """Record torch.cuda.Event pairs around each gradient-producer launch (kind
+    0) or backward GEMM launch (kind 1) of later kd_bwd calls; () stops."""
+    starts, stops = list(starts), list(stops)
+    assert len(starts) == len(stops)
+    n = len(starts)
+    arr_s = (ctypes.c_void_p * max(n, 1))(*[e.cuda_event for e in starts])
+    arr_t = (ctypes.c_void_p * max(n, 1))(*[e.cuda_event for e in stops])
+    st = load_library().kd_set_profile_launch_events(kind, ctypes.addressof(arr_s),
+                                                     ctypes.addressof(arr_t), n)
+    if st != KD_OK:
+        raise KDError(st, "kd_set_profile_launch_events")
+    if n:
+        _launch_event_arrays[kind] = (arr_s, arr_t, starts + stops)
+    else:
+        _launch_event_arrays.pop(kind, None)
 
 
 def kd_plan_info(problem: kd_problem) -> dict:
