@@ -65,10 +65,18 @@ __device__ __forceinline__ float2 splat(float v) { return make_float2(v, v); }
 __device__ __forceinline__ float2 unpack(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
 __device__ __forceinline__ float2 ex2x2(float2 v) { return make_float2(ex2(v.x), ex2(v.y)); }
 __device__ __forceinline__ float hsum(float2 v) { return v.x + v.y; }
-__device__ __forceinline__ float max8(const uint4& u) {
-  const uint32_t m = max_bf16x2(max_bf16x2(u.x, u.y), max_bf16x2(u.z, u.w));
-  return fmaxf(bf16lo(m), bf16hi(m));
+// maxima of the even and odd elements of 8 bf16 values, as bf16x2
+__device__ __forceinline__ uint32_t max4w(const uint4& u) {
+  return max_bf16x2(max_bf16x2(u.x, u.y), max_bf16x2(u.z, u.w));
 }
+__device__ __forceinline__ float hmax(uint32_t w) { return fmaxf(bf16lo(w), bf16hi(w)); }
+// bf16x2 with x rounded toward -inf in both halves
+__device__ __forceinline__ uint32_t bf16x2_floor(float x) {
+  uint16_t h;
+  asm("cvt.rm.bf16.f32 %0, %1;" : "=h"(h) : "f"(x));
+  return ((uint32_t)h << 16) | h;
+}
+constexpr uint32_t kNegInfX2 = 0xff80ff80u;  // -inf, -inf as bf16x2
 __device__ __forceinline__ uint32_t word(const uint4& u, int i) {
   return i == 0 ? u.x : (i == 1 ? u.y : (i == 2 ? u.z : u.w));
 }
@@ -86,6 +94,7 @@ struct PackedAcc {
     uint4 s, t;
   };
   float ms, mt, cq, cp;
+  uint32_t ths, tht;  // bf16x2 rescale thresholds: offset + kStale (rounded down)
   float2 osT, otT;  // -m k_T per side (exponent offsets)
   float2 ls1[NS], lsT[NS], lt1[NS], ltT[NS], qd[NS], qx[NS], pd[NS], px[NS];
 
@@ -103,6 +112,7 @@ struct PackedAcc {
   }
   __device__ void init() {
     ms = mt = neg_inf();
+    ths = tht = kNegInfX2;
     cq = cp = 0.f;
     osT = otT = splat(0.f);
 #pragma unroll
@@ -127,6 +137,7 @@ struct PackedAcc {
       }
       ms = cms;
       osT = splat(-ms * c.k_sT);
+      ths = bf16x2_floor(ms + kStale / c.k_sT);
       grew = true;
     }
     if (HAS_T && cmt > mt) {
@@ -143,6 +154,7 @@ struct PackedAcc {
       }
       mt = cmt;
       otT = splat(-mt * c.k_tT);
+      tht = bf16x2_floor(mt + kStale / c.k_tT);
       grew = true;
     }
     if (HAS_T && grew) {
@@ -184,18 +196,20 @@ struct PackedAcc {
   }
   // nv is 0 or 8 here (the vocabulary is a multiple of 8)
   __device__ __forceinline__ void step(const Frag (&f)[NS], const int (&nv)[NS], const Consts& c) {
-    float cms = neg_inf(), cmt = neg_inf();
+    uint32_t ws = kNegInfX2, wt = kNegInfX2;
 #pragma unroll
     for (int j = 0; j < NS; ++j)
       if (nv[j] > 0) {
-        cms = fmaxf(cms, max8(f[j].s));
-        if (HAS_T) cmt = fmaxf(cmt, max8(f[j].t));
+        ws = j == 0 ? max4w(f[j].s) : max_bf16x2(ws, max4w(f[j].s));
+        if (HAS_T) wt = j == 0 ? max4w(f[j].t) : max_bf16x2(wt, max4w(f[j].t));
       }
     // The running maxima are only exponent offsets: a stale one is exact as
     // long as no term exceeds 2^8 (squares 2^16), so the sums are rescaled
     // only when a chunk's maximum passes the offset by that much -- after a
-    // row's first chunk, almost never.
-    if ((cms - ms) * c.k_sT > kStale || (HAS_T && (cmt - mt) * c.k_tT > kStale)) grow(cms, cmt, c);
+    // row's first chunk, almost never.  The test runs on the raw bf16x2
+    // words against a threshold rounded down (a spurious rescale is harmless).
+    if (max_bf16x2(ws, ths) != ths || (HAS_T && max_bf16x2(wt, tht) != tht))
+      grow(hmax(ws), HAS_T ? hmax(wt) : neg_inf(), c);
 #pragma unroll
     for (int j = 0; j < NS; ++j)
       if (nv[j] > 0) slot(j, f[j], c);
