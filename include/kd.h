@@ -74,6 +74,7 @@ typedef enum kd_status {
 #define KD_DEV_BAD_LABEL 0x1u
 #define KD_DEV_BAD_TOPK 0x2u
 #define KD_DEV_TIMEOUT 0x4u
+#define KD_DEV_BAD_MAP 0x8u   /* token map entry outside [-1, V_student) */
 
 typedef enum kd_dtype { KD_BF16 = 0, KD_FP32 = 1 } kd_dtype;
 
@@ -193,6 +194,35 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* inputs, const float
  * pointer may be NULL. */
 kd_status kd_plan_info(const kd_problem* problem, int32_t* path, int32_t* vocab_splits,
                        int64_t* chunk_rows, int64_t* chunk_cols);
+
+/* Cross-vocabulary token-map projection (orda-kernel README, "Cross-vocabulary
+ * distillation", token-map projection -> PrecomputedTeacher).  When student and
+ * teacher tokenizers differ, per-column KL is undefined; the teacher
+ * distribution is moved onto the student vocabulary instead:
+ *   out[n, i] = log sum_{j : token_map[j] = i} exp(logits_t[n, j] / temperature)
+ * for every token row n < n_tokens and student id i < v_student.  Duplicate
+ * teacher tokens of one student id sum in probability space; the tempering is
+ * applied before the aggregation, so pass the result to kd_fwd / kd_bwd as a
+ * KD_TEACHER_LOGITS teacher with t_teacher = 1 (the pages declare it with
+ * logits_temperature = T).  A student id no teacher token maps to has
+ * probability 0: it gets the most negative finite value of out_dtype (its
+ * exponential is exactly 0, as -inf's would be, and the divergences of the
+ * distillation kernels need no special case for it).
+ *   token_map  device int32 [v_teacher]: student id of teacher token j, or -1
+ *              (entries outside [-1, v_student) set KD_DEV_BAD_MAP in
+ *              *dev_status and are skipped)
+ *   logits_t   device [n_tokens, v_teacher] in in_dtype (KD_BF16 / KD_FP32)
+ *   out        device [n_tokens, v_student] in out_dtype
+ *   workspace  >= kd_project_workspace_size() bytes, 256-byte aligned; the
+ *              inverse map is rebuilt in it on every call (its contents need
+ *              not be initialised)
+ * Asynchronous on `stream`; host-checkable errors return synchronously. */
+kd_status kd_project_workspace_size(int64_t v_teacher, int64_t v_student, size_t* bytes);
+kd_status kd_project_teacher_logits(const int32_t* token_map, int64_t v_teacher,
+                                    int64_t v_student, const void* logits_t, int64_t n_tokens,
+                                    int32_t in_dtype, float temperature, void* out,
+                                    int32_t out_dtype, uint32_t* dev_status, void* workspace,
+                                    size_t ws_bytes, void* stream);
 
 /* Static description of a status code. */
 const char* kd_status_string(kd_status status);

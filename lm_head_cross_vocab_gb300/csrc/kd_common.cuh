@@ -31,6 +31,9 @@ namespace kd {
 
 constexpr float kL2E = 1.4426950408889634f;  // log2(e)
 constexpr int kRec = 16;                     // floats per partial-state record
+// Teacher logits at or below this carry no probability (ids a cross-vocabulary
+// projection left unmatched): they never set a running maximum.
+constexpr float kNoMass = -1e30f;
 
 // fields of the saved per-token statistics (KD_STATS_PER_TOKEN floats)
 // S_DLSE = logsumexp(a_t) - logsumexp(a_s), taken from the accurate log1p form
@@ -274,7 +277,7 @@ __device__ __forceinline__ void update(RowState& st, const float* zs, const floa
   // after a row's first chunk, almost never, and never divergently per chunk.
   const float kss = fmaxf(c.k_s1, c.k_sT), kst = fmaxf(c.k_t1, c.k_tT);
   const bool grow_s = (cms - st.ms) * kss > 8.f;
-  const bool grow_t = HAS_T && (cmt - st.mt) * kst > 8.f;
+  const bool grow_t = HAS_T && cmt > kNoMass && (cmt - st.mt) * kst > 8.f;
   bool grew = false;
   if (grow_s) {
     const float f1 = ex2((st.ms - cms) * c.k_s1), fT = ex2((st.ms - cms) * c.k_sT);
@@ -302,7 +305,10 @@ __device__ __forceinline__ void update(RowState& st, const float* zs, const floa
   }
   const float cq = st.cq, cp = st.cp;
   const float os1 = -ms * c.k_s1, osT = -ms * c.k_sT;
-  const float ot1 = -mt * c.k_t1, otT = -mt * c.k_tT;
+  // a teacher offset never set (no teacher mass yet) contributes nothing: the
+  // no-mass logits still give e^{...} = 0, without -inf + inf
+  const float mt_off = mt > kNoMass ? mt : 0.f;
+  const float ot1 = -mt_off * c.k_t1, otT = -mt_off * c.k_tT;
   float ls1 = 0.f, lsT = 0.f, lt1 = 0.f, ltT = 0.f, qd = 0.f, qx = 0.f, pd = 0.f, px = 0.f;
   // T = 1 sums (for CE): with T = 1 they are the tempered sums; with T = 2,
   // e^{z-m} = (e^{(z-m)/2})^2 exactly, so neither needs its own exponential.
@@ -371,36 +377,40 @@ __device__ __forceinline__ RowOut finalize(const RowState& s, const Consts& c, i
   return o;
 }
 
-// Skew-JS terms in x = log p - log q = (a_s - a_t) + (lse(a_t) - lse(a_s)):
-// with m = (1-b) q + b p,  w = log(m/q) = log((1-b) + b e^x), evaluated as
-//   x <= 0:  log1p(b expm1(x)),   x > 0:  x + log1p((1-b) expm1(-x)),
-// which neither overflows nor loses the small divergences of nearby
-// distributions; then log(q/m) = -w and log(p/m) = x - w.
-__device__ __forceinline__ float js_w(float x, const Consts& c) {
+// Skew-JS logarithms from x = log p - log q = (a_s - a_t) + (lse(a_t) - lse(a_s)),
+// with m = (1-b) q + b p:
+//   x <= 0:  l = log(m/q) = log1p(b expm1(x)),      log(q/m) = -l,  log(p/m) = x - l
+//   x >  0:  l = log(m/p) = log1p((1-b) expm1(-x)),  log(p/m) = -l,  log(q/m) = -x - l
+// No form subtracts two large values: nearby distributions keep their small
+// divergences, and an id with q = 0 (a teacher id no token maps to: x huge)
+// still gives log(p/m) = -log b exactly.
+__device__ __forceinline__ void js_logs(float x, const Consts& c, float& lqm, float& lpm) {
   const bool neg = x <= 0.f;
   const float coef = neg ? c.beta : 1.f - c.beta;
   const float y = neg ? x : -x;
-  float e, l;
+  float l;
   if (c.precise) {
-    e = expm1f(y);
-    l = log1pf(coef * e);
+    l = log1pf(coef * expm1f(y));
   } else {
-    e = ex2(y * kL2E) - 1.f;
-    l = __logf(fmaf(coef, e, 1.f));
+    l = __logf(fmaf(coef, ex2(y * kL2E) - 1.f, 1.f));
   }
-  return neg ? l : x + l;
+  lqm = neg ? -l : -x - l;
+  lpm = neg ? x - l : -l;
 }
 
 // Skew-JS second pass: with the final normalisers known, accumulate
-// jq += q log(q/m) and jp += p log(p/m).
+// jq += q log(q/m) and jp += p log(p/m) (p and q each from its own
+// log-normaliser, so neither inherits the other's range).
 __device__ __forceinline__ void js_terms(float zs, float zt, float lse_tT, float dlse,
                                          const Consts& c, float& jq, float& jp) {
   const float x = fmaf(zs, c.inv_ts, -zt * c.inv_tt) + dlse;
   const float lq = zt * c.inv_tt - lse_tT;
-  const float w = js_w(x, c);
-  const float q = ex2(lq * kL2E), p = ex2((lq + x) * kL2E);
-  jq = fmaf(q, -w, jq);
-  jp = fmaf(p, x - w, jp);
+  const float lp = fmaf(zs, c.inv_ts, dlse - lse_tT);  // a_s - lse(a_s)
+  float lqm, lpm;
+  js_logs(x, c, lqm, lpm);
+  const float q = ex2(lq * kL2E), p = ex2(lp * kL2E);
+  jq = fmaf(q, lqm, jq);
+  jp = fmaf(p, lpm, jp);
 }
 
 // Gradient of the KL part w.r.t. a_s (teacher detached), per element, from
@@ -414,7 +424,9 @@ __device__ __forceinline__ float kl_grad(float zs, float zt, const float* stt, i
   const float p = ex2(lp * kL2E);
   if (variant == KD_KL_SKEW_JS) {
     const float x = fmaf(zs, c.inv_ts, -zt * c.inv_tt) + stt[S_DLSE];
-    return c.beta * p * (x - js_w(x, c) - stt[S_KL_PM]);
+    float lqm, lpm;
+    js_logs(x, c, lqm, lpm);
+    return c.beta * p * (lpm - stt[S_KL_PM]);
   }
   float g = 0.f;
   if (variant != KD_KL_REVERSE) g = p - ex2(lq * kL2E);
@@ -428,7 +440,9 @@ __device__ __forceinline__ float kl_grad_pq(float zs, float zt, float lp, float 
                                             const Consts& c) {
   if (variant == KD_KL_SKEW_JS) {
     const float x = fmaf(zs, c.inv_ts, -zt * c.inv_tt) + stt[S_DLSE];
-    return c.beta * p * (x - js_w(x, c) - stt[S_KL_PM]);
+    float lqm, lpm;
+    js_logs(x, c, lqm, lpm);
+    return c.beta * p * (lpm - stt[S_KL_PM]);
   }
   float g = 0.f;
   if (variant != KD_KL_REVERSE) g = p - q;

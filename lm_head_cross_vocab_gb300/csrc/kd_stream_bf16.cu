@@ -140,7 +140,7 @@ struct PackedAcc {
       ths = bf16x2_floor(ms + kStale / c.k_sT);
       grew = true;
     }
-    if (HAS_T && cmt > mt) {
+    if (HAS_T && cmt > mt && cmt > kNoMass) {  // no-mass chunks never set the offset
       const float2 fT = splat(ex2((mt - cmt) * c.k_tT));
       const float2 f1 = splat(NEED1 ? ex2((mt - cmt) * c.k_t1) : 0.f);
 #pragma unroll

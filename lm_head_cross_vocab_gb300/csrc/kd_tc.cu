@@ -526,7 +526,9 @@ __device__ __forceinline__ void grad32(float* vs, const float* vt, const GradRow
       g = r.wk * p;
     } else if (VAR == GV_SJS) {
       const float x = fmaf(vs[j], c.inv_ts, -vt[j] * c.inv_tt) + r.dlse;
-      g = r.bwk * p * (x - js_w(x, c) - r.klpm);
+      float lqm, lpm;
+      js_logs(x, c, lqm, lpm);
+      g = r.bwk * p * (lpm - r.klpm);
     } else {
       const float l2q = fmaf(vt[j], r.kt, r.nt);
       if (VAR == GV_FWD) {

@@ -26,7 +26,7 @@ LIB_PATH = os.path.join(_PKG, "libkdgb.so")
 # ---------------------------------------------------------------- enums
 KD_OK, KD_ERR_INVALID_ARG, KD_ERR_UNSUPPORTED, KD_ERR_WORKSPACE = 0, 1, 2, 3
 KD_ERR_BAD_LABEL, KD_ERR_BAD_TOPK, KD_ERR_TIMEOUT, KD_ERR_CUDA, KD_ERR_NO_DEVICE = 4, 5, 6, 7, 8
-KD_DEV_BAD_LABEL, KD_DEV_BAD_TOPK, KD_DEV_TIMEOUT = 0x1, 0x2, 0x4
+KD_DEV_BAD_LABEL, KD_DEV_BAD_TOPK, KD_DEV_TIMEOUT, KD_DEV_BAD_MAP = 0x1, 0x2, 0x4, 0x8
 KD_BF16, KD_FP32 = 0, 1
 KD_STUDENT_HIDDEN, KD_STUDENT_LOGITS = 0, 1
 KD_TEACHER_NONE, KD_TEACHER_TIED, KD_TEACHER_SEPARATE, KD_TEACHER_LOGITS, KD_TEACHER_TOPK = range(5)
@@ -100,10 +100,14 @@ def load_library(path: str = LIB_PATH):
     lib.kd_plan_info.argtypes = [P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
                                  ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]
     lib.kd_fwd_static_scratch.argtypes = [P, I, vp, vp, vp, vp, vp, vp, vp]
+    lib.kd_project_workspace_size.argtypes = [ctypes.c_int64, ctypes.c_int64, sz]
+    lib.kd_project_teacher_logits.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, vp,
+                                              ctypes.c_int64, ctypes.c_int32, ctypes.c_float, vp,
+                                              ctypes.c_int32, vp, vp, ctypes.c_size_t, vp]
     lib.kd_launch_count.restype = ctypes.c_uint64
     for f in ("kd_workspace_size", "kd_fwd", "kd_bwd", "kd_device_supported", "kd_abi_version",
               "kd_diag_gemm_bf16", "kd_set_profile_events", "kd_set_profile_launch_events",
-              "kd_fwd_static_scratch",
+              "kd_fwd_static_scratch", "kd_project_workspace_size", "kd_project_teacher_logits",
               "kd_plan_info"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
@@ -370,3 +374,50 @@ def problem_for(w, **overrides) -> Problem:
               ignore_index=w.ignore_index, vocab_chunk=w.vocab_chunk, seq_chunk=w.seq_chunk)
     kw.update(overrides)
     return Problem(**kw)
+
+
+# ---------------------------------------------------------------- cross-vocabulary
+
+def build_exact_token_map(student_vocab, teacher_vocab) -> torch.Tensor:
+    """Token map for kd_project_teacher_logits: entry j is the student id of the
+    teacher token string teacher_vocab[j], or -1 when the student vocabulary has
+    no identical string (orda-kernel README, "Cross-vocabulary distillation":
+    build_exact_token_map).  Vocabularies are sequences of token strings indexed
+    by id; a string listed twice in the student vocabulary maps to its first id.
+    Host-side preparation of a constant input (int32 CPU tensor)."""
+    first = {}
+    for i, tok in enumerate(student_vocab):
+        first.setdefault(tok, i)
+    return torch.tensor([first.get(tok, -1) for tok in teacher_vocab], dtype=torch.int32)
+
+
+def project_teacher_logits(token_map: torch.Tensor, logits_t: torch.Tensor, v_student: int,
+                           temperature: float = 1.0, out_dtype=None,
+                           workspace: Optional[Workspace] = None, check: bool = True):
+    """kd_project_teacher_logits: teacher logits [N, V_t] -> student-vocabulary
+    logits [N, V_s] (tempered; unmatched ids at the dtype's most negative value)."""
+    dev = logits_t.device
+    dtype = logits_t.dtype if out_dtype is None else out_dtype
+    tm = token_map.to(device=dev, dtype=torch.int32).contiguous()
+    zt = logits_t.contiguous()
+    n, vt = zt.shape
+    assert tm.numel() == vt
+    out = torch.empty(n, v_student, device=dev, dtype=dtype)
+    dev_status = torch.zeros(1, device=dev, dtype=torch.int32)
+    nbytes = ctypes.c_size_t(0)
+    lib = load_library()
+    st = lib.kd_project_workspace_size(vt, v_student, ctypes.byref(nbytes))
+    if st != KD_OK:
+        raise KDError(st, "kd_project_workspace_size")
+    ws = workspace or Workspace()
+    wptr, wbytes = ws.get(nbytes.value, dev)
+    dt = {torch.bfloat16: KD_BF16, torch.float32: KD_FP32}
+    st = lib.kd_project_teacher_logits(tm.data_ptr(), vt, v_student, zt.data_ptr(), n,
+                                       dt[zt.dtype], float(temperature), out.data_ptr(),
+                                       dt[dtype], dev_status.data_ptr(), wptr, wbytes,
+                                       _stream(dev))
+    if st != KD_OK:
+        raise KDError(st, "kd_project_teacher_logits")
+    if check and int(dev_status.item()) & KD_DEV_BAD_MAP:
+        raise KDError(KD_ERR_INVALID_ARG, "token map entry outside [-1, V_student)")
+    return out

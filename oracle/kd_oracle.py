@@ -81,7 +81,8 @@ def log_softmax(x):
 
 def _xlogy_rows(a, log_a_minus_log_b):
     """sum_v a_v (log a_v - log b_v) with the 0 log 0 = 0 convention."""
-    return np.sum(np.where(a > 0, a * log_a_minus_log_b, 0.0), axis=-1)
+    with np.errstate(invalid="ignore"):  # 0 * -inf in the discarded branch
+        return np.sum(np.where(a > 0, a * log_a_minus_log_b, 0.0), axis=-1)
 
 
 # ----------------------------------------------------------------------------
@@ -135,14 +136,11 @@ def kl_grad_rows(variant, aux, beta=0.5):
       skew_js  (1-beta) skew_fwd + beta skew_rev         ->  beta p (log p - log m - KL(p||m))
     """
     p, q, logp, logq = aux["p"], aux["q"], aux["logp"], aux["logq"]
-    g_f = p - q
-    g_r = p * (logp - logq - aux["kl_rev"][:, None])
     if variant == "forward":
-        return g_f
-    if variant == "reverse":
-        return g_r
-    if variant == "jeffreys":
-        return g_f + g_r
+        return p - q
+    if variant in ("reverse", "jeffreys"):
+        g_r = p * (logp - logq - aux["kl_rev"][:, None])
+        return g_r if variant == "reverse" else (p - q) + g_r
     logm = aux["logm"]
     m = np.exp(logm)
     if variant == "skew_forward":
@@ -153,6 +151,38 @@ def kl_grad_rows(variant, aux, beta=0.5):
     if variant == "skew_js":
         return beta * p * (logp - logm - aux["kl_pm"][:, None])
     raise ValueError(f"unknown variant {variant!r}")
+
+
+# ----------------------------------------------------------------------------
+# cross-vocabulary token map (orda-kernel README, "Cross-vocabulary
+# distillation", token-map projection)
+# ----------------------------------------------------------------------------
+
+def project_teacher_logits(z_t, token_map, v_student, temperature=1.0):
+    """Teacher logits over the teacher vocabulary -> logits over the student
+    vocabulary.  token_map[j] is the student id of teacher token j, or -1.
+    The teacher logits are tempered first (z / T), then each student id i
+    receives log sum_{j: map[j] = i} exp(z_j / T): duplicate teacher tokens of
+    one id sum in probability space, and an id no teacher token maps to gets
+    -inf (probability 0).  Written out per student id with numpy's grouped
+    reductions over the teacher columns sorted by student id.
+    """
+    z = as_f64(z_t) / float(temperature)
+    tm = np.asarray(token_map, dtype=np.int64)
+    out = np.full((z.shape[0], int(v_student)), -np.inf)
+    cols = np.flatnonzero(tm >= 0)
+    if cols.size == 0:
+        return out
+    ids = tm[cols]
+    order = np.argsort(ids, kind="stable")
+    cols, ids = cols[order], ids[order]
+    starts = np.flatnonzero(np.r_[True, ids[1:] != ids[:-1]])
+    lengths = np.diff(np.r_[starts, ids.size])
+    zz = z[:, cols]
+    m = np.maximum.reduceat(zz, starts, axis=1)                 # per-id maximum
+    s = np.add.reduceat(np.exp(zz - np.repeat(m, lengths, axis=1)), starts, axis=1)
+    out[:, ids[starts]] = m + np.log(s)
+    return out
 
 
 # ----------------------------------------------------------------------------
@@ -183,6 +213,11 @@ def topk_grad_rows(a, idx, pk):
 # ----------------------------------------------------------------------------
 # full loss: forward
 # ----------------------------------------------------------------------------
+
+def _weighted(w, x):
+    """w * x, with a zero weight giving 0 whatever x is."""
+    return w * np.asarray(x) if w != 0 else np.zeros_like(np.asarray(x, dtype=np.float64))
+
 
 def _valid_mask(labels, n, ignore_index):
     if labels is None:
@@ -242,8 +277,10 @@ def forward(z_s, z_t=None, labels=None, *, topk_idx=None, topk_p=None,
                        else np.zeros(n))
     kl = np.where(valid, kl, 0.0)
     out["kl"] = kl
-    per_token = (w_student_ce * out["ce_s"] + w_teacher_ce * out["ce_t"]
-                 + w_kl * t_student ** 2 * kl)
+    # a term with weight 0 is absent (its CE may be infinite, e.g. a projected
+    # teacher with no mass on the label)
+    per_token = (_weighted(w_student_ce, out["ce_s"]) + _weighted(w_teacher_ce, out["ce_t"])
+                 + _weighted(w_kl * t_student ** 2, kl))
     out["loss"] = float(np.sum(np.where(valid, per_token, 0.0))
                         / loss_denominator(valid, reduction, num_batch_labels))
     return out

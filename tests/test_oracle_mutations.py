@@ -53,6 +53,20 @@ def _topk_renormalised(orig):
     return topk_rows
 
 
+def _temper_after_aggregation(orig):
+    def project_teacher_logits(z_t, token_map, v_student, temperature=1.0):
+        return orig(z_t, token_map, v_student, 1.0) / temperature
+    return project_teacher_logits
+
+
+def _unmatched_get_zero_logit(orig):
+    def project_teacher_logits(z_t, token_map, v_student, temperature=1.0):
+        out = orig(z_t, token_map, v_student, temperature)
+        out[np.isneginf(out)] = 0.0
+        return out
+    return project_teacher_logits
+
+
 def _no_t_squared():
     orig = O.forward
 
@@ -73,6 +87,10 @@ MUTATIONS = [
     ("cross_entropy_rows", _label_off_by_one, P.test_ce_matches_torch_cross_entropy),
     ("hidden_grads", _transposed_dw, lambda: P.test_finite_difference_gradients("tied", "forward")),
     ("topk_rows", _topk_renormalised, P.test_golden_closed_forms),
+    ("project_teacher_logits", _temper_after_aggregation,
+     P.test_projection_moves_teacher_probability_mass),
+    ("project_teacher_logits", _unmatched_get_zero_logit,
+     P.test_projection_moves_teacher_probability_mass),
 ]
 
 

@@ -401,3 +401,66 @@ def test_no_teacher_is_plain_cross_entropy():
     torch.nn.functional.cross_entropy(zt, torch.from_numpy(labels)).backward()
     g, _ = O.grad_logits(z, None, labels)
     np.testing.assert_allclose(g, zt.grad.numpy(), rtol=1e-10, atol=1e-14)
+
+
+# ---------------------------------------------------------------- token-map projection
+
+def test_projection_identity_map_is_tempered_logits():
+    """With every teacher token mapped to the student id of the same index, the
+    projection is the tempered logits themselves."""
+    z = _rand_logits(3, 11, std=3.0)
+    out = O.project_teacher_logits(z, np.arange(11), 11, temperature=1.7)
+    np.testing.assert_allclose(out, z / 1.7, rtol=0, atol=1e-13)
+
+
+def test_projection_brute_force_with_duplicates_and_unmatched():
+    """Pure-Python sum of exponentials per student id (math.fsum) on a map with
+    repeated ids, unmatched teacher tokens and student ids nothing maps to."""
+    rng = np.random.default_rng(77)
+    v_t, v_s, T = 13, 7, 2.0
+    tmap = np.array([3, -1, 0, 3, 5, 0, 0, -1, 6, 3, 1, -1, 5])  # id 2 and 4 unmatched
+    z = rng.normal(0.0, 2.0, size=(4, v_t))
+    out = O.project_teacher_logits(z, tmap, v_s, temperature=T)
+    for n in range(z.shape[0]):
+        for i in range(v_s):
+            src = [j for j in range(v_t) if tmap[j] == i]
+            if not src:
+                assert out[n, i] == -math.inf
+            else:
+                ref = math.log(math.fsum(math.exp(z[n, j] / T) for j in src))
+                assert abs(out[n, i] - ref) <= 1e-12 * max(1.0, abs(ref))
+
+
+def test_projection_moves_teacher_probability_mass():
+    """softmax of the projected row = the tempered teacher distribution summed
+    over each id's teacher tokens, renormalised over the matched tokens
+    (scipy softmax on the teacher vocabulary)."""
+    rng = np.random.default_rng(5)
+    v_t, v_s, T = 40, 25, 1.5
+    tmap = rng.integers(-1, v_s, size=v_t)
+    z = rng.normal(0.0, 3.0, size=(5, v_t))
+    q_t = sps.softmax(z / T, axis=1)
+    matched = tmap >= 0
+    q_ref = np.zeros((5, v_s))
+    for j in np.flatnonzero(matched):
+        q_ref[:, tmap[j]] += q_t[:, j]
+    q_ref /= q_t[:, matched].sum(axis=1, keepdims=True)
+    q = sps.softmax(O.project_teacher_logits(z, tmap, v_s, temperature=T), axis=1)
+    np.testing.assert_allclose(q, q_ref, rtol=1e-12, atol=1e-15)
+
+
+def test_projected_teacher_kl_drops_zero_probability_ids():
+    """Forward KL(q'||p) of a projected teacher with unmatched student ids is finite
+    and equals the brute-force sum over the ids that carry teacher mass."""
+    rng = np.random.default_rng(9)
+    v_t, v_s = 9, 6
+    tmap = np.array([0, 0, 1, 2, -1, 2, 4, 4, 1])  # student ids 3 and 5 unmatched
+    z_t = rng.normal(0.0, 2.0, size=(2, v_t))
+    a_s = rng.normal(0.0, 2.0, size=(2, v_s))
+    a_t = O.project_teacher_logits(z_t, tmap, v_s)
+    kl, _ = O.kl_rows(a_s, a_t, "forward")
+    for n in range(2):
+        q = sps.softmax(a_t[n])
+        p = sps.softmax(a_s[n])
+        ref = math.fsum(q[i] * (math.log(q[i]) - math.log(p[i])) for i in range(v_s) if q[i] > 0)
+        assert np.isfinite(kl[n]) and abs(kl[n] - ref) <= 1e-12
