@@ -100,7 +100,9 @@ typedef enum kd_variant {
   KD_KL_FORWARD = 0,  /* KL(q||p)                                   */
   KD_KL_REVERSE = 1,  /* KL(p||q)                                   */
   KD_KL_JEFFREYS = 2, /* KL(q||p) + KL(p||q)                        */
-  KD_KL_SKEW_JS = 3   /* (1-b) KL(q||m) + b KL(p||m), m=(1-b)q+bp   */
+  KD_KL_SKEW_JS = 3,  /* (1-b) KL(q||m) + b KL(p||m), m=(1-b)q+bp   */
+  KD_KL_SKEW_FORWARD = 4, /* KL(q||m) (orda "skew_forward")              */
+  KD_KL_SKEW_REVERSE = 5  /* KL(p||m) (orda "skew_reverse")              */
 } kd_variant;
 
 typedef enum kd_reduction { KD_REDUCE_MEAN = 0, KD_REDUCE_SUM = 1 } kd_reduction;
@@ -122,7 +124,7 @@ typedef struct kd_problem {
   float w_student_ce;    /* >= 0, finite                                      */
   float w_teacher_ce;    /* >= 0, finite; 0 for top-K                         */
   float w_kl;            /* >= 0, finite                                      */
-  float beta;            /* skew-JS b in (0,1)                                */
+  float beta;            /* skew variants: b in (0,1) (kl_beta)              */
   int64_t ignore_index;  /* label value excluded from CE and KL               */
   int64_t num_batch_labels; /* > 0: mean divides by this instead of N_valid  */
   int32_t assume_valid_labels; /* 1: caller promises labels in range          */
@@ -148,8 +150,8 @@ typedef struct kd_inputs {
 
 /* Number of floats per token in the saved statistics written by kd_fwd and
  * read by kd_bwd: logsumexp(z_s), logsumexp(a_s), logsumexp(z_t),
- * logsumexp(a_t), KL(p||q), KL(p||m), top-K mass M, and
- * logsumexp(a_t) - logsumexp(a_s) evaluated to full relative precision. */
+ * logsumexp(a_t), KL(p||q), KL(p||m), top-K mass M (skew variants: E_p[p/m]),
+ * and logsumexp(a_t) - logsumexp(a_s) evaluated to full relative precision. */
 #define KD_STATS_PER_TOKEN 8
 
 /* Bytes of device workspace kd_fwd and kd_bwd need for this problem on the

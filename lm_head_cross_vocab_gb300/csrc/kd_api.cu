@@ -98,7 +98,7 @@ kd_status check_problem(const kd_problem* p) {
   if (p->student != KD_STUDENT_HIDDEN && p->student != KD_STUDENT_LOGITS)
     return KD_ERR_INVALID_ARG;
   if (p->teacher < KD_TEACHER_NONE || p->teacher > KD_TEACHER_TOPK) return KD_ERR_INVALID_ARG;
-  if (p->variant < KD_KL_FORWARD || p->variant > KD_KL_SKEW_JS) return KD_ERR_INVALID_ARG;
+  if (p->variant < KD_KL_FORWARD || p->variant > KD_KL_SKEW_REVERSE) return KD_ERR_INVALID_ARG;
   if (p->reduction != KD_REDUCE_MEAN && p->reduction != KD_REDUCE_SUM) return KD_ERR_INVALID_ARG;
   // orda-kernel README, "Parameters": term weights finite and >= 0
   if (!finite_nonneg(p->w_student_ce) || !finite_nonneg(p->w_teacher_ce) ||
@@ -108,7 +108,7 @@ kd_status check_problem(const kd_problem* p) {
       !(std::isfinite(p->t_teacher) && p->t_teacher > 0.f))
     return KD_ERR_INVALID_ARG;
   // orda-kernel README, "KL variants": kl_beta in (0, 1) for the skew family
-  if (p->variant == KD_KL_SKEW_JS && !(p->beta > 0.f && p->beta < 1.f)) return KD_ERR_INVALID_ARG;
+  if (is_skew(p->variant) && !(p->beta > 0.f && p->beta < 1.f)) return KD_ERR_INVALID_ARG;
   if (p->student == KD_STUDENT_HIDDEN && p->d_student < 1) return KD_ERR_INVALID_ARG;
   if (p->teacher == KD_TEACHER_SEPARATE && p->d_teacher < 1) return KD_ERR_INVALID_ARG;
   if (p->teacher == KD_TEACHER_TIED) {
@@ -169,7 +169,7 @@ Consts make_consts(const kd_problem* p, bool has_labels, bool has_t) {
     if (p->variant == KD_KL_FORWARD) c.kl_mode = 1;
     else if (p->variant == KD_KL_REVERSE) c.kl_mode = 2;
     else if (p->variant == KD_KL_JEFFREYS) c.kl_mode = 3;
-    else c.kl_mode = 1;  // skew-JS: forward sums give the accurate normaliser gap
+    else c.kl_mode = 1;  // skew variants: forward sums give the accurate normaliser gap
   }
   c.precise = p->dtype == KD_FP32 ? 1 : 0;
   // exact shortcuts for the T = 1 sums when the temperature is 1 or 2 (both sides)
@@ -476,7 +476,7 @@ kd_status kd_fwd(const kd_problem* problem, const kd_inputs* in, float* ce_s, fl
     launch_topk_prep(in->topk_idx, in->topk_p, n, (int)p->topk, P.v, sidx, sp, mass, ent,
                      dev_status, s);
   }
-  const bool js = P.has_t && p->variant == KD_KL_SKEW_JS;
+  const bool js = P.has_t && is_skew(p->variant);
   if (P.path == PATH_STREAM) {
     StreamArgs a;
     memset(&a, 0, sizeof(a));

@@ -124,9 +124,10 @@ __global__ void k_combine(CombineArgs a) {
   }
   float* srow = a.stats + r * KD_STATS_PER_TOKEN;
   if (a.js_pass) {
-    // skew-JS: the first pass already wrote the log-normalisers
-    const float kl = (1.f - a.c.beta) * st.jq + a.c.beta * st.jp;
+    // skew variants: the first pass already wrote the log-normalisers
+    const float kl = skew_kl(a.variant, a.c.beta, st.jq, st.jp);
     srow[S_KL_PM] = st.jp;
+    if (a.variant != KD_KL_SKEW_JS) srow[S_EPPM] = st.jx;
     if (a.kl) a.kl[r] = valid ? kl : 0.f;
     return;
   }

@@ -38,7 +38,22 @@ constexpr float kNoMass = -1e30f;
 // fields of the saved per-token statistics (KD_STATS_PER_TOKEN floats)
 // S_DLSE = logsumexp(a_t) - logsumexp(a_s), taken from the accurate log1p form
 // of the forward-KL sums rather than from the difference of the two stored values.
+// S_MASS holds the top-K mass M for top-K teachers and E_p[p/m] for the
+// skew variants (never both).
 enum StatField { S_LSE_S1 = 0, S_LSE_ST, S_LSE_T1, S_LSE_TT, S_KL_REV, S_KL_PM, S_MASS, S_DLSE };
+constexpr int S_EPPM = S_MASS;
+
+// Variants whose divergence is against the mixture m = (1-b) q + b p (a
+// second sweep once both normalisers are known).
+__host__ __device__ __forceinline__ bool is_skew(int v) {
+  return v == KD_KL_SKEW_JS || v == KD_KL_SKEW_FORWARD || v == KD_KL_SKEW_REVERSE;
+}
+// The divergence of a skew variant from the second-sweep sums
+// jq = KL(q||m) and jp = KL(p||m).
+__host__ __device__ __forceinline__ float skew_kl(int v, float beta, float jq, float jp) {
+  return v == KD_KL_SKEW_FORWARD ? jq : v == KD_KL_SKEW_REVERSE ? jp
+                                                                : (1.f - beta) * jq + beta * jp;
+}
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -74,12 +89,12 @@ struct Consts {
 };
 
 struct RowState {
-  float ms, ls1, lsT, mt, lt1, ltT, qd, qx, pd, px, zys, zyt, tk, jq, jp;
+  float ms, ls1, lsT, mt, lt1, ltT, qd, qx, pd, px, zys, zyt, tk, jq, jp, jx;
   float cq, cp;  // cached e^{Ms-Mt}, e^{Mt-Ms} for the current maxima (< 0: stale)
 
   __device__ __forceinline__ void init() {
     ms = mt = neg_inf();
-    ls1 = lsT = lt1 = ltT = qd = qx = pd = px = zys = zyt = tk = jq = jp = 0.f;
+    ls1 = lsT = lt1 = ltT = qd = qx = pd = px = zys = zyt = tk = jq = jp = jx = 0.f;
     cq = cp = -1.f;
   }
   __device__ __forceinline__ void store(float* r) const {
@@ -87,7 +102,7 @@ struct RowState {
     o[0] = make_float4(ms, ls1, lsT, mt);
     o[1] = make_float4(lt1, ltT, qd, qx);
     o[2] = make_float4(pd, px, zys, zyt);
-    o[3] = make_float4(tk, jq, jp, 0.f);
+    o[3] = make_float4(tk, jq, jp, jx);
   }
   __device__ __forceinline__ void load(const float* r) {
     const float4* i = reinterpret_cast<const float4*>(r);
@@ -95,7 +110,7 @@ struct RowState {
     ms = a.x; ls1 = a.y; lsT = a.z; mt = a.w;
     lt1 = b.x; ltT = b.y; qd = b.z; qx = b.w;
     pd = c.x; px = c.y; zys = c.z; zyt = c.w;
-    tk = d.x; jq = d.y; jp = d.z;
+    tk = d.x; jq = d.y; jp = d.z; jx = d.w;
     cq = cp = -1.f;
   }
 };
@@ -132,6 +147,7 @@ __device__ __forceinline__ void merge(RowState& a, const RowState& b, const Cons
   a.tk += b.tk;
   a.jq += b.jq;
   a.jp += b.jp;
+  a.jx += b.jx;
   a.cq = a.cp = -1.f;
 }
 
@@ -152,6 +168,7 @@ __device__ __forceinline__ RowState shfl_xor(const RowState& s, int m) {
   o.tk = __shfl_xor_sync(0xffffffffu, s.tk, m);
   o.jq = __shfl_xor_sync(0xffffffffu, s.jq, m);
   o.jp = __shfl_xor_sync(0xffffffffu, s.jp, m);
+  o.jx = __shfl_xor_sync(0xffffffffu, s.jx, m);
   o.cq = o.cp = -1.f;
   return o;
 }
@@ -169,12 +186,12 @@ __device__ __forceinline__ void warp_merge(RowState& s, const Consts& c) {
   }
   const float fs1 = rescale(s.ms, m_s, c.k_s1), fsT = rescale(s.ms, m_s, c.k_sT);
   const float ft1 = rescale(s.mt, m_t, c.k_t1), ftT = rescale(s.mt, m_t, c.k_tT);
-  float v[13] = {s.ls1 * fs1, s.lsT * fsT, s.pd * fsT, s.px * fsT, s.lt1 * ft1, s.ltT * ftT,
-                 s.qd * ftT, s.qx * ftT, s.zys, s.zyt, s.tk, s.jq, s.jp};
+  float v[14] = {s.ls1 * fs1, s.lsT * fsT, s.pd * fsT, s.px * fsT, s.lt1 * ft1, s.ltT * ftT,
+                 s.qd * ftT, s.qx * ftT, s.zys, s.zyt, s.tk, s.jq, s.jp, s.jx};
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
 #pragma unroll
-    for (int i = 0; i < 13; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
+    for (int i = 0; i < 14; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
   }
   s.ms = m_s;
   s.mt = m_t;
@@ -191,6 +208,7 @@ __device__ __forceinline__ void warp_merge(RowState& s, const Consts& c) {
   s.tk = v[10];
   s.jq = v[11];
   s.jp = v[12];
+  s.jx = v[13];
   s.cq = s.cp = -1.f;
 }
 
@@ -369,9 +387,9 @@ __device__ __forceinline__ RowOut finalize(const RowState& s, const Consts& c, i
     if (variant == KD_KL_FORWARD) o.kl = kl_f;
     else if (variant == KD_KL_REVERSE) o.kl = kl_r;
     else if (variant == KD_KL_JEFFREYS) o.kl = kl_f + kl_r;
-    else {  // skew-JS: second-pass sums jq = sum q log(q/m), jp = sum p log(p/m)
+    else {  // skew variants: second-pass sums jq = sum q log(q/m), jp = sum p log(p/m)
       o.kl_pm = s.jp;
-      o.kl = (1.f - c.beta) * s.jq + c.beta * s.jp;
+      o.kl = skew_kl(variant, c.beta, s.jq, s.jp);
     }
   }
   return o;
@@ -398,11 +416,13 @@ __device__ __forceinline__ void js_logs(float x, const Consts& c, float& lqm, fl
   lpm = neg ? x - l : -l;
 }
 
-// Skew-JS second pass: with the final normalisers known, accumulate
-// jq += q log(q/m) and jp += p log(p/m) (p and q each from its own
-// log-normaliser, so neither inherits the other's range).
+// Skew second pass: with the final normalisers known, accumulate
+// jq += q log(q/m), jp += p log(p/m) and, when the variant's gradient needs
+// E_p[p/m] (skew-forward, skew-reverse), jx += p (p/m).  p and q come each
+// from its own log-normaliser, so neither inherits the other's range.
 __device__ __forceinline__ void js_terms(float zs, float zt, float lse_tT, float dlse,
-                                         const Consts& c, float& jq, float& jp) {
+                                         const Consts& c, float& jq, float& jp, float& jx,
+                                         bool want_x) {
   const float x = fmaf(zs, c.inv_ts, -zt * c.inv_tt) + dlse;
   const float lq = zt * c.inv_tt - lse_tT;
   const float lp = fmaf(zs, c.inv_ts, dlse - lse_tT);  // a_s - lse(a_s)
@@ -411,22 +431,40 @@ __device__ __forceinline__ void js_terms(float zs, float zt, float lse_tT, float
   const float q = ex2(lq * kL2E), p = ex2(lp * kL2E);
   jq = fmaf(q, lqm, jq);
   jp = fmaf(p, lpm, jp);
+  if (want_x) jx = fmaf(p, ex2(lpm * kL2E), jx);
+}
+
+// d KL / d a_s of the skew variants (teacher detached), from p, log(q/m),
+// log(p/m), KL(p||m) and E_p[p/m] (with (1-b) q/m + b p/m = 1):
+//   skew-JS       b p (log(p/m) - KL(p||m))
+//   skew-forward  -b p (q/m - E_p[q/m]),  E_p[q/m] = (1 - b E_p[p/m]) / (1 - b)
+//   skew-reverse  p (log(p/m) - KL(p||m)) - b p (p/m - E_p[p/m])
+__device__ __forceinline__ float skew_grad(int variant, float p, float lqm, float lpm,
+                                           float kl_pm, float eppm, const Consts& c) {
+  const float b = c.beta;
+  if (variant == KD_KL_SKEW_FORWARD) {
+    const float eqm = (1.f - b * eppm) / (1.f - b);
+    return -b * p * (ex2(lqm * kL2E) - eqm);
+  }
+  if (variant == KD_KL_SKEW_REVERSE)
+    return p * (lpm - kl_pm) - b * p * (ex2(lpm * kL2E) - eppm);
+  return b * p * (lpm - kl_pm);
 }
 
 // Gradient of the KL part w.r.t. a_s (teacher detached), per element, from
 // the saved statistics:
 //   forward  p - q;  reverse p (log p - log q - KL(p||q));  Jeffreys the sum;
-//   skew-JS  b p (log p - log m - KL(p||m)).
+//   skew variants: skew_grad().
 __device__ __forceinline__ float kl_grad(float zs, float zt, const float* stt, int variant,
                                          const Consts& c) {
   const float lp = zs * c.inv_ts - stt[S_LSE_ST];
   const float lq = zt * c.inv_tt - stt[S_LSE_TT];
   const float p = ex2(lp * kL2E);
-  if (variant == KD_KL_SKEW_JS) {
+  if (is_skew(variant)) {
     const float x = fmaf(zs, c.inv_ts, -zt * c.inv_tt) + stt[S_DLSE];
     float lqm, lpm;
     js_logs(x, c, lqm, lpm);
-    return c.beta * p * (lpm - stt[S_KL_PM]);
+    return skew_grad(variant, p, lqm, lpm, stt[S_KL_PM], stt[S_EPPM], c);
   }
   float g = 0.f;
   if (variant != KD_KL_REVERSE) g = p - ex2(lq * kL2E);
@@ -438,11 +476,11 @@ __device__ __forceinline__ float kl_grad(float zs, float zt, const float* stt, i
 __device__ __forceinline__ float kl_grad_pq(float zs, float zt, float lp, float lq, float p,
                                             float q, const float* stt, int variant,
                                             const Consts& c) {
-  if (variant == KD_KL_SKEW_JS) {
+  if (is_skew(variant)) {
     const float x = fmaf(zs, c.inv_ts, -zt * c.inv_tt) + stt[S_DLSE];
     float lqm, lpm;
     js_logs(x, c, lqm, lpm);
-    return c.beta * p * (lpm - stt[S_KL_PM]);
+    return skew_grad(variant, p, lqm, lpm, stt[S_KL_PM], stt[S_EPPM], c);
   }
   float g = 0.f;
   if (variant != KD_KL_REVERSE) g = p - q;

@@ -194,22 +194,25 @@ __device__ __forceinline__ bool async_merge(RowState& st, const Consts& c, const
   return true;
 }
 
-__device__ __forceinline__ float2 consumer_sum2(float x, float y, const Ring& R) {
+__device__ __forceinline__ float3 consumer_sum3(float x, float y, float z, const Ring& R) {
   for (int o = 16; o > 0; o >>= 1) {
     x += __shfl_xor_sync(0xffffffffu, x, o);
     y += __shfl_xor_sync(0xffffffffu, y, o);
+    z += __shfl_xor_sync(0xffffffffu, z, o);
   }
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   if (l == 0) {
-    R.recs[2 * w] = x;
-    R.recs[2 * w + 1] = y;
+    R.recs[3 * w] = x;
+    R.recs[3 * w + 1] = y;
+    R.recs[3 * w + 2] = z;
   }
   ptx::named_sync(1, kCT);
-  float2 r = make_float2(0.f, 0.f);
+  float3 r = make_float3(0.f, 0.f, 0.f);
   if (threadIdx.x == 0)
     for (int i = 0; i < kCW; ++i) {
-      r.x += R.recs[2 * i];
-      r.y += R.recs[2 * i + 1];
+      r.x += R.recs[3 * i];
+      r.y += R.recs[3 * i + 1];
+      r.z += R.recs[3 * i + 2];
     }
   ptx::named_sync(1, kCT);
   return r;
@@ -350,7 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd(StreamArgs a, uint32_t* sta
       }
       ptx::named_sync(1, kCT);
       const float dlse = R.bcast[0], lse_tT = R.bcast[1];
-      float jq = 0.f, jp = 0.f;
+      const bool want_x = a.variant != KD_KL_SKEW_JS;
+      float jq = 0.f, jp = 0.f, jx = 0.f;
       for (int ch = 0; ch < nch; ++ch) {
         const uint8_t* buf = cur.acquire(R, status);
         float fs[kSlots][EPT], ft[kSlots][EPT];
@@ -369,13 +373,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd(StreamArgs a, uint32_t* sta
         for (int j = 0; j < kSlots; ++j)
 #pragma unroll
           for (int u = 0; u < EPT; ++u)
-            if (u < nv[j]) js_terms(fs[j][u], ft[j][u], lse_tT, dlse, c, jq, jp);
+            if (u < nv[j]) js_terms(fs[j][u], ft[j][u], lse_tT, dlse, c, jq, jp, jx, want_x);
       }
-      const float2 r = consumer_sum2(jq, jp, R);
+      const float3 r = consumer_sum3(jq, jp, jx, R);
       if (ct == 0) {
         const bool v_ok = !a.labels || y != a.ignore;
         a.stats[row * KD_STATS_PER_TOKEN + S_KL_PM] = r.y;
-        if (a.kl) a.kl[row] = v_ok ? (1.f - c.beta) * r.x + c.beta * r.y : 0.f;
+        if (want_x) a.stats[row * KD_STATS_PER_TOKEN + S_EPPM] = r.z;
+        if (a.kl) a.kl[row] = v_ok ? skew_kl(a.variant, c.beta, r.x, r.y) : 0.f;
       }
       ptx::named_sync(1, kCT);  // reduction slots are reused by the next row
     }
@@ -439,7 +444,7 @@ inline void launch(K kernel, const StreamArgs& a, cudaStream_t s) {
 template <typename T, bool HAS_T, class Acc>
 inline void launch_fwd(const StreamArgs& a, cudaStream_t s) {
   if constexpr (HAS_T) {
-    if (a.variant == KD_KL_SKEW_JS) {
+    if (is_skew(a.variant)) {
       launch(k_fwd<T, HAS_T, Acc, 2>, a, s);
       return;
     }

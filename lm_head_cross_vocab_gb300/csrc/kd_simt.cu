@@ -114,7 +114,8 @@ __global__ void __launch_bounds__(NT) k_simt_fwd(SimtArgs a) {
       }
       if (a.js_pass) {
         for (int j = 0; j < nv; ++j)
-          js_terms(zs[j], zt[j], stt[S_LSE_TT], stt[S_DLSE], c, st.jq, st.jp);
+          js_terms(zs[j], zt[j], stt[S_LSE_TT], stt[S_DLSE], c, st.jq, st.jp, st.jx,
+                   a.variant != KD_KL_SKEW_JS);
       } else {
         if (has_t) update<8, true, true>(st, zs, zt, nv, c);
         else update<8, false, true>(st, zs, zt, nv, c);

@@ -36,23 +36,26 @@ __device__ __forceinline__ void block_merge(RowState& st, const Consts& c, float
   }
 }
 
-__device__ __forceinline__ float2 block_sum2(float a, float b, float* sh) {
+__device__ __forceinline__ float3 block_sum3(float a, float b, float d, float* sh) {
   for (int o = 16; o > 0; o >>= 1) {
     a += __shfl_xor_sync(0xffffffffu, a, o);
     b += __shfl_xor_sync(0xffffffffu, b, o);
+    d += __shfl_xor_sync(0xffffffffu, d, o);
   }
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   __syncthreads();
   if (l == 0) {
-    sh[2 * w] = a;
-    sh[2 * w + 1] = b;
+    sh[3 * w] = a;
+    sh[3 * w + 1] = b;
+    sh[3 * w + 2] = d;
   }
   __syncthreads();
-  float2 r = make_float2(0.f, 0.f);
+  float3 r = make_float3(0.f, 0.f, 0.f);
   if (threadIdx.x == 0)
     for (int i = 0; i < (int)(blockDim.x >> 5); ++i) {
-      r.x += sh[2 * i];
-      r.y += sh[2 * i + 1];
+      r.x += sh[3 * i];
+      r.y += sh[3 * i + 1];
+      r.z += sh[3 * i + 2];
     }
   return r;
 }
@@ -112,24 +115,26 @@ __global__ void __launch_bounds__(kThreads) k_stream_fwd(StreamArgs a) {
       const float nan = __int_as_float(0x7fc00000);
       if (a.ce_s) a.ce_s[row] = !valid ? 0.f : (bad ? nan : o.ce_s);
       if (a.ce_t) a.ce_t[row] = !valid ? 0.f : (bad ? nan : o.ce_t);
-      if (a.kl && !(HAS_T && a.variant == KD_KL_SKEW_JS)) a.kl[row] = valid ? o.kl : 0.f;
+      if (a.kl && !(HAS_T && is_skew(a.variant))) a.kl[row] = valid ? o.kl : 0.f;
       float4* s4 = reinterpret_cast<float4*>(a.stats + row * KD_STATS_PER_TOKEN);
       s4[0] = make_float4(o.lse_s1, o.lse_sT, o.lse_t1, o.lse_tT);
       s4[1] = make_float4(o.kl_rev, 0.f, mass, o.dlse);
       sh_lse[0] = o.dlse;
       sh_lse[1] = o.lse_tT;
     }
-    if (HAS_T && a.variant == KD_KL_SKEW_JS) {
+    if (HAS_T && is_skew(a.variant)) {
       __syncthreads();
       const float dlse = sh_lse[0], lse_tT = sh_lse[1];
-      float jq = 0.f, jp = 0.f;
+      const bool want_x = a.variant != KD_KL_SKEW_JS;
+      float jq = 0.f, jp = 0.f, jx = 0.f;
       for (int64_t e = threadIdx.x; e < V; e += kThreads)
-        js_terms(ld1<T>(zs + e), ld1<T>(zt + e), lse_tT, dlse, c, jq, jp);
-      const float2 r = block_sum2(jq, jp, sh);
+        js_terms(ld1<T>(zs + e), ld1<T>(zt + e), lse_tT, dlse, c, jq, jp, jx, want_x);
+      const float3 r = block_sum3(jq, jp, jx, sh);
       if (threadIdx.x == 0) {
         const bool v_ok = !a.labels || a.labels[row] != a.ignore;
         a.stats[row * KD_STATS_PER_TOKEN + S_KL_PM] = r.y;
-        if (a.kl) a.kl[row] = v_ok ? (1.f - c.beta) * r.x + c.beta * r.y : 0.f;
+        if (want_x) a.stats[row * KD_STATS_PER_TOKEN + S_EPPM] = r.z;
+        if (a.kl) a.kl[row] = v_ok ? skew_kl(a.variant, c.beta, r.x, r.y) : 0.f;
       }
     }
     __syncthreads();

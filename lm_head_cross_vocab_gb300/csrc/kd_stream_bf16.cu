@@ -275,7 +275,7 @@ struct PackedGrad {
     csq = (CE && PW == 2) ? swc * ex2((2.f * st[S_LSE_ST] - st[S_LSE_S1]) * kL2E) : swc;
     kl_r = HAS_T ? st[S_KL_REV] : 0.f;
     y = (CE && a.labels) ? a.labels[r] : -1;
-    if (HAS_T && VAR == KD_KL_SKEW_JS) {
+    if (HAS_T && is_skew(VAR)) {
       c = a.c;
 #pragma unroll
       for (int i = 0; i < KD_STATS_PER_TOKEN; ++i) sv[i] = st[i];
@@ -296,8 +296,8 @@ struct PackedGrad {
         if (VAR == KD_KL_REVERSE) g = mul2(mul2(p, splat(sw)), r);
         else g = mul2(fma2(p, r, sub2(p, ex2x2(lq2))), splat(sw));
       } else {
-        g.x = sw * kl_grad_pq(s.x, t.x, 0.f, 0.f, p.x, 0.f, sv, KD_KL_SKEW_JS, c);
-        g.y = sw * kl_grad_pq(s.y, t.y, 0.f, 0.f, p.y, 0.f, sv, KD_KL_SKEW_JS, c);
+        g.x = sw * kl_grad_pq(s.x, t.x, 0.f, 0.f, p.x, 0.f, sv, VAR, c);
+        g.y = sw * kl_grad_pq(s.y, t.y, 0.f, 0.f, p.y, 0.f, sv, VAR, c);
       }
     } else {
       g = mul2(p, splat(sw));
@@ -384,6 +384,8 @@ bool launch_stream_bwd_packed(const StreamArgs& a, cudaStream_t s) {
     case KD_KL_REVERSE: bwd_pw<true, KD_KL_REVERSE>(a, s); return true;
     case KD_KL_JEFFREYS: bwd_pw<true, KD_KL_JEFFREYS>(a, s); return true;
     case KD_KL_SKEW_JS: bwd_pw<true, KD_KL_SKEW_JS>(a, s); return true;
+    case KD_KL_SKEW_FORWARD: bwd_pw<true, KD_KL_SKEW_FORWARD>(a, s); return true;
+    case KD_KL_SKEW_REVERSE: bwd_pw<true, KD_KL_SKEW_REVERSE>(a, s); return true;
     default: return false;
   }
 }

@@ -411,9 +411,10 @@ struct FwdEpi {
     if (a.js_pass) {
       const float* stt = a.stats + row * KD_STATS_PER_TOKEN;
       const float lt = stt[S_LSE_TT], dl = stt[S_DLSE];
+      const bool want_x = a.variant != KD_KL_SKEW_JS;
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if (j < nv) js_terms(vs[j], vt[j], lt, dl, a.c, st.jq, st.jp);
+        if (j < nv) js_terms(vs[j], vt[j], lt, dl, a.c, st.jq, st.jp, st.jx, want_x);
       return;
     }
     if (nv == 32) update<32, HAS_T, false>(st, vs, vt, 32, a.c);
@@ -476,7 +477,9 @@ struct GradRow {
   float wk_r, klr;       // s w_kl T_s ln 2, s w_kl T_s KL(p||q)   (reverse terms)
   float wc, cs, n1s;     // s w_sce; its p^2 coefficient (T = 2); -lse(z_s) log2 e
   float wt, ct, n1t;     // tied teacher CE: s w_tce; its q^2 coefficient; -lse(z_t) log2 e
-  float bwk, dlse, klpm; // skew-JS: s w_kl T_s b; lse(a_t) - lse(a_s); KL(p||m)
+  float dlse, klpm;      // skew variants: lse(a_t) - lse(a_s); KL(p||m)
+  float eppm;            // skew-forward / skew-reverse: E_p[p/m]
+  int var;               // kd_variant
   bool live;             // row inside the chunk with a nonzero scale
 };
 
@@ -506,9 +509,10 @@ __device__ __forceinline__ GradRow grad_row(const TcGradArgs& a, int64_t row, bo
   r.wt = scale * a.w_tce;
   r.ct = (pw == 2 && a.gt) ? r.wt * ex2((2.f * sv[S_LSE_TT] - sv[S_LSE_T1]) * kL2E) : 0.f;
   r.n1t = -sv[S_LSE_T1] * kL2E;
-  r.bwk = wkl * c.beta;
   r.dlse = sv[S_DLSE];
   r.klpm = sv[S_KL_PM];
+  r.eppm = sv[S_EPPM];
+  r.var = a.variant;
   return r;
 }
 
@@ -528,7 +532,7 @@ __device__ __forceinline__ void grad32(float* vs, const float* vt, const GradRow
       const float x = fmaf(vs[j], c.inv_ts, -vt[j] * c.inv_tt) + r.dlse;
       float lqm, lpm;
       js_logs(x, c, lqm, lpm);
-      g = r.bwk * p * (lpm - r.klpm);
+      g = r.wk * skew_grad(r.var, p, lqm, lpm, r.klpm, r.eppm, c);
     } else {
       const float l2q = fmaf(vt[j], r.kt, r.nt);
       if (VAR == GV_FWD) {

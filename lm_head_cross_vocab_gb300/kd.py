@@ -31,6 +31,7 @@ KD_BF16, KD_FP32 = 0, 1
 KD_STUDENT_HIDDEN, KD_STUDENT_LOGITS = 0, 1
 KD_TEACHER_NONE, KD_TEACHER_TIED, KD_TEACHER_SEPARATE, KD_TEACHER_LOGITS, KD_TEACHER_TOPK = range(5)
 KD_KL_FORWARD, KD_KL_REVERSE, KD_KL_JEFFREYS, KD_KL_SKEW_JS = range(4)
+KD_KL_SKEW_FORWARD, KD_KL_SKEW_REVERSE = 4, 5
 KD_REDUCE_MEAN, KD_REDUCE_SUM = 0, 1
 KD_STATS_PER_TOKEN = 8
 KD_STATIC_SCRATCH_BYTES = 32 << 20
@@ -41,7 +42,8 @@ STUDENTS = {"hidden": KD_STUDENT_HIDDEN, "logits": KD_STUDENT_LOGITS}
 TEACHERS = {"none": KD_TEACHER_NONE, "tied": KD_TEACHER_TIED, "separate": KD_TEACHER_SEPARATE,
             "logits": KD_TEACHER_LOGITS, "topk": KD_TEACHER_TOPK}
 VARIANTS = {"forward": KD_KL_FORWARD, "reverse": KD_KL_REVERSE, "jeffreys": KD_KL_JEFFREYS,
-            "skew_js": KD_KL_SKEW_JS}
+            "skew_js": KD_KL_SKEW_JS, "skew_forward": KD_KL_SKEW_FORWARD,
+            "skew_reverse": KD_KL_SKEW_REVERSE}
 REDUCTIONS = {"mean": KD_REDUCE_MEAN, "sum": KD_REDUCE_SUM}
 
 

@@ -23,14 +23,14 @@ def _lib():
 
 # ----------------------------------------------------------- streaming path
 
-@pytest.mark.parametrize("variant", ["forward", "reverse", "jeffreys", "skew_js"])
+@pytest.mark.parametrize("variant", ["forward", "reverse", "jeffreys", "skew_js", "skew_forward", "skew_reverse"])
 @pytest.mark.parametrize("vocab", [4104, 4099])  # vectorised rows, ragged scalar rows
 def test_logit_pair_streaming(variant, vocab):
     w = W[5].scaled(n_tokens=67, vocab=vocab, variant=variant)
     assert_parity(run_and_compare(w), "bf16")
 
 
-@pytest.mark.parametrize("variant", ["jeffreys", "skew_js"])
+@pytest.mark.parametrize("variant", ["jeffreys", "skew_js", "skew_reverse"])
 def test_logit_pair_streaming_more_rows_than_ctas(variant):
     """More rows than persistent CTAs: each CTA streams several rows (two sweeps
     each for skew-JS) through one ring, so stage phases carry across rows."""
@@ -46,7 +46,7 @@ def test_logit_pair_streaming_rows_longer_than_the_ring(variant):
     assert_parity(run_and_compare(w), "bf16")
 
 
-@pytest.mark.parametrize("variant", ["forward", "reverse", "jeffreys", "skew_js"])
+@pytest.mark.parametrize("variant", ["forward", "reverse", "jeffreys", "skew_js", "skew_forward", "skew_reverse"])
 def test_logit_pair_streaming_t1_with_student_ce(variant):
     """T = 1 with a student CE term: the packed kernels' T = 1 shortcut and
     their label-column correction."""
@@ -97,7 +97,7 @@ def test_topk_with_logit_student_t2_and_ce_streaming():
 
 # ----------------------------------------------------------- fp32 CUDA cores
 
-@pytest.mark.parametrize("variant", ["forward", "reverse", "jeffreys", "skew_js"])
+@pytest.mark.parametrize("variant", ["forward", "reverse", "jeffreys", "skew_js", "skew_forward", "skew_reverse"])
 def test_tiny_tied_fp32(variant):
     """The tiny tied fp32 workload (64 tokens, D=64, V=512, T=2), all variants."""
     assert_parity(run_and_compare(W[1].scaled(variant=variant)), "fp32")
@@ -140,7 +140,7 @@ def test_separate_teacher_bf16_small():
     assert_parity(run_and_compare(w), "bf16")
 
 
-@pytest.mark.parametrize("variant", ["forward", "reverse", "skew_js"])
+@pytest.mark.parametrize("variant", ["forward", "reverse", "skew_js", "skew_forward", "skew_reverse"])
 def test_separate_teacher_bf16_variants(variant):
     w = W[2].scaled(n_tokens=200, d_student=64, d_teacher=192, vocab=1500, variant=variant,
                     t_teacher=1.5)
