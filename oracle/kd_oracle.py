@@ -31,6 +31,10 @@ Sources (page title, section):
     renormalised; "Full Chunked KL": closed-form gradient M softmax(z) - p.
   * nemo_automodel kd_loss API doc, KDLoss: loss multiplied by T^2; mean
     over valid tokens, or sum / num_batch_labels.
+  * orda-kernel README, "Cross-vocabulary distillation": token-map
+    projection (duplicates sum in probability space, unmatched ids -inf,
+    tempering before aggregation) and multi-teacher mixing (probability
+    average or product of experts of cached teacher distributions).
 
 Readings where the pages are silent (each is also listed in the design notes):
   * Skew-JS(beta) = (1-beta) KL(q||m) + beta KL(p||m), m = (1-beta) q + beta p.
@@ -41,6 +45,8 @@ Readings where the pages are silent (each is also listed in the design notes):
   * The loss is sum_valid(w_sce CE_s + w_tce CE_t + w_kl T_s^2 KL) / denom.
   * Top-K teachers use a_s = z_s / T_s in the objective (T_s = 1 in the
     pages' workload) and no labels unless CE is requested.
+  * Multi-teacher mixing normalises its weights to sum to 1 and returns the
+    mixture's log-probabilities; a teacher with weight 0 takes no part.
 
 Parity pins: every function here is checked against closed forms, scipy
 library routines, finite differences and brute force in
@@ -183,6 +189,44 @@ def project_teacher_logits(z_t, token_map, v_student, temperature=1.0):
     s = np.add.reduceat(np.exp(zz - np.repeat(m, lengths, axis=1)), starts, axis=1)
     out[:, ids[starts]] = m + np.log(s)
     return out
+
+
+# ----------------------------------------------------------------------------
+# multi-teacher mixing (orda-kernel README, "Cross-vocabulary distillation",
+# multi-teacher mixing)
+# ----------------------------------------------------------------------------
+
+MIX_MODES = ("arithmetic", "geometric")
+
+
+def mix_teacher_logits(logits, weights=None, mode="arithmetic"):
+    """Mix K cached teacher distributions over one vocabulary into one, returned
+    as normalised log-probabilities (logits of the mixture).  Teacher k gives
+    q_k = softmax(z_k); the weights are non-negative and are normalised to sum
+    to 1 (uniform when omitted).
+      arithmetic (probability average): q = sum_k w_k q_k
+      geometric (product of experts):  q proportional to prod_k q_k ** w_k
+    """
+    zs = [as_f64(z) for z in logits]
+    k = len(zs)
+    if k == 0:
+        raise ValueError("need at least one teacher")
+    w = np.ones(k) if weights is None else np.asarray(weights, dtype=np.float64)
+    if w.shape != (k,) or np.any(w < 0) or not np.any(w > 0):
+        raise ValueError("weights: k non-negative values, not all zero")
+    w = w / w.sum()
+    if mode == "arithmetic":
+        # log sum_k w_k exp(log q_k), over the teachers with w_k > 0
+        terms = np.stack([np.log(w[i]) + log_softmax(zs[i]) for i in range(k) if w[i] > 0])
+        top = terms.max(axis=0)
+        with np.errstate(invalid="ignore", divide="ignore"):
+            shifted = np.where(np.isneginf(top), -np.inf, terms - top)
+            return top + np.log(np.exp(shifted).sum(axis=0))
+    if mode == "geometric":
+        # log prod_k q_k^{w_k} = sum_k w_k log q_k, then normalised
+        g = sum(w[i] * log_softmax(zs[i]) for i in range(k) if w[i] > 0)
+        return g - logsumexp(g)[:, None]
+    raise ValueError(f"unknown mode {mode!r}")
 
 
 # ----------------------------------------------------------------------------

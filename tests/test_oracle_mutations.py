@@ -67,6 +67,30 @@ def _unmatched_get_zero_logit(orig):
     return project_teacher_logits
 
 
+def _mix_logits_not_probabilities(orig):
+    def mix_teacher_logits(logits, weights=None, mode="arithmetic"):
+        return orig(logits, weights, "geometric")  # a weighted sum of log-probabilities
+    return mix_teacher_logits
+
+
+def _mix_weights_unnormalised(orig):
+    def mix_teacher_logits(logits, weights=None, mode="arithmetic"):
+        w = np.ones(len(logits)) if weights is None else np.asarray(weights, dtype=np.float64)
+        return orig(logits, w, mode) + (np.log(w.sum()) if mode == "arithmetic" else 0.0)
+    return mix_teacher_logits
+
+
+def _geometric_not_renormalised(orig):
+    def mix_teacher_logits(logits, weights=None, mode="arithmetic"):
+        out = orig(logits, weights, mode)
+        if mode == "geometric":
+            w = np.ones(len(logits)) if weights is None else np.asarray(weights, dtype=np.float64)
+            w = w / w.sum()
+            out = sum(w[k] * O.log_softmax(O.as_f64(z)) for k, z in enumerate(logits))
+        return out
+    return mix_teacher_logits
+
+
 def _no_t_squared():
     orig = O.forward
 
@@ -91,6 +115,9 @@ MUTATIONS = [
      P.test_projection_moves_teacher_probability_mass),
     ("project_teacher_logits", _unmatched_get_zero_logit,
      P.test_projection_moves_teacher_probability_mass),
+    ("mix_teacher_logits", _mix_logits_not_probabilities, P.test_mix_hand_worked_example),
+    ("mix_teacher_logits", _mix_weights_unnormalised, P.test_mix_hand_worked_example),
+    ("mix_teacher_logits", _geometric_not_renormalised, P.test_mix_brute_force_probabilities),
 ]
 
 

@@ -464,3 +464,76 @@ def test_projected_teacher_kl_drops_zero_probability_ids():
         p = sps.softmax(a_s[n])
         ref = math.fsum(q[i] * (math.log(q[i]) - math.log(p[i])) for i in range(v_s) if q[i] > 0)
         assert np.isfinite(kl[n]) and abs(kl[n] - ref) <= 1e-12
+
+
+# ---------------------------------------------------------------- multi-teacher mixing
+
+@pytest.mark.parametrize("mode", O.MIX_MODES)
+def test_mix_of_one_teacher_is_its_log_softmax(mode):
+    """A single teacher (any positive weight) is returned as its own
+    log-probabilities (scipy log_softmax)."""
+    z = _rand_logits(4, 13, std=3.0)
+    out = O.mix_teacher_logits([z], [2.5], mode)
+    np.testing.assert_allclose(out, sps.log_softmax(z, axis=-1), rtol=0, atol=1e-13)
+
+
+def test_mix_hand_worked_example():
+    """Two teachers over three tokens with known probabilities, weights 1 : 3.
+    Probability average: 0.25 [.5 .25 .25] + 0.75 [.1 .2 .7] = [.2 .2125 .5875].
+    Product of experts: p1^(1/4) p2^(3/4) per token, divided by its sum
+    (math.pow products, not the oracle's log-space sum)."""
+    p1, p2 = [0.5, 0.25, 0.25], [0.1, 0.2, 0.7]
+    z1 = np.log([p1]) + 5.0  # logits = log-probabilities up to a row constant
+    z2 = np.log([p2]) - 2.0
+    ari = np.exp(O.mix_teacher_logits([z1, z2], [1.0, 3.0], "arithmetic"))[0]
+    np.testing.assert_allclose(ari, [0.2, 0.2125, 0.5875], rtol=1e-14, atol=0)
+    r = [math.pow(a, 0.25) * math.pow(b, 0.75) for a, b in zip(p1, p2)]
+    geo = np.exp(O.mix_teacher_logits([z1, z2], [1.0, 3.0], "geometric"))[0]
+    np.testing.assert_allclose(geo, [x / math.fsum(r) for x in r], rtol=1e-13, atol=0)
+
+
+def test_mix_brute_force_probabilities():
+    """Three teachers with random logits and weights: the arithmetic mixture is
+    sum_k w_k softmax(z_k) and the geometric one prod_k softmax(z_k)^w_k
+    renormalised, both computed token by token in probability space."""
+    rng = np.random.default_rng(31)
+    zs = [rng.normal(0.0, 2.0, size=(3, 7)) for _ in range(3)]
+    w = np.array([0.2, 1.3, 0.5])
+    wn = w / w.sum()
+    ari = O.mix_teacher_logits(zs, w, "arithmetic")
+    geo = O.mix_teacher_logits(zs, w, "geometric")
+    for n in range(3):
+        qs = [sps.softmax(z[n]) for z in zs]
+        mix = [math.fsum(wn[k] * qs[k][v] for k in range(3)) for v in range(7)]
+        np.testing.assert_allclose(np.exp(ari[n]), mix, rtol=1e-13, atol=0)
+        poe = [math.prod(math.pow(qs[k][v], wn[k]) for k in range(3)) for v in range(7)]
+        np.testing.assert_allclose(np.exp(geo[n]), [x / math.fsum(poe) for x in poe], rtol=1e-12)
+
+
+@pytest.mark.parametrize("mode", O.MIX_MODES)
+def test_mix_invariances_and_zero_weight(mode):
+    """Shifting a teacher's row by a constant or scaling all weights changes
+    nothing; a teacher with weight 0 takes no part; the output is a normalised
+    log-distribution."""
+    rng = np.random.default_rng(5)
+    zs = [rng.normal(0.0, 3.0, size=(5, 17)) for _ in range(3)]
+    base = O.mix_teacher_logits(zs[:2], [0.3, 0.7], mode)
+    shifted = O.mix_teacher_logits([zs[0] + 4.0, zs[1] - 11.0], [3.0, 7.0], mode)
+    np.testing.assert_allclose(shifted, base, rtol=0, atol=1e-12)
+    with_zero = O.mix_teacher_logits([zs[0], zs[2] * 50.0, zs[1]], [0.3, 0.0, 0.7], mode)
+    np.testing.assert_allclose(with_zero, base, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(sps.logsumexp(base, axis=-1), 0.0, atol=1e-13)
+
+
+def test_mix_of_projected_teachers_with_zero_probability_ids():
+    """Ids with probability 0 (-inf logits, as projection gives unmatched ids):
+    the probability average keeps an id that any teacher supports, the product
+    of experts drops an id that any teacher with weight > 0 rules out."""
+    z1 = np.array([[0.0, -np.inf, 1.0, -np.inf]])
+    z2 = np.array([[0.5, 2.0, -np.inf, -np.inf]])
+    ari = O.mix_teacher_logits([z1, z2], None, "arithmetic")[0]
+    geo = O.mix_teacher_logits([z1, z2], None, "geometric")[0]
+    q1, q2 = sps.softmax(z1[0]), sps.softmax(z2[0])
+    np.testing.assert_allclose(np.exp(ari), 0.5 * q1 + 0.5 * q2, rtol=1e-14)
+    assert np.isneginf(ari[3]) and np.all(np.isfinite(ari[:3]))
+    assert np.all(np.isneginf(geo[1:])) and geo[0] == 0.0
