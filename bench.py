@@ -222,6 +222,99 @@ def run_reference(args, w: I.Workload, rank: int):
 
 # ---------------------------------------------------------------- GPU arm
 
+def run_projection(args, rank):
+    """Cross-vocabulary token-map projection (kd_project_teacher_logits) on a
+    synthetic cross-tokenizer case: bf16 teacher logits ~N(0,4) over a
+    151936-id vocabulary projected at T = 2 onto a 128256-id student vocabulary
+    through a seeded exact-map-like token map (80 % of the student ids reached
+    by one teacher token, 3 % by two, the other teacher tokens unmatched)."""
+    from lm_head_cross_vocab_gb300 import kd
+    kd.load_library()
+    n = args.tokens or 16384
+    v_t, v_s = 151936, 128256
+    dev = torch.device("cuda", 0)
+    rng = np.random.default_rng(1006)
+    tmap = np.full(v_t, -1, dtype=np.int32)
+    src = rng.permutation(v_t)
+    one = rng.permutation(v_s)[: int(0.8 * v_s)]
+    tmap[src[: one.size]] = one
+    two = rng.choice(one, int(0.03 * v_s), replace=False)
+    tmap[src[one.size: one.size + two.size]] = two
+    tmap_d = torch.from_numpy(tmap).to(dev)
+    g = torch.Generator(device=dev).manual_seed(1006)
+    z = (torch.randn(n, v_t, generator=g, device=dev) * 4.0).to(torch.bfloat16)
+    out = torch.empty(n, v_s, device=dev, dtype=torch.bfloat16)
+    ws = kd.Workspace()
+    for _ in range(args.warmup):
+        kd.project_teacher_logits(tmap_d, z, v_s, temperature=2.0, workspace=ws, check=False)
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = kd.kd_launch_count()
+    s.record()
+    for _ in range(args.steps):
+        out = kd.project_teacher_logits(tmap_d, z, v_s, temperature=2.0, workspace=ws,
+                                        check=False)
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / args.steps
+    nbytes = n * v_t * 2 + n * v_s * 2  # teacher logits read once, projected logits written
+    peaks, peak_src = load_peaks()
+    gbs = nbytes / (ms / 1e3) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": "token-map projection tokens/s", "value": n / (ms / 1e3), "unit": "tokens/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "cross_vocab_projection", "tokens": n, "v_teacher": v_t,
+                       "v_student": v_s, "temperature": 2.0,
+                       "l2": "inputs larger than L2"},
+            "roofline": {"bound": "hbm", "kernel": "k_project (+ inverse-map build)",
+                         "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "peak_source": f"{peak_src} copy",
+                         "bytes_per_launch": nbytes},
+            "gpu_launches": kd.kd_launch_count() - launches0}), flush=True)
+
+
+def run_mix(args, rank):
+    """Multi-teacher mixing (kd_mix_teacher_logits): two bf16 teachers' cached
+    logits ~N(0, 2^2) and ~N(0, 3^2) over a 151936-id vocabulary, weights
+    0.6 / 0.4, mixed into one bf16 log-distribution per token."""
+    from lm_head_cross_vocab_gb300 import kd
+    kd.load_library()
+    n = args.tokens or 16384
+    v = 151936
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev).manual_seed(2718)
+    zs = [(torch.randn(n, v, generator=g, device=dev) * s).to(torch.bfloat16) for s in (2.0, 3.0)]
+    w = [0.6, 0.4]
+    for _ in range(args.warmup):
+        kd.mix_teacher_logits(zs, w, args.mix, check=False)
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = kd.kd_launch_count()
+    s.record()
+    for _ in range(args.steps):
+        out = kd.mix_teacher_logits(zs, w, args.mix, check=False)
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / args.steps
+    nbytes = 2 * n * v * 2 + n * v * 2  # both teachers read once, the mixture written once
+    peaks, peak_src = load_peaks()
+    gbs = nbytes / (ms / 1e3) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": "multi-teacher mixing tokens/s", "value": n / (ms / 1e3), "unit": "tokens/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"mix_2_teachers_{args.mix}", "tokens": n, "vocab": v,
+                       "teachers": 2, "weights": w, "l2": "inputs larger than L2"},
+            "roofline": {"bound": "hbm", "kernel": "k_mix_cluster", "achieved": gbs,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                         "peak_source": f"{peak_src} copy", "bytes_per_launch": nbytes},
+            "gpu_launches": kd.kd_launch_count() - launches0}), flush=True)
+    del out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -234,6 +327,10 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=32)
     ap.add_argument("--cpu-rows", type=int, default=0, help="oracle sample size (0: sized by time)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--project", action="store_true",
+                    help="time the cross-vocabulary token-map projection instead of the loss")
+    ap.add_argument("--mix", choices=["arithmetic", "geometric"],
+                    help="time multi-teacher mixing (this mode) instead of the loss")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
@@ -247,6 +344,12 @@ def main():
 
     if args.impl == "reference":
         run_reference(args, w, rank)
+        return
+    if args.project:
+        run_projection(args, rank)
+        return
+    if args.mix:
+        run_mix(args, rank)
         return
 
     from lm_head_cross_vocab_gb300 import kd

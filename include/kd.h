@@ -56,7 +56,7 @@
 extern "C" {
 #endif
 
-#define KD_ABI_VERSION 2
+#define KD_ABI_VERSION 3
 
 typedef enum kd_status {
   KD_OK = 0,
@@ -225,6 +225,33 @@ kd_status kd_project_teacher_logits(const int32_t* token_map, int64_t v_teacher,
                                     int32_t in_dtype, float temperature, void* out,
                                     int32_t out_dtype, uint32_t* dev_status, void* workspace,
                                     size_t ws_bytes, void* stream);
+
+/* Multi-teacher mixing (orda-kernel README, "Cross-vocabulary distillation",
+ * multi-teacher mixing -> PrecomputedTeacher).  K cached teacher logit rows
+ * over one vocabulary are mixed into one distribution, written as its
+ * log-probabilities (pass them to kd_fwd / kd_bwd as a KD_TEACHER_LOGITS
+ * teacher with t_teacher = 1):
+ *   KD_MIX_ARITHMETIC  probability average: out = log sum_k w_k softmax(z_k)
+ *   KD_MIX_GEOMETRIC   product of experts:  out = log of prod_k softmax(z_k)^w_k,
+ *                      renormalised (= g - logsumexp(g), g = sum_k w_k z_k)
+ * with the weights normalised to sum to 1.  A token the mixture gives no
+ * probability gets the most negative finite value of out_dtype, as
+ * kd_project_teacher_logits writes unmatched ids; teacher values at or below
+ * -1e30 count as probability 0.
+ *   logits     host array of k device pointers, each [n_tokens, vocab] in
+ *              in_dtype (KD_BF16 / KD_FP32), row-major, rows contiguous
+ *   k          1 .. KD_MIX_MAX_TEACHERS
+ *   weights    host array of k non-negative finite floats, not all 0 (a
+ *              teacher with weight 0 takes no part), or NULL for uniform
+ *   out        device [n_tokens, vocab] in out_dtype; may not alias an input
+ * No workspace.  Asynchronous on `stream`; argument errors return
+ * KD_ERR_INVALID_ARG synchronously. */
+#define KD_MIX_MAX_TEACHERS 8
+typedef enum kd_mix_mode { KD_MIX_ARITHMETIC = 0, KD_MIX_GEOMETRIC = 1 } kd_mix_mode;
+kd_status kd_mix_teacher_logits(const void* const* logits, int32_t k, const float* weights,
+                                int64_t n_tokens, int64_t vocab, int32_t in_dtype,
+                                int32_t mode, void* out, int32_t out_dtype,
+                                uint32_t* dev_status, void* stream);
 
 /* Static description of a status code. */
 const char* kd_status_string(kd_status status);

@@ -1,0 +1,457 @@
+// Multi-teacher mixing (orda-kernel README, "Cross-vocabulary distillation",
+// multi-teacher mixing): K cached teacher logit rows over one vocabulary are
+// mixed into one distribution, written as its log-probabilities,
+//   arithmetic (probability average):  out = log sum_k w_k softmax(z_k)
+//   geometric (product of experts):    out = g - logsumexp(g),  g = sum_k w_k z_k
+// with the weights normalised to sum to 1 (the product of the teachers'
+// softmaxes differs from exp(g) by a per-row factor only, which the
+// normalisation removes).  A token the mixture gives no probability gets the
+// most negative finite value of the output type, as the projection writes it.
+//
+// Every output needs the logsumexp of whole teacher rows (or of g).  A cluster
+// of C CTAs (C = 1, 2, 4, 8 or 16) therefore holds one token row of all K
+// teachers in shared memory -- CTA r columns [r*sc, r*sc + sc), one bulk copy
+// per teacher -- reduces its columns to a (max, sum of exp) pair per stream,
+// exchanges the pairs through distributed shared memory, and writes its
+// columns of the output with vector stores: each input byte is read from HBM
+// once and each output byte written once.  Rows too long for a 16-CTA cluster
+// take a one-CTA-per-row kernel that reads the row from global memory twice.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cfloat>
+#include <cmath>
+#include <cstring>
+
+#include "../../include/kd.h"
+#include "kd_internal.h"
+#include "kd_ptx.cuh"
+
+namespace kd {
+namespace {
+
+constexpr int kMaxT = KD_MIX_MAX_TEACHERS;
+constexpr int kMT = 512;                  // threads per CTA
+constexpr int kMW = kMT / 32;             // warps per CTA
+constexpr int64_t kMixBuf = 100 * 1024;   // bytes of staged teacher rows per CTA
+constexpr float kL2E = 1.4426950408889634f;
+
+struct MixParams {
+  const void* z[kMaxT];  // teacher logits [n, v], K of them (weights > 0 only)
+  float w[kMaxT];        // weights, normalised to sum to 1
+  float lw[kMaxT];       // log w
+  int k;
+  int64_t n, v;
+  int64_t sc;            // columns per CTA of the cluster kernel
+  void* out;             // [n, v]
+  uint32_t* status;
+};
+
+template <typename T>
+__device__ __forceinline__ float to_f(T x);
+template <>
+__device__ __forceinline__ float to_f<float>(float x) {
+  return x;
+}
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+template <typename T>
+__device__ __forceinline__ T from_f(float x);
+template <>
+__device__ __forceinline__ float from_f<float>(float x) {
+  return x;
+}
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
+  return __float2bfloat16(x);
+}
+template <typename T>
+__device__ __forceinline__ float lowest_of();
+template <>
+__device__ __forceinline__ float lowest_of<float>() {
+  return -FLT_MAX;
+}
+template <>
+__device__ __forceinline__ float lowest_of<__nv_bfloat16>() {
+  return __uint_as_float(0xff7f0000u);  // most negative finite bf16
+}
+
+__device__ __forceinline__ float fast_exp(float x) { return exp2f(x * kL2E); }
+
+// (m, s) running pair of a logsumexp: the maximum and sum_v exp(x_v - m)
+struct Lse {
+  float m, s;
+};
+__device__ __forceinline__ Lse lse_merge(Lse a, Lse b) {
+  if (b.s == 0.f) return a;
+  if (a.s == 0.f) return b;
+  const float m = fmaxf(a.m, b.m);
+  return {m, a.s * fast_exp(a.m - m) + b.s * fast_exp(b.m - m)};
+}
+__device__ __forceinline__ float lse_value(Lse a) {
+  return a.s > 0.f ? a.m + __logf(a.s) : -INFINITY;
+}
+// block-wide merge of one pair per thread; every thread gets the result
+__device__ Lse block_lse(Lse v, Lse* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Lse u{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.s, o)};
+    v = lse_merge(v, u);
+  }
+  __syncthreads();  // red[] may still be read from the previous call
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  Lse r = red[0];
+#pragma unroll
+  for (int i = 1; i < kMW; ++i) r = lse_merge(r, red[i]);
+  return r;
+}
+
+// Pass 1 over columns [0, len) of one stream: stream t < K is teacher t,
+// stream K (geometric) is g = sum_k w_k z_k.  get(k, j) reads teacher k at
+// column j.  Thread-local maximum first, then the sum at that maximum.
+template <bool GEO, typename Get>
+__device__ __forceinline__ Lse stream_lse(const MixParams& P, int t, int64_t len, Get get) {
+  auto val = [&](int64_t j) {
+    if (!GEO) return get(t, j);
+    float g = 0.f;
+    for (int k = 0; k < P.k; ++k) g = fmaf(P.w[k], get(k, j), g);
+    return g;
+  };
+  float m = -INFINITY;
+  for (int64_t j = threadIdx.x; j < len; j += kMT) m = fmaxf(m, val(j));
+  float s = 0.f;
+  if (m > -INFINITY)
+    for (int64_t j = threadIdx.x; j < len; j += kMT) s += fast_exp(val(j) - m);
+  return {m, s};
+}
+
+// output value at one column from the row logsumexps lse[] (per teacher, or
+// of g in slot 0 for the geometric mode)
+template <bool GEO, typename TO, typename Get>
+__device__ __forceinline__ float mix_value(const MixParams& P, const float* lse, int64_t j,
+                                           Get get) {
+  float r;
+  if (GEO) {
+    float g = 0.f;
+    for (int k = 0; k < P.k; ++k) g = fmaf(P.w[k], get(k, j), g);
+    r = g - lse[0];
+  } else {
+    // log sum_k exp(t_k), t_k = z_k - lse_k + log w_k, folded one teacher at a
+    // time around the running maximum (K - 1 exponentials and one logarithm)
+    float m = -INFINITY, s = 0.f;
+    for (int k = 0; k < P.k; ++k) {
+      const float t = get(k, j) - lse[k] + P.lw[k];
+      if (!(t > -INFINITY)) continue;  // no probability (or a teacher row without any)
+      if (s == 0.f) {
+        m = t;
+        s = 1.f;
+        continue;
+      }
+      const float e = fast_exp(-fabsf(t - m));
+      if (t > m) {
+        s = fmaf(s, e, 1.f);
+        m = t;
+      } else {
+        s += e;
+      }
+    }
+    r = s > 0.f ? m + __logf(s) : -INFINITY;
+  }
+  return r > kNoMass ? r : lowest_of<TO>();
+}
+
+
+__device__ __forceinline__ uint32_t cl_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cl_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cl_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float cl_load(const float* p, uint32_t rank) {
+  uint32_t a = ptx::smem_u32(p);
+  asm volatile("mapa.shared::cluster.u32 %0, %0, %1;" : "+r"(a) : "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+
+// Cluster kernel: see the top of this file.  Rows are taken cluster by
+// cluster (all CTAs of a cluster loop over the same rows, so the cluster
+// barriers match); the staged slices are single-buffered (two CTAs share an
+// SM, so one stages while the other computes).
+template <typename TI, typename TO, bool GEO>
+__global__ void __launch_bounds__(kMT, 2) k_mix_cluster(const MixParams P) {
+  extern __shared__ __align__(16) uint8_t mix_smem[];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ Lse red[kMW];
+  __shared__ float stats[2][kMaxT][2];  // this CTA's (max, sum) per stream, by row parity
+  __shared__ float lse[kMaxT];
+  __shared__ int abort_flag;
+  const uint32_t rank = cl_rank(), csize = cl_size();
+  const int64_t ncl = gridDim.x / csize;
+  const int64_t c0 = (int64_t)rank * P.sc;
+  const int64_t clen = P.v - c0 < P.sc ? (P.v - c0 > 0 ? P.v - c0 : 0) : P.sc;
+  const int nstreams = GEO ? 1 : P.k;
+  TI* zs = reinterpret_cast<TI*>(mix_smem);  // teacher k at zs + k * sc
+  const uint32_t bar_sa = ptx::smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar_sa, 1);
+    ptx::fence_mbar_init();
+    abort_flag = 0;
+  }
+  __syncthreads();
+  auto get = [&](int k, int64_t j) { return to_f<TI>(zs[k * P.sc + j]); };
+  uint32_t parity = 0;
+  // the first wait that gave up (its copies may still be in flight; none
+  // starts after it, the abort flag being set by then): its phase parity
+  int pend = -1;
+  int it = 0;
+  for (int64_t row = blockIdx.x / csize; row < P.n; row += ncl, ++it) {
+    // stage: the 16-byte-aligned bulk of each teacher's columns by bulk copy,
+    // the rest (a ragged tail, or a whole unaligned row) by plain loads
+    auto nbytes = [&](int k) -> int64_t {  // bytes of teacher k the bulk copy takes
+      const TI* src = static_cast<const TI*>(P.z[k]) + row * P.v + c0;
+      const bool al = ((reinterpret_cast<uintptr_t>(src) | ptx::smem_u32(zs + k * P.sc)) & 15) == 0;
+      return al ? clen * (int64_t)sizeof(TI) / 16 * 16 : 0;
+    };
+    uint32_t total = 0;
+    for (int k = 0; k < P.k; ++k) total += (uint32_t)nbytes(k);
+    if (threadIdx.x == 0 && !*reinterpret_cast<volatile int*>(&abort_flag)) {
+      ptx::mbar_expect_tx(bar_sa, total);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      for (int k = 0; k < P.k; ++k) {
+        const int64_t nb = nbytes(k);
+        if (nb > 0)
+          ptx::bulk_load(ptx::smem_u32(zs + k * P.sc),
+                         static_cast<const TI*>(P.z[k]) + row * P.v + c0, (uint32_t)nb, bar_sa);
+      }
+    }
+    for (int k = 0; k < P.k; ++k) {
+      const TI* src = static_cast<const TI*>(P.z[k]) + row * P.v + c0;
+      for (int64_t q = nbytes(k) / (int64_t)sizeof(TI) + threadIdx.x; q < clen; q += kMT)
+        zs[k * P.sc + q] = src[q];
+    }
+    if (!ptx::warp_wait(bar_sa, parity, &abort_flag, P.status) && pend < 0) pend = (int)parity;
+    parity ^= 1u;
+    __syncthreads();  // the plain-loaded columns too
+    // pass 1: this CTA's (max, sum) per stream
+    const int pb = it & 1;
+    for (int t = 0; t < nstreams; ++t) {
+      const Lse r = block_lse(stream_lse<GEO>(P, t, clen, get), red);
+      if (threadIdx.x == 0) {
+        stats[pb][t][0] = r.m;
+        stats[pb][t][1] = r.s;
+      }
+    }
+    // every CTA's pairs of this row are written (and every CTA is done with
+    // the previous row's, which the next row overwrites)
+    cl_sync();
+    if (threadIdx.x < (unsigned)nstreams) {
+      Lse acc{-INFINITY, 0.f};
+      for (uint32_t q = 0; q < csize; ++q)
+        acc = lse_merge(acc, Lse{cl_load(&stats[pb][threadIdx.x][0], q),
+                                 cl_load(&stats[pb][threadIdx.x][1], q)});
+      lse[threadIdx.x] = lse_value(acc);
+    }
+    __syncthreads();
+    // pass 2: the output columns, 8 per thread step (vector stores when aligned)
+    TO* o = static_cast<TO*>(P.out) + row * P.v + c0;
+    const bool ov = (reinterpret_cast<uintptr_t>(o) & 15) == 0;
+    for (int64_t j0 = (int64_t)threadIdx.x * 8; j0 < clen; j0 += (int64_t)kMT * 8) {
+      float r[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) r[q] = j0 + q < clen ? mix_value<GEO, TO>(P, lse, j0 + q, get) : 0.f;
+      if (ov && j0 + 8 <= clen) {
+        if constexpr (sizeof(TO) == 4) {
+          reinterpret_cast<float4*>(o + j0)[0] = make_float4(r[0], r[1], r[2], r[3]);
+          reinterpret_cast<float4*>(o + j0)[1] = make_float4(r[4], r[5], r[6], r[7]);
+        } else {
+          uint4 u;
+          u.x = pack_bf16(r[0], r[1]);
+          u.y = pack_bf16(r[2], r[3]);
+          u.z = pack_bf16(r[4], r[5]);
+          u.w = pack_bf16(r[6], r[7]);
+          *reinterpret_cast<uint4*>(o + j0) = u;
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (j0 + q < clen) o[j0 + q] = from_f<TO>(r[q]);
+      }
+    }
+    __syncthreads();  // the staged slices are read; the next row may overwrite them
+  }
+  // no CTA leaves while another may still read its pairs, nor with a copy of
+  // its own in flight (bounded, whatever the abort flag)
+  cl_sync();
+  if (pend >= 0 && threadIdx.x < 32)
+    ptx::warp_wait(bar_sa, (uint32_t)pend, &abort_flag, P.status, false);
+}
+
+// One CTA per row (grid-strided): pass 1 and pass 2 read the row from global
+// memory, for rows of K teachers too long for a 16-CTA cluster.
+template <typename TI, typename TO, bool GEO>
+__global__ void __launch_bounds__(kMT) k_mix_rows(const MixParams P) {
+  __shared__ Lse red[kMW];
+  __shared__ float lse[kMaxT];
+  const int nstreams = GEO ? 1 : P.k;
+  for (int64_t row = blockIdx.x; row < P.n; row += gridDim.x) {
+    auto get = [&](int k, int64_t j) {
+      return to_f<TI>(static_cast<const TI*>(P.z[k])[row * P.v + j]);
+    };
+    for (int t = 0; t < nstreams; ++t) {
+      const float l = lse_value(block_lse(stream_lse<GEO>(P, t, P.v, get), red));
+      if (threadIdx.x == 0) lse[t] = l;
+    }
+    __syncthreads();
+    TO* o = static_cast<TO*>(P.out) + row * P.v;
+    for (int64_t j = threadIdx.x; j < P.v; j += kMT) o[j] = from_f<TO>(mix_value<GEO, TO>(P, lse, j, get));
+    __syncthreads();  // lse[] is rewritten for the next row
+  }
+}
+
+// smallest cluster (1, 2, 4, 8, 16 CTAs) whose per-CTA columns of all K
+// teachers, sc a multiple of 8, fit the staging budget; 0 when none does
+int mix_cluster_for(int64_t v, int k, int64_t elem, int64_t* sc) {
+  for (int c = 1; c <= 16; c *= 2) {
+    const int64_t cols = ((v + c - 1) / c + 7) / 8 * 8;
+    if (cols * elem * k <= kMixBuf) {
+      *sc = cols;
+      return c;
+    }
+  }
+  return 0;
+}
+
+template <typename TI, typename TO, bool GEO>
+int launch_mix(MixParams P, cudaStream_t s) {
+  int64_t sc = 0;
+  const int c = mix_cluster_for(P.v, P.k, (int64_t)sizeof(TI), &sc);
+  const int nsm = tc_num_sms() > 0 ? tc_num_sms() : 1;
+  if (c > 0) {
+    const size_t smem = (size_t)sc * sizeof(TI) * (size_t)P.k;
+    auto kern = k_mix_cluster<TI, TO, GEO>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return 1;
+    if (c > 8 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess)
+      return 1;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)c;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kMT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // co-resident clusters of this shape (cached per cluster size and buffer)
+    static int cached_c = 0, cached_max = 0;
+    static size_t cached_smem = 0;
+    if (cached_c != c || cached_smem != smem) {
+      cfg.gridDim = dim3((unsigned)(c * std::max(1, 2 * nsm / c)));
+      int m = 0;
+      if (cudaOccupancyMaxActiveClusters(&m, kern, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        m = 0;
+      }
+      cached_c = c;
+      cached_smem = smem;
+      cached_max = m;
+    }
+    if (cached_max > 0) {
+      P.sc = sc;
+      const int64_t clusters = P.n < cached_max ? P.n : cached_max;
+      cfg.gridDim = dim3((unsigned)(c * clusters));
+      note_launch();
+      return cudaLaunchKernelEx(&cfg, kern, P) != cudaSuccess;
+    }
+  }
+  const int grid = (int)std::min<int64_t>(P.n, (int64_t)nsm * 2);
+  note_launch();
+  k_mix_rows<TI, TO, GEO><<<grid, kMT, 0, s>>>(P);
+  return cudaGetLastError() != cudaSuccess;
+}
+
+}  // namespace
+}  // namespace kd
+
+using namespace kd;
+
+extern "C" {
+
+kd_status kd_mix_teacher_logits(const void* const* logits, int32_t k, const float* weights,
+                                int64_t n_tokens, int64_t vocab, int32_t in_dtype,
+                                int32_t mode, void* out, int32_t out_dtype,
+                                uint32_t* dev_status, void* stream) {
+  if (!logits || k < 1 || k > KD_MIX_MAX_TEACHERS || n_tokens < 0 || vocab < 1 ||
+      vocab > ((int64_t)1 << 31) || (n_tokens > 0 && !out) ||
+      (in_dtype != KD_BF16 && in_dtype != KD_FP32) ||
+      (out_dtype != KD_BF16 && out_dtype != KD_FP32) ||
+      (mode != KD_MIX_ARITHMETIC && mode != KD_MIX_GEOMETRIC))
+    return KD_ERR_INVALID_ARG;
+  MixParams P;
+  memset(&P, 0, sizeof(P));
+  double wsum = 0.0;
+  for (int i = 0; i < k; ++i) {
+    const double w = weights ? (double)weights[i] : 1.0;
+    if (!(w >= 0.0 && w < 1e30)) return KD_ERR_INVALID_ARG;
+    if (n_tokens > 0 && !logits[i]) return KD_ERR_INVALID_ARG;
+    wsum += w;
+  }
+  if (!(wsum > 0.0)) return KD_ERR_INVALID_ARG;
+  // teachers with weight 0 take no part
+  for (int i = 0; i < k; ++i) {
+    const double w = (weights ? (double)weights[i] : 1.0) / wsum;
+    if (w <= 0.0) continue;
+    P.z[P.k] = logits[i];
+    P.w[P.k] = (float)w;
+    P.lw[P.k] = (float)std::log(w);
+    ++P.k;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || !kd_device_supported(dev)) return KD_ERR_NO_DEVICE;
+  if (n_tokens == 0) return KD_OK;
+  P.n = n_tokens;
+  P.v = vocab;
+  P.out = out;
+  P.status = dev_status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool geo = mode == KD_MIX_GEOMETRIC;
+  int e;
+  if (in_dtype == KD_BF16) {
+    if (out_dtype == KD_BF16)
+      e = geo ? launch_mix<__nv_bfloat16, __nv_bfloat16, true>(P, s)
+              : launch_mix<__nv_bfloat16, __nv_bfloat16, false>(P, s);
+    else
+      e = geo ? launch_mix<__nv_bfloat16, float, true>(P, s)
+              : launch_mix<__nv_bfloat16, float, false>(P, s);
+  } else {
+    if (out_dtype == KD_BF16)
+      e = geo ? launch_mix<float, __nv_bfloat16, true>(P, s)
+              : launch_mix<float, __nv_bfloat16, false>(P, s);
+    else
+      e = geo ? launch_mix<float, float, true>(P, s) : launch_mix<float, float, false>(P, s);
+  }
+  return e ? KD_ERR_CUDA : KD_OK;
+}
+
+}  // extern "C"

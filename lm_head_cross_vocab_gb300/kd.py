@@ -35,7 +35,7 @@ KD_KL_SKEW_FORWARD, KD_KL_SKEW_REVERSE = 4, 5
 KD_REDUCE_MEAN, KD_REDUCE_SUM = 0, 1
 KD_STATS_PER_TOKEN = 8
 KD_STATIC_SCRATCH_BYTES = 32 << 20
-KD_ABI_VERSION = 2  # the kd.h this binding follows
+KD_ABI_VERSION = 3  # the kd.h this binding follows
 
 DTYPES = {"bf16": KD_BF16, "fp32": KD_FP32}
 STUDENTS = {"hidden": KD_STUDENT_HIDDEN, "logits": KD_STUDENT_LOGITS}
@@ -106,11 +106,14 @@ def load_library(path: str = LIB_PATH):
     lib.kd_project_teacher_logits.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, vp,
                                               ctypes.c_int64, ctypes.c_int32, ctypes.c_float, vp,
                                               ctypes.c_int32, vp, vp, ctypes.c_size_t, vp]
+    lib.kd_mix_teacher_logits.argtypes = [vp, ctypes.c_int32, vp, ctypes.c_int64, ctypes.c_int64,
+                                          ctypes.c_int32, ctypes.c_int32, vp, ctypes.c_int32, vp,
+                                          vp]
     lib.kd_launch_count.restype = ctypes.c_uint64
     for f in ("kd_workspace_size", "kd_fwd", "kd_bwd", "kd_device_supported", "kd_abi_version",
               "kd_diag_gemm_bf16", "kd_set_profile_events", "kd_set_profile_launch_events",
               "kd_fwd_static_scratch", "kd_project_workspace_size", "kd_project_teacher_logits",
-              "kd_plan_info"):
+              "kd_plan_info", "kd_mix_teacher_logits"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -422,4 +425,42 @@ def project_teacher_logits(token_map: torch.Tensor, logits_t: torch.Tensor, v_st
         raise KDError(st, "kd_project_teacher_logits")
     if check and int(dev_status.item()) & KD_DEV_BAD_MAP:
         raise KDError(KD_ERR_INVALID_ARG, "token map entry outside [-1, V_student)")
+    return out
+
+
+KD_MIX_ARITHMETIC, KD_MIX_GEOMETRIC = 0, 1
+KD_MIX_MAX_TEACHERS = 8
+MIX_MODES = {"arithmetic": KD_MIX_ARITHMETIC, "geometric": KD_MIX_GEOMETRIC}
+
+
+def mix_teacher_logits(logits, weights=None, mode: str = "arithmetic", out_dtype=None,
+                       check: bool = True):
+    """kd_mix_teacher_logits: K teacher logit tensors [N, V] (same device, dtype
+    and shape) -> the mixture's log-probabilities [N, V] (probability average
+    or product of experts; weights normalised, uniform when None)."""
+    zs = [z.contiguous() for z in logits]
+    if not zs or len(zs) > KD_MIX_MAX_TEACHERS:
+        raise ValueError(f"1..{KD_MIX_MAX_TEACHERS} teachers")
+    z0 = zs[0]
+    if any(z.shape != z0.shape or z.dtype != z0.dtype or z.device != z0.device for z in zs):
+        raise ValueError("teachers must share shape, dtype and device")
+    n, v = z0.shape
+    dev = z0.device
+    dtype = z0.dtype if out_dtype is None else out_dtype
+    out = torch.empty(n, v, device=dev, dtype=dtype)
+    ptrs = (ctypes.c_void_p * len(zs))(*[z.data_ptr() for z in zs])
+    w = None
+    if weights is not None:
+        w = (ctypes.c_float * len(zs))(*[float(x) for x in weights])
+        if len(weights) != len(zs):
+            raise ValueError("one weight per teacher")
+    dev_status = torch.zeros(1, device=dev, dtype=torch.int32)
+    dt = {torch.bfloat16: KD_BF16, torch.float32: KD_FP32}
+    st = load_library().kd_mix_teacher_logits(ptrs, len(zs), w, n, v, dt[z0.dtype],
+                                              MIX_MODES[mode], out.data_ptr(), dt[dtype],
+                                              dev_status.data_ptr(), _stream(dev))
+    if st != KD_OK:
+        raise KDError(st, "kd_mix_teacher_logits")
+    if check and int(dev_status.item()) & KD_DEV_TIMEOUT:
+        raise KDError(KD_ERR_TIMEOUT, "a bounded wait timed out")
     return out

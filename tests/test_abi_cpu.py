@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(kd):
 
 
 def test_abi_version_and_status_strings(kd):
-    assert kd.kd_abi_version() == 2
+    assert kd.kd_abi_version() == kd.KD_ABI_VERSION == 3
     for code in range(9):
         s = kd.kd_status_string(code)
         assert s and s != "unknown status"
@@ -162,3 +162,25 @@ def test_device_query_without_gpu(kd):
     if torch.cuda.is_available():
         pytest.skip("GPU present")
     assert kd.kd_device_supported(0) is False
+
+
+def test_mix_argument_rules(kd):
+    """kd_mix_teacher_logits rejects bad arguments synchronously (before any
+    device work); well-formed calls reach the device check."""
+    lib = kd.load_library()
+    fake = 1 << 20
+    ptrs = (ctypes.c_void_p * 9)(*([fake] * 9))
+
+    def call(k=2, weights=(1.0, 1.0), n=4, v=10, din=kd.KD_BF16, mode=kd.KD_MIX_ARITHMETIC,
+             dout=kd.KD_FP32, out=fake):
+        w = None if weights is None else (ctypes.c_float * len(weights))(*weights)
+        return lib.kd_mix_teacher_logits(ptrs, k, w, n, v, din, mode, out, dout, None, None)
+
+    bad = [dict(k=0), dict(k=9, weights=None), dict(weights=(1.0, -1.0)), dict(weights=(0.0, 0.0)),
+           dict(weights=(1.0, float("nan"))), dict(v=0), dict(n=-1), dict(din=7), dict(dout=7),
+           dict(mode=2), dict(out=None)]
+    for kw in bad:
+        assert call(**kw) == kd.KD_ERR_INVALID_ARG, kw
+    for kw in (dict(), dict(weights=None), dict(weights=(0.0, 2.0), mode=kd.KD_MIX_GEOMETRIC),
+               dict(k=8, weights=None)):
+        assert call(**kw) == kd.KD_ERR_NO_DEVICE, kw

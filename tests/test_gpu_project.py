@@ -34,10 +34,17 @@ def _map(v_t, v_s, seed):
 
 
 @pytest.mark.parametrize("din,dout", [("fp32", "fp32"), ("bf16", "fp32"), ("bf16", "bf16")])
-@pytest.mark.parametrize("v_t,v_s", [(1000, 700), (513, 2049)])
-def test_projection_matches_oracle(din, dout, v_t, v_s):
+@pytest.mark.parametrize("v_t,v_s,n", [(1000, 700, 37), (513, 2049, 37), (60000, 70001, 5),
+                                       (120000, 5000, 6), (220000, 3000, 3), (430000, 2000, 2),
+                                       (30000, 20000, 400)])
+def test_projection_matches_oracle(din, dout, v_t, v_s, n):
+    """Teacher rows held by one CTA, by clusters of 2, 4 and 8 CTAs (60000 and
+    120000 ids in bf16 and fp32, 220000 in bf16), rows too long for a cluster
+    of 8 (220000 fp32, 430000 ids) on the sliced kernel, unaligned rows (513
+    ids), ragged student vocabularies, and many rows per cluster (400 rows, so
+    the double-buffered staging turns over)."""
     g = torch.Generator().manual_seed(v_t + v_s)
-    z = (torch.randn(37, v_t, generator=g) * 3.0).to(DT[din])
+    z = (torch.randn(n, v_t, generator=g) * 3.0).to(DT[din])
     tmap = _map(v_t, v_s, 11)
     out = kd.project_teacher_logits(torch.from_numpy(tmap), z.cuda(), v_s, temperature=1.5,
                                     out_dtype=DT[dout])
