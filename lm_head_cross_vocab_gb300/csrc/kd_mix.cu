@@ -34,8 +34,8 @@ namespace {
 constexpr int kMaxT = KD_MIX_MAX_TEACHERS;
 constexpr int kMT = 512;                  // threads per CTA
 constexpr int kMW = kMT / 32;             // warps per CTA
-constexpr int64_t kMixBuf = 100 * 1024;   // bytes of staged teacher rows per CTA
-constexpr float kL2E = 1.4426950408889634f;
+constexpr int64_t kMixBuf = 200 * 1024;   // bytes of staged teacher rows per CTA
+constexpr float kLN2 = 0.6931471805599453f;
 
 struct MixParams {
   const void* z[kMaxT];  // teacher logits [n, v], K of them (weights > 0 only)
@@ -79,7 +79,7 @@ __device__ __forceinline__ float lowest_of<__nv_bfloat16>() {
   return __uint_as_float(0xff7f0000u);  // most negative finite bf16
 }
 
-__device__ __forceinline__ float fast_exp(float x) { return exp2f(x * kL2E); }
+__device__ __forceinline__ float fast_exp(float x) { return ex2(x * kL2E); }
 
 // (m, s) running pair of a logsumexp: the maximum and sum_v exp(x_v - m)
 struct Lse {
@@ -188,55 +188,174 @@ __device__ __forceinline__ float cl_load(const float* p, uint32_t rank) {
   return v;
 }
 
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 8 consecutive staged values (16-byte aligned shared memory) as floats
+__device__ __forceinline__ void ld8(const __nv_bfloat16* p, float v[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ void ld8(const float* p, float v[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0];
+  const float4 b = reinterpret_cast<const float4*>(p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+// the stream's values at 8 columns: teacher t, or g = sum_k w_k z_k
+template <bool GEO, typename TI>
+__device__ __forceinline__ void stream8(const MixParams& P, const TI* zs, int t, int64_t j0,
+                                        float x[8]) {
+  if (!GEO) {
+    ld8(zs + t * P.sc + j0, x);
+    return;
+  }
+  float y[8];
+  ld8(zs + j0, y);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) x[q] = P.w[0] * y[q];
+  for (int k = 1; k < P.k; ++k) {
+    ld8(zs + k * P.sc + j0, y);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) x[q] = fmaf(P.w[k], y[q], x[q]);
+  }
+}
+
+// Pass 1 of the cluster kernel: this thread's (max, sum of exp) of one stream
+// over the staged columns [0, clen), 8 columns a step, one exponential per
+// value (the running sum is rescaled when a step raises the maximum).
+template <bool GEO, typename TI>
+__device__ __forceinline__ Lse pass1(const MixParams& P, const TI* zs, int t, int64_t clen) {
+  float m = -INFINITY, s = 0.f;
+  for (int64_t j0 = (int64_t)threadIdx.x * 8; j0 < clen; j0 += (int64_t)kMT * 8) {
+    float x[8];
+    stream8<GEO>(P, zs, t, j0, x);
+    if (j0 + 8 > clen) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (j0 + q >= clen) x[q] = -INFINITY;
+    }
+    float m8 = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])),
+                     fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
+    // values at or below kNoMass carry no probability: they never set the
+    // maximum (so m * log2(e) below stays finite) and their terms are 0
+    if (m8 > m && m8 > kNoMass) {
+      s *= ex2((m - m8) * kL2E);  // 0 while m is still -inf (s is 0 then too)
+      m = m8;
+    }
+    // (x - m first: exact near the maximum, whatever the logits' magnitude)
+    if (m > -INFINITY) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) s += ex2((x[q] - m) * kL2E);
+    }
+  }
+  return {m, s};
+}
+
+// Pass 2 of the cluster kernel: 8 output values at columns j0.. from the row
+// logsumexps lse[] (per teacher, or of g in slot 0).
+template <bool GEO, typename TI, typename TO>
+__device__ __forceinline__ void pass2_8(const MixParams& P, const TI* zs, const float* lse,
+                                        int64_t j0, float r[8]) {
+  if (GEO) {
+    float g[8];
+    stream8<true>(P, zs, 0, j0, g);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) r[q] = g[q] - lse[0];
+  } else {
+    // log sum_k exp(t_k), t_k = z_k - lse_k + log w_k, folded teacher by
+    // teacher around the running maximum in base 2 (K - 1 exponentials and
+    // one logarithm); z_k - lse_k first, exact for a row's dominant token
+    float m[8], s[8], x[8];
+    ld8(zs + j0, x);
+    const float l0 = lse[0], w0 = P.lw[0] * kL2E;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      m[q] = fmaf(x[q] - l0, kL2E, w0);
+      s[q] = m[q] > -INFINITY ? 1.f : 0.f;
+    }
+    for (int k = 1; k < P.k; ++k) {
+      ld8(zs + k * P.sc + j0, x);
+      const float lk = lse[k], wk = P.lw[k] * kL2E;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float t = fmaf(x[q] - lk, kL2E, wk);
+        if (t > -INFINITY) {
+          if (s[q] == 0.f) {
+            m[q] = t;
+            s[q] = 1.f;
+          } else {
+            const float e = ex2(-fabsf(t - m[q]));
+            const bool up = t > m[q];
+            s[q] = up ? fmaf(s[q], e, 1.f) : s[q] + e;
+            m[q] = up ? t : m[q];
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) r[q] = s[q] > 0.f ? (m[q] + lg2(s[q])) * kLN2 : -INFINITY;
+  }
+#pragma unroll
+  for (int q = 0; q < 8; ++q) r[q] = r[q] > kNoMass ? r[q] : lowest_of<TO>();
+}
+
 // Cluster kernel: see the top of this file.  Rows are taken cluster by
 // cluster (all CTAs of a cluster loop over the same rows, so the cluster
-// barriers match); the staged slices are single-buffered (two CTAs share an
-// SM, so one stages while the other computes).
+// barriers match).  With `dbuf` the staged rows are double-buffered: the next
+// row's bulk copies run under this row's passes.
 template <typename TI, typename TO, bool GEO>
-__global__ void __launch_bounds__(kMT, 2) k_mix_cluster(const MixParams P) {
+__global__ void __launch_bounds__(kMT, 1) k_mix_cluster(const MixParams P, int dbuf) {
   extern __shared__ __align__(16) uint8_t mix_smem[];
-  __shared__ __align__(8) uint64_t bar;
+  __shared__ __align__(8) uint64_t bars[2];
   __shared__ Lse red[kMW];
   __shared__ float stats[2][kMaxT][2];  // this CTA's (max, sum) per stream, by row parity
-  __shared__ float lse[kMaxT];
+  __shared__ float off_sh[kMaxT];  // the row logsumexp per stream
   __shared__ int abort_flag;
   const uint32_t rank = cl_rank(), csize = cl_size();
   const int64_t ncl = gridDim.x / csize;
   const int64_t c0 = (int64_t)rank * P.sc;
   const int64_t clen = P.v - c0 < P.sc ? (P.v - c0 > 0 ? P.v - c0 : 0) : P.sc;
   const int nstreams = GEO ? 1 : P.k;
-  TI* zs = reinterpret_cast<TI*>(mix_smem);  // teacher k at zs + k * sc
-  const uint32_t bar_sa = ptx::smem_u32(&bar);
+  const int64_t buf_elems = (int64_t)P.k * P.sc;  // a buffer: teacher k at k * sc
+  TI* const base = reinterpret_cast<TI*>(mix_smem);
   if (threadIdx.x == 0) {
-    ptx::mbar_init(bar_sa, 1);
+    ptx::mbar_init(ptx::smem_u32(&bars[0]), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars[1]), 1);
     ptx::fence_mbar_init();
     abort_flag = 0;
   }
   __syncthreads();
-  auto get = [&](int k, int64_t j) { return to_f<TI>(zs[k * P.sc + j]); };
-  uint32_t parity = 0;
-  // the first wait that gave up (its copies may still be in flight; none
-  // starts after it, the abort flag being set by then): its phase parity
-  int pend = -1;
-  int it = 0;
-  for (int64_t row = blockIdx.x / csize; row < P.n; row += ncl, ++it) {
-    // stage: the 16-byte-aligned bulk of each teacher's columns by bulk copy,
-    // the rest (a ragged tail, or a whole unaligned row) by plain loads
-    auto nbytes = [&](int k) -> int64_t {  // bytes of teacher k the bulk copy takes
+  // stage `row` into buffer b: the 16-byte-aligned bulk of each teacher's
+  // columns by bulk copy, the rest (a ragged tail, or a whole unaligned row)
+  // by plain loads
+  auto stage = [&](int64_t row, int b) {
+    TI* zs = base + b * buf_elems;
+    const uint32_t bar = ptx::smem_u32(&bars[b]);
+    auto nbytes = [&](int k) -> int64_t {
       const TI* src = static_cast<const TI*>(P.z[k]) + row * P.v + c0;
       const bool al = ((reinterpret_cast<uintptr_t>(src) | ptx::smem_u32(zs + k * P.sc)) & 15) == 0;
       return al ? clen * (int64_t)sizeof(TI) / 16 * 16 : 0;
     };
-    uint32_t total = 0;
-    for (int k = 0; k < P.k; ++k) total += (uint32_t)nbytes(k);
     if (threadIdx.x == 0 && !*reinterpret_cast<volatile int*>(&abort_flag)) {
-      ptx::mbar_expect_tx(bar_sa, total);
+      // (after a timed-out wait no new copy starts; later waits give up)
+      uint32_t total = 0;
+      for (int k = 0; k < P.k; ++k) total += (uint32_t)nbytes(k);
+      ptx::mbar_expect_tx(bar, total);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       for (int k = 0; k < P.k; ++k) {
         const int64_t nb = nbytes(k);
         if (nb > 0)
           ptx::bulk_load(ptx::smem_u32(zs + k * P.sc),
-                         static_cast<const TI*>(P.z[k]) + row * P.v + c0, (uint32_t)nb, bar_sa);
+                         static_cast<const TI*>(P.z[k]) + row * P.v + c0, (uint32_t)nb, bar);
       }
     }
     for (int k = 0; k < P.k; ++k) {
@@ -244,27 +363,45 @@ __global__ void __launch_bounds__(kMT, 2) k_mix_cluster(const MixParams P) {
       for (int64_t q = nbytes(k) / (int64_t)sizeof(TI) + threadIdx.x; q < clen; q += kMT)
         zs[k * P.sc + q] = src[q];
     }
-    if (!ptx::warp_wait(bar_sa, parity, &abort_flag, P.status) && pend < 0) pend = (int)parity;
-    parity ^= 1u;
+  };
+  const int64_t first = blockIdx.x / csize;
+  if (first < P.n) stage(first, 0);
+  uint32_t parity = 0;  // bit b: phase parity to wait for on buffer b
+  // the first wait that gave up: its copies may still be in flight (none
+  // starts after it, the abort flag being set by then)
+  int pend_b = -1;
+  uint32_t pend_p = 0;
+  int it = 0;
+  for (int64_t row = first; row < P.n; row += ncl, ++it) {
+    const int b = dbuf ? (it & 1) : 0;
+    // buffer b ^ 1 held the previous row, which every thread is done with
+    if (dbuf && row + ncl < P.n) stage(row + ncl, b ^ 1);
+    if (!ptx::warp_wait(ptx::smem_u32(&bars[b]), (parity >> b) & 1u, &abort_flag, P.status) &&
+        pend_b < 0) {
+      pend_b = b;
+      pend_p = (parity >> b) & 1u;
+    }
+    parity ^= 1u << b;
     __syncthreads();  // the plain-loaded columns too
+    const TI* zs = base + b * buf_elems;
     // pass 1: this CTA's (max, sum) per stream
     const int pb = it & 1;
     for (int t = 0; t < nstreams; ++t) {
-      const Lse r = block_lse(stream_lse<GEO>(P, t, clen, get), red);
+      const Lse r = block_lse(pass1<GEO>(P, zs, t, clen), red);
       if (threadIdx.x == 0) {
         stats[pb][t][0] = r.m;
         stats[pb][t][1] = r.s;
       }
     }
     // every CTA's pairs of this row are written (and every CTA is done with
-    // the previous row's, which the next row overwrites)
+    // the previous row's pairs in this parity slot)
     cl_sync();
     if (threadIdx.x < (unsigned)nstreams) {
       Lse acc{-INFINITY, 0.f};
       for (uint32_t q = 0; q < csize; ++q)
         acc = lse_merge(acc, Lse{cl_load(&stats[pb][threadIdx.x][0], q),
                                  cl_load(&stats[pb][threadIdx.x][1], q)});
-      lse[threadIdx.x] = lse_value(acc);
+      off_sh[threadIdx.x] = lse_value(acc);
     }
     __syncthreads();
     // pass 2: the output columns, 8 per thread step (vector stores when aligned)
@@ -272,8 +409,7 @@ __global__ void __launch_bounds__(kMT, 2) k_mix_cluster(const MixParams P) {
     const bool ov = (reinterpret_cast<uintptr_t>(o) & 15) == 0;
     for (int64_t j0 = (int64_t)threadIdx.x * 8; j0 < clen; j0 += (int64_t)kMT * 8) {
       float r[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) r[q] = j0 + q < clen ? mix_value<GEO, TO>(P, lse, j0 + q, get) : 0.f;
+      pass2_8<GEO, TI, TO>(P, zs, off_sh, j0, r);
       if (ov && j0 + 8 <= clen) {
         if constexpr (sizeof(TO) == 4) {
           reinterpret_cast<float4*>(o + j0)[0] = make_float4(r[0], r[1], r[2], r[3]);
@@ -292,13 +428,14 @@ __global__ void __launch_bounds__(kMT, 2) k_mix_cluster(const MixParams P) {
           if (j0 + q < clen) o[j0 + q] = from_f<TO>(r[q]);
       }
     }
-    __syncthreads();  // the staged slices are read; the next row may overwrite them
+    __syncthreads();  // this buffer is read; a later row may overwrite it
+    if (!dbuf && row + ncl < P.n) stage(row + ncl, 0);
   }
   // no CTA leaves while another may still read its pairs, nor with a copy of
   // its own in flight (bounded, whatever the abort flag)
   cl_sync();
-  if (pend >= 0 && threadIdx.x < 32)
-    ptx::warp_wait(bar_sa, (uint32_t)pend, &abort_flag, P.status, false);
+  if (pend_b >= 0 && threadIdx.x < 32)
+    ptx::warp_wait(ptx::smem_u32(&bars[pend_b]), pend_p, &abort_flag, P.status, false);
 }
 
 // One CTA per row (grid-strided): pass 1 and pass 2 read the row from global
@@ -324,25 +461,29 @@ __global__ void __launch_bounds__(kMT) k_mix_rows(const MixParams P) {
 }
 
 // smallest cluster (1, 2, 4, 8, 16 CTAs) whose per-CTA columns of all K
-// teachers, sc a multiple of 8, fit the staging budget; 0 when none does
-int mix_cluster_for(int64_t v, int k, int64_t elem, int64_t* sc) {
-  for (int c = 1; c <= 16; c *= 2) {
-    const int64_t cols = ((v + c - 1) / c + 7) / 8 * 8;
-    if (cols * elem * k <= kMixBuf) {
-      *sc = cols;
-      return c;
+// teachers, sc a multiple of 8, fit the staging budget twice (double
+// buffering, *dbuf = 1), else once; 0 when none does
+int mix_cluster_for(int64_t v, int k, int64_t elem, int64_t* sc, int* dbuf) {
+  for (int nb = 2; nb >= 1; --nb)
+    for (int c = 1; c <= 16; c *= 2) {
+      const int64_t cols = ((v + c - 1) / c + 7) / 8 * 8;
+      if (cols * elem * k * nb <= kMixBuf) {
+        *sc = cols;
+        *dbuf = nb == 2;
+        return c;
+      }
     }
-  }
   return 0;
 }
 
 template <typename TI, typename TO, bool GEO>
 int launch_mix(MixParams P, cudaStream_t s) {
   int64_t sc = 0;
-  const int c = mix_cluster_for(P.v, P.k, (int64_t)sizeof(TI), &sc);
+  int dbuf = 0;
+  const int c = mix_cluster_for(P.v, P.k, (int64_t)sizeof(TI), &sc, &dbuf);
   const int nsm = tc_num_sms() > 0 ? tc_num_sms() : 1;
   if (c > 0) {
-    const size_t smem = (size_t)sc * sizeof(TI) * (size_t)P.k;
+    const size_t smem = (size_t)sc * sizeof(TI) * (size_t)P.k * (dbuf ? 2 : 1);
     auto kern = k_mix_cluster<TI, TO, GEO>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
@@ -367,7 +508,7 @@ int launch_mix(MixParams P, cudaStream_t s) {
     static int cached_c = 0, cached_max = 0;
     static size_t cached_smem = 0;
     if (cached_c != c || cached_smem != smem) {
-      cfg.gridDim = dim3((unsigned)(c * std::max(1, 2 * nsm / c)));
+      cfg.gridDim = dim3((unsigned)(c * std::max(1, nsm / c)));
       int m = 0;
       if (cudaOccupancyMaxActiveClusters(&m, kern, &cfg) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -382,7 +523,7 @@ int launch_mix(MixParams P, cudaStream_t s) {
       const int64_t clusters = P.n < cached_max ? P.n : cached_max;
       cfg.gridDim = dim3((unsigned)(c * clusters));
       note_launch();
-      return cudaLaunchKernelEx(&cfg, kern, P) != cudaSuccess;
+      return cudaLaunchKernelEx(&cfg, kern, P, dbuf) != cudaSuccess;
     }
   }
   const int grid = (int)std::min<int64_t>(P.n, (int64_t)nsm * 2);
