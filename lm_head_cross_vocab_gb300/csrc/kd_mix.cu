@@ -32,7 +32,7 @@ namespace kd {
 namespace {
 
 constexpr int kMaxT = KD_MIX_MAX_TEACHERS;
-constexpr int kMT = 512;                  // threads per CTA
+constexpr int kMT = 1024;                 // threads per CTA
 constexpr int kMW = kMT / 32;             // warps per CTA
 constexpr int64_t kMixBuf = 200 * 1024;   // bytes of staged teacher rows per CTA
 constexpr float kLN2 = 0.6931471805599453f;
@@ -180,11 +180,12 @@ __device__ __forceinline__ void cl_sync() {
       "barrier.cluster.arrive.release.aligned;\n\t"
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// a float of CTA `rank`'s shared memory (read between cluster barriers)
 __device__ __forceinline__ float cl_load(const float* p, uint32_t rank) {
   uint32_t a = ptx::smem_u32(p);
-  asm volatile("mapa.shared::cluster.u32 %0, %0, %1;" : "+r"(a) : "r"(rank));
+  asm("mapa.shared::cluster.u32 %0, %0, %1;" : "+r"(a) : "r"(rank));
   float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a));
   return v;
 }
 
@@ -273,36 +274,33 @@ __device__ __forceinline__ void pass2_8(const MixParams& P, const TI* zs, const 
   } else {
     // log sum_k exp(t_k), t_k = z_k - lse_k + log w_k, folded teacher by
     // teacher around the running maximum in base 2 (K - 1 exponentials and
-    // one logarithm); z_k - lse_k first, exact for a row's dominant token
+    // one logarithm); z_k - lse_k first, exact for a row's dominant token.
+    // Terms are clamped below at kNoMass (base 2), so the fold needs no
+    // special case: a clamped term adds 2^-huge = 0 beside any real one, and
+    // a token with only clamped terms stays at or below kNoMass.
+    constexpr float kFloor = kNoMass * kL2E;
     float m[8], s[8], x[8];
     ld8(zs + j0, x);
     const float l0 = lse[0], w0 = P.lw[0] * kL2E;
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      m[q] = fmaf(x[q] - l0, kL2E, w0);
-      s[q] = m[q] > -INFINITY ? 1.f : 0.f;
+      m[q] = fmaxf(fmaf(x[q] - l0, kL2E, w0), kFloor);
+      s[q] = 1.f;
     }
     for (int k = 1; k < P.k; ++k) {
       ld8(zs + k * P.sc + j0, x);
       const float lk = lse[k], wk = P.lw[k] * kL2E;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        const float t = fmaf(x[q] - lk, kL2E, wk);
-        if (t > -INFINITY) {
-          if (s[q] == 0.f) {
-            m[q] = t;
-            s[q] = 1.f;
-          } else {
-            const float e = ex2(-fabsf(t - m[q]));
-            const bool up = t > m[q];
-            s[q] = up ? fmaf(s[q], e, 1.f) : s[q] + e;
-            m[q] = up ? t : m[q];
-          }
-        }
+        const float t = fmaxf(fmaf(x[q] - lk, kL2E, wk), kFloor);
+        const float d = t - m[q];
+        const float e = ex2(-fabsf(d));
+        s[q] = d > 0.f ? fmaf(s[q], e, 1.f) : s[q] + e;
+        m[q] = fmaxf(m[q], t);
       }
     }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) r[q] = s[q] > 0.f ? (m[q] + lg2(s[q])) * kLN2 : -INFINITY;
+    for (int q = 0; q < 8; ++q) r[q] = m[q] > kFloor ? (m[q] + lg2(s[q])) * kLN2 : -INFINITY;
   }
 #pragma unroll
   for (int q = 0; q < 8; ++q) r[q] = r[q] > kNoMass ? r[q] : lowest_of<TO>();
@@ -319,6 +317,7 @@ __global__ void __launch_bounds__(kMT, 1) k_mix_cluster(const MixParams P, int d
   __shared__ Lse red[kMW];
   __shared__ float stats[2][kMaxT][2];  // this CTA's (max, sum) per stream, by row parity
   __shared__ float off_sh[kMaxT];  // the row logsumexp per stream
+  __shared__ Lse peer[16][kMaxT];  // every CTA's pair per stream, fetched
   __shared__ int abort_flag;
   const uint32_t rank = cl_rank(), csize = cl_size();
   const int64_t ncl = gridDim.x / csize;
@@ -396,11 +395,16 @@ __global__ void __launch_bounds__(kMT, 1) k_mix_cluster(const MixParams P, int d
     // every CTA's pairs of this row are written (and every CTA is done with
     // the previous row's pairs in this parity slot)
     cl_sync();
+    // one thread per (CTA, stream) pair fetches it, so all the remote loads
+    // are in flight together; then one thread per stream merges them
+    if (threadIdx.x < csize * (unsigned)nstreams) {
+      const uint32_t q = threadIdx.x / nstreams, t = threadIdx.x % nstreams;
+      peer[q][t] = Lse{cl_load(&stats[pb][t][0], q), cl_load(&stats[pb][t][1], q)};
+    }
+    __syncthreads();
     if (threadIdx.x < (unsigned)nstreams) {
       Lse acc{-INFINITY, 0.f};
-      for (uint32_t q = 0; q < csize; ++q)
-        acc = lse_merge(acc, Lse{cl_load(&stats[pb][threadIdx.x][0], q),
-                                 cl_load(&stats[pb][threadIdx.x][1], q)});
+      for (uint32_t q = 0; q < csize; ++q) acc = lse_merge(acc, peer[q][threadIdx.x]);
       off_sh[threadIdx.x] = lse_value(acc);
     }
     __syncthreads();
@@ -461,18 +465,19 @@ __global__ void __launch_bounds__(kMT) k_mix_rows(const MixParams P) {
 }
 
 // smallest cluster (1, 2, 4, 8, 16 CTAs) whose per-CTA columns of all K
-// teachers, sc a multiple of 8, fit the staging budget twice (double
-// buffering, *dbuf = 1), else once; 0 when none does
+// teachers, sc a multiple of 8, fit the staging budget, double-buffered
+// (*dbuf = 1) when twice that fits too; 0 when none does.  (Smaller clusters
+// win over double buffering: more SMs can host them, and the per-row cluster
+// barrier and reductions cost less.)
 int mix_cluster_for(int64_t v, int k, int64_t elem, int64_t* sc, int* dbuf) {
-  for (int nb = 2; nb >= 1; --nb)
-    for (int c = 1; c <= 16; c *= 2) {
-      const int64_t cols = ((v + c - 1) / c + 7) / 8 * 8;
-      if (cols * elem * k * nb <= kMixBuf) {
-        *sc = cols;
-        *dbuf = nb == 2;
-        return c;
-      }
+  for (int c = 1; c <= 16; c *= 2) {
+    const int64_t cols = ((v + c - 1) / c + 7) / 8 * 8;
+    if (cols * elem * k <= kMixBuf) {
+      *sc = cols;
+      *dbuf = 2 * cols * elem * k <= kMixBuf;
+      return c;
     }
+  }
   return 0;
 }
 
