@@ -56,7 +56,7 @@
 extern "C" {
 #endif
 
-#define KD_ABI_VERSION 3
+#define KD_ABI_VERSION 4
 
 typedef enum kd_status {
   KD_OK = 0,
@@ -128,7 +128,8 @@ typedef struct kd_problem {
   int64_t ignore_index;  /* label value excluded from CE and KL               */
   int64_t num_batch_labels; /* > 0: mean divides by this instead of N_valid  */
   int32_t assume_valid_labels; /* 1: caller promises labels in range          */
-  int32_t reserved0;
+  int32_t teacher_grads;  /* 1: kd_bwd_grads may be asked for d_h_t / d_w_t  */
+                         /* (the workspace is sized for them); else 0        */
   int64_t vocab_chunk;   /* backward G-workspace vocab chunk (0 = auto); the  */
   int64_t seq_chunk;     /* token chunk (0 = auto). Results do not depend on  */
                          /* either beyond rounding (flash_kd chunk_size,      */
@@ -187,6 +188,32 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* inputs, const float
                  const float* d_loss, float grad_scale, void* d_h_s, void* d_w_s,
                  void* d_logits_s, uint32_t* dev_status, void* workspace, size_t ws_bytes,
                  void* stream);
+
+/* Gradients kd_bwd_grads may write; NULL skips one. */
+typedef struct kd_grads {
+  void* d_h_s;       /* [N, D_s] d loss / d H_s (hidden students)             */
+  void* d_w_s;       /* [V, D_s] d loss / d W_s (hidden students; with a tied  */
+                     /* teacher's CE term included, as in kd_bwd)             */
+  void* d_logits_s;  /* [N, V]   d loss / d z_s (logit students)               */
+  void* d_h_t;       /* [N, D_t] d loss / d H_t: tied or separate teachers     */
+  void* d_w_t;       /* [V, D_t] d loss / d W_t: separate teachers             */
+} kd_grads;
+
+/* Backward with teacher gradients (orda-kernel README, "Teacher descriptors":
+ * a teacher whose teacher_ce_weight is > 0 is trained by its CE term;
+ * "Parameters" list teacher_ce_weight).  Everything kd_bwd writes, plus the
+ * teacher's: the teacher is detached from every KL variant, so its gradient
+ * is that of w_teacher_ce * CE_t alone, G_t = d loss / d z_t =
+ * s_n w_teacher_ce (softmax(z_t) - e_y) per valid token (s_n the row scale
+ * of the reduction), and
+ *   d_h_t = G_t W_t   (W_s for a tied teacher)     [N, D_t]
+ *   d_w_t = G_t^T H_t (separate teachers only)     [V, D_t]
+ * in kd_problem.dtype.  They need a hidden student, a tied or separate
+ * teacher and problem->teacher_grads = 1 (KD_ERR_INVALID_ARG otherwise); with
+ * w_teacher_ce = 0 they are written as zeros. */
+kd_status kd_bwd_grads(const kd_problem* problem, const kd_inputs* inputs, const float* stats,
+                       const float* d_loss, float grad_scale, const kd_grads* grads,
+                       uint32_t* dev_status, void* workspace, size_t ws_bytes, void* stream);
 
 /* Plan introspection: how kd_fwd / kd_bwd will run this problem on the current
  * device.  path: 0 logits streaming, 1 fp32 CUDA cores, 2 tensor cores;

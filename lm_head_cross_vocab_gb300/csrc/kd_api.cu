@@ -80,7 +80,7 @@ struct Plan {
   size_t f_count, f_ce_s, f_ce_t, f_kl, f_stats, f_part, f_sidx, f_sp, f_mass, f_ent, f_bytes;
   // backward workspace
   size_t b_count, b_scale, b_sidx, b_sp, b_mass, b_ent, b_g, b_gt, b_wt, b_hst, b_htt, b_dh,
-      b_dw, b_bytes;
+      b_dw, b_dht, b_dwt, b_bytes;
   int64_t ldv, ldn;  // pitches of W^T [D, ldv] and H^T [D, ldn]
   bool kmajor_b;     // backward GEMMs take W^T / H^T (transposed per backward) as B
   bool two_streams;  // backward GEMMs of chunk k on a side stream beside chunk k+1
@@ -301,7 +301,9 @@ kd_status make_plan(const kd_problem* p, bool has_labels, Plan& P) {
     // Two bf16 gradient chunks (the producer fills one while the GEMMs read
     // the other), each at most N*V/4 elements (N*V/8 with a tied teacher-CE
     // chunk beside it): never more than half a bf16 (tokens x vocab) matrix.
-    const bool tce = P.tied && p->w_teacher_ce != 0.f;
+    // a teacher-CE gradient chunk G_t: into d W_s for a tied teacher, and
+    // for d H_t / d W_t when those are requested (tied or separate teachers)
+    const bool tce = P.t_gemm && p->w_teacher_ce != 0.f && (P.tied || p->teacher_grads);
     choose_chunk(p, (int64_t)64 << 20, 256, tce ? 8 : 4, P.R, P.C);
     if (P.s_gemm) {
       // The tensor cores read an MN-major B operand about 6 % slower than a
@@ -317,17 +319,21 @@ kd_status make_plan(const kd_problem* p, bool has_labels, Plan& P) {
       if (P.kmajor_b) {
         P.b_wt = b.take(P.ds * P.ldv * 2);            // W_s^T (B operand of dH)
         P.b_hst = b.take(P.ds * P.ldn * 2);           // H_s^T (B operand of dW)
-        if (tce) P.b_htt = b.take(P.ds * P.ldn * 2);  // H_t^T
+        if (tce && P.tied) P.b_htt = b.take(P.ds * P.ldn * 2);  // H_t^T
       }
       P.b_g = b.take(2 * P.R * P.C * 2);
       if (tce) P.b_gt = b.take(2 * P.R * P.C * 2);
       if (cdiv(v, P.C) > 1) P.b_dh = b.take(n * P.ds * 4);
       if (cdiv(n, P.R) > 1) P.b_dw = b.take(v * P.ds * 4);
+      // fp32 accumulators of d H_t (over vocab chunks) and d W_t (over token chunks)
+      if (tce && cdiv(v, P.C) > 1) P.b_dht = b.take(n * P.dt * 4);
+      if (tce && !P.tied && cdiv(n, P.R) > 1) P.b_dwt = b.take(v * P.dt * 4);
     }
   } else if (P.path == PATH_SIMT) {
     choose_chunk(p, (int64_t)8 << 20, 64, 8, P.R, P.C);
     P.b_g = b.take(P.R * P.C * 4);
-    if (P.tied) P.b_gt = b.take(P.R * P.C * 4);  // teacher-CE gradient tile
+    if (P.tied || (P.t_gemm && p->teacher_grads))
+      P.b_gt = b.take(P.R * P.C * 4);  // teacher-CE gradient tile
   }
   P.b_bytes = b.off;
   return KD_OK;
@@ -608,10 +614,10 @@ kd_status kd_fwd(const kd_problem* problem, const kd_inputs* in, float* ce_s, fl
   return cuda_status(cudaGetLastError());
 }
 
-kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* stats,
-                 const float* d_loss, float grad_scale, void* d_h_s, void* d_w_s,
-                 void* d_logits_s, uint32_t* dev_status, void* workspace, size_t ws_bytes,
-                 void* stream_) {
+static kd_status bwd_impl(const kd_problem* problem, const kd_inputs* in, const float* stats,
+                          const float* d_loss, float grad_scale, void* d_h_s, void* d_w_s,
+                          void* d_logits_s, void* d_h_t, void* d_w_t, uint32_t* dev_status,
+                          void* workspace, size_t ws_bytes, void* stream_) {
   kd_status st = check_problem(problem);
   if (st != KD_OK) return st;
   st = check_inputs(problem, in);
@@ -620,16 +626,41 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
   if (!std::isfinite(grad_scale)) return KD_ERR_INVALID_ARG;
   if (p->student == KD_STUDENT_HIDDEN && d_logits_s) return KD_ERR_INVALID_ARG;
   if (p->student == KD_STUDENT_LOGITS && (d_h_s || d_w_s)) return KD_ERR_INVALID_ARG;
+  // teacher gradients: hidden student, tied / separate teacher, workspace
+  // sized for them; d W_t only for a separate teacher (a tied teacher's
+  // weight is W_s, whose gradient d_w_s carries)
+  if ((d_h_t || d_w_t) &&
+      (p->student != KD_STUDENT_HIDDEN || !p->teacher_grads ||
+       (p->teacher != KD_TEACHER_TIED && p->teacher != KD_TEACHER_SEPARATE) ||
+       (d_w_t && p->teacher != KD_TEACHER_SEPARATE)))
+    return KD_ERR_INVALID_ARG;
   Plan P;
   st = make_plan(p, in->labels != nullptr, P);
   if (st != KD_OK) return st;
-  if (P.n == 0 || (!d_h_s && !d_w_s && !d_logits_s)) return KD_OK;
+  if (!d_h_s && !d_w_s && !d_logits_s && !d_h_t && !d_w_t) return KD_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream_);
+  const size_t esz = P.is_bf16 ? 2 : 4;
+  // no tokens (or a teacher CE weight of 0): the weight / teacher gradients
+  // are zero, written as such
+  const bool no_tce = p->w_teacher_ce == 0.f;
+  if (P.n == 0 || (no_tce && (d_h_t || d_w_t))) {
+    st = check_device();
+    if (st != KD_OK) return st;
+    if (P.n == 0 && d_w_s && cudaMemsetAsync(d_w_s, 0, (size_t)P.v * P.ds * esz, s) != cudaSuccess)
+      return KD_ERR_CUDA;
+    if (d_w_t && cudaMemsetAsync(d_w_t, 0, (size_t)P.v * P.dt * esz, s) != cudaSuccess)
+      return KD_ERR_CUDA;
+    if (d_h_t && P.n > 0 &&
+        cudaMemsetAsync(d_h_t, 0, (size_t)P.n * P.dt * esz, s) != cudaSuccess)
+      return KD_ERR_CUDA;
+    d_h_t = d_w_t = nullptr;
+    if (P.n == 0 || (!d_h_s && !d_w_s && !d_logits_s)) return KD_OK;
+  }
   if (!stats) return KD_ERR_INVALID_ARG;
   if (!workspace || ws_bytes < P.b_bytes || (reinterpret_cast<uintptr_t>(workspace) % kAlign))
     return KD_ERR_WORKSPACE;
   st = check_device();
   if (st != KD_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream_);
   const int64_t n = P.n, v = P.v;
   int32_t* count = at<int32_t>(workspace, P.b_count);
   float* scale = at<float>(workspace, P.b_scale);
@@ -648,7 +679,10 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
                      dev_status, s);
   }
   const float w_kl_ts = (P.has_t || P.topk) ? p->w_kl * p->t_student : 0.f;
-  const float w_tce = (P.tied && d_w_s) ? p->w_teacher_ce : 0.f;
+  // the teacher-CE gradient chunk G_t is made when something consumes it
+  const float w_tce = ((P.tied && d_w_s) || d_h_t || d_w_t) ? p->w_teacher_ce : 0.f;
+  const bool tied_tce = P.tied && d_w_s && w_tce != 0.f;  // G_t^T H_t into d W_s
+  const void* w_teach = P.tied ? in->w_s : in->w_t;      // the teacher's head weight
   if (P.path == PATH_STREAM) {
     StreamArgs a;
     memset(&a, 0, sizeof(a));
@@ -726,10 +760,17 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
         if (d_w_s) {  // dW[c0.., :] (+)= G^T H[r0.., :]
           float* dw = static_cast<float*>(d_w_s) + c0 * D;
           launch_simt_gemm(g, 1, cc, H + r0 * D, D, 1, dw, D, cc, D, rc, ri > 0, s);
-          if (gt)
+          if (gt && tied_tce)
             launch_simt_gemm(gt, 1, cc, static_cast<const float*>(in->h_t) + r0 * D, D, 1, dw, D,
                              cc, D, rc, true, s);
         }
+        const int64_t Dt = P.dt;
+        if (gt && d_h_t)  // dH_t[r0.., :] (+)= G_t W_t[c0.., :]
+          launch_simt_gemm(gt, cc, 1, static_cast<const float*>(w_teach) + c0 * Dt, Dt, 1,
+                           static_cast<float*>(d_h_t) + r0 * Dt, Dt, rc, Dt, cc, ci > 0, s);
+        if (gt && d_w_t)  // dW_t[c0.., :] (+)= G_t^T H_t[r0.., :]
+          launch_simt_gemm(gt, 1, cc, static_cast<const float*>(in->h_t) + r0 * Dt, Dt, 1,
+                           static_cast<float*>(d_w_t) + c0 * Dt, Dt, cc, Dt, rc, ri > 0, s);
       }
     }
     prof_record(3, s);
@@ -742,7 +783,7 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
   const bool kb = P.s_gemm && P.kmajor_b;
   __nv_bfloat16* wT = (kb && d_h_s) ? at<__nv_bfloat16>(workspace, P.b_wt) : nullptr;
   __nv_bfloat16* hsT = (kb && d_w_s) ? at<__nv_bfloat16>(workspace, P.b_hst) : nullptr;
-  __nv_bfloat16* htT = (kb && gt && d_w_s) ? at<__nv_bfloat16>(workspace, P.b_htt) : nullptr;
+  __nv_bfloat16* htT = (kb && tied_tce) ? at<__nv_bfloat16>(workspace, P.b_htt) : nullptr;
   if (wT)
     launch_transpose_bf16(static_cast<const __nv_bfloat16*>(in->w_s), v, D, D, wT, P.ldv, s);
   if (hsT)
@@ -751,6 +792,8 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
     launch_transpose_bf16(static_cast<const __nv_bfloat16*>(in->h_t), n, D, D, htT, P.ldn, s);
   float* dh_acc = (P.s_gemm && nc > 1) ? at<float>(workspace, P.b_dh) : nullptr;
   float* dw_acc = (P.s_gemm && nr > 1) ? at<float>(workspace, P.b_dw) : nullptr;
+  float* dht_acc = (d_h_t && nc > 1) ? at<float>(workspace, P.b_dht) : nullptr;
+  float* dwt_acc = (d_w_t && nr > 1) ? at<float>(workspace, P.b_dwt) : nullptr;
   prof_record(2, s);
   // Two-stream schedule: gradient chunk k is produced on the caller's stream
   // into buffer k%2 while the dH / dW GEMMs of chunk k-1 run on a side
@@ -878,7 +921,7 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
         m.M = cc;
         m.N = D;
         m.K0 = rc;
-        if (gtk) {
+        if (gtk && tied_tce) {
           m.a1 = gtk;
           m.lda1 = C;
           m.a1_mn = 1;
@@ -907,6 +950,54 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
         if (launch_tc_gemm(m, P.nsm, s2) != 0) return KD_ERR_CUDA;
         launch_record(1, 2 * k + 1, true, s2);
       }
+      const int64_t Dt = P.dt;
+      if (gtk && d_h_t) {  // dH_t[r0.., :] (+)= G_t[:, chunk] W_t[chunk, :] (W_t as stored)
+        TcGemmArgs m;
+        memset(&m, 0, sizeof(m));
+        m.a0 = gtk;
+        m.lda0 = C;
+        m.b0 = static_cast<const __nv_bfloat16*>(w_teach) + c0 * Dt;
+        m.ldb0 = Dt;
+        m.b0_mn = 1;
+        m.M = rc;
+        m.N = Dt;
+        m.K0 = cc;
+        m.status = dev_status;
+        if (nc == 1) {
+          m.mode = TC_OUT_BF16;
+        } else {
+          m.mode = ci == 0 ? TC_OUT_F32 : (ci + 1 < nc ? TC_OUT_F32_ACC : TC_OUT_F32_ACC_BF16);
+          m.c32 = dht_acc + r0 * Dt;
+          m.ldc32 = Dt;
+        }
+        m.c16 = static_cast<__nv_bfloat16*>(d_h_t) + r0 * Dt;
+        m.ldc16 = Dt;
+        if (launch_tc_gemm(m, P.nsm, s2) != 0) return KD_ERR_CUDA;
+      }
+      if (gtk && d_w_t) {  // dW_t[chunk, :] (+)= G_t[:, chunk]^T H_t[r0.., :] (H_t as stored)
+        TcGemmArgs m;
+        memset(&m, 0, sizeof(m));
+        m.a0 = gtk;
+        m.lda0 = C;
+        m.a0_mn = 1;
+        m.b0 = static_cast<const __nv_bfloat16*>(in->h_t) + r0 * Dt;
+        m.ldb0 = Dt;
+        m.b0_mn = 1;
+        m.M = cc;
+        m.N = Dt;
+        m.K0 = rc;
+        m.status = dev_status;
+        if (nr == 1) {
+          m.mode = TC_OUT_BF16;
+        } else {
+          m.mode = ri == 0 ? TC_OUT_F32 : (ri + 1 < nr ? TC_OUT_F32_ACC : TC_OUT_F32_ACC_BF16);
+          m.c32 = dwt_acc + c0 * Dt;
+          m.ldc32 = Dt;
+        }
+        m.c16 = static_cast<__nv_bfloat16*>(d_w_t) + c0 * Dt;
+        m.ldc16 = Dt;
+        if (launch_tc_gemm(m, P.nsm, s2) != 0) return KD_ERR_CUDA;
+      }
       if (ss && cudaEventRecord(ss->consumed[buf], s2) != cudaSuccess) return KD_ERR_CUDA;
     }
   }
@@ -915,6 +1006,23 @@ kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* st
     return KD_ERR_CUDA;
   prof_record(3, s);
   return cuda_status(cudaGetLastError());
+}
+
+kd_status kd_bwd(const kd_problem* problem, const kd_inputs* in, const float* stats,
+                 const float* d_loss, float grad_scale, void* d_h_s, void* d_w_s,
+                 void* d_logits_s, uint32_t* dev_status, void* workspace, size_t ws_bytes,
+                 void* stream) {
+  return bwd_impl(problem, in, stats, d_loss, grad_scale, d_h_s, d_w_s, d_logits_s, nullptr,
+                  nullptr, dev_status, workspace, ws_bytes, stream);
+}
+
+kd_status kd_bwd_grads(const kd_problem* problem, const kd_inputs* in, const float* stats,
+                       const float* d_loss, float grad_scale, const kd_grads* grads,
+                       uint32_t* dev_status, void* workspace, size_t ws_bytes, void* stream) {
+  if (!grads) return KD_ERR_INVALID_ARG;
+  return bwd_impl(problem, in, stats, d_loss, grad_scale, grads->d_h_s, grads->d_w_s,
+                  grads->d_logits_s, grads->d_h_t, grads->d_w_t, dev_status, workspace, ws_bytes,
+                  stream);
 }
 
 kd_status kd_set_profile_launch_events(int kind, void* const* starts, void* const* stops,

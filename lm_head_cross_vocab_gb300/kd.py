@@ -35,7 +35,7 @@ KD_KL_SKEW_FORWARD, KD_KL_SKEW_REVERSE = 4, 5
 KD_REDUCE_MEAN, KD_REDUCE_SUM = 0, 1
 KD_STATS_PER_TOKEN = 8
 KD_STATIC_SCRATCH_BYTES = 32 << 20
-KD_ABI_VERSION = 3  # the kd.h this binding follows
+KD_ABI_VERSION = 4  # the kd.h this binding follows
 
 DTYPES = {"bf16": KD_BF16, "fp32": KD_FP32}
 STUDENTS = {"hidden": KD_STUDENT_HIDDEN, "logits": KD_STUDENT_LOGITS}
@@ -57,7 +57,7 @@ class kd_problem(ctypes.Structure):
         ("w_student_ce", ctypes.c_float), ("w_teacher_ce", ctypes.c_float),
         ("w_kl", ctypes.c_float), ("beta", ctypes.c_float),
         ("ignore_index", ctypes.c_int64), ("num_batch_labels", ctypes.c_int64),
-        ("assume_valid_labels", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("assume_valid_labels", ctypes.c_int32), ("teacher_grads", ctypes.c_int32),
         ("vocab_chunk", ctypes.c_int64), ("seq_chunk", ctypes.c_int64),
     ]
 
@@ -109,11 +109,12 @@ def load_library(path: str = LIB_PATH):
     lib.kd_mix_teacher_logits.argtypes = [vp, ctypes.c_int32, vp, ctypes.c_int64, ctypes.c_int64,
                                           ctypes.c_int32, ctypes.c_int32, vp, ctypes.c_int32, vp,
                                           vp]
+    lib.kd_bwd_grads.argtypes = [P, I, vp, vp, ctypes.c_float, vp, vp, vp, ctypes.c_size_t, vp]
     lib.kd_launch_count.restype = ctypes.c_uint64
     for f in ("kd_workspace_size", "kd_fwd", "kd_bwd", "kd_device_supported", "kd_abi_version",
               "kd_diag_gemm_bf16", "kd_set_profile_events", "kd_set_profile_launch_events",
               "kd_fwd_static_scratch", "kd_project_workspace_size", "kd_project_teacher_logits",
-              "kd_plan_info", "kd_mix_teacher_logits"):
+              "kd_plan_info", "kd_mix_teacher_logits", "kd_bwd_grads"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -256,6 +257,7 @@ class Problem:
     assume_valid_labels: bool = False
     vocab_chunk: int = 0
     seq_chunk: int = 0
+    teacher_grads: bool = False  # the backward may be asked for d_h_t / d_w_t
 
     def to_c(self) -> kd_problem:
         p = kd_problem()
@@ -270,8 +272,13 @@ class Problem:
         p.beta, p.ignore_index = self.beta, self.ignore_index
         p.num_batch_labels = self.num_batch_labels
         p.assume_valid_labels = int(self.assume_valid_labels)
+        p.teacher_grads = int(self.teacher_grads)
         p.vocab_chunk, p.seq_chunk = self.vocab_chunk, self.seq_chunk
         return p
+
+
+class kd_grads(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_void_p) for k in ("d_h_s", "d_w_s", "d_logits_s", "d_h_t", "d_w_t")]
 
 
 def make_inputs(t: dict) -> kd_inputs:
@@ -360,11 +367,21 @@ def backward(problem: Problem, tensors: dict, stats: torch.Tensor, *, d_loss=Non
     _, bb = kd_workspace_size(cp)
     ws = workspace or Workspace()
     wptr, wbytes = ws.get(bb, dev)
-    st = kd_bwd(cp, make_inputs(tensors), _ptr(stats), _ptr(d_loss), grad_scale,
-                _ptr(out.get("d_h_s")), _ptr(out.get("d_w_s")), _ptr(out.get("d_logits_s")),
-                _ptr(out["dev_status"]), wptr, wbytes, _stream(dev))
+    if out.get("d_h_t") is None and out.get("d_w_t") is None:
+        st = kd_bwd(cp, make_inputs(tensors), _ptr(stats), _ptr(d_loss), grad_scale,
+                    _ptr(out.get("d_h_s")), _ptr(out.get("d_w_s")), _ptr(out.get("d_logits_s")),
+                    _ptr(out["dev_status"]), wptr, wbytes, _stream(dev))
+        name = "kd_bwd"
+    else:
+        g = kd_grads(*[_ptr(out.get(k)) for k in ("d_h_s", "d_w_s", "d_logits_s", "d_h_t",
+                                                   "d_w_t")])
+        st = load_library().kd_bwd_grads(ctypes.byref(cp), ctypes.byref(make_inputs(tensors)),
+                                         _ptr(stats), _ptr(d_loss), ctypes.c_float(grad_scale),
+                                         ctypes.byref(g), _ptr(out["dev_status"]), wptr, wbytes,
+                                         _stream(dev))
+        name = "kd_bwd_grads"
     if st != KD_OK:
-        raise KDError(st, "kd_bwd")
+        raise KDError(st, name)
     if check:
         check_status(out["dev_status"], problem.assume_valid_labels)
     return out

@@ -385,3 +385,13 @@ def hidden_grads(h_s, w_s, g_s, h_t=None, g_t=None, tied=False):
     if tied and g_t is not None:
         d_w = d_w + g_t.T @ as_f64(h_t)
     return d_h, d_w
+
+
+def teacher_hidden_grads(h_t, w_t, g_t):
+    """Gradients reaching a trained teacher (orda-kernel README, "Teacher
+    descriptors": teacher_ce_weight > 0 trains the teacher through its CE; the
+    KL variants detach it): with G_t = d loss / d z_t from grad_logits,
+    dH_t = G_t W_t and dW_t = G_t^T H_t (W_t = W_s for a tied teacher)."""
+    h_t, w_t = as_f64(h_t), as_f64(w_t)
+    g_t = np.broadcast_to(as_f64(g_t), (h_t.shape[0], w_t.shape[0]))  # 0 without a teacher CE
+    return g_t @ w_t, g_t.T @ h_t

@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(kd):
 
 
 def test_abi_version_and_status_strings(kd):
-    assert kd.kd_abi_version() == kd.KD_ABI_VERSION == 3
+    assert kd.kd_abi_version() == kd.KD_ABI_VERSION == 4
     for code in range(9):
         s = kd.kd_status_string(code)
         assert s and s != "unknown status"
@@ -184,3 +184,25 @@ def test_mix_argument_rules(kd):
     for kw in (dict(), dict(weights=None), dict(weights=(0.0, 2.0), mode=kd.KD_MIX_GEOMETRIC),
                dict(k=8, weights=None)):
         assert call(**kw) == kd.KD_ERR_NO_DEVICE, kw
+
+
+def test_teacher_grads_argument_rules(kd):
+    """kd_bwd_grads: teacher gradients need a hidden student, a tied / separate
+    teacher and teacher_grads = 1; d_w_t only for a separate teacher."""
+    lib = kd.load_library()
+    fake = 1 << 20
+    ins = kd.kd_inputs(h_s=fake, w_s=fake, h_t=fake, w_t=fake, labels=fake)
+
+    def call(teacher="separate", tg=1, **g):
+        p = _prob(kd, teacher=teacher, d_teacher=64)
+        p.teacher_grads = tg
+        grads = kd.kd_grads(**{k: fake for k in g})
+        return lib.kd_bwd_grads(ctypes.byref(p), ctypes.byref(ins), fake, None, 1.0,
+                                ctypes.byref(grads), None, None, 0, None)
+
+    assert call(tg=0, d_h_t=1) == kd.KD_ERR_INVALID_ARG
+    assert call(teacher="tied", d_w_t=1) == kd.KD_ERR_INVALID_ARG
+    assert lib.kd_bwd_grads(ctypes.byref(_prob(kd)), ctypes.byref(ins), fake, None, 1.0, None,
+                            None, None, 0, None) == kd.KD_ERR_INVALID_ARG
+    # well-formed requests get as far as the workspace / device checks
+    assert call(d_h_t=1, d_w_t=1) in (kd.KD_ERR_WORKSPACE, kd.KD_ERR_NO_DEVICE)

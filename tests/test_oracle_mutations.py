@@ -91,6 +91,13 @@ def _geometric_not_renormalised(orig):
     return mix_teacher_logits
 
 
+def _teacher_dw_sign(orig):
+    def teacher_hidden_grads(h_t, w_t, g_t):
+        d_h, d_w = orig(h_t, w_t, g_t)
+        return d_h, -d_w
+    return teacher_hidden_grads
+
+
 def _no_t_squared():
     orig = O.forward
 
@@ -118,6 +125,8 @@ MUTATIONS = [
     ("mix_teacher_logits", _mix_logits_not_probabilities, P.test_mix_hand_worked_example),
     ("mix_teacher_logits", _mix_weights_unnormalised, P.test_mix_hand_worked_example),
     ("mix_teacher_logits", _geometric_not_renormalised, P.test_mix_brute_force_probabilities),
+    ("teacher_hidden_grads", _teacher_dw_sign,
+     lambda: P.test_teacher_gradients_finite_differences("separate", "forward")),
 ]
 
 

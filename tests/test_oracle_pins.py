@@ -537,3 +537,35 @@ def test_mix_of_projected_teachers_with_zero_probability_ids():
     np.testing.assert_allclose(np.exp(ari), 0.5 * q1 + 0.5 * q2, rtol=1e-14)
     assert np.isneginf(ari[3]) and np.all(np.isfinite(ari[:3]))
     assert np.all(np.isneginf(geo[1:])) and geo[0] == 0.0
+
+
+# ---------------------------------------------------------------- teacher gradients
+
+@pytest.mark.parametrize("kind", ["separate", "tied"])
+@pytest.mark.parametrize("variant", ["forward", "jeffreys", "skew_reverse"])
+def test_teacher_gradients_finite_differences(kind, variant):
+    """d loss / d H_t and d loss / d W_t (separate) of a teacher trained by its
+    CE term, against central differences of the loss with the teacher detached
+    from the KL: only w_tce * mean CE_t moves with the teacher."""
+    rng = np.random.default_rng(17)
+    n, v, d = 5, 12, 6
+    h_s, h_t = rng.normal(size=(n, d)), rng.normal(size=(n, d))
+    w_s = rng.normal(0, 0.4, size=(v, d))
+    w_t = rng.normal(0, 0.4, size=(v, d)) if kind == "separate" else w_s
+    labels = rng.integers(0, v, size=n)
+    labels[3] = -100
+    kw = dict(variant=variant, t_student=1.5, t_teacher=1.5, beta=0.3, w_student_ce=0.7,
+              w_teacher_ce=0.45, w_kl=1.2, ignore_index=-100)
+    z_s = O.project(h_s, w_s)
+    z_t_kl = O.project(h_t, w_t)  # what the KL sees: fixed while the teacher moves
+
+    def loss():
+        out = O.forward(z_s, z_t_kl, labels, **{**kw, "w_teacher_ce": 0.0})
+        ce_t = O.cross_entropy_rows(O.project(h_t, w_t), labels, labels != -100)
+        return out["loss"] + kw["w_teacher_ce"] * ce_t.sum() / (labels != -100).sum()
+
+    _, g_t = O.grad_logits(z_s, z_t_kl, labels, **kw)
+    d_ht, d_wt = O.teacher_hidden_grads(h_t, w_t, g_t)
+    np.testing.assert_allclose(d_ht, _fd(loss, h_t), rtol=1e-6, atol=1e-8)
+    if kind == "separate":
+        np.testing.assert_allclose(d_wt, _fd(loss, w_t), rtol=1e-6, atol=1e-8)
