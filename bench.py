@@ -63,31 +63,43 @@ def bytes_per_step(w: I.Workload):
     return fwd, bwd
 
 
-def kernel_sources_hash() -> str:
-    """Hash of the library sources (kernels and launch planning)."""
+# library sources behind each measured family: the projection and the mixing
+# kernels stand alone; the loss path is everything else in csrc/
+SOURCE_GROUPS = {"project": ("kd_project.cu",), "mix": ("kd_mix.cu",)}
+
+
+def kernel_sources_hash(group: str = "loss") -> str:
+    """Hash of the library sources a kernel family depends on (its kernels,
+    the shared headers and the launch planning)."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "lm_head_cross_vocab_gb300", "csrc")
+    own = {f for g in SOURCE_GROUPS.values() for f in g}
     for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(f.encode())
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
+        if not f.endswith((".cu", ".cuh", ".h")):
+            continue
+        if f.endswith(".cu") and (f not in SOURCE_GROUPS[group] if group in SOURCE_GROUPS
+                                  else f in own):
+            continue
+        h.update(f.encode())
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def load_traffic() -> dict:
+def load_traffic(group: str = "loss") -> dict:
     """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum from
     one ncu capture, profiles/traffic.json), keyed "workload:kernel family";
-    empty once the library sources differ from the ones that were captured."""
+    empty once the sources of that group differ from the ones captured."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return {}
-    if d.get("sources_sha256_16") != kernel_sources_hash():
+    g = d.get("groups", {}).get(group, {})
+    if g.get("sources_sha256_16") != kernel_sources_hash(group):
         return {}
-    return d.get("bytes_per_launch", {})
+    return g.get("bytes_per_launch", {})
 
 
 class ClockSampler:
@@ -271,7 +283,9 @@ def run_projection(args, rank):
             "roofline": {"bound": "hbm", "kernel": "k_project (+ inverse-map build)",
                          "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm_gbs"], "peak_source": f"{peak_src} copy",
-                         "bytes_per_launch": nbytes},
+                         "bytes_per_launch": nbytes,
+                         "traffic": None if args.tokens else
+                         load_traffic("project").get("cross_vocab_projection:k_project")},
             "gpu_launches": kd.kd_launch_count() - launches0}), flush=True)
 
 
@@ -310,7 +324,9 @@ def run_mix(args, rank):
                        "teachers": 2, "weights": w, "l2": "inputs larger than L2"},
             "roofline": {"bound": "hbm", "kernel": "k_mix_cluster", "achieved": gbs,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
-                         "peak_source": f"{peak_src} copy", "bytes_per_launch": nbytes},
+                         "peak_source": f"{peak_src} copy", "bytes_per_launch": nbytes,
+                         "traffic": None if args.tokens else
+                         load_traffic("mix").get(f"mix_2_teachers_{args.mix}:k_mix")},
             "gpu_launches": kd.kd_launch_count() - launches0}), flush=True)
     del out
 
