@@ -347,6 +347,9 @@ def main():
                     help="time the cross-vocabulary token-map projection instead of the loss")
     ap.add_argument("--mix", choices=["arithmetic", "geometric"],
                     help="time multi-teacher mixing (this mode) instead of the loss")
+    ap.add_argument("--variant", choices=["forward", "reverse", "jeffreys", "skew_js",
+                                          "skew_forward", "skew_reverse"],
+                    help="run the workload with this KL variant")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
@@ -357,6 +360,8 @@ def main():
     w = I.WORKLOADS[args.config]
     if args.tokens > 0:
         w = w.scaled(n_tokens=args.tokens)
+    if args.variant:
+        w = w.scaled(variant=args.variant)
 
     if args.impl == "reference":
         run_reference(args, w, rank)
@@ -483,7 +488,9 @@ def main():
     name, k_ms, k_n, k_work = fams[dom]
     per_launch_ms = k_ms / k_n
     achieved = (k_work / k_n) / (per_launch_ms / 1e3) / scale
-    traffic = load_traffic().get(f"{w.name}:{dom}") if not args.tokens else None
+    # (captured at the workload's own size and variant only)
+    traffic = (load_traffic().get(f"{w.name}:{dom}")
+               if not args.tokens and not args.variant else None)
     roofline = {"bound": bound, "kernel": name, "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak, "peak_source": psrc, "traffic": traffic,
                 ("flops_per_launch" if bound == "tensor" else "bytes_per_launch"): k_work / k_n,
