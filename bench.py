@@ -280,7 +280,7 @@ def run_projection(args, rank):
             "config": {"workload": "cross_vocab_projection", "tokens": n, "v_teacher": v_t,
                        "v_student": v_s, "temperature": 2.0,
                        "l2": "inputs larger than L2"},
-            "roofline": {"bound": "hbm", "kernel": "k_project (+ inverse-map build)",
+            "roofline": {"bound": "hbm", "kernel": "k_project_exchange (+ inverse map, exchange lists)",
                          "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm_gbs"], "peak_source": f"{peak_src} copy",
                          "bytes_per_launch": nbytes,

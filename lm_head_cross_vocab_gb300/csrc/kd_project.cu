@@ -9,12 +9,20 @@
 // output type, whose exponential is exactly 0 like that of -inf, so the
 // distillation kernels need no special case for it (0 * log 0 terms stay 0).
 //
-// The inverse map is built on the device in the caller's workspace on every
-// call (count -> exclusive scan -> scatter -> per-id sort, so the summation
-// order and the result are deterministic, plus a per-id column for the common
-// case of exactly one teacher token); then one CTA per SM takes token rows in
-// turn, stages each in shared memory and takes, for every student id, the
-// log-sum-exp over the teacher columns of its id.
+// Every call first builds, in the caller's workspace, the inverse map (count
+// -> exclusive scan -> scatter -> per-id sort, so summation orders are fixed
+// and results deterministic) and a partition of the student ids by the slice
+// of the teacher row that produces them.  The teacher row is cut into C
+// slices of at most kSliceMax bytes; the id list of slice r holds, in
+// ascending id order, the ids whose (first) teacher column lies in slice r,
+// plus a share of the unmatched ids.  Then the work items are (token row,
+// slice): a CTA stages the slice in shared memory with one bulk copy
+// (double-buffered across its items), reads each listed id's column there --
+// every random access is a local shared-memory read -- and stores the id's
+// output straight to global memory.  A warp writes 32 consecutive list
+// entries, i.e. ids within a short ascending run, so the stores of the C
+// slices of a row fill each other's sectors in L2 and each output byte goes
+// to HBM once.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -30,6 +38,9 @@ namespace kd {
 namespace {
 
 constexpr int kT = 256;
+constexpr int kPT = 1024;                 // threads per projection CTA
+constexpr int64_t kSliceMax = 96 * 1024;  // bytes of a staged slice (two per CTA)
+constexpr int kMaxSlices = 1024;          // teacher rows up to 96 MiB
 
 __global__ void k_map_count(const int32_t* __restrict__ map, int64_t vt, int64_t vs,
                             int32_t* __restrict__ cnt, uint32_t* status) {
@@ -92,22 +103,16 @@ __global__ void __launch_bounds__(1024) k_map_scan(const int32_t* __restrict__ c
   if (t == 0) off[vs] = carry;
 }
 
-// one[i] for student id i: -1 when no teacher token maps to it, -2 when
-// several do, and when exactly one does, its teacher column c -- or, for the
-// cluster kernel (sc > 0), where that column is staged: the CTA c / sc of the
-// cluster in bits 17.. and the element c % sc in bits 0..16.
-constexpr int kEncBits = 17;
+// one[i] for student id i: its teacher column when exactly one teacher token
+// maps to it, -1 when none does, -2 when several do; eid[e]: the student id of
+// map edge e (the e-th entry of the id-sorted column list).
 __global__ void k_map_single(const int32_t* __restrict__ off, const int32_t* __restrict__ cols,
-                             int64_t vs, int32_t sc, int32_t* __restrict__ one) {
+                             int64_t vs, int32_t* __restrict__ one, int32_t* __restrict__ eid) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < vs;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int32_t b = off[i], e = off[i + 1];
-    int32_t v = e == b ? -1 : -2;
-    if (e - b == 1) {
-      v = cols[b];
-      if (sc > 0) v = (v / sc) << kEncBits | (v % sc);
-    }
-    one[i] = v;
+    one[i] = e - b == 1 ? cols[b] : (e == b ? -1 : -2);
+    for (int32_t k = b; k < e; ++k) eid[k] = (int32_t)i;
   }
 }
 
@@ -166,19 +171,6 @@ __device__ __forceinline__ float lowest<__nv_bfloat16>() {
   return __uint_as_float(0xff7f0000u);  // most negative finite bf16
 }
 
-// One CTA per SM, one token row at a time.  The teacher row is staged in
-// shared memory in slices of at most kSlice bytes (one slice when it fits, two
-// for a 152k bf16 vocabulary), with coalesced 16-byte loads; every student id
-// then folds the teacher tokens of its segment that fall in the slice into a
-// running log-sum-exp (logaddexp; a single token gives z / T exactly).
-// Between slices the running values live in a per-CTA fp32 scratch row (it
-// stays in L2); the last slice writes the output row with vector stores.  So
-// the random gathers hit shared memory and all global traffic is coalesced.
-constexpr int kPT = 1024;               // threads per projection CTA
-constexpr int kIds = 8;                 // student ids per thread per step
-constexpr int64_t kSlice = 200 * 1024;  // bytes of a staged teacher-row slice
-
-__host__ __device__ __forceinline__ int64_t scratch_pitch(int64_t vs) { return (vs + 7) / 8 * 8; }
 
 __device__ __forceinline__ float logaddexp(float a, float b) {
   if (a == -INFINITY) return b;
@@ -199,172 +191,263 @@ __device__ __forceinline__ void store_vec(__nv_bfloat16* o, const float* r) {
   *reinterpret_cast<uint4*>(o) = u;
 }
 
-template <typename TI, typename TO>
-__global__ void __launch_bounds__(kPT, 1) k_project(const TI* __restrict__ zt, int64_t n,
-                                                    int64_t vt, int64_t vs, float inv_t,
-                                                    const int32_t* __restrict__ off,
-                                                    const int32_t* __restrict__ cols,
-                                                    const int32_t* __restrict__ one,
-                                                    TO* __restrict__ out,
-                                                    float* __restrict__ scratch, int64_t span) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  TI* zsm = reinterpret_cast<TI*>(smem_raw);
-  // scratch rows have a pitch of vs rounded up to 8 floats, so every row and
-  // every 8-id group in it is 16-byte aligned for the float4 accesses below
-  float* part = scratch ? scratch + (int64_t)blockIdx.x * scratch_pitch(vs) : nullptr;
-  const int passes = (int)((vt + span - 1) / span);
-  constexpr int EV = 16 / (int)sizeof(TI);  // elements per 16-byte vector
-  for (int64_t row = blockIdx.x; row < n; row += gridDim.x) {
-    const TI* z = zt + row * vt;
-    TO* o = out + row * vs;
-    for (int p = 0; p < passes; ++p) {
-      const int64_t lo = (int64_t)p * span, hi = lo + span < vt ? lo + span : vt;
-      const int64_t len = hi - lo;
-      __syncthreads();  // the previous slice is no longer read
-      if ((reinterpret_cast<uintptr_t>(z + lo) & 15) == 0) {
-        const int64_t nvec = len / EV;
-        for (int64_t q = threadIdx.x; q < nvec; q += kPT)
-          reinterpret_cast<uint4*>(zsm)[q] = reinterpret_cast<const uint4*>(z + lo)[q];
-        for (int64_t q = nvec * EV + threadIdx.x; q < len; q += kPT) zsm[q] = z[lo + q];
-      } else {
-        for (int64_t q = threadIdx.x; q < len; q += kPT) zsm[q] = z[lo + q];
-      }
-      __syncthreads();
-      const bool last = p + 1 == passes;
-      for (int64_t i0 = (int64_t)threadIdx.x * kIds; i0 < vs; i0 += (int64_t)kPT * kIds) {
-        const bool full = i0 + kIds <= vs;
-        // one coalesced load classifies the 8 ids; only ids with several
-        // teacher tokens read their segment bounds
-        int32_t oc[kIds];
-        if (full) {
-          const int4 a = reinterpret_cast<const int4*>(one + i0)[0];
-          const int4 b = reinterpret_cast<const int4*>(one + i0)[1];
-          oc[0] = a.x; oc[1] = a.y; oc[2] = a.z; oc[3] = a.w;
-          oc[4] = b.x; oc[5] = b.y; oc[6] = b.z; oc[7] = b.w;
-        } else {
-#pragma unroll
-          for (int k = 0; k < kIds; ++k) oc[k] = i0 + k < vs ? one[i0 + k] : -1;
-        }
-        float r[kIds];
-        if (p == 0) {
-#pragma unroll
-          for (int k = 0; k < kIds; ++k) r[k] = -INFINITY;
-        } else if (full) {
-          const float4 a = reinterpret_cast<const float4*>(part + i0)[0];
-          const float4 b = reinterpret_cast<const float4*>(part + i0)[1];
-          r[0] = a.x; r[1] = a.y; r[2] = a.z; r[3] = a.w;
-          r[4] = b.x; r[5] = b.y; r[6] = b.z; r[7] = b.w;
-        } else {
-#pragma unroll
-          for (int k = 0; k < kIds; ++k) r[k] = i0 + k < vs ? part[i0 + k] : -INFINITY;
-        }
-#pragma unroll
-        for (int k = 0; k < kIds; ++k) {
-          const int64_t c = oc[k];
-          if (c >= lo && c < hi) {  // the id's only teacher token lies in this slice
-            r[k] = logaddexp(r[k], ld<TI>(zsm + (c - lo)) * inv_t);
-          } else if (c == -2) {
-            const int32_t e = off[i0 + k + 1];
-#pragma unroll 1
-            for (int32_t t = off[i0 + k]; t < e; ++t) {
-              const int64_t ct = cols[t];
-              if (ct >= lo && ct < hi) r[k] = logaddexp(r[k], ld<TI>(zsm + (ct - lo)) * inv_t);
-            }
-          }
-        }
-        if (last) {
-#pragma unroll
-          for (int k = 0; k < kIds; ++k)
-            if (r[k] == -INFINITY) r[k] = lowest<TO>();
-          if (full && (reinterpret_cast<uintptr_t>(o + i0) & 15) == 0) {
-            store_vec(o + i0, r);
-          } else {
-#pragma unroll
-            for (int k = 0; k < kIds; ++k)
-              if (i0 + k < vs) st<TO>(o + i0 + k, r[k]);
-          }
-        } else if (full) {
-          store_vec(part + i0, r);
-        } else {
-#pragma unroll
-          for (int k = 0; k < kIds; ++k)
-            if (i0 + k < vs) part[i0 + k] = r[k];
-        }
-      }
+// ---------------------------------------------------------------- exchange lists
+
+// The exchange path (see k_project_exchange): a cluster of C <= kMaxC CTAs per
+// token row; CTA r stages teacher columns [r*sc, r*sc + sc) and writes student
+// ids [q*so, q*so + so) for q = r.  Map edge e (teacher column cols[e] ->
+// student id eid[e]) travels from CTA r = cols[e] / sc to CTA q = eid[e] / so
+// in segment (r, q).  Segments are padded to 8 elements so that every bulk
+// copy starts and ends on 16 bytes.
+constexpr int kMaxC = 8;
+struct XLayout {
+  int32_t cnt[kMaxC * kMaxC];      // edges of segment (r, q), at r * C + q
+  int32_t sendoff[kMaxC * kMaxC];  // offset of segment (r, q) in CTA r's send buffer
+  int32_t recvoff[kMaxC * kMaxC];  // offset of segment (r, q) in CTA q's receive buffer
+  int32_t sendbase[kMaxC + 1];     // start of CTA r's gather list in send_src
+  int32_t sendtot[kMaxC];          // padded elements CTA r sends
+  int32_t recvtot[kMaxC];          // padded elements CTA q receives
+  int32_t fits;                    // 1: every buffer fits, the exchange kernel runs
+};
+__host__ __device__ __forceinline__ int32_t pad8(int32_t x) { return (x + 7) & ~7; }
+
+__device__ __forceinline__ int edge_key(int32_t e, const int32_t* __restrict__ cols,
+                                        const int32_t* __restrict__ eid, int32_t sc, int32_t so,
+                                        int C) {
+  return (cols[e] / sc) * C + eid[e] / so;
+}
+
+__global__ void k_edge_count(const int32_t* __restrict__ off, const int32_t* __restrict__ cols,
+                             const int32_t* __restrict__ eid, int64_t vs, int32_t sc, int32_t so,
+                             int C, XLayout* __restrict__ X) {
+  __shared__ int32_t h[kMaxC * kMaxC];
+  for (int k = threadIdx.x; k < C * C; k += blockDim.x) h[k] = 0;
+  __syncthreads();
+  const int32_t E = off[vs];
+  const int32_t stride = gridDim.x * blockDim.x;
+  for (int32_t e0 = blockIdx.x * blockDim.x; e0 < E; e0 += stride) {
+    const int32_t e = e0 + (int32_t)threadIdx.x;
+    const int k = e < E ? edge_key(e, cols, eid, sc, so, C) : -1;
+    const unsigned same = __match_any_sync(0xffffffffu, k);
+    if (k >= 0 && (threadIdx.x & 31) == __ffs(same) - 1) atomicAdd(&h[k], __popc(same));
+  }
+  __syncthreads();
+  for (int k = threadIdx.x; k < C * C; k += blockDim.x)
+    if (h[k]) atomicAdd(&X->cnt[k], h[k]);
+}
+
+// padded offsets of every segment, and whether the buffers fit: send_cap and
+// recv_cap are the elements the exchange kernel's shared memory holds
+__global__ void k_exchange_layout(XLayout* X, int C, int32_t send_cap, int32_t recv_cap) {
+  if (threadIdx.x != 0) return;
+  int fits = 1;
+  int32_t base = 0;
+  for (int r = 0; r < C; ++r) {
+    int32_t o = 0;
+    for (int q = 0; q < C; ++q) {
+      X->sendoff[r * C + q] = o;
+      o += pad8(X->cnt[r * C + q]);
     }
+    X->sendtot[r] = o;
+    X->sendbase[r] = base;
+    base += o;
+    fits &= o <= send_cap;
+  }
+  X->sendbase[C] = base;
+  for (int q = 0; q < C; ++q) {
+    int32_t o = 0;
+    for (int r = 0; r < C; ++r) {
+      X->recvoff[r * C + q] = o;
+      o += pad8(X->cnt[r * C + q]);
+    }
+    X->recvtot[q] = o;
+    fits &= o <= recv_cap;
+  }
+  X->fits = fits;
+}
+
+// Block k = (r, q) places the edges of segment k in ascending edge order:
+// CTA r's gather list gets the column offset within its slice, and epos[e]
+// the edge's slot in CTA q's receive buffer.
+__global__ void __launch_bounds__(1024) k_edge_partition(
+    const int32_t* __restrict__ off, const int32_t* __restrict__ cols,
+    const int32_t* __restrict__ eid, int64_t vs, int32_t sc, int32_t so, int C,
+    const XLayout* __restrict__ X, int32_t* __restrict__ send_src, int32_t* __restrict__ epos) {
+  __shared__ int32_t wsum[32];
+  const int k = blockIdx.x, r = k / C;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int32_t E = off[vs];
+  int32_t* dst = send_src + X->sendbase[r] + X->sendoff[k];
+  const int32_t rbase = X->recvoff[k];
+  int32_t base = 0;
+  for (int32_t t0 = 0; t0 < E; t0 += 1024 * 8) {
+    const int32_t e0 = t0 + (int32_t)threadIdx.x * 8;
+    uint32_t hit = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (e0 + q < E && edge_key(e0 + q, cols, eid, sc, so, C) == k) hit |= 1u << q;
+    const int32_t own = __popc(hit);
+    int32_t inc = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t u = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += u;
+    }
+    if (lane == 31) wsum[w] = inc;
+    __syncthreads();
+    if (w == 0) {
+      int32_t x = wsum[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t u = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += u;
+      }
+      wsum[lane] = x;
+    }
+    __syncthreads();
+    int32_t pos = base + (w > 0 ? wsum[w - 1] : 0) + inc - own;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (hit >> q & 1u) {
+        dst[pos] = cols[e0 + q] - r * sc;
+        epos[e0 + q] = rbase + pos;
+        ++pos;
+      }
+    base += wsum[31];
+    __syncthreads();  // wsum is rewritten by the next tile
   }
 }
 
-// Cluster projection.  A cluster of C CTAs (C = 1, 2, 4 or 8, one CTA per SM)
-// works on one token row at a time: CTA r holds teacher columns
-// [r*sc, r*sc + sc) of the row in its shared memory, brought in by one bulk
-// copy (double-buffered, so the copy of the cluster's next row runs under the
-// gathers of this one), and writes student ids [r*so, r*so + so) of the output
-// row.  Each id's teacher column is read from whichever CTA of the cluster
-// holds it (distributed shared memory), so the row is read from HBM once, the
-// output written once with vector stores, and no partial results are kept.
-constexpr int64_t kBuf = 104 * 1024;  // bytes of one staged slice (two per CTA)
-constexpr int kGroups = 1;  // groups of 8 ids per thread whose gathers are in flight together
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_size() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-// every thread of every CTA of the cluster; release / acquire at cluster scope
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-// element `e` of the staged-row buffer at shared-memory offset `base` of
-// CTA `r` of the cluster.  (Plain loads, free to be batched by the compiler:
-// the buffers do not change between the cluster barriers that bracket them.)
-template <typename TI>
-__device__ __forceinline__ float dsmem_get(uint32_t base, uint32_t r, uint32_t e) {
-  uint32_t a = base + e * (uint32_t)sizeof(TI);
-  asm("mapa.shared::cluster.u32 %0, %0, %1;" : "+r"(a) : "r"(r));
-  if constexpr (sizeof(TI) == 2) {
-    uint16_t v;
-    asm("ld.shared::cluster.u16 %0, [%1];" : "=h"(v) : "r"(a));
-    return __bfloat162float(__ushort_as_bfloat16(v));
-  } else {
-    float v;
-    asm("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a));
-    return v;
+// code[i]: the receive-buffer slot of student id i's single edge, -1 for no
+// teacher token, -2 for several (their slots: epos[off[i] .. off[i+1]))
+__global__ void k_exchange_codes(const int32_t* __restrict__ off,
+                                 const int32_t* __restrict__ epos, int64_t vs,
+                                 int32_t* __restrict__ code) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < vs;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t b = off[i], e = off[i + 1];
+    code[i] = e - b == 1 ? epos[b] : (e == b ? -1 : -2);
   }
 }
-// teacher value at column c of the staged row
-template <typename TI>
-__device__ __forceinline__ float dsmem_col(uint32_t base, uint32_t c, uint32_t sc) {
-  const uint32_t r = c / sc;
-  return dsmem_get<TI>(base, r, c - r * sc);
+
+// ---------------------------------------------------------------- slice lists
+
+// The slice that writes student id i: the one holding its teacher column (its
+// first, for an id with several); unmatched ids are spread over the slices in
+// contiguous id ranges.
+__device__ __forceinline__ int slice_of(int64_t i, const int32_t* __restrict__ one,
+                                        const int32_t* __restrict__ off,
+                                        const int32_t* __restrict__ cols, int64_t vs, int32_t sc,
+                                        int nsl) {
+  const int32_t c = one[i];
+  if (c >= 0) return c / sc;
+  if (c == -2) return cols[off[i]] / sc;
+  return (int)(i * nsl / vs);
 }
 
+// ids per slice: a shared-memory histogram per block (one atomic per warp
+// and slice, via __match_any_sync), then one global atomic per block and slice
+__global__ void k_slice_count(const int32_t* __restrict__ one, const int32_t* __restrict__ off,
+                              const int32_t* __restrict__ cols, int64_t vs, int32_t sc, int nsl,
+                              int32_t* __restrict__ slice_cnt, const XLayout* X) {
+  if (X && X->fits) return;  // the exchange path runs instead
+  __shared__ int32_t h[kMaxSlices];
+  for (int s = threadIdx.x; s < nsl; s += blockDim.x) h[s] = 0;
+  __syncthreads();
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x; i0 < vs; i0 += stride) {
+    const int64_t i = i0 + threadIdx.x;
+    const int s = i < vs ? slice_of(i, one, off, cols, vs, sc, nsl) : -1;
+    const unsigned same = __match_any_sync(0xffffffffu, s);
+    if (s >= 0 && (threadIdx.x & 31) == __ffs(same) - 1) atomicAdd(&h[s], __popc(same));
+  }
+  __syncthreads();
+  for (int s = threadIdx.x; s < nsl; s += blockDim.x)
+    if (h[s]) atomicAdd(&slice_cnt[s], h[s]);
+}
+
+// Block r lists the ids of slice r in ascending order (a stable partition:
+// 8 ids per thread per tile, block-wide prefix sums of the matches), with
+// their column within the slice, or -1 (unmatched) / -2 (several columns).
+// It also writes slice_off[r] (and slice_off[nsl] from the last block).
+__global__ void __launch_bounds__(1024) k_slice_partition(
+    const int32_t* __restrict__ one, const int32_t* __restrict__ off,
+    const int32_t* __restrict__ cols, int64_t vs, int32_t sc, int nsl,
+    const int32_t* __restrict__ slice_cnt, int32_t* __restrict__ slice_off,
+    int32_t* __restrict__ list_id, int32_t* __restrict__ list_val, const XLayout* X) {
+  if (X && X->fits) return;  // the exchange path runs instead
+  __shared__ int32_t wsum[32];
+  __shared__ int32_t base_sh;
+  const int r = blockIdx.x;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    int32_t b = 0;
+    for (int s = 0; s < r; ++s) b += slice_cnt[s];
+    base_sh = b;
+    slice_off[r] = b;
+    if (r == nsl - 1) slice_off[nsl] = b + slice_cnt[r];
+  }
+  __syncthreads();
+  int32_t base = base_sh;
+  for (int64_t t0 = 0; t0 < vs; t0 += 1024 * 8) {
+    const int64_t i0 = t0 + (int64_t)threadIdx.x * 8;
+    uint32_t hit = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (i0 + q < vs && slice_of(i0 + q, one, off, cols, vs, sc, nsl) == r) hit |= 1u << q;
+    const int32_t own = __popc(hit);
+    int32_t inc = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t u = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += u;
+    }
+    if (lane == 31) wsum[w] = inc;
+    __syncthreads();
+    if (w == 0) {
+      int32_t x = wsum[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t u = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += u;
+      }
+      wsum[lane] = x;
+    }
+    __syncthreads();
+    int32_t pos = base + (w > 0 ? wsum[w - 1] : 0) + inc - own;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (hit >> q & 1u) {
+        const int32_t c = one[i0 + q];
+        list_id[pos] = (int32_t)(i0 + q);
+        list_val[pos] = c >= 0 ? c - r * sc : c;
+        ++pos;
+      }
+    base += wsum[31];
+    __syncthreads();  // wsum is rewritten by the next tile
+  }
+}
+
+// ---------------------------------------------------------------- projection
+
+// Work items (token row, slice), grid-strided over one CTA per SM.  Each item
+// stages its slice of the teacher row (buffer it & 1; the copy of the next
+// item is started before this one is processed), then writes the output of
+// every id on the slice's list: a single teacher column is read from shared
+// memory, several are read from the row in global memory (still in L2, the
+// other slices' CTAs having just streamed it) and folded in column order.
 template <typename TI, typename TO>
 __global__ void __launch_bounds__(kPT, 1)
-    k_project_cluster(const TI* __restrict__ zt, int64_t n, int64_t vt, int64_t vs, float inv_t,
-                      const int32_t* __restrict__ off, const int32_t* __restrict__ cols,
-                      const int32_t* __restrict__ one, TO* __restrict__ out, int64_t sc,
-                      int64_t so, uint32_t* status) {
+    k_project_slices(const TI* __restrict__ zt, int64_t n, int64_t vt, int64_t vs, float inv_t,
+                     const int32_t* __restrict__ off, const int32_t* __restrict__ cols,
+                     const int32_t* __restrict__ list_id, const int32_t* __restrict__ list_val,
+                     const int32_t* __restrict__ slice_off, int64_t sc, int nsl,
+                     TO* __restrict__ out, uint32_t* status, const XLayout* X) {
+  if (X && X->fits) return;  // the exchange path runs instead
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[2];
   __shared__ int abort_flag;
-  const uint32_t rank = cluster_rank(), csize = cluster_size();
-  const int64_t ncl = gridDim.x / csize;
-  const int64_t c0 = (int64_t)rank * sc;
-  const int64_t clen = vt - c0 < sc ? (vt - c0 > 0 ? vt - c0 : 0) : sc;  // my columns
-  const int64_t i_lo = (int64_t)rank * so, i_hi = i_lo + so < vs ? i_lo + so : vs;
-  const uint32_t buf_sa = ptx::smem_u32(smem_raw);
-  const uint32_t buf_bytes = (uint32_t)(sc * (int64_t)sizeof(TI));
+  const size_t buf_bytes = (size_t)sc * sizeof(TI);
   if (threadIdx.x == 0) {
     ptx::mbar_init(ptx::smem_u32(&bars[0]), 1);
     ptx::mbar_init(ptx::smem_u32(&bars[1]), 1);
@@ -372,9 +455,12 @@ __global__ void __launch_bounds__(kPT, 1)
     abort_flag = 0;
   }
   __syncthreads();
-  // stage my columns of `row` into buffer b: the 16-byte-aligned bulk by one
-  // bulk copy, a ragged tail (or a whole unaligned row) by plain loads
-  auto stage = [&](int64_t row, int b) {
+  const int64_t items = n * nsl;
+  // stage item `item` into buffer b: the 16-byte-aligned bulk by one bulk
+  // copy, a ragged tail (or a whole unaligned slice) by plain loads
+  auto stage = [&](int64_t item, int b) {
+    const int64_t row = item / nsl, c0 = (item % nsl) * sc;
+    const int64_t clen = vt - c0 < sc ? vt - c0 : sc;
     const TI* src = zt + row * vt + c0;
     TI* dst = reinterpret_cast<TI*>(smem_raw + (size_t)b * buf_bytes);
     const bool al = ((reinterpret_cast<uintptr_t>(src) | ptx::smem_u32(dst)) & 15) == 0;
@@ -384,203 +470,326 @@ __global__ void __launch_bounds__(kPT, 1)
       const uint32_t bar = ptx::smem_u32(&bars[b]);
       ptx::mbar_expect_tx(bar, (uint32_t)nb);
       if (nb > 0) {
-        fence_proxy_async();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         ptx::bulk_load(ptx::smem_u32(dst), src, (uint32_t)nb, bar);
       }
     }
     for (int64_t q = nb / (int64_t)sizeof(TI) + threadIdx.x; q < clen; q += kPT) dst[q] = src[q];
   };
-  const int64_t first = blockIdx.x / csize;
-  if (first < n) stage(first, 0);
+  if (blockIdx.x < items) stage(blockIdx.x, 0);
   uint32_t parity = 0;  // bit b: phase parity to wait for on buffer b
   // the first wait that gave up: its copy may still be in flight (none starts
   // after it, the abort flag being set by then)
   int pend_b = -1;
   uint32_t pend_p = 0;
-  int k = 0;
-  for (int64_t row = first; row < n; row += ncl, ++k) {
-    const int b = k & 1;
+  int it = 0;
+  for (int64_t item = blockIdx.x; item < items; item += gridDim.x, ++it) {
+    const int b = it & 1;
+    // buffer b ^ 1 held the previous item, which every thread is done with
+    if (item + gridDim.x < items) stage(item + gridDim.x, b ^ 1);
     if (!ptx::warp_wait(ptx::smem_u32(&bars[b]), (parity >> b) & 1u, &abort_flag, status) &&
         pend_b < 0) {
       pend_b = b;
       pend_p = (parity >> b) & 1u;
     }
     parity ^= 1u << b;
-    // every CTA's slice of this row has landed, and every CTA is done with
-    // the row before it, whose buffer the next copy reuses
-    cluster_sync();
-    if (row + ncl < n) stage(row + ncl, b ^ 1);
-    const uint32_t base = buf_sa + (uint32_t)b * buf_bytes;
+    __syncthreads();  // the plain-loaded columns too
+    const int64_t row = item / nsl;
+    const int r = (int)(item % nsl);
+    const TI* zs = reinterpret_cast<const TI*>(smem_raw + (size_t)b * buf_bytes);
+    const TI* zrow = zt + row * vt;
     TO* o = out + row * vs;
-    for (int64_t g0 = i_lo + (int64_t)threadIdx.x * kIds; g0 < i_hi; g0 += (int64_t)kPT * kIds * kGroups) {
-      // the entries of up to kGroups groups of 8 ids, loaded together
-      int32_t oc[kGroups][kIds];
+    const int32_t k0 = slice_off[r], k1 = slice_off[r + 1];
+    // four list entries per thread in flight; a warp's stores at each step
+    // go to 32 consecutive entries, i.e. one short ascending run of ids
+    for (int32_t k = k0 + (int32_t)threadIdx.x; k < k1; k += kPT * 4) {
+      int32_t id[4], v[4];
 #pragma unroll
-      for (int j = 0; j < kGroups; ++j) {
-        const int64_t i0 = g0 + (int64_t)j * kPT * kIds;
-        if (i0 + kIds <= i_hi) {  // one is 256-byte aligned, i0 - i_lo a multiple of 8
-          const int4 a = reinterpret_cast<const int4*>(one + i0)[0];
-          const int4 c = reinterpret_cast<const int4*>(one + i0)[1];
-          oc[j][0] = a.x; oc[j][1] = a.y; oc[j][2] = a.z; oc[j][3] = a.w;
-          oc[j][4] = c.x; oc[j][5] = c.y; oc[j][6] = c.z; oc[j][7] = c.w;
-        } else {
-#pragma unroll
-          for (int q = 0; q < kIds; ++q) oc[j][q] = i0 + q < i_hi ? one[i0 + q] : -1;
-        }
+      for (int u = 0; u < 4; ++u) {
+        const int32_t kk = k + u * kPT;
+        id[u] = kk < k1 ? list_id[kk] : -1;
+        v[u] = kk < k1 ? list_val[kk] : -1;
       }
-      // all single-token gathers of the groups first (each entry's
-      // register then holds its value), then the rest; bit 8j+q of `multi` /
-      // `none` marks an id with several / no teacher tokens
-      float v[kGroups][kIds];
-      uint32_t multi = 0, none = 0;
 #pragma unroll
-      for (int j = 0; j < kGroups; ++j)
-#pragma unroll
-        for (int q = 0; q < kIds; ++q) {
-          const int32_t c = oc[j][q];
-          multi |= (c == -2 ? 1u : 0u) << (8 * j + q);
-          none |= (c == -1 ? 1u : 0u) << (8 * j + q);
-          v[j][q] = c >= 0 ? dsmem_get<TI>(base, (uint32_t)c >> kEncBits,
-                                           (uint32_t)c & ((1u << kEncBits) - 1))
-                           : 0.f;
-        }
-#pragma unroll
-      for (int j = 0; j < kGroups; ++j) {
-        const int64_t i0 = g0 + (int64_t)j * kPT * kIds;
-        if (i0 >= i_hi) break;
-        float r[kIds];
-#pragma unroll
-        for (int q = 0; q < kIds; ++q) {
-          if (!((multi | none) >> (8 * j + q) & 1u)) {
-            r[q] = v[j][q] * inv_t;
-          } else if (multi >> (8 * j + q) & 1u) {  // several teacher tokens: fold in column order
-            const int32_t e = off[i0 + q + 1];
-            float acc = -INFINITY;
+      for (int u = 0; u < 4; ++u) {
+        if (id[u] < 0) continue;
+        float r_;
+        if (v[u] >= 0) {
+          r_ = ld<TI>(zs + v[u]) * inv_t;
+        } else if (v[u] == -2) {
+          const int32_t e = off[id[u] + 1];
+          r_ = -INFINITY;
 #pragma unroll 1
-            for (int32_t t = off[i0 + q]; t < e; ++t)
-              acc = logaddexp(acc, dsmem_col<TI>(base, (uint32_t)cols[t], (uint32_t)sc) * inv_t);
-            r[q] = acc;
-          } else {
-            r[q] = -INFINITY;
-          }
-          if (r[q] == -INFINITY) r[q] = lowest<TO>();
-        }
-        if (i0 + kIds <= i_hi && (reinterpret_cast<uintptr_t>(o + i0) & 15) == 0) {
-          store_vec(o + i0, r);
+          for (int32_t t = off[id[u]]; t < e; ++t)
+            r_ = logaddexp(r_, ld<TI>(zrow + cols[t]) * inv_t);
         } else {
-#pragma unroll
-          for (int q = 0; q < kIds; ++q)
-            if (i0 + q < i_hi) st<TO>(o + i0 + q, r[q]);
+          r_ = -INFINITY;
         }
+        st<TO>(o + id[u], r_ > -INFINITY ? r_ : lowest<TO>());
       }
     }
+    __syncthreads();  // buffer b is read; the item after next overwrites it
   }
-  // no CTA leaves while another may still read its shared memory, nor with
-  // a copy of its own still in flight (bounded again, whatever the abort flag)
-  cluster_sync();
   if (pend_b >= 0 && threadIdx.x < 32)
     ptx::warp_wait(ptx::smem_u32(&bars[pend_b]), pend_p, &abort_flag, status, false);
 }
 
-size_t align256(size_t x) { return (x + 255) / 256 * 256; }
-
-// teacher columns per staged slice (a multiple of 8, so every slice of an
-// aligned row starts 16-byte aligned)
-template <typename TI>
-int64_t slice_cols() {
-  return kSlice / (int64_t)sizeof(TI) / 8 * 8;
+__device__ __forceinline__ uint32_t cl_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cl_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cl_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cl_map(uint32_t a, uint32_t rank) {
+  asm("mapa.shared::cluster.u32 %0, %0, %1;" : "+r"(a) : "r"(rank));
+  return a;
 }
 
-// smallest cluster (1, 2, 4, 8 CTAs) whose per-CTA share of a teacher row,
-// sc columns (a multiple of 8), fits one staging buffer; 0 when eight CTAs
-// cannot hold the row (the sliced kernel takes it then)
-int cluster_for(int64_t vt, int64_t elem, int64_t* sc) {
-  for (int c = 1; c <= 8; c *= 2) {
-    const int64_t cols = ((vt + c - 1) / c + 7) / 8 * 8;
-    if (cols * elem <= kBuf) {
-      if (sc) *sc = cols;
-      return c;
-    }
+// Exchange path.  A cluster of C CTAs takes one token row at a time.  CTA r
+// stages its slice of the teacher row (one bulk copy; the next row's copy
+// starts as soon as the gather below has read the slice), gathers the values
+// its map edges need into a send buffer ordered by destination CTA -- random
+// reads of local shared memory only -- and ships segment (r, q) to CTA q with
+// one shared::cta -> shared::cluster bulk copy completing on q's receive
+// barrier.  CTA q then writes student ids [q*so, q*so + so) of the output row
+// from its receive buffer with 16-byte stores.  One cluster barrier per row:
+// after it every CTA has received (so every send buffer is free again) and
+// read its receive buffer (so it may be refilled); the receive barrier of the
+// next row is armed before it, so no copy can arrive early.
+template <typename TI, typename TO>
+__global__ void __launch_bounds__(kPT, 1)
+    k_project_exchange(const TI* __restrict__ zt, int64_t n, int64_t vt, int64_t vs,
+                       float inv_t, const int32_t* __restrict__ off,
+                       const int32_t* __restrict__ epos, const int32_t* __restrict__ code,
+                       const int32_t* __restrict__ send_src, const XLayout* __restrict__ X,
+                       int64_t sc, int64_t so, int64_t send_cap, TO* __restrict__ out,
+                       uint32_t* status) {
+  if (!X->fits) return;  // the slice path runs instead
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[2];  // 0: the staged slice, 1: the receive buffer
+  __shared__ int abort_flag;
+  const uint32_t r = cl_rank(), C = cl_size();
+  const int64_t ncl = gridDim.x / C;
+  TI* const slice = reinterpret_cast<TI*>(smem_raw);
+  TI* const send = slice + sc;        // sc and send_cap are multiples of 8
+  TI* const recv = send + send_cap;
+  const int64_t c0 = (int64_t)r * sc;
+  const int64_t clen = vt - c0 < sc ? (vt - c0 > 0 ? vt - c0 : 0) : sc;
+  const int64_t i_lo = (int64_t)r * so, i_hi = i_lo + so < vs ? i_lo + so : vs;
+  const int32_t nsend = X->sendtot[r];
+  const int32_t* gl = send_src + X->sendbase[r];
+  const uint32_t rx_bytes = (uint32_t)X->recvtot[r] * (uint32_t)sizeof(TI);
+  const uint32_t bar_s = ptx::smem_u32(&bars[0]), bar_r = ptx::smem_u32(&bars[1]);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar_s, 1);
+    ptx::mbar_init(bar_r, 1);
+    ptx::fence_mbar_init();
+    abort_flag = 0;
   }
-  return 0;
+  __syncthreads();
+  auto stage = [&](int64_t row) {
+    const TI* src = zt + row * vt + c0;
+    const bool al = ((reinterpret_cast<uintptr_t>(src) | ptx::smem_u32(slice)) & 15) == 0;
+    const int64_t nb = al ? clen * (int64_t)sizeof(TI) / 16 * 16 : 0;
+    if (threadIdx.x == 0 && !*reinterpret_cast<volatile int*>(&abort_flag)) {
+      ptx::mbar_expect_tx(bar_s, (uint32_t)nb);
+      if (nb > 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        ptx::bulk_load(ptx::smem_u32(slice), src, (uint32_t)nb, bar_s);
+      }
+    }
+    for (int64_t q = nb / (int64_t)sizeof(TI) + threadIdx.x; q < clen; q += kPT) slice[q] = src[q];
+  };
+  const int64_t first = blockIdx.x / C;
+  if (first < n) {
+    stage(first);
+    if (threadIdx.x == 0) ptx::mbar_expect_tx(bar_r, rx_bytes);
+  }
+  cl_sync();  // every receive barrier is armed before any copy is sent
+  uint32_t ps = 0, pr = 0;
+  int pend = 0;  // bit 0 / 1: a wait on the slice / receive barrier gave up
+  uint32_t pend_ps = 0, pend_pr = 0;
+  for (int64_t row = first; row < n; row += ncl) {
+    if (!ptx::warp_wait(bar_s, ps, &abort_flag, status) && !(pend & 1)) {
+      pend |= 1;
+      pend_ps = ps;
+    }
+    ps ^= 1u;
+    __syncthreads();  // the plain-loaded columns too
+    for (int32_t t = threadIdx.x; t < nsend; t += kPT) send[t] = slice[gl[t]];
+    __syncthreads();  // send is complete; the slice is free for the next row
+    if (row + ncl < n) stage(row + ncl);
+    if (threadIdx.x == 0 && !*reinterpret_cast<volatile int*>(&abort_flag)) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      for (uint32_t q = 0; q < C; ++q) {
+        const int k = (int)(r * C + q);
+        const int32_t len = pad8(X->cnt[k]);
+        if (len == 0) continue;
+        const uint32_t dst = cl_map(ptx::smem_u32(recv + X->recvoff[k]), q);
+        const uint32_t mb = cl_map(bar_r, q);
+        asm volatile(
+            "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], "
+            "%2, [%3];" ::"r"(dst),
+            "r"(ptx::smem_u32(send + X->sendoff[k])), "r"((uint32_t)len * (uint32_t)sizeof(TI)),
+            "r"(mb)
+            : "memory");
+      }
+    }
+    if (!ptx::warp_wait(bar_r, pr, &abort_flag, status) && !(pend & 2)) {
+      pend |= 2;
+      pend_pr = pr;
+    }
+    pr ^= 1u;
+    // the output row, 8 ids per thread step
+    TO* o = out + row * vs;
+    for (int64_t j0 = i_lo + (int64_t)threadIdx.x * 8; j0 < i_hi; j0 += (int64_t)kPT * 8) {
+      int32_t c[8];
+      if (j0 + 8 <= i_hi) {  // code is 256-byte aligned, j0 a multiple of 8
+        const int4 a = reinterpret_cast<const int4*>(code + j0)[0];
+        const int4 b = reinterpret_cast<const int4*>(code + j0)[1];
+        c[0] = a.x; c[1] = a.y; c[2] = a.z; c[3] = a.w;
+        c[4] = b.x; c[5] = b.y; c[6] = b.z; c[7] = b.w;
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) c[q] = j0 + q < i_hi ? code[j0 + q] : -1;
+      }
+      float v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float x;
+        if (c[q] >= 0) {
+          x = ld<TI>(recv + c[q]) * inv_t;
+        } else if (c[q] == -2) {
+          const int32_t e = off[j0 + q + 1];
+          x = -INFINITY;
+#pragma unroll 1
+          for (int32_t t = off[j0 + q]; t < e; ++t) x = logaddexp(x, ld<TI>(recv + epos[t]) * inv_t);
+        } else {
+          x = -INFINITY;
+        }
+        v[q] = x > -INFINITY ? x : lowest<TO>();
+      }
+      if (j0 + 8 <= i_hi && (reinterpret_cast<uintptr_t>(o + j0) & 15) == 0) {
+        store_vec(o + j0, v);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (j0 + q < i_hi) st<TO>(o + j0 + q, v[q]);
+      }
+    }
+    if (threadIdx.x == 0 && row + ncl < n) ptx::mbar_expect_tx(bar_r, rx_bytes);
+    cl_sync();
+  }
+  // copies still in flight after a wait that gave up (bounded again)
+  if (threadIdx.x < 32) {
+    if (pend & 1) ptx::warp_wait(bar_s, pend_ps, &abort_flag, status, false);
+    if (pend & 2) ptx::warp_wait(bar_r, pend_pr, &abort_flag, status, false);
+  }
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// slices of a teacher row of vt elements: the fewest whose columns (sc, a
+// multiple of 8) fit kSliceMax bytes; 0 when more than kMaxSlices are needed
+int slices_for(int64_t vt, int64_t elem, int64_t* sc) {
+  int64_t nsl = (vt * elem + kSliceMax - 1) / kSliceMax;
+  if (nsl < 1) nsl = 1;
+  const int64_t cols = ((vt + nsl - 1) / nsl + 7) / 8 * 8;
+  nsl = (vt + cols - 1) / cols;
+  if (nsl > kMaxSlices) return 0;
+  *sc = cols;
+  return (int)nsl;
 }
 
 struct ProjLayout {
-  size_t cnt, off, cols, one, scratch, bytes;
+  size_t cnt, off, cols, one, list_id, list_val, slice_cnt, slice_off, eid, epos, code, send_src,
+      xl, bytes;
 };
-// inverse map, plus one fp32 scratch row per CTA when the sliced kernel may
-// take the row in more than one slice (sized for fp32 logits, the larger
-// element, which needs a cluster soonest)
-ProjLayout proj_layout(int64_t vt, int64_t vs, int ctas) {
+ProjLayout proj_layout(int64_t vt, int64_t vs) {
   ProjLayout L;
   L.cnt = 0;
   L.off = align256(L.cnt + (size_t)vs * 4);
   L.cols = align256(L.off + (size_t)(vs + 1) * 4);
   L.one = align256(L.cols + (size_t)vt * 4);
-  L.scratch = align256(L.one + (size_t)vs * 4);
-  const bool multi = cluster_for(vt, 4, nullptr) == 0 && vt > slice_cols<float>();
-  L.bytes = align256(L.scratch + (multi ? (size_t)ctas * (size_t)scratch_pitch(vs) * 4 : 0));
+  L.list_id = align256(L.one + (size_t)vs * 4);
+  L.list_val = align256(L.list_id + (size_t)vs * 4);
+  L.slice_cnt = align256(L.list_val + (size_t)vs * 4);
+  L.slice_off = align256(L.slice_cnt + (size_t)kMaxSlices * 4);
+  L.eid = align256(L.slice_off + (size_t)(kMaxSlices + 1) * 4);
+  L.epos = align256(L.eid + (size_t)vt * 4);
+  L.code = align256(L.epos + (size_t)vt * 4);
+  L.send_src = align256(L.code + (size_t)vs * 4);
+  L.xl = align256(L.send_src + ((size_t)vt + 8 * kMaxC * kMaxC) * 4);
+  L.bytes = align256(L.xl + sizeof(XLayout));
   return L;
 }
 
-int proj_ctas() { return tc_num_sms() > 0 ? tc_num_sms() : 1; }
-
-// Launch shape of the cluster kernel: cluster size, columns and student ids
-// per CTA, staging bytes, co-resident clusters.
-struct ClusterPlan {
-  int c = 0;
-  int64_t sc = 0, so = 0;
+// Exchange plan: C = the fewest CTAs whose slices of a teacher row fit
+// kXSlice bytes (at most kMaxC), the columns sc and student ids so per CTA,
+// and the send / receive capacities that fill the rest of kXSmem.  A CTA sends
+// at most its sc columns (+ padding); what it receives depends on the map,
+// so the device checks it (XLayout::fits) and the slice path runs otherwise.
+constexpr int64_t kXSlice = 76 * 1024;
+constexpr int64_t kXSmem = 220 * 1024;
+struct XPlan {
+  int C = 0;
+  int64_t sc = 0, so = 0, send_cap = 0, recv_cap = 0;
   size_t smem = 0;
   int max_clusters = 0;
 };
 
 template <typename TI, typename TO>
-cudaLaunchConfig_t cluster_config(const ClusterPlan& P, cudaLaunchAttribute* attr,
-                                  cudaStream_t s) {
-  cudaLaunchConfig_t cfg;
-  memset(&cfg, 0, sizeof(cfg));
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)P.c;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kPT);
-  cfg.dynamicSmemBytes = P.smem;
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cfg;
-}
-
-// true when a cluster of at most 8 CTAs can hold a teacher row and such
-// clusters can be resident (the cluster kernel takes the rows); false leaves
-// them to the sliced kernel.  *err is set on a CUDA error.
-template <typename TI, typename TO>
-bool cluster_plan(int64_t vt, int64_t vs, ClusterPlan* P, bool* err) {
-  *err = false;
-  P->c = cluster_for(vt, (int64_t)sizeof(TI), &P->sc);
-  if (P->c == 0) return false;
-  P->so = ((vs + P->c - 1) / P->c + 7) / 8 * 8;
-  P->smem = 2 * (size_t)P->sc * sizeof(TI);
-  auto kern = k_project_cluster<TI, TO>;
+bool x_plan(int64_t vt, int64_t vs, XPlan* P) {
+  const int64_t elem = (int64_t)sizeof(TI);
+  int64_t C = (vt * elem + kXSlice - 1) / kXSlice;
+  if (C < 1) C = 1;
+  if (C > kMaxC) return false;
+  P->sc = ((vt + C - 1) / C + 7) / 8 * 8;
+  C = (vt + P->sc - 1) / P->sc;
+  P->C = (int)C;
+  P->so = ((vs + C - 1) / C + 7) / 8 * 8;
+  P->send_cap = P->sc + 8 * C;
+  P->recv_cap = (kXSmem / elem - P->sc - P->send_cap) / 8 * 8;
+  if (P->recv_cap < 8) return false;
+  P->smem = (size_t)(P->sc + P->send_cap + P->recv_cap) * (size_t)elem;
+  auto kern = k_project_exchange<TI, TO>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P->smem) !=
       cudaSuccess) {
-    *err = true;
+    (void)cudaGetLastError();
     return false;
   }
   // co-resident clusters of this shape (cached per cluster size and buffer)
   static int cached_c = 0, cached_max = 0;
   static size_t cached_smem = 0;
-  if (cached_c != P->c || cached_smem != P->smem) {
+  if (cached_c != P->C || cached_smem != P->smem) {
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = cluster_config<TI, TO>(*P, attr, nullptr);
-    const int nsm = proj_ctas();
-    cfg.gridDim = dim3((unsigned)(P->c * (nsm / P->c > 0 ? nsm / P->c : 1)));
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)P->C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    const int nsm = tc_num_sms() > 0 ? tc_num_sms() : 1;
+    cfg.gridDim = dim3((unsigned)(P->C * std::max(1, nsm / P->C)));
+    cfg.blockDim = dim3(kPT);
+    cfg.dynamicSmemBytes = P->smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     int m = 0;
     if (cudaOccupancyMaxActiveClusters(&m, kern, &cfg) != cudaSuccess) {
       (void)cudaGetLastError();
       m = 0;
     }
-    cached_c = P->c;
+    cached_c = P->C;
     cached_smem = P->smem;
     cached_max = m;
   }
@@ -589,58 +798,71 @@ bool cluster_plan(int64_t vt, int64_t vs, ClusterPlan* P, bool* err) {
 }
 
 template <typename TI, typename TO>
-int launch_cluster(const ClusterPlan& P, const void* zt, int64_t n, int64_t vt, int64_t vs,
-                   float inv_t, const int32_t* off, const int32_t* cols, const int32_t* one,
-                   void* out, uint32_t* status, cudaStream_t s) {
+int launch_exchange(const XPlan& P, const void* zt, int64_t n, int64_t vt, int64_t vs,
+                    float inv_t, const int32_t* off, const int32_t* epos, const int32_t* code,
+                    const int32_t* send_src, const XLayout* X, void* out, uint32_t* status,
+                    cudaStream_t s) {
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = cluster_config<TI, TO>(P, attr, s);
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)P.C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
   const int64_t clusters = n < P.max_clusters ? n : P.max_clusters;
-  cfg.gridDim = dim3((unsigned)(P.c * clusters));
+  cfg.gridDim = dim3((unsigned)(P.C * clusters));
+  cfg.blockDim = dim3(kPT);
+  cfg.dynamicSmemBytes = P.smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   note_launch();
-  return cudaLaunchKernelEx(&cfg, k_project_cluster<TI, TO>, static_cast<const TI*>(zt), n, vt,
-                            vs, inv_t, off, cols, one, static_cast<TO*>(out), P.sc, P.so,
-                            status) != cudaSuccess;
+  return cudaLaunchKernelEx(&cfg, k_project_exchange<TI, TO>, static_cast<const TI*>(zt), n, vt,
+                            vs, inv_t, off, epos, code, send_src, X, P.sc, P.so, P.send_cap,
+                            static_cast<TO*>(out), status) != cudaSuccess;
 }
 
 template <typename TI, typename TO>
-int launch_sliced(const void* zt, int64_t n, int64_t vt, int64_t vs, float inv_t,
-                  const int32_t* off, const int32_t* cols, const int32_t* one, void* out,
-                  float* scratch, int grid, cudaStream_t s) {
-  const int64_t span = slice_cols<TI>();
-  const size_t smem = (size_t)(vt < span ? vt : span) * sizeof(TI);
-  auto kern = k_project<TI, TO>;
+int launch_project(const void* zt, int64_t n, int64_t vt, int64_t vs, float inv_t,
+                   const int32_t* off, const int32_t* cols, const int32_t* list_id,
+                   const int32_t* list_val, const int32_t* slice_off, int64_t sc, int nsl,
+                   void* out, uint32_t* status, const XLayout* X, cudaStream_t s) {
+  const size_t smem = 2 * (size_t)sc * sizeof(TI);
+  auto kern = k_project_slices<TI, TO>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return 1;
+  const int nsm = tc_num_sms() > 0 ? tc_num_sms() : 1;
+  const int grid = (int)std::min<int64_t>(n * nsl, (int64_t)nsm);
   note_launch();
-  kern<<<grid, kPT, smem, s>>>(static_cast<const TI*>(zt), n, vt, vs, inv_t, off, cols, one,
-                               static_cast<TO*>(out), vt > span ? scratch : nullptr, span);
-  return 0;
+  kern<<<grid, kPT, smem, s>>>(static_cast<const TI*>(zt), n, vt, vs, inv_t, off, cols, list_id,
+                               list_val, slice_off, sc, nsl, static_cast<TO*>(out), status, X);
+  return cudaGetLastError() != cudaSuccess;
 }
 
-// Map the build-time plan and the projection itself onto one dtype pair.
-struct ProjArgs {
+// the launches of one call, per dtype pair
+struct ProjRun {
   const void* zt;
   int64_t n, vt, vs;
   float inv_t;
-  const int32_t *off, *cols, *one;
+  const int32_t *off, *cols, *list_id, *list_val, *slice_off, *epos, *code, *send_src;
+  const XLayout* X;  // non-null when the exchange path may run
+  int64_t sc;        // slice path: columns per slice
+  int nsl;
   void* out;
-  float* scratch;
   uint32_t* status;
   cudaStream_t s;
 };
 template <typename TI, typename TO>
 struct ProjOps {
-  static bool plan(const ProjArgs& A, ClusterPlan* P, bool* err) {
-    return cluster_plan<TI, TO>(A.vt, A.vs, P, err);
-  }
-  static int run(const ProjArgs& A, const ClusterPlan* P) {
-    if (P)
-      return launch_cluster<TI, TO>(*P, A.zt, A.n, A.vt, A.vs, A.inv_t, A.off, A.cols, A.one,
-                                    A.out, A.status, A.s);
-    const int grid = (int)std::min<int64_t>(A.n, (int64_t)proj_ctas());
-    return launch_sliced<TI, TO>(A.zt, A.n, A.vt, A.vs, A.inv_t, A.off, A.cols, A.one, A.out,
-                                 A.scratch, grid, A.s);
+  static bool plan(int64_t vt, int64_t vs, XPlan* P) { return x_plan<TI, TO>(vt, vs, P); }
+  static int run(const XPlan* xp, const ProjRun& a) {
+    if (xp && launch_exchange<TI, TO>(*xp, a.zt, a.n, a.vt, a.vs, a.inv_t, a.off, a.epos, a.code,
+                                      a.send_src, a.X, a.out, a.status, a.s))
+      return 1;
+    return launch_project<TI, TO>(a.zt, a.n, a.vt, a.vs, a.inv_t, a.off, a.cols, a.list_id,
+                                  a.list_val, a.slice_off, a.sc, a.nsl, a.out, a.status, a.X,
+                                  a.s);
   }
 };
 
@@ -655,7 +877,7 @@ kd_status kd_project_workspace_size(int64_t v_teacher, int64_t v_student, size_t
   if (!bytes || v_teacher < 1 || v_student < 1 || v_teacher > ((int64_t)1 << 30) ||
       v_student > ((int64_t)1 << 30))
     return KD_ERR_INVALID_ARG;
-  *bytes = proj_layout(v_teacher, v_student, proj_ctas()).bytes;
+  *bytes = proj_layout(v_teacher, v_student).bytes;
   return KD_OK;
 }
 
@@ -671,25 +893,31 @@ kd_status kd_project_teacher_logits(const int32_t* token_map, int64_t v_teacher,
       (out_dtype != KD_BF16 && out_dtype != KD_FP32) ||
       !(temperature > 0.f && temperature < FLT_MAX))
     return KD_ERR_INVALID_ARG;
+  int64_t sc = 0;
+  const int nsl = slices_for(v_teacher, in_dtype == KD_BF16 ? 2 : 4, &sc);
+  if (nsl == 0) return KD_ERR_UNSUPPORTED;  // a teacher row above 96 MiB
   if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
     return KD_ERR_WORKSPACE;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || !kd_device_supported(dev)) return KD_ERR_NO_DEVICE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const ProjLayout L = proj_layout(v_teacher, v_student, proj_ctas());
+  const ProjLayout L = proj_layout(v_teacher, v_student);
   char* ws = static_cast<char*>(workspace);
   int32_t* cnt = reinterpret_cast<int32_t*>(ws + L.cnt);
   int32_t* off = reinterpret_cast<int32_t*>(ws + L.off);
   int32_t* cols = reinterpret_cast<int32_t*>(ws + L.cols);
   int32_t* one = reinterpret_cast<int32_t*>(ws + L.one);
-  float* scratch = reinterpret_cast<float*>(ws + L.scratch);
-  const int nsm = tc_num_sms() > 0 ? tc_num_sms() : 1;
-  const int gmap = (int)std::min<int64_t>((v_teacher + kT - 1) / kT, (int64_t)nsm * 8);
-  const int gid = (int)std::min<int64_t>((v_student + kT - 1) / kT, (int64_t)nsm * 8);
-  ProjArgs A{logits_t, n_tokens, v_teacher, v_student, 1.f / temperature, off, cols, one,
-             out, scratch, dev_status, s};
-  bool (*plan)(const ProjArgs&, ClusterPlan*, bool*);
-  int (*run)(const ProjArgs&, const ClusterPlan*);
+  int32_t* list_id = reinterpret_cast<int32_t*>(ws + L.list_id);
+  int32_t* list_val = reinterpret_cast<int32_t*>(ws + L.list_val);
+  int32_t* slice_cnt = reinterpret_cast<int32_t*>(ws + L.slice_cnt);
+  int32_t* slice_off = reinterpret_cast<int32_t*>(ws + L.slice_off);
+  int32_t* eid = reinterpret_cast<int32_t*>(ws + L.eid);
+  int32_t* epos = reinterpret_cast<int32_t*>(ws + L.epos);
+  int32_t* code = reinterpret_cast<int32_t*>(ws + L.code);
+  int32_t* send_src = reinterpret_cast<int32_t*>(ws + L.send_src);
+  XLayout* X = reinterpret_cast<XLayout*>(ws + L.xl);
+  bool (*plan)(int64_t, int64_t, XPlan*);
+  int (*run)(const XPlan*, const ProjRun&);
   if (in_dtype == KD_BF16) {
     plan = out_dtype == KD_BF16 ? ProjOps<__nv_bfloat16, __nv_bfloat16>::plan
                                 : ProjOps<__nv_bfloat16, float>::plan;
@@ -699,11 +927,14 @@ kd_status kd_project_teacher_logits(const int32_t* token_map, int64_t v_teacher,
     plan = out_dtype == KD_BF16 ? ProjOps<float, __nv_bfloat16>::plan : ProjOps<float, float>::plan;
     run = out_dtype == KD_BF16 ? ProjOps<float, __nv_bfloat16>::run : ProjOps<float, float>::run;
   }
-  ClusterPlan P;
-  bool err = false;
-  const bool clustered = n_tokens > 0 && plan(A, &P, &err);
-  if (err) return KD_ERR_CUDA;
-  if (cudaMemsetAsync(cnt, 0, (size_t)v_student * 4, s) != cudaSuccess) return KD_ERR_CUDA;
+  XPlan xp;
+  const bool xok = plan(v_teacher, v_student, &xp);
+  const int nsm = tc_num_sms() > 0 ? tc_num_sms() : 1;
+  const int gmap = (int)std::min<int64_t>((v_teacher + kT - 1) / kT, (int64_t)nsm * 8);
+  const int gid = (int)std::min<int64_t>((v_student + kT - 1) / kT, (int64_t)nsm * 8);
+  if (cudaMemsetAsync(cnt, 0, (size_t)v_student * 4, s) != cudaSuccess ||
+      cudaMemsetAsync(slice_cnt, 0, (size_t)nsl * 4, s) != cudaSuccess)
+    return KD_ERR_CUDA;
   note_launch();
   k_map_count<<<gmap, kT, 0, s>>>(token_map, v_teacher, v_student, cnt, dev_status);
   note_launch();
@@ -714,8 +945,34 @@ kd_status kd_project_teacher_logits(const int32_t* token_map, int64_t v_teacher,
   note_launch();
   k_map_sort<<<gid, kT, 0, s>>>(off, v_student, cols);
   note_launch();
-  k_map_single<<<gid, kT, 0, s>>>(off, cols, v_student, clustered ? (int32_t)P.sc : 0, one);
-  if (n_tokens > 0 && run(A, clustered ? &P : nullptr)) return KD_ERR_CUDA;
+  k_map_single<<<gid, kT, 0, s>>>(off, cols, v_student, one, eid);
+  if (xok) {  // the exchange lists; X->fits then picks the path on the device
+    if (cudaMemsetAsync(X, 0, sizeof(XLayout), s) != cudaSuccess ||
+        cudaMemsetAsync(send_src, 0, ((size_t)v_teacher + 8 * kMaxC * kMaxC) * 4, s) !=
+            cudaSuccess)
+      return KD_ERR_CUDA;
+    note_launch();
+    k_edge_count<<<gmap, kT, 0, s>>>(off, cols, eid, v_student, (int32_t)xp.sc, (int32_t)xp.so,
+                                      xp.C, X);
+    note_launch();
+    k_exchange_layout<<<1, 32, 0, s>>>(X, xp.C, (int32_t)xp.send_cap, (int32_t)xp.recv_cap);
+    note_launch();
+    k_edge_partition<<<xp.C * xp.C, 1024, 0, s>>>(off, cols, eid, v_student, (int32_t)xp.sc,
+                                                  (int32_t)xp.so, xp.C, X, send_src, epos);
+    note_launch();
+    k_exchange_codes<<<gid, kT, 0, s>>>(off, epos, v_student, code);
+  }
+  const XLayout* Xp = xok ? X : nullptr;
+  note_launch();
+  k_slice_count<<<gid, kT, 0, s>>>(one, off, cols, v_student, (int32_t)sc, nsl, slice_cnt, Xp);
+  note_launch();
+  k_slice_partition<<<nsl, 1024, 0, s>>>(one, off, cols, v_student, (int32_t)sc, nsl, slice_cnt,
+                                         slice_off, list_id, list_val, Xp);
+  if (n_tokens > 0) {
+    ProjRun a{logits_t, n_tokens, v_teacher, v_student, 1.f / temperature, off, cols, list_id,
+              list_val, slice_off, epos, code, send_src, Xp, sc, nsl, out, dev_status, s};
+    if (run(xok ? &xp : nullptr, a)) return KD_ERR_CUDA;
+  }
   return cudaGetLastError() == cudaSuccess ? KD_OK : KD_ERR_CUDA;
 }
 

@@ -38,11 +38,11 @@ def _map(v_t, v_s, seed):
                                        (120000, 5000, 6), (220000, 3000, 3), (430000, 2000, 2),
                                        (30000, 20000, 400)])
 def test_projection_matches_oracle(din, dout, v_t, v_s, n):
-    """Teacher rows held by one CTA, by clusters of 2, 4 and 8 CTAs (60000 and
-    120000 ids in bf16 and fp32, 220000 in bf16), rows too long for a cluster
-    of 8 (220000 fp32, 430000 ids) on the sliced kernel, unaligned rows (513
-    ids), ragged student vocabularies, and many rows per cluster (400 rows, so
-    the double-buffered staging turns over)."""
+    """Teacher rows held by one CTA (1000 / 513 ids, the latter unaligned), by
+    clusters of 2 to 7 CTAs exchanging their gathered values (60000 to 220000
+    ids), rows too long for a cluster of 8 on the slice path (220000 fp32,
+    430000 ids: 12 to 18 slices), ragged student vocabularies, and 400 rows
+    per launch."""
     g = torch.Generator().manual_seed(v_t + v_s)
     z = (torch.randn(n, v_t, generator=g) * 3.0).to(DT[din])
     tmap = _map(v_t, v_s, 11)
@@ -111,3 +111,26 @@ def test_cross_vocab_distillation_end_to_end(dtype, variant):
     gz = bwd["d_logits_s"].cpu().double().numpy()
     assert rel_l2(gz, g_s) <= GRAD_TOL[dtype]
     assert np.all(gz[~valid] == 0) and np.all(kl[~valid] == 0)
+
+
+@pytest.mark.parametrize("dout", ["fp32", "bf16"])
+def test_projection_skewed_map(dout):
+    """Every teacher token maps into the first few student ids: one CTA's
+    receive buffer of the exchange path would overflow, so the device takes
+    the slice path instead; the result must not change."""
+    v_t, v_s, n = 100000, 70001, 3
+    rng = np.random.default_rng(21)
+    tmap = rng.integers(0, 4000, size=v_t).astype(np.int32)
+    tmap[rng.random(v_t) < 0.1] = -1
+    g = torch.Generator().manual_seed(5)
+    z = (torch.randn(n, v_t, generator=g) * 3.0).to(torch.bfloat16)
+    out = kd.project_teacher_logits(torch.from_numpy(tmap), z.cuda(), v_s, temperature=0.7,
+                                    out_dtype=DT[dout])
+    torch.cuda.synchronize()
+    got = out.cpu().double().numpy()
+    ref = O.project_teacher_logits(z, tmap, v_s, temperature=0.7)
+    empty = np.isneginf(ref)
+    assert np.all(got[empty] <= -1e38)
+    tol = 1e-6 if dout == "fp32" else 2.0 ** -8
+    err = np.abs(got[~empty] - ref[~empty]) / np.maximum(1.0, np.abs(ref[~empty]))
+    assert err.max() <= tol, err.max()
