@@ -318,15 +318,40 @@ __global__ void __launch_bounds__(1024) k_edge_partition(
   }
 }
 
-// code[i]: the receive-buffer slot of student id i's single edge, -1 for no
-// teacher token, -2 for several (their slots: epos[off[i] .. off[i+1]))
+// code[i]: the receive-buffer slot of student id i's single edge; -1 for no
+// teacher token; for k >= 2 tokens, -2 - (8 * off[i] + min(k, 9) - 2): their
+// slots are epos[off[i] .. off[i] + k), and the count field 7 means "read
+// off[i + 1]" (the exchange path holds at most 8 x 76 KiB of teacher row, so
+// 8 * off[i] stays far below 2^31)
 __global__ void k_exchange_codes(const int32_t* __restrict__ off,
                                  const int32_t* __restrict__ epos, int64_t vs,
                                  int32_t* __restrict__ code) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < vs;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const int32_t b = off[i], e = off[i + 1];
-    code[i] = e - b == 1 ? epos[b] : (e == b ? -1 : -2);
+    const int32_t b = off[i], k = off[i + 1] - b;
+    code[i] = k == 1 ? epos[b] : (k == 0 ? -1 : -2 - (8 * b + (k < 9 ? k : 9) - 2));
+  }
+}
+
+// Student ids with several teacher tokens, in ascending order: mflag[i] = 1
+// for them; after an exclusive scan (k_map_scan) mpre[i] is the number of
+// them below i, and mlist / mcode list each one with its code.
+__global__ void k_multi_flag(const int32_t* __restrict__ code, int64_t vs,
+                             int32_t* __restrict__ mflag) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < vs;
+       i += (int64_t)gridDim.x * blockDim.x)
+    mflag[i] = code[i] <= -2;
+}
+__global__ void k_multi_scatter(const int32_t* __restrict__ code,
+                                const int32_t* __restrict__ mpre, int64_t vs,
+                                int32_t* __restrict__ mlist, int32_t* __restrict__ mcode) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < vs;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t c = code[i];
+    if (c <= -2) {
+      mlist[mpre[i]] = (int32_t)i;
+      mcode[mpre[i]] = c;
+    }
   }
 }
 
@@ -570,9 +595,10 @@ __global__ void __launch_bounds__(kPT, 1)
     k_project_exchange(const TI* __restrict__ zt, int64_t n, int64_t vt, int64_t vs,
                        float inv_t, const int32_t* __restrict__ off,
                        const int32_t* __restrict__ epos, const int32_t* __restrict__ code,
-                       const int32_t* __restrict__ send_src, const XLayout* __restrict__ X,
-                       int64_t sc, int64_t so, int64_t send_cap, TO* __restrict__ out,
-                       uint32_t* status) {
+                       const int32_t* __restrict__ mpre, const int32_t* __restrict__ mlist,
+                       const int32_t* __restrict__ mcode, const int32_t* __restrict__ send_src,
+                       const XLayout* __restrict__ X, int64_t sc, int64_t so, int64_t send_cap,
+                       TO* __restrict__ out, uint32_t* status) {
   if (!X->fits) return;  // the slice path runs instead
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[2];  // 0: the staged slice, 1: the receive buffer
@@ -649,42 +675,58 @@ __global__ void __launch_bounds__(kPT, 1)
       pend_pr = pr;
     }
     pr ^= 1u;
-    // the output row, 8 ids per thread step
+    // the output row: 8 ids per thread step, the codes of up to four steps
+    // loaded together (one round trip to L2 per row for most threads)
     TO* o = out + row * vs;
-    for (int64_t j0 = i_lo + (int64_t)threadIdx.x * 8; j0 < i_hi; j0 += (int64_t)kPT * 8) {
-      int32_t c[8];
-      if (j0 + 8 <= i_hi) {  // code is 256-byte aligned, j0 a multiple of 8
-        const int4 a = reinterpret_cast<const int4*>(code + j0)[0];
-        const int4 b = reinterpret_cast<const int4*>(code + j0)[1];
-        c[0] = a.x; c[1] = a.y; c[2] = a.z; c[3] = a.w;
-        c[4] = b.x; c[5] = b.y; c[6] = b.z; c[7] = b.w;
-      } else {
+    for (int64_t g0 = i_lo + (int64_t)threadIdx.x * 8; g0 < i_hi; g0 += (int64_t)kPT * 32) {
+      int32_t c[4][8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) c[q] = j0 + q < i_hi ? code[j0 + q] : -1;
-      }
-      float v[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        float x;
-        if (c[q] >= 0) {
-          x = ld<TI>(recv + c[q]) * inv_t;
-        } else if (c[q] == -2) {
-          const int32_t e = off[j0 + q + 1];
-          x = -INFINITY;
-#pragma unroll 1
-          for (int32_t t = off[j0 + q]; t < e; ++t) x = logaddexp(x, ld<TI>(recv + epos[t]) * inv_t);
+      for (int u = 0; u < 4; ++u) {
+        const int64_t j0 = g0 + (int64_t)u * kPT * 8;
+        if (j0 + 8 <= i_hi) {  // code is 256-byte aligned, j0 a multiple of 8
+          const int4 a = reinterpret_cast<const int4*>(code + j0)[0];
+          const int4 b = reinterpret_cast<const int4*>(code + j0)[1];
+          c[u][0] = a.x; c[u][1] = a.y; c[u][2] = a.z; c[u][3] = a.w;
+          c[u][4] = b.x; c[u][5] = b.y; c[u][6] = b.z; c[u][7] = b.w;
         } else {
-          x = -INFINITY;
-        }
-        v[q] = x > -INFINITY ? x : lowest<TO>();
-      }
-      if (j0 + 8 <= i_hi && (reinterpret_cast<uintptr_t>(o + j0) & 15) == 0) {
-        store_vec(o + j0, v);
-      } else {
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (j0 + q < i_hi) st<TO>(o + j0 + q, v[q]);
+          for (int q = 0; q < 8; ++q) c[u][q] = j0 + q < i_hi ? code[j0 + q] : -1;
+        }
       }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t j0 = g0 + (int64_t)u * kPT * 8;
+        if (j0 >= i_hi) break;
+        float v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int32_t cq = c[u][q];
+          float x = -INFINITY;
+          // (ids with several teacher tokens are written by the pass below)
+          if (cq >= 0) x = ld<TI>(recv + cq) * inv_t;
+          v[q] = x > -INFINITY ? x : lowest<TO>();
+        }
+        if (j0 + 8 <= i_hi && (reinterpret_cast<uintptr_t>(o + j0) & 15) == 0) {
+          store_vec(o + j0, v);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            if (j0 + q < i_hi) st<TO>(o + j0 + q, v[q]);
+        }
+      }
+    }
+    // ids with several teacher tokens: their columns' values are folded in
+    // column order and overwrite the placeholders above (same CTA, after the
+    // barrier, so the later store wins; the sectors are already whole)
+    __syncthreads();
+    const int32_t m1 = mpre[i_hi];  // (i_hi <= vs; a CTA past the last id has i_lo > vs)
+    for (int32_t t = mpre[i_lo < i_hi ? i_lo : i_hi] + (int32_t)threadIdx.x; t < m1; t += kPT) {
+      const int32_t id = mlist[t], m = -2 - mcode[t], e0 = m >> 3;
+      const int32_t e1 = (m & 7) == 7 ? off[id + 1] : e0 + (m & 7) + 2;
+      float x = -INFINITY;
+#pragma unroll 1
+      for (int32_t e = e0; e < e1; ++e) x = logaddexp(x, ld<TI>(recv + epos[e]) * inv_t);
+      st<TO>(o + id, x > -INFINITY ? x : lowest<TO>());
     }
     if (threadIdx.x == 0 && row + ncl < n) ptx::mbar_expect_tx(bar_r, rx_bytes);
     cl_sync();
@@ -712,7 +754,7 @@ int slices_for(int64_t vt, int64_t elem, int64_t* sc) {
 
 struct ProjLayout {
   size_t cnt, off, cols, one, list_id, list_val, slice_cnt, slice_off, eid, epos, code, send_src,
-      xl, bytes;
+      mflag, mpre, mlist, mcode, xl, bytes;
 };
 ProjLayout proj_layout(int64_t vt, int64_t vs) {
   ProjLayout L;
@@ -728,7 +770,11 @@ ProjLayout proj_layout(int64_t vt, int64_t vs) {
   L.epos = align256(L.eid + (size_t)vt * 4);
   L.code = align256(L.epos + (size_t)vt * 4);
   L.send_src = align256(L.code + (size_t)vs * 4);
-  L.xl = align256(L.send_src + ((size_t)vt + 8 * kMaxC * kMaxC) * 4);
+  L.mflag = align256(L.send_src + ((size_t)vt + 8 * kMaxC * kMaxC) * 4);
+  L.mpre = align256(L.mflag + (size_t)vs * 4);
+  L.mlist = align256(L.mpre + (size_t)(vs + 1) * 4);
+  L.mcode = align256(L.mlist + (size_t)vs * 4);
+  L.xl = align256(L.mcode + (size_t)vs * 4);
   L.bytes = align256(L.xl + sizeof(XLayout));
   return L;
 }
@@ -800,6 +846,7 @@ bool x_plan(int64_t vt, int64_t vs, XPlan* P) {
 template <typename TI, typename TO>
 int launch_exchange(const XPlan& P, const void* zt, int64_t n, int64_t vt, int64_t vs,
                     float inv_t, const int32_t* off, const int32_t* epos, const int32_t* code,
+                    const int32_t* mpre, const int32_t* mlist, const int32_t* mcode,
                     const int32_t* send_src, const XLayout* X, void* out, uint32_t* status,
                     cudaStream_t s) {
   cudaLaunchConfig_t cfg;
@@ -818,8 +865,8 @@ int launch_exchange(const XPlan& P, const void* zt, int64_t n, int64_t vt, int64
   cfg.numAttrs = 1;
   note_launch();
   return cudaLaunchKernelEx(&cfg, k_project_exchange<TI, TO>, static_cast<const TI*>(zt), n, vt,
-                            vs, inv_t, off, epos, code, send_src, X, P.sc, P.so, P.send_cap,
-                            static_cast<TO*>(out), status) != cudaSuccess;
+                            vs, inv_t, off, epos, code, mpre, mlist, mcode, send_src, X, P.sc,
+                            P.so, P.send_cap, static_cast<TO*>(out), status) != cudaSuccess;
 }
 
 template <typename TI, typename TO>
@@ -845,7 +892,8 @@ struct ProjRun {
   const void* zt;
   int64_t n, vt, vs;
   float inv_t;
-  const int32_t *off, *cols, *list_id, *list_val, *slice_off, *epos, *code, *send_src;
+  const int32_t *off, *cols, *list_id, *list_val, *slice_off, *epos, *code, *mpre, *mlist, *mcode,
+      *send_src;
   const XLayout* X;  // non-null when the exchange path may run
   int64_t sc;        // slice path: columns per slice
   int nsl;
@@ -858,7 +906,8 @@ struct ProjOps {
   static bool plan(int64_t vt, int64_t vs, XPlan* P) { return x_plan<TI, TO>(vt, vs, P); }
   static int run(const XPlan* xp, const ProjRun& a) {
     if (xp && launch_exchange<TI, TO>(*xp, a.zt, a.n, a.vt, a.vs, a.inv_t, a.off, a.epos, a.code,
-                                      a.send_src, a.X, a.out, a.status, a.s))
+                                      a.mpre, a.mlist, a.mcode, a.send_src, a.X, a.out,
+                                      a.status, a.s))
       return 1;
     return launch_project<TI, TO>(a.zt, a.n, a.vt, a.vs, a.inv_t, a.off, a.cols, a.list_id,
                                   a.list_val, a.slice_off, a.sc, a.nsl, a.out, a.status, a.X,
@@ -915,6 +964,10 @@ kd_status kd_project_teacher_logits(const int32_t* token_map, int64_t v_teacher,
   int32_t* epos = reinterpret_cast<int32_t*>(ws + L.epos);
   int32_t* code = reinterpret_cast<int32_t*>(ws + L.code);
   int32_t* send_src = reinterpret_cast<int32_t*>(ws + L.send_src);
+  int32_t* mflag = reinterpret_cast<int32_t*>(ws + L.mflag);
+  int32_t* mpre = reinterpret_cast<int32_t*>(ws + L.mpre);
+  int32_t* mlist = reinterpret_cast<int32_t*>(ws + L.mlist);
+  int32_t* mcode = reinterpret_cast<int32_t*>(ws + L.mcode);
   XLayout* X = reinterpret_cast<XLayout*>(ws + L.xl);
   bool (*plan)(int64_t, int64_t, XPlan*);
   int (*run)(const XPlan*, const ProjRun&);
@@ -961,6 +1014,12 @@ kd_status kd_project_teacher_logits(const int32_t* token_map, int64_t v_teacher,
                                                   (int32_t)xp.so, xp.C, X, send_src, epos);
     note_launch();
     k_exchange_codes<<<gid, kT, 0, s>>>(off, epos, v_student, code);
+    note_launch();
+    k_multi_flag<<<gid, kT, 0, s>>>(code, v_student, mflag);
+    note_launch();
+    k_map_scan<<<1, 1024, 0, s>>>(mflag, v_student, mpre);
+    note_launch();
+    k_multi_scatter<<<gid, kT, 0, s>>>(code, mpre, v_student, mlist, mcode);
   }
   const XLayout* Xp = xok ? X : nullptr;
   note_launch();
@@ -970,7 +1029,8 @@ kd_status kd_project_teacher_logits(const int32_t* token_map, int64_t v_teacher,
                                          slice_off, list_id, list_val, Xp);
   if (n_tokens > 0) {
     ProjRun a{logits_t, n_tokens, v_teacher, v_student, 1.f / temperature, off, cols, list_id,
-              list_val, slice_off, epos, code, send_src, Xp, sc, nsl, out, dev_status, s};
+              list_val, slice_off, epos, code, mpre, mlist, mcode, send_src, Xp, sc, nsl, out,
+              dev_status, s};
     if (run(xok ? &xp : nullptr, a)) return KD_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? KD_OK : KD_ERR_CUDA;
