@@ -200,6 +200,7 @@ __device__ __forceinline__ void store_vec(__nv_bfloat16* o, const float* r) {
 // in segment (r, q).  Segments are padded to 8 elements so that every bulk
 // copy starts and ends on 16 bytes.
 constexpr int kMaxC = 8;
+constexpr int kXSteps = 4;  // 8-id steps per thread: a CTA's range is at most 32 Ki ids
 struct XLayout {
   int32_t cnt[kMaxC * kMaxC];      // edges of segment (r, q), at r * C + q
   int32_t sendoff[kMaxC * kMaxC];  // offset of segment (r, q) in CTA r's send buffer
@@ -641,6 +642,23 @@ __global__ void __launch_bounds__(kPT, 1)
     if (threadIdx.x == 0) ptx::mbar_expect_tx(bar_r, rx_bytes);
   }
   cl_sync();  // every receive barrier is armed before any copy is sent
+  // this thread's output ids are the same in every row: their codes, two
+  // 16-bit slots per register, are loaded once (ranges longer than
+  // kXSteps * 8 * kPT ids are not planned for this kernel)
+  uint32_t c16[kXSteps][4];
+#pragma unroll
+  for (int u = 0; u < kXSteps; ++u) {
+    const int64_t j0 = i_lo + ((int64_t)u * kPT + threadIdx.x) * 8;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) c16[u][q] = 0xffffffffu;
+    if (j0 >= i_hi) continue;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int32_t cq = j0 + q < i_hi ? code[j0 + q] : -1;
+      const uint32_t h = cq >= 0 ? (uint32_t)cq : (cq == -1 ? 0xffffu : 0xfffeu);
+      c16[u][q >> 1] = (c16[u][q >> 1] & ~(0xffffu << (16 * (q & 1)))) | (h << (16 * (q & 1)));
+    }
+  }
   uint32_t ps = 0, pr = 0;
   int pend = 0;  // bit 0 / 1: a wait on the slice / receive barrier gave up
   uint32_t pend_ps = 0, pend_pr = 0;
@@ -651,7 +669,21 @@ __global__ void __launch_bounds__(kPT, 1)
     }
     ps ^= 1u;
     __syncthreads();  // the plain-loaded columns too
-    for (int32_t t = threadIdx.x; t < nsend; t += kPT) send[t] = slice[gl[t]];
+    // 8 slots per thread step: nsend, the list start and send are multiples of 8
+    for (int32_t t0 = (int32_t)threadIdx.x * 8; t0 < nsend; t0 += kPT * 8) {
+      const int4 a = reinterpret_cast<const int4*>(gl + t0)[0];
+      const int4 b = reinterpret_cast<const int4*>(gl + t0)[1];
+      const int32_t g[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      TI v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = slice[g[q]];
+      if constexpr (sizeof(TI) == 2) {
+        *reinterpret_cast<uint4*>(send + t0) = *reinterpret_cast<const uint4*>(v);
+      } else {
+        reinterpret_cast<uint4*>(send + t0)[0] = reinterpret_cast<const uint4*>(v)[0];
+        reinterpret_cast<uint4*>(send + t0)[1] = reinterpret_cast<const uint4*>(v)[1];
+      }
+    }
     __syncthreads();  // send is complete; the slice is free for the next row
     if (row + ncl < n) stage(row + ncl);
     if (threadIdx.x == 0 && !*reinterpret_cast<volatile int*>(&abort_flag)) {
@@ -675,44 +707,26 @@ __global__ void __launch_bounds__(kPT, 1)
       pend_pr = pr;
     }
     pr ^= 1u;
-    // the output row: 8 ids per thread step, the codes of up to four steps
-    // loaded together (one round trip to L2 per row for most threads)
+    // the output row: 8 ids per thread step, from the codes held in registers
     TO* o = out + row * vs;
-    for (int64_t g0 = i_lo + (int64_t)threadIdx.x * 8; g0 < i_hi; g0 += (int64_t)kPT * 32) {
-      int32_t c[4][8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int64_t j0 = g0 + (int64_t)u * kPT * 8;
-        if (j0 + 8 <= i_hi) {  // code is 256-byte aligned, j0 a multiple of 8
-          const int4 a = reinterpret_cast<const int4*>(code + j0)[0];
-          const int4 b = reinterpret_cast<const int4*>(code + j0)[1];
-          c[u][0] = a.x; c[u][1] = a.y; c[u][2] = a.z; c[u][3] = a.w;
-          c[u][4] = b.x; c[u][5] = b.y; c[u][6] = b.z; c[u][7] = b.w;
-        } else {
+    for (int u = 0; u < kXSteps; ++u) {
+      const int64_t j0 = i_lo + ((int64_t)u * kPT + threadIdx.x) * 8;
+      if (j0 >= i_hi) break;
+      float v[8];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) c[u][q] = j0 + q < i_hi ? code[j0 + q] : -1;
-        }
+      for (int q = 0; q < 8; ++q) {
+        const uint32_t cq = (c16[u][q >> 1] >> (16 * (q & 1))) & 0xffffu;
+        // (0xffff: no teacher token; 0xfffe: several, written by the pass below)
+        const float x = cq < 0xfffeu ? ld<TI>(recv + cq) * inv_t : -INFINITY;
+        v[q] = x > -INFINITY ? x : lowest<TO>();
       }
+      if (j0 + 8 <= i_hi && (reinterpret_cast<uintptr_t>(o + j0) & 15) == 0) {
+        store_vec(o + j0, v);
+      } else {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int64_t j0 = g0 + (int64_t)u * kPT * 8;
-        if (j0 >= i_hi) break;
-        float v[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int32_t cq = c[u][q];
-          float x = -INFINITY;
-          // (ids with several teacher tokens are written by the pass below)
-          if (cq >= 0) x = ld<TI>(recv + cq) * inv_t;
-          v[q] = x > -INFINITY ? x : lowest<TO>();
-        }
-        if (j0 + 8 <= i_hi && (reinterpret_cast<uintptr_t>(o + j0) & 15) == 0) {
-          store_vec(o + j0, v);
-        } else {
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            if (j0 + q < i_hi) st<TO>(o + j0 + q, v[q]);
-        }
+        for (int q = 0; q < 8; ++q)
+          if (j0 + q < i_hi) st<TO>(o + j0 + q, v[q]);
       }
     }
     // ids with several teacher tokens: their columns' values are folded in
@@ -803,8 +817,10 @@ bool x_plan(int64_t vt, int64_t vs, XPlan* P) {
   C = (vt + P->sc - 1) / P->sc;
   P->C = (int)C;
   P->so = ((vs + C - 1) / C + 7) / 8 * 8;
+  if (P->so > (int64_t)kXSteps * 8 * kPT) return false;  // longer ranges: the slice path
   P->send_cap = P->sc + 8 * C;
   P->recv_cap = (kXSmem / elem - P->sc - P->send_cap) / 8 * 8;
+  if (P->recv_cap > 65528) P->recv_cap = 65528;  // slots fit the kernel's 16-bit codes
   if (P->recv_cap < 8) return false;
   P->smem = (size_t)(P->sc + P->send_cap + P->recv_cap) * (size_t)elem;
   auto kern = k_project_exchange<TI, TO>;
