@@ -32,9 +32,9 @@ namespace kd {
 namespace {
 
 constexpr int kMaxT = KD_MIX_MAX_TEACHERS;
-constexpr int kMT = 1024;                 // threads per CTA
+constexpr int kMT = 512;                  // threads per CTA (two CTAs per SM)
 constexpr int kMW = kMT / 32;             // warps per CTA
-constexpr int64_t kMixBuf = 200 * 1024;   // bytes of staged teacher rows per CTA
+constexpr int64_t kMixBuf = 100 * 1024;   // bytes of staged teacher rows per CTA
 constexpr float kLN2 = 0.6931471805599453f;
 
 struct MixParams {
@@ -234,15 +234,16 @@ __device__ __forceinline__ void stream8(const MixParams& P, const TI* zs, int t,
 // over the staged columns [0, clen), 8 columns a step, one exponential per
 // value (the running sum is rescaled when a step raises the maximum).
 template <bool GEO, typename TI>
-__device__ __forceinline__ Lse pass1(const MixParams& P, const TI* zs, int t, int64_t clen) {
-  float m = -INFINITY, s = 0.f;
-  for (int64_t j0 = (int64_t)threadIdx.x * 8; j0 < clen; j0 += (int64_t)kMT * 8) {
+__device__ __forceinline__ Lse pass1(const MixParams& P, const TI* zs, int t, int64_t lo,
+                                     int64_t hi, Lse acc) {
+  float m = acc.m, s = acc.s;
+  for (int64_t j0 = lo + (int64_t)threadIdx.x * 8; j0 < hi; j0 += (int64_t)kMT * 8) {
     float x[8];
     stream8<GEO>(P, zs, t, j0, x);
-    if (j0 + 8 > clen) {
+    if (j0 + 8 > hi) {
 #pragma unroll
       for (int q = 0; q < 8; ++q)
-        if (j0 + q >= clen) x[q] = -INFINITY;
+        if (j0 + q >= hi) x[q] = -INFINITY;
     }
     float m8 = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])),
                      fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
@@ -308,12 +309,16 @@ __device__ __forceinline__ void pass2_8(const MixParams& P, const TI* zs, const 
 
 // Cluster kernel: see the top of this file.  Rows are taken cluster by
 // cluster (all CTAs of a cluster loop over the same rows, so the cluster
-// barriers match).  With `dbuf` the staged rows are double-buffered: the next
-// row's bulk copies run under this row's passes.
+// barriers match).  A CTA's columns are staged in two halves, each with its
+// own barrier: pass 1 starts on the first half while the second lands, and
+// pass 2 frees the first half (whose copy for the next row starts at once)
+// before it writes the second.  So the staging of the next row runs under
+// this row's pass 2 and the next row's pass 1, and two CTAs share an SM, so
+// one CTA's waits are the other's compute.
 template <typename TI, typename TO, bool GEO>
-__global__ void __launch_bounds__(kMT, 1) k_mix_cluster(const MixParams P, int dbuf) {
+__global__ void __launch_bounds__(kMT, 2) k_mix_cluster(const MixParams P) {
   extern __shared__ __align__(16) uint8_t mix_smem[];
-  __shared__ __align__(8) uint64_t bars[2];
+  __shared__ __align__(8) uint64_t bars[2];  // one per half
   __shared__ Lse red[kMW];
   __shared__ float stats[2][kMaxT][2];  // this CTA's (max, sum) per stream, by row parity
   __shared__ float off_sh[kMaxT];  // the row logsumexp per stream
@@ -323,9 +328,9 @@ __global__ void __launch_bounds__(kMT, 1) k_mix_cluster(const MixParams P, int d
   const int64_t ncl = gridDim.x / csize;
   const int64_t c0 = (int64_t)rank * P.sc;
   const int64_t clen = P.v - c0 < P.sc ? (P.v - c0 > 0 ? P.v - c0 : 0) : P.sc;
+  const int64_t h0 = clen / 2 / 8 * 8;  // halves [0, h0) and [h0, clen)
   const int nstreams = GEO ? 1 : P.k;
-  const int64_t buf_elems = (int64_t)P.k * P.sc;  // a buffer: teacher k at k * sc
-  TI* const base = reinterpret_cast<TI*>(mix_smem);
+  TI* const zs = reinterpret_cast<TI*>(mix_smem);  // teacher k at zs + k * sc
   if (threadIdx.x == 0) {
     ptx::mbar_init(ptx::smem_u32(&bars[0]), 1);
     ptx::mbar_init(ptx::smem_u32(&bars[1]), 1);
@@ -333,16 +338,17 @@ __global__ void __launch_bounds__(kMT, 1) k_mix_cluster(const MixParams P, int d
     abort_flag = 0;
   }
   __syncthreads();
-  // stage `row` into buffer b: the 16-byte-aligned bulk of each teacher's
-  // columns by bulk copy, the rest (a ragged tail, or a whole unaligned row)
-  // by plain loads
-  auto stage = [&](int64_t row, int b) {
-    TI* zs = base + b * buf_elems;
-    const uint32_t bar = ptx::smem_u32(&bars[b]);
+  // stage half hh of `row`: the 16-byte-aligned bulk of each teacher's columns
+  // by bulk copy, the rest (a ragged tail, or a whole unaligned row) by plain
+  // loads
+  auto stage = [&](int64_t row, int hh) {
+    const int64_t lo = hh ? h0 : 0, hi = hh ? clen : h0;
+    const uint32_t bar = ptx::smem_u32(&bars[hh]);
     auto nbytes = [&](int k) -> int64_t {
-      const TI* src = static_cast<const TI*>(P.z[k]) + row * P.v + c0;
-      const bool al = ((reinterpret_cast<uintptr_t>(src) | ptx::smem_u32(zs + k * P.sc)) & 15) == 0;
-      return al ? clen * (int64_t)sizeof(TI) / 16 * 16 : 0;
+      const TI* src = static_cast<const TI*>(P.z[k]) + row * P.v + c0 + lo;
+      const bool al =
+          ((reinterpret_cast<uintptr_t>(src) | ptx::smem_u32(zs + k * P.sc + lo)) & 15) == 0;
+      return al ? (hi - lo) * (int64_t)sizeof(TI) / 16 * 16 : 0;
     };
     if (threadIdx.x == 0 && !*reinterpret_cast<volatile int*>(&abort_flag)) {
       // (after a timed-out wait no new copy starts; later waits give up)
@@ -353,40 +359,45 @@ __global__ void __launch_bounds__(kMT, 1) k_mix_cluster(const MixParams P, int d
       for (int k = 0; k < P.k; ++k) {
         const int64_t nb = nbytes(k);
         if (nb > 0)
-          ptx::bulk_load(ptx::smem_u32(zs + k * P.sc),
-                         static_cast<const TI*>(P.z[k]) + row * P.v + c0, (uint32_t)nb, bar);
+          ptx::bulk_load(ptx::smem_u32(zs + k * P.sc + lo),
+                         static_cast<const TI*>(P.z[k]) + row * P.v + c0 + lo, (uint32_t)nb, bar);
       }
     }
     for (int k = 0; k < P.k; ++k) {
       const TI* src = static_cast<const TI*>(P.z[k]) + row * P.v + c0;
-      for (int64_t q = nbytes(k) / (int64_t)sizeof(TI) + threadIdx.x; q < clen; q += kMT)
+      for (int64_t q = lo + nbytes(k) / (int64_t)sizeof(TI) + threadIdx.x; q < hi; q += kMT)
         zs[k * P.sc + q] = src[q];
     }
   };
-  const int64_t first = blockIdx.x / csize;
-  if (first < P.n) stage(first, 0);
-  uint32_t parity = 0;  // bit b: phase parity to wait for on buffer b
+  uint32_t parity = 0;  // bit hh: phase parity to wait for on half hh
   // the first wait that gave up: its copies may still be in flight (none
   // starts after it, the abort flag being set by then)
-  int pend_b = -1;
+  int pend_h = -1;
   uint32_t pend_p = 0;
+  auto wait_half = [&](int hh) {
+    if (!ptx::warp_wait(ptx::smem_u32(&bars[hh]), (parity >> hh) & 1u, &abort_flag, P.status) &&
+        pend_h < 0) {
+      pend_h = hh;
+      pend_p = (parity >> hh) & 1u;
+    }
+    parity ^= 1u << hh;
+    __syncthreads();  // the plain-loaded columns too
+  };
+  const int64_t first = blockIdx.x / csize;
+  if (first < P.n) {
+    stage(first, 0);
+    stage(first, 1);
+  }
   int it = 0;
   for (int64_t row = first; row < P.n; row += ncl, ++it) {
-    const int b = dbuf ? (it & 1) : 0;
-    // buffer b ^ 1 held the previous row, which every thread is done with
-    if (dbuf && row + ncl < P.n) stage(row + ncl, b ^ 1);
-    if (!ptx::warp_wait(ptx::smem_u32(&bars[b]), (parity >> b) & 1u, &abort_flag, P.status) &&
-        pend_b < 0) {
-      pend_b = b;
-      pend_p = (parity >> b) & 1u;
-    }
-    parity ^= 1u << b;
-    __syncthreads();  // the plain-loaded columns too
-    const TI* zs = base + b * buf_elems;
-    // pass 1: this CTA's (max, sum) per stream
+    // pass 1: this CTA's (max, sum) per stream, the first half as soon as it lands
     const int pb = it & 1;
+    wait_half(0);
     for (int t = 0; t < nstreams; ++t) {
-      const Lse r = block_lse(pass1<GEO>(P, zs, t, clen), red);
+      Lse a = pass1<GEO>(P, zs, t, 0, h0, Lse{-INFINITY, 0.f});
+      if (t == 0) wait_half(1);
+      a = pass1<GEO>(P, zs, t, h0, clen, a);
+      const Lse r = block_lse(a, red);
       if (threadIdx.x == 0) {
         stats[pb][t][0] = r.m;
         stats[pb][t][1] = r.s;
@@ -408,38 +419,43 @@ __global__ void __launch_bounds__(kMT, 1) k_mix_cluster(const MixParams P, int d
       off_sh[threadIdx.x] = lse_value(acc);
     }
     __syncthreads();
-    // pass 2: the output columns, 8 per thread step (vector stores when aligned)
+    // pass 2: the output columns, 8 per thread step (vector stores when
+    // aligned), half by half; each half is restaged for the next row as soon
+    // as every thread is done with it
     TO* o = static_cast<TO*>(P.out) + row * P.v + c0;
     const bool ov = (reinterpret_cast<uintptr_t>(o) & 15) == 0;
-    for (int64_t j0 = (int64_t)threadIdx.x * 8; j0 < clen; j0 += (int64_t)kMT * 8) {
-      float r[8];
-      pass2_8<GEO, TI, TO>(P, zs, off_sh, j0, r);
-      if (ov && j0 + 8 <= clen) {
-        if constexpr (sizeof(TO) == 4) {
-          reinterpret_cast<float4*>(o + j0)[0] = make_float4(r[0], r[1], r[2], r[3]);
-          reinterpret_cast<float4*>(o + j0)[1] = make_float4(r[4], r[5], r[6], r[7]);
+    for (int hh = 0; hh < 2; ++hh) {
+      const int64_t lo = hh ? h0 : 0, hi = hh ? clen : h0;
+      for (int64_t j0 = lo + (int64_t)threadIdx.x * 8; j0 < hi; j0 += (int64_t)kMT * 8) {
+        float r[8];
+        pass2_8<GEO, TI, TO>(P, zs, off_sh, j0, r);
+        if (ov && j0 + 8 <= hi) {
+          if constexpr (sizeof(TO) == 4) {
+            reinterpret_cast<float4*>(o + j0)[0] = make_float4(r[0], r[1], r[2], r[3]);
+            reinterpret_cast<float4*>(o + j0)[1] = make_float4(r[4], r[5], r[6], r[7]);
+          } else {
+            uint4 u;
+            u.x = pack_bf16(r[0], r[1]);
+            u.y = pack_bf16(r[2], r[3]);
+            u.z = pack_bf16(r[4], r[5]);
+            u.w = pack_bf16(r[6], r[7]);
+            *reinterpret_cast<uint4*>(o + j0) = u;
+          }
         } else {
-          uint4 u;
-          u.x = pack_bf16(r[0], r[1]);
-          u.y = pack_bf16(r[2], r[3]);
-          u.z = pack_bf16(r[4], r[5]);
-          u.w = pack_bf16(r[6], r[7]);
-          *reinterpret_cast<uint4*>(o + j0) = u;
-        }
-      } else {
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (j0 + q < clen) o[j0 + q] = from_f<TO>(r[q]);
+          for (int q = 0; q < 8; ++q)
+            if (j0 + q < hi) o[j0 + q] = from_f<TO>(r[q]);
+        }
       }
+      __syncthreads();  // half hh is read
+      if (row + ncl < P.n) stage(row + ncl, hh);
     }
-    __syncthreads();  // this buffer is read; a later row may overwrite it
-    if (!dbuf && row + ncl < P.n) stage(row + ncl, 0);
   }
   // no CTA leaves while another may still read its pairs, nor with a copy of
   // its own in flight (bounded, whatever the abort flag)
   cl_sync();
-  if (pend_b >= 0 && threadIdx.x < 32)
-    ptx::warp_wait(ptx::smem_u32(&bars[pend_b]), pend_p, &abort_flag, P.status, false);
+  if (pend_h >= 0 && threadIdx.x < 32)
+    ptx::warp_wait(ptx::smem_u32(&bars[pend_h]), pend_p, &abort_flag, P.status, false);
 }
 
 // One CTA per row (grid-strided): pass 1 and pass 2 read the row from global
@@ -465,16 +481,15 @@ __global__ void __launch_bounds__(kMT) k_mix_rows(const MixParams P) {
 }
 
 // smallest cluster (1, 2, 4, 8, 16 CTAs) whose per-CTA columns of all K
-// teachers, sc a multiple of 8, fit the staging budget, double-buffered
-// (*dbuf = 1) when twice that fits too; 0 when none does.  (Smaller clusters
-// win over double buffering: more SMs can host them, and the per-row cluster
-// barrier and reductions cost less.)
-int mix_cluster_for(int64_t v, int k, int64_t elem, int64_t* sc, int* dbuf) {
+// teachers, sc a multiple of 8, fit the staging budget; 0 when none does.
+// (Smaller clusters win over whole-row double buffering: more SMs can host
+// them, and the per-row cluster barrier and reductions cost less; the
+// two-half staging hides most of the copies instead.)
+int mix_cluster_for(int64_t v, int k, int64_t elem, int64_t* sc) {
   for (int c = 1; c <= 16; c *= 2) {
     const int64_t cols = ((v + c - 1) / c + 7) / 8 * 8;
     if (cols * elem * k <= kMixBuf) {
       *sc = cols;
-      *dbuf = 2 * cols * elem * k <= kMixBuf;
       return c;
     }
   }
@@ -484,11 +499,10 @@ int mix_cluster_for(int64_t v, int k, int64_t elem, int64_t* sc, int* dbuf) {
 template <typename TI, typename TO, bool GEO>
 int launch_mix(MixParams P, cudaStream_t s) {
   int64_t sc = 0;
-  int dbuf = 0;
-  const int c = mix_cluster_for(P.v, P.k, (int64_t)sizeof(TI), &sc, &dbuf);
+  const int c = mix_cluster_for(P.v, P.k, (int64_t)sizeof(TI), &sc);
   const int nsm = tc_num_sms() > 0 ? tc_num_sms() : 1;
   if (c > 0) {
-    const size_t smem = (size_t)sc * sizeof(TI) * (size_t)P.k * (dbuf ? 2 : 1);
+    const size_t smem = (size_t)sc * sizeof(TI) * (size_t)P.k;
     auto kern = k_mix_cluster<TI, TO, GEO>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
@@ -513,7 +527,7 @@ int launch_mix(MixParams P, cudaStream_t s) {
     static int cached_c = 0, cached_max = 0;
     static size_t cached_smem = 0;
     if (cached_c != c || cached_smem != smem) {
-      cfg.gridDim = dim3((unsigned)(c * std::max(1, nsm / c)));
+      cfg.gridDim = dim3((unsigned)(c * std::max(1, 2 * nsm / c)));
       int m = 0;
       if (cudaOccupancyMaxActiveClusters(&m, kern, &cfg) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -528,7 +542,7 @@ int launch_mix(MixParams P, cudaStream_t s) {
       const int64_t clusters = P.n < cached_max ? P.n : cached_max;
       cfg.gridDim = dim3((unsigned)(c * clusters));
       note_launch();
-      return cudaLaunchKernelEx(&cfg, kern, P, dbuf) != cudaSuccess;
+      return cudaLaunchKernelEx(&cfg, kern, P) != cudaSuccess;
     }
   }
   const int grid = (int)std::min<int64_t>(P.n, (int64_t)nsm * 2);
