@@ -402,6 +402,44 @@ __device__ __forceinline__ RowOut finalize(const RowState& s, const Consts& c, i
 // No form subtracts two large values: nearby distributions keep their small
 // divergences, and an id with q = 0 (a teacher id no token maps to: x huge)
 // still gives log(p/m) = -log b exactly.
+// Paired fp32 arithmetic (fma / add / sub / mul .f32x2): one instruction for
+// two columns.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
 __device__ __forceinline__ void js_logs(float x, const Consts& c, float& lqm, float& lpm) {
   const bool neg = x <= 0.f;
   const float coef = neg ? c.beta : 1.f - c.beta;
@@ -432,6 +470,39 @@ __device__ __forceinline__ void js_terms(float zs, float zt, float lse_tT, float
   jq = fmaf(q, lqm, jq);
   jp = fmaf(p, lpm, jp);
   if (want_x) jx = fmaf(p, ex2(lpm * kL2E), jx);
+}
+
+// js_terms for two columns at once (the fast, non-precise path), the fp32
+// arithmetic on .f32x2 pairs; the sums stay per lane.
+__device__ __forceinline__ void js_terms2(float2 zs, float2 zt, float lse_tT, float dlse,
+                                          const Consts& c, float2& jq, float2& jp, float2& jx,
+                                          bool want_x) {
+  const float2 its = make_float2(c.inv_ts, c.inv_ts), itt = make_float2(c.inv_tt, c.inv_tt);
+  const float2 l2e = make_float2(kL2E, kL2E);
+  const float2 at = mul2(zt, itt);
+  const float2 x = add2(fma2(zs, its, make_float2(-at.x, -at.y)), make_float2(dlse, dlse));
+  const float2 lq = sub2(at, make_float2(lse_tT, lse_tT));
+  const float2 lp = fma2(zs, its, make_float2(dlse - lse_tT, dlse - lse_tT));
+  // per column: y = -|x| and the weight of the smaller distribution
+  const bool n0 = x.x <= 0.f, n1 = x.y <= 0.f;
+  const float2 y = make_float2(-fabsf(x.x), -fabsf(x.y));
+  const float2 coef = make_float2(n0 ? c.beta : 1.f - c.beta, n1 ? c.beta : 1.f - c.beta);
+  const float2 yl = mul2(y, l2e);
+  const float2 e = make_float2(ex2(yl.x), ex2(yl.y));
+  const float2 t = fma2(coef, add2(e, make_float2(-1.f, -1.f)), make_float2(1.f, 1.f));
+  const float2 l = make_float2(__logf(t.x), __logf(t.y));
+  const float2 xl = add2(x, l);  // -(lqm) when x > 0
+  const float2 lqm = make_float2(n0 ? -l.x : -xl.x, n1 ? -l.y : -xl.y);
+  const float2 lpm = sub2(make_float2(n0 ? x.x : 0.f, n1 ? x.y : 0.f), l);
+  const float2 a2 = mul2(lq, l2e), b2 = mul2(lp, l2e);
+  const float2 q = make_float2(ex2(a2.x), ex2(a2.y));
+  const float2 p = make_float2(ex2(b2.x), ex2(b2.y));
+  jq = fma2(q, lqm, jq);
+  jp = fma2(p, lpm, jp);
+  if (want_x) {
+    const float2 r = mul2(lpm, l2e);
+    jx = fma2(p, make_float2(ex2(r.x), ex2(r.y)), jx);
+  }
 }
 
 // d KL / d a_s of the skew variants (teacher detached), from p, log(q/m),

@@ -355,6 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd(StreamArgs a, uint32_t* sta
       const float dlse = R.bcast[0], lse_tT = R.bcast[1];
       const bool want_x = a.variant != KD_KL_SKEW_JS;
       float jq = 0.f, jp = 0.f, jx = 0.f;
+      float2 jq2 = make_float2(0.f, 0.f), jp2 = jq2, jx2 = jq2;
       for (int ch = 0; ch < nch; ++ch) {
         const uint8_t* buf = cur.acquire(R, status);
         float fs[kSlots][EPT], ft[kSlots][EPT];
@@ -369,12 +370,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd(StreamArgs a, uint32_t* sta
           }
         }
         cur.release(R);
+        if (c.precise) {
 #pragma unroll
-        for (int j = 0; j < kSlots; ++j)
+          for (int j = 0; j < kSlots; ++j)
 #pragma unroll
-          for (int u = 0; u < EPT; ++u)
-            if (u < nv[j]) js_terms(fs[j][u], ft[j][u], lse_tT, dlse, c, jq, jp, jx, want_x);
+            for (int u = 0; u < EPT; ++u)
+              if (u < nv[j]) js_terms(fs[j][u], ft[j][u], lse_tT, dlse, c, jq, jp, jx, want_x);
+        } else {  // two columns per .f32x2 instruction
+#pragma unroll
+          for (int j = 0; j < kSlots; ++j)
+#pragma unroll
+            for (int u = 0; u < EPT; u += 2) {
+              if (u + 1 < nv[j]) {
+                js_terms2(make_float2(fs[j][u], fs[j][u + 1]), make_float2(ft[j][u], ft[j][u + 1]),
+                          lse_tT, dlse, c, jq2, jp2, jx2, want_x);
+              } else if (u < nv[j]) {
+                js_terms(fs[j][u], ft[j][u], lse_tT, dlse, c, jq, jp, jx, want_x);
+              }
+            }
+        }
       }
+      jq += jq2.x + jq2.y;
+      jp += jp2.x + jp2.y;
+      jx += jx2.x + jx2.y;
       const float3 r = consumer_sum3(jq, jp, jx, R);
       if (ct == 0) {
         const bool v_ok = !a.labels || y != a.ignore;
