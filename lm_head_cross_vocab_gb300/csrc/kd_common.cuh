@@ -472,6 +472,35 @@ __device__ __forceinline__ void js_terms(float zs, float zt, float lse_tT, float
   if (want_x) jx = fmaf(p, ex2(lpm * kL2E), jx);
 }
 
+// js_logs for two columns (the fast path): log(q/m), log(p/m) from x = log p - log q
+__device__ __forceinline__ void js_logs2(float2 x, const Consts& c, float2& lqm, float2& lpm) {
+  const bool n0 = x.x <= 0.f, n1 = x.y <= 0.f;
+  const float2 yl = make_float2(-fabsf(x.x) * kL2E, -fabsf(x.y) * kL2E);
+  const float2 coef = make_float2(n0 ? c.beta : 1.f - c.beta, n1 ? c.beta : 1.f - c.beta);
+  const float2 t = fma2(coef, make_float2(ex2(yl.x) - 1.f, ex2(yl.y) - 1.f), make_float2(1.f, 1.f));
+  const float2 l = make_float2(__logf(t.x), __logf(t.y));
+  const float2 xl = add2(x, l);
+  lqm = make_float2(n0 ? -l.x : -xl.x, n1 ? -l.y : -xl.y);
+  lpm = sub2(make_float2(n0 ? x.x : 0.f, n1 ? x.y : 0.f), l);
+}
+
+// skew_grad for two columns, p and the logs of js_logs2 given
+__device__ __forceinline__ float2 skew_grad2(int variant, float2 p, float2 lqm, float2 lpm,
+                                             float kl_pm, float eppm, const Consts& c) {
+  const float b = c.beta;
+  if (variant == KD_KL_SKEW_FORWARD) {
+    const float eqm = (1.f - b * eppm) / (1.f - b);
+    const float2 e = make_float2(ex2(lqm.x * kL2E) - eqm, ex2(lqm.y * kL2E) - eqm);
+    return mul2(mul2(p, make_float2(-b, -b)), e);
+  }
+  const float2 d = sub2(lpm, make_float2(kl_pm, kl_pm));
+  if (variant == KD_KL_SKEW_REVERSE) {
+    const float2 e = make_float2(ex2(lpm.x * kL2E) - eppm, ex2(lpm.y * kL2E) - eppm);
+    return mul2(p, fma2(make_float2(-b, -b), e, d));
+  }
+  return mul2(mul2(p, make_float2(b, b)), d);
+}
+
 // js_terms for two columns at once (the fast, non-precise path), the fp32
 // arithmetic on .f32x2 pairs; the sums stay per lane.
 __device__ __forceinline__ void js_terms2(float2 zs, float2 zt, float lse_tT, float dlse,

@@ -259,9 +259,13 @@ struct PackedGrad {
         const float2 r = fma2(sub2(lp2, lq2), splat(1.f / kL2E), splat(-kl_r));
         if (VAR == KD_KL_REVERSE) g = mul2(mul2(p, splat(sw)), r);
         else g = mul2(fma2(p, r, sub2(p, ex2x2(lq2))), splat(sw));
-      } else {
-        g.x = sw * kl_grad_pq(s.x, t.x, 0.f, 0.f, p.x, 0.f, sv, VAR, c);
-        g.y = sw * kl_grad_pq(s.y, t.y, 0.f, 0.f, p.y, 0.f, sv, VAR, c);
+      } else {  // skew variants, two columns per .f32x2 instruction
+        const float2 at = mul2(t, splat(c.inv_tt));
+        const float2 x =
+            add2(fma2(s, splat(c.inv_ts), make_float2(-at.x, -at.y)), splat(sv[S_DLSE]));
+        float2 lqm, lpm;
+        js_logs2(x, c, lqm, lpm);
+        g = mul2(skew_grad2(VAR, p, lqm, lpm, sv[S_KL_PM], sv[S_EPPM], c), splat(sw));
       }
     } else {
       g = mul2(p, splat(sw));
