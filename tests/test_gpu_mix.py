@@ -118,3 +118,19 @@ def test_distillation_from_a_mixture(mode):
     assert abs(fwd["loss"].item() - ref["loss"]) <= TOK_TOL["bf16"] * abs(ref["loss"])
     g_s, _ = O.grad_logits(O.as_f64(z_s), zt_ref, lab, **kw)
     assert rel_l2(bwd["d_logits_s"].cpu().double().numpy(), g_s) <= GRAD_TOL["bf16"]
+
+
+@pytest.mark.parametrize("mode", ["arithmetic", "geometric"])
+def test_mix_edge_cases(mode):
+    """No tokens (nothing written, no error), a one-id vocabulary (the mixture
+    is log 1 = 0), and eight teachers with uniform weights."""
+    z = torch.randn(0, 1000, device="cuda")
+    assert kd.mix_teacher_logits([z, z], None, mode).shape == (0, 1000)
+    one = kd.mix_teacher_logits([torch.randn(3, 1, device="cuda") * 5 for _ in range(2)], None,
+                                mode)
+    torch.cuda.synchronize()
+    assert torch.all(one.abs() <= 1e-6)
+    zs = _teachers(8, 5003, 4, "bf16", seed=12, holes=False)
+    got = kd.mix_teacher_logits([t.cuda() for t in zs], None, mode, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    _check(got.cpu().double().numpy(), O.mix_teacher_logits(zs, None, mode), "fp32")

@@ -134,3 +134,19 @@ def test_projection_skewed_map(dout):
     tol = 1e-6 if dout == "fp32" else 2.0 ** -8
     err = np.abs(got[~empty] - ref[~empty]) / np.maximum(1.0, np.abs(ref[~empty]))
     assert err.max() <= tol, err.max()
+
+
+def test_projection_edge_cases():
+    """No tokens (the map is still checked), one student id, and a map with
+    no matched teacher token at all (every output at the lowest value)."""
+    tmap = _map(300, 200, 3)
+    out = kd.project_teacher_logits(torch.from_numpy(tmap), torch.randn(0, 300, device="cuda"), 200)
+    assert out.shape == (0, 200)
+    z = torch.randn(4, 300, device="cuda")
+    one = kd.project_teacher_logits(torch.zeros(300, dtype=torch.int32), z, 1, temperature=1.0)
+    ref = O.project_teacher_logits(z.cpu(), np.zeros(300, dtype=np.int64), 1)
+    torch.cuda.synchronize()
+    assert np.allclose(one.cpu().double().numpy(), ref, rtol=0, atol=2e-4)  # 300 folds in fp32
+    none = kd.project_teacher_logits(torch.full((300,), -1, dtype=torch.int32), z, 50)
+    torch.cuda.synchronize()
+    assert torch.all(none <= -1e38)
