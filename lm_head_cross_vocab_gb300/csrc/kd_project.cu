@@ -11,18 +11,24 @@
 //
 // Every call first builds, in the caller's workspace, the inverse map (count
 // -> exclusive scan -> scatter -> per-id sort, so summation orders are fixed
-// and results deterministic) and a partition of the student ids by the slice
-// of the teacher row that produces them.  The teacher row is cut into C
-// slices of at most kSliceMax bytes; the id list of slice r holds, in
-// ascending id order, the ids whose (first) teacher column lies in slice r,
-// plus a share of the unmatched ids.  Then the work items are (token row,
-// slice): a CTA stages the slice in shared memory with one bulk copy
-// (double-buffered across its items), reads each listed id's column there --
-// every random access is a local shared-memory read -- and stores the id's
-// output straight to global memory.  A warp writes 32 consecutive list
-// entries, i.e. ids within a short ascending run, so the stores of the C
-// slices of a row fill each other's sectors in L2 and each output byte goes
-// to HBM once.
+// and results deterministic) and the lists of one of two paths:
+//
+// * exchange (k_project_exchange, the normal path): a cluster of C <= 8 CTAs
+//   shares each token row.  CTA r stages teacher columns [r*sc, r*sc + sc)
+//   with one bulk copy, gathers the values its map edges need into a send
+//   buffer ordered by destination CTA (random reads of its own shared memory
+//   only), and ships each segment to the CTA that writes those student ids
+//   with one shared::cta -> shared::cluster bulk copy; the owner then writes
+//   its id range of the output row with 16-byte stores.  Random accesses
+//   never leave an SM, and every output byte is written once in whole
+//   sectors.
+// * slices (k_project_slices, the fallback when a receive buffer would
+//   overflow -- a map that sends most edges to one range, decided on the
+//   device -- or when a row needs more than 8 CTAs or a CTA more than 32 Ki
+//   student ids): work items (token row,
+//   slice); a CTA stages the slice and stores each listed id's output straight
+//   to global memory.  Correct for any map, but its 2-byte stores leave
+//   sectors partial, which costs DRAM read-modify-writes.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
