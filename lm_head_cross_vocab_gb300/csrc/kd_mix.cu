@@ -184,8 +184,8 @@ __device__ __forceinline__ void cl_sync() {
 __device__ __forceinline__ float cl_load(const float* p, uint32_t rank) {
   uint32_t a = ptx::smem_u32(p);
   asm("mapa.shared::cluster.u32 %0, %0, %1;" : "+r"(a) : "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  float v;  // (volatile: never moved above the cluster barrier that publishes it)
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
   return v;
 }
 
@@ -319,10 +319,9 @@ template <typename TI, typename TO, bool GEO>
 __global__ void __launch_bounds__(kMT, 2) k_mix_cluster(const MixParams P) {
   extern __shared__ __align__(16) uint8_t mix_smem[];
   __shared__ __align__(8) uint64_t bars[2];  // one per half
-  __shared__ Lse red[kMW];
+  __shared__ Lse red_all[kMW][kMaxT];   // per warp and stream
   __shared__ float stats[2][kMaxT][2];  // this CTA's (max, sum) per stream, by row parity
-  __shared__ float off_sh[kMaxT];  // the row logsumexp per stream
-  __shared__ Lse peer[16][kMaxT];  // every CTA's pair per stream, fetched
+  __shared__ float off_sh[kMaxT];       // the row logsumexp per stream
   __shared__ int abort_flag;
   const uint32_t rank = cl_rank(), csize = cl_size();
   const int64_t ncl = gridDim.x / csize;
@@ -341,7 +340,9 @@ __global__ void __launch_bounds__(kMT, 2) k_mix_cluster(const MixParams P) {
   // stage half hh of `row`: the 16-byte-aligned bulk of each teacher's columns
   // by bulk copy, the rest (a ragged tail, or a whole unaligned row) by plain
   // loads
-  auto stage = [&](int64_t row, int hh) {
+  // (returns whether some columns were plain-loaded: the wait then needs a
+  // CTA barrier to see them; the bulk-copied ones come with the barrier wait)
+  auto stage = [&](int64_t row, int hh) -> bool {
     const int64_t lo = hh ? h0 : 0, hi = hh ? clen : h0;
     const uint32_t bar = ptx::smem_u32(&bars[hh]);
     auto nbytes = [&](int k) -> int64_t {
@@ -363,17 +364,21 @@ __global__ void __launch_bounds__(kMT, 2) k_mix_cluster(const MixParams P) {
                          static_cast<const TI*>(P.z[k]) + row * P.v + c0 + lo, (uint32_t)nb, bar);
       }
     }
+    bool plain = false;
     for (int k = 0; k < P.k; ++k) {
       const TI* src = static_cast<const TI*>(P.z[k]) + row * P.v + c0;
-      for (int64_t q = lo + nbytes(k) / (int64_t)sizeof(TI) + threadIdx.x; q < hi; q += kMT)
-        zs[k * P.sc + q] = src[q];
+      const int64_t q0 = lo + nbytes(k) / (int64_t)sizeof(TI);
+      plain |= q0 < hi;
+      for (int64_t q = q0 + threadIdx.x; q < hi; q += kMT) zs[k * P.sc + q] = src[q];
     }
+    return plain;
   };
   uint32_t parity = 0;  // bit hh: phase parity to wait for on half hh
   // the first wait that gave up: its copies may still be in flight (none
   // starts after it, the abort flag being set by then)
   int pend_h = -1;
   uint32_t pend_p = 0;
+  bool plain0 = false, plain1 = false;  // a half has plain-loaded columns
   auto wait_half = [&](int hh) {
     if (!ptx::warp_wait(ptx::smem_u32(&bars[hh]), (parity >> hh) & 1u, &abort_flag, P.status) &&
         pend_h < 0) {
@@ -381,41 +386,56 @@ __global__ void __launch_bounds__(kMT, 2) k_mix_cluster(const MixParams P) {
       pend_p = (parity >> hh) & 1u;
     }
     parity ^= 1u << hh;
-    __syncthreads();  // the plain-loaded columns too
+    if (hh ? plain1 : plain0) __syncthreads();  // the plain-loaded columns too
   };
   const int64_t first = blockIdx.x / csize;
   if (first < P.n) {
-    stage(first, 0);
-    stage(first, 1);
+    plain0 = stage(first, 0);
+    plain1 = stage(first, 1);
   }
   int it = 0;
   for (int64_t row = first; row < P.n; row += ncl, ++it) {
     // pass 1: this CTA's (max, sum) per stream, the first half as soon as it lands
     const int pb = it & 1;
     wait_half(0);
+    // every stream's pair folded per thread, then per warp (shuffles), then
+    // across the warps by one thread per stream: one CTA barrier for all
     for (int t = 0; t < nstreams; ++t) {
       Lse a = pass1<GEO>(P, zs, t, 0, h0, Lse{-INFINITY, 0.f});
       if (t == 0) wait_half(1);
       a = pass1<GEO>(P, zs, t, h0, clen, a);
-      const Lse r = block_lse(a, red);
-      if (threadIdx.x == 0) {
-        stats[pb][t][0] = r.m;
-        stats[pb][t][1] = r.s;
-      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+        a = lse_merge(a, Lse{__shfl_xor_sync(0xffffffffu, a.m, o),
+                             __shfl_xor_sync(0xffffffffu, a.s, o)});
+      if ((threadIdx.x & 31) == 0) red_all[threadIdx.x >> 5][t] = a;
+    }
+    __syncthreads();
+    if (threadIdx.x < (unsigned)nstreams) {
+      Lse r = red_all[0][threadIdx.x];
+      for (int w = 1; w < kMW; ++w) r = lse_merge(r, red_all[w][threadIdx.x]);
+      stats[pb][threadIdx.x][0] = r.m;
+      stats[pb][threadIdx.x][1] = r.s;
     }
     // every CTA's pairs of this row are written (and every CTA is done with
     // the previous row's pairs in this parity slot)
     cl_sync();
-    // one thread per (CTA, stream) pair fetches it, so all the remote loads
-    // are in flight together; then one thread per stream merges them
-    if (threadIdx.x < csize * (unsigned)nstreams) {
-      const uint32_t q = threadIdx.x / nstreams, t = threadIdx.x % nstreams;
-      peer[q][t] = Lse{cl_load(&stats[pb][t][0], q), cl_load(&stats[pb][t][1], q)};
-    }
-    __syncthreads();
+    // one thread per stream loads every CTA's pair (all loads issued before
+    // any is used) and merges them
     if (threadIdx.x < (unsigned)nstreams) {
       Lse acc{-INFINITY, 0.f};
-      for (uint32_t q = 0; q < csize; ++q) acc = lse_merge(acc, peer[q][threadIdx.x]);
+      for (uint32_t q0 = 0; q0 < csize; q0 += 4) {
+        float pm[4], ps[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (q0 + q < csize) {
+            pm[q] = cl_load(&stats[pb][threadIdx.x][0], q0 + q);
+            ps[q] = cl_load(&stats[pb][threadIdx.x][1], q0 + q);
+          }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (q0 + q < csize) acc = lse_merge(acc, Lse{pm[q], ps[q]});
+      }
       off_sh[threadIdx.x] = lse_value(acc);
     }
     __syncthreads();
@@ -448,7 +468,7 @@ __global__ void __launch_bounds__(kMT, 2) k_mix_cluster(const MixParams P) {
         }
       }
       __syncthreads();  // half hh is read
-      if (row + ncl < P.n) stage(row + ncl, hh);
+      if (row + ncl < P.n) (hh ? plain1 : plain0) = stage(row + ncl, hh);
     }
   }
   // no CTA leaves while another may still read its pairs, nor with a copy of
