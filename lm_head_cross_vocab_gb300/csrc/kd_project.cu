@@ -629,7 +629,9 @@ __global__ void __launch_bounds__(kPT, 1)
     abort_flag = 0;
   }
   __syncthreads();
-  auto stage = [&](int64_t row) {
+  // (returns whether some columns were plain-loaded: the wait then needs a
+  // CTA barrier to see them; the bulk-copied ones come with the barrier wait)
+  auto stage = [&](int64_t row) -> bool {
     const TI* src = zt + row * vt + c0;
     const bool al = ((reinterpret_cast<uintptr_t>(src) | ptx::smem_u32(slice)) & 15) == 0;
     const int64_t nb = al ? clen * (int64_t)sizeof(TI) / 16 * 16 : 0;
@@ -640,11 +642,14 @@ __global__ void __launch_bounds__(kPT, 1)
         ptx::bulk_load(ptx::smem_u32(slice), src, (uint32_t)nb, bar_s);
       }
     }
-    for (int64_t q = nb / (int64_t)sizeof(TI) + threadIdx.x; q < clen; q += kPT) slice[q] = src[q];
+    const int64_t q0 = nb / (int64_t)sizeof(TI);
+    for (int64_t q = q0 + threadIdx.x; q < clen; q += kPT) slice[q] = src[q];
+    return q0 < clen;
   };
+  bool plain = false;
   const int64_t first = blockIdx.x / C;
   if (first < n) {
-    stage(first);
+    plain = stage(first);
     if (threadIdx.x == 0) ptx::mbar_expect_tx(bar_r, rx_bytes);
   }
   cl_sync();  // every receive barrier is armed before any copy is sent
@@ -674,7 +679,7 @@ __global__ void __launch_bounds__(kPT, 1)
       pend_ps = ps;
     }
     ps ^= 1u;
-    __syncthreads();  // the plain-loaded columns too
+    if (plain) __syncthreads();  // the plain-loaded columns too
     // 8 slots per thread step: nsend, the list start and send are multiples of 8
     for (int32_t t0 = (int32_t)threadIdx.x * 8; t0 < nsend; t0 += kPT * 8) {
       const int4 a = reinterpret_cast<const int4*>(gl + t0)[0];
@@ -691,7 +696,7 @@ __global__ void __launch_bounds__(kPT, 1)
       }
     }
     __syncthreads();  // send is complete; the slice is free for the next row
-    if (row + ncl < n) stage(row + ncl);
+    if (row + ncl < n) plain = stage(row + ncl);
     if (threadIdx.x == 0 && !*reinterpret_cast<volatile int*>(&abort_flag)) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       for (uint32_t q = 0; q < C; ++q) {
