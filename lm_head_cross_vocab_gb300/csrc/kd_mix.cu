@@ -544,15 +544,19 @@ int launch_mix(MixParams P, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     // co-resident clusters of this shape (cached per cluster size and buffer)
-    static int cached_c = 0, cached_max = 0;
+    // (per template instance; keyed by device, cluster size and buffer bytes)
+    static int cached_dev = -1, cached_c = 0, cached_max = 0;
     static size_t cached_smem = 0;
-    if (cached_c != c || cached_smem != smem) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (cached_dev != dev || cached_c != c || cached_smem != smem) {
       cfg.gridDim = dim3((unsigned)(c * std::max(1, 2 * nsm / c)));
       int m = 0;
       if (cudaOccupancyMaxActiveClusters(&m, kern, &cfg) != cudaSuccess) {
         (void)cudaGetLastError();
         m = 0;
       }
+      cached_dev = dev;
       cached_c = c;
       cached_smem = smem;
       cached_max = m;

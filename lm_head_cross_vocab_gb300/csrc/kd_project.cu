@@ -841,9 +841,12 @@ bool x_plan(int64_t vt, int64_t vs, XPlan* P) {
     return false;
   }
   // co-resident clusters of this shape (cached per cluster size and buffer)
-  static int cached_c = 0, cached_max = 0;
+  // (per template instance; keyed by device, cluster size and buffer bytes)
+  static int cached_dev = -1, cached_c = 0, cached_max = 0;
   static size_t cached_smem = 0;
-  if (cached_c != P->C || cached_smem != P->smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (cached_dev != dev || cached_c != P->C || cached_smem != P->smem) {
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cudaLaunchAttribute attr[1];
@@ -862,6 +865,7 @@ bool x_plan(int64_t vt, int64_t vs, XPlan* P) {
       (void)cudaGetLastError();
       m = 0;
     }
+    cached_dev = dev;
     cached_c = P->C;
     cached_smem = P->smem;
     cached_max = m;
