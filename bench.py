@@ -234,6 +234,20 @@ def run_reference(args, w: I.Workload, rank: int):
 
 # ---------------------------------------------------------------- GPU arm
 
+def time_cpu_oracle(fn, seconds):
+    """Tokens/s of fn(rows) (the CPU oracle on a seeded sample of `rows` token
+    rows), the sample grown from 8 rows until one call takes about `seconds`;
+    returns (rate, rows, elapsed)."""
+    rows = 8
+    while True:
+        t0 = time.perf_counter()
+        fn(rows)
+        dt = time.perf_counter() - t0
+        if dt >= seconds or rows >= 4096:
+            return rows / dt, rows, dt
+        rows = min(4096, rows * 4, max(rows * 2, int(rows * seconds / max(dt, 1e-3))))
+
+
 def run_projection(args, rank):
     """Cross-vocabulary token-map projection (kd_project_teacher_logits) on a
     synthetic cross-tokenizer case: bf16 teacher logits ~N(0,4) over a
@@ -262,13 +276,26 @@ def run_projection(args, rank):
     torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = kd.kd_launch_count()
-    s.record()
-    for _ in range(args.steps):
-        out = kd.project_teacher_logits(tmap_d, z, v_s, temperature=2.0, workspace=ws,
-                                        check=False)
-    e.record()
-    torch.cuda.synchronize()
+    with ClockSampler(0) as clk:
+        s.record()
+        for _ in range(args.steps):
+            out = kd.project_teacher_logits(tmap_d, z, v_s, temperature=2.0, workspace=ws,
+                                            check=False)
+        e.record()
+        torch.cuda.synchronize()
     ms = s.elapsed_time(e) / args.steps
+    cpu_base = None
+    if rank == 0 and not args.no_cpu_baseline:
+        from oracle import kd_oracle as O
+        gc = torch.Generator().manual_seed(1007)
+
+        def oracle(rows):
+            O.project_teacher_logits((torch.randn(rows, v_t, generator=gc) * 4.0).to(
+                torch.bfloat16), tmap, v_s, temperature=2.0)
+        v_cpu, rows, dt = time_cpu_oracle(oracle, min(args.cpu_seconds, 6.0))
+        cpu_base = {"value": v_cpu, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+                    "sample": f"{rows} seeded token rows of the same map, fp64 numpy oracle "
+                              f"({dt:.1f} s)"}
     nbytes = n * v_t * 2 + n * v_s * 2  # teacher logits read once, projected logits written
     peaks, peak_src = load_peaks()
     gbs = nbytes / (ms / 1e3) / 1e9
@@ -286,6 +313,7 @@ def run_projection(args, rank):
                          "bytes_per_launch": nbytes,
                          "traffic": None if args.tokens else
                          load_traffic("project").get("cross_vocab_projection:k_project")},
+            "cpu_baseline": cpu_base, "clocks": clk.summary(),
             "gpu_launches": kd.kd_launch_count() - launches0}), flush=True)
 
 
@@ -306,12 +334,25 @@ def run_mix(args, rank):
     torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = kd.kd_launch_count()
-    s.record()
-    for _ in range(args.steps):
-        out = kd.mix_teacher_logits(zs, w, args.mix, check=False)
-    e.record()
-    torch.cuda.synchronize()
+    with ClockSampler(0) as clk:
+        s.record()
+        for _ in range(args.steps):
+            out = kd.mix_teacher_logits(zs, w, args.mix, check=False)
+        e.record()
+        torch.cuda.synchronize()
     ms = s.elapsed_time(e) / args.steps
+    cpu_base = None
+    if rank == 0 and not args.no_cpu_baseline:
+        from oracle import kd_oracle as O
+        gc = torch.Generator().manual_seed(2719)
+
+        def oracle(rows):
+            O.mix_teacher_logits([(torch.randn(rows, v, generator=gc) * sd).to(torch.bfloat16)
+                                  for sd in (2.0, 3.0)], w, args.mix)
+        v_cpu, rows, dt = time_cpu_oracle(oracle, min(args.cpu_seconds, 6.0))
+        cpu_base = {"value": v_cpu, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+                    "sample": f"{rows} seeded token rows of two teachers, fp64 numpy oracle "
+                              f"({dt:.1f} s)"}
     nbytes = 2 * n * v * 2 + n * v * 2  # both teachers read once, the mixture written once
     peaks, peak_src = load_peaks()
     gbs = nbytes / (ms / 1e3) / 1e9
@@ -327,6 +368,7 @@ def run_mix(args, rank):
                          "peak_source": f"{peak_src} copy", "bytes_per_launch": nbytes,
                          "traffic": None if args.tokens else
                          load_traffic("mix").get(f"mix_2_teachers_{args.mix}:k_mix")},
+            "cpu_baseline": cpu_base, "clocks": clk.summary(),
             "gpu_launches": kd.kd_launch_count() - launches0}), flush=True)
     del out
 
