@@ -109,6 +109,77 @@ __global__ void __launch_bounds__(1024) k_map_scan(const int32_t* __restrict__ c
   if (t == 0) off[vs] = carry;
 }
 
+// Multi-block form of the same exclusive scan, for long arrays: tile sums
+// (k_scan_tiles), the scan of those sums (k_map_scan on them), then every
+// tile scanned from its offset (k_scan_apply).  Tiles are 4096 entries.
+constexpr int kScanTile = 4096;
+
+__device__ __forceinline__ void load4(const int32_t* __restrict__ in, int64_t i, int64_t n,
+                                      int32_t v[4]) {
+  if (i + 4 <= n) {  // in is 256-byte aligned and i a multiple of 4
+    const int4 q = *reinterpret_cast<const int4*>(in + i);
+    v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = i + k < n ? in[i + k] : 0;
+  }
+}
+
+__global__ void __launch_bounds__(1024) k_scan_tiles(const int32_t* __restrict__ in, int64_t n,
+                                                     int32_t* __restrict__ tsum) {
+  __shared__ int32_t ws[32];
+  const int64_t i = (int64_t)blockIdx.x * kScanTile + 4 * (int64_t)threadIdx.x;
+  int32_t v[4];
+  load4(in, i, n, v);
+  int32_t x = v[0] + v[1] + v[2] + v[3];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  if ((threadIdx.x & 31) == 0) ws[threadIdx.x >> 5] = x;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    int32_t y = ws[threadIdx.x];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
+    if (threadIdx.x == 0) tsum[blockIdx.x] = y;
+  }
+}
+
+__global__ void __launch_bounds__(1024) k_scan_apply(const int32_t* __restrict__ in, int64_t n,
+                                                     const int32_t* __restrict__ toff,
+                                                     int32_t* __restrict__ out) {
+  __shared__ int32_t wsum[32];
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int64_t i = (int64_t)blockIdx.x * kScanTile + 4 * (int64_t)t;
+  int32_t v[4];
+  load4(in, i, n, v);
+  const int32_t own = v[0] + v[1] + v[2] + v[3];
+  int32_t inc = own;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t u = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += u;
+  }
+  if (lane == 31) wsum[w] = inc;
+  __syncthreads();
+  if (w == 0) {
+    int32_t x = wsum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t u = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += u;
+    }
+    wsum[lane] = x;
+  }
+  __syncthreads();
+  int32_t run = toff[blockIdx.x] + (w > 0 ? wsum[w - 1] : 0) + inc - own;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if (i + k < n) out[i + k] = run;
+    run += v[k];
+  }
+  if (blockIdx.x == 0 && t == 0) out[n] = toff[gridDim.x];
+}
+
 // one[i] for student id i: its teacher column when exactly one teacher token
 // maps to it, -1 when none does, -2 when several do; eid[e]: the student id of
 // map edge e (the e-th entry of the id-sorted column list).
@@ -779,7 +850,7 @@ int slices_for(int64_t vt, int64_t elem, int64_t* sc) {
 
 struct ProjLayout {
   size_t cnt, off, cols, one, list_id, list_val, slice_cnt, slice_off, eid, epos, code, send_src,
-      mflag, mpre, mlist, mcode, xl, bytes;
+      mflag, mpre, mlist, mcode, stmp, xl, bytes;
 };
 ProjLayout proj_layout(int64_t vt, int64_t vs) {
   ProjLayout L;
@@ -799,7 +870,8 @@ ProjLayout proj_layout(int64_t vt, int64_t vs) {
   L.mpre = align256(L.mflag + (size_t)vs * 4);
   L.mlist = align256(L.mpre + (size_t)(vs + 1) * 4);
   L.mcode = align256(L.mlist + (size_t)vs * 4);
-  L.xl = align256(L.mcode + (size_t)vs * 4);
+  L.stmp = align256(L.mcode + (size_t)vs * 4);
+  L.xl = align256(L.stmp + (size_t)(2 * (vs / kScanTile + 2)) * 4);
   L.bytes = align256(L.xl + sizeof(XLayout));
   return L;
 }
@@ -918,6 +990,25 @@ int launch_project(const void* zt, int64_t n, int64_t vt, int64_t vs, float inv_
   return cudaGetLastError() != cudaSuccess;
 }
 
+// out[0..n] = exclusive scan of in[0..n) with tile sums in tmp (2 * (n /
+// kScanTile + 2) entries); one CTA does it alone when there is one tile.
+void launch_scan(const int32_t* in, int64_t n, int32_t* out, int32_t* tmp, cudaStream_t s) {
+  const int64_t tiles = (n + kScanTile - 1) / kScanTile;
+  if (tiles <= 1) {
+    note_launch();
+    k_map_scan<<<1, 1024, 0, s>>>(in, n, out);
+    return;
+  }
+  int32_t* tsum = tmp;
+  int32_t* toff = tmp + tiles + 1;
+  note_launch();
+  k_scan_tiles<<<(unsigned)tiles, 1024, 0, s>>>(in, n, tsum);
+  note_launch();
+  k_map_scan<<<1, 1024, 0, s>>>(tsum, tiles, toff);
+  note_launch();
+  k_scan_apply<<<(unsigned)tiles, 1024, 0, s>>>(in, n, toff, out);
+}
+
 // the launches of one call, per dtype pair
 struct ProjRun {
   const void* zt;
@@ -999,6 +1090,7 @@ kd_status kd_project_teacher_logits(const int32_t* token_map, int64_t v_teacher,
   int32_t* mpre = reinterpret_cast<int32_t*>(ws + L.mpre);
   int32_t* mlist = reinterpret_cast<int32_t*>(ws + L.mlist);
   int32_t* mcode = reinterpret_cast<int32_t*>(ws + L.mcode);
+  int32_t* stmp = reinterpret_cast<int32_t*>(ws + L.stmp);
   XLayout* X = reinterpret_cast<XLayout*>(ws + L.xl);
   bool (*plan)(int64_t, int64_t, XPlan*);
   int (*run)(const XPlan*, const ProjRun&);
@@ -1021,8 +1113,7 @@ kd_status kd_project_teacher_logits(const int32_t* token_map, int64_t v_teacher,
     return KD_ERR_CUDA;
   note_launch();
   k_map_count<<<gmap, kT, 0, s>>>(token_map, v_teacher, v_student, cnt, dev_status);
-  note_launch();
-  k_map_scan<<<1, 1024, 0, s>>>(cnt, v_student, off);
+  launch_scan(cnt, v_student, off, stmp, s);
   if (cudaMemsetAsync(cnt, 0, (size_t)v_student * 4, s) != cudaSuccess) return KD_ERR_CUDA;
   note_launch();
   k_map_scatter<<<gmap, kT, 0, s>>>(token_map, v_teacher, v_student, off, cnt, cols);
@@ -1047,8 +1138,7 @@ kd_status kd_project_teacher_logits(const int32_t* token_map, int64_t v_teacher,
     k_exchange_codes<<<gid, kT, 0, s>>>(off, epos, v_student, code);
     note_launch();
     k_multi_flag<<<gid, kT, 0, s>>>(code, v_student, mflag);
-    note_launch();
-    k_map_scan<<<1, 1024, 0, s>>>(mflag, v_student, mpre);
+    launch_scan(mflag, v_student, mpre, stmp, s);
     note_launch();
     k_multi_scatter<<<gid, kT, 0, s>>>(code, mpre, v_student, mlist, mcode);
   }
