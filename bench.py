@@ -234,6 +234,13 @@ def run_reference(args, w: I.Workload, rank: int):
 
 # ---------------------------------------------------------------- GPU arm
 
+def smi_index(local: int) -> int:
+    """nvidia-smi index of this process's GPU (the first CUDA_VISIBLE_DEVICES
+    entry when it is numeric, else the local rank)."""
+    first = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0]
+    return int(first) if first.isdigit() else local
+
+
 def time_cpu_oracle(fn, seconds):
     """Tokens/s of fn(rows) (the CPU oracle on a seeded sample of `rows` token
     rows), the sample grown from 8 rows until one call takes about `seconds`;
@@ -276,7 +283,7 @@ def run_projection(args, rank):
     torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = kd.kd_launch_count()
-    with ClockSampler(0) as clk:
+    with ClockSampler(smi_index(0)) as clk:
         s.record()
         for _ in range(args.steps):
             out = kd.project_teacher_logits(tmap_d, z, v_s, temperature=2.0, workspace=ws,
@@ -334,7 +341,7 @@ def run_mix(args, rank):
     torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = kd.kd_launch_count()
-    with ClockSampler(0) as clk:
+    with ClockSampler(smi_index(0)) as clk:
         s.record()
         for _ in range(args.steps):
             out = kd.mix_teacher_logits(zs, w, args.mix, check=False)
@@ -466,8 +473,7 @@ def main():
             e.record()  # materialise the handles
     torch.cuda.synchronize()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0] or 0) \
-        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local
+    gpu_index = smi_index(local)
     launches0 = kd.kd_launch_count()
     with ClockSampler(gpu_index) as clk:
         if dist:
