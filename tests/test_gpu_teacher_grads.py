@@ -100,3 +100,13 @@ def test_teacher_grads_need_the_workspace_flag():
     fwd = kd.forward(prob, t)
     with pytest.raises(kd.KDError):
         kd.backward(prob, t, fwd["stats"], want=("h_s", "h_t"))
+
+
+@pytest.mark.parametrize("streams", ["1", "2"])
+def test_separate_teacher_grads_bf16_stream_schedules(streams, monkeypatch):
+    """The teacher GEMMs on the backward's single-stream and two-stream
+    schedules (KD_BWD_STREAMS, read on every call), several chunks each way."""
+    monkeypatch.setenv("KD_BWD_STREAMS", streams)
+    w = W[2].scaled(n_tokens=300, d_student=64, d_teacher=128, vocab=1100)
+    got, ref, valid = _run(w, vocab_chunk=256, seq_chunk=128)
+    _check(got, ref, valid, "bf16")
