@@ -34,7 +34,8 @@ namespace {
 constexpr int kMaxT = KD_MIX_MAX_TEACHERS;
 constexpr int kMT = 512;                  // threads per CTA (two CTAs per SM)
 constexpr int kMW = kMT / 32;             // warps per CTA
-constexpr int64_t kMixBuf = 100 * 1024;   // bytes of staged teacher rows per CTA
+constexpr int64_t kMixBuf = 100 * 1024;   // bytes of staged teacher rows per CTA (two per SM)
+constexpr int64_t kMixBufWide = 200 * 1024;  // one CTA per SM, for longer rows
 constexpr float kLN2 = 0.6931471805599453f;
 
 struct MixParams {
@@ -315,8 +316,8 @@ __device__ __forceinline__ void pass2_8(const MixParams& P, const TI* zs, const 
 // before it writes the second.  So the staging of the next row runs under
 // this row's pass 2 and the next row's pass 1, and two CTAs share an SM, so
 // one CTA's waits are the other's compute.
-template <typename TI, typename TO, bool GEO>
-__global__ void __launch_bounds__(kMT, 2) k_mix_cluster(const MixParams P) {
+template <typename TI, typename TO, bool GEO, bool WIDE>
+__global__ void __launch_bounds__(kMT, WIDE ? 1 : 2) k_mix_cluster(const MixParams P) {
   extern __shared__ __align__(16) uint8_t mix_smem[];
   __shared__ __align__(8) uint64_t bars[2];  // one per half
   __shared__ Lse red_all[kMW][kMaxT];   // per warp and stream
@@ -500,15 +501,16 @@ __global__ void __launch_bounds__(kMT) k_mix_rows(const MixParams P) {
   }
 }
 
-// smallest cluster (1, 2, 4, 8, 16 CTAs) whose per-CTA columns of all K
-// teachers, sc a multiple of 8, fit the staging budget; 0 when none does.
+// smallest cluster (1, 2, 4 or 8 CTAs) whose per-CTA columns of all K
+// teachers, sc a multiple of 8, fit `budget` bytes; 0 when none does.
 // (Smaller clusters win over whole-row double buffering: more SMs can host
 // them, and the per-row cluster barrier and reductions cost less; the
-// two-half staging hides most of the copies instead.)
-int mix_cluster_for(int64_t v, int k, int64_t elem, int64_t* sc) {
-  for (int c = 1; c <= 16; c *= 2) {
+// two-half staging hides most of the copies instead.  Clusters of 16 CTAs
+// measured worse than one wide CTA per SM in clusters of 8.)
+int mix_cluster_for(int64_t v, int k, int64_t elem, int64_t budget, int64_t* sc) {
+  for (int c = 1; c <= 8; c *= 2) {
     const int64_t cols = ((v + c - 1) / c + 7) / 8 * 8;
-    if (cols * elem * k <= kMixBuf) {
+    if (cols * elem * k <= budget) {
       *sc = cols;
       return c;
     }
@@ -516,59 +518,68 @@ int mix_cluster_for(int64_t v, int k, int64_t elem, int64_t* sc) {
   return 0;
 }
 
+// The cluster kernel in one shape (WIDE: one CTA per SM and twice the
+// staging); returns 1 on a CUDA error, and sets *launched.
+template <typename TI, typename TO, bool GEO, bool WIDE>
+int launch_mix_cluster(MixParams P, int c, int64_t sc, cudaStream_t s, bool* launched) {
+  *launched = false;
+  const int nsm = tc_num_sms() > 0 ? tc_num_sms() : 1;
+  const size_t smem = (size_t)sc * sizeof(TI) * (size_t)P.k;
+  auto kern = k_mix_cluster<TI, TO, GEO, WIDE>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return 1;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)c;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kMT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // co-resident clusters of this shape (per template instance; keyed by
+  // device, cluster size and buffer bytes)
+  static int cached_dev = -1, cached_c = 0, cached_max = 0;
+  static size_t cached_smem = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cached_dev != dev || cached_c != c || cached_smem != smem) {
+    cfg.gridDim = dim3((unsigned)(c * std::max(1, (WIDE ? 1 : 2) * nsm / c)));
+    int m = 0;
+    if (cudaOccupancyMaxActiveClusters(&m, kern, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      m = 0;
+    }
+    cached_dev = dev;
+    cached_c = c;
+    cached_smem = smem;
+    cached_max = m;
+  }
+  if (cached_max <= 0) return 0;
+  P.sc = sc;
+  const int64_t clusters = P.n < cached_max ? P.n : cached_max;
+  cfg.gridDim = dim3((unsigned)(c * clusters));
+  note_launch();
+  if (cudaLaunchKernelEx(&cfg, kern, P) != cudaSuccess) return 1;
+  *launched = true;
+  return 0;
+}
+
 template <typename TI, typename TO, bool GEO>
 int launch_mix(MixParams P, cudaStream_t s) {
-  int64_t sc = 0;
-  const int c = mix_cluster_for(P.v, P.k, (int64_t)sizeof(TI), &sc);
   const int nsm = tc_num_sms() > 0 ? tc_num_sms() : 1;
-  if (c > 0) {
-    const size_t smem = (size_t)sc * sizeof(TI) * (size_t)P.k;
-    auto kern = k_mix_cluster<TI, TO, GEO>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return 1;
-    if (c > 8 &&
-        cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-            cudaSuccess)
-      return 1;
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof(cfg));
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)c;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kMT);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    // co-resident clusters of this shape (cached per cluster size and buffer)
-    // (per template instance; keyed by device, cluster size and buffer bytes)
-    static int cached_dev = -1, cached_c = 0, cached_max = 0;
-    static size_t cached_smem = 0;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-    if (cached_dev != dev || cached_c != c || cached_smem != smem) {
-      cfg.gridDim = dim3((unsigned)(c * std::max(1, 2 * nsm / c)));
-      int m = 0;
-      if (cudaOccupancyMaxActiveClusters(&m, kern, &cfg) != cudaSuccess) {
-        (void)cudaGetLastError();
-        m = 0;
-      }
-      cached_dev = dev;
-      cached_c = c;
-      cached_smem = smem;
-      cached_max = m;
-    }
-    if (cached_max > 0) {
-      P.sc = sc;
-      const int64_t clusters = P.n < cached_max ? P.n : cached_max;
-      cfg.gridDim = dim3((unsigned)(c * clusters));
-      note_launch();
-      return cudaLaunchKernelEx(&cfg, kern, P) != cudaSuccess;
-    }
-  }
+  int64_t sc = 0;
+  bool launched = false;
+  int c = mix_cluster_for(P.v, P.k, (int64_t)sizeof(TI), kMixBuf, &sc);
+  if (c > 0 && launch_mix_cluster<TI, TO, GEO, false>(P, c, sc, s, &launched)) return 1;
+  if (launched) return 0;
+  c = mix_cluster_for(P.v, P.k, (int64_t)sizeof(TI), kMixBufWide, &sc);
+  if (c > 0 && launch_mix_cluster<TI, TO, GEO, true>(P, c, sc, s, &launched)) return 1;
+  if (launched) return 0;
   const int grid = (int)std::min<int64_t>(P.n, (int64_t)nsm * 2);
   note_launch();
   k_mix_rows<TI, TO, GEO><<<grid, kMT, 0, s>>>(P);
