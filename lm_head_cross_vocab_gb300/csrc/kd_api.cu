@@ -14,6 +14,7 @@
 
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 using namespace kd;
 
@@ -22,6 +23,36 @@ namespace {
 std::atomic<uint64_t> g_launches{0};
 }
 void note_launch(int k) { g_launches.fetch_add((uint64_t)k, std::memory_order_relaxed); }
+
+int max_active_clusters(const void* kern, const cudaLaunchConfig_t& cfg) {
+  struct Entry {
+    const void* kern;
+    int dev;
+    unsigned cluster;
+    size_t smem;
+    int value;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  unsigned cluster = 1;
+  for (unsigned i = 0; i < cfg.numAttrs; ++i)
+    if (cfg.attrs[i].id == cudaLaunchAttributeClusterDimension)
+      cluster = cfg.attrs[i].val.clusterDim.x * cfg.attrs[i].val.clusterDim.y *
+                cfg.attrs[i].val.clusterDim.z;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& e : cache)
+    if (e.kern == kern && e.dev == dev && e.cluster == cluster && e.smem == cfg.dynamicSmemBytes)
+      return e.value;
+  int m = 0;
+  if (cudaOccupancyMaxActiveClusters(&m, kern, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    m = 0;
+  }
+  cache.push_back(Entry{kern, dev, cluster, cfg.dynamicSmemBytes, m});
+  return m;
+}
 }  // namespace kd
 
 namespace {

@@ -14,6 +14,13 @@ namespace kd {
 // Count `k` kernel launches (reported by kd_launch_count()).
 void note_launch(int k = 1);
 
+// Clusters of `kern` that can be co-resident on the current device when it is
+// launched with `cfg` (its cluster dimension attribute and dynamic shared
+// memory); 0 if the query fails.  Cached per (kernel, device, cluster size,
+// shared memory bytes) under a mutex, so host threads driving different
+// devices at the same time each see their own device's answer.
+int max_active_clusters(const void* kern, const cudaLaunchConfig_t& cfg);
+
 // ---------------------------------------------------------------- aux kernels
 // Count valid labels into *count (int32, zeroed by the caller) and flag bad ones.
 void launch_label_check(const int64_t* labels, int64_t n, int64_t vocab, int64_t ignore,

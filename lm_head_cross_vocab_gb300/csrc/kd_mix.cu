@@ -9,13 +9,16 @@
 // most negative finite value of the output type, as the projection writes it.
 //
 // Every output needs the logsumexp of whole teacher rows (or of g).  A cluster
-// of C CTAs (C = 1, 2, 4, 8 or 16) therefore holds one token row of all K
+// of C CTAs (C = 1, 2, 4 or 8) therefore holds one token row of all K
 // teachers in shared memory -- CTA r columns [r*sc, r*sc + sc), one bulk copy
 // per teacher -- reduces its columns to a (max, sum of exp) pair per stream,
 // exchanges the pairs through distributed shared memory, and writes its
 // columns of the output with vector stores: each input byte is read from HBM
-// once and each output byte written once.  Rows too long for a 16-CTA cluster
-// take a one-CTA-per-row kernel that reads the row from global memory twice.
+// once and each output byte written once.  Two shapes exist: two CTAs per SM
+// with 100 KiB of staging each, and, for rows that need more than 8 x 100 KiB,
+// a wide shape of one CTA per SM with 200 KiB.  Rows too long for an 8-CTA
+// cluster of the wide shape take a one-CTA-per-row kernel that reads the row
+// from global memory twice.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -541,24 +544,10 @@ int launch_mix_cluster(MixParams P, int c, int64_t sc, cudaStream_t s, bool* lau
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // co-resident clusters of this shape (per template instance; keyed by
-  // device, cluster size and buffer bytes)
-  static int cached_dev = -1, cached_c = 0, cached_max = 0;
-  static size_t cached_smem = 0;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-  if (cached_dev != dev || cached_c != c || cached_smem != smem) {
-    cfg.gridDim = dim3((unsigned)(c * std::max(1, (WIDE ? 1 : 2) * nsm / c)));
-    int m = 0;
-    if (cudaOccupancyMaxActiveClusters(&m, kern, &cfg) != cudaSuccess) {
-      (void)cudaGetLastError();
-      m = 0;
-    }
-    cached_dev = dev;
-    cached_c = c;
-    cached_smem = smem;
-    cached_max = m;
-  }
+  // co-resident clusters of this shape (cached per device, cluster size and
+  // buffer bytes)
+  cfg.gridDim = dim3((unsigned)(c * std::max(1, (WIDE ? 1 : 2) * nsm / c)));
+  const int cached_max = max_active_clusters(reinterpret_cast<const void*>(kern), cfg);
   if (cached_max <= 0) return 0;
   P.sc = sc;
   const int64_t clusters = P.n < cached_max ? P.n : cached_max;

@@ -912,36 +912,22 @@ bool x_plan(int64_t vt, int64_t vs, XPlan* P) {
     (void)cudaGetLastError();
     return false;
   }
-  // co-resident clusters of this shape (cached per cluster size and buffer)
-  // (per template instance; keyed by device, cluster size and buffer bytes)
-  static int cached_dev = -1, cached_c = 0, cached_max = 0;
-  static size_t cached_smem = 0;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  if (cached_dev != dev || cached_c != P->C || cached_smem != P->smem) {
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof(cfg));
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)P->C;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    const int nsm = tc_num_sms() > 0 ? tc_num_sms() : 1;
-    cfg.gridDim = dim3((unsigned)(P->C * std::max(1, nsm / P->C)));
-    cfg.blockDim = dim3(kPT);
-    cfg.dynamicSmemBytes = P->smem;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int m = 0;
-    if (cudaOccupancyMaxActiveClusters(&m, kern, &cfg) != cudaSuccess) {
-      (void)cudaGetLastError();
-      m = 0;
-    }
-    cached_dev = dev;
-    cached_c = P->C;
-    cached_smem = P->smem;
-    cached_max = m;
-  }
+  // co-resident clusters of this shape (cached per device, cluster size and
+  // buffer bytes)
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)P->C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  const int nsm = tc_num_sms() > 0 ? tc_num_sms() : 1;
+  cfg.gridDim = dim3((unsigned)(P->C * std::max(1, nsm / P->C)));
+  cfg.blockDim = dim3(kPT);
+  cfg.dynamicSmemBytes = P->smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int cached_max = max_active_clusters(reinterpret_cast<const void*>(kern), cfg);
   P->max_clusters = cached_max;
   return cached_max > 0;
 }

@@ -1050,7 +1050,6 @@ template <int EPI, int BN, bool HAS_T, bool PAIR>
 int launch(const TcParams& P, int num_sms, cudaStream_t s) {
   using C = Cfg<BN, PAIR>;
   auto kern = k_tc<EPI, BN, HAS_T, PAIR>;
-  static int max_clusters = -1;  // co-resident CTA pairs (cached per instantiation)
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return (int)e;
@@ -1073,12 +1072,9 @@ int launch(const TcParams& P, int num_sms, cudaStream_t s) {
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (max_clusters < 0) {
-    cfg.gridDim = dim3(2 * (num_sms / 2));
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = num_sms / 2;
-    max_clusters = n;
-  }
+  cfg.gridDim = dim3(2 * (num_sms / 2));
+  int max_clusters = max_active_clusters(reinterpret_cast<const void*>(kern), cfg);
+  if (max_clusters <= 0) max_clusters = num_sms / 2;
   const int clusters = P.items < max_clusters ? P.items : max_clusters;
   cfg.gridDim = dim3(2 * clusters);
   note_launch();

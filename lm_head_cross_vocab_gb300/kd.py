@@ -324,8 +324,12 @@ def check_status(dev_status: torch.Tensor, assume_valid: bool = False):
 
 
 def forward(problem: Problem, tensors: dict, workspace: Optional[Workspace] = None,
-            check: bool = True, out: Optional[dict] = None):
-    """Run kd_fwd; returns dict(ce_s, ce_t, kl, stats, loss, dev_status)."""
+            check: bool = True, out: Optional[dict] = None, save_stats: bool = True):
+    """Run kd_fwd; returns dict(ce_s, ce_t, kl, stats, loss, dev_status).
+
+    save_stats=False is forward-only scoring (flash_kd API doc: only the
+    forward pass exists, scoring runs without gradients): no per-token
+    statistics are kept for a backward, and ``stats`` is None."""
     dev = _device_of(tensors)
     n = problem.n_tokens
     if out is None:
@@ -333,7 +337,8 @@ def forward(problem: Problem, tensors: dict, workspace: Optional[Workspace] = No
             "ce_s": torch.empty(n, device=dev, dtype=torch.float32),
             "ce_t": torch.empty(n, device=dev, dtype=torch.float32),
             "kl": torch.empty(n, device=dev, dtype=torch.float32),
-            "stats": torch.empty(n, KD_STATS_PER_TOKEN, device=dev, dtype=torch.float32),
+            "stats": (torch.empty(n, KD_STATS_PER_TOKEN, device=dev, dtype=torch.float32)
+                      if save_stats else None),
             "loss": torch.empty((), device=dev, dtype=torch.float32),
             "dev_status": torch.zeros((), device=dev, dtype=torch.int32),
         }

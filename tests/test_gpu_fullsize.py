@@ -5,7 +5,16 @@
   every gradient element against the oracle, evaluated in row blocks;
 * top-K (32768 tokens, V 151936), scoring (8192 tokens, V 248320) and logit pairs
   (16384 tokens, V 128256): the oracle evaluates a seeded sample of tokens one by one
-  (row-local quantities: per-token CE / KL, dH rows, d z_s rows).
+  (row-local quantities: per-token CE / KL, dH rows, d z_s rows);
+* top-K dW [151936, 4096]: every row of dW sums over all 32768 tokens, and each
+  token's G row needs its full logsumexp (1.2 GFLOP per token, 41 TFLOP for the
+  batch: out of reach of the fp64 oracle on the host).  The test therefore keeps
+  the full-size launch (32768 tokens in 16 sequence chunks, fp32 accumulation of
+  dW across the chunks) but gives only a seeded set of tokens, spread over every
+  chunk, a non-zero teacher: a token whose top-K probabilities are all 0 has
+  M = 0 and a G row of exactly 0 (Full-Chunked-KL-Loss README, "Full Chunked
+  KL": G = M softmax(z) - p), so dW is the sum over the chosen tokens alone,
+  which the oracle evaluates in full.
 """
 import numpy as np
 import pytest
@@ -74,7 +83,7 @@ def _sample(n, k, seed):
 def test_fullsize_topk_sampled_tokens():
     w = W[4]
     t, prob, fwd, bwd = _run(w)
-    rows = _sample(w.n_tokens, 12, 4)
+    rows = _sample(w.n_tokens, 32, 4)
     cpu = {k: t[k][rows].cpu() for k in ("h_s", "topk_idx", "topk_p")}
     w_s = t["w_s"].cpu()
     z = O.project(cpu["h_s"], w_s)
@@ -94,7 +103,7 @@ def test_fullsize_topk_sampled_tokens():
 def test_fullsize_scoring_sampled_tokens():
     w = W[3]
     t, prob, fwd, _ = _run(w, backward=False)
-    rows = _sample(w.n_tokens, 12, 3)
+    rows = _sample(w.n_tokens, 48, 3)
     z_s = O.as_f64(t["logits_s"][rows].cpu())
     z_t = O.project(t["h_t"][rows].cpu(), t["w_t"].cpu())
     labels = t["labels"][rows].cpu().numpy()
@@ -105,7 +114,8 @@ def test_fullsize_scoring_sampled_tokens():
         assert err <= TOK_TOL["bf16"], (key, err)
 
 
-@pytest.mark.parametrize("variant", ["forward", "reverse", "skew_js"])
+@pytest.mark.parametrize("variant", ["forward", "reverse", "jeffreys", "skew_js", "skew_forward",
+                                     "skew_reverse"])
 def test_fullsize_logit_pair_sampled_tokens(variant):
     w = W[5].scaled(variant=variant)
     t, prob, fwd, bwd = _run(w)
@@ -122,3 +132,53 @@ def test_fullsize_logit_pair_sampled_tokens(variant):
     g, _ = O.grad_logits(z_s, z_t, labels, **kw)
     got = bwd["d_logits_s"][rows].cpu().double().numpy()
     assert rel_l2(got, g / n_valid) <= GRAD_TOL["bf16"]
+
+
+def test_fullsize_topk_dw_from_chosen_tokens():
+    """Full-size top-K backward, dW and dH compared in full with the oracle.
+
+    256 seeded tokens (16 in each 2048-token sequence chunk) keep their teacher;
+    every other token gets top-K probabilities of 0 (same ids), so its G row is 0
+    and dW = sum over the chosen tokens of G[n]^T H[n]."""
+    w = W[4]
+    t = I.make_inputs(w, "cuda")
+    chunk = w.seq_chunk
+    rng = np.random.default_rng(44)
+    rows = np.sort(np.concatenate([c0 + rng.choice(chunk, 16, replace=False)
+                                   for c0 in range(0, w.n_tokens, chunk)]))
+    keep = torch.zeros(w.n_tokens, dtype=torch.bool, device="cuda")
+    keep[torch.from_numpy(rows).cuda()] = True
+    t["topk_p"] = torch.where(keep[:, None], t["topk_p"], torch.zeros_like(t["topk_p"]))
+    prob = kd.problem_for(w, vocab_chunk=0, seq_chunk=0)
+    fwd = kd.forward(prob, t)
+    bwd = kd.backward(prob, t, fwd["stats"], want=("h_s", "w_s"))
+    torch.cuda.synchronize()
+    # oracle on the chosen tokens (the mean divides by all 32768 tokens)
+    h = t["h_s"][rows].cpu()
+    w_s = t["w_s"].cpu()
+    z = O.project(h, w_s)
+    idx, p = t["topk_idx"][rows].cpu().numpy(), t["topk_p"][rows].cpu().numpy()
+    kw = {**oracle_kwargs(w, prob), "reduction": "sum"}
+    out = O.forward(z, None, None, topk_idx=idx, topk_p=p, **kw)
+    err = token_rel_err(fwd["kl"][rows].cpu().double().numpy(), out["kl"],
+                        np.ones(len(rows), bool))
+    assert err <= TOK_TOL["bf16"], err
+    assert not fwd["kl"].cpu()[~keep.cpu()].any(), "M = 0 tokens have a loss of exactly 0"
+    g, _ = O.grad_logits(z, None, None, topk_idx=idx, topk_p=p, **kw)
+    g /= w.n_tokens
+    del z
+    w64 = O.as_f64(w_s)
+    d_h = g @ w64
+    gh = bwd["d_h_s"].cpu()
+    assert rel_l2(gh[rows].double().numpy(), d_h) <= GRAD_TOL["bf16"]
+    assert not gh[~keep.cpu()].any(), "M = 0 tokens have dH rows of exactly 0"
+    # dW in vocabulary blocks: ||got - ref||_2 / ||ref||_2 over the whole matrix
+    h64 = O.as_f64(h)
+    gw = bwd["d_w_s"].cpu()
+    num = den = 0.0
+    for v0 in range(0, w.vocab, 8192):
+        ref = g[:, v0:v0 + 8192].T @ h64
+        got = gw[v0:v0 + 8192].double().numpy()
+        num += float(np.sum((got - ref) ** 2))
+        den += float(np.sum(ref ** 2))
+    assert np.sqrt(num / den) <= GRAD_TOL["bf16"], np.sqrt(num / den)

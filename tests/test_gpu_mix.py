@@ -49,13 +49,16 @@ def _check(got, ref, dout):
 @pytest.mark.parametrize("mode", ["arithmetic", "geometric"])
 @pytest.mark.parametrize("din,dout", [("fp32", "fp32"), ("bf16", "fp32"), ("bf16", "bf16")])
 @pytest.mark.parametrize("k,v,n", [(1, 1000, 37), (2, 513, 37), (3, 30000, 9), (2, 151936, 4),
-                                   (4, 151936, 3), (8, 70001, 3), (8, 151936, 2),
-                                   (2, 20000, 300)])
+                                   (3, 151936, 5), (4, 151936, 3), (8, 70001, 3),
+                                   (8, 151936, 2), (2, 20000, 300)])
 def test_mix_matches_oracle(mode, din, dout, k, v, n):
     """One CTA per row (1000 / 513 ids, the latter unaligned; double-buffered),
-    clusters of 2 to 16 CTAs (30000 to 151936 ids, 2 to 8 teachers), rows too
-    long for a 16-CTA cluster on the row kernel (8 teachers of 151936 ids in
-    bf16 and fp32), and 300 rows per launch, double- and single-buffered."""
+    clusters of 2 to 8 CTAs at two CTAs per SM (30000 to 151936 ids, 2 to 8
+    teachers), the wide one-CTA-per-SM shape for rows that need more than
+    8 x 100 KiB (three or four teachers of 151936 ids in bf16; in fp32 these
+    take the row kernel), rows too long for an 8-CTA wide cluster on the row
+    kernel (8 teachers of 151936 ids), and 300 rows per launch, double- and
+    single-buffered."""
     zs = _teachers(k, v, n, din, seed=k * 1000 + v)
     rng = np.random.default_rng(v)
     w = rng.uniform(0.2, 2.0, size=k)
