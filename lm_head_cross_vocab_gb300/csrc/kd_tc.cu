@@ -16,7 +16,11 @@
 //
 // Roles (320 threads): warp 0 issues TMA loads into a STAGES-deep shared
 // memory ring; warp 1 owns the TMEM allocation (512 columns: one or two
-// accumulator stages) and issues tcgen05.mma from one lane; warps 2..9 drain
+// accumulator stages) and issues tcgen05.mma; both warps run their loops
+// converged, with warp-uniform operands, and one lane picked by elect.sync
+// issues each copy, MMA and commit (a branch on lane 0 instead put the
+// descriptors in per-thread registers and cost 10-15 % of the tensor pipe's
+// time on GB300); warps 2..9 drain
 // TMEM with tcgen05.ld (warp w reads TMEM lanes 32*(w%4).., half (w-2)/4 of
 // the tile's columns); with two stages the epilogue of tile i overlaps the
 // MMAs of tile i+1.
@@ -64,10 +68,6 @@ __device__ __forceinline__ uint64_t globaltimer() {
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
 }
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -81,14 +81,6 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
-      : "memory");
 }
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -108,19 +100,6 @@ __device__ __forceinline__ void tmem_relinquish() {
 }
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
-}
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
-}
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
 }
 // ---- CTA-pair (cta_group::2) forms
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -153,15 +132,6 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
                : "memory");
 }
-// TMA load into this CTA's shared memory, completing on a barrier of either CTA
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
-                                                 uint32_t bar_cluster, int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
-      : "memory");
-}
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
                "r"(ncols));
@@ -172,27 +142,86 @@ __device__ __forceinline__ void tmem_relinquish_pair() {
 __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
 }
-__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                              uint32_t idesc, uint32_t accumulate) {
+
+// ---- issue forms for a whole warp: every lane executes them with the same
+// (warp-uniform) operands and elect.sync picks the one lane that issues, so
+// the operands stay in uniform registers and the issuing warps never diverge
+// around their TMA / MMA / commit instructions.  The elected lane is always the
+// lowest active one (lane 0 in a converged warp), so the commits track the
+// MMAs that lane issued.
+__device__ __forceinline__ void expect_tx_e(uint32_t bar, uint32_t bytes) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(bar), "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_e(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                              int x, int y) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];\n\t}" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+// TMA load into this CTA's shared memory, completing on a barrier of either
+// CTA of the pair
+__device__ __forceinline__ void tma_load_2d_pair_e(uint32_t dst, const CUtensorMap* map,
+                                                   uint32_t bar_cluster, int x, int y) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile"
+      ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];\n\t}" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void mma_bf16_e(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
+__device__ __forceinline__ void mma_bf16_pair_e(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_commit_e(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar)
+      : "memory");
+}
 // arrive on the barrier at this offset in both CTAs of the pair
-__device__ __forceinline__ void mma_commit_pair_both(uint32_t bar) {
+__device__ __forceinline__ void mma_commit_pair_both_e(uint32_t bar) {
   const uint16_t mask = 3;
   asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n\t}" ::"r"(bar),
       "h"(mask)
       : "memory");
 }
-__device__ __forceinline__ void mma_commit_pair_local(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
+__device__ __forceinline__ void mma_commit_pair_local_e(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar)
+      : "memory");
 }
 
 // 32 lanes x 16 consecutive 32-bit columns
@@ -294,39 +323,35 @@ struct Sync {
   bool cluster_acquire;  // waits on barriers the peer CTA arrives on remotely
 };
 
-// Lane 0 waits (bounded in time), the outcome is broadcast to the warp, and
-// then every lane tests the completed phase itself, so that each thread has
-// the acquire ordering of a successful try_wait before it touches the data the
-// barrier guards.
+// Every lane tests the phase (each successful try_wait gives that lane acquire
+// ordering on the data the barrier guards) and the warp leaves together once
+// all lanes have seen it complete; the phase stays complete until this warp
+// itself takes part in the next one, so no lane can miss it.  The wait is
+// bounded in time: lane 0 checks the clock every 64 rounds and the warp gives
+// up together.
 __device__ __forceinline__ bool warp_wait(const Sync& s, uint32_t bar, uint32_t parity,
                                           bool honour_abort = true) {
-  int ok = 1;
   auto probe = [&]() {
     return s.cluster_acquire ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity);
   };
-  if ((threadIdx.x & 31) == 0) {
-    if (!probe()) {
-      const uint64_t t0 = globaltimer();
-      ok = 0;
-      for (uint32_t it = 1;; ++it) {
-        if (probe()) {
-          ok = 1;
-          break;
-        }
-        if ((it & 63) == 0) {
-          if (honour_abort && *s.abort_flag) break;
-          if (globaltimer() - t0 > kWaitLimitNs) {
-            *s.abort_flag = 1;
-            set_status(s.status, KD_DEV_TIMEOUT);
-            break;
-          }
+  if (__all_sync(0xffffffffu, probe())) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (__all_sync(0xffffffffu, probe())) return true;
+    if ((it & 63) == 0) {
+      int give_up = 0;
+      if ((threadIdx.x & 31) == 0) {
+        if (honour_abort && *s.abort_flag) {
+          give_up = 1;
+        } else if (globaltimer() - t0 > kWaitLimitNs) {
+          *s.abort_flag = 1;
+          set_status(s.status, KD_DEV_TIMEOUT);
+          give_up = 1;
         }
       }
+      if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
     }
   }
-  const bool done = __shfl_sync(0xffffffffu, ok, 0) != 0;
-  if (done) probe();  // completed phase: succeeds at once, with acquire
-  return done;
 }
 
 // Items (row tile, vocabulary split) are ordered in bands of m_band row tiles:
@@ -670,17 +695,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
               ok = false;
               break;
             }
-            if (lane == 0) {
+            {  // the whole warp, one elected lane issuing
               const uint32_t fb = S.full + 8 * stage;
               const int ay = P.a_row0[sg] + m_tile * C::ROWS + (int)rank * BM;
               const int by = P.b_row0[sg] + t * BN + (int)rank * C::B_ROWS;
               // both CTAs' copies of a pair complete on the leader's barrier,
               // which expects the bytes of the whole pair
               const uint32_t fbar = PAIR ? mapa_shared(fb, 0) : fb;
-              if (!PAIR || leader) mbar_expect_tx(fb, C::TX_BYTES);
+              if (!PAIR || leader) expect_tx_e(fb, C::TX_BYTES);
               auto load = [&](uint32_t dst, const CUtensorMap* map, int x, int y) {
-                if (PAIR) tma_load_2d_pair(dst, map, fbar, x, y);
-                else tma_load_2d(dst, map, fbar, x, y);
+                if (PAIR) tma_load_2d_pair_e(dst, map, fbar, x, y);
+                else tma_load_2d_e(dst, map, fbar, x, y);
               };
               const uint32_t dA = sA + stage * C::A_BYTES, dB = sB + stage * C::B_BYTES;
               // only the plain GEMM takes MN-major operands
@@ -740,18 +765,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
               break;
             }
             tc_fence_after();
-            if (lane == 0) {
+            {  // the whole warp, one elected lane issuing
               const uint32_t a_addr = sA + stage * C::A_BYTES, b_addr = sB + stage * C::B_BYTES;
               const uint64_t ad = a_mn ? smem_desc_mn(a_addr) : smem_desc(a_addr);
               const uint64_t bd = b_mn ? smem_desc_mn(b_addr) : smem_desc(b_addr);
 #pragma unroll
               for (int k = 0; k < BK / 16; ++k) {
                 const uint32_t accum = (kb > 0 || k > 0 || P.seg_accum[sg]) ? 1u : 0u;
-                if (PAIR) mma_bf16_pair(d, ad + a_step * k, bd + b_step * k, idesc, accum);
-                else mma_bf16(d, ad + a_step * k, bd + b_step * k, idesc, accum);
+                if (PAIR) mma_bf16_pair_e(d, ad + a_step * k, bd + b_step * k, idesc, accum);
+                else mma_bf16_e(d, ad + a_step * k, bd + b_step * k, idesc, accum);
               }
-              if (PAIR) mma_commit_pair_both(S.empty + 8 * stage);  // frees the stage in both CTAs
-              else mma_commit(S.empty + 8 * stage);
+              if (PAIR) mma_commit_pair_both_e(S.empty + 8 * stage);  // frees the stage in both CTAs
+              else mma_commit_e(S.empty + 8 * stage);
             }
             __syncwarp();
             if (++stage == C::STAGES) {
@@ -761,10 +786,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
           }
         }
         if (!ok) break;
-        if (lane == 0) {
-          if (PAIR) mma_commit_pair_both(S.acc_full + 8 * acc);
-          else mma_commit(S.acc_full + 8 * acc);
-        }
+        if (PAIR) mma_commit_pair_both_e(S.acc_full + 8 * acc);
+        else mma_commit_e(S.acc_full + 8 * acc);
         __syncwarp();
         if (++acc == P.acc_stages) {
           acc = 0;
@@ -773,10 +796,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
       }
     }
     // wait until every MMA this thread issued has completed
-    if (lane == 0) {
-      if (PAIR) mma_commit_pair_local(S.drain);
-      else mma_commit(S.drain);
-    }
+    if (PAIR) mma_commit_pair_local_e(S.drain);
+    else mma_commit_e(S.drain);
     __syncwarp();
     warp_wait(S, S.drain, 0, false);
   } else if (warp >= 2) {

@@ -117,7 +117,8 @@ def test_fp32_topk():
 
 @pytest.mark.parametrize("a_kmajor,b_kmajor", [(True, True), (True, False), (False, True),
                                                 (False, False)])
-@pytest.mark.parametrize("m,n,k", [(128, 256, 64), (304, 504, 136), (1000, 776, 1024)])
+@pytest.mark.parametrize("m,n,k", [(128, 256, 64), (304, 504, 136), (600, 520, 200),
+                                   (1000, 776, 1024)])
 def test_tensor_core_gemm_matches_torch(m, n, k, a_kmajor, b_kmajor):
     """GEMM core against fp64 torch for every operand layout (K-major [rows, K]
     or MN-major [K, rows]); ragged in M, N and K."""
@@ -137,6 +138,12 @@ def test_tensor_core_gemm_matches_torch(m, n, k, a_kmajor, b_kmajor):
 def test_separate_teacher_bf16_small():
     """Separate-teacher bf16 workload at reduced size, ragged in every dim."""
     w = W[2].scaled(n_tokens=300, d_student=128, d_teacher=256, vocab=1000)
+    assert_parity(run_and_compare(w), "bf16")
+
+
+def test_separate_teacher_bf16_odd_row_tiles():
+    """Three 256-row tiles, the last one ragged."""
+    w = W[2].scaled(n_tokens=700, d_student=192, d_teacher=128, vocab=2600)
     assert_parity(run_and_compare(w), "bf16")
 
 
