@@ -58,37 +58,33 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-// Lane 0 waits (bounded in time), the outcome is broadcast to the warp, and
-// then every lane tests the completed phase itself: a successful try_wait is
-// what gives a thread acquire ordering on the data the barrier guards (the
-// bulk copies' bytes), which the broadcast alone does not.  On expiry the wait
-// sets *abort and the status bit; later waits that see *abort give up at once.
+// Every lane tests the phase (each successful try_wait gives that lane acquire
+// ordering on the data the barrier guards, the bulk copies' bytes) and the warp
+// leaves together once all lanes have seen it complete; the phase stays
+// complete until this warp itself takes part in the next one.  Bounded in
+// time: lane 0 checks the clock every 64 rounds; on expiry it sets *abort and
+// the status bit and the warp gives up together; later waits that see *abort
+// give up at once.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           uint32_t* status, bool honour_abort = true) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0) {
-    if (!mbar_try(bar, parity)) {
-      const uint64_t t0 = globaltimer();
-      ok = 0;
-      for (uint32_t it = 1;; ++it) {
-        if (mbar_try(bar, parity)) {
-          ok = 1;
-          break;
-        }
-        if ((it & 63) == 0) {
-          if (honour_abort && *abort) break;
-          if (globaltimer() - t0 > kWaitLimitNs) {
-            *abort = 1;
-            set_status(status, KD_DEV_TIMEOUT);
-            break;
-          }
+  if (__all_sync(0xffffffffu, mbar_try(bar, parity))) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (__all_sync(0xffffffffu, mbar_try(bar, parity))) return true;
+    if ((it & 63) == 0) {
+      int give_up = 0;
+      if ((threadIdx.x & 31) == 0) {
+        if (honour_abort && *abort) {
+          give_up = 1;
+        } else if (globaltimer() - t0 > kWaitLimitNs) {
+          *abort = 1;
+          set_status(status, KD_DEV_TIMEOUT);
+          give_up = 1;
         }
       }
+      if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
     }
   }
-  const bool done = __shfl_sync(0xffffffffu, ok, 0) != 0;
-  if (done) mbar_try(bar, parity);  // completed phase: succeeds at once, with acquire
-  return done;
 }
 
 }  // namespace ptx
