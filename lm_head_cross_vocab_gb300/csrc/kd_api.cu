@@ -537,6 +537,10 @@ kd_status kd_fwd(const kd_problem* problem, const kd_inputs* in, float* ce_s, fl
     a.kl = w_kl;
     a.stats = w_stats;
     a.status = dev_status;
+    // test hooks of the ring kernels: a shorter wait limit and one withheld
+    // consumer release (tests of the bounded-wait timeout path)
+    if (const char* e = getenv("KD_TEST_WAIT_LIMIT_NS")) a.wait_limit_ns = strtoull(e, nullptr, 10);
+    if (const char* e = getenv("KD_TEST_WITHHOLD_RELEASE")) a.debug_withhold_release = e[0] == '1';
     prof_record(0, s);
     launch_stream_fwd(a, s);
     prof_record(1, s);

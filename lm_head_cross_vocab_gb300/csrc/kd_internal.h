@@ -88,6 +88,12 @@ struct StreamArgs {
   float w_sce, w_kl_ts;  // w_sce, w_kl * T_s
   void* dz;              // [n, vocab] gradient of the student logits
   uint32_t* status;      // device status word (bounded-wait timeouts)
+  // test hooks of the ring kernels (0 in normal use): a shorter limit for
+  // every bounded wait, and one withheld consumer release (CTA 0, consumer
+  // warp 0, its first stage), so that a test can make the producer's wait for
+  // that stage run out with no copy in flight
+  uint64_t wait_limit_ns;
+  int debug_withhold_release;
 };
 void launch_stream_fwd(const StreamArgs& a, cudaStream_t s);
 void launch_stream_bwd(const StreamArgs& a, cudaStream_t s);

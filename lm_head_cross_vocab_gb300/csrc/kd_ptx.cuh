@@ -66,7 +66,8 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
 // the status bit and the warp gives up together; later waits that see *abort
 // give up at once.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          uint32_t* status, bool honour_abort = true) {
+                                          uint32_t* status, bool honour_abort = true,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (__all_sync(0xffffffffu, mbar_try(bar, parity))) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
@@ -76,7 +77,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
       if ((threadIdx.x & 31) == 0) {
         if (honour_abort && *abort) {
           give_up = 1;
-        } else if (globaltimer() - t0 > kWaitLimitNs) {
+        } else if (globaltimer() - t0 > limit_ns) {
           *abort = 1;
           set_status(status, KD_DEV_TIMEOUT);
           give_up = 1;

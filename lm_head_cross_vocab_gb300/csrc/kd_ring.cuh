@@ -58,13 +58,17 @@ struct Ring {
   uint8_t* base;         // [stage][tensor][kChunk]
   uint32_t full, empty;  // mbarrier arrays (8 bytes each)
   volatile int* abort;
+  uint64_t limit;        // time limit of every wait (ns)
+  bool withhold;         // test hook: CTA 0's consumer warp 0 keeps its first release
   int* cnt;              // [kMergeSlots] arrivals per merge record set
   float* recs;           // [kMergeSlots][kCW][kRec] per-warp row states
   float* bcast;          // small broadcast area
 };
 
-__device__ __forceinline__ Ring make_ring(uint8_t* smem) {
+__device__ __forceinline__ Ring make_ring(uint8_t* smem, const StreamArgs& a) {
   Ring r;
+  r.limit = a.wait_limit_ns ? a.wait_limit_ns : ptx::kWaitLimitNs;
+  r.withhold = a.debug_withhold_release != 0 && blockIdx.x == 0;
   const uint32_t raw = ptx::smem_u32(smem);
   const uint32_t pad = ((raw + 127u) & ~127u) - raw;
   r.base = smem + pad;
@@ -110,7 +114,7 @@ __device__ void producer(const Ring& R, const StreamArgs& a, bool has_t, int pas
     const T* zt = has_t ? static_cast<const T*>(a.zt) + row * V : nullptr;
     for (int pass = 0; ok && pass < passes; ++pass)
       for (int64_t ch = 0; ch < nch; ++ch) {
-        if (!ptx::warp_wait(R.empty + 8 * stage, phase ^ 1, R.abort, status)) {
+        if (!ptx::warp_wait(R.empty + 8 * stage, phase ^ 1, R.abort, status, true, R.limit)) {
           ok = false;
           break;
         }
@@ -135,20 +139,23 @@ __device__ void producer(const Ring& R, const StreamArgs& a, bool has_t, int pas
   if (!ok)  // let our own copies land before the CTA exits
     for (int st = 0; st < kStages; ++st)
       if (issued & (1u << st))
-        ptx::warp_wait(R.full + 8 * st, (par >> st) & 1u, R.abort, status, false);
+        ptx::warp_wait(R.full + 8 * st, (par >> st) & 1u, R.abort, status, false, R.limit);
 }
 
 // Consumer side of one ring slot.
 struct Cursor {
   int stage = 0;
   uint32_t phase = 0;
+  bool first = true;
   __device__ __forceinline__ const uint8_t* acquire(const Ring& R, uint32_t* status) {
-    ptx::warp_wait(R.full + 8 * stage, phase, R.abort, status);
+    ptx::warp_wait(R.full + 8 * stage, phase, R.abort, status, true, R.limit);
     return R.base + (size_t)stage * 2 * kChunk;
   }
   __device__ __forceinline__ void release(const Ring& R) {
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(R.empty + 8 * stage);
+    const bool keep = R.withhold && first && threadIdx.x < 32;  // test hook only
+    first = false;
+    if ((threadIdx.x & 31) == 0 && !keep) ptx::mbar_arrive(R.empty + 8 * stage);
     if (++stage == kStages) {
       stage = 0;
       phase ^= 1;
@@ -284,7 +291,7 @@ __device__ __forceinline__ RowOut finish_row(const StreamArgs& a, int64_t row, R
 template <typename T, bool HAS_T, class Acc, int PASSES>
 __global__ void __launch_bounds__(kThreads, 1) k_fwd(StreamArgs a, uint32_t* status) {
   extern __shared__ uint8_t smem_raw[];
-  const Ring R = make_ring(smem_raw);
+  const Ring R = make_ring(smem_raw, a);
   ring_init(R);
   constexpr int passes = PASSES;
   if ((threadIdx.x >> 5) == kCW) {
@@ -411,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd(StreamArgs a, uint32_t* sta
 template <typename T, bool HAS_T, class Grad>
 __global__ void __launch_bounds__(kThreads, 1) k_bwd(StreamArgs a, uint32_t* status) {
   extern __shared__ uint8_t smem_raw[];
-  const Ring R = make_ring(smem_raw);
+  const Ring R = make_ring(smem_raw, a);
   ring_init(R);
   if ((threadIdx.x >> 5) == kCW) {
     producer<T>(R, a, HAS_T, 1, status);
