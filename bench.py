@@ -256,6 +256,106 @@ def time_cpu_oracle(fn, seconds):
         rows = min(4096, rows * 4, max(rows * 2, int(rows * seconds / max(dt, 1e-3))))
 
 
+def _projection_map(v_t, v_s):
+    """The synthetic cross-tokenizer token map of the projection legs: 80 % of
+    the student ids reached by one teacher token, 3 % by two, the other teacher
+    tokens unmatched (seeded)."""
+    rng = np.random.default_rng(1006)
+    tmap = np.full(v_t, -1, dtype=np.int32)
+    src = rng.permutation(v_t)
+    one = rng.permutation(v_s)[: int(0.8 * v_s)]
+    tmap[src[: one.size]] = one
+    two = rng.choice(one, int(0.03 * v_s), replace=False)
+    tmap[src[one.size: one.size + two.size]] = two
+    return tmap
+
+
+def run_project_loss(args, rank):
+    """Cross-tokenizer distillation with the projected teacher inside the loss
+    (KD_TEACHER_PROJECTED): bf16 teacher logits ~N(0,4) over 151936 ids, the
+    projection map of --project, bf16 student logits ~N(0,4) over 128256 ids,
+    8 % ignored labels, forward KL, T = 2, w_sce = 0.  One step = kd_fwd +
+    kd_bwd (d z_s); no projected tensor is stored.  The same step through the
+    unfused composition (kd_project_teacher_logits, then a logits teacher at
+    T = 1) is timed beside it."""
+    from lm_head_cross_vocab_gb300 import kd
+    kd.load_library()
+    n = args.tokens or 16384
+    v_t, v_s, T = 151936, 128256, 2.0
+    dev = torch.device("cuda", 0)
+    tmap_d = torch.from_numpy(_projection_map(v_t, v_s)).to(dev)
+    g = torch.Generator(device=dev).manual_seed(1008)
+    z_t = (torch.randn(n, v_t, generator=g, device=dev) * 4.0).to(torch.bfloat16)
+    z_s = (torch.randn(n, v_s, generator=g, device=dev) * 4.0).to(torch.bfloat16)
+    labels = torch.randint(0, v_s, (n,), generator=g, device=dev)
+    labels[torch.rand(n, generator=g, device=dev) < 0.08] = -100
+    t = {"logits_s": z_s, "logits_t": z_t, "labels": labels, "token_map": tmap_d}
+    common = dict(n_tokens=n, vocab=v_s, dtype="bf16", student="logits", variant="forward",
+                  t_student=T, w_student_ce=0.0, w_teacher_ce=0.0, w_kl=1.0, ignore_index=-100)
+    prob = kd.Problem(teacher="projected", t_teacher=T, vocab_teacher=v_t, **common)
+    prob_u = kd.Problem(teacher="logits", t_teacher=1.0, **common)
+    ws_f, ws_b, ws_p = kd.Workspace(), kd.Workspace(), kd.Workspace()
+    fo = bo = fu = bu = None
+    zp = None
+
+    def fused():
+        nonlocal fo, bo
+        fo = kd.forward(prob, t, ws_f, check=False, out=fo)
+        bo = kd.backward(prob, t, fo["stats"], want=("logits_s",), workspace=ws_b, check=False,
+                         out=bo)
+
+    def unfused():
+        nonlocal fu, bu, zp
+        zp = kd.project_teacher_logits(tmap_d, z_t, v_s, temperature=T, workspace=ws_p,
+                                       check=False)
+        tu = {"logits_s": z_s, "logits_t": zp, "labels": labels}
+        fu = kd.forward(prob_u, tu, ws_f, check=False, out=fu)
+        bu = kd.backward(prob_u, tu, fu["stats"], want=("logits_s",), workspace=ws_b,
+                         check=False, out=bu)
+
+    def timed(fn, steps):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(steps):
+            fn()
+        e.record()
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / steps
+
+    launches0 = kd.kd_launch_count()
+    with ClockSampler(smi_index(0)) as clk:
+        ms = timed(fused, args.steps)
+    launches = kd.kd_launch_count() - launches0
+    kd.check_status(fo["dev_status"])
+    ms_u = timed(unfused, max(3, args.steps // 2))
+    zp = None
+    peak_gib = torch.cuda.max_memory_allocated(dev) / 2 ** 30
+    nbytes = n * (4 * v_t + 6 * v_s)  # fwd: z_t, z_s; bwd: z_t, z_s, d z_s (bf16)
+    peaks, peak_src = load_peaks()
+    gbs = nbytes / (ms / 1e3) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": "cross-vocab fused linear+KD fwd+bwd tokens/s (projected teacher)",
+            "value": n / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "cross_vocab_projected_teacher", "tokens": n,
+                       "v_teacher": v_t, "v_student": v_s, "temperature": T,
+                       "variant": "forward", "l2": "inputs larger than L2"},
+            "roofline": {"bound": "hbm", "kernel": "k_proj_loss (fwd + bwd, + inverse map)",
+                         "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "peak_source": f"{peak_src} copy",
+                         "bytes_per_step": nbytes, "traffic": None},
+            "sections": {"unfused_project_then_logits_teacher": {
+                "ms_per_step": ms_u, "tokens_per_s": n / (ms_u / 1e3),
+                "note": "kd_project_teacher_logits -> kd_fwd / kd_bwd, projected logits stored"}},
+            "peak_hbm_gib": peak_gib, "clocks": clk.summary(), "gpu_launches": launches}),
+            flush=True)
+
+
 def run_projection(args, rank):
     """Cross-vocabulary token-map projection (kd_project_teacher_logits) on a
     synthetic cross-tokenizer case: bf16 teacher logits ~N(0,4) over a
@@ -267,13 +367,7 @@ def run_projection(args, rank):
     n = args.tokens or 16384
     v_t, v_s = 151936, 128256
     dev = torch.device("cuda", 0)
-    rng = np.random.default_rng(1006)
-    tmap = np.full(v_t, -1, dtype=np.int32)
-    src = rng.permutation(v_t)
-    one = rng.permutation(v_s)[: int(0.8 * v_s)]
-    tmap[src[: one.size]] = one
-    two = rng.choice(one, int(0.03 * v_s), replace=False)
-    tmap[src[one.size: one.size + two.size]] = two
+    tmap = _projection_map(v_t, v_s)
     tmap_d = torch.from_numpy(tmap).to(dev)
     g = torch.Generator(device=dev).manual_seed(1006)
     z = (torch.randn(n, v_t, generator=g, device=dev) * 4.0).to(torch.bfloat16)
@@ -395,6 +489,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--project", action="store_true",
                     help="time the cross-vocabulary token-map projection instead of the loss")
+    ap.add_argument("--project-loss", action="store_true",
+                    help="time cross-vocabulary distillation with the projected teacher inside "
+                         "the loss (fwd + bwd)")
     ap.add_argument("--mix", choices=["arithmetic", "geometric"],
                     help="time multi-teacher mixing (this mode) instead of the loss")
     ap.add_argument("--variant", choices=["forward", "reverse", "jeffreys", "skew_js",
@@ -425,6 +522,9 @@ def main():
         return
     if args.project:
         run_projection(args, rank)
+        return
+    if args.project_loss:
+        run_project_loss(args, rank)
         return
     if args.mix:
         run_mix(args, rank)

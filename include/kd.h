@@ -56,7 +56,7 @@
 extern "C" {
 #endif
 
-#define KD_ABI_VERSION 4
+#define KD_ABI_VERSION 5
 
 typedef enum kd_status {
   KD_OK = 0,
@@ -75,6 +75,12 @@ typedef enum kd_status {
 #define KD_DEV_BAD_TOPK 0x2u
 #define KD_DEV_TIMEOUT 0x4u
 #define KD_DEV_BAD_MAP 0x8u   /* token map entry outside [-1, V_student) */
+#define KD_DEV_MAP_UNSUPPORTED 0x10u /* KD_TEACHER_PROJECTED: the token map sends more
+                                     * teacher tokens into one student id range
+                                     * than the fused kernel's receive buffers
+                                     * hold; nothing was computed (use
+                                     * kd_project_teacher_logits + a
+                                     * KD_TEACHER_LOGITS teacher instead) */
 
 typedef enum kd_dtype { KD_BF16 = 0, KD_FP32 = 1 } kd_dtype;
 
@@ -86,13 +92,25 @@ typedef enum kd_student_kind { KD_STUDENT_HIDDEN = 0, KD_STUDENT_LOGITS = 1 } kd
  * through the student's W_s), SeparateTeacher / PrecomputedTeacher with
  * teacher_hidden + teacher_weight (own W_t), PrecomputedTeacher(logits=...);
  * Full-Chunked-KL-Loss README, "Methods": cached top-K probabilities.
- * KD_TEACHER_NONE: plain fused linear + CE (no KL, no teacher). */
+ * KD_TEACHER_NONE: plain fused linear + CE (no KL, no teacher).
+ * KD_TEACHER_PROJECTED: teacher logits over another vocabulary
+ * (kd_inputs.logits_t [N, vocab_teacher]) moved onto the student vocabulary
+ * by kd_inputs.token_map inside the loss kernels (orda-kernel README,
+ * "Cross-vocabulary distillation": token-map projection into a
+ * PrecomputedTeacher with logits_temperature = t_teacher):
+ *   z_p[n, i] = log sum_{j : token_map[j] = i} exp(logits_t[n, j] / t_teacher),
+ * an id no teacher token maps to having probability 0.  z_p is then the
+ * teacher's logits at temperature 1 (CE_t = logsumexp(z_p) - z_p[y]); the
+ * student is KD_STUDENT_LOGITS at t_student.  Results equal
+ * kd_project_teacher_logits followed by a KD_TEACHER_LOGITS teacher with
+ * t_teacher = 1, but the projected [N, V] tensor is never stored. */
 typedef enum kd_teacher_kind {
   KD_TEACHER_NONE = 0,
   KD_TEACHER_TIED = 1,
   KD_TEACHER_SEPARATE = 2,
   KD_TEACHER_LOGITS = 3,
-  KD_TEACHER_TOPK = 4
+  KD_TEACHER_TOPK = 4,
+  KD_TEACHER_PROJECTED = 5
 } kd_teacher_kind;
 
 /* orda-kernel README, "KL variants" (teacher-detached subset). */
@@ -134,6 +152,7 @@ typedef struct kd_problem {
   int64_t seq_chunk;     /* token chunk (0 = auto). Results do not depend on  */
                          /* either beyond rounding (flash_kd chunk_size,      */
                          /* Full-Chunked-KL-Loss --chunk-sizes: memory knobs). */
+  int64_t vocab_teacher; /* V_t of a KD_TEACHER_PROJECTED teacher, else 0     */
 } kd_problem;
 
 /* Input tensors (device pointers; NULL where the problem does not use one). */
@@ -147,6 +166,8 @@ typedef struct kd_inputs {
   const int64_t* labels; /* [N] or NULL: every token valid, no CE allowed     */
   const int32_t* topk_idx; /* [N, K] distinct ids in [0, V), any order        */
   const float* topk_p;   /* [N, K] teacher probabilities (not renormalised)   */
+  const int32_t* token_map; /* [V_t] KD_TEACHER_PROJECTED: student id of each  */
+                         /* teacher token, or -1 (logits_t is then [N, V_t])  */
 } kd_inputs;
 
 /* Number of floats per token in the saved statistics written by kd_fwd and

@@ -82,7 +82,7 @@ void launch_record(int kind, int64_t idx, bool stop, cudaStream_t s) {
   if (idx < e.n) cudaEventRecord(static_cast<cudaEvent_t>(stop ? e.stops[idx] : e.starts[idx]), s);
 }
 
-enum Path { PATH_STREAM = 0, PATH_SIMT = 1, PATH_TC = 2 };
+enum Path { PATH_STREAM = 0, PATH_SIMT = 1, PATH_TC = 2, PATH_PROJ = 3 };
 
 constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -108,10 +108,11 @@ struct Plan {
   int n_parts;    // partial records per row
   int64_t R, C;   // backward chunk (rows x vocabulary columns)
   // forward workspace
-  size_t f_count, f_ce_s, f_ce_t, f_kl, f_stats, f_part, f_sidx, f_sp, f_mass, f_ent, f_bytes;
+  size_t f_count, f_ce_s, f_ce_t, f_kl, f_stats, f_part, f_sidx, f_sp, f_mass, f_ent, f_proj,
+      f_bytes;
   // backward workspace
   size_t b_count, b_scale, b_sidx, b_sp, b_mass, b_ent, b_g, b_gt, b_wt, b_hst, b_htt, b_dh,
-      b_dw, b_dht, b_dwt, b_bytes;
+      b_dw, b_dht, b_dwt, b_proj, b_bytes;
   int64_t ldv, ldn;  // pitches of W^T [D, ldv] and H^T [D, ldn]
   bool kmajor_b;     // backward GEMMs take W^T / H^T (transposed per backward) as B
   bool two_streams;  // backward GEMMs of chunk k on a side stream beside chunk k+1
@@ -128,7 +129,7 @@ kd_status check_problem(const kd_problem* p) {
   if (p->dtype != KD_BF16 && p->dtype != KD_FP32) return KD_ERR_INVALID_ARG;
   if (p->student != KD_STUDENT_HIDDEN && p->student != KD_STUDENT_LOGITS)
     return KD_ERR_INVALID_ARG;
-  if (p->teacher < KD_TEACHER_NONE || p->teacher > KD_TEACHER_TOPK) return KD_ERR_INVALID_ARG;
+  if (p->teacher < KD_TEACHER_NONE || p->teacher > KD_TEACHER_PROJECTED) return KD_ERR_INVALID_ARG;
   if (p->variant < KD_KL_FORWARD || p->variant > KD_KL_SKEW_REVERSE) return KD_ERR_INVALID_ARG;
   if (p->reduction != KD_REDUCE_MEAN && p->reduction != KD_REDUCE_SUM) return KD_ERR_INVALID_ARG;
   // orda-kernel README, "Parameters": term weights finite and >= 0
@@ -151,6 +152,14 @@ kd_status check_problem(const kd_problem* p) {
     if (p->w_teacher_ce != 0.f) return KD_ERR_UNSUPPORTED;  // no teacher logits
   }
   if (p->teacher == KD_TEACHER_NONE && p->w_teacher_ce != 0.f) return KD_ERR_INVALID_ARG;
+  if (p->teacher == KD_TEACHER_PROJECTED) {
+    // orda-kernel README, "Cross-vocabulary distillation": teacher logits over
+    // their own vocabulary, moved onto the student's by a token map
+    if (p->vocab_teacher < 1 || p->vocab_teacher > (int64_t)1 << 30) return KD_ERR_INVALID_ARG;
+    if (p->student != KD_STUDENT_LOGITS) return KD_ERR_UNSUPPORTED;  // project, then kd_fwd
+    if (!proj_loss_supported(p->vocab_teacher, p->vocab, p->dtype == KD_BF16))
+      return KD_ERR_UNSUPPORTED;
+  }
   return KD_OK;
 }
 
@@ -171,6 +180,9 @@ kd_status check_inputs(const kd_problem* p, const kd_inputs* in) {
       break;
     case KD_TEACHER_TOPK:
       if (!in->topk_idx || !in->topk_p) return KD_ERR_INVALID_ARG;
+      break;
+    case KD_TEACHER_PROJECTED:
+      if (!in->logits_t || !in->token_map) return KD_ERR_INVALID_ARG;
       break;
     default:
       break;
@@ -273,16 +285,24 @@ kd_status make_plan(const kd_problem* p, bool has_labels, Plan& P) {
   P.s_logits = !P.s_gemm;
   P.t_gemm = p->teacher == KD_TEACHER_TIED || p->teacher == KD_TEACHER_SEPARATE;
   P.t_logits = p->teacher == KD_TEACHER_LOGITS;
+  const bool proj = p->teacher == KD_TEACHER_PROJECTED;
   P.topk = p->teacher == KD_TEACHER_TOPK;
   P.tied = p->teacher == KD_TEACHER_TIED;
-  P.has_t = P.t_gemm || P.t_logits;
+  P.has_t = P.t_gemm || P.t_logits || proj;
   P.ds = P.s_gemm ? p->d_student : 0;
   P.dt = p->teacher == KD_TEACHER_TIED ? p->d_student
          : p->teacher == KD_TEACHER_SEPARATE ? p->d_teacher
                                              : 0;
-  P.c = make_consts(p, has_labels, P.has_t);
+  if (proj) {  // the projected distribution enters the loss at temperature 1
+    kd_problem q = *p;
+    q.t_teacher = 1.f;
+    P.c = make_consts(&q, has_labels, true);
+  } else {
+    P.c = make_consts(p, has_labels, P.has_t);
+  }
   P.nsm = std::max(1, tc_num_sms());
-  if (!P.s_gemm && !P.t_gemm) P.path = PATH_STREAM;
+  if (proj) P.path = PATH_PROJ;
+  else if (!P.s_gemm && !P.t_gemm) P.path = PATH_STREAM;
   else if (!P.is_bf16) P.path = PATH_SIMT;
   else P.path = PATH_TC;
   if (P.path == PATH_TC) {
@@ -317,6 +337,7 @@ kd_status make_plan(const kd_problem* p, bool has_labels, Plan& P) {
     P.n_parts = P.n_splits;
   }
   if (P.n_parts) P.f_part = f.take((size_t)P.n_parts * n * kRec * 4);
+  if (proj) P.f_proj = f.take(proj_loss_workspace_bytes(p->vocab_teacher, v));
   P.f_bytes = f.off;
   // ---- backward
   Layout b;
@@ -366,6 +387,7 @@ kd_status make_plan(const kd_problem* p, bool has_labels, Plan& P) {
     if (P.tied || (P.t_gemm && p->teacher_grads))
       P.b_gt = b.take(P.R * P.C * 4);  // teacher-CE gradient tile
   }
+  if (proj) P.b_proj = b.take(proj_loss_workspace_bytes(p->vocab_teacher, v));
   P.b_bytes = b.off;
   return KD_OK;
 }
@@ -514,7 +536,31 @@ kd_status kd_fwd(const kd_problem* problem, const kd_inputs* in, float* ce_s, fl
                      dev_status, s);
   }
   const bool js = P.has_t && is_skew(p->variant);
-  if (P.path == PATH_STREAM) {
+  if (P.path == PATH_PROJ) {
+    ProjLossArgs a;
+    memset(&a, 0, sizeof(a));
+    a.token_map = in->token_map;
+    a.zt = in->logits_t;
+    a.zs = in->logits_s;
+    a.n = n;
+    a.vt = p->vocab_teacher;
+    a.vs = P.v;
+    a.is_bf16 = P.is_bf16;
+    a.inv_tp = 1.f / p->t_teacher;
+    a.c = P.c;
+    a.variant = p->variant;
+    a.labels = in->labels;
+    a.ignore = p->ignore_index;
+    a.ce_s = w_ce_s;
+    a.ce_t = w_ce_t;
+    a.kl = w_kl;
+    a.stats = w_stats;
+    a.mode = 0;
+    a.status = dev_status;
+    prof_record(0, s);
+    if (launch_proj_loss(a, at<char>(workspace, P.f_proj), s)) return KD_ERR_CUDA;
+    prof_record(1, s);
+  } else if (P.path == PATH_STREAM) {
     StreamArgs a;
     memset(&a, 0, sizeof(a));
     a.zs = in->logits_s;
@@ -718,6 +764,34 @@ static kd_status bwd_impl(const kd_problem* problem, const kd_inputs* in, const 
   const float w_tce = ((P.tied && d_w_s) || d_h_t || d_w_t) ? p->w_teacher_ce : 0.f;
   const bool tied_tce = P.tied && d_w_s && w_tce != 0.f;  // G_t^T H_t into d W_s
   const void* w_teach = P.tied ? in->w_s : in->w_t;      // the teacher's head weight
+  if (P.path == PATH_PROJ) {
+    if (!d_logits_s) return cuda_status(cudaGetLastError());
+    ProjLossArgs a;
+    memset(&a, 0, sizeof(a));
+    a.token_map = in->token_map;
+    a.zt = in->logits_t;
+    a.zs = in->logits_s;
+    a.n = n;
+    a.vt = p->vocab_teacher;
+    a.vs = v;
+    a.is_bf16 = P.is_bf16;
+    a.inv_tp = 1.f / p->t_teacher;
+    a.c = P.c;
+    a.variant = p->variant;
+    a.labels = in->labels;
+    a.ignore = p->ignore_index;
+    a.stats = const_cast<float*>(stats);  // read only by the backward
+    a.row_scale = scale;
+    a.w_sce = p->w_student_ce;
+    a.w_kl_ts = w_kl_ts;
+    a.dz = d_logits_s;
+    a.mode = 1;
+    a.status = dev_status;
+    prof_record(2, s);
+    if (launch_proj_loss(a, at<char>(workspace, P.b_proj), s)) return KD_ERR_CUDA;
+    prof_record(3, s);
+    return cuda_status(cudaGetLastError());
+  }
   if (P.path == PATH_STREAM) {
     StreamArgs a;
     memset(&a, 0, sizeof(a));

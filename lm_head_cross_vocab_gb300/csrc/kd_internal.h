@@ -102,6 +102,35 @@ void launch_stream_bwd(const StreamArgs& a, cudaStream_t s);
 bool launch_stream_fwd_packed(const StreamArgs& a, cudaStream_t s);
 bool launch_stream_bwd_packed(const StreamArgs& a, cudaStream_t s);
 
+// ------------------------------------------- projected teacher (fused loss)
+// Logit students against teacher logits over another vocabulary, moved onto
+// the student vocabulary by a token map inside the loss kernels
+// (kd_project.cu, k_proj_loss): the forward writes the per-token outputs and
+// statistics, the backward d z_s; no projected [n, vs] tensor is stored.
+struct ProjLossArgs {
+  const int32_t* token_map;  // [vt]
+  const void* zt;            // [n, vt]
+  const void* zs;            // [n, vs]
+  int64_t n, vt, vs;
+  int is_bf16;
+  float inv_tp;              // 1 / projection temperature
+  Consts c;                  // teacher side at T = 1
+  int variant;
+  const int64_t* labels;
+  int64_t ignore;
+  float *ce_s, *ce_t, *kl, *stats;
+  const float* row_scale;
+  float w_sce, w_kl_ts;
+  void* dz;
+  int mode;                  // 0 forward, 1 backward
+  uint32_t* status;
+};
+size_t proj_loss_workspace_bytes(int64_t vt, int64_t vs);
+// false: a teacher row needs more than 8 CTAs or a CTA more than 32 Ki ids
+bool proj_loss_supported(int64_t vt, int64_t vs, bool bf16);
+// Builds the maps in `workspace` and launches the fused kernel; 1 on error.
+int launch_proj_loss(const ProjLossArgs& a, void* workspace, cudaStream_t s);
+
 // ------------------------------------------------------------- fp32 SIMT path
 struct SimtArgs {
   // student: hidden (h_s, w_s, d_s); teacher: hidden (h_t, w_t, d_t) or logits zt

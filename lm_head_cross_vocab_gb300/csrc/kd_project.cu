@@ -834,6 +834,523 @@ __global__ void __launch_bounds__(kPT, 1)
   }
 }
 
+// ---------------------------------------------------------------- fused loss
+// The projected teacher inside the distillation loss (orda-kernel README,
+// "Cross-vocabulary distillation": token-map projection into a
+// PrecomputedTeacher, whose logits the loss then reads at temperature 1).
+// k_proj_loss runs the exchange of k_project_exchange -- the cluster shares a
+// teacher row, CTA q receives the values of the teacher tokens that map into
+// its student ids [q*so, q*so + so) -- and, instead of storing the projected
+// values, uses them on chip against the student logits of the same ids:
+//   forward:  the online-softmax state of each thread's ids (student at T_s,
+//             projected teacher at 1), merged over the CTA and then over the
+//             cluster in CTA 0, which finalises the token (CE, CE_t, KL,
+//             saved statistics); the skew variants take a second sweep over
+//             the same ids once CTA 0 has broadcast both normalisers;
+//   backward: d z_s of each id from the saved statistics, stored directly.
+// The projected [N, V_s] tensor never exists.  Ids no teacher token maps to
+// take the lowest finite float, as the unfused projection writes them.
+constexpr int kLT = 512;  // threads of the fused kernel (128 registers each)
+// Student ids with several teacher tokens, per CTA, whose folded value is kept
+// in shared memory for the row (beyond this, an id folds from global memory).
+constexpr int kMCap = 1024;
+constexpr int64_t kPLSmem = 212 * 1024;  // dynamic shared memory of the fused kernel
+struct PLParams {
+  const void* zt;      // [n, vt] teacher logits
+  const void* zs;      // [n, vs] student logits (same dtype)
+  int64_t n, vt, vs;
+  float inv_tp;        // 1 / projection temperature
+  Consts c;            // the projected distribution enters at T = 1
+  int variant;
+  const int64_t* labels;
+  int64_t ignore;
+  float *ce_s, *ce_t, *kl, *stats;  // forward outputs (stats never NULL)
+  const float* row_scale;           // backward
+  float w_sce, w_kl_ts;
+  void* dz;                         // [n, vs] d loss / d z_s
+  const int32_t *off, *epos, *code, *send_src, *mpre, *mlist, *mcode;
+  const XLayout* X;
+  int64_t sc, so, send_cap, recv_cap;
+  uint32_t* status;
+};
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x),
+               "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// the projected (tempered) teacher logits of ids j0 .. j0 + 7 from the
+// receive buffer; ids with several teacher tokens fold their columns' values
+// in column order (their edges from the code array), ids with none take the
+// lowest finite float
+template <typename TI>
+__device__ __forceinline__ void proj_values(const PLParams& P, const TI* recv, const float* mval,
+                                            uint32_t rcap, const uint32_t (&cw)[4], int64_t j0,
+                                            int nv, float* v) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const uint32_t cq = (cw[q >> 1] >> (16 * (q & 1))) & 0xffffu;
+    float x;
+    if (cq < rcap) {  // one teacher token: its receive slot
+      x = ld<TI>(recv + cq) * P.inv_tp;
+    } else if (cq < 0xfffeu) {  // several, folded for this row in shared memory
+      x = mval[cq - rcap];
+    } else if (cq == 0xfffeu && q < nv) {  // several, beyond the table: fold here
+      const int64_t id = j0 + q;
+      const int32_t m = -2 - P.code[id], e0 = m >> 3;
+      const int32_t e1 = (m & 7) == 7 ? P.off[id + 1] : e0 + (m & 7) + 2;
+      x = -INFINITY;
+#pragma unroll 1
+      for (int32_t e = e0; e < e1; ++e) x = logaddexp(x, ld<TI>(recv + P.epos[e]) * P.inv_tp);
+    } else {
+      x = -INFINITY;
+    }
+    v[q] = x > -INFINITY ? x : -FLT_MAX;
+  }
+}
+
+// student logits of ids j0 .. j0 + nv - 1 of one row (16-byte loads when whole)
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, int nv, float* s) {
+  if (nv == 8 && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+    const uint4 w = *reinterpret_cast<const uint4*>(p);
+    s[0] = bf16lo(w.x); s[1] = bf16hi(w.x); s[2] = bf16lo(w.y); s[3] = bf16hi(w.y);
+    s[4] = bf16lo(w.z); s[5] = bf16hi(w.z); s[6] = bf16lo(w.w); s[7] = bf16hi(w.w);
+  } else {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) s[q] = q < nv ? __bfloat162float(p[q]) : 0.f;
+  }
+}
+__device__ __forceinline__ void load8(const float* p, int nv, float* s) {
+  if (nv == 8 && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    s[0] = a.x; s[1] = a.y; s[2] = a.z; s[3] = a.w; s[4] = b.x; s[5] = b.y; s[6] = b.z; s[7] = b.w;
+  } else {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) s[q] = q < nv ? p[q] : 0.f;
+  }
+}
+
+// 8 consecutive logits as raw 16-byte words (one for bf16, two for fp32),
+// loaded ahead of their use and converted when needed
+template <typename TI>
+struct Vec8 {
+  uint4 w[sizeof(TI) / 2];
+};
+template <typename TI>
+__device__ __forceinline__ void ldv8(const TI* p, Vec8<TI>& v) {
+#pragma unroll
+  for (int i = 0; i < (int)(sizeof(TI) / 2); ++i) v.w[i] = reinterpret_cast<const uint4*>(p)[i];
+}
+__device__ __forceinline__ void cvt8(const Vec8<__nv_bfloat16>& v, float* s) {
+  const uint4 w = v.w[0];
+  s[0] = bf16lo(w.x); s[1] = bf16hi(w.x); s[2] = bf16lo(w.y); s[3] = bf16hi(w.y);
+  s[4] = bf16lo(w.z); s[5] = bf16hi(w.z); s[6] = bf16lo(w.w); s[7] = bf16hi(w.w);
+}
+__device__ __forceinline__ void cvt8(const Vec8<float>& v, float* s) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    s[4 * i + 0] = __uint_as_float(v.w[i].x);
+    s[4 * i + 1] = __uint_as_float(v.w[i].y);
+    s[4 * i + 2] = __uint_as_float(v.w[i].z);
+    s[4 * i + 3] = __uint_as_float(v.w[i].w);
+  }
+}
+
+// Visit this thread's student ids, 8 per step (steps kLT * 8 ids apart), in a
+// loop that is not unrolled (the per-step work is large: unrolled, it
+// overflowed the instruction cache).  The step's receive codes are selected
+// from the register array by compare (no dynamic register indexing), and the
+// next step's student logits are loaded while this step computes.
+// body(j0, nv, cw, s): ids j0 .. j0 + nv - 1, their codes and student logits.
+template <typename TI, int STEPS, class Body>
+__device__ __forceinline__ void for_ids(const TI* zsr, int64_t i_lo, int64_t i_hi, bool vec,
+                                        const uint32_t (&c16)[STEPS][4], Body&& body) {
+  Vec8<TI> cur, nxt;
+  int64_t j0 = i_lo + (int64_t)threadIdx.x * 8;
+  bool cur_ok = vec && j0 + 8 <= i_hi;
+  if (cur_ok) ldv8(zsr + j0, cur);
+#pragma unroll 1
+  for (int u = 0; u < STEPS; ++u, j0 += (int64_t)kLT * 8) {
+    if (j0 >= i_hi) break;
+    const int nv = (int)(i_hi - j0 < 8 ? i_hi - j0 : 8);
+    const int64_t j1 = j0 + (int64_t)kLT * 8;
+    const bool nxt_ok = vec && u + 1 < STEPS && j1 + 8 <= i_hi;
+    if (nxt_ok) ldv8(zsr + j1, nxt);
+    uint32_t cw[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+#pragma unroll
+    for (int k = 0; k < STEPS; ++k)
+      if (k == u) {
+        cw[0] = c16[k][0];
+        cw[1] = c16[k][1];
+        cw[2] = c16[k][2];
+        cw[3] = c16[k][3];
+      }
+    float s[8];
+    if (cur_ok) cvt8(cur, s);
+    else load8(zsr + j0, nv, s);
+    body(j0, nv, cw, s);
+    cur = nxt;
+    cur_ok = nxt_ok;
+  }
+}
+
+// merge every thread's state into thread 0 (red: 16 x kRec floats)
+__device__ __forceinline__ void pl_block_merge(RowState& st, const Consts& c, float* red) {
+  warp_merge(st, c);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) st.store(red + w * kRec);
+  __syncthreads();
+  if (w == 0) {
+    if (l < kLT / 32) st.load(red + l * kRec);
+    else st.init();
+    warp_merge(st, c);
+  }
+  __syncthreads();  // red is reused by the next merge
+}
+__device__ __forceinline__ float3 pl_block_sum3(float a, float b, float d, float* red) {
+  for (int o = 16; o > 0; o >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, o);
+    b += __shfl_xor_sync(0xffffffffu, b, o);
+    d += __shfl_xor_sync(0xffffffffu, d, o);
+  }
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) {
+    red[3 * w] = a;
+    red[3 * w + 1] = b;
+    red[3 * w + 2] = d;
+  }
+  __syncthreads();
+  float3 r = make_float3(0.f, 0.f, 0.f);
+  if (threadIdx.x == 0)
+    for (int i = 0; i < kLT / 32; ++i) {
+      r.x += red[3 * i];
+      r.y += red[3 * i + 1];
+      r.z += red[3 * i + 2];
+    }
+  __syncthreads();
+  return r;
+}
+
+// per-token outputs from the cluster-merged state (CTA 0, thread 0)
+__device__ __forceinline__ RowOut pl_finish(const PLParams& P, int64_t row, RowState& st,
+                                            bool write_kl) {
+  bool valid = true, bad = false;
+  if (P.labels) {
+    const int64_t y = P.labels[row];
+    valid = y != P.ignore;
+    bad = valid && (y < 0 || y >= P.vs);
+  }
+  const RowOut o = finalize(st, P.c, P.variant, true, false, 0.f, 0.f);
+  const float nan = __int_as_float(0x7fc00000);
+  if (P.ce_s) P.ce_s[row] = !valid ? 0.f : (bad ? nan : o.ce_s);
+  if (P.ce_t) P.ce_t[row] = !valid ? 0.f : (bad ? nan : o.ce_t);
+  if (P.kl && write_kl) P.kl[row] = valid ? o.kl : 0.f;
+  float4* s4 = reinterpret_cast<float4*>(P.stats + row * KD_STATS_PER_TOKEN);
+  s4[0] = make_float4(o.lse_s1, o.lse_sT, o.lse_t1, o.lse_tT);
+  s4[1] = make_float4(o.kl_rev, 0.f, 0.f, o.dlse);
+  return o;
+}
+
+template <typename TI, int MODE, bool SKEW, int STEPS>
+__global__ void __launch_bounds__(kLT, 1) k_proj_loss(const __grid_constant__ PLParams P) {
+  const XLayout* __restrict__ X = P.X;
+  if (!X->fits) {  // the map overflows a receive buffer: the fused path cannot run it
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_status(P.status, KD_DEV_MAP_UNSUPPORTED);
+    return;
+  }
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[2];  // 0: the staged slice, 1: the receive buffer
+  __shared__ int abort_flag;
+  __shared__ __align__(16) float red[(kLT / 32) * kRec];   // block reductions
+  __shared__ __align__(16) float mslot[2][kMaxC][kRec];    // CTA 0: each CTA's row state
+  __shared__ __align__(16) float jslot[2][kMaxC][4];       // CTA 0: each CTA's skew sums
+  __shared__ float bc[2][2];                               // skew: dlse, lse(a_t) from CTA 0
+  __shared__ uint32_t mtab[kMCap];  // ids with several teacher tokens: 2 receive slots, or ~0
+  __shared__ float mval[kMCap];     // ... their folded (tempered) values in the current row
+  const uint32_t r = cl_rank(), C = cl_size();
+  const int64_t ncl = gridDim.x / C;
+  const int64_t n = P.n, vt = P.vt, vs = P.vs, sc = P.sc;
+  const TI* __restrict__ zt = static_cast<const TI*>(P.zt);
+  TI* const slice = reinterpret_cast<TI*>(smem_raw);
+  TI* const send = slice + sc;
+  TI* const recv = send + P.send_cap;
+  const int64_t c0 = (int64_t)r * sc;
+  const int64_t clen = vt - c0 < sc ? (vt - c0 > 0 ? vt - c0 : 0) : sc;
+  const int64_t i_lo = (int64_t)r * P.so, i_hi = i_lo + P.so < vs ? i_lo + P.so : vs;
+  const int32_t nsend = X->sendtot[r];
+  const int32_t* gl = P.send_src + X->sendbase[r];
+  const uint32_t rx_bytes = (uint32_t)X->recvtot[r] * (uint32_t)sizeof(TI);
+  const uint32_t bar_s = ptx::smem_u32(&bars[0]), bar_r = ptx::smem_u32(&bars[1]);
+  uint32_t* status = P.status;
+  const Consts c = P.c;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar_s, 1);
+    ptx::mbar_init(bar_r, 1);
+    ptx::fence_mbar_init();
+    abort_flag = 0;
+  }
+  __syncthreads();
+  auto stage = [&](int64_t row) -> bool {
+    const TI* src = zt + row * vt + c0;
+    const bool al = ((reinterpret_cast<uintptr_t>(src) | ptx::smem_u32(slice)) & 15) == 0;
+    const int64_t nb = al ? clen * (int64_t)sizeof(TI) / 16 * 16 : 0;
+    if (threadIdx.x == 0 && !*reinterpret_cast<volatile int*>(&abort_flag)) {
+      ptx::mbar_expect_tx(bar_s, (uint32_t)nb);
+      if (nb > 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        ptx::bulk_load(ptx::smem_u32(slice), src, (uint32_t)nb, bar_s);
+      }
+    }
+    const int64_t q0 = nb / (int64_t)sizeof(TI);
+    for (int64_t q = q0 + threadIdx.x; q < clen; q += kLT) slice[q] = src[q];
+    return q0 < clen;
+  };
+  bool plain = false;
+  const int64_t first = blockIdx.x / C;
+  if (first < n) {
+    plain = stage(first);
+    if (threadIdx.x == 0) ptx::mbar_expect_tx(bar_r, rx_bytes);
+  }
+  cl_sync();  // every receive barrier is armed before any copy is sent
+  // this thread's student ids are the same in every row: their receive codes
+  // (two 16-bit slots per register) are loaded once
+  // ids with several teacher tokens: the first kMCap of this CTA's range get a
+  // table entry (their two receive slots; ~0 for three or more tokens) and
+  // codes rcap + k; the rest keep the marker 0xfffe (folded from global memory)
+  const uint32_t rcap = (uint32_t)P.recv_cap;
+  const int32_t m_lo = P.mpre[i_lo < i_hi ? i_lo : i_hi], m_hi = P.mpre[i_hi];
+  const int32_t nm = m_hi - m_lo < kMCap ? m_hi - m_lo : kMCap;
+  for (int32_t k = threadIdx.x; k < nm; k += kLT) {
+    const int32_t m = -2 - P.mcode[m_lo + k], e0 = m >> 3;
+    mtab[k] = (m & 7) == 0 ? ((uint32_t)P.epos[e0] | ((uint32_t)P.epos[e0 + 1] << 16)) : ~0u;
+  }
+  uint32_t c16[STEPS][4];
+#pragma unroll
+  for (int u = 0; u < STEPS; ++u) {
+    const int64_t j0 = i_lo + ((int64_t)u * kLT + threadIdx.x) * 8;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) c16[u][q] = 0xffffffffu;
+    if (j0 >= i_hi) continue;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int32_t cq = j0 + q < i_hi ? P.code[j0 + q] : -1;
+      uint32_t h = cq >= 0 ? (uint32_t)cq : 0xffffu;
+      if (cq <= -2) {
+        const int32_t k = P.mpre[j0 + q] - m_lo;
+        h = k < nm ? rcap + (uint32_t)k : 0xfffeu;
+      }
+      c16[u][q >> 1] = (c16[u][q >> 1] & ~(0xffffu << (16 * (q & 1)))) | (h << (16 * (q & 1)));
+    }
+  }
+  uint32_t ps = 0, pr = 0;
+  int pend = 0;
+  uint32_t pend_ps = 0, pend_pr = 0;
+  int lr = 0;  // local row count (parity selects the merge slots)
+  for (int64_t row = first; row < n; row += ncl, ++lr) {
+    if (!ptx::warp_wait(bar_s, ps, &abort_flag, status) && !(pend & 1)) {
+      pend |= 1;
+      pend_ps = ps;
+    }
+    ps ^= 1u;
+    if (plain) __syncthreads();
+    for (int32_t t0 = (int32_t)threadIdx.x * 8; t0 < nsend; t0 += kLT * 8) {
+      const int4 a = reinterpret_cast<const int4*>(gl + t0)[0];
+      const int4 b = reinterpret_cast<const int4*>(gl + t0)[1];
+      const int32_t g[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      TI v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = slice[g[q]];
+      if constexpr (sizeof(TI) == 2) {
+        *reinterpret_cast<uint4*>(send + t0) = *reinterpret_cast<const uint4*>(v);
+      } else {
+        reinterpret_cast<uint4*>(send + t0)[0] = reinterpret_cast<const uint4*>(v)[0];
+        reinterpret_cast<uint4*>(send + t0)[1] = reinterpret_cast<const uint4*>(v)[1];
+      }
+    }
+    __syncthreads();  // send is complete; the slice is free for the next row
+    if (row + ncl < n) plain = stage(row + ncl);
+    if (threadIdx.x == 0 && !*reinterpret_cast<volatile int*>(&abort_flag)) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      for (uint32_t q = 0; q < C; ++q) {
+        const int k = (int)(r * C + q);
+        const int32_t len = pad8(X->cnt[k]);
+        if (len == 0) continue;
+        const uint32_t dst = cl_map(ptx::smem_u32(recv + X->recvoff[k]), q);
+        const uint32_t mb = cl_map(bar_r, q);
+        asm volatile(
+            "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], "
+            "%2, [%3];" ::"r"(dst),
+            "r"(ptx::smem_u32(send + X->sendoff[k])), "r"((uint32_t)len * (uint32_t)sizeof(TI)),
+            "r"(mb)
+            : "memory");
+      }
+    }
+    if (!ptx::warp_wait(bar_r, pr, &abort_flag, status) && !(pend & 2)) {
+      pend |= 2;
+      pend_pr = pr;
+    }
+    pr ^= 1u;
+    // this row's values of the tabled ids with several teacher tokens
+    for (int32_t k = threadIdx.x; k < nm; k += kLT) {
+      const uint32_t e = mtab[k];
+      float x = -INFINITY;
+      if (e != ~0u) {
+        x = logaddexp(ld<TI>(recv + (e & 0xffffu)) * P.inv_tp, ld<TI>(recv + (e >> 16)) * P.inv_tp);
+      } else {  // three or more tokens: their edges from global memory
+        const int32_t id = P.mlist[m_lo + k], m = -2 - P.mcode[m_lo + k], e0 = m >> 3;
+        const int32_t e1 = (m & 7) == 7 ? P.off[id + 1] : e0 + (m & 7) + 2;
+#pragma unroll 1
+        for (int32_t ed = e0; ed < e1; ++ed) x = logaddexp(x, ld<TI>(recv + P.epos[ed]) * P.inv_tp);
+      }
+      mval[k] = x;
+    }
+    __syncthreads();
+    const TI* zsr = static_cast<const TI*>(P.zs) + row * vs;
+    // whole 8-id groups load as 16-byte words when the rows are 16-byte aligned
+    const bool vec = ((reinterpret_cast<uintptr_t>(zsr) | (uintptr_t)(i_lo * (int64_t)sizeof(TI))) & 15) == 0;
+    const int par = lr & 1;
+    const int64_t y = P.labels ? P.labels[row] : -1;
+    if constexpr (MODE == 0) {
+      // ---- forward: this thread's ids into one online-softmax state
+      RowState st;
+      st.init();
+      float zys = 0.f, zyt = 0.f;
+      for_ids<TI, STEPS>(zsr, i_lo, i_hi, vec, c16,
+                         [&](int64_t j0, int nv, const uint32_t(&cw)[4], const float* s) {
+                           float v[8];
+                           proj_values<TI>(P, recv, mval, rcap, cw, j0, nv, v);
+                           update<8, true, true>(st, s, v, nv, c);
+                           if (y >= j0 && y < j0 + nv) {
+                             const int jy = (int)(y - j0);
+#pragma unroll
+                             for (int q = 0; q < 8; ++q)
+                               if (q == jy) {
+                                 zys = s[q];
+                                 zyt = v[q];
+                               }
+                           }
+                         });
+      st.zys = zys;
+      st.zyt = zyt;
+      pl_block_merge(st, c, red);
+      if (threadIdx.x == 0) {  // this CTA's state into CTA 0's slot
+        const uint32_t dst = cl_map(ptx::smem_u32(&mslot[par][r][0]), 0);
+        st_cluster_v4(dst, make_float4(st.ms, st.ls1, st.lsT, st.mt));
+        st_cluster_v4(dst + 16, make_float4(st.lt1, st.ltT, st.qd, st.qx));
+        st_cluster_v4(dst + 32, make_float4(st.pd, st.px, st.zys, st.zyt));
+        st_cluster_v4(dst + 48, make_float4(st.tk, st.jq, st.jp, st.jx));
+      }
+      if constexpr (SKEW) {
+        // both normalisers before the second sweep: CTA 0 merges and
+        // broadcasts them
+        cl_sync();
+        if (r == 0 && threadIdx.x == 0) {
+          RowState m;
+          m.load(&mslot[par][0][0]);
+          for (uint32_t k = 1; k < C; ++k) {
+            RowState o;
+            o.load(&mslot[par][k][0]);
+            merge(m, o, c);
+          }
+          const RowOut o = pl_finish(P, row, m, false);
+          for (uint32_t k = 0; k < C; ++k) {
+            st_cluster_f32(cl_map(ptx::smem_u32(&bc[par][0]), k), o.dlse);
+            st_cluster_f32(cl_map(ptx::smem_u32(&bc[par][1]), k), o.lse_tT);
+          }
+        }
+        cl_sync();
+        const float dlse = bc[par][0], lse_tT = bc[par][1];
+        const bool want_x = P.variant != KD_KL_SKEW_JS;
+        float jq = 0.f, jp = 0.f, jx = 0.f;
+        for_ids<TI, STEPS>(zsr, i_lo, i_hi, vec, c16,
+                           [&](int64_t j0, int nv, const uint32_t(&cw)[4], const float* s) {
+                             float v[8];
+                             proj_values<TI>(P, recv, mval, rcap, cw, j0, nv, v);
+#pragma unroll
+                             for (int q = 0; q < 8; ++q)
+                               if (q < nv) js_terms(s[q], v[q], lse_tT, dlse, c, jq, jp, jx, want_x);
+                           });
+        const float3 js = pl_block_sum3(jq, jp, jx, red);
+        if (threadIdx.x == 0)
+          st_cluster_v4(cl_map(ptx::smem_u32(&jslot[par][r][0]), 0),
+                        make_float4(js.x, js.y, js.z, 0.f));
+      }
+    } else {
+      // ---- backward: d z_s of this thread's ids
+      const float scale = P.row_scale[row];
+      float sv[KD_STATS_PER_TOKEN];
+#pragma unroll
+      for (int i = 0; i < KD_STATS_PER_TOKEN; ++i) sv[i] = P.stats[row * KD_STATS_PER_TOKEN + i];
+      const float sq_s = c.pw == 2 ? ex2((2.f * sv[S_LSE_ST] - sv[S_LSE_S1]) * kL2E) : 0.f;
+      TI* dzr = static_cast<TI*>(P.dz) + row * vs;
+      for_ids<TI, STEPS>(zsr, i_lo, i_hi, vec, c16,
+                         [&](int64_t j0, int nv, const uint32_t(&cw)[4], const float* s) {
+        float v[8], g[8];
+        proj_values<TI>(P, recv, mval, rcap, cw, j0, nv, v);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float gg = 0.f;
+          if (scale != 0.f) {
+            const float lp = fmaf(s[q], c.inv_ts, -sv[S_LSE_ST]);
+            const float p = ex2(lp * kL2E);
+            const float lq = fmaf(v[q], c.inv_tt, -sv[S_LSE_TT]);
+            gg = P.w_kl_ts * kl_grad_pq(s[q], v[q], lp, lq, p, ex2(lq * kL2E), sv, P.variant, c);
+            if (P.w_sce != 0.f)
+              gg = fmaf(P.w_sce,
+                        softmax_t1(s[q], p, sv[S_LSE_S1], sq_s, c.pw) - (j0 + q == y ? 1.f : 0.f),
+                        gg);
+            gg *= scale;
+          }
+          g[q] = gg;
+        }
+        if (nv == 8 && (reinterpret_cast<uintptr_t>(dzr + j0) & 15) == 0) {
+          store_vec(dzr + j0, g);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            if (q < nv) st<TI>(dzr + j0 + q, g[q]);
+        }
+      });
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && row + ncl < n) ptx::mbar_expect_tx(bar_r, rx_bytes);
+    cl_sync();
+    if constexpr (MODE == 0) {
+      if (r == 0 && threadIdx.x == 0) {
+        if constexpr (SKEW) {
+          float jq = 0.f, jp = 0.f, jx = 0.f;
+          for (uint32_t k = 0; k < C; ++k) {
+            jq += jslot[par][k][0];
+            jp += jslot[par][k][1];
+            jx += jslot[par][k][2];
+          }
+          const bool v_ok = !P.labels || y != P.ignore;
+          P.stats[row * KD_STATS_PER_TOKEN + S_KL_PM] = jp;
+          if (P.variant != KD_KL_SKEW_JS) P.stats[row * KD_STATS_PER_TOKEN + S_EPPM] = jx;
+          if (P.kl) P.kl[row] = v_ok ? skew_kl(P.variant, c.beta, jq, jp) : 0.f;
+        } else {
+          RowState m;
+          m.load(&mslot[par][0][0]);
+          for (uint32_t k = 1; k < C; ++k) {
+            RowState o;
+            o.load(&mslot[par][k][0]);
+            merge(m, o, c);
+          }
+          pl_finish(P, row, m, true);
+        }
+      }
+    }
+  }
+  if (threadIdx.x < 32) {
+    if (pend & 1) ptx::warp_wait(bar_s, pend_ps, &abort_flag, status, false);
+    if (pend & 2) ptx::warp_wait(bar_r, pend_pr, &abort_flag, status, false);
+  }
+}
+
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 // slices of a teacher row of vt elements: the fewest whose columns (sc, a
@@ -995,6 +1512,66 @@ void launch_scan(const int32_t* in, int64_t n, int32_t* out, int32_t* tmp, cudaS
   k_scan_apply<<<(unsigned)tiles, 1024, 0, s>>>(in, n, toff, out);
 }
 
+// The inverse map (count -> scan -> scatter -> per-id sort) and, with an
+// exchange plan, the exchange lists (segments, send lists, receive slots,
+// per-id codes); `multi`: also the list of ids with several teacher tokens
+// (the unfused exchange kernel writes those in a second pass).  Returns 1 on a
+// CUDA error.
+int build_maps(const int32_t* token_map, int64_t vt, int64_t vs, char* ws, const ProjLayout& L,
+               const XPlan* xp, bool multi, uint32_t* dev_status, cudaStream_t s) {
+  int32_t* cnt = reinterpret_cast<int32_t*>(ws + L.cnt);
+  int32_t* off = reinterpret_cast<int32_t*>(ws + L.off);
+  int32_t* cols = reinterpret_cast<int32_t*>(ws + L.cols);
+  int32_t* one = reinterpret_cast<int32_t*>(ws + L.one);
+  int32_t* eid = reinterpret_cast<int32_t*>(ws + L.eid);
+  int32_t* epos = reinterpret_cast<int32_t*>(ws + L.epos);
+  int32_t* code = reinterpret_cast<int32_t*>(ws + L.code);
+  int32_t* send_src = reinterpret_cast<int32_t*>(ws + L.send_src);
+  int32_t* mflag = reinterpret_cast<int32_t*>(ws + L.mflag);
+  int32_t* mpre = reinterpret_cast<int32_t*>(ws + L.mpre);
+  int32_t* mlist = reinterpret_cast<int32_t*>(ws + L.mlist);
+  int32_t* mcode = reinterpret_cast<int32_t*>(ws + L.mcode);
+  int32_t* stmp = reinterpret_cast<int32_t*>(ws + L.stmp);
+  XLayout* X = reinterpret_cast<XLayout*>(ws + L.xl);
+  const int nsm = tc_num_sms() > 0 ? tc_num_sms() : 1;
+  const int gmap = (int)std::min<int64_t>((vt + kT - 1) / kT, (int64_t)nsm * 8);
+  const int gid = (int)std::min<int64_t>((vs + kT - 1) / kT, (int64_t)nsm * 8);
+  if (cudaMemsetAsync(cnt, 0, (size_t)vs * 4, s) != cudaSuccess) return 1;
+  note_launch();
+  k_map_count<<<gmap, kT, 0, s>>>(token_map, vt, vs, cnt, dev_status);
+  launch_scan(cnt, vs, off, stmp, s);
+  if (cudaMemsetAsync(cnt, 0, (size_t)vs * 4, s) != cudaSuccess) return 1;
+  note_launch();
+  k_map_scatter<<<gmap, kT, 0, s>>>(token_map, vt, vs, off, cnt, cols);
+  note_launch();
+  k_map_sort<<<gid, kT, 0, s>>>(off, vs, cols);
+  note_launch();
+  k_map_single<<<gid, kT, 0, s>>>(off, cols, vs, one, eid);
+  if (xp) {  // the exchange lists; X->fits then picks the path on the device
+    if (cudaMemsetAsync(X, 0, sizeof(XLayout), s) != cudaSuccess ||
+        cudaMemsetAsync(send_src, 0, ((size_t)vt + 8 * kMaxC * kMaxC) * 4, s) != cudaSuccess)
+      return 1;
+    note_launch();
+    k_edge_count<<<gmap, kT, 0, s>>>(off, cols, eid, vs, (int32_t)xp->sc, (int32_t)xp->so, xp->C,
+                                      X);
+    note_launch();
+    k_exchange_layout<<<1, 32, 0, s>>>(X, xp->C, (int32_t)xp->send_cap, (int32_t)xp->recv_cap);
+    note_launch();
+    k_edge_partition<<<xp->C * xp->C, 1024, 0, s>>>(off, cols, eid, vs, (int32_t)xp->sc,
+                                                    (int32_t)xp->so, xp->C, X, send_src, epos);
+    note_launch();
+    k_exchange_codes<<<gid, kT, 0, s>>>(off, epos, vs, code);
+    if (multi) {
+      note_launch();
+      k_multi_flag<<<gid, kT, 0, s>>>(code, vs, mflag);
+      launch_scan(mflag, vs, mpre, stmp, s);
+      note_launch();
+      k_multi_scatter<<<gid, kT, 0, s>>>(code, mpre, vs, mlist, mcode);
+    }
+  }
+  return cudaGetLastError() != cudaSuccess;
+}
+
 // the launches of one call, per dtype pair
 struct ProjRun {
   const void* zt;
@@ -1023,7 +1600,133 @@ struct ProjOps {
   }
 };
 
+
+// Exchange plan of the fused kernel: as x_plan, with the fused kernel's own
+// thread count (STEPS 8-id steps per thread cover a CTA's student ids).
+template <typename TI>
+bool pl_plan(int64_t vt, int64_t vs, XPlan* P, int* steps) {
+  const int64_t elem = (int64_t)sizeof(TI);
+  int64_t C = (vt * elem + kXSlice - 1) / kXSlice;
+  if (C < 1) C = 1;
+  if (C > kMaxC) return false;
+  P->sc = ((vt + C - 1) / C + 7) / 8 * 8;
+  C = (vt + P->sc - 1) / P->sc;
+  P->C = (int)C;
+  P->so = ((vs + C - 1) / C + 7) / 8 * 8;
+  const int64_t st = (P->so + 8 * kLT - 1) / (8 * kLT);
+  if (st > 8) return false;
+  *steps = st <= 1 ? 1 : st <= 2 ? 2 : st <= 4 ? 4 : 8;
+  P->send_cap = P->sc + 8 * C;
+  P->recv_cap = (kPLSmem / elem - P->sc - P->send_cap) / 8 * 8;
+  // receive slots and table codes share the 16-bit code space below 0xfffe
+  if (P->recv_cap > 0xfffe - kMCap) P->recv_cap = (0xfffe - kMCap) / 8 * 8;
+  if (P->recv_cap < 8) return false;
+  P->smem = (size_t)(P->sc + P->send_cap + P->recv_cap) * (size_t)elem;
+  return true;
+}
+
+template <typename TI, int MODE, bool SKEW, int STEPS>
+int launch_pl(const XPlan& xp, const PLParams& P, cudaStream_t s) {
+  auto kern = k_proj_loss<TI, MODE, SKEW, STEPS>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)xp.smem) !=
+      cudaSuccess)
+    return 1;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)xp.C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  const int nsm = tc_num_sms() > 0 ? tc_num_sms() : 1;
+  cfg.gridDim = dim3((unsigned)(xp.C * std::max(1, nsm / xp.C)));
+  cfg.blockDim = dim3(kLT);
+  cfg.dynamicSmemBytes = xp.smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int maxc = max_active_clusters(reinterpret_cast<const void*>(kern), cfg);
+  if (maxc <= 0) return 1;
+  const int64_t clusters = P.n < maxc ? P.n : maxc;
+  cfg.gridDim = dim3((unsigned)(xp.C * clusters));
+  note_launch();
+  return cudaLaunchKernelEx(&cfg, kern, P) != cudaSuccess;
+}
+
+template <typename TI, int MODE, bool SKEW>
+int launch_pl_steps(const XPlan& xp, int steps, const PLParams& P, cudaStream_t s) {
+  switch (steps) {
+    case 1: return launch_pl<TI, MODE, SKEW, 1>(xp, P, s);
+    case 2: return launch_pl<TI, MODE, SKEW, 2>(xp, P, s);
+    case 4: return launch_pl<TI, MODE, SKEW, 4>(xp, P, s);
+    default: return launch_pl<TI, MODE, SKEW, 8>(xp, P, s);
+  }
+}
+
+template <typename TI>
+int launch_pl_any(const XPlan& xp, int steps, const PLParams& P, int mode, cudaStream_t s) {
+  if (mode == 1) return launch_pl_steps<TI, 1, false>(xp, steps, P, s);
+  return is_skew(P.variant) ? launch_pl_steps<TI, 0, true>(xp, steps, P, s)
+                            : launch_pl_steps<TI, 0, false>(xp, steps, P, s);
+}
+
 }  // namespace
+
+size_t proj_loss_workspace_bytes(int64_t vt, int64_t vs) { return proj_layout(vt, vs).bytes; }
+
+bool proj_loss_supported(int64_t vt, int64_t vs, bool bf16) {
+  XPlan xp;
+  int steps = 0;
+  return bf16 ? pl_plan<__nv_bfloat16>(vt, vs, &xp, &steps) : pl_plan<float>(vt, vs, &xp, &steps);
+}
+
+int launch_proj_loss(const ProjLossArgs& a, void* workspace, cudaStream_t s) {
+  XPlan xp;
+  int steps = 0;
+  const bool ok = a.is_bf16 ? pl_plan<__nv_bfloat16>(a.vt, a.vs, &xp, &steps)
+                            : pl_plan<float>(a.vt, a.vs, &xp, &steps);
+  if (!ok) return 1;
+  const ProjLayout L = proj_layout(a.vt, a.vs);
+  char* ws = static_cast<char*>(workspace);
+  if (build_maps(a.token_map, a.vt, a.vs, ws, L, &xp, true, a.status, s)) return 1;
+  if (a.n <= 0) return 0;
+  PLParams P;
+  memset(&P, 0, sizeof(P));
+  P.zt = a.zt;
+  P.zs = a.zs;
+  P.n = a.n;
+  P.vt = a.vt;
+  P.vs = a.vs;
+  P.inv_tp = a.inv_tp;
+  P.c = a.c;
+  P.variant = a.variant;
+  P.labels = a.labels;
+  P.ignore = a.ignore;
+  P.ce_s = a.ce_s;
+  P.ce_t = a.ce_t;
+  P.kl = a.kl;
+  P.stats = a.stats;
+  P.row_scale = a.row_scale;
+  P.w_sce = a.w_sce;
+  P.w_kl_ts = a.w_kl_ts;
+  P.dz = a.dz;
+  P.off = reinterpret_cast<const int32_t*>(ws + L.off);
+  P.epos = reinterpret_cast<const int32_t*>(ws + L.epos);
+  P.code = reinterpret_cast<const int32_t*>(ws + L.code);
+  P.send_src = reinterpret_cast<const int32_t*>(ws + L.send_src);
+  P.mpre = reinterpret_cast<const int32_t*>(ws + L.mpre);
+  P.mlist = reinterpret_cast<const int32_t*>(ws + L.mlist);
+  P.mcode = reinterpret_cast<const int32_t*>(ws + L.mcode);
+  P.X = reinterpret_cast<const XLayout*>(ws + L.xl);
+  P.sc = xp.sc;
+  P.so = xp.so;
+  P.send_cap = xp.send_cap;
+  P.recv_cap = xp.recv_cap;
+  P.status = a.status;
+  return a.is_bf16 ? launch_pl_any<__nv_bfloat16>(xp, steps, P, a.mode, s)
+                   : launch_pl_any<float>(xp, steps, P, a.mode, s);
+}
+
 }  // namespace kd
 
 using namespace kd;
@@ -1060,7 +1763,6 @@ kd_status kd_project_teacher_logits(const int32_t* token_map, int64_t v_teacher,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const ProjLayout L = proj_layout(v_teacher, v_student);
   char* ws = static_cast<char*>(workspace);
-  int32_t* cnt = reinterpret_cast<int32_t*>(ws + L.cnt);
   int32_t* off = reinterpret_cast<int32_t*>(ws + L.off);
   int32_t* cols = reinterpret_cast<int32_t*>(ws + L.cols);
   int32_t* one = reinterpret_cast<int32_t*>(ws + L.one);
@@ -1068,15 +1770,12 @@ kd_status kd_project_teacher_logits(const int32_t* token_map, int64_t v_teacher,
   int32_t* list_val = reinterpret_cast<int32_t*>(ws + L.list_val);
   int32_t* slice_cnt = reinterpret_cast<int32_t*>(ws + L.slice_cnt);
   int32_t* slice_off = reinterpret_cast<int32_t*>(ws + L.slice_off);
-  int32_t* eid = reinterpret_cast<int32_t*>(ws + L.eid);
   int32_t* epos = reinterpret_cast<int32_t*>(ws + L.epos);
   int32_t* code = reinterpret_cast<int32_t*>(ws + L.code);
   int32_t* send_src = reinterpret_cast<int32_t*>(ws + L.send_src);
-  int32_t* mflag = reinterpret_cast<int32_t*>(ws + L.mflag);
   int32_t* mpre = reinterpret_cast<int32_t*>(ws + L.mpre);
   int32_t* mlist = reinterpret_cast<int32_t*>(ws + L.mlist);
   int32_t* mcode = reinterpret_cast<int32_t*>(ws + L.mcode);
-  int32_t* stmp = reinterpret_cast<int32_t*>(ws + L.stmp);
   XLayout* X = reinterpret_cast<XLayout*>(ws + L.xl);
   bool (*plan)(int64_t, int64_t, XPlan*);
   int (*run)(const XPlan*, const ProjRun&);
@@ -1091,43 +1790,12 @@ kd_status kd_project_teacher_logits(const int32_t* token_map, int64_t v_teacher,
   }
   XPlan xp;
   const bool xok = plan(v_teacher, v_student, &xp);
-  const int nsm = tc_num_sms() > 0 ? tc_num_sms() : 1;
-  const int gmap = (int)std::min<int64_t>((v_teacher + kT - 1) / kT, (int64_t)nsm * 8);
-  const int gid = (int)std::min<int64_t>((v_student + kT - 1) / kT, (int64_t)nsm * 8);
-  if (cudaMemsetAsync(cnt, 0, (size_t)v_student * 4, s) != cudaSuccess ||
-      cudaMemsetAsync(slice_cnt, 0, (size_t)nsl * 4, s) != cudaSuccess)
+  if (cudaMemsetAsync(slice_cnt, 0, (size_t)nsl * 4, s) != cudaSuccess) return KD_ERR_CUDA;
+  if (build_maps(token_map, v_teacher, v_student, ws, L, xok ? &xp : nullptr, true, dev_status,
+                 s))
     return KD_ERR_CUDA;
-  note_launch();
-  k_map_count<<<gmap, kT, 0, s>>>(token_map, v_teacher, v_student, cnt, dev_status);
-  launch_scan(cnt, v_student, off, stmp, s);
-  if (cudaMemsetAsync(cnt, 0, (size_t)v_student * 4, s) != cudaSuccess) return KD_ERR_CUDA;
-  note_launch();
-  k_map_scatter<<<gmap, kT, 0, s>>>(token_map, v_teacher, v_student, off, cnt, cols);
-  note_launch();
-  k_map_sort<<<gid, kT, 0, s>>>(off, v_student, cols);
-  note_launch();
-  k_map_single<<<gid, kT, 0, s>>>(off, cols, v_student, one, eid);
-  if (xok) {  // the exchange lists; X->fits then picks the path on the device
-    if (cudaMemsetAsync(X, 0, sizeof(XLayout), s) != cudaSuccess ||
-        cudaMemsetAsync(send_src, 0, ((size_t)v_teacher + 8 * kMaxC * kMaxC) * 4, s) !=
-            cudaSuccess)
-      return KD_ERR_CUDA;
-    note_launch();
-    k_edge_count<<<gmap, kT, 0, s>>>(off, cols, eid, v_student, (int32_t)xp.sc, (int32_t)xp.so,
-                                      xp.C, X);
-    note_launch();
-    k_exchange_layout<<<1, 32, 0, s>>>(X, xp.C, (int32_t)xp.send_cap, (int32_t)xp.recv_cap);
-    note_launch();
-    k_edge_partition<<<xp.C * xp.C, 1024, 0, s>>>(off, cols, eid, v_student, (int32_t)xp.sc,
-                                                  (int32_t)xp.so, xp.C, X, send_src, epos);
-    note_launch();
-    k_exchange_codes<<<gid, kT, 0, s>>>(off, epos, v_student, code);
-    note_launch();
-    k_multi_flag<<<gid, kT, 0, s>>>(code, v_student, mflag);
-    launch_scan(mflag, v_student, mpre, stmp, s);
-    note_launch();
-    k_multi_scatter<<<gid, kT, 0, s>>>(code, mpre, v_student, mlist, mcode);
-  }
+  const int nsm = tc_num_sms() > 0 ? tc_num_sms() : 1;
+  const int gid = (int)std::min<int64_t>((v_student + kT - 1) / kT, (int64_t)nsm * 8);
   const XLayout* Xp = xok ? X : nullptr;
   note_launch();
   k_slice_count<<<gid, kT, 0, s>>>(one, off, cols, v_student, (int32_t)sc, nsl, slice_cnt, Xp);

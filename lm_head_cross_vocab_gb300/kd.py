@@ -27,20 +27,23 @@ LIB_PATH = os.path.join(_PKG, "libkdgb.so")
 KD_OK, KD_ERR_INVALID_ARG, KD_ERR_UNSUPPORTED, KD_ERR_WORKSPACE = 0, 1, 2, 3
 KD_ERR_BAD_LABEL, KD_ERR_BAD_TOPK, KD_ERR_TIMEOUT, KD_ERR_CUDA, KD_ERR_NO_DEVICE = 4, 5, 6, 7, 8
 KD_DEV_BAD_LABEL, KD_DEV_BAD_TOPK, KD_DEV_TIMEOUT, KD_DEV_BAD_MAP = 0x1, 0x2, 0x4, 0x8
+KD_DEV_MAP_UNSUPPORTED = 0x10
 KD_BF16, KD_FP32 = 0, 1
 KD_STUDENT_HIDDEN, KD_STUDENT_LOGITS = 0, 1
 KD_TEACHER_NONE, KD_TEACHER_TIED, KD_TEACHER_SEPARATE, KD_TEACHER_LOGITS, KD_TEACHER_TOPK = range(5)
+KD_TEACHER_PROJECTED = 5
 KD_KL_FORWARD, KD_KL_REVERSE, KD_KL_JEFFREYS, KD_KL_SKEW_JS = range(4)
 KD_KL_SKEW_FORWARD, KD_KL_SKEW_REVERSE = 4, 5
 KD_REDUCE_MEAN, KD_REDUCE_SUM = 0, 1
 KD_STATS_PER_TOKEN = 8
 KD_STATIC_SCRATCH_BYTES = 32 << 20
-KD_ABI_VERSION = 4  # the kd.h this binding follows
+KD_ABI_VERSION = 5  # the kd.h this binding follows
 
 DTYPES = {"bf16": KD_BF16, "fp32": KD_FP32}
 STUDENTS = {"hidden": KD_STUDENT_HIDDEN, "logits": KD_STUDENT_LOGITS}
 TEACHERS = {"none": KD_TEACHER_NONE, "tied": KD_TEACHER_TIED, "separate": KD_TEACHER_SEPARATE,
-            "logits": KD_TEACHER_LOGITS, "topk": KD_TEACHER_TOPK}
+            "logits": KD_TEACHER_LOGITS, "topk": KD_TEACHER_TOPK,
+            "projected": KD_TEACHER_PROJECTED}
 VARIANTS = {"forward": KD_KL_FORWARD, "reverse": KD_KL_REVERSE, "jeffreys": KD_KL_JEFFREYS,
             "skew_js": KD_KL_SKEW_JS, "skew_forward": KD_KL_SKEW_FORWARD,
             "skew_reverse": KD_KL_SKEW_REVERSE}
@@ -59,13 +62,14 @@ class kd_problem(ctypes.Structure):
         ("ignore_index", ctypes.c_int64), ("num_batch_labels", ctypes.c_int64),
         ("assume_valid_labels", ctypes.c_int32), ("teacher_grads", ctypes.c_int32),
         ("vocab_chunk", ctypes.c_int64), ("seq_chunk", ctypes.c_int64),
+        ("vocab_teacher", ctypes.c_int64),
     ]
 
 
 class kd_inputs(ctypes.Structure):
     _fields_ = [(name, ctypes.c_void_p) for name in
                 ("h_s", "w_s", "logits_s", "h_t", "w_t", "logits_t", "labels", "topk_idx",
-                 "topk_p")]
+                 "topk_p", "token_map")]
 
 
 class KDError(RuntimeError):
@@ -258,6 +262,7 @@ class Problem:
     vocab_chunk: int = 0
     seq_chunk: int = 0
     teacher_grads: bool = False  # the backward may be asked for d_h_t / d_w_t
+    vocab_teacher: int = 0       # V_t of a "projected" teacher (token map over V_t ids)
 
     def to_c(self) -> kd_problem:
         p = kd_problem()
@@ -274,6 +279,7 @@ class Problem:
         p.assume_valid_labels = int(self.assume_valid_labels)
         p.teacher_grads = int(self.teacher_grads)
         p.vocab_chunk, p.seq_chunk = self.vocab_chunk, self.seq_chunk
+        p.vocab_teacher = self.vocab_teacher
         return p
 
 
@@ -283,7 +289,8 @@ class kd_grads(ctypes.Structure):
 
 def make_inputs(t: dict) -> kd_inputs:
     i = kd_inputs()
-    for k in ("h_s", "w_s", "logits_s", "h_t", "w_t", "logits_t", "labels", "topk_idx", "topk_p"):
+    for k in ("h_s", "w_s", "logits_s", "h_t", "w_t", "logits_t", "labels", "topk_idx", "topk_p",
+              "token_map"):
         v = t.get(k)
         if v is not None:
             assert v.is_cuda and v.is_contiguous(), f"{k} must be a contiguous CUDA tensor"
@@ -316,6 +323,10 @@ def check_status(dev_status: torch.Tensor, assume_valid: bool = False):
     s = int(dev_status.item())
     if s & KD_DEV_TIMEOUT:
         raise KDError(KD_ERR_TIMEOUT, "device")
+    if s & KD_DEV_MAP_UNSUPPORTED:
+        raise KDError(KD_ERR_UNSUPPORTED, "token map too skewed for the fused projected teacher")
+    if s & KD_DEV_BAD_MAP:
+        raise KDError(KD_ERR_INVALID_ARG, "token map entry outside [-1, V_student)")
     if not assume_valid:
         if s & KD_DEV_BAD_LABEL:
             raise KDError(KD_ERR_BAD_LABEL, "device")

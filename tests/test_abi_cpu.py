@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(kd):
 
 
 def test_abi_version_and_status_strings(kd):
-    assert kd.kd_abi_version() == kd.KD_ABI_VERSION == 4
+    assert kd.kd_abi_version() == kd.KD_ABI_VERSION == 5
     for code in range(9):
         s = kd.kd_status_string(code)
         assert s and s != "unknown status"
@@ -105,6 +105,31 @@ def test_unsupported_combinations(kd):
     # top-K teachers carry no logits for a teacher CE
     p = _prob(kd, teacher="topk", topk=4, w_teacher_ce=1.0)
     assert lib.kd_workspace_size(ctypes.byref(p), ctypes.byref(f), None) == kd.KD_ERR_UNSUPPORTED
+
+
+def test_projected_teacher_argument_rules(kd):
+    """KD_TEACHER_PROJECTED (orda-kernel README, "Cross-vocabulary distillation"):
+    the teacher vocabulary size is required, the student must arrive as logits,
+    and the token map and teacher logits are required inputs."""
+    lib = kd.load_library()
+    f, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    base = dict(student="logits", teacher="projected", d_student=0, vocab=5000)
+    p = _prob(kd, **base, vocab_teacher=7000)
+    assert lib.kd_workspace_size(ctypes.byref(p), ctypes.byref(f), ctypes.byref(b)) == kd.KD_OK
+    assert f.value > 0 and b.value > 0
+    p = _prob(kd, **base, vocab_teacher=0)
+    assert lib.kd_workspace_size(ctypes.byref(p), ctypes.byref(f), None) == kd.KD_ERR_INVALID_ARG
+    p = _prob(kd, teacher="projected", vocab_teacher=7000)  # hidden student
+    assert lib.kd_workspace_size(ctypes.byref(p), ctypes.byref(f), None) == kd.KD_ERR_UNSUPPORTED
+    # a teacher row that would need more than 8 CTAs of the fused kernel
+    p = _prob(kd, **base, vocab_teacher=1 << 22)
+    assert lib.kd_workspace_size(ctypes.byref(p), ctypes.byref(f), None) == kd.KD_ERR_UNSUPPORTED
+    fake = 1 << 20
+    p = _prob(kd, **base, vocab_teacher=7000)
+    ins = kd.kd_inputs(logits_s=fake, logits_t=fake, labels=fake)  # no token map
+    st = lib.kd_fwd(ctypes.byref(p), ctypes.byref(ins), None, None, None, None, None, None, None,
+                    0, None)
+    assert st == kd.KD_ERR_INVALID_ARG
 
 
 def test_null_inputs_and_workspace_errors(kd):
