@@ -399,9 +399,16 @@ __device__ __forceinline__ RowOut finalize(const RowState& s, const Consts& c, i
 // with m = (1-b) q + b p:
 //   x <= 0:  l = log(m/q) = log1p(b expm1(x)),      log(q/m) = -l,  log(p/m) = x - l
 //   x >  0:  l = log(m/p) = log1p((1-b) expm1(-x)),  log(p/m) = -l,  log(q/m) = -x - l
-// No form subtracts two large values: nearby distributions keep their small
-// divergences, and an id with q = 0 (a teacher id no token maps to: x huge)
-// still gives log(p/m) = -log b exactly.
+// No form subtracts two large values, and an id with q = 0 (a teacher id no
+// token maps to: x huge) still gives log(p/m) = -log b exactly.  The precise
+// form (fp32 problems: libm expm1 / log1p) keeps the relative accuracy of each
+// term near x = 0.  The fast form (bf16 problems) takes e^{-|x|} from ex2 and
+// the logarithm from __logf of 1 + coef (e - 1), each with an absolute error of
+// about 1e-7 near x = 0; summed over a row this stays at the ~1e-7 absolute
+// floor that the fp32 accumulation of every variant has anyway, so skew
+// divergences below ~1e-4 per token are resolved to about 1e-7 absolute rather
+// than to their relative tolerance (bf16 logits cannot hold distributions
+// closer than their 2^-8 resolution).
 // Paired fp32 arithmetic (fma / add / sub / mul .f32x2): one instruction for
 // two columns.
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {

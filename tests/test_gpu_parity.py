@@ -239,3 +239,33 @@ def test_sum_reduction_and_num_batch_labels():
     w = W[2].scaled(n_tokens=128, d_student=64, d_teacher=64, vocab=512)
     assert_parity(run_and_compare(w, reduction="sum"), "bf16")
     assert_parity(run_and_compare(w, num_batch_labels=1000), "bf16")
+
+
+@pytest.mark.parametrize("variant", ["skew_js", "skew_forward", "skew_reverse"])
+def test_skew_near_identical_distributions(variant):
+    """Teacher = student with one bf16 ulp of noise on a third of the logits:
+    the skew divergences are 5e-7 to 2e-4 per token.  Both the bf16 fast
+    logarithms and the fp32 precise path resolve them to about 1e-7 absolute
+    (the fp32 summation floor every variant shares; the relative tolerances hold
+    above ~1e-4)."""
+    from oracle import kd_oracle as O
+    n, v = 40, 8200
+    g = torch.Generator().manual_seed(77)
+    zs = (torch.randn(n, v, generator=g) * 4.0).to(torch.bfloat16)
+    bump = (torch.rand(n, v, generator=g) < 1 / 3).to(torch.int16)
+    zt = (zs.view(torch.int16) + bump).view(torch.bfloat16)  # next bf16 value
+    labels = torch.randint(0, v, (n,), generator=g)
+    for dtype, tol_abs, tol_rel in (("bf16", 2e-7, 2e-3), ("fp32", 1e-7, 1e-5)):
+        dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+        t = {"logits_s": zs.to(dt).cuda(), "logits_t": zt.to(dt).cuda(), "labels": labels.cuda()}
+        prob = kd.Problem(n_tokens=n, vocab=v, dtype=dtype, student="logits", teacher="logits",
+                          variant=variant, t_student=2.0, t_teacher=2.0, w_student_ce=0.0,
+                          w_kl=1.0, beta=0.1)
+        fwd = kd.forward(prob, t)
+        torch.cuda.synchronize()
+        ref = O.forward(O.as_f64(zs), O.as_f64(zt), labels.numpy(), variant=variant,
+                        t_student=2.0, t_teacher=2.0, beta=0.1, w_student_ce=0.0, w_kl=1.0)
+        got = fwd["kl"].cpu().double().numpy()
+        assert np.all(ref["kl"] > 0) and ref["kl"].max() < 3e-4
+        err = np.abs(got - ref["kl"])
+        assert np.all(err <= tol_abs + tol_rel * np.abs(ref["kl"])), (dtype, err.max())
