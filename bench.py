@@ -256,6 +256,47 @@ def time_cpu_oracle(fn, seconds):
         rows = min(4096, rows * 4, max(rows * 2, int(rows * seconds / max(dt, 1e-3))))
 
 
+def run_diag_gemm(args, rank):
+    """The tensor-core GEMM core on its own (kd_diag_gemm_bf16: C = A B^T, bf16
+    operands stored K-major, fp32 C) against torch.matmul (cuBLAS) on the same
+    bf16 operands: a check of the mainloop shared by the fused kernels."""
+    from lm_head_cross_vocab_gb300 import kd
+    lib = kd.load_library()
+    dev = torch.device("cuda", 0)
+    out = []
+    for (m, n, k) in ((8192, 8192, 8192), (4096, 6400, 6144), (16384, 8192, 4096)):
+        g = torch.Generator(device=dev).manual_seed(m + n + k)
+        a = torch.randn(m, k, generator=g, device=dev).to(torch.bfloat16)
+        b = torch.randn(n, k, generator=g, device=dev).to(torch.bfloat16)
+        c = torch.empty(m, n, device=dev, dtype=torch.float32)
+        st = torch.cuda.current_stream(dev).cuda_stream
+
+        def ours():
+            r = lib.kd_diag_gemm_bf16(a.data_ptr(), b.data_ptr(), c.data_ptr(), m, n, k, 0, st)
+            assert r == kd.KD_OK, r
+
+        def cublas():
+            torch.matmul(a, b.t())
+
+        res = {"m": m, "n": n, "k": k}
+        for name, fn in (("kd_diag_gemm_bf16", ours), ("torch_matmul", cublas)):
+            for _ in range(args.warmup):
+                fn()
+            torch.cuda.synchronize()
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record()
+            for _ in range(args.steps):
+                fn()
+            s1.record()
+            torch.cuda.synchronize()
+            res[name + "_tflops"] = 2 * m * n * k / (s0.elapsed_time(s1) / args.steps) / 1e9
+        out.append(res)
+    if rank == 0:
+        print(json.dumps({"metric": "tensor-core GEMM TFLOP/s (diagnostic)", "unit": "TFLOP/s",
+                          "dtype": "bf16", "data": "synthetic", "steps": args.steps,
+                          "warmup": args.warmup, "shapes": out}), flush=True)
+
+
 def _projection_map(v_t, v_s):
     """The synthetic cross-tokenizer token map of the projection legs: 80 % of
     the student ids reached by one teacher token, 3 % by two, the other teacher
@@ -489,6 +530,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--project", action="store_true",
                     help="time the cross-vocabulary token-map projection instead of the loss")
+    ap.add_argument("--diag-gemm", action="store_true",
+                    help="time the tensor-core GEMM core against torch.matmul (diagnostic)")
     ap.add_argument("--project-loss", action="store_true",
                     help="time cross-vocabulary distillation with the projected teacher inside "
                          "the loss (fwd + bwd)")
@@ -525,6 +568,9 @@ def main():
         return
     if args.project_loss:
         run_project_loss(args, rank)
+        return
+    if args.diag_gemm:
+        run_diag_gemm(args, rank)
         return
     if args.mix:
         run_mix(args, rank)
