@@ -541,6 +541,80 @@ __device__ __forceinline__ void js_terms2(float2 zs, float2 zt, float lse_tT, fl
   }
 }
 
+// Second sweep of the skew variants on bf16 rows, the fast form in base 2.
+// Per column, with x2 = log2 p - log2 q, the larger of p and q is
+// B = 2^max(log2 p, log2 q) and the smaller is B e, e = 2^-|x2|; m divided by
+// the larger is t = 1 + w (e - 1), w the mixture weight of the smaller (b when
+// p <= q, 1 - b otherwise), and l = log2 t.  Then, in base-2 units,
+//   p <= q:  q log(q/m) = -B l,        p log(p/m) = -B v
+//   p >  q:  p log(p/m) = -B l,        q log(q/m) = -B v,    v = e (|x2| + l)
+// so the sums of the two sides are (S + D)/2 and (S - D)/2 with S = sum B (l + v)
+// and D = sum B (v - l) sign(x2): the case split becomes a sign-bit transfer
+// (w = 1/2 + (1/2 - b) sign(x2) likewise), no compare or select per column.
+// With E_p[p/m]: p (p/m) = B g^2 / t, g = e (p <= q) or 1, 1/t = 2^-l.
+// Three transcendentals a column (two ex2 and one lg2; one more ex2 for
+// E_p[p/m]).  x2 is formed in the natural scale first (a_s - a_t + dlse, exact
+// products for power-of-two temperatures) so that it keeps its absolute
+// accuracy near 0; only the weight B comes from tempered logits minus their
+// log-normalisers.  At x2 = 0 both cases agree (e = 1, t = 1, v = l = 0), so
+// the sign of a zero does not matter.
+struct SkewK {
+  float2 its, nitt;  // 1/T_s and -1/T_t
+  float2 dl, l2e;    // dlse, log2 e
+  float2 ks, kt;     // log2 e / T_s, log2 e / T_t
+  float2 cp, cq;     // (dlse - lse_tT) log2 e, -lse_tT log2 e
+  float hb;          // 1/2 - b
+};
+__device__ __forceinline__ SkewK skew_consts(const Consts& c, float lse_tT, float dlse) {
+  SkewK k;
+  k.its = make_float2(c.inv_ts, c.inv_ts);
+  k.nitt = make_float2(-c.inv_tt, -c.inv_tt);
+  k.dl = make_float2(dlse, dlse);
+  k.l2e = make_float2(kL2E, kL2E);
+  k.ks = make_float2(c.inv_ts * kL2E, c.inv_ts * kL2E);
+  k.kt = make_float2(c.inv_tt * kL2E, c.inv_tt * kL2E);
+  const float cp = (dlse - lse_tT) * kL2E, cq = -lse_tT * kL2E;
+  k.cp = make_float2(cp, cp);
+  k.cq = make_float2(cq, cq);
+  k.hb = 0.5f - c.beta;
+  return k;
+}
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// a with the sign bit of b flipped into it (a xor (b & sign))
+__device__ __forceinline__ float sign_xor(float a, float b) {
+  return __uint_as_float(__float_as_uint(a) ^ (__float_as_uint(b) & 0x80000000u));
+}
+// Two columns: sv accumulates B (l + v), dv accumulates B (v - l) sign(x2)
+// (base 2: jq = -ln2 (sv + dv) / 2, jp = -ln2 (sv - dv) / 2); ax accumulates
+// p (p/m) when WANT_X.
+template <bool WANT_X>
+__device__ __forceinline__ void skew_pair_b2(float2 s, float2 t, const SkewK& k, float2& sv,
+                                             float2& dv, float2& ax) {
+  const float2 xn = add2(fma2(s, k.its, mul2(t, k.nitt)), k.dl);  // ln p - ln q
+  const float2 x2 = mul2(xn, k.l2e);
+  const float2 lp = fma2(s, k.ks, k.cp), lq = fma2(t, k.kt, k.cq);
+  const float2 e = make_float2(ex2(-fabsf(x2.x)), ex2(-fabsf(x2.y)));
+  const float2 B = make_float2(ex2(fmaxf(lp.x, lq.x)), ex2(fmaxf(lp.y, lq.y)));
+  // w - 1/2 = (1/2 - b) sign(x2); t = 1 + w (e - 1) = (1 + e)/2 + (w - 1/2)(e - 1)
+  const float2 h = make_float2(sign_xor(k.hb, x2.x), sign_xor(k.hb, x2.y));
+  const float2 half = make_float2(0.5f, 0.5f);
+  const float2 tt = fma2(h, add2(e, make_float2(-1.f, -1.f)), fma2(e, half, half));
+  const float2 l = make_float2(lg2(tt.x), lg2(tt.y));
+  const float2 v = mul2(e, make_float2(l.x + fabsf(x2.x), l.y + fabsf(x2.y)));
+  const float2 d = sub2(v, l);
+  sv = fma2(B, add2(l, v), sv);
+  dv = fma2(B, make_float2(sign_xor(d.x, x2.x), sign_xor(d.y, x2.y)), dv);
+  if constexpr (WANT_X) {
+    const float2 g = make_float2(x2.x <= 0.f ? e.x : 1.f, x2.y <= 0.f ? e.y : 1.f);
+    const float2 r = make_float2(ex2(-l.x), ex2(-l.y));
+    ax = fma2(mul2(mul2(B, g), g), r, ax);
+  }
+}
+
 // d KL / d a_s of the skew variants (teacher detached), from p, log(q/m),
 // log(p/m), KL(p||m) and E_p[p/m] (with (1-b) q/m + b p/m = 1):
 //   skew-JS       b p (log(p/m) - KL(p||m))

@@ -35,6 +35,9 @@ constexpr int kMergeSlots = 16;
 constexpr int kRecBytes = kMergeSlots * kCW * kRec * 4;
 constexpr int kSmem = 128 + kRingBytes + 256 + kRecBytes + 64;
 static_assert(kMergeSlots >= kStages + 4, "merge records could be reused too early");
+// control area after the ring: full / empty barriers, the abort word, the
+// merge counters, all inside its 256 bytes and apart from one another
+static_assert(16 * kStages + 16 + 4 * kMergeSlots <= 256, "ring control words overlap");
 static_assert(kSlots * 16 * kCT == kChunk, "a stage splits evenly over the consumers");
 
 template <typename T>
@@ -76,7 +79,7 @@ __device__ __forceinline__ Ring make_ring(uint8_t* smem, const StreamArgs& a) {
   r.full = ptx::smem_u32(tail);
   r.empty = r.full + 8 * kStages;
   r.abort = reinterpret_cast<volatile int*>(tail + 16 * kStages);
-  r.cnt = reinterpret_cast<int*>(tail + 128);
+  r.cnt = reinterpret_cast<int*>(tail + 16 * kStages + 16);
   r.recs = reinterpret_cast<float*>(tail + 256);
   r.bcast = r.recs + kMergeSlots * kCW * kRec;
   return r;
@@ -282,6 +285,95 @@ __device__ __forceinline__ RowOut finish_row(const StreamArgs& a, int64_t row, R
   return o;
 }
 
+// Second sweep of one row for the skew variants, once both normalisers are
+// known: per-thread partial sums (jq, jp, jx) of q log(q/m), p log(p/m) and
+// p (p/m) (the last only for want_x).
+template <typename T>
+__device__ __forceinline__ float3 skew_sweep(const Ring& R, Cursor& cur, uint32_t* status, int V,
+                                             const Consts& c, float lse_tT, float dlse,
+                                             bool want_x) {
+  constexpr int EPT = 16 / (int)sizeof(T);
+  constexpr int EPC = kChunk / (int)sizeof(T);
+  const int nch = (V + EPC - 1) / EPC, ct = threadIdx.x;
+  float jq = 0.f, jp = 0.f, jx = 0.f;
+  float2 jq2 = make_float2(0.f, 0.f), jp2 = jq2, jx2 = jq2;
+  for (int ch = 0; ch < nch; ++ch) {
+    const uint8_t* buf = cur.acquire(R, status);
+    float fs[kSlots][EPT], ft[kSlots][EPT];
+    int nv[kSlots];
+#pragma unroll
+    for (int j = 0; j < kSlots; ++j) {
+      const int slot = j * kCT + ct;
+      nv[j] = valid_cols(V - (ch * EPC + slot * EPT), EPT);
+      if (nv[j] > 0) {
+        Chunk<T>::load(buf, slot, fs[j]);
+        Chunk<T>::load(buf + kChunk, slot, ft[j]);
+      }
+    }
+    cur.release(R);
+    if (c.precise) {
+#pragma unroll
+      for (int j = 0; j < kSlots; ++j)
+#pragma unroll
+        for (int u = 0; u < EPT; ++u)
+          if (u < nv[j]) js_terms(fs[j][u], ft[j][u], lse_tT, dlse, c, jq, jp, jx, want_x);
+    } else {  // two columns per .f32x2 instruction
+#pragma unroll
+      for (int j = 0; j < kSlots; ++j)
+#pragma unroll
+        for (int u = 0; u < EPT; u += 2) {
+          if (u + 1 < nv[j]) {
+            js_terms2(make_float2(fs[j][u], fs[j][u + 1]), make_float2(ft[j][u], ft[j][u + 1]),
+                      lse_tT, dlse, c, jq2, jp2, jx2, want_x);
+          } else if (u < nv[j]) {
+            js_terms(fs[j][u], ft[j][u], lse_tT, dlse, c, jq, jp, jx, want_x);
+          }
+        }
+    }
+  }
+  return make_float3(jq + jq2.x + jq2.y, jp + jp2.x + jp2.y, jx + jx2.x + jx2.y);
+}
+
+// The same sweep over bf16 rows in the base-2 form of skew_pair_b2.  The
+// dispatch keeps bf16 rows a multiple of 8 columns, so every slot is whole.
+template <bool WANT_X>
+__device__ __forceinline__ float3 skew_sweep_bf16(const Ring& R, Cursor& cur, uint32_t* status,
+                                                  int V, const Consts& c, float lse_tT,
+                                                  float dlse) {
+  constexpr int EPT = 8, EPC = kChunk / 2;
+  const int nch = (V + EPC - 1) / EPC, ct = threadIdx.x;
+  const SkewK k = skew_consts(c, lse_tT, dlse);
+  float2 sv = make_float2(0.f, 0.f), dv = sv, ax = sv;
+  for (int ch = 0; ch < nch; ++ch) {
+    const uint8_t* buf = cur.acquire(R, status);
+    uint4 us[kSlots], ut[kSlots];
+    bool full[kSlots];
+#pragma unroll
+    for (int j = 0; j < kSlots; ++j) {
+      const int slot = j * kCT + ct;
+      full[j] = ch * EPC + slot * EPT < V;
+      if (full[j]) {
+        us[j] = *reinterpret_cast<const uint4*>(buf + slot * 16);
+        ut[j] = *reinterpret_cast<const uint4*>(buf + kChunk + slot * 16);
+      }
+    }
+    cur.release(R);
+#pragma unroll
+    for (int j = 0; j < kSlots; ++j)
+      if (full[j]) {
+        const uint32_t ws[4] = {us[j].x, us[j].y, us[j].z, us[j].w};
+        const uint32_t wt[4] = {ut[j].x, ut[j].y, ut[j].z, ut[j].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          skew_pair_b2<WANT_X>(make_float2(bf16lo(ws[i]), bf16hi(ws[i])),
+                               make_float2(bf16lo(wt[i]), bf16hi(wt[i])), k, sv, dv, ax);
+      }
+  }
+  constexpr float kHalfLn2 = 0.34657359027997264f;
+  const float S = sv.x + sv.y, D = dv.x + dv.y;
+  return make_float3(-kHalfLn2 * (S + D), -kHalfLn2 * (S - D), ax.x + ax.y);
+}
+
 // Forward.  Acc: init(); static load(Frag&, buf, slot); static pick(const
 // Frag&, i, zs, zt) (element i of a slot); step(const Frag[kSlots],
 // const int nv[kSlots], c); RowState fold(c).  Column indices within a row are
@@ -361,46 +453,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd(StreamArgs a, uint32_t* sta
       ptx::named_sync(1, kCT);
       const float dlse = R.bcast[0], lse_tT = R.bcast[1];
       const bool want_x = a.variant != KD_KL_SKEW_JS;
-      float jq = 0.f, jp = 0.f, jx = 0.f;
-      float2 jq2 = make_float2(0.f, 0.f), jp2 = jq2, jx2 = jq2;
-      for (int ch = 0; ch < nch; ++ch) {
-        const uint8_t* buf = cur.acquire(R, status);
-        float fs[kSlots][EPT], ft[kSlots][EPT];
-        int nv[kSlots];
-#pragma unroll
-        for (int j = 0; j < kSlots; ++j) {
-          const int slot = j * kCT + ct;
-          nv[j] = valid_cols(V - (ch * EPC + slot * EPT), EPT);
-          if (nv[j] > 0) {
-            Chunk<T>::load(buf, slot, fs[j]);
-            Chunk<T>::load(buf + kChunk, slot, ft[j]);
-          }
-        }
-        cur.release(R);
-        if (c.precise) {
-#pragma unroll
-          for (int j = 0; j < kSlots; ++j)
-#pragma unroll
-            for (int u = 0; u < EPT; ++u)
-              if (u < nv[j]) js_terms(fs[j][u], ft[j][u], lse_tT, dlse, c, jq, jp, jx, want_x);
-        } else {  // two columns per .f32x2 instruction
-#pragma unroll
-          for (int j = 0; j < kSlots; ++j)
-#pragma unroll
-            for (int u = 0; u < EPT; u += 2) {
-              if (u + 1 < nv[j]) {
-                js_terms2(make_float2(fs[j][u], fs[j][u + 1]), make_float2(ft[j][u], ft[j][u + 1]),
-                          lse_tT, dlse, c, jq2, jp2, jx2, want_x);
-              } else if (u < nv[j]) {
-                js_terms(fs[j][u], ft[j][u], lse_tT, dlse, c, jq, jp, jx, want_x);
-              }
-            }
-        }
+      float3 part;
+      if constexpr (sizeof(T) == 2) {  // bf16 problems take the fast (non-precise) forms
+        part = want_x ? skew_sweep_bf16<true>(R, cur, status, V, c, lse_tT, dlse)
+                      : skew_sweep_bf16<false>(R, cur, status, V, c, lse_tT, dlse);
+      } else {
+        part = skew_sweep<T>(R, cur, status, V, c, lse_tT, dlse, want_x);
       }
-      jq += jq2.x + jq2.y;
-      jp += jp2.x + jp2.y;
-      jx += jx2.x + jx2.y;
-      const float3 r = consumer_sum3(jq, jp, jx, R);
+      const float3 r = consumer_sum3(part.x, part.y, part.z, R);
       if (ct == 0) {
         const bool v_ok = !a.labels || y != a.ignore;
         a.stats[row * KD_STATS_PER_TOKEN + S_KL_PM] = r.y;

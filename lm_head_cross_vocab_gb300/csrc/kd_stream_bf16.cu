@@ -46,7 +46,9 @@ __device__ __forceinline__ uint32_t word(const uint4& u, int i) {
 }
 
 // ------------------------------------------------------------------ forward
-// KLM: bit0 forward cross sums (q d, q (e^{-d} - 1)), bit1 reverse ones.
+// KLM: bit0 forward cross sums (q d, q (e^{-d} - 1)), bit1 reverse ones,
+// bit2 only q (e^{-d} - 1) (the skew variants: the gap between the two
+// log-normalisers, to the accuracy of a single term, for their second sweep).
 // PW: 1 (T = 1, the CE sums are the tempered ones) or 2 (T = 2, e^{z-m} =
 // (e^{(z-m)/2})^2).  NEED1: labels present, so the T = 1 sums are kept.
 constexpr float kStale = 8.f;  // log2 of the largest term a stale maximum may leave
@@ -110,10 +112,8 @@ struct PackedAcc {
 #pragma unroll
       for (int j = 0; j < NS; ++j) {
         ltT[j] = mul2(ltT[j], fT);
-        if (KLM & 1) {
-          qd[j] = mul2(qd[j], fT);
-          qx[j] = mul2(qx[j], fT);
-        }
+        if (KLM & 1) qd[j] = mul2(qd[j], fT);
+        if (KLM & 5) qx[j] = mul2(qx[j], fT);
         if (NEED1) lt1[j] = mul2(lt1[j], f1);
       }
       mt = cmt;
@@ -142,10 +142,8 @@ struct PackedAcc {
       const float2 dt = sub2(t, s);
       // e^{-d} - 1 terms as (sum + e_s c_q) - e_t: the partial sum is rounded
       // at the size of one term, as fine as ex2's own error
-      if (KLM & 1) {
-        qd[J] = fma2(et, dt, qd[J]);
-        qx[J] = sub2(fma2(es, splat(cq), qx[J]), et);
-      }
+      if (KLM & 1) qd[J] = fma2(et, dt, qd[J]);
+      if (KLM & 5) qx[J] = sub2(fma2(es, splat(cq), qx[J]), et);
       if (KLM & 2) {
         pd[J] = fma2(es, dt, pd[J]);  // sum of p d: the state keeps its negative
         px[J] = sub2(fma2(et, splat(cp), px[J]), es);
@@ -331,6 +329,10 @@ bool launch_stream_fwd_packed(const StreamArgs& a, cudaStream_t s) {
   if (!packed_ok(a)) return false;
   if (a.zt == nullptr) {
     fwd_pw<false, 0>(a, s);
+    return true;
+  }
+  if (is_skew(a.variant)) {
+    fwd_pw<true, 4>(a, s);
     return true;
   }
   switch (a.c.kl_mode) {
