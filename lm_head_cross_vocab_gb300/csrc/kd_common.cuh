@@ -557,7 +557,9 @@ __device__ __forceinline__ void js_terms2(float2 zs, float2 zt, float lse_tT, fl
 // products for power-of-two temperatures) so that it keeps its absolute
 // accuracy near 0; only the weight B comes from tempered logits minus their
 // log-normalisers.  At x2 = 0 both cases agree (e = 1, t = 1, v = l = 0), so
-// the sign of a zero does not matter.
+// the sign of a zero does not matter.  A teacher logit at the lowest finite
+// value (no mass) may overflow x2 to infinity: e is then 0 and only the sign
+// of x2 and 2^-|x2| are taken from it.
 struct SkewK {
   float2 its, nitt;  // 1/T_s and -1/T_t
   float2 dl, l2e;    // dlse, log2 e
@@ -604,7 +606,10 @@ __device__ __forceinline__ void skew_pair_b2(float2 s, float2 t, const SkewK& k,
   const float2 half = make_float2(0.5f, 0.5f);
   const float2 tt = fma2(h, add2(e, make_float2(-1.f, -1.f)), fma2(e, half, half));
   const float2 l = make_float2(lg2(tt.x), lg2(tt.y));
-  const float2 v = mul2(e, make_float2(l.x + fabsf(x2.x), l.y + fabsf(x2.y)));
+  // v = e l + (e log2 e) |xn|: xn stays finite where x2 may not (a projected
+  // teacher's lowest finite logit at T_t = 1), and e = 0 there
+  const float2 el = mul2(e, l), ek = mul2(e, k.l2e);
+  const float2 v = make_float2(fmaf(ek.x, fabsf(xn.x), el.x), fmaf(ek.y, fabsf(xn.y), el.y));
   const float2 d = sub2(v, l);
   sv = fma2(B, add2(l, v), sv);
   dv = fma2(B, make_float2(sign_xor(d.x, x2.x), sign_xor(d.y, x2.y)), dv);
