@@ -278,6 +278,9 @@ __device__ __forceinline__ void store_vec(__nv_bfloat16* o, const float* r) {
 // copy starts and ends on 16 bytes.
 constexpr int kMaxC = 8;
 constexpr int kXSteps = 4;  // 8-id steps per thread: a CTA's range is at most 32 Ki ids
+// ids with several teacher tokens that a CTA keeps in a shared-memory table
+// (their receive slots; codes recv_cap + k name entry k)
+constexpr int kMCap = 1024;
 struct XLayout {
   int32_t cnt[kMaxC * kMaxC];      // edges of segment (r, q), at r * C + q
   int32_t sendoff[kMaxC * kMaxC];  // offset of segment (r, q) in CTA r's send buffer
@@ -668,6 +671,13 @@ __device__ __forceinline__ uint32_t cl_map(uint32_t a, uint32_t rank) {
 // after it every CTA has received (so every send buffer is free again) and
 // read its receive buffer (so it may be refilled); the receive barrier of the
 // next row is armed before it, so no copy can arrive early.
+//
+// Everything that depends only on the map stays on chip across rows: each
+// thread's output codes in registers, and, for up to kMCap ids with several
+// teacher tokens, their id and (with two tokens) both receive slots in a
+// shared-memory table, so a row's output needs no global loads but its own
+// gather list.  That list is read one 8-slot step ahead of the gather (the
+// first step before the slice wait).
 template <typename TI, typename TO>
 __global__ void __launch_bounds__(kPT, 1)
     k_project_exchange(const TI* __restrict__ zt, int64_t n, int64_t vt, int64_t vs,
@@ -675,12 +685,15 @@ __global__ void __launch_bounds__(kPT, 1)
                        const int32_t* __restrict__ epos, const int32_t* __restrict__ code,
                        const int32_t* __restrict__ mpre, const int32_t* __restrict__ mlist,
                        const int32_t* __restrict__ mcode, const int32_t* __restrict__ send_src,
-                       const XLayout* __restrict__ X, int64_t sc, int64_t so, int64_t send_cap,
-                       TO* __restrict__ out, uint32_t* status) {
+                       const XLayout* __restrict__ X, int64_t sc, int64_t so,
+                       int64_t send_cap, int64_t recv_cap, TO* __restrict__ out,
+                       uint32_t* status) {
   if (!X->fits) return;  // the slice path runs instead
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[2];  // 0: the staged slice, 1: the receive buffer
   __shared__ int abort_flag;
+  __shared__ uint32_t mtab[kMCap];  // ids with several teacher tokens: 2 receive slots, or ~0
+  __shared__ uint16_t mid[kMCap];   // ... their offsets in this CTA's id range
   const uint32_t r = cl_rank(), C = cl_size();
   const int64_t ncl = gridDim.x / C;
   TI* const slice = reinterpret_cast<TI*>(smem_raw);
@@ -693,11 +706,21 @@ __global__ void __launch_bounds__(kPT, 1)
   const int32_t* gl = send_src + X->sendbase[r];
   const uint32_t rx_bytes = (uint32_t)X->recvtot[r] * (uint32_t)sizeof(TI);
   const uint32_t bar_s = ptx::smem_u32(&bars[0]), bar_r = ptx::smem_u32(&bars[1]);
+  const uint32_t rcap = (uint32_t)recv_cap;  // < 0xfffe (planned)
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar_s, 1);
     ptx::mbar_init(bar_r, 1);
     ptx::fence_mbar_init();
     abort_flag = 0;
+  }
+  // ids with several teacher tokens: the first kMCap of this CTA's range get a
+  // table entry (two receive slots; ~0 for three or more tokens)
+  const int32_t m_lo = mpre[i_lo < i_hi ? i_lo : i_hi], m_hi = mpre[i_hi];
+  const int32_t nm = m_hi - m_lo < kMCap ? m_hi - m_lo : kMCap;
+  for (int32_t k = threadIdx.x; k < nm; k += kPT) {
+    const int32_t m = -2 - mcode[m_lo + k], e0 = m >> 3;
+    mtab[k] = (m & 7) == 0 ? ((uint32_t)epos[e0] | ((uint32_t)epos[e0 + 1] << 16)) : ~0u;
+    mid[k] = (uint16_t)(mlist[m_lo + k] - i_lo);
   }
   __syncthreads();
   // (returns whether some columns were plain-loaded: the wait then needs a
@@ -726,7 +749,10 @@ __global__ void __launch_bounds__(kPT, 1)
   cl_sync();  // every receive barrier is armed before any copy is sent
   // this thread's output ids are the same in every row: their codes, two
   // 16-bit slots per register, are loaded once (ranges longer than
-  // kXSteps * 8 * kPT ids are not planned for this kernel)
+  // kXSteps * 8 * kPT ids are not planned for this kernel).  A code below
+  // rcap is the receive slot of the id's single teacher token; 0xfffe marks
+  // an id with several (written by the pass after the output), 0xffff one
+  // that no teacher token reaches.
   uint32_t c16[kXSteps][4];
 #pragma unroll
   for (int u = 0; u < kXSteps; ++u) {
@@ -741,10 +767,26 @@ __global__ void __launch_bounds__(kPT, 1)
       c16[u][q >> 1] = (c16[u][q >> 1] & ~(0xffffu << (16 * (q & 1)))) | (h << (16 * (q & 1)));
     }
   }
+  // an id with several teacher tokens, folded from its edges in global memory
+  auto fold = [&](int64_t id) -> float {
+    const int32_t m = -2 - code[id], e0 = m >> 3;
+    const int32_t e1 = (m & 7) == 7 ? off[id + 1] : e0 + (m & 7) + 2;
+    float x = -INFINITY;
+#pragma unroll 1
+    for (int32_t e = e0; e < e1; ++e) x = logaddexp(x, ld<TI>(recv + epos[e]) * inv_t);
+    return x;
+  };
   uint32_t ps = 0, pr = 0;
   int pend = 0;  // bit 0 / 1: a wait on the slice / receive barrier gave up
   uint32_t pend_ps = 0, pend_pr = 0;
+  const int32_t t_first = (int32_t)threadIdx.x * 8;
   for (int64_t row = first; row < n; row += ncl) {
+    // the gather list's first step (the same in every row), ahead of the wait
+    int4 ga = make_int4(0, 0, 0, 0), gb = ga;
+    if (t_first < nsend) {
+      ga = reinterpret_cast<const int4*>(gl + t_first)[0];
+      gb = reinterpret_cast<const int4*>(gl + t_first)[1];
+    }
     if (!ptx::warp_wait(bar_s, ps, &abort_flag, status) && !(pend & 1)) {
       pend |= 1;
       pend_ps = ps;
@@ -752,10 +794,14 @@ __global__ void __launch_bounds__(kPT, 1)
     ps ^= 1u;
     if (plain) __syncthreads();  // the plain-loaded columns too
     // 8 slots per thread step: nsend, the list start and send are multiples of 8
-    for (int32_t t0 = (int32_t)threadIdx.x * 8; t0 < nsend; t0 += kPT * 8) {
-      const int4 a = reinterpret_cast<const int4*>(gl + t0)[0];
-      const int4 b = reinterpret_cast<const int4*>(gl + t0)[1];
-      const int32_t g[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    for (int32_t t0 = t_first; t0 < nsend; t0 += kPT * 8) {
+      const int32_t t1 = t0 + kPT * 8;
+      int4 na = ga, nb = gb;
+      if (t1 < nsend) {
+        na = reinterpret_cast<const int4*>(gl + t1)[0];
+        nb = reinterpret_cast<const int4*>(gl + t1)[1];
+      }
+      const int32_t g[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
       TI v[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) v[q] = slice[g[q]];
@@ -765,6 +811,8 @@ __global__ void __launch_bounds__(kPT, 1)
         reinterpret_cast<uint4*>(send + t0)[0] = reinterpret_cast<const uint4*>(v)[0];
         reinterpret_cast<uint4*>(send + t0)[1] = reinterpret_cast<const uint4*>(v)[1];
       }
+      ga = na;
+      gb = nb;
     }
     __syncthreads();  // send is complete; the slice is free for the next row
     if (row + ncl < n) plain = stage(row + ncl);
@@ -799,9 +847,9 @@ __global__ void __launch_bounds__(kPT, 1)
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const uint32_t cq = (c16[u][q >> 1] >> (16 * (q & 1))) & 0xffffu;
-        // (0xffff: no teacher token; 0xfffe: several, written by the pass below)
-        const float x = cq < 0xfffeu ? ld<TI>(recv + cq) * inv_t : -INFINITY;
-        v[q] = x > -INFINITY ? x : lowest<TO>();
+        // slot 0 stands in for ids without a single slot (always in bounds)
+        const float x = ld<TI>(recv + (cq < rcap ? cq : 0u)) * inv_t;
+        v[q] = cq < rcap && x > -INFINITY ? x : lowest<TO>();
       }
       if (j0 + 8 <= i_hi && (reinterpret_cast<uintptr_t>(o + j0) & 15) == 0) {
         store_vec(o + j0, v);
@@ -815,13 +863,17 @@ __global__ void __launch_bounds__(kPT, 1)
     // column order and overwrite the placeholders above (same CTA, after the
     // barrier, so the later store wins; the sectors are already whole)
     __syncthreads();
-    const int32_t m1 = mpre[i_hi];  // (i_hi <= vs; a CTA past the last id has i_lo > vs)
-    for (int32_t t = mpre[i_lo < i_hi ? i_lo : i_hi] + (int32_t)threadIdx.x; t < m1; t += kPT) {
-      const int32_t id = mlist[t], m = -2 - mcode[t], e0 = m >> 3;
-      const int32_t e1 = (m & 7) == 7 ? off[id + 1] : e0 + (m & 7) + 2;
-      float x = -INFINITY;
-#pragma unroll 1
-      for (int32_t e = e0; e < e1; ++e) x = logaddexp(x, ld<TI>(recv + epos[e]) * inv_t);
+    for (int32_t k = threadIdx.x; k < m_hi - m_lo; k += kPT) {
+      float x;
+      int64_t id;
+      const uint32_t e = k < nm ? mtab[k] : ~0u;
+      if (e != ~0u) {  // two tokens, both slots from the table
+        id = i_lo + mid[k];
+        x = logaddexp(ld<TI>(recv + (e & 0xffffu)) * inv_t, ld<TI>(recv + (e >> 16)) * inv_t);
+      } else {  // three or more tokens, or beyond the table: edges from global memory
+        id = k < nm ? i_lo + mid[k] : mlist[m_lo + k];
+        x = fold(id);
+      }
       st<TO>(o + id, x > -INFINITY ? x : lowest<TO>());
     }
     if (threadIdx.x == 0 && row + ncl < n) ptx::mbar_expect_tx(bar_r, rx_bytes);
@@ -853,7 +905,6 @@ __global__ void __launch_bounds__(kPT, 1)
 constexpr int kLT = 512;  // threads of the fused kernel (128 registers each)
 // Student ids with several teacher tokens, per CTA, whose folded value is kept
 // in shared memory for the row (beyond this, an id folds from global memory).
-constexpr int kMCap = 1024;
 constexpr int64_t kPLSmem = 212 * 1024;  // dynamic shared memory of the fused kernel
 struct PLParams {
   const void* zt;      // [n, vt] teacher logits
@@ -1150,17 +1201,29 @@ __global__ void __launch_bounds__(kLT, 1) k_proj_loss(const __grid_constant__ PL
   int pend = 0;
   uint32_t pend_ps = 0, pend_pr = 0;
   int lr = 0;  // local row count (parity selects the merge slots)
+  const int32_t t_first = (int32_t)threadIdx.x * 8;
   for (int64_t row = first; row < n; row += ncl, ++lr) {
+    // the gather list's first step (the same in every row), ahead of the wait;
+    // later steps are loaded one step ahead of the gather
+    int4 ga = make_int4(0, 0, 0, 0), gb = ga;
+    if (t_first < nsend) {
+      ga = reinterpret_cast<const int4*>(gl + t_first)[0];
+      gb = reinterpret_cast<const int4*>(gl + t_first)[1];
+    }
     if (!ptx::warp_wait(bar_s, ps, &abort_flag, status) && !(pend & 1)) {
       pend |= 1;
       pend_ps = ps;
     }
     ps ^= 1u;
     if (plain) __syncthreads();
-    for (int32_t t0 = (int32_t)threadIdx.x * 8; t0 < nsend; t0 += kLT * 8) {
-      const int4 a = reinterpret_cast<const int4*>(gl + t0)[0];
-      const int4 b = reinterpret_cast<const int4*>(gl + t0)[1];
-      const int32_t g[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    for (int32_t t0 = t_first; t0 < nsend; t0 += kLT * 8) {
+      const int32_t t1 = t0 + kLT * 8;
+      int4 na = ga, nb = gb;
+      if (t1 < nsend) {
+        na = reinterpret_cast<const int4*>(gl + t1)[0];
+        nb = reinterpret_cast<const int4*>(gl + t1)[1];
+      }
+      const int32_t g[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
       TI v[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) v[q] = slice[g[q]];
@@ -1170,6 +1233,8 @@ __global__ void __launch_bounds__(kLT, 1) k_proj_loss(const __grid_constant__ PL
         reinterpret_cast<uint4*>(send + t0)[0] = reinterpret_cast<const uint4*>(v)[0];
         reinterpret_cast<uint4*>(send + t0)[1] = reinterpret_cast<const uint4*>(v)[1];
       }
+      ga = na;
+      gb = nb;
     }
     __syncthreads();  // send is complete; the slice is free for the next row
     if (row + ncl < n) plain = stage(row + ncl);
@@ -1472,7 +1537,8 @@ int launch_exchange(const XPlan& P, const void* zt, int64_t n, int64_t vt, int64
   note_launch();
   return cudaLaunchKernelEx(&cfg, k_project_exchange<TI, TO>, static_cast<const TI*>(zt), n, vt,
                             vs, inv_t, off, epos, code, mpre, mlist, mcode, send_src, X, P.sc,
-                            P.so, P.send_cap, static_cast<TO*>(out), status) != cudaSuccess;
+                            P.so, P.send_cap, P.recv_cap, static_cast<TO*>(out),
+                            status) != cudaSuccess;
 }
 
 template <typename TI, typename TO>
@@ -1515,7 +1581,8 @@ void launch_scan(const int32_t* in, int64_t n, int32_t* out, int32_t* tmp, cudaS
 // The inverse map (count -> scan -> scatter -> per-id sort) and, with an
 // exchange plan, the exchange lists (segments, send lists, receive slots,
 // per-id codes); `multi`: also the list of ids with several teacher tokens
-// (the unfused exchange kernel writes those in a second pass).  Returns 1 on a
+// (the exchange kernels fold those in a pass of their own, from a table in
+// shared memory for the first kMCap of a CTA's range).  Returns 1 on a
 // CUDA error.
 int build_maps(const int32_t* token_map, int64_t vt, int64_t vs, char* ws, const ProjLayout& L,
                const XPlan* xp, bool multi, uint32_t* dev_status, cudaStream_t s) {
