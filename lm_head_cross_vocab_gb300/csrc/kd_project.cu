@@ -660,6 +660,41 @@ __device__ __forceinline__ uint32_t cl_map(uint32_t a, uint32_t rank) {
   return a;
 }
 
+// A CTA's outgoing segments, read once from the exchange layout: for each
+// destination CTA q, the mapped receive address and barrier, the local
+// source and the byte count (0: nothing to send).  Per row only thread 0
+// reads them, from shared memory, so shipping a row's segments waits on no
+// global load.
+struct SendDesc {
+  uint32_t dst[kMaxC], bar[kMaxC], src[kMaxC], bytes[kMaxC];
+};
+template <typename TI>
+__device__ __forceinline__ void send_desc_init(SendDesc& d, const XLayout* X, uint32_t r,
+                                               uint32_t C, const TI* send, const TI* recv,
+                                               uint32_t bar_r) {
+  const uint32_t q = threadIdx.x;
+  if (q < C) {
+    const int k = (int)(r * C + q);
+    d.bytes[q] = (uint32_t)pad8(X->cnt[k]) * (uint32_t)sizeof(TI);
+    d.dst[q] = cl_map(ptx::smem_u32(recv + X->recvoff[k]), q);
+    d.bar[q] = cl_map(bar_r, q);
+    d.src[q] = ptx::smem_u32(send + X->sendoff[k]);
+  }
+}
+// Thread 0, after the CTA barrier that completes the send buffer: one
+// shared::cta -> shared::cluster bulk copy per non-empty segment.
+__device__ __forceinline__ void send_segments(const SendDesc& d, uint32_t C) {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  for (uint32_t q = 0; q < C; ++q) {
+    if (d.bytes[q] == 0) continue;
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];" ::"r"(d.dst[q]),
+        "r"(d.src[q]), "r"(d.bytes[q]), "r"(d.bar[q])
+        : "memory");
+  }
+}
+
 // Exchange path.  A cluster of C CTAs takes one token row at a time.  CTA r
 // stages its slice of the teacher row (one bulk copy; the next row's copy
 // starts as soon as the gather below has read the slice), gathers the values
@@ -694,6 +729,7 @@ __global__ void __launch_bounds__(kPT, 1)
   __shared__ int abort_flag;
   __shared__ uint32_t mtab[kMCap];  // ids with several teacher tokens: 2 receive slots, or ~0
   __shared__ uint16_t mid[kMCap];   // ... their offsets in this CTA's id range
+  __shared__ SendDesc sd;
   const uint32_t r = cl_rank(), C = cl_size();
   const int64_t ncl = gridDim.x / C;
   TI* const slice = reinterpret_cast<TI*>(smem_raw);
@@ -713,6 +749,7 @@ __global__ void __launch_bounds__(kPT, 1)
     ptx::fence_mbar_init();
     abort_flag = 0;
   }
+  send_desc_init<TI>(sd, X, r, C, send, recv, bar_r);
   // ids with several teacher tokens: the first kMCap of this CTA's range get a
   // table entry (two receive slots; ~0 for three or more tokens)
   const int32_t m_lo = mpre[i_lo < i_hi ? i_lo : i_hi], m_hi = mpre[i_hi];
@@ -816,22 +853,7 @@ __global__ void __launch_bounds__(kPT, 1)
     }
     __syncthreads();  // send is complete; the slice is free for the next row
     if (row + ncl < n) plain = stage(row + ncl);
-    if (threadIdx.x == 0 && !*reinterpret_cast<volatile int*>(&abort_flag)) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      for (uint32_t q = 0; q < C; ++q) {
-        const int k = (int)(r * C + q);
-        const int32_t len = pad8(X->cnt[k]);
-        if (len == 0) continue;
-        const uint32_t dst = cl_map(ptx::smem_u32(recv + X->recvoff[k]), q);
-        const uint32_t mb = cl_map(bar_r, q);
-        asm volatile(
-            "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], "
-            "%2, [%3];" ::"r"(dst),
-            "r"(ptx::smem_u32(send + X->sendoff[k])), "r"((uint32_t)len * (uint32_t)sizeof(TI)),
-            "r"(mb)
-            : "memory");
-      }
-    }
+    if (threadIdx.x == 0 && !*reinterpret_cast<volatile int*>(&abort_flag)) send_segments(sd, C);
     if (!ptx::warp_wait(bar_r, pr, &abort_flag, status) && !(pend & 2)) {
       pend |= 2;
       pend_pr = pr;
@@ -1122,6 +1144,7 @@ __global__ void __launch_bounds__(kLT, 1) k_proj_loss(const __grid_constant__ PL
   __shared__ float bc[2][2];                               // skew: dlse, lse(a_t) from CTA 0
   __shared__ uint32_t mtab[kMCap];  // ids with several teacher tokens: 2 receive slots, or ~0
   __shared__ float mval[kMCap];     // ... their folded (tempered) values in the current row
+  __shared__ SendDesc sd;
   const uint32_t r = cl_rank(), C = cl_size();
   const int64_t ncl = gridDim.x / C;
   const int64_t n = P.n, vt = P.vt, vs = P.vs, sc = P.sc;
@@ -1144,6 +1167,7 @@ __global__ void __launch_bounds__(kLT, 1) k_proj_loss(const __grid_constant__ PL
     ptx::fence_mbar_init();
     abort_flag = 0;
   }
+  send_desc_init<TI>(sd, X, r, C, send, recv, bar_r);
   __syncthreads();
   auto stage = [&](int64_t row) -> bool {
     const TI* src = zt + row * vt + c0;
@@ -1238,22 +1262,7 @@ __global__ void __launch_bounds__(kLT, 1) k_proj_loss(const __grid_constant__ PL
     }
     __syncthreads();  // send is complete; the slice is free for the next row
     if (row + ncl < n) plain = stage(row + ncl);
-    if (threadIdx.x == 0 && !*reinterpret_cast<volatile int*>(&abort_flag)) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      for (uint32_t q = 0; q < C; ++q) {
-        const int k = (int)(r * C + q);
-        const int32_t len = pad8(X->cnt[k]);
-        if (len == 0) continue;
-        const uint32_t dst = cl_map(ptx::smem_u32(recv + X->recvoff[k]), q);
-        const uint32_t mb = cl_map(bar_r, q);
-        asm volatile(
-            "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], "
-            "%2, [%3];" ::"r"(dst),
-            "r"(ptx::smem_u32(send + X->sendoff[k])), "r"((uint32_t)len * (uint32_t)sizeof(TI)),
-            "r"(mb)
-            : "memory");
-      }
-    }
+    if (threadIdx.x == 0 && !*reinterpret_cast<volatile int*>(&abort_flag)) send_segments(sd, C);
     if (!ptx::warp_wait(bar_r, pr, &abort_flag, status) && !(pend & 2)) {
       pend |= 2;
       pend_pr = pr;
