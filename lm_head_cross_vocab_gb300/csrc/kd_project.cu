@@ -852,8 +852,9 @@ __global__ void __launch_bounds__(kPT, 1)
       gb = nb;
     }
     __syncthreads();  // send is complete; the slice is free for the next row
-    if (row + ncl < n) plain = stage(row + ncl);
+    // the segments first (the cluster waits on them), then the next row's slice
     if (threadIdx.x == 0 && !*reinterpret_cast<volatile int*>(&abort_flag)) send_segments(sd, C);
+    if (row + ncl < n) plain = stage(row + ncl);
     if (!ptx::warp_wait(bar_r, pr, &abort_flag, status) && !(pend & 2)) {
       pend |= 2;
       pend_pr = pr;
@@ -1261,8 +1262,9 @@ __global__ void __launch_bounds__(kLT, 1) k_proj_loss(const __grid_constant__ PL
       gb = nb;
     }
     __syncthreads();  // send is complete; the slice is free for the next row
-    if (row + ncl < n) plain = stage(row + ncl);
+    // the segments first (the cluster waits on them), then the next row's slice
     if (threadIdx.x == 0 && !*reinterpret_cast<volatile int*>(&abort_flag)) send_segments(sd, C);
+    if (row + ncl < n) plain = stage(row + ncl);
     if (!ptx::warp_wait(bar_r, pr, &abort_flag, status) && !(pend & 2)) {
       pend |= 2;
       pend_pr = pr;
