@@ -70,6 +70,19 @@ __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); 
 
 __device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+// raw bf16x2 words: the larger of each half; x rounded toward -inf into both
+// halves; two -inf
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bf16x2_floor(float x) {
+  uint16_t h;
+  asm("cvt.rm.bf16.f32 %0, %1;" : "=h"(h) : "f"(x));
+  return ((uint32_t)h << 16) | h;
+}
+constexpr uint32_t kNegInfX2 = 0xff80ff80u;
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);

@@ -199,16 +199,8 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
-// 8 consecutive staged values (16-byte aligned shared memory) as floats
-__device__ __forceinline__ void ld8(const __nv_bfloat16* p, float v[8]) {
-  const uint4 u = *reinterpret_cast<const uint4*>(p);
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[2 * i] = __uint_as_float(w[i] << 16);
-    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
-}
+// 8 consecutive staged fp32 values (16-byte aligned shared memory); bf16
+// teachers take the packed passes below
 __device__ __forceinline__ void ld8(const float* p, float v[8]) {
   const float4 a = reinterpret_cast<const float4*>(p)[0];
   const float4 b = reinterpret_cast<const float4*>(p)[1];
@@ -311,6 +303,165 @@ __device__ __forceinline__ void pass2_8(const MixParams& P, const TI* zs, const 
   for (int q = 0; q < 8; ++q) r[q] = r[q] > kNoMass ? r[q] : lowest_of<TO>();
 }
 
+// Packed passes for bf16 teachers: 32-bit slice indices, the values of a
+// step taken as raw bf16x2 words, the fp32 work on f32x2 pairs (one
+// instruction for two columns).
+constexpr float kStaleMix = 8.f;  // log2 of the largest term a stale offset may leave
+
+__device__ __forceinline__ float2 unpack2(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
+
+// Pass 1, packed: this thread's (max, sum of exp) of one stream over the
+// staged columns [lo, hi).  The sum is kept around an offset m that moves only
+// when a step's maximum passes it by kStaleMix in base 2 (so no term exceeds
+// 2^8; the sum is rescaled then): for a teacher stream the test runs on the
+// raw words (max.bf16x2 against a threshold rounded down), for g on floats.
+// Values at or below kNoMass never move the offset and add 0.
+template <bool GEO>
+__device__ __forceinline__ Lse pass1_bf16(const MixParams& P, const __nv_bfloat16* zs, int t,
+                                          int lo, int hi, Lse acc) {
+  const int sc = (int)P.sc;
+  float m = acc.m;
+  float2 s2 = make_float2(acc.s, 0.f);
+  float2 om = make_float2(-m * kL2E, -m * kL2E);
+  uint32_t th = m > -INFINITY ? bf16x2_floor(m + kStaleMix * kLN2) : kNegInfX2;
+  const float2 l2e = make_float2(kL2E, kL2E);
+  for (int j0 = lo + (int)threadIdx.x * 8; j0 < hi; j0 += kMT * 8) {
+    const bool tail = j0 + 8 > hi;
+    float2 x[4];
+    float m8;
+    bool up;
+    if (!GEO) {
+      const uint4 u = *reinterpret_cast<const uint4*>(zs + t * sc + j0);
+      uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      if (tail) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (j0 + 2 * i >= hi) w[i] = kNegInfX2;
+          else if (j0 + 2 * i + 1 >= hi) w[i] = (w[i] & 0xffffu) | 0xff800000u;
+        }
+      }
+      const uint32_t mx = max_bf16x2(max_bf16x2(w[0], w[1]), max_bf16x2(w[2], w[3]));
+      up = max_bf16x2(mx, th) != th;
+      m8 = fmaxf(bf16lo(mx), bf16hi(mx));
+#pragma unroll
+      for (int i = 0; i < 4; ++i) x[i] = unpack2(w[i]);
+    } else {  // g = sum_k w_k z_k
+      const uint4 u = *reinterpret_cast<const uint4*>(zs + j0);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      const float2 w0 = make_float2(P.w[0], P.w[0]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) x[i] = mul2(unpack2(w[i]), w0);
+      for (int k = 1; k < P.k; ++k) {
+        const uint4 v = *reinterpret_cast<const uint4*>(zs + k * sc + j0);
+        const uint32_t y[4] = {v.x, v.y, v.z, v.w};
+        const float2 wk = make_float2(P.w[k], P.w[k]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[i] = fma2(unpack2(y[i]), wk, x[i]);
+      }
+      if (tail) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (j0 + 2 * i >= hi) x[i].x = -INFINITY;
+          if (j0 + 2 * i + 1 >= hi) x[i].y = -INFINITY;
+        }
+      }
+      m8 = fmaxf(fmaxf(fmaxf(x[0].x, x[0].y), fmaxf(x[1].x, x[1].y)),
+                 fmaxf(fmaxf(x[2].x, x[2].y), fmaxf(x[3].x, x[3].y)));
+      up = m8 > m + kStaleMix * kLN2 || !(m > -INFINITY);
+    }
+    if (up && m8 > m && m8 > kNoMass) {
+      const float f = ex2((m - m8) * kL2E);  // 0 while m is still -inf (s is 0 then too)
+      s2 = mul2(s2, make_float2(f, f));
+      m = m8;
+      om = make_float2(-m * kL2E, -m * kL2E);
+      th = bf16x2_floor(m + kStaleMix * kLN2);
+    }
+    if (m > -INFINITY) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 a = fma2(x[i], l2e, om);
+        s2 = add2(s2, make_float2(ex2(a.x), ex2(a.y)));
+      }
+    }
+  }
+  return {m, s2.x + s2.y};
+}
+
+// Pass 2, packed: 8 output values at columns j0.. (as pass2_8) from the row
+// logsumexps lse_sh[] (per teacher, or of g in slot 0).
+template <bool GEO, typename TO>
+__device__ __forceinline__ void pass2_bf16(const MixParams& P, const __nv_bfloat16* zs,
+                                           const float* lse_sh, int j0, float r[8]) {
+  const int sc = (int)P.sc;
+  float2 res[4];
+  const uint4 u0 = *reinterpret_cast<const uint4*>(zs + j0);
+  const uint32_t w0[4] = {u0.x, u0.y, u0.z, u0.w};
+  if (GEO) {
+    const float2 wt = make_float2(P.w[0], P.w[0]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) res[i] = mul2(unpack2(w0[i]), wt);
+    for (int k = 1; k < P.k; ++k) {
+      const uint4 v = *reinterpret_cast<const uint4*>(zs + k * sc + j0);
+      const uint32_t y[4] = {v.x, v.y, v.z, v.w};
+      const float2 wk = make_float2(P.w[k], P.w[k]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) res[i] = fma2(unpack2(y[i]), wk, res[i]);
+    }
+    const float2 nl = make_float2(-lse_sh[0], -lse_sh[0]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) res[i] = add2(res[i], nl);
+  } else {
+    // log sum_k exp(t_k), t_k = z_k - lse_k + log w_k, in base 2 around the
+    // running maximum (K - 1 exponentials, one logarithm); z_k - lse_k first,
+    // exact for a row's dominant token; terms clamped below at kNoMass
+    constexpr float kFloor = kNoMass * kL2E;
+    const float2 l2e = make_float2(kL2E, kL2E);
+    float2 m[4], sum[4];
+    {
+      const float lw = P.lw[0] * kL2E;
+      const float2 l = make_float2(lse_sh[0], lse_sh[0]), w = make_float2(lw, lw);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 tt = fma2(sub2(unpack2(w0[i]), l), l2e, w);
+        m[i] = make_float2(fmaxf(tt.x, kFloor), fmaxf(tt.y, kFloor));
+        sum[i] = make_float2(1.f, 1.f);
+      }
+    }
+    for (int k = 1; k < P.k; ++k) {
+      const uint4 v = *reinterpret_cast<const uint4*>(zs + k * sc + j0);
+      const uint32_t y[4] = {v.x, v.y, v.z, v.w};
+      const float lw = P.lw[k] * kL2E;
+      const float2 l = make_float2(lse_sh[k], lse_sh[k]), w = make_float2(lw, lw);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 tt = fma2(sub2(unpack2(y[i]), l), l2e, w);
+        const float2 t2 = make_float2(fmaxf(tt.x, kFloor), fmaxf(tt.y, kFloor));
+        const float2 d = sub2(t2, m[i]);
+        const float2 e = make_float2(ex2(-fabsf(d.x)), ex2(-fabsf(d.y)));
+        if (P.k == 2) {  // the sum starts at 1: either order gives 1 + e
+          sum[i] = add2(sum[i], e);
+        } else {
+          sum[i].x = d.x > 0.f ? fmaf(sum[i].x, e.x, 1.f) : sum[i].x + e.x;
+          sum[i].y = d.y > 0.f ? fmaf(sum[i].y, e.y, 1.f) : sum[i].y + e.y;
+        }
+        m[i] = make_float2(fmaxf(m[i].x, t2.x), fmaxf(m[i].y, t2.y));
+      }
+    }
+    const float2 ln2 = make_float2(kLN2, kLN2);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 rr = mul2(add2(m[i], make_float2(lg2(sum[i].x), lg2(sum[i].y))), ln2);
+      res[i].x = m[i].x > kFloor ? rr.x : -INFINITY;
+      res[i].y = m[i].y > kFloor ? rr.y : -INFINITY;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    r[2 * i] = res[i].x > kNoMass ? res[i].x : lowest_of<TO>();
+    r[2 * i + 1] = res[i].y > kNoMass ? res[i].y : lowest_of<TO>();
+  }
+}
+
 // Cluster kernel: see the top of this file.  Rows are taken cluster by
 // cluster (all CTAs of a cluster loop over the same rows, so the cluster
 // barriers match).  A CTA's columns are staged in two halves, each with its
@@ -405,9 +556,16 @@ __global__ void __launch_bounds__(kMT, WIDE ? 1 : 2) k_mix_cluster(const MixPara
     // every stream's pair folded per thread, then per warp (shuffles), then
     // across the warps by one thread per stream: one CTA barrier for all
     for (int t = 0; t < nstreams; ++t) {
-      Lse a = pass1<GEO>(P, zs, t, 0, h0, Lse{-INFINITY, 0.f});
-      if (t == 0) wait_half(1);
-      a = pass1<GEO>(P, zs, t, h0, clen, a);
+      Lse a;
+      if constexpr (sizeof(TI) == 2) {  // bf16 teachers: the packed pass
+        a = pass1_bf16<GEO>(P, zs, t, 0, (int)h0, Lse{-INFINITY, 0.f});
+        if (t == 0) wait_half(1);
+        a = pass1_bf16<GEO>(P, zs, t, (int)h0, (int)clen, a);
+      } else {
+        a = pass1<GEO>(P, zs, t, 0, h0, Lse{-INFINITY, 0.f});
+        if (t == 0) wait_half(1);
+        a = pass1<GEO>(P, zs, t, h0, clen, a);
+      }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1)
         a = lse_merge(a, Lse{__shfl_xor_sync(0xffffffffu, a.m, o),
@@ -452,7 +610,10 @@ __global__ void __launch_bounds__(kMT, WIDE ? 1 : 2) k_mix_cluster(const MixPara
       const int64_t lo = hh ? h0 : 0, hi = hh ? clen : h0;
       for (int64_t j0 = lo + (int64_t)threadIdx.x * 8; j0 < hi; j0 += (int64_t)kMT * 8) {
         float r[8];
-        pass2_8<GEO, TI, TO>(P, zs, off_sh, j0, r);
+        if constexpr (sizeof(TI) == 2)
+          pass2_bf16<GEO, TO>(P, zs, off_sh, (int)j0, r);
+        else
+          pass2_8<GEO, TI, TO>(P, zs, off_sh, j0, r);
         if (ov && j0 + 8 <= hi) {
           if constexpr (sizeof(TO) == 4) {
             reinterpret_cast<float4*>(o + j0)[0] = make_float4(r[0], r[1], r[2], r[3]);

@@ -20,11 +20,6 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 
-__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
 __device__ __forceinline__ float2 splat(float v) { return make_float2(v, v); }
 __device__ __forceinline__ float2 unpack(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
 __device__ __forceinline__ float2 ex2x2(float2 v) { return make_float2(ex2(v.x), ex2(v.y)); }
@@ -34,13 +29,6 @@ __device__ __forceinline__ uint32_t max4w(const uint4& u) {
   return max_bf16x2(max_bf16x2(u.x, u.y), max_bf16x2(u.z, u.w));
 }
 __device__ __forceinline__ float hmax(uint32_t w) { return fmaxf(bf16lo(w), bf16hi(w)); }
-// bf16x2 with x rounded toward -inf in both halves
-__device__ __forceinline__ uint32_t bf16x2_floor(float x) {
-  uint16_t h;
-  asm("cvt.rm.bf16.f32 %0, %1;" : "=h"(h) : "f"(x));
-  return ((uint32_t)h << 16) | h;
-}
-constexpr uint32_t kNegInfX2 = 0xff80ff80u;  // -inf, -inf as bf16x2
 __device__ __forceinline__ uint32_t word(const uint4& u, int i) {
   return i == 0 ? u.x : (i == 1 ? u.y : (i == 2 ? u.z : u.w));
 }
