@@ -316,10 +316,11 @@ __device__ __forceinline__ float2 unpack2(uint32_t w) { return make_float2(bf16l
 // 2^8; the sum is rescaled then): for a teacher stream the test runs on the
 // raw words (max.bf16x2 against a threshold rounded down), for g on floats.
 // Values at or below kNoMass never move the offset and add 0.
-template <bool GEO>
+template <bool GEO, int KT>
 __device__ __forceinline__ Lse pass1_bf16(const MixParams& P, const __nv_bfloat16* zs, int t,
                                           int lo, int hi, Lse acc) {
   const int sc = (int)P.sc;
+  const int K = KT ? KT : P.k;  // KT: the teacher count when fixed at compile time
   float m = acc.m;
   float2 s2 = make_float2(acc.s, 0.f);
   float2 om = make_float2(-m * kL2E, -m * kL2E);
@@ -351,7 +352,9 @@ __device__ __forceinline__ Lse pass1_bf16(const MixParams& P, const __nv_bfloat1
       const float2 w0 = make_float2(P.w[0], P.w[0]);
 #pragma unroll
       for (int i = 0; i < 4; ++i) x[i] = mul2(unpack2(w[i]), w0);
-      for (int k = 1; k < P.k; ++k) {
+#pragma unroll
+      for (int k = 1; k < (KT ? KT : kMaxT); ++k) {
+        if (!KT && k >= K) break;
         const uint4 v = *reinterpret_cast<const uint4*>(zs + k * sc + j0);
         const uint32_t y[4] = {v.x, v.y, v.z, v.w};
         const float2 wk = make_float2(P.w[k], P.w[k]);
@@ -389,10 +392,11 @@ __device__ __forceinline__ Lse pass1_bf16(const MixParams& P, const __nv_bfloat1
 
 // Pass 2, packed: 8 output values at columns j0.. (as pass2_8) from the row
 // logsumexps lse_sh[] (per teacher, or of g in slot 0).
-template <bool GEO, typename TO>
+template <bool GEO, typename TO, int KT>
 __device__ __forceinline__ void pass2_bf16(const MixParams& P, const __nv_bfloat16* zs,
                                            const float* lse_sh, int j0, float r[8]) {
   const int sc = (int)P.sc;
+  const int K = KT ? KT : P.k;
   float2 res[4];
   const uint4 u0 = *reinterpret_cast<const uint4*>(zs + j0);
   const uint32_t w0[4] = {u0.x, u0.y, u0.z, u0.w};
@@ -400,7 +404,9 @@ __device__ __forceinline__ void pass2_bf16(const MixParams& P, const __nv_bfloat
     const float2 wt = make_float2(P.w[0], P.w[0]);
 #pragma unroll
     for (int i = 0; i < 4; ++i) res[i] = mul2(unpack2(w0[i]), wt);
-    for (int k = 1; k < P.k; ++k) {
+#pragma unroll
+    for (int k = 1; k < (KT ? KT : kMaxT); ++k) {
+      if (!KT && k >= K) break;
       const uint4 v = *reinterpret_cast<const uint4*>(zs + k * sc + j0);
       const uint32_t y[4] = {v.x, v.y, v.z, v.w};
       const float2 wk = make_float2(P.w[k], P.w[k]);
@@ -427,7 +433,9 @@ __device__ __forceinline__ void pass2_bf16(const MixParams& P, const __nv_bfloat
         sum[i] = make_float2(1.f, 1.f);
       }
     }
-    for (int k = 1; k < P.k; ++k) {
+#pragma unroll
+    for (int k = 1; k < (KT ? KT : kMaxT); ++k) {
+      if (!KT && k >= K) break;
       const uint4 v = *reinterpret_cast<const uint4*>(zs + k * sc + j0);
       const uint32_t y[4] = {v.x, v.y, v.z, v.w};
       const float lw = P.lw[k] * kL2E;
@@ -438,7 +446,7 @@ __device__ __forceinline__ void pass2_bf16(const MixParams& P, const __nv_bfloat
         const float2 t2 = make_float2(fmaxf(tt.x, kFloor), fmaxf(tt.y, kFloor));
         const float2 d = sub2(t2, m[i]);
         const float2 e = make_float2(ex2(-fabsf(d.x)), ex2(-fabsf(d.y)));
-        if (P.k == 2) {  // the sum starts at 1: either order gives 1 + e
+        if (K == 2) {  // the sum starts at 1: either order gives 1 + e
           sum[i] = add2(sum[i], e);
         } else {
           sum[i].x = d.x > 0.f ? fmaf(sum[i].x, e.x, 1.f) : sum[i].x + e.x;
@@ -470,7 +478,7 @@ __device__ __forceinline__ void pass2_bf16(const MixParams& P, const __nv_bfloat
 // before it writes the second.  So the staging of the next row runs under
 // this row's pass 2 and the next row's pass 1, and two CTAs share an SM, so
 // one CTA's waits are the other's compute.
-template <typename TI, typename TO, bool GEO, bool WIDE>
+template <typename TI, typename TO, bool GEO, bool WIDE, int KT>
 __global__ void __launch_bounds__(kMT, WIDE ? 1 : 2) k_mix_cluster(const MixParams P) {
   extern __shared__ __align__(16) uint8_t mix_smem[];
   __shared__ __align__(8) uint64_t bars[2];  // one per half
@@ -483,7 +491,7 @@ __global__ void __launch_bounds__(kMT, WIDE ? 1 : 2) k_mix_cluster(const MixPara
   const int64_t c0 = (int64_t)rank * P.sc;
   const int64_t clen = P.v - c0 < P.sc ? (P.v - c0 > 0 ? P.v - c0 : 0) : P.sc;
   const int64_t h0 = clen / 2 / 8 * 8;  // halves [0, h0) and [h0, clen)
-  const int nstreams = GEO ? 1 : P.k;
+  const int nstreams = GEO ? 1 : (KT ? KT : P.k);
   TI* const zs = reinterpret_cast<TI*>(mix_smem);  // teacher k at zs + k * sc
   if (threadIdx.x == 0) {
     ptx::mbar_init(ptx::smem_u32(&bars[0]), 1);
@@ -558,9 +566,9 @@ __global__ void __launch_bounds__(kMT, WIDE ? 1 : 2) k_mix_cluster(const MixPara
     for (int t = 0; t < nstreams; ++t) {
       Lse a;
       if constexpr (sizeof(TI) == 2) {  // bf16 teachers: the packed pass
-        a = pass1_bf16<GEO>(P, zs, t, 0, (int)h0, Lse{-INFINITY, 0.f});
+        a = pass1_bf16<GEO, KT>(P, zs, t, 0, (int)h0, Lse{-INFINITY, 0.f});
         if (t == 0) wait_half(1);
-        a = pass1_bf16<GEO>(P, zs, t, (int)h0, (int)clen, a);
+        a = pass1_bf16<GEO, KT>(P, zs, t, (int)h0, (int)clen, a);
       } else {
         a = pass1<GEO>(P, zs, t, 0, h0, Lse{-INFINITY, 0.f});
         if (t == 0) wait_half(1);
@@ -611,7 +619,7 @@ __global__ void __launch_bounds__(kMT, WIDE ? 1 : 2) k_mix_cluster(const MixPara
       for (int64_t j0 = lo + (int64_t)threadIdx.x * 8; j0 < hi; j0 += (int64_t)kMT * 8) {
         float r[8];
         if constexpr (sizeof(TI) == 2)
-          pass2_bf16<GEO, TO>(P, zs, off_sh, (int)j0, r);
+          pass2_bf16<GEO, TO, KT>(P, zs, off_sh, (int)j0, r);
         else
           pass2_8<GEO, TI, TO>(P, zs, off_sh, j0, r);
         if (ov && j0 + 8 <= hi) {
@@ -684,12 +692,12 @@ int mix_cluster_for(int64_t v, int k, int64_t elem, int64_t budget, int64_t* sc)
 
 // The cluster kernel in one shape (WIDE: one CTA per SM and twice the
 // staging); returns 1 on a CUDA error, and sets *launched.
-template <typename TI, typename TO, bool GEO, bool WIDE>
+template <typename TI, typename TO, bool GEO, bool WIDE, int KT = 0>
 int launch_mix_cluster(MixParams P, int c, int64_t sc, cudaStream_t s, bool* launched) {
   *launched = false;
   const int nsm = tc_num_sms() > 0 ? tc_num_sms() : 1;
   const size_t smem = (size_t)sc * sizeof(TI) * (size_t)P.k;
-  auto kern = k_mix_cluster<TI, TO, GEO, WIDE>;
+  auto kern = k_mix_cluster<TI, TO, GEO, WIDE, KT>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return 1;
@@ -725,6 +733,12 @@ int launch_mix(MixParams P, cudaStream_t s) {
   int64_t sc = 0;
   bool launched = false;
   int c = mix_cluster_for(P.v, P.k, (int64_t)sizeof(TI), kMixBuf, &sc);
+  if constexpr (sizeof(TI) == 2) {  // two bf16 teachers: the teacher loops unrolled
+    if (P.k == 2) {
+      if (c > 0 && launch_mix_cluster<TI, TO, GEO, false, 2>(P, c, sc, s, &launched)) return 1;
+      if (launched) return 0;
+    }
+  }
   if (c > 0 && launch_mix_cluster<TI, TO, GEO, false>(P, c, sc, s, &launched)) return 1;
   if (launched) return 0;
   c = mix_cluster_for(P.v, P.k, (int64_t)sizeof(TI), kMixBufWide, &sc);
