@@ -4,9 +4,11 @@
 // One persistent CTA per SM.  A producer warp copies each token row in
 // kChunk-byte pieces (z_s and, with a teacher, z_t) into a kStages-deep
 // shared-memory ring with 1-D bulk copies (cp.async.bulk, completion counted
-// on an mbarrier); kCW consumer warps read the ring, each thread owning 16
-// bytes of every piece, and release each stage as soon as their registers hold
-// it, so memory traffic never waits on the arithmetic.  The per-chunk work is a
+// on an mbarrier); kCW consumer warps read the ring, each thread owning
+// kSlots 16-byte slots of every piece, and release each stage as soon as
+// their registers hold it, so memory traffic never waits on the arithmetic.
+// Two slots a stage halve the per-stage cost (barrier wait, release, loop)
+// per byte; the policies fold the slots one at a time into one set of sums.  The per-chunk work is a
 // policy: an accumulator (forward online softmax) or a gradient writer
 // (backward), in a generic form (any dtype and temperature) or a packed bf16
 // form.  Every wait is bounded (see kd_ptx.cuh); after a timeout the kernel
@@ -24,21 +26,30 @@ namespace ring {
 constexpr int kCW = 24;                       // consumer warps
 constexpr int kCT = 32 * kCW;                 // consumer threads
 constexpr int kThreads = kCT + 32;            // + one producer warp
-constexpr int kChunk = 12288;                 // bytes of one tensor per stage
-constexpr int kStages = 8;
-constexpr int kSlots = kChunk / (16 * kCT);   // 16-byte slots per consumer thread per stage
-constexpr int kRingBytes = kStages * 2 * kChunk;
+constexpr int kRingBytes = 192 * 1024;       // the ring: stages x 2 tensors x piece
+constexpr int kMaxStages = 8;
+// Ring geometry: NSL 16-byte slots per consumer thread per stage, pieces of
+// NSL * 12 KiB per tensor, 8 / NSL stages.  Two slots halve the per-stage cost
+// per byte (the one-sweep forwards and the backwards); one slot and eight
+// stages leave the warps more slack between one another (the compute-bound
+// two-sweep forward of the skew variants).
+template <int NSL>
+struct Geo {
+  static constexpr int kSlots = NSL;
+  static constexpr int kChunk = NSL * 16 * kCT;  // bytes of one tensor per stage
+  static constexpr int kStages = kRingBytes / (2 * kChunk);
+  static_assert(kStages * 2 * kChunk == kRingBytes && kStages <= kMaxStages, "ring geometry");
+};
 // Per-row merge records.  A consumer warp runs at most kStages + 1 chunks
 // (so at most kStages + 2 rows) ahead of the slowest one, so 16 record sets
 // are never reused while still being read.
 constexpr int kMergeSlots = 16;
 constexpr int kRecBytes = kMergeSlots * kCW * kRec * 4;
 constexpr int kSmem = 128 + kRingBytes + 256 + kRecBytes + 64;
-static_assert(kMergeSlots >= kStages + 4, "merge records could be reused too early");
+static_assert(kMergeSlots >= kMaxStages + 4, "merge records could be reused too early");
 // control area after the ring: full / empty barriers, the abort word, the
 // merge counters, all inside its 256 bytes and apart from one another
-static_assert(16 * kStages + 16 + 4 * kMergeSlots <= 256, "ring control words overlap");
-static_assert(kSlots * 16 * kCT == kChunk, "a stage splits evenly over the consumers");
+static_assert(16 * kMaxStages + 16 + 4 * kMergeSlots <= 256, "ring control words overlap");
 
 template <typename T>
 __device__ __forceinline__ float ld1(const T* p) {
@@ -58,7 +69,7 @@ __device__ __forceinline__ void st1<__nv_bfloat16>(__nv_bfloat16* p, float v) {
 }
 
 struct Ring {
-  uint8_t* base;         // [stage][tensor][kChunk]
+  uint8_t* base;         // [stage][tensor][piece]
   uint32_t full, empty;  // mbarrier arrays (8 bytes each)
   volatile int* abort;
   uint64_t limit;        // time limit of every wait (ns)
@@ -77,17 +88,18 @@ __device__ __forceinline__ Ring make_ring(uint8_t* smem, const StreamArgs& a) {
   r.base = smem + pad;
   uint8_t* tail = r.base + kRingBytes;
   r.full = ptx::smem_u32(tail);
-  r.empty = r.full + 8 * kStages;
-  r.abort = reinterpret_cast<volatile int*>(tail + 16 * kStages);
-  r.cnt = reinterpret_cast<int*>(tail + 16 * kStages + 16);
+  r.empty = r.full + 8 * kMaxStages;
+  r.abort = reinterpret_cast<volatile int*>(tail + 16 * kMaxStages);
+  r.cnt = reinterpret_cast<int*>(tail + 16 * kMaxStages + 16);
   r.recs = reinterpret_cast<float*>(tail + 256);
   r.bcast = r.recs + kMergeSlots * kCW * kRec;
   return r;
 }
 
+template <class G>
 __device__ __forceinline__ void ring_init(const Ring& R) {
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < G::kStages; ++i) {
       ptx::mbar_init(R.full + 8 * i, 1);
       ptx::mbar_init(R.empty + 8 * i, kCW);  // one arrival per consumer warp
     }
@@ -99,13 +111,14 @@ __device__ __forceinline__ void ring_init(const Ring& R) {
 }
 
 // Producer: stream `passes` sweeps of every row this CTA owns (rows
-// blockIdx.x, +gridDim.x, ...) in kChunk pieces into the ring.  Rows are
+// blockIdx.x, +gridDim.x, ...) in G::kChunk pieces into the ring.  Rows are
 // 16-byte aligned and the vocabulary a multiple of 16 bytes (the dispatch
 // checks both), so every copy has a 16-byte aligned source, destination and
 // size.
-template <typename T>
+template <typename T, class G>
 __device__ void producer(const Ring& R, const StreamArgs& a, bool has_t, int passes,
                          uint32_t* status) {
+  constexpr int kChunk = G::kChunk, kStages = G::kStages;
   constexpr int EPC = kChunk / (int)sizeof(T);
   const int64_t V = a.vocab, nch = (V + EPC - 1) / EPC;
   const int lane = threadIdx.x & 31;
@@ -145,21 +158,22 @@ __device__ void producer(const Ring& R, const StreamArgs& a, bool has_t, int pas
         ptx::warp_wait(R.full + 8 * st, (par >> st) & 1u, R.abort, status, false, R.limit);
 }
 
-// Consumer side of one ring slot.
+// Consumer side of the ring.
+template <class G>
 struct Cursor {
   int stage = 0;
   uint32_t phase = 0;
   bool first = true;
   __device__ __forceinline__ const uint8_t* acquire(const Ring& R, uint32_t* status) {
     ptx::warp_wait(R.full + 8 * stage, phase, R.abort, status, true, R.limit);
-    return R.base + (size_t)stage * 2 * kChunk;
+    return R.base + (size_t)stage * 2 * G::kChunk;
   }
   __device__ __forceinline__ void release(const Ring& R) {
     __syncwarp();
     const bool keep = R.withhold && first && threadIdx.x < 32;  // test hook only
     first = false;
     if ((threadIdx.x & 31) == 0 && !keep) ptx::mbar_arrive(R.empty + 8 * stage);
-    if (++stage == kStages) {
+    if (++stage == G::kStages) {
       stage = 0;
       phase ^= 1;
     }
@@ -288,11 +302,12 @@ __device__ __forceinline__ RowOut finish_row(const StreamArgs& a, int64_t row, R
 // Second sweep of one row for the skew variants, once both normalisers are
 // known: per-thread partial sums (jq, jp, jx) of q log(q/m), p log(p/m) and
 // p (p/m) (the last only for want_x).
-template <typename T>
-__device__ __forceinline__ float3 skew_sweep(const Ring& R, Cursor& cur, uint32_t* status, int V,
-                                             const Consts& c, float lse_tT, float dlse,
+template <typename T, class G>
+__device__ __forceinline__ float3 skew_sweep(const Ring& R, Cursor<G>& cur, uint32_t* status,
+                                             int V, const Consts& c, float lse_tT, float dlse,
                                              bool want_x) {
   constexpr int EPT = 16 / (int)sizeof(T);
+  constexpr int kSlots = G::kSlots, kChunk = G::kChunk;
   constexpr int EPC = kChunk / (int)sizeof(T);
   const int nch = (V + EPC - 1) / EPC, ct = threadIdx.x;
   float jq = 0.f, jp = 0.f, jx = 0.f;
@@ -336,10 +351,11 @@ __device__ __forceinline__ float3 skew_sweep(const Ring& R, Cursor& cur, uint32_
 
 // The same sweep over bf16 rows in the base-2 form of skew_pair_b2.  The
 // dispatch keeps bf16 rows a multiple of 8 columns, so every slot is whole.
-template <bool WANT_X>
-__device__ __forceinline__ float3 skew_sweep_bf16(const Ring& R, Cursor& cur, uint32_t* status,
-                                                  int V, const Consts& c, float lse_tT,
-                                                  float dlse) {
+template <bool WANT_X, class G>
+__device__ __forceinline__ float3 skew_sweep_bf16(const Ring& R, Cursor<G>& cur,
+                                                  uint32_t* status, int V, const Consts& c,
+                                                  float lse_tT, float dlse) {
+  constexpr int kSlots = G::kSlots, kChunk = G::kChunk;
   constexpr int EPT = 8, EPC = kChunk / 2;
   const int nch = (V + EPC - 1) / EPC, ct = threadIdx.x;
   const SkewK k = skew_consts(c, lse_tT, dlse);
@@ -358,7 +374,7 @@ __device__ __forceinline__ float3 skew_sweep_bf16(const Ring& R, Cursor& cur, ui
       }
     }
     cur.release(R);
-#pragma unroll
+#pragma unroll 1  // one slot's pairs live at a time (registers)
     for (int j = 0; j < kSlots; ++j)
       if (full[j]) {
         const uint32_t ws[4] = {us[j].x, us[j].y, us[j].z, us[j].w};
@@ -375,26 +391,29 @@ __device__ __forceinline__ float3 skew_sweep_bf16(const Ring& R, Cursor& cur, ui
 }
 
 // Forward.  Acc: init(); static load(Frag&, buf, slot); static pick(const
-// Frag&, i, zs, zt) (element i of a slot); step(const Frag[kSlots],
-// const int nv[kSlots], c); RowState fold(c).  Column indices within a row are
+// Frag&, i, zs, zt) (element i of a slot); step(const Frag[NS], const int
+// nv[NS], c) for NS slots; RowState fold(c).  Frags are loaded from a stage
+// by load(Frag&, buf, slot, piece bytes).  Column indices within a row are
 // 32-bit (the dispatch keeps rows below 2^30 elements).  PASSES = 2 for
 // skew-JS (a second sweep once both normalisers are known), else 1; a
 // template parameter so single-pass kernels carry no second-sweep code.
-template <typename T, bool HAS_T, class Acc, int PASSES>
+template <typename T, bool HAS_T, class Acc, int PASSES, int NSL>
 __global__ void __launch_bounds__(kThreads, 1) k_fwd(StreamArgs a, uint32_t* status) {
+  using G = Geo<NSL>;
+  constexpr int kSlots = G::kSlots, kChunk = G::kChunk;
   extern __shared__ uint8_t smem_raw[];
   const Ring R = make_ring(smem_raw, a);
-  ring_init(R);
+  ring_init<G>(R);
   constexpr int passes = PASSES;
   if ((threadIdx.x >> 5) == kCW) {
-    producer<T>(R, a, HAS_T, passes, status);
+    producer<T, G>(R, a, HAS_T, passes, status);
   } else {
     constexpr int EPT = 16 / (int)sizeof(T);
     constexpr int EPC = kChunk / (int)sizeof(T);
     const Consts c = a.c;
     const int V = (int)a.vocab, nch = (V + EPC - 1) / EPC;
     const int ct = threadIdx.x;
-    Cursor cur;
+    Cursor<G> cur;
     int local_row = 0;
     // labels one row ahead: the load's latency hides behind a whole row
     int64_t y_next = (a.labels && (int64_t)blockIdx.x < a.n) ? a.labels[blockIdx.x] : -1;
@@ -416,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd(StreamArgs a, uint32_t* sta
           const int e0 = ch * EPC + slot * EPT;
           nv[j] = valid_cols(V - e0, EPT);
           if (nv[j] > 0) {
-            Acc::load(f[j], buf, slot);
+            Acc::load(f[j], buf, slot, kChunk);
             // the label's logits, from the staged copy (one thread per row)
             if ((unsigned)(yc - e0) < (unsigned)EPT) Acc::pick(f[j], yc - e0, zys, zyt);
           }
@@ -455,10 +474,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd(StreamArgs a, uint32_t* sta
       const bool want_x = a.variant != KD_KL_SKEW_JS;
       float3 part;
       if constexpr (sizeof(T) == 2) {  // bf16 problems take the fast (non-precise) forms
-        part = want_x ? skew_sweep_bf16<true>(R, cur, status, V, c, lse_tT, dlse)
-                      : skew_sweep_bf16<false>(R, cur, status, V, c, lse_tT, dlse);
+        part = want_x ? skew_sweep_bf16<true, G>(R, cur, status, V, c, lse_tT, dlse)
+                      : skew_sweep_bf16<false, G>(R, cur, status, V, c, lse_tT, dlse);
       } else {
-        part = skew_sweep<T>(R, cur, status, V, c, lse_tT, dlse, want_x);
+        part = skew_sweep<T, G>(R, cur, status, V, c, lse_tT, dlse, want_x);
       }
       const float3 r = consumer_sum3(part.x, part.y, part.z, R);
       if (ct == 0) {
@@ -473,21 +492,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd(StreamArgs a, uint32_t* sta
   __syncthreads();
 }
 
-// Backward.  Grad: row(a, row) once per row; static load(Frag&, buf, slot);
-// chunk(const Frag&, e0, nv, dz_row) writes the d z_s of one 16-byte slot.
-template <typename T, bool HAS_T, class Grad>
+// Backward.  Grad: row(a, row) once per row; static load(Frag&, buf, slot,
+// piece bytes); chunk(const Frag&, e0, nv, dz_row) writes the d z_s of one
+// 16-byte slot.
+template <typename T, bool HAS_T, class Grad, int NSL>
 __global__ void __launch_bounds__(kThreads, 1) k_bwd(StreamArgs a, uint32_t* status) {
+  using G = Geo<NSL>;
+  constexpr int kSlots = G::kSlots, kChunk = G::kChunk;
   extern __shared__ uint8_t smem_raw[];
   const Ring R = make_ring(smem_raw, a);
-  ring_init(R);
+  ring_init<G>(R);
   if ((threadIdx.x >> 5) == kCW) {
-    producer<T>(R, a, HAS_T, 1, status);
+    producer<T, G>(R, a, HAS_T, 1, status);
   } else {
     constexpr int EPT = 16 / (int)sizeof(T);
     constexpr int EPC = kChunk / (int)sizeof(T);
     const int V = (int)a.vocab, nch = (V + EPC - 1) / EPC;
     const int ct = threadIdx.x;
-    Cursor cur;
+    Cursor<G> cur;
     for (int64_t row = blockIdx.x; row < a.n; row += gridDim.x) {
       Grad g;
       g.row(a, row);
@@ -501,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd(StreamArgs a, uint32_t* sta
           const int slot = j * kCT + ct;
           e0[j] = ch * EPC + slot * EPT;
           nv[j] = valid_cols(V - e0[j], EPT);
-          if (nv[j] > 0) Grad::load(f[j], buf, slot);
+          if (nv[j] > 0) Grad::load(f[j], buf, slot, kChunk);
         }
         cur.release(R);
 #pragma unroll
@@ -528,13 +550,18 @@ inline void launch(K kernel, const StreamArgs& a, cudaStream_t s) {
 
 template <typename T, bool HAS_T, class Acc>
 inline void launch_fwd(const StreamArgs& a, cudaStream_t s) {
-  if constexpr (HAS_T) {
+  if constexpr (HAS_T && Acc::kSecondSweep) {  // (only policies that serve the skew variants)
     if (is_skew(a.variant)) {
-      launch(k_fwd<T, HAS_T, Acc, 2>, a, s);
+      launch(k_fwd<T, HAS_T, Acc, 2, 1>, a, s);
       return;
     }
   }
-  launch(k_fwd<T, HAS_T, Acc, 1>, a, s);
+  launch(k_fwd<T, HAS_T, Acc, 1, 2>, a, s);
+}
+
+template <typename T, bool HAS_T, class Grad>
+inline void launch_bwd(const StreamArgs& a, cudaStream_t s) {
+  launch(k_bwd<T, HAS_T, Grad, 2>, a, s);
 }
 
 }  // namespace ring

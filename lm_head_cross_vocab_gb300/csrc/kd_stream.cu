@@ -206,32 +206,57 @@ __global__ void k_stream_bwd_topk(StreamArgs a) {
 // kd_stream_bf16.cu instead.
 namespace {
 
+// 16 bytes of staged values as floats
+template <typename T>
+__device__ __forceinline__ void raw_to_f(const uint4& u, float* v);
+template <>
+__device__ __forceinline__ void raw_to_f<__nv_bfloat16>(const uint4& u, float* v) {
+  v[0] = bf16lo(u.x); v[1] = bf16hi(u.x); v[2] = bf16lo(u.y); v[3] = bf16hi(u.y);
+  v[4] = bf16lo(u.z); v[5] = bf16hi(u.z); v[6] = bf16lo(u.w); v[7] = bf16hi(u.w);
+}
+template <>
+__device__ __forceinline__ void raw_to_f<float>(const uint4& u, float* v) {
+  v[0] = __uint_as_float(u.x); v[1] = __uint_as_float(u.y);
+  v[2] = __uint_as_float(u.z); v[3] = __uint_as_float(u.w);
+}
+
+// The slots of a stage stay raw 16-byte words until their turn in step(),
+// which converts and folds one slot at a time (registers).
 template <typename T, bool HAS_T>
 struct GenericAcc {
   static constexpr int EPT = ring::Chunk<T>::EPT;
+  static constexpr bool kSecondSweep = true;  // serves every variant
   struct Frag {
-    float s[EPT], t[EPT];
+    uint4 s, t;
   };
   RowState st;
-  __device__ static void load(Frag& f, const uint8_t* buf, int ct) {
-    ring::Chunk<T>::load(buf, ct, f.s);
-    if (HAS_T) ring::Chunk<T>::load(buf + ring::kChunk, ct, f.t);
+  __device__ static void load(Frag& f, const uint8_t* buf, int ct, int piece) {
+    f.s = *reinterpret_cast<const uint4*>(buf + ct * 16);
+    if (HAS_T) f.t = *reinterpret_cast<const uint4*>(buf + piece + ct * 16);
   }
   __device__ static void pick(const Frag& f, int i, float& zs, float& zt) {
+    float v[EPT];
+    raw_to_f<T>(f.s, v);
 #pragma unroll
     for (int u = 0; u < EPT; ++u)
-      if (u == i) {
-        zs = f.s[u];
-        if (HAS_T) zt = f.t[u];
-      }
+      if (u == i) zs = v[u];
+    if (HAS_T) {
+      raw_to_f<T>(f.t, v);
+#pragma unroll
+      for (int u = 0; u < EPT; ++u)
+        if (u == i) zt = v[u];
+    }
   }
   __device__ void init() { st.init(); }
-  __device__ void step(const Frag (&f)[ring::kSlots], const int (&nv)[ring::kSlots],
-                       const Consts& c) {
-#pragma unroll
-    for (int j = 0; j < ring::kSlots; ++j) {
-      if (nv[j] == EPT) update<EPT, HAS_T, false>(st, f[j].s, f[j].t, EPT, c);
-      else if (nv[j] > 0) update<EPT, HAS_T, true>(st, f[j].s, f[j].t, nv[j], c);
+  template <int NS>
+  __device__ void step(const Frag (&f)[NS], const int (&nv)[NS], const Consts& c) {
+#pragma unroll 1
+    for (int j = 0; j < NS; ++j) {
+      float s[EPT], t[EPT];
+      raw_to_f<T>(f[j].s, s);
+      if (HAS_T) raw_to_f<T>(f[j].t, t);
+      if (nv[j] == EPT) update<EPT, HAS_T, false>(st, s, t, EPT, c);
+      else if (nv[j] > 0) update<EPT, HAS_T, true>(st, s, t, nv[j], c);
     }
   }
   __device__ RowState fold(const Consts&) const { return st; }
@@ -251,9 +276,9 @@ struct GenericGrad {
   float scale, sq_s, wk, wc;
   int64_t y;
   int variant, topk;
-  __device__ static void load(Frag& f, const uint8_t* buf, int ct) {
+  __device__ static void load(Frag& f, const uint8_t* buf, int ct, int piece) {
     ring::Chunk<T>::load(buf, ct, f.s);
-    if (HAS_T) ring::Chunk<T>::load(buf + ring::kChunk, ct, f.t);
+    if (HAS_T) ring::Chunk<T>::load(buf + piece, ct, f.t);
   }
   __device__ void row(const StreamArgs& a, int64_t r) {
     c = a.c;
@@ -333,8 +358,8 @@ static void bwd_dispatch(const StreamArgs& a, cudaStream_t s) {
   note_launch();
   if (vec) {  // rows 16-byte aligned: TMA-staged ring kernels
     if (!launch_stream_bwd_packed(a, s)) {
-      if (has_t) ring::launch(ring::k_bwd<T, true, GenericGrad<T, true>>, a, s);
-      else ring::launch(ring::k_bwd<T, false, GenericGrad<T, false>>, a, s);
+      if (has_t) ring::launch_bwd<T, true, GenericGrad<T, true>>(a, s);
+      else ring::launch_bwd<T, false, GenericGrad<T, false>>(a, s);
     }
   } else if (has_t) {
     k_stream_bwd<T, true><<<grid, 256, 0, s>>>(a);

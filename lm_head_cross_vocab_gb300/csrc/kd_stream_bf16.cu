@@ -43,18 +43,19 @@ constexpr float kStale = 8.f;  // log2 of the largest term a stale maximum may l
 
 template <bool HAS_T, int KLM, int PW, bool NEED1>
 struct PackedAcc {
-  static constexpr int NS = ring::kSlots;  // one set of partial sums per slot
+  static constexpr int NA = 1;  // partial-sum sets, shared by the slots of a stage
+  static constexpr bool kSecondSweep = KLM == 4;  // the skew variants' policy
   struct Frag {
     uint4 s, t;
   };
   float ms, mt, cq, cp;
   uint32_t ths, tht;  // bf16x2 rescale thresholds: offset + kStale (rounded down)
   float2 osT, otT;  // -m k_T per side (exponent offsets)
-  float2 ls1[NS], lsT[NS], lt1[NS], ltT[NS], qd[NS], qx[NS], pd[NS], px[NS];
+  float2 ls1[NA], lsT[NA], lt1[NA], ltT[NA], qd[NA], qx[NA], pd[NA], px[NA];
 
-  __device__ static void load(Frag& f, const uint8_t* buf, int slot) {
+  __device__ static void load(Frag& f, const uint8_t* buf, int slot, int piece) {
     f.s = *reinterpret_cast<const uint4*>(buf + slot * 16);
-    if (HAS_T) f.t = *reinterpret_cast<const uint4*>(buf + ring::kChunk + slot * 16);
+    if (HAS_T) f.t = *reinterpret_cast<const uint4*>(buf + piece + slot * 16);
   }
   __device__ static void pick(const Frag& f, int i, float& zs, float& zt) {
     const uint32_t ws = word(f.s, i >> 1);
@@ -70,7 +71,7 @@ struct PackedAcc {
     cq = cp = 0.f;
     osT = otT = splat(0.f);
 #pragma unroll
-    for (int j = 0; j < NS; ++j)
+    for (int j = 0; j < NA; ++j)
       ls1[j] = lsT[j] = lt1[j] = ltT[j] = qd[j] = qx[j] = pd[j] = px[j] = splat(0.f);
   }
   // Rescale the running sums to a larger maximum (rare after a row's first
@@ -81,7 +82,7 @@ struct PackedAcc {
       const float2 fT = splat(ex2((ms - cms) * c.k_sT));
       const float2 f1 = splat(NEED1 ? ex2((ms - cms) * c.k_s1) : 0.f);
 #pragma unroll
-      for (int j = 0; j < NS; ++j) {
+      for (int j = 0; j < NA; ++j) {
         lsT[j] = mul2(lsT[j], fT);
         if (KLM & 2) {
           pd[j] = mul2(pd[j], fT);
@@ -98,7 +99,7 @@ struct PackedAcc {
       const float2 fT = splat(ex2((mt - cmt) * c.k_tT));
       const float2 f1 = splat(NEED1 ? ex2((mt - cmt) * c.k_t1) : 0.f);
 #pragma unroll
-      for (int j = 0; j < NS; ++j) {
+      for (int j = 0; j < NA; ++j) {
         ltT[j] = mul2(ltT[j], fT);
         if (KLM & 1) qd[j] = mul2(qd[j], fT);
         if (KLM & 5) qx[j] = mul2(qx[j], fT);
@@ -145,6 +146,7 @@ struct PackedAcc {
     pair(J, f.s.w, HAS_T ? f.t.w : 0u, c);
   }
   // nv is 0 or 8 here (the vocabulary is a multiple of 8)
+  template <int NS>
   __device__ __forceinline__ void step(const Frag (&f)[NS], const int (&nv)[NS], const Consts& c) {
     uint32_t ws = kNegInfX2, wt = kNegInfX2;
 #pragma unroll
@@ -162,12 +164,12 @@ struct PackedAcc {
       grow(hmax(ws), HAS_T ? hmax(wt) : neg_inf(), c);
 #pragma unroll
     for (int j = 0; j < NS; ++j)
-      if (nv[j] > 0) slot(j, f[j], c);
+      if (nv[j] > 0) slot(j % NA, f[j], c);
   }
-  __device__ static float total(const float2 (&v)[NS]) {
+  __device__ static float total(const float2 (&v)[NA]) {
     float2 t = v[0];
 #pragma unroll
-    for (int j = 1; j < NS; ++j) t = add2(t, v[j]);
+    for (int j = 1; j < NA; ++j) t = add2(t, v[j]);
     return hsum(t);
   }
   __device__ RowState fold(const Consts& c) const {
@@ -208,9 +210,9 @@ struct PackedGrad {
   float sv[KD_STATS_PER_TOKEN];  // skew-JS only
   Consts c;                      // skew-JS only
 
-  __device__ static void load(Frag& f, const uint8_t* buf, int slot) {
+  __device__ static void load(Frag& f, const uint8_t* buf, int slot, int piece) {
     f.s = *reinterpret_cast<const uint4*>(buf + slot * 16);
-    if (HAS_T) f.t = *reinterpret_cast<const uint4*>(buf + ring::kChunk + slot * 16);
+    if (HAS_T) f.t = *reinterpret_cast<const uint4*>(buf + piece + slot * 16);
   }
   __device__ void row(const StreamArgs& a, int64_t r) {
     const float* st = a.stats + r * KD_STATS_PER_TOKEN;
@@ -296,8 +298,8 @@ void fwd_pw(const StreamArgs& a, cudaStream_t s) {
 
 template <bool HAS_T, int VAR, int PW>
 void bwd_ce(const StreamArgs& a, cudaStream_t s) {
-  if (a.w_sce != 0.f) ring::launch(ring::k_bwd<bf16, HAS_T, PackedGrad<HAS_T, VAR, PW, true>>, a, s);
-  else ring::launch(ring::k_bwd<bf16, HAS_T, PackedGrad<HAS_T, VAR, PW, false>>, a, s);
+  if (a.w_sce != 0.f) ring::launch_bwd<bf16, HAS_T, PackedGrad<HAS_T, VAR, PW, true>>(a, s);
+  else ring::launch_bwd<bf16, HAS_T, PackedGrad<HAS_T, VAR, PW, false>>(a, s);
 }
 template <bool HAS_T, int VAR>
 void bwd_pw(const StreamArgs& a, cudaStream_t s) {
