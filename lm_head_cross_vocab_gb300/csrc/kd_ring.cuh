@@ -559,9 +559,19 @@ inline void launch_fwd(const StreamArgs& a, cudaStream_t s) {
   launch(k_fwd<T, HAS_T, Acc, 1, 2>, a, s);
 }
 
+// Backward: two slots a stage, one (and 8 stages) for the skew variants'
+// heavier gradients.  Grad::kSlotsFor: 1 or 2 when its variant fixes it, 0 to
+// decide from the problem's variant.
 template <typename T, bool HAS_T, class Grad>
 inline void launch_bwd(const StreamArgs& a, cudaStream_t s) {
-  launch(k_bwd<T, HAS_T, Grad, 2>, a, s);
+  if constexpr (Grad::kSlotsFor == 1) {
+    launch(k_bwd<T, HAS_T, Grad, 1>, a, s);
+  } else if constexpr (Grad::kSlotsFor == 2) {
+    launch(k_bwd<T, HAS_T, Grad, 2>, a, s);
+  } else {
+    if (HAS_T && is_skew(a.variant)) launch(k_bwd<T, HAS_T, Grad, 1>, a, s);
+    else launch(k_bwd<T, HAS_T, Grad, 2>, a, s);
+  }
 }
 
 }  // namespace ring

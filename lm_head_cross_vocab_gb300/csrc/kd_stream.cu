@@ -268,6 +268,7 @@ struct GenericAcc {
 template <typename T, bool HAS_T>
 struct GenericGrad {
   static constexpr int EPT = ring::Chunk<T>::EPT;
+  static constexpr int kSlotsFor = 0;  // from the problem's variant
   struct Frag {
     float s[EPT], t[EPT];
   };

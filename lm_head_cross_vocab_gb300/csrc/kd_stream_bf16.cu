@@ -200,6 +200,8 @@ struct PackedAcc {
 // each times s_row w_kl T_s, plus s_row w_sce (softmax(z_s) - e_y).
 template <bool HAS_T, int VAR, int PW, bool CE>
 struct PackedGrad {
+  static constexpr int kSlotsFor = HAS_T && (VAR == KD_KL_SKEW_JS || VAR == KD_KL_SKEW_FORWARD ||
+                                             VAR == KD_KL_SKEW_REVERSE) ? 1 : 2;
   struct Frag {
     uint4 s, t;
   };
