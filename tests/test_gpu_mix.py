@@ -88,6 +88,27 @@ def test_mix_single_teacher_is_log_softmax():
 
 
 @pytest.mark.parametrize("mode", ["arithmetic", "geometric"])
+@pytest.mark.parametrize("dout", ["fp32", "bf16"])
+def test_mix_rows_whose_maximum_keeps_rising(mode, dout):
+    """Rows built so that the running maximum of a stream moves many times: a
+    rising ramp (every step of every thread passes the previous offset), a
+    falling one, and a flat row with one spike at the last id of a CTA's slice
+    and one at the very end.  The packed bf16 passes keep each sum around an
+    offset that moves only when a step's maximum passes it by 2^8 in base 2; every
+    move rescales the sum."""
+    v, n = 151936, 4
+    ramp = torch.linspace(-30.0, 60.0, v)
+    a = torch.stack([ramp, ramp.flip(0), torch.zeros(v), torch.sin(ramp) * 3]).to(torch.bfloat16)
+    a[2, v // 8 - 1] = 25.0
+    a[2, -1] = 30.0
+    b = torch.stack([ramp.flip(0), ramp, torch.full((v,), -2.0), ramp * 0.5]).to(torch.bfloat16)
+    w = [0.7, 0.3]
+    out = kd.mix_teacher_logits([a.cuda(), b.cuda()], w, mode, out_dtype=DT[dout])
+    torch.cuda.synchronize()
+    _check(out.cpu().double().numpy(), O.mix_teacher_logits([a, b], w, mode), dout)
+
+
+@pytest.mark.parametrize("mode", ["arithmetic", "geometric"])
 def test_distillation_from_a_mixture(mode):
     """Mix three teachers (bf16), then distil student logits from the mixture
     (forward KL, T_s = 2, mixture at T_t = 1) against the oracle's own mixture

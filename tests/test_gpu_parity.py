@@ -40,9 +40,62 @@ def test_logit_pair_streaming_more_rows_than_ctas(variant):
 
 @pytest.mark.parametrize("variant", ["forward", "reverse"])
 def test_logit_pair_streaming_rows_longer_than_the_ring(variant):
-    """Rows of 13+ staged chunks: every ring slot is refilled within a row, so
-    consumers often wait on a slot whose copy is still in flight."""
+    """Rows longer than the ring (53256 ids: 4.3 pieces of 12288 ids over the
+    one-sweep kernels' 4 stages): stages are refilled within a row, so
+    consumers often wait on a stage whose copy is still in flight."""
     w = W[5].scaled(n_tokens=180, vocab=53256, variant=variant)
+    assert_parity(run_and_compare(w), "bf16")
+
+
+@pytest.mark.parametrize("variant", ["forward", "jeffreys", "skew_js"])
+@pytest.mark.parametrize("t", [1.0, 2.0])
+def test_logit_pair_streaming_rows_whose_maximum_keeps_rising(variant, t):
+    """Rows built so that the running maxima move many times: rising and
+    falling ramps, a flat row with two late spikes, a wave; the teacher is the
+    student plus a small wave.  The packed kernels keep their sums around
+    offsets that move only when a step's maximum passes them by 2^8 in base 2
+    (tested on the raw bf16 words); every move rescales the sums."""
+    v = 40968
+
+    def mutate(cpu):
+        n = cpu["logits_s"].shape[0]
+        ramp = torch.linspace(-20.0, 40.0, v)
+        rows = [ramp, ramp.flip(0), torch.zeros(v), torch.sin(ramp) * 4.0]
+        for i in range(n):
+            base = rows[i % 4].clone()
+            if i % 4 == 2:
+                base[v // 3] = 15.0
+                base[-1] = 22.0
+            wave = 0.5 * torch.sin(torch.arange(v, dtype=torch.float32) * 0.37 + i)
+            cpu["logits_s"][i] = base.to(cpu["logits_s"].dtype)
+            cpu["logits_t"][i] = (base + wave).to(cpu["logits_t"].dtype)
+
+    w = W[5].scaled(n_tokens=24, vocab=v, variant=variant, t_student=t, t_teacher=t)
+    res = run_and_compare(w, mutate=mutate)
+    # The flat rows with spikes at T = 1 put nearly all of both distributions on
+    # one id: their divergences are 1e-7 to 1e-5, formed in fp32 as the
+    # difference of two terms of the size of the logit gap there (~0.3), so the
+    # approximate exponentials' ~2-ulp error on the dominant terms leaves a few
+    # 1e-7 absolute: 1e-6 absolute on top of the per-token relative bound.
+    ref, valid = res["ref"]["kl"], res["valid"]
+    got = res.pop("gpu_fwd")["kl"].cpu().double().numpy()
+    res.pop("err_kl")
+    floor = 1e-3 * np.mean(np.abs(ref[valid]))
+    err = np.abs(got - ref)[valid]
+    assert np.all(err <= 1e-6 + 2e-3 * np.maximum(np.abs(ref[valid]), floor)), err.max()
+    assert_parity(res, "bf16")
+
+
+@pytest.mark.parametrize("variant", ["forward", "jeffreys", "skew_js", "skew_forward"])
+@pytest.mark.parametrize("vocab", [8, 6144, 6152, 12288, 12296, 24576, 24584, 110600])
+def test_logit_pair_streaming_piece_boundaries(variant, vocab):
+    """Rows at and just past the ring's piece boundaries.  The one-sweep
+    forwards and their backwards stream 12288 bf16 ids a stage (two 16-byte
+    slots per consumer thread), the skew variants' two-sweep forward and
+    backward 6144 (one slot, 8 stages): rows of one 8-id group, of exactly
+    one, two and four pieces, one group past each, and of ~9 and ~18 pieces
+    (every stage refilled within a row)."""
+    w = W[5].scaled(n_tokens=37, vocab=vocab, variant=variant)
     assert_parity(run_and_compare(w), "bf16")
 
 
