@@ -44,7 +44,8 @@ namespace kd {
 namespace {
 
 constexpr int kT = 256;
-constexpr int kPT = 1024;                 // threads per projection CTA
+constexpr int kPT = 1024;                 // threads per projection CTA (slice kernel, wide exchange)
+constexpr int kXTNarrow = 512;            // threads per exchange CTA of the narrow shape
 constexpr int64_t kSliceMax = 96 * 1024;  // bytes of a staged slice (two per CTA)
 constexpr int kMaxSlices = 1024;          // teacher rows up to 96 MiB
 
@@ -713,8 +714,8 @@ __device__ __forceinline__ void send_segments(const SendDesc& d, uint32_t C) {
 // shared-memory table, so a row's output needs no global loads but its own
 // gather list.  That list is read one 8-slot step ahead of the gather (the
 // first step before the slice wait).
-template <typename TI, typename TO>
-__global__ void __launch_bounds__(kPT, 1)
+template <typename TI, typename TO, int XT>
+__global__ void __launch_bounds__(XT, XT == kXTNarrow ? 2 : 1)
     k_project_exchange(const TI* __restrict__ zt, int64_t n, int64_t vt, int64_t vs,
                        float inv_t, const int32_t* __restrict__ off,
                        const int32_t* __restrict__ epos, const int32_t* __restrict__ code,
@@ -754,7 +755,7 @@ __global__ void __launch_bounds__(kPT, 1)
   // table entry (two receive slots; ~0 for three or more tokens)
   const int32_t m_lo = mpre[i_lo < i_hi ? i_lo : i_hi], m_hi = mpre[i_hi];
   const int32_t nm = m_hi - m_lo < kMCap ? m_hi - m_lo : kMCap;
-  for (int32_t k = threadIdx.x; k < nm; k += kPT) {
+  for (int32_t k = threadIdx.x; k < nm; k += XT) {
     const int32_t m = -2 - mcode[m_lo + k], e0 = m >> 3;
     mtab[k] = (m & 7) == 0 ? ((uint32_t)epos[e0] | ((uint32_t)epos[e0 + 1] << 16)) : ~0u;
     mid[k] = (uint16_t)(mlist[m_lo + k] - i_lo);
@@ -774,7 +775,7 @@ __global__ void __launch_bounds__(kPT, 1)
       }
     }
     const int64_t q0 = nb / (int64_t)sizeof(TI);
-    for (int64_t q = q0 + threadIdx.x; q < clen; q += kPT) slice[q] = src[q];
+    for (int64_t q = q0 + threadIdx.x; q < clen; q += XT) slice[q] = src[q];
     return q0 < clen;
   };
   bool plain = false;
@@ -786,14 +787,14 @@ __global__ void __launch_bounds__(kPT, 1)
   cl_sync();  // every receive barrier is armed before any copy is sent
   // this thread's output ids are the same in every row: their codes, two
   // 16-bit slots per register, are loaded once (ranges longer than
-  // kXSteps * 8 * kPT ids are not planned for this kernel).  A code below
+  // kXSteps * 8 * XT ids are not planned for this kernel).  A code below
   // rcap is the receive slot of the id's single teacher token; 0xfffe marks
   // an id with several (written by the pass after the output), 0xffff one
   // that no teacher token reaches.
   uint32_t c16[kXSteps][4];
 #pragma unroll
   for (int u = 0; u < kXSteps; ++u) {
-    const int64_t j0 = i_lo + ((int64_t)u * kPT + threadIdx.x) * 8;
+    const int64_t j0 = i_lo + ((int64_t)u * XT + threadIdx.x) * 8;
 #pragma unroll
     for (int q = 0; q < 4; ++q) c16[u][q] = 0xffffffffu;
     if (j0 >= i_hi) continue;
@@ -831,8 +832,8 @@ __global__ void __launch_bounds__(kPT, 1)
     ps ^= 1u;
     if (plain) __syncthreads();  // the plain-loaded columns too
     // 8 slots per thread step: nsend, the list start and send are multiples of 8
-    for (int32_t t0 = t_first; t0 < nsend; t0 += kPT * 8) {
-      const int32_t t1 = t0 + kPT * 8;
+    for (int32_t t0 = t_first; t0 < nsend; t0 += XT * 8) {
+      const int32_t t1 = t0 + XT * 8;
       int4 na = ga, nb = gb;
       if (t1 < nsend) {
         na = reinterpret_cast<const int4*>(gl + t1)[0];
@@ -864,7 +865,7 @@ __global__ void __launch_bounds__(kPT, 1)
     TO* o = out + row * vs;
 #pragma unroll
     for (int u = 0; u < kXSteps; ++u) {
-      const int64_t j0 = i_lo + ((int64_t)u * kPT + threadIdx.x) * 8;
+      const int64_t j0 = i_lo + ((int64_t)u * XT + threadIdx.x) * 8;
       if (j0 >= i_hi) break;
       float v[8];
 #pragma unroll
@@ -886,7 +887,7 @@ __global__ void __launch_bounds__(kPT, 1)
     // column order and overwrite the placeholders above (same CTA, after the
     // barrier, so the later store wins; the sectors are already whole)
     __syncthreads();
-    for (int32_t k = threadIdx.x; k < m_hi - m_lo; k += kPT) {
+    for (int32_t k = threadIdx.x; k < m_hi - m_lo; k += XT) {
       float x;
       int64_t id;
       const uint32_t e = k < nm ? mtab[k] : ~0u;
@@ -1469,37 +1470,47 @@ ProjLayout proj_layout(int64_t vt, int64_t vs) {
   return L;
 }
 
-// Exchange plan: C = the fewest CTAs whose slices of a teacher row fit
-// kXSlice bytes (at most kMaxC), the columns sc and student ids so per CTA,
-// and the send / receive capacities that fill the rest of kXSmem.  A CTA sends
+// Exchange plan: C = the fewest CTAs whose slices of a teacher row fit the
+// slice bytes of a shape (at most kMaxC), the columns sc and student ids so
+// per CTA, and the send / receive capacities that fill the rest of its shared
+// memory.  The narrow shape (512 threads, two CTAs per SM, 38 KiB slices in
+// 106 KiB) comes first: the two CTAs of an SM belong to different clusters and
+// are in different phases of their rows, so one's waits are the other's work.
+// Rows longer than 8 of its slices take the wide shape (1024 threads, one CTA
+// per SM, 76 KiB slices in 220 KiB).  A CTA sends
 // at most its sc columns (+ padding); what it receives depends on the map,
 // so the device checks it (XLayout::fits) and the slice path runs otherwise.
-constexpr int64_t kXSlice = 76 * 1024;
-constexpr int64_t kXSmem = 220 * 1024;
+struct XShape {
+  int threads;
+  int64_t slice, smem;  // bytes (the tables, about 6 KiB, come on top)
+};
+constexpr XShape kXNarrow{kXTNarrow, 38 * 1024, 106 * 1024};
+constexpr XShape kXWide{kPT, 76 * 1024, 220 * 1024};
 struct XPlan {
   int C = 0;
+  bool wide = false;
   int64_t sc = 0, so = 0, send_cap = 0, recv_cap = 0;
   size_t smem = 0;
   int max_clusters = 0;
 };
 
-template <typename TI, typename TO>
-bool x_plan(int64_t vt, int64_t vs, XPlan* P) {
+template <typename TI, typename TO, int XT>
+bool x_plan_shape(int64_t vt, int64_t vs, const XShape& sh, XPlan* P) {
   const int64_t elem = (int64_t)sizeof(TI);
-  int64_t C = (vt * elem + kXSlice - 1) / kXSlice;
+  int64_t C = (vt * elem + sh.slice - 1) / sh.slice;
   if (C < 1) C = 1;
   if (C > kMaxC) return false;
   P->sc = ((vt + C - 1) / C + 7) / 8 * 8;
   C = (vt + P->sc - 1) / P->sc;
   P->C = (int)C;
   P->so = ((vs + C - 1) / C + 7) / 8 * 8;
-  if (P->so > (int64_t)kXSteps * 8 * kPT) return false;  // longer ranges: the slice path
+  if (P->so > (int64_t)kXSteps * 8 * XT) return false;  // longer ranges: the slice path
   P->send_cap = P->sc + 8 * C;
-  P->recv_cap = (kXSmem / elem - P->sc - P->send_cap) / 8 * 8;
+  P->recv_cap = (sh.smem / elem - P->sc - P->send_cap) / 8 * 8;
   if (P->recv_cap > 65528) P->recv_cap = 65528;  // slots fit the kernel's 16-bit codes
   if (P->recv_cap < 8) return false;
   P->smem = (size_t)(P->sc + P->send_cap + P->recv_cap) * (size_t)elem;
-  auto kern = k_project_exchange<TI, TO>;
+  auto kern = k_project_exchange<TI, TO, XT>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P->smem) !=
       cudaSuccess) {
     (void)cudaGetLastError();
@@ -1515,14 +1526,26 @@ bool x_plan(int64_t vt, int64_t vs, XPlan* P) {
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   const int nsm = tc_num_sms() > 0 ? tc_num_sms() : 1;
-  cfg.gridDim = dim3((unsigned)(P->C * std::max(1, nsm / P->C)));
-  cfg.blockDim = dim3(kPT);
+  const int per_sm = XT == kXTNarrow ? 2 : 1;
+  cfg.gridDim = dim3((unsigned)(P->C * std::max(1, per_sm * nsm / P->C)));
+  cfg.blockDim = dim3(XT);
   cfg.dynamicSmemBytes = P->smem;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const int cached_max = max_active_clusters(reinterpret_cast<const void*>(kern), cfg);
   P->max_clusters = cached_max;
   return cached_max > 0;
+}
+
+template <typename TI, typename TO>
+bool x_plan(int64_t vt, int64_t vs, XPlan* P) {
+  *P = XPlan{};
+  if (x_plan_shape<TI, TO, kXTNarrow>(vt, vs, kXNarrow, P)) return true;
+  *P = XPlan{};
+  P->wide = true;
+  if (x_plan_shape<TI, TO, kPT>(vt, vs, kXWide, P)) return true;
+  *P = XPlan{};
+  return false;
 }
 
 template <typename TI, typename TO>
@@ -1540,16 +1563,16 @@ int launch_exchange(const XPlan& P, const void* zt, int64_t n, int64_t vt, int64
   attr[0].val.clusterDim.z = 1;
   const int64_t clusters = n < P.max_clusters ? n : P.max_clusters;
   cfg.gridDim = dim3((unsigned)(P.C * clusters));
-  cfg.blockDim = dim3(kPT);
+  cfg.blockDim = dim3(P.wide ? kPT : kXTNarrow);
   cfg.dynamicSmemBytes = P.smem;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   note_launch();
-  return cudaLaunchKernelEx(&cfg, k_project_exchange<TI, TO>, static_cast<const TI*>(zt), n, vt,
-                            vs, inv_t, off, epos, code, mpre, mlist, mcode, send_src, X, P.sc,
-                            P.so, P.send_cap, P.recv_cap, static_cast<TO*>(out),
-                            status) != cudaSuccess;
+  auto kern = P.wide ? k_project_exchange<TI, TO, kPT> : k_project_exchange<TI, TO, kXTNarrow>;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<const TI*>(zt), n, vt, vs, inv_t, off, epos,
+                            code, mpre, mlist, mcode, send_src, X, P.sc, P.so, P.send_cap,
+                            P.recv_cap, static_cast<TO*>(out), status) != cudaSuccess;
 }
 
 template <typename TI, typename TO>
@@ -1684,7 +1707,7 @@ struct ProjOps {
 template <typename TI>
 bool pl_plan(int64_t vt, int64_t vs, XPlan* P, int* steps) {
   const int64_t elem = (int64_t)sizeof(TI);
-  int64_t C = (vt * elem + kXSlice - 1) / kXSlice;
+  int64_t C = (vt * elem + kXWide.slice - 1) / kXWide.slice;
   if (C < 1) C = 1;
   if (C > kMaxC) return false;
   P->sc = ((vt + C - 1) / C + 7) / 8 * 8;
