@@ -25,9 +25,8 @@
 // * slices (k_project_slices, the fallback when a receive buffer would
 //   overflow -- a map that sends most edges to one range, decided on the
 //   device -- or when a row needs more than 8 CTAs or a CTA more than 32 Ki
-//   student ids): work items (token row,
-//   slice); a CTA stages the slice and stores each listed id's output straight
-//   to global memory.  Correct for any map, but its 2-byte stores leave
+//   student ids): work items (token row, slice); a CTA stages the slice and
+//   stores each listed id's output straight to global memory.  Correct for any map, but its 2-byte stores leave
 //   sectors partial, which costs DRAM read-modify-writes.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -1477,15 +1476,14 @@ ProjLayout proj_layout(int64_t vt, int64_t vs) {
 // 106 KiB) comes first: the two CTAs of an SM belong to different clusters and
 // are in different phases of their rows, so one's waits are the other's work.
 // Rows longer than 8 of its slices take the wide shape (1024 threads, one CTA
-// per SM, 76 KiB slices in 220 KiB).  A CTA sends
-// at most its sc columns (+ padding); what it receives depends on the map,
-// so the device checks it (XLayout::fits) and the slice path runs otherwise.
+// per SM, 76 KiB slices in 220 KiB).  A CTA sends at most its sc columns
+// (+ padding); what it receives depends on the map, so the device checks it
+// (XLayout::fits) and the slice path runs otherwise.
 struct XShape {
-  int threads;
   int64_t slice, smem;  // bytes (the tables, about 6 KiB, come on top)
 };
-constexpr XShape kXNarrow{kXTNarrow, 38 * 1024, 106 * 1024};
-constexpr XShape kXWide{kPT, 76 * 1024, 220 * 1024};
+constexpr XShape kXNarrow{38 * 1024, 106 * 1024};  // kXTNarrow threads, two CTAs per SM
+constexpr XShape kXWide{76 * 1024, 220 * 1024};    // kPT threads, one CTA per SM
 struct XPlan {
   int C = 0;
   bool wide = false;
