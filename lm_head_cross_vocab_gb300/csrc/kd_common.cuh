@@ -232,7 +232,7 @@ __device__ __forceinline__ void accum(const float* zs, const float* zt, int nval
                                       const Consts& c, float os1, float osT, float ot1, float otT,
                                       float& ls1, float& lsT, float& lt1, float& ltT, float& qd,
                                       float& qx, float& pd, float& px, float cq, float cp) {
-  if (!HAS_T) {
+  if constexpr (!HAS_T) {
 #pragma unroll
     for (int j = 0; j < NC; ++j) {
       if (!MASKED || j < nvalid) {
@@ -245,44 +245,44 @@ __device__ __forceinline__ void accum(const float* zs, const float* zt, int nval
         }
       }
     }
-    return;
-  }
-  // e^{a_s-Mt} = e^{a_s-Ms} * cq and e^{a_t-Ms} = e^{a_t-Mt} * cp.  Both
-  // directions' cross sums and (T = 1 or 2) the CE sums cost a few FMAs each,
-  // less than a branch per element, so they are always formed; finalize()
-  // reads only what the variant needs (an overflowed unused sum falls back to
-  // the log-sum-exp difference there).
+  } else {
+    // e^{a_s-Mt} = e^{a_s-Ms} * cq and e^{a_t-Ms} = e^{a_t-Mt} * cp.  Both
+    // directions' cross sums and (T = 1 or 2) the CE sums cost a few FMAs each,
+    // less than a branch per element, so they are always formed; finalize()
+    // reads only what the variant needs (an overflowed unused sum falls back to
+    // the log-sum-exp difference there).
 #pragma unroll
-  for (int j = 0; j < NC; ++j) {
-    if (!MASKED || j < nvalid) {
-      const float es = ex2(fmaf(zs[j], c.k_sT, osT));
-      const float et = ex2(fmaf(zt[j], c.k_tT, otT));
-      lsT += es;
-      ltT += et;
-      const float d = zt[j] * c.inv_tt - zs[j] * c.inv_ts;
-      qd = fmaf(et, d, qd);
-      qx += fmaf(es, cq, -et);
-      pd = fmaf(es, -d, pd);
-      px += fmaf(et, cp, -es);
-      if (PW == 2) {
-        ls1 = fmaf(es, es, ls1);
-        lt1 = fmaf(et, et, lt1);
-      } else if (PW == 1) {
-        ls1 += es;
-        lt1 += et;
+    for (int j = 0; j < NC; ++j) {
+      if (!MASKED || j < nvalid) {
+        const float es = ex2(fmaf(zs[j], c.k_sT, osT));
+        const float et = ex2(fmaf(zt[j], c.k_tT, otT));
+        lsT += es;
+        ltT += et;
+        const float d = zt[j] * c.inv_tt - zs[j] * c.inv_ts;
+        qd = fmaf(et, d, qd);
+        qx += fmaf(es, cq, -et);
+        pd = fmaf(es, -d, pd);
+        px += fmaf(et, cp, -es);
+        if (PW == 2) {
+          ls1 = fmaf(es, es, ls1);
+          lt1 = fmaf(et, et, lt1);
+        } else if (PW == 1) {
+          ls1 += es;
+          lt1 += et;
+        }
       }
     }
-  }
-  if (PW == 0) {
-    if (c.need_s1) {
+    if (PW == 0) {
+      if (c.need_s1) {
 #pragma unroll
-      for (int j = 0; j < NC; ++j)
-        if (!MASKED || j < nvalid) ls1 += ex2(fmaf(zs[j], c.k_s1, os1));
-    }
-    if (c.need_t1) {
+        for (int j = 0; j < NC; ++j)
+          if (!MASKED || j < nvalid) ls1 += ex2(fmaf(zs[j], c.k_s1, os1));
+      }
+      if (c.need_t1) {
 #pragma unroll
-      for (int j = 0; j < NC; ++j)
-        if (!MASKED || j < nvalid) lt1 += ex2(fmaf(zt[j], c.k_t1, ot1));
+        for (int j = 0; j < NC; ++j)
+          if (!MASKED || j < nvalid) lt1 += ex2(fmaf(zt[j], c.k_t1, ot1));
+      }
     }
   }
 }

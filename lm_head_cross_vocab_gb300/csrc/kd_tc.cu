@@ -282,7 +282,7 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
 }
 
 // ------------------------------------------------------------------ params
-struct __align__(64) TcParams {
+struct TcParams {  // (128-byte aligned by its tensor maps)
   CUtensorMap ma[2];
   CUtensorMap mb[2];
   int kb[2];          // k blocks per segment (0: segment absent)
