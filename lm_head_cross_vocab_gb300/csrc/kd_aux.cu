@@ -107,15 +107,20 @@ void launch_topk_prep(const int32_t* idx, const float* p, int64_t n, int k, int6
 
 // ---------------------------------------------------------------- combine
 __global__ void k_combine(CombineArgs a) {
-  const int64_t r = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-  if (r >= a.n) return;
+  // one warp per row: lane i folds parts i, i + 32, ..., then the warp merges
+  // its lanes (a fixed tree, so the result does not depend on timing)
+  const int64_t r = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (r >= a.n) return;  // (r is the same in the whole warp)
   RowState st;
   st.init();
-  for (int i = 0; i < a.n_parts; ++i) {
+  for (int i = lane; i < a.n_parts; i += 32) {
     RowState o;
     o.load(a.partials + ((int64_t)i * a.n + r) * kRec);
     merge(st, o, a.c);
   }
+  warp_merge(st, a.c);
+  if (lane != 0) return;
   bool valid = true, bad = false;
   if (a.labels) {
     const int64_t y = a.labels[r];
@@ -146,7 +151,7 @@ __global__ void k_combine(CombineArgs a) {
 void launch_combine(const CombineArgs& a, cudaStream_t s) {
   if (a.n <= 0) return;
   note_launch();
-  k_combine<<<(unsigned)((a.n + 255) / 256), 256, 0, s>>>(a);
+  k_combine<<<(unsigned)((a.n + 7) / 8), 256, 0, s>>>(a);  // 8 rows (warps) a block
 }
 
 // ---------------------------------------------------------------- loss
