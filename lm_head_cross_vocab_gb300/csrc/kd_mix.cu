@@ -615,11 +615,12 @@ __global__ void __launch_bounds__(kMT, WIDE ? 1 : 2) k_mix_cluster(const MixPara
     TO* o = static_cast<TO*>(P.out) + row * P.v + c0;
     const bool ov = (reinterpret_cast<uintptr_t>(o) & 15) == 0;
     for (int hh = 0; hh < 2; ++hh) {
-      const int64_t lo = hh ? h0 : 0, hi = hh ? clen : h0;
-      for (int64_t j0 = lo + (int64_t)threadIdx.x * 8; j0 < hi; j0 += (int64_t)kMT * 8) {
+      // (32-bit indices within the CTA's columns: sc is far below 2^31)
+      const int lo = hh ? (int)h0 : 0, hi = hh ? (int)clen : (int)h0;
+      for (int j0 = lo + (int)threadIdx.x * 8; j0 < hi; j0 += kMT * 8) {
         float r[8];
         if constexpr (sizeof(TI) == 2)
-          pass2_bf16<GEO, TO, KT>(P, zs, off_sh, (int)j0, r);
+          pass2_bf16<GEO, TO, KT>(P, zs, off_sh, j0, r);
         else
           pass2_8<GEO, TI, TO>(P, zs, off_sh, j0, r);
         if (ov && j0 + 8 <= hi) {
