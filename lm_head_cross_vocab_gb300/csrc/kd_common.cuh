@@ -61,6 +61,52 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Paired fp32 arithmetic (fma / add / sub / mul .f32x2): one instruction for
+// two columns.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// three-input maximum (one instruction on sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // number of valid columns in a chunk of `width` that starts `rem` columns before the end
 __device__ __forceinline__ int valid_cols(int64_t rem, int width) {
   return rem <= 0 ? 0 : (rem >= width ? width : (int)rem);
@@ -287,18 +333,76 @@ __device__ __forceinline__ void accum(const float* zs, const float* zt, int nval
   }
 }
 
+// accum() over NC columns (all valid, NC even) two at a time on the paired
+// fp32 instructions, with a teacher: the same terms, each column pair's sums
+// kept in a float2 and added up at the end.  The e^{-d} - 1 terms accumulate
+// as (sum + e_s c_q) - e_t, so the partial sum is rounded at the size of one
+// term (as fine as ex2's own error); pd is summed as e_s d and negated once.
+template <int NC, int PW>
+__device__ __forceinline__ void accum_pairs(const float* zs, const float* zt, const Consts& c,
+                                            float osT, float otT, float& ls1, float& lsT,
+                                            float& lt1, float& ltT, float& qd, float& qx,
+                                            float& pd, float& px, float cq, float cp) {
+  const float2 ksT = make_float2(c.k_sT, c.k_sT), oS = make_float2(osT, osT);
+  const float2 ktT = make_float2(c.k_tT, c.k_tT), oT = make_float2(otT, otT);
+  const float2 itt = make_float2(c.inv_tt, c.inv_tt), nits = make_float2(-c.inv_ts, -c.inv_ts);
+  const float2 cq2 = make_float2(cq, cq), cp2 = make_float2(cp, cp);
+  const float2 z = make_float2(0.f, 0.f);
+  float2 s1 = z, sT = z, t1 = z, tT = z, sqd = z, sqx = z, spd = z, spx = z;
+#pragma unroll
+  for (int j = 0; j < NC; j += 2) {
+    const float2 a_s = make_float2(zs[j], zs[j + 1]), a_t = make_float2(zt[j], zt[j + 1]);
+    const float2 gs = fma2(a_s, ksT, oS), gt = fma2(a_t, ktT, oT);
+    const float2 es = make_float2(ex2(gs.x), ex2(gs.y));
+    const float2 et = make_float2(ex2(gt.x), ex2(gt.y));
+    sT = add2(sT, es);
+    tT = add2(tT, et);
+    const float2 d = fma2(a_t, itt, mul2(a_s, nits));
+    sqd = fma2(et, d, sqd);
+    sqx = sub2(fma2(es, cq2, sqx), et);
+    spd = fma2(es, d, spd);
+    spx = sub2(fma2(et, cp2, spx), es);
+    if (PW == 2) {
+      s1 = fma2(es, es, s1);
+      t1 = fma2(et, et, t1);
+    } else if (PW == 1) {
+      s1 = add2(s1, es);
+      t1 = add2(t1, et);
+    }
+  }
+  lsT += sT.x + sT.y;
+  ltT += tT.x + tT.y;
+  qd += sqd.x + sqd.y;
+  qx += sqx.x + sqx.y;
+  pd -= spd.x + spd.y;
+  px += spx.x + spx.y;
+  if (PW != 0) {
+    ls1 += s1.x + s1.y;
+    lt1 += t1.x + t1.y;
+  }
+}
+
 // Chunk update of the online state with NC columns of student (and, when
 // HAS_T, teacher) logits.  With MASKED, only the first `nvalid` columns count
 // (the ragged end of the vocabulary).
-template <int NC, bool HAS_T, bool MASKED>
+template <int NC, bool HAS_T, bool MASKED, bool PAIRS = false>
 __device__ __forceinline__ void update(RowState& st, const float* zs, const float* zt,
                                        int nvalid, const Consts& c) {
+  static_assert(!PAIRS || (!MASKED && NC % 2 == 0), "paired columns: whole, even chunks");
   float cms = neg_inf(), cmt = neg_inf();
+  if constexpr (PAIRS) {
 #pragma unroll
-  for (int j = 0; j < NC; ++j) {
-    if (!MASKED || j < nvalid) {
-      cms = fmaxf(cms, zs[j]);
-      if (HAS_T) cmt = fmaxf(cmt, zt[j]);
+    for (int j = 0; j < NC; j += 2) {
+      cms = fmax3(cms, zs[j], zs[j + 1]);
+      if (HAS_T) cmt = fmax3(cmt, zt[j], zt[j + 1]);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+      if (!MASKED || j < nvalid) {
+        cms = fmaxf(cms, zs[j]);
+        if (HAS_T) cmt = fmaxf(cmt, zt[j]);
+      }
     }
   }
   if (MASKED && nvalid <= 0) return;
@@ -343,7 +447,12 @@ __device__ __forceinline__ void update(RowState& st, const float* zs, const floa
   float ls1 = 0.f, lsT = 0.f, lt1 = 0.f, ltT = 0.f, qd = 0.f, qx = 0.f, pd = 0.f, px = 0.f;
   // T = 1 sums (for CE): with T = 1 they are the tempered sums; with T = 2,
   // e^{z-m} = (e^{(z-m)/2})^2 exactly, so neither needs its own exponential.
-  if (c.pw == 2) {
+  if (PAIRS && HAS_T && c.pw != 0) {
+    if (c.pw == 2)
+      accum_pairs<NC, 2>(zs, zt, c, osT, otT, ls1, lsT, lt1, ltT, qd, qx, pd, px, cq, cp);
+    else
+      accum_pairs<NC, 1>(zs, zt, c, osT, otT, ls1, lsT, lt1, ltT, qd, qx, pd, px, cq, cp);
+  } else if (c.pw == 2) {
     accum<NC, HAS_T, MASKED, 2>(zs, zt, nvalid, c, os1, osT, ot1, otT, ls1, lsT, lt1, ltT, qd,
                                 qx, pd, px, cq, cp);
   } else if (c.pw == 1) {
@@ -422,44 +531,6 @@ __device__ __forceinline__ RowOut finalize(const RowState& s, const Consts& c, i
 // divergences below ~1e-4 per token are resolved to about 1e-7 absolute rather
 // than to their relative tolerance (bf16 logits cannot hold distributions
 // closer than their 2^-8 resolution).
-// Paired fp32 arithmetic (fma / add / sub / mul .f32x2): one instruction for
-// two columns.
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
-      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  return d;
-}
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
-__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
 __device__ __forceinline__ void js_logs(float x, const Consts& c, float& lqm, float& lpm) {
   const bool neg = x <= 0.f;
   const float coef = neg ? c.beta : 1.f - c.beta;

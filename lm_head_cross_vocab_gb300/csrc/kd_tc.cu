@@ -442,7 +442,7 @@ struct FwdEpi {
         if (j < nv) js_terms(vs[j], vt[j], lt, dl, a.c, st.jq, st.jp, st.jx, want_x);
       return;
     }
-    if (nv == 32) update<32, HAS_T, false>(st, vs, vt, 32, a.c);
+    if (nv == 32) update<32, HAS_T, false, true>(st, vs, vt, 32, a.c);
     else update<32, HAS_T, true>(st, vs, vt, nv, a.c);
     if (y >= col0 && y < col0 + nv) {
       const int j = (int)(y - col0);
@@ -466,23 +466,25 @@ struct FwdEpi {
   }
 };
 
-// 32 consecutive values of one row as bf16 (16-byte stores when aligned).
+// 32 consecutive values of one row as bf16 (16-byte stores when aligned);
+// zeros instead when !keep (a masked row), selected on the packed words.
 __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v, int nv,
-                                              int64_t ld) {
+                                              int64_t ld, bool keep = true) {
+  const uint32_t mask = keep ? 0xffffffffu : 0u;
   if (nv == 32 && (ld % 8) == 0 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
 #pragma unroll
     for (int qv = 0; qv < 4; ++qv) {
       uint4 u;
-      u.x = pack_bf16(v[8 * qv + 0], v[8 * qv + 1]);
-      u.y = pack_bf16(v[8 * qv + 2], v[8 * qv + 3]);
-      u.z = pack_bf16(v[8 * qv + 4], v[8 * qv + 5]);
-      u.w = pack_bf16(v[8 * qv + 6], v[8 * qv + 7]);
+      u.x = pack_bf16(v[8 * qv + 0], v[8 * qv + 1]) & mask;
+      u.y = pack_bf16(v[8 * qv + 2], v[8 * qv + 3]) & mask;
+      u.z = pack_bf16(v[8 * qv + 4], v[8 * qv + 5]) & mask;
+      u.w = pack_bf16(v[8 * qv + 6], v[8 * qv + 7]) & mask;
       *reinterpret_cast<uint4*>(dst + 8 * qv) = u;
     }
   } else {
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      if (j < nv) dst[j] = __float2bfloat16(v[j]);
+      if (j < nv) dst[j] = __float2bfloat16(keep ? v[j] : 0.f);
   }
 }
 
@@ -541,37 +543,64 @@ __device__ __forceinline__ GradRow grad_row(const TcGradArgs& a, int64_t row, bo
   return r;
 }
 
-// vs <- G for 32 columns (vt: teacher logits of the same columns); jy: the
-// label's column within the 32, or -1.
+// vs <- G for 32 columns (vt: teacher logits of the same columns), without the
+// label term and the row mask, which the caller applies once per 32 columns.
+// Columns go in pairs through the paired fp32 instructions (the same
+// roundings as the scalar forms); the skew form stays per column.
 template <int VAR, int PW>
 __device__ __forceinline__ void grad32(float* vs, const float* vt, const GradRow& r,
-                                       const Consts& c, int jy) {
+                                       const Consts& c) {
+  if constexpr (VAR == GV_SJS) {
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const float l2p = fmaf(vs[j], r.ks, r.ns);
-    const float p = ex2(l2p);
-    float g;
-    if (VAR == GV_P) {
-      g = r.wk * p;
-    } else if (VAR == GV_SJS) {
+    for (int j = 0; j < 32; ++j) {
+      const float p = ex2(fmaf(vs[j], r.ks, r.ns));
       const float x = fmaf(vs[j], c.inv_ts, -vt[j] * c.inv_tt) + r.dlse;
       float lqm, lpm;
       js_logs(x, c, lqm, lpm);
-      g = r.wk * skew_grad(r.var, p, lqm, lpm, r.klpm, r.eppm, c);
-    } else {
-      const float l2q = fmaf(vt[j], r.kt, r.nt);
-      if (VAR == GV_FWD) {
-        g = r.wk * (p - ex2(l2q));
-      } else {
-        const float rr = fmaf(l2p - l2q, r.wk_r, -r.klr);
-        g = VAR == GV_REV ? p * rr : fmaf(p, rr, r.wk * (p - ex2(l2q)));
-      }
+      float g = r.wk * skew_grad(r.var, p, lqm, lpm, r.klpm, r.eppm, c);
+      if (PW == 2) g = fmaf(r.cs * p, p, g);
+      else if (PW == 1) g = fmaf(r.wc, p, g);
+      else g = fmaf(r.wc, ex2(fmaf(vs[j], kL2E, r.n1s)), g);
+      vs[j] = g;
     }
-    if (PW == 2) g = fmaf(r.cs * p, p, g);
-    else if (PW == 1) g = fmaf(r.wc, p, g);
-    else g = fmaf(r.wc, ex2(fmaf(vs[j], kL2E, r.n1s)), g);
-    if (j == jy) g -= r.wc;
-    vs[j] = r.live ? g : 0.f;
+  } else {
+    const float2 ks = make_float2(r.ks, r.ks), ns = make_float2(r.ns, r.ns);
+    const float2 kt = make_float2(r.kt, r.kt), nt = make_float2(r.nt, r.nt);
+    const float2 wk = make_float2(r.wk, r.wk), wc = make_float2(r.wc, r.wc);
+    const float2 wkr = make_float2(r.wk_r, r.wk_r), nklr = make_float2(-r.klr, -r.klr);
+    const float2 cs = make_float2(r.cs, r.cs);
+    const float2 l2e = make_float2(kL2E, kL2E), n1s = make_float2(r.n1s, r.n1s);
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      const float2 zs = make_float2(vs[j], vs[j + 1]);
+      const float2 l2p = fma2(zs, ks, ns);
+      const float2 p = make_float2(ex2(l2p.x), ex2(l2p.y));
+      float2 g;
+      if constexpr (VAR == GV_P) {
+        g = mul2(wk, p);
+      } else {
+        const float2 l2q = fma2(make_float2(vt[j], vt[j + 1]), kt, nt);
+        if constexpr (VAR == GV_FWD) {
+          g = mul2(wk, sub2(p, make_float2(ex2(l2q.x), ex2(l2q.y))));
+        } else {
+          const float2 rr = fma2(sub2(l2p, l2q), wkr, nklr);
+          if constexpr (VAR == GV_REV)
+            g = mul2(p, rr);
+          else
+            g = fma2(p, rr, mul2(wk, sub2(p, make_float2(ex2(l2q.x), ex2(l2q.y)))));
+        }
+      }
+      if constexpr (PW == 2) {
+        g = fma2(mul2(cs, p), p, g);
+      } else if constexpr (PW == 1) {
+        g = fma2(wc, p, g);
+      } else {
+        const float2 l1 = fma2(zs, l2e, n1s);
+        g = fma2(wc, make_float2(ex2(l1.x), ex2(l1.y)), g);
+      }
+      vs[j] = g.x;
+      vs[j + 1] = g.y;
+    }
   }
 }
 
@@ -596,25 +625,38 @@ __device__ __forceinline__ void grad32_teacher_ce(float* vt, const GradRow& r, i
 
 template <int VAR>
 __device__ __forceinline__ void grad32_pw(int pw, float* vs, const float* vt, const GradRow& r,
-                                          const Consts& c, int jy) {
-  if (pw == 2) grad32<VAR, 2>(vs, vt, r, c, jy);
-  else if (pw == 1) grad32<VAR, 1>(vs, vt, r, c, jy);
-  else grad32<VAR, 0>(vs, vt, r, c, jy);
+                                          const Consts& c) {
+  if (pw == 2) grad32<VAR, 2>(vs, vt, r, c);
+  else if (pw == 1) grad32<VAR, 1>(vs, vt, r, c);
+  else grad32<VAR, 0>(vs, vt, r, c);
 }
 
 template <bool HAS_T>
-__device__ __forceinline__ void grad32_any(int gv, int pw, float* vs, const float* vt,
-                                           const GradRow& r, const Consts& c, int jy) {
+__device__ __forceinline__ void grad32_var(int gv, int pw, float* vs, const float* vt,
+                                           const GradRow& r, const Consts& c) {
   if constexpr (HAS_T) {
     switch (gv) {
-      case GV_FWD: grad32_pw<GV_FWD>(pw, vs, vt, r, c, jy); return;
-      case GV_REV: grad32_pw<GV_REV>(pw, vs, vt, r, c, jy); return;
-      case GV_JEF: grad32_pw<GV_JEF>(pw, vs, vt, r, c, jy); return;
-      case GV_SJS: grad32_pw<GV_SJS>(pw, vs, vt, r, c, jy); return;
+      case GV_FWD: grad32_pw<GV_FWD>(pw, vs, vt, r, c); return;
+      case GV_REV: grad32_pw<GV_REV>(pw, vs, vt, r, c); return;
+      case GV_JEF: grad32_pw<GV_JEF>(pw, vs, vt, r, c); return;
+      case GV_SJS: grad32_pw<GV_SJS>(pw, vs, vt, r, c); return;
       default: break;
     }
   }
-  grad32_pw<GV_P>(pw, vs, vt, r, c, jy);
+  grad32_pw<GV_P>(pw, vs, vt, r, c);
+}
+
+// G for 32 columns with the label's -w_ce (jy: the label's column within the
+// 32, or -1; at most one column, so the element loop carries no compare)
+template <bool HAS_T>
+__device__ __forceinline__ void grad32_any(int gv, int pw, float* vs, const float* vt,
+                                           const GradRow& r, const Consts& c, int jy) {
+  grad32_var<HAS_T>(gv, pw, vs, vt, r, c);
+  if (jy >= 0) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j == jy) vs[j] -= r.wc;
+  }
 }
 
 // ------------------------------------------------------------------ kernel
@@ -816,6 +858,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
       const int64_t tile_row = (int64_t)m_tile * C::ROWS + r_in_pair;
       FwdEpi<BN> fe;
       if (EPI == EPI_FWD) fe.begin(P, tile_row, t0, half);
+      // gradient epilogue: the row's constants, loaded while the MMAs run
+      GradRow gr;
+      int64_t g_row = 0, g_y = -1;
+      bool g_ok = false;
+      if constexpr (EPI == EPI_GRAD) {
+        const TcGradArgs& a = P.grad;
+        g_row = a.r0 + tile_row;
+        g_ok = g_row < a.r0 + a.rc;
+        gr = grad_row(a, g_row, g_ok, HAS_T && (a.t_gemm || a.t_logits));
+        g_y = (g_ok && a.labels) ? a.labels[g_row] : -1;
+      }
       for (int t = t0; t < t1; ++t) {
         if (!warp_wait(S, S.acc_full + 8 * acc, acc_phase)) {
           ok = false;
@@ -855,17 +908,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
           }
         } else if (EPI == EPI_GRAD) {
           const TcGradArgs& a = P.grad;
-          const int64_t row = a.r0 + tile_row;
-          const bool row_ok = row < a.r0 + a.rc;
+          const int64_t row = g_row, y = g_y;
+          const bool row_ok = g_ok;
           const bool has_t = HAS_T && (a.t_gemm || a.t_logits);
-          const GradRow gr = grad_row(a, row, row_ok, has_t);
           const int gv = !has_t ? GV_P
                          : a.variant == KD_KL_FORWARD ? GV_FWD
                          : a.variant == KD_KL_REVERSE ? GV_REV
                          : a.variant == KD_KL_JEFFREYS ? GV_JEF
                                                        : GV_SJS;
           const int pw = a.c.pw;
-          const int64_t y = (row_ok && a.labels) ? a.labels[row] : -1;
           const int32_t* ids = nullptr;
           const float* ps = nullptr;
           int kp = 0;
@@ -923,7 +974,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
                 }
               }
               // row-major G (or d z_s) and G_t: 32 consecutive bf16 of this row
-              store_bf16x32(a.g + (row - a.r0) * a.ldg + lc0, g, nv, a.ldg);
+              store_bf16x32(a.g + (row - a.r0) * a.ldg + lc0, g, nv, a.ldg, gr.live);
               if (want_gt) store_bf16x32(a.gt + (row - a.r0) * a.ldg + lc0, vt, nv, a.ldg);
             }
           }
