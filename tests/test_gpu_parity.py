@@ -207,6 +207,16 @@ def test_separate_teacher_bf16_variants(variant):
     assert_parity(run_and_compare(w), "bf16")
 
 
+@pytest.mark.parametrize("variant", ["reverse", "jeffreys"])
+def test_separate_teacher_bf16_t1(variant):
+    """T = 1 on both sides (the T = 1 sums are the tempered ones): the paired
+    forward update and the producer's reverse / Jeffreys element loops at
+    that temperature, with both CE terms."""
+    w = W[2].scaled(n_tokens=280, d_student=96, d_teacher=160, vocab=2200, variant=variant,
+                    t_student=1.0, t_teacher=1.0, w_student_ce=0.7)
+    assert_parity(run_and_compare(w), "bf16")
+
+
 def test_tied_bf16_teacher_ce_flows_into_weight():
     w = W[1].scaled(n_tokens=257, d_student=64, d_teacher=64, vocab=777, dtype="bf16")
     assert_parity(run_and_compare(w), "bf16")
